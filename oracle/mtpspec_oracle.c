@@ -1,0 +1,668 @@
+/*
+ * mtpspec oracle: a plain, slow, double-precision CPU statement of what the MTP
+ * speculative-decoding hot path computes.
+ *
+ * TEST INFRASTRUCTURE ONLY.  It is loaded by the test suite, by the package's smoke
+ * check and by the benchmark's CPU-baseline leg; the product library never links,
+ * loads or calls it, and the two share no code (no headers, helpers or tables).
+ *
+ * Sources, cited by page title and section:
+ *  [HB] "14. MTP: speculative decoding with the built-in draft head" (Transformer by
+ *       Hand, stage 2): "The draft head" (the MTP module: two RMSNorms, concatenation
+ *       with the embedding first, fc = Linear(2H, H, bias=False)) and "The speculative
+ *       decoding loop (greedy version)" (accept a draft when it equals the main
+ *       model's argmax, else take the main model's own token).
+ *  [DL] "The decoding loop and MTP" (agent-loop-visualizer docs): "Why a hand-written
+ *       decoding loop" (temperature, then top-k, then top-p, then sample; argmax takes
+ *       the lower id on ties) and "MTP speculative decoding" items 2-3 (first rejected
+ *       guess replaced, later guesses dropped, one extra token when all guesses hold;
+ *       a guess is kept with its probability and otherwise the token is drawn from the
+ *       other candidates).
+ *  [ZH] "MPT (MTP, Multi-Token Prediction) 原理详解": section 二.2 (enorm/hnorm, concat,
+ *       eh_proj), section 三 stage 3 (greedy and rejection-sampling verification),
+ *       stage 4 (1 to D+1 tokens per verification), section 四 (worked example).
+ *  [PX] Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+ *       SC'11: the Philox4x32-10 counter-based generator.
+ *
+ * Readings where the pages are silent or garbled (each is restated in the design notes):
+ *  - RMSNorm is x * 1/sqrt(mean(x^2) + eps) * w, and the normalised activations are
+ *    rounded to bf16 before the projection, as a bf16 module would store them.
+ *  - top-k keeps every value >= the k-th largest (ties at the boundary all kept);
+ *    top-p keeps a token when the filtered mass of strictly larger logits is < p.
+ *  - rejection-sampling residual is normalize(max(0, p_target - p_draft)); the page
+ *    prints max(0, 1 - P_target/P_draft), which is not a distribution over tokens.
+ *  - uniforms: Philox4x32-10, key = (seed lo, seed hi), counter = (row, position, 0, 0);
+ *    U_acc from output word 0, U_smp from word 1, U = (2*(w >> 9) + 1) * 2^-24.
+ *  - draws use the inverse CDF in ascending token-id order.
+ *  - a temperature of 0 makes a row greedy: it takes the greedy rule and reports
+ *    p_target = [d == argmax], p_draft = 1 (the greedy drafter's point mass).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_OK = 0, ORC_ERR_ARG = -1, ORC_ERR_DTYPE = -2, ORC_ERR_NAN = -7, ORC_ERR_NOMEM = -8 };
+enum { ORC_STATUS_BAD_DRAFT_ID = 1 };
+
+/* ------------------------------------------------------------------ value access */
+
+static double bf16_bits_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double logit_at(const void *base, int dt, int64_t i)
+{
+    if (dt == ORC_F32)
+        return (double)((const float *)base)[i];
+    return bf16_bits_to_double(((const uint16_t *)base)[i]);
+}
+
+/* Round a double to the nearest bfloat16 (ties to even) and return its bit pattern.
+ * bfloat16 keeps 8 significant bits and float's exponent range; its subnormal
+ * quantum is 2^-133. */
+uint16_t orc_double_to_bf16(double v)
+{
+    if (isnan(v))
+        return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return sign | 0x7F80;
+    int e;
+    (void)frexp(a, &e); /* a = f * 2^e, f in [0.5, 1) */
+    int q = e - 8;      /* quantum of an 8-significant-bit number in that binade */
+    if (q < -133)
+        q = -133;
+    double r = ldexp(nearbyint(ldexp(a, -q)), q);
+    if (r >= ldexp(1.0, 128))
+        return sign | 0x7F80;
+    float f = (float)r; /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (u >> 16));
+}
+
+/* ------------------------------------------------------------------ Philox4x32-10 [PX] */
+
+/* One Philox4x32 bijection with 10 rounds.  Each round multiplies words 0 and 2 by the
+ * two round multipliers, swaps the halves and mixes in the key; the key is bumped by the
+ * two Weyl constants between rounds (constants as published with the algorithm). */
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    const uint64_t mul0 = 0xD2511F53u, mul1 = 0xCD9E8D57u;
+    const uint32_t weyl0 = 0x9E3779B9u, weyl1 = 0xBB67AE85u;
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        uint64_t p0 = mul0 * (uint64_t)c0;
+        uint64_t p1 = mul1 * (uint64_t)c2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        uint32_t n0 = hi1 ^ c1 ^ k0;
+        uint32_t n1 = lo1;
+        uint32_t n2 = hi0 ^ c3 ^ k1;
+        uint32_t n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += weyl0;
+        k1 += weyl1;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Map a 32-bit word to an odd multiple of 2^-24 in (0, 1); exactly representable in
+ * float and double. */
+static double word_to_uniform(uint32_t w)
+{
+    return (double)(2u * (w >> 9) + 1u) * ldexp(1.0, -24);
+}
+
+/* The two uniforms of verification unit (row, position): U_acc for the accept test,
+ * U_smp for the draw at that position. */
+void orc_uniforms(uint64_t seed, uint64_t row, uint32_t pos, double *u_acc, double *u_smp)
+{
+    uint32_t ctr[4] = {(uint32_t)row, pos, 0u, 0u};
+    uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
+    uint32_t o[4];
+    orc_philox4x32_10(ctr, key, o);
+    *u_acc = word_to_uniform(o[0]);
+    *u_smp = word_to_uniform(o[1]);
+}
+
+/* ------------------------------------------------------------------ argmax [DL] */
+
+/* Index of the largest logit, the lowest index among equal maxima ("takes the lower
+ * id", [DL] "Why a hand-written decoding loop").  -inf is an ordinary value, so an
+ * all -inf row gives 0.  Returns -1 for V < 1 and -2 if a NaN is present. */
+int64_t orc_argmax(const void *x, int dt, int64_t V)
+{
+    if (V < 1)
+        return -1;
+    int64_t best = 0;
+    double bv = logit_at(x, dt, 0);
+    if (isnan(bv))
+        return -2;
+    for (int64_t i = 1; i < V; ++i) {
+        double v = logit_at(x, dt, i);
+        if (isnan(v))
+            return -2;
+        if (v > bv) {
+            bv = v;
+            best = i;
+        }
+    }
+    return best;
+}
+
+/* Greedy draft ([HB] "The draft head": draft = argmax of the draft logits; [ZH] 三
+ * stages 1-2, greedy sample of each draft step): one argmax per row of [M, V]. */
+int orc_greedy_draft(const void *logits, int dt, int64_t M, int64_t V, int32_t *ids)
+{
+    if (dt != ORC_F32 && dt != ORC_BF16)
+        return ORC_ERR_DTYPE;
+    if (M < 0 || V < 1 || (M > 0 && (!logits || !ids)))
+        return ORC_ERR_ARG;
+    size_t es = dt == ORC_F32 ? 4 : 2;
+    for (int64_t r = 0; r < M; ++r) {
+        int64_t a = orc_argmax((const char *)logits + (size_t)r * (size_t)V * es, dt, V);
+        if (a < 0)
+            return ORC_ERR_NAN;
+        ids[r] = (int32_t)a;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ greedy verify */
+
+/* Greedy verification ([HB] greedy loop; [ZH] 三 stage 3 "greedy strategy", stage 4;
+ * [DL] item 2).  Row b has target logits T[b, 0..D, :] over the D+1 positions
+ * [bonus, d_0 .. d_{D-1}] and drafts d[b, 0..D-1].  a = the first j with
+ * d_j != argmax T[b, j] (D if none); the row emits d_0 .. d_{a-1} then argmax T[b, a]
+ * (the correction, or the bonus when a = D); -1 pads to D+1.  An id outside [0, V)
+ * never equals an argmax, so it is rejected, and it sets ORC_STATUS_BAD_DRAFT_ID. */
+int orc_verify_greedy(const void *T, int dt, const int32_t *d, int64_t B, int32_t D, int64_t V,
+                      int32_t *out, int32_t *num_accepted, int32_t *status)
+{
+    if (dt != ORC_F32 && dt != ORC_BF16)
+        return ORC_ERR_DTYPE;
+    if (B < 0 || D < 1 || V < 1)
+        return ORC_ERR_ARG;
+    size_t es = dt == ORC_F32 ? 4 : 2;
+    int32_t st = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        const char *rowT = (const char *)T + (size_t)b * (size_t)(D + 1) * (size_t)V * es;
+        int32_t a = D;
+        for (int32_t j = 0; j < D; ++j) {
+            int32_t dj = d[b * D + j];
+            if (dj < 0 || (int64_t)dj >= V)
+                st |= ORC_STATUS_BAD_DRAFT_ID;
+        }
+        for (int32_t j = 0; j < D; ++j) {
+            int64_t g = orc_argmax(rowT + (size_t)j * (size_t)V * es, dt, V);
+            if (g < 0)
+                return ORC_ERR_NAN;
+            if ((int64_t)d[b * D + j] != g) {
+                a = j;
+                break;
+            }
+        }
+        int64_t last = orc_argmax(rowT + (size_t)a * (size_t)V * es, dt, V);
+        if (last < 0)
+            return ORC_ERR_NAN;
+        for (int32_t j = 0; j <= D; ++j)
+            out[b * (D + 1) + j] = -1;
+        for (int32_t j = 0; j < a; ++j)
+            out[b * (D + 1) + j] = d[b * D + j];
+        out[b * (D + 1) + a] = (int32_t)last;
+        num_accepted[b] = a;
+    }
+    if (status)
+        *status |= st;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ filtering [DL] */
+
+typedef struct {
+    double v;
+    int64_t i;
+} orc_vi;
+
+static int orc_vi_desc(const void *pa, const void *pb)
+{
+    const orc_vi *a = (const orc_vi *)pa, *b = (const orc_vi *)pb;
+    if (a->v > b->v) return -1;
+    if (a->v < b->v) return 1;
+    return (a->i > b->i) - (a->i < b->i);
+}
+
+/* The sampling distribution of one logit row under temperature tau > 0, then top-k,
+ * then top-p, "in turn" ([DL] "Why a hand-written decoding loop"):
+ *   - top-k is on for 1 <= k < V: keep every logit >= the k-th largest one;
+ *   - weights w_i = exp((x_i - max) / tau) over the kept set;
+ *   - top-p is on for p < 1: keep a token when the normalised weight of the kept
+ *     tokens with strictly larger logits is < p (the largest logits always stay);
+ *   - the result is renormalised over what is left.
+ * Writes the unnormalised kept weights to w[V], support membership to in[V] (a kept
+ * token whose weight underflows is still in the support), their sum to *Z and the row
+ * maximum to *mx.  A row whose logits are all -inf is a point mass on id 0, its
+ * argmax.  *margin_p (if given)
+ * receives the distance from p of the two masses that decide the top-p boundary
+ * (+inf when top-p is off). */
+static int orc_filter_weights(const void *x, int dt, int64_t V, double tau, int32_t k, double p,
+                              double *w, unsigned char *in, double *Z, double *mx, double *margin_p)
+{
+    if (margin_p)
+        *margin_p = INFINITY;
+    orc_vi *s = (orc_vi *)malloc((size_t)V * sizeof(orc_vi));
+    if (!s)
+        return ORC_ERR_NOMEM;
+    double m = -INFINITY;
+    for (int64_t i = 0; i < V; ++i) {
+        s[i].v = logit_at(x, dt, i);
+        s[i].i = i;
+        if (isnan(s[i].v)) {
+            free(s);
+            return ORC_ERR_NAN;
+        }
+        if (s[i].v > m)
+            m = s[i].v;
+    }
+    *mx = m;
+    for (int64_t i = 0; i < V; ++i) {
+        w[i] = 0.0;
+        in[i] = 0;
+    }
+    if (m == -INFINITY) {
+        w[0] = 1.0;
+        in[0] = 1;
+        *Z = 1.0;
+        free(s);
+        return ORC_OK;
+    }
+    qsort(s, (size_t)V, sizeof(orc_vi), orc_vi_desc);
+
+    /* top-k: the threshold is the k-th largest value, counting repeats */
+    double theta = -INFINITY;
+    if (k >= 1 && (int64_t)k < V)
+        theta = s[k - 1].v;
+
+    int64_t kept = 0; /* kept entries form a prefix of the sorted order */
+    double z = 0.0;
+    while (kept < V && s[kept].v >= theta) {
+        double wi = exp((s[kept].v - m) / tau);
+        w[s[kept].i] = wi;
+        in[s[kept].i] = 1;
+        z += wi;
+        ++kept;
+    }
+
+    if (p < 1.0) {
+        /* walk groups of equal logits from the top; S = normalised mass strictly above */
+        double above = 0.0;
+        int64_t g = 0;
+        while (g < kept) {
+            int64_t h = g;
+            double gm = 0.0;
+            while (h < kept && s[h].v == s[g].v) {
+                gm += w[s[h].i];
+                ++h;
+            }
+            double S = above / z;
+            if (S < p) {
+                above += gm;
+                if (margin_p) {
+                    double mk = p - S; /* how far the kept group was from dropping */
+                    double md = fabs(above / z - p); /* mass that the next group would see */
+                    double mm = mk < md ? mk : md;
+                    *margin_p = mm;
+                }
+                g = h;
+            } else {
+                for (int64_t t = g; t < kept; ++t) {
+                    w[s[t].i] = 0.0;
+                    in[s[t].i] = 0;
+                }
+                kept = g;
+                break;
+            }
+        }
+        z = 0.0;
+        for (int64_t t = 0; t < kept; ++t)
+            z += w[s[t].i];
+    }
+    *Z = z;
+    free(s);
+    return ORC_OK;
+}
+
+/* Normalised filtered probabilities of one row (see orc_filter_weights). */
+int orc_filter(const void *x, int dt, int64_t V, double tau, int32_t k, double p, double *prob,
+               double *margin_p)
+{
+    if (dt != ORC_F32 && dt != ORC_BF16)
+        return ORC_ERR_DTYPE;
+    if (V < 1 || !(tau > 0.0) || !(p > 0.0))
+        return ORC_ERR_ARG;
+    double Z, m;
+    unsigned char *in = (unsigned char *)malloc((size_t)V);
+    if (!in)
+        return ORC_ERR_NOMEM;
+    int rc = orc_filter_weights(x, dt, V, tau, k, p, prob, in, &Z, &m, margin_p);
+    free(in);
+    if (rc != ORC_OK)
+        return rc;
+    for (int64_t i = 0; i < V; ++i)
+        prob[i] /= Z;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ draws */
+
+/* Inverse-CDF draw over non-negative weights in ascending id order: the smallest i with
+ * C(i) = sum_{y <= i} w_y > u * sum(w); if rounding leaves none, the largest i with
+ * w_i > 0.  *margin receives min(u*S - C(i-1), C(i) - u*S) / S. */
+static int64_t orc_inverse_cdf(const double *w, int64_t V, double u, double *margin)
+{
+    double S = 0.0;
+    for (int64_t i = 0; i < V; ++i)
+        S += w[i];
+    double t = u * S;
+    double c = 0.0;
+    for (int64_t i = 0; i < V; ++i) {
+        double prev = c;
+        c += w[i];
+        if (c > t) {
+            if (margin) {
+                double a = (t - prev) / S, b = (c - t) / S;
+                *margin = a < b ? a : b;
+            }
+            return i;
+        }
+    }
+    if (margin)
+        *margin = 0.0;
+    for (int64_t i = V - 1; i >= 0; --i)
+        if (w[i] > 0.0)
+            return i;
+    return 0;
+}
+
+/* ------------------------------------------------------------------ sampling verify */
+
+/* Speculative-sampling verification ([ZH] 三 stage 3 "rejection sampling", stage 4;
+ * [DL] "MTP speculative decoding" items 2-3).  For row b with temperature tau_b > 0
+ * and positions j = 0..D:
+ *   p_j = filtered distribution of T[b, j];  q_j = filtered distribution of Q[b, j] (j < D)
+ *   position j < D accepts d_j iff d_j is in the support of p_j and (d_j is outside the
+ *       support of q_j, or U_acc(b, j) <= p_j(d_j) / q_j(d_j));  an id outside [0, V)
+ *       is rejected;
+ *   a = the first rejected position (D if none);
+ *   a < D: the token at a is drawn from normalize(max(0, p_a - q_a)) with U_smp(b, a)
+ *          (from p_a when that residual is identically 0);
+ *   a = D: the bonus token is drawn from p_D with U_smp(b, D).
+ * tau_b = 0 makes row b greedy (orc_verify_greedy's rule).  top_k / top_p may be NULL
+ * (off).  row0 offsets the Philox row counter (the rows passed are rows row0.. of a
+ * larger batch).  out[B, D+1] (-1 padded), num_accepted[B]; p_target / p_draft [B, D]
+ * receive p_j(d_j), q_j(d_j).  margins (optional) [B, D+1, 4] receive per unit:
+ * |U_acc - p/q|, the top-p margin of T, of Q, and the draw's inverse-CDF margin
+ * (+inf where not applicable). */
+int orc_verify_sample(const void *T, const void *Q, int dt, const int32_t *d, const float *tau,
+                      const int32_t *top_k, const float *top_p, uint64_t seed, int64_t row0,
+                      int64_t B, int32_t D, int64_t V, int32_t *out, int32_t *num_accepted,
+                      double *p_target, double *p_draft, int32_t *status, double *margins)
+{
+    if (dt != ORC_F32 && dt != ORC_BF16)
+        return ORC_ERR_DTYPE;
+    if (B < 0 || D < 1 || V < 1 || row0 < 0)
+        return ORC_ERR_ARG;
+    if (B == 0)
+        return ORC_OK;
+    if (!T || !Q || !d || !tau || !out || !num_accepted)
+        return ORC_ERR_ARG;
+    size_t es = dt == ORC_F32 ? 4 : 2;
+    double *wp = (double *)malloc((size_t)V * sizeof(double) * 3);
+    unsigned char *inp = (unsigned char *)malloc((size_t)V * 2);
+    if (!wp || !inp) {
+        free(wp);
+        free(inp);
+        return ORC_ERR_NOMEM;
+    }
+    double *wq = wp + V, *wr = wq + V;
+    unsigned char *inq = inp + V;
+    int32_t st = 0;
+    int rc = ORC_OK;
+
+    for (int64_t b = 0; b < B && rc == ORC_OK; ++b) {
+        const char *rowT = (const char *)T + (size_t)b * (size_t)(D + 1) * (size_t)V * es;
+        const char *rowQ = (const char *)Q + (size_t)b * (size_t)D * (size_t)V * es;
+        double tb = (double)tau[b];
+        int32_t kb = top_k ? top_k[b] : 0;
+        double pb = top_p ? (double)top_p[b] : 1.0;
+        if (!(tb >= 0.0) || !(pb > 0.0)) {
+            rc = ORC_ERR_ARG;
+            break;
+        }
+        double *mg = margins ? margins + (size_t)b * (size_t)(D + 1) * 4 : NULL;
+        if (mg)
+            for (int32_t t = 0; t < (D + 1) * 4; ++t)
+                mg[t] = INFINITY;
+        for (int32_t j = 0; j < D; ++j) {
+            int32_t dj = d[b * D + j];
+            if (dj < 0 || (int64_t)dj >= V)
+                st |= ORC_STATUS_BAD_DRAFT_ID;
+        }
+
+        if (tb == 0.0) { /* greedy row */
+            int32_t a = D;
+            int64_t g_at_a = -1;
+            for (int32_t j = 0; j <= D; ++j) {
+                int64_t g = orc_argmax(rowT + (size_t)j * (size_t)V * es, dt, V);
+                if (g < 0) {
+                    rc = ORC_ERR_NAN;
+                    break;
+                }
+                if (j < D) {
+                    int32_t dj = d[b * D + j];
+                    int valid = dj >= 0 && (int64_t)dj < V;
+                    if (p_target)
+                        p_target[b * D + j] = (valid && dj == g) ? 1.0 : 0.0;
+                    if (p_draft)
+                        p_draft[b * D + j] = valid ? 1.0 : 0.0;
+                    if (a == D && (int64_t)dj != g)
+                        a = j;
+                }
+                if (j == a && g_at_a < 0)
+                    g_at_a = g;
+            }
+            if (rc != ORC_OK)
+                break;
+            for (int32_t j = 0; j <= D; ++j)
+                out[b * (D + 1) + j] = -1;
+            for (int32_t j = 0; j < a; ++j)
+                out[b * (D + 1) + j] = d[b * D + j];
+            out[b * (D + 1) + a] = (int32_t)g_at_a;
+            num_accepted[b] = a;
+            continue;
+        }
+
+        /* sampling row: accept tests at every position j < D */
+        int32_t a = D;
+        for (int32_t j = 0; j < D && rc == ORC_OK; ++j) {
+            double Zp, Zq, mp, mq, xp, xq;
+            rc = orc_filter_weights(rowT + (size_t)j * (size_t)V * es, dt, V, tb, kb, pb, wp, inp,
+                                    &Zp, &xp, &mp);
+            if (rc == ORC_OK)
+                rc = orc_filter_weights(rowQ + (size_t)j * (size_t)V * es, dt, V, tb, kb, pb, wq,
+                                        inq, &Zq, &xq, &mq);
+            if (rc != ORC_OK)
+                break;
+            int32_t dj = d[b * D + j];
+            int valid = dj >= 0 && (int64_t)dj < V;
+            double pt = valid ? wp[dj] / Zp : 0.0;
+            double pd = valid ? wq[dj] / Zq : 0.0;
+            if (p_target)
+                p_target[b * D + j] = pt;
+            if (p_draft)
+                p_draft[b * D + j] = pd;
+            double ua, us;
+            orc_uniforms(seed, (uint64_t)(row0 + b), (uint32_t)j, &ua, &us);
+            int accept;
+            if (!valid || !inp[dj]) {
+                accept = 0;
+            } else if (!inq[dj]) {
+                accept = 1;
+            } else {
+                /* p/q written with both row maxima factored out, so that it does not
+                 * underflow when both probabilities are tiny */
+                double xt = logit_at(rowT + (size_t)j * (size_t)V * es, dt, dj);
+                double xd = logit_at(rowQ + (size_t)j * (size_t)V * es, dt, dj);
+                double ratio = exp(((xt - xp) - (xd - xq)) / tb) * (Zq / Zp);
+                accept = ua <= ratio;
+                if (mg)
+                    mg[j * 4 + 0] = fabs(ua - ratio);
+            }
+            if (mg) {
+                mg[j * 4 + 1] = mp;
+                mg[j * 4 + 2] = mq;
+            }
+            if (!accept && a == D) {
+                a = j;
+                /* residual draw at the first rejection */
+                double R = 0.0;
+                for (int64_t i = 0; i < V; ++i) {
+                    double r = wp[i] / Zp - wq[i] / Zq;
+                    wr[i] = r > 0.0 ? r : 0.0;
+                    R += wr[i];
+                }
+                double dm;
+                int64_t tok;
+                if (R > 0.0)
+                    tok = orc_inverse_cdf(wr, V, us, &dm);
+                else
+                    tok = orc_inverse_cdf(wp, V, us, &dm);
+                if (mg)
+                    mg[j * 4 + 3] = dm;
+                for (int32_t t = 0; t <= D; ++t)
+                    out[b * (D + 1) + t] = -1;
+                for (int32_t t = 0; t < a; ++t)
+                    out[b * (D + 1) + t] = d[b * D + t];
+                out[b * (D + 1) + a] = (int32_t)tok;
+                num_accepted[b] = a;
+            }
+        }
+        if (rc != ORC_OK)
+            break;
+        if (a == D) { /* every draft held: bonus token from position D */
+            double Zp, mp, xp, ua, us, dm;
+            rc = orc_filter_weights(rowT + (size_t)D * (size_t)V * es, dt, V, tb, kb, pb, wp, inp,
+                                    &Zp, &xp, &mp);
+            if (rc != ORC_OK)
+                break;
+            orc_uniforms(seed, (uint64_t)(row0 + b), (uint32_t)D, &ua, &us);
+            int64_t tok = orc_inverse_cdf(wp, V, us, &dm);
+            if (mg) {
+                mg[D * 4 + 1] = mp;
+                mg[D * 4 + 3] = dm;
+            }
+            for (int32_t t = 0; t < D; ++t)
+                out[b * (D + 1) + t] = d[b * D + t];
+            out[b * (D + 1) + D] = (int32_t)tok;
+            num_accepted[b] = D;
+        }
+    }
+    free(wp);
+    free(inp);
+    if (status)
+        *status |= st;
+    return rc;
+}
+
+/* ------------------------------------------------------------------ draft input [HB][ZH] */
+
+/* RMSNorm of one H-vector with the pages' module layout ([HB] "The draft head":
+ * RMSNorm(H, eps); [ZH] 二.2 step 2): out_i = bf16(v_i * r * w_i), r = 1/sqrt(mean(v^2)+eps). */
+static void orc_rmsnorm_bf16(const uint16_t *v, const uint16_t *w, int64_t H, double eps,
+                             double *out)
+{
+    double ss = 0.0;
+    for (int64_t i = 0; i < H; ++i) {
+        double x = bf16_bits_to_double(v[i]);
+        ss += x * x;
+    }
+    double r = 1.0 / sqrt(ss / (double)H + eps);
+    for (int64_t i = 0; i < H; ++i) {
+        double y = bf16_bits_to_double(v[i]) * r * bf16_bits_to_double(w[i]);
+        out[i] = bf16_bits_to_double(orc_double_to_bf16(y));
+    }
+}
+
+/* The draft head's input stage ([HB] "The draft head": fc(cat(norm(e_{t+1}), norm(h_t)));
+ * [ZH] 二.2 steps 2-3: eh_proj(cat(enorm(embeds), hnorm(hidden)))).  For each token t:
+ * x = [enorm(e_t); hnorm(h_t)] (embedding first, 2H values), y_t = W x with W [H, 2H]
+ * row-major (out x in, no bias), accumulated in double and returned before any output
+ * rounding.  xn (optional) [M, 2H] receives the bf16 bits of x. */
+int orc_draft_input(const uint16_t *e, const uint16_t *h, const uint16_t *we, const uint16_t *wh,
+                    const uint16_t *W, int64_t M, int64_t H, double eps, double *y, uint16_t *xn)
+{
+    if (M < 0 || H < 1 || !(eps >= 0.0))
+        return ORC_ERR_ARG;
+    double *x = (double *)malloc((size_t)(2 * H) * sizeof(double));
+    if (!x)
+        return ORC_ERR_NOMEM;
+    for (int64_t t = 0; t < M; ++t) {
+        orc_rmsnorm_bf16(e + t * H, we, H, eps, x);
+        orc_rmsnorm_bf16(h + t * H, wh, H, eps, x + H);
+        if (xn)
+            for (int64_t i = 0; i < 2 * H; ++i)
+                xn[t * 2 * H + i] = orc_double_to_bf16(x[i]);
+        for (int64_t o = 0; o < H; ++o) {
+            const uint16_t *wrow = W + o * 2 * H;
+            double acc = 0.0;
+            for (int64_t i = 0; i < 2 * H; ++i)
+                acc += bf16_bits_to_double(wrow[i]) * x[i];
+            y[t * H + o] = acc;
+        }
+    }
+    free(x);
+    return ORC_OK;
+}
+
+/* Selected outputs y[tok[i], col[i]] of orc_draft_input, one at a time, for checks at
+ * sizes where the full product is too slow on the host. */
+int orc_draft_input_at(const uint16_t *e, const uint16_t *h, const uint16_t *we,
+                       const uint16_t *wh, const uint16_t *W, int64_t M, int64_t H, double eps,
+                       const int64_t *tok, const int64_t *col, int64_t n, double *y)
+{
+    if (M < 1 || H < 1 || n < 0 || !(eps >= 0.0))
+        return ORC_ERR_ARG;
+    double *x = (double *)malloc((size_t)(2 * H) * sizeof(double));
+    if (!x)
+        return ORC_ERR_NOMEM;
+    int64_t cur = -1;
+    for (int64_t i = 0; i < n; ++i) {
+        if (tok[i] < 0 || tok[i] >= M || col[i] < 0 || col[i] >= H) {
+            free(x);
+            return ORC_ERR_ARG;
+        }
+        if (tok[i] != cur) {
+            cur = tok[i];
+            orc_rmsnorm_bf16(e + cur * H, we, H, eps, x);
+            orc_rmsnorm_bf16(h + cur * H, wh, H, eps, x + H);
+        }
+        const uint16_t *wrow = W + col[i] * 2 * H;
+        double acc = 0.0;
+        for (int64_t k = 0; k < 2 * H; ++k)
+            acc += bf16_bits_to_double(wrow[k]) * x[k];
+        y[i] = acc;
+    }
+    free(x);
+    return ORC_OK;
+}
