@@ -1,0 +1,190 @@
+/*
+ * libmtpspec — the data-parallel hot path of MTP (multi-token prediction) speculative
+ * decoding on one NVIDIA GB300 GPU (sm_103a): the draft head's input stage, greedy
+ * drafting, and greedy or speculative-sampling verification of a batch of drafts.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every array pointer is a DEVICE pointer owned by the caller.  The library never
+ *    allocates, frees or keeps any of them after the call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL: the legacy default stream).  All
+ *    work is enqueued on it asynchronously; nothing synchronises the host.
+ *  - The return value reports what the host can see before launching: MTPSPEC_OK, or a
+ *    negative mtpspec_status for a bad argument, dtype, shape or workspace, or a launch
+ *    failure.  Nothing is enqueued when the return value is not MTPSPEC_OK.
+ *  - What only the device can see (a draft id outside [0, V), a bad per-row sampling
+ *    parameter) is OR-ed into the optional device word `*status` as MTPSPEC_STATUS_*
+ *    bits; the caller zeroes that word beforehand.  No kernel traps.
+ *  - Row-major, contiguous arrays.  Logits are float32 or bfloat16 (mtpspec_dtype);
+ *    bfloat16 arrays are passed as their 16-bit patterns.  Token ids are int32.
+ *  - Inputs must be finite or -inf.  NaN logits give unspecified (but in-bounds)
+ *    results.
+ *
+ * Sources, cited by page title and section:
+ *  [HB] "14. MTP: speculative decoding with the built-in draft head" (Transformer by
+ *       Hand, stage 2), sections "The draft head" and "The speculative decoding loop
+ *       (greedy version)".
+ *  [DL] "The decoding loop and MTP" (agent-loop-visualizer docs), sections "Why a
+ *       hand-written decoding loop" and "MTP speculative decoding".
+ *  [ZH] "MPT (MTP, Multi-Token Prediction) 原理详解", sections 二.2 (forward 流程),
+ *       三 (stages 0-4) and 四 (worked example).
+ *  [PX] Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3"
+ *       (SC'11), Philox4x32-10.
+ */
+#ifndef LIBMTPSPEC_H
+#define LIBMTPSPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MTPSPEC_OK = 0,
+    MTPSPEC_ERR_ARG = -1,          /* null pointer, misaligned pointer, bad scalar */
+    MTPSPEC_ERR_DTYPE = -2,        /* dtype is not MTPSPEC_F32 / MTPSPEC_BF16 */
+    MTPSPEC_ERR_SHAPE = -3,        /* a size is out of the supported range */
+    MTPSPEC_ERR_WORKSPACE = -4,    /* workspace null or smaller than required */
+    MTPSPEC_ERR_CUDA = -5,         /* a CUDA runtime call or kernel launch failed */
+    MTPSPEC_ERR_UNSUPPORTED = -6   /* the current device is not sm_103 */
+} mtpspec_status;
+
+typedef enum { MTPSPEC_F32 = 0, MTPSPEC_BF16 = 1 } mtpspec_dtype;
+
+/* Bits OR-ed into the device status word. */
+#define MTPSPEC_STATUS_BAD_DRAFT_ID 0x1 /* a draft id outside [0, V); that draft is rejected */
+#define MTPSPEC_STATUS_BAD_PARAM 0x2    /* a row with temperature < 0 or NaN, or top_p <= 0 or
+                                           NaN; that row is verified greedily */
+#define MTPSPEC_STATUS_TIMEOUT 0x4      /* a bounded wait inside a kernel gave up (a copy
+                                           engine fault); outputs of that call are invalid */
+
+/* ------------------------------------------------------------------ draft input stage */
+
+/*
+ * mtp_draft_input — the MTP draft head's input stage ([HB] "The draft head":
+ * fc(cat(norm(e_{t+1}), norm(h_t))); [ZH] 二.2 steps 2-3: eh_proj(cat(enorm(embeds),
+ * hnorm(previous_hidden_states)))).  For each of M tokens:
+ *     x   = [ rmsnorm(emb_next[t]) * enorm_w ; rmsnorm(hidden[t]) * hnorm_w ]   (2H)
+ *     out[t] = eh_proj_w @ x                                                    (H)
+ * with rmsnorm(v) = v / sqrt(mean(v^2) + eps).  The normalised activations are rounded
+ * to bf16; the projection accumulates in fp32 and rounds its output to bf16.
+ *
+ *   emb_next, hidden  bf16 [M, H]    embedding of token t+1 and main-model hidden state
+ *                                    at position t (after the main model's final norm)
+ *   enorm_w, hnorm_w  bf16 [H]       RMSNorm weights
+ *   eh_proj_w         bf16 [H, 2H]   row-major (out x in); columns 0..H-1 multiply the
+ *                                    embedding half, H..2H-1 the hidden half
+ *   out               bf16 [M, H]
+ *   M >= 0 tokens, 1 <= H <= 65536 with H % 8 == 0, eps >= 0.
+ *   workspace         device scratch of at least mtp_draft_input_workspace_bytes(M, H)
+ *                     bytes (may be NULL when that is 0), 256-byte aligned.
+ * Every pointer must be 16-byte aligned.  Small M streams the weight once through a
+ * fused norm + GEMV; large M normalises into the workspace and runs a tcgen05 GEMM.
+ * Returns MTPSPEC_OK (also for M == 0, with nothing enqueued) or an error as above.
+ */
+int mtp_draft_input(const void *emb_next, const void *hidden, const void *enorm_w,
+                    const void *hnorm_w, const void *eh_proj_w, void *out, int64_t M, int64_t H,
+                    float eps, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace mtp_draft_input needs for (M, H); 0 on the GEMV path.
+ * Returns 0 as well for arguments mtp_draft_input would reject. */
+size_t mtp_draft_input_workspace_bytes(int64_t M, int64_t H);
+
+/* ------------------------------------------------------------------ greedy drafting */
+
+/*
+ * mtp_greedy_draft — greedy draft tokens: the argmax of each row of draft logits
+ * ([HB] "The speculative decoding loop": the draft is the argmax of the draft head's
+ * logits; [ZH] 三 stages 1-2, greedy sample of each MTP step), taking the LOWEST id
+ * among equal maxima ([DL] "Why a hand-written decoding loop").  bf16 values are
+ * compared as stored; -inf is an ordinary value, so an all -inf row gives id 0.
+ *
+ *   logits   [M, V] of dtype        out_ids  int32 [M]
+ *   M >= 0, 1 <= V <= 2^31 - 1.  logits aligned to its element size.
+ */
+int mtp_greedy_draft(const void *logits, int dtype, int64_t M, int64_t V, int32_t *out_ids,
+                     void *stream);
+
+/* ------------------------------------------------------------------ greedy verification */
+
+/*
+ * spec_verify_greedy — greedy verification of D drafts per row ([HB] "The speculative
+ * decoding loop (greedy version)": a draft is kept when it equals the main model's own
+ * argmax, otherwise the main model's token replaces it; [ZH] 三 stage 3 "greedy
+ * strategy" and stage 4, 四 steps C-D; [DL] "MTP speculative decoding" item 2: when
+ * all guesses hold the last position gives one more token).
+ *
+ *   target_logits  [B, D+1, V]  row b, position j predicts the token after position j
+ *                               of the verified sequence [bonus, d_0, .., d_{D-1}]
+ *   draft_ids      int32 [B, D]
+ *   out_tokens     int32 [B, D+1]  d_0 .. d_{a-1}, then argmax(target[b, a]) (the
+ *                                  correction, or the bonus token when a = D), then -1
+ *   num_accepted   int32 [B]       a = the number of leading drafts equal to the argmax
+ *                                  at their position (0..D).  Tokens emitted = a + 1;
+ *                                  a KV cache of the verified sequence keeps 1 + a
+ *                                  entries.
+ *   status         int32 [1] or NULL   MTPSPEC_STATUS_BAD_DRAFT_ID for ids outside [0, V)
+ *   B >= 0, 1 <= D <= 64, 1 <= V <= 2^31 - 1.
+ */
+int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draft_ids, int64_t B,
+                       int32_t D, int64_t V, int32_t *out_tokens, int32_t *num_accepted,
+                       int32_t *status, void *stream);
+
+/* ------------------------------------------------------------------ sampling verification */
+
+/*
+ * spec_verify_sample — speculative-sampling verification ([ZH] 三 stage 3 "rejection
+ * sampling" and stage 4; [DL] "Why a hand-written decoding loop" for the filters and
+ * "MTP speculative decoding" items 2-3; [HB] "How to explain it": the output
+ * distribution is unchanged).  For each row b with temperature tau_b > 0:
+ *   p_j = filter(target_logits[b, j]), q_j = filter(draft_logits[b, j]), where filter
+ *         is: divide by tau_b, keep logits >= the k-th largest (top-k, ties kept), form
+ *         the softmax, keep a token when the mass of strictly larger kept logits is
+ *         < top_p (top-p), renormalise;
+ *   draft j < D is accepted when d_j is in the support of p_j and (d_j is outside the
+ *         support of q_j, or U_acc(b, j) <= p_j(d_j) / q_j(d_j));
+ *   at the first rejected position a the token is drawn from
+ *         normalize(max(0, p_a - q_a)) (from p_a if that is identically zero);
+ *   when all D drafts are accepted the bonus token is drawn from p_D.
+ * Draws take the inverse CDF in ascending id order with U_smp(b, j).  U_acc, U_smp are
+ * Philox4x32-10 ([PX]) outputs 0 and 1 for key (seed lo, seed hi) and counter
+ * (b, j, 0, 0), each mapped to (2 * (word >> 9) + 1) * 2^-24.  A row with tau_b = 0 is
+ * verified greedily as in spec_verify_greedy (reported p_target = [d_j == argmax],
+ * p_draft = 1).
+ *
+ *   target_logits  [B, D+1, V]     draft_logits [B, D, V] (same dtype)
+ *   draft_ids      int32 [B, D]
+ *   temperature    float [B]       0 => greedy row
+ *   top_k          int32 [B] or NULL   <= 0 or >= V => off
+ *   top_p          float [B] or NULL   >= 1 => off; must be > 0
+ *   seed           Philox key
+ *   out_tokens, num_accepted   as in spec_verify_greedy
+ *   p_target, p_draft  float [B, D] or NULL   p_j(d_j) and q_j(d_j) for every j < D
+ *   workspace      >= spec_verify_workspace_bytes(B, D, V) bytes, 256-byte aligned;
+ *                  no initial contents are needed
+ *   status         int32 [1] or NULL
+ *   B >= 0, 1 <= D <= 64, 1 <= V <= 2^31 - 1.
+ */
+int spec_verify_sample(const void *target_logits, const void *draft_logits, int dtype,
+                       const int32_t *draft_ids, const float *temperature, const int32_t *top_k,
+                       const float *top_p, uint64_t seed, int64_t B, int32_t D, int64_t V,
+                       int32_t *out_tokens, int32_t *num_accepted, float *p_target,
+                       float *p_draft, void *workspace, size_t workspace_bytes, int32_t *status,
+                       void *stream);
+
+/* Bytes of device workspace spec_verify_sample needs for (B, D, V); 0 for B == 0 or
+ * for arguments spec_verify_sample would reject. */
+size_t spec_verify_workspace_bytes(int64_t B, int32_t D, int64_t V);
+
+/* ------------------------------------------------------------------ misc */
+
+/* A static, human-readable name for an mtpspec_status value. */
+const char *mtpspec_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBMTPSPEC_H */

@@ -521,10 +521,16 @@ int orc_verify_sample(const void *T, const void *Q, int dt, const int32_t *d, co
                 accept = 1;
             } else {
                 /* p/q written with both row maxima factored out, so that it does not
-                 * underflow when both probabilities are tiny */
-                double xt = logit_at(rowT + (size_t)j * (size_t)V * es, dt, dj);
-                double xd = logit_at(rowQ + (size_t)j * (size_t)V * es, dt, dj);
-                double ratio = exp(((xt - xp) - (xd - xq)) / tb) * (Zq / Zp);
+                 * underflow when both probabilities are tiny; a row of all -inf is a
+                 * point mass, whose probability is exact */
+                double ratio;
+                if (xp == -INFINITY || xq == -INFINITY) {
+                    ratio = pt / pd;
+                } else {
+                    double xt = logit_at(rowT + (size_t)j * (size_t)V * es, dt, dj);
+                    double xd = logit_at(rowQ + (size_t)j * (size_t)V * es, dt, dj);
+                    ratio = exp(((xt - xp) - (xd - xq)) / tb) * (Zq / Zp);
+                }
                 accept = ua <= ratio;
                 if (mg)
                     mg[j * 4 + 0] = fabs(ua - ratio);

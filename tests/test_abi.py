@@ -1,0 +1,62 @@
+"""The C-ABI library loads on any host and exports every entry point its header
+declares; host-side argument checks answer before any CUDA call (no GPU needed)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import verify_spec_greedy_gb300 as lib
+from verify_spec_greedy_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def so():
+    cuda_build.build()
+    return lib.load()
+
+
+def _declared():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                            src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    assert _declared() == sorted([
+        "mtp_draft_input", "mtp_draft_input_workspace_bytes", "mtp_greedy_draft",
+        "spec_verify_greedy", "spec_verify_sample", "spec_verify_workspace_bytes",
+        "mtpspec_status_string"])
+
+
+def test_every_declared_symbol_is_exported(so):
+    for name in _declared():
+        assert hasattr(so, name), name
+
+
+def test_status_strings(so):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.status_string(code).startswith("MTPSPEC")
+    assert "unknown" in lib.status_string(42)
+
+
+def test_host_side_validation(so):
+    nul = None
+    assert so.mtp_greedy_draft(nul, 7, 1, 10, nul, nul) == -2           # dtype
+    assert so.mtp_greedy_draft(nul, 0, 1, 0, nul, nul) == -3            # V < 1
+    assert so.mtp_greedy_draft(nul, 0, 0, 10, nul, nul) == 0            # empty: no work
+    assert so.mtp_greedy_draft(nul, 0, 1, 10, nul, nul) == -1           # null pointers
+    assert so.mtp_greedy_draft(C.c_void_p(2), 0, 1, 10, C.c_void_p(16), nul) == -1  # misaligned
+    assert so.spec_verify_greedy(nul, 0, nul, 1, 0, 10, nul, nul, nul, nul) == -3   # D < 1
+    assert so.spec_verify_greedy(nul, 0, nul, 1, 65, 10, nul, nul, nul, nul) == -3  # D > 64
+    assert so.spec_verify_greedy(nul, 0, nul, 0, 3, 10, nul, nul, nul, nul) == 0    # B == 0
+    assert so.spec_verify_greedy(nul, 1, nul, 2, 3, 10, nul, nul, nul, nul) == -1
+    assert so.spec_verify_greedy(nul, 0, nul, 1, 1, 2**31, nul, nul, nul, nul) == -3

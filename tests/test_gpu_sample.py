@@ -1,0 +1,241 @@
+"""GPU parity of spec_verify_sample against the CPU oracle.
+
+The bar: token ids and accepted counts are bit-exact on every row except "margin rows",
+rows where a floating-point decision of some unit sits within 1e-5 of its boundary: the
+accept test |U - p/q| (the stated rule; these rows must stay below 1e-4 of the rows), and,
+by the same reading, a top-p boundary |S - p| or the draw's inverse-CDF position relative
+to the draw's total.  Each category is counted; every row that differs must be a margin
+row.  p_target / p_draft agree to 1e-5 relative (with an absolute floor of 1e-30 for
+values below fp32's normal range) on every unit whose top-p boundaries are not marginal.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import verify_spec_greedy_gb300 as lib
+from verify_spec_greedy_gb300.inputs import (WORKLOADS, Workload, f32_to_bf16_bits,
+                                             make_verify_inputs)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+MARGIN = 1e-5
+P_RTOL = 1e-5
+P_ATOL = 1e-30
+
+TOTAL = {"rows": 0, "margin_rows": 0, "accept_margin_rows": 0, "topp_margin_rows": 0,
+         "cdf_margin_rows": 0, "mismatch_rows": 0}
+
+
+def _dev(a):
+    if a is None:
+        return None
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(DEV).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def gpu_verify(x, T_dev=None, Q_dev=None):
+    B, D = x["d"].shape
+    T = _dev(x["T"]) if T_dev is None else T_dev
+    Q = _dev(x["Q"]) if Q_dev is None else Q_dev
+    out = torch.full((B, D + 1), -9, dtype=torch.int32, device=DEV)
+    na = torch.full((B,), -9, dtype=torch.int32, device=DEV)
+    pt = torch.full((B, D), -1.0, dtype=torch.float32, device=DEV)
+    pd = torch.full((B, D), -1.0, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(lib.spec_verify_workspace_bytes(B, D, T.shape[-1]), dtype=torch.uint8,
+                     device=DEV)
+    lib.spec_verify_sample(T, Q, _dev(x["d"]), _dev(x["tau"]), _dev(x.get("top_k")),
+                           _dev(x.get("top_p")), x["seed"], out, na, pt, pd, ws, st)
+    torch.cuda.synchronize()
+    return dict(out=out.cpu().numpy(), num_accepted=na.cpu().numpy(), p_target=pt.cpu().numpy(),
+                p_draft=pd.cpu().numpy(), status=int(st.item()))
+
+
+def oracle_verify(x, rows=None):
+    return oracle.verify_sample_rows(x["T"], x["Q"], x["d"], x["tau"], x.get("top_k"),
+                                     x.get("top_p"), x["seed"], rows=rows)
+
+
+def compare(g, o, rows=None, label=""):
+    """Assert parity under the margin rule; returns (rows, margin rows)."""
+    if rows is not None:
+        g = {k: (v[rows] if isinstance(v, np.ndarray) else v) for k, v in g.items()}
+    mg = o["margins"]                        # [B, D+1, 4]
+    acc_m = (mg[:, :, 0] < MARGIN).any(1)
+    topp_m = (mg[:, :, 1:3] < MARGIN).any((1, 2))
+    cdf_m = (mg[:, :, 3] < MARGIN).any(1)
+    margin_row = acc_m | topp_m | cdf_m
+    same = (g["out"] == o["out"]).all(1) & (g["num_accepted"] == o["num_accepted"])
+    for b in np.nonzero(~same)[0]:
+        print(f"[{label}] row {b} differs: gpu {g['out'][b]} oracle {o['out'][b]}; "
+              f"min margins accept {mg[b, :, 0].min():.3g} top-p {mg[b, :, 1:3].min():.3g} "
+              f"cdf {mg[b, :, 3].min():.3g}")
+    bad = ~same & ~margin_row
+    assert not bad.any(), (
+        f"{label}: {bad.sum()} non-margin rows differ, e.g. row {np.argmax(bad)}: gpu "
+        f"{g['out'][np.argmax(bad)]} / oracle {o['out'][np.argmax(bad)]}")
+    # probabilities on units whose top-p boundaries are not marginal
+    D = g["p_target"].shape[1]
+    ok_t = ~(mg[:, :D, 1] < MARGIN)
+    ok_q = ~(mg[:, :D, 2] < MARGIN) & ok_t
+    for key, ok in (("p_target", ok_t), ("p_draft", ok_q)):
+        gv, ov = g[key][ok].astype(np.float64), o[key][ok]
+        err = np.abs(gv - ov)
+        tol = P_RTOL * np.abs(ov) + P_ATOL
+        assert (err <= tol).all(), (
+            f"{label}: {key} off by {np.max(err / (np.abs(ov) + 1e-300)):.3g} relative")
+    n = len(g["out"])
+    TOTAL["rows"] += n
+    TOTAL["margin_rows"] += int(margin_row.sum())
+    TOTAL["accept_margin_rows"] += int(acc_m.sum())
+    TOTAL["topp_margin_rows"] += int(topp_m.sum())
+    TOTAL["cdf_margin_rows"] += int(cdf_m.sum())
+    TOTAL["mismatch_rows"] += int((~same).sum())
+    return n, int(margin_row.sum())
+
+
+# ---------------------------------------------------------------- the five workloads
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_full_size(name):
+    w = WORKLOADS[name]
+    if w.mode == "greedy":
+        w = w.scaled(mode="sample", tau=0.9, top_k=40, top_p=0.95, greedy_frac=0.0)
+    x = make_verify_inputs(w)
+    g = gpu_verify(x)
+    o = oracle_verify(x)
+    assert g["status"] == o["status"] == 0
+    compare(g, o, label=name)
+    assert ((g["num_accepted"] >= 0) & (g["num_accepted"] <= w.D)).all()
+
+
+@pytest.mark.parametrize("seed", [11, 12, 13])
+def test_serving_mix_more_seeds(seed):
+    w = WORKLOADS["serve_b256_d3_v152k"].scaled(B=96, seed=seed, philox_seed=seed * 7)
+    x = make_verify_inputs(w)
+    compare(gpu_verify(x), oracle_verify(x), label=f"serve seed {seed}")
+
+
+# ---------------------------------------------------------------- ragged sizes, filters
+
+CASES = [
+    # V, D, dtype, tau, k, p
+    (16, 1, "f32", 1.0, 0, 1.0),
+    (17, 2, "f32", 0.7, 5, 0.9),
+    (33, 3, "bf16", 1.0, 8, 0.95),
+    (1000, 2, "f32", 0.5, 1, 1.0),
+    (4097, 5, "f32", 1.3, 0, 0.8),
+    (4099, 3, "bf16", 0.9, 100, 0.6),
+    (40001, 4, "f32", 0.8, 2000, 0.9),
+    (65537, 2, "bf16", 1.0, 0, 0.97),
+    (151936, 1, "f32", 2.0, 0, 0.5),
+    (262147, 2, "bf16", 1.0, 64, 0.95),
+]
+
+
+@pytest.mark.parametrize("V,D,dtype,tau,k,p", CASES)
+def test_ragged_and_filters(V, D, dtype, tau, k, p):
+    w = Workload(name="c", B=6 if V > 60000 else 24, D=D, V=V, H=8, dtype=dtype, tau=tau,
+                 top_k=k, top_p=p, t_std=3.0, q_noise=1.0, seed=V + D, philox_seed=V)
+    x = make_verify_inputs(w)
+    compare(gpu_verify(x), oracle_verify(x), label=f"V={V} D={D} {dtype} k={k} p={p}")
+
+
+def test_mixed_rows_in_one_batch():
+    # per-row temperature (0 = greedy), top-k and top-p all differ across the batch
+    rng = np.random.default_rng(3)
+    w = Workload(name="mix", B=48, D=3, V=20011, H=8, tau=1.0, t_std=3.0, q_noise=1.5, seed=9,
+                 philox_seed=99)
+    x = make_verify_inputs(w)
+    x["tau"] = rng.choice([0.0, 0.3, 0.8, 1.5, 4.0], size=w.B).astype(np.float32)
+    x["top_k"] = rng.choice([0, 1, 3, 50, 20011, 30000], size=w.B).astype(np.int32)
+    x["top_p"] = rng.choice([1.0, 0.99, 0.9, 0.5, 1e-4], size=w.B).astype(np.float32)
+    compare(gpu_verify(x), oracle_verify(x), label="mixed rows")
+
+
+@pytest.mark.parametrize("p", [0.9999, 0.99999])
+def test_top_p_near_one_uses_exact_search(p):
+    # the boundary falls where the weights are below the binned range
+    w = Workload(name="p1", B=8, D=2, V=30000, H=8, tau=0.25, top_p=p, t_std=3.0, q_noise=0.5,
+                 seed=4, philox_seed=4)
+    x = make_verify_inputs(w)
+    compare(gpu_verify(x), oracle_verify(x), label=f"p={p}")
+
+
+def test_large_k_and_flat_rows_use_exact_search():
+    # k far beyond the binned range at a small temperature; and rows of one repeated value
+    w = Workload(name="k", B=8, D=2, V=50000, H=8, tau=0.05, top_k=40000, top_p=0.9, t_std=3.0,
+                 q_noise=0.5, seed=5, philox_seed=5)
+    x = make_verify_inputs(w)
+    compare(gpu_verify(x), oracle_verify(x), label="large k")
+    w2 = Workload(name="flat", B=6, D=2, V=9000, H=8, dtype="bf16", tau=1.0, top_k=100,
+                  top_p=0.5, seed=6, philox_seed=6)
+    x2 = make_verify_inputs(w2)
+    x2["T"][:] = f32_to_bf16_bits(np.float32(1.5))
+    x2["T"][:, :, ::7] = f32_to_bf16_bits(np.float32(1.25))
+    compare(gpu_verify(x2), oracle_verify(x2), label="flat bf16")
+
+
+def test_negative_infinity_and_degenerate_rows():
+    w = Workload(name="ninf", B=12, D=2, V=5000, H=8, tau=1.0, top_k=30, top_p=0.9, seed=7,
+                 philox_seed=7)
+    x = make_verify_inputs(w)
+    x["T"][:, :, 100:4000] = -np.inf
+    x["Q"][:, :, 200:4500] = -np.inf
+    x["T"][0] = -np.inf          # row 0: every target position is a point mass on id 0
+    x["Q"][1] = -np.inf          # row 1: every draft position is a point mass on id 0
+    x["d"][0] = 0
+    x["d"][1, 0] = 0
+    compare(gpu_verify(x), oracle_verify(x), label="-inf")
+
+
+def test_invalid_draft_ids_and_bad_params_set_status():
+    w = Workload(name="bad", B=6, D=3, V=3001, H=8, tau=1.0, top_p=0.9, seed=8, philox_seed=8)
+    x = make_verify_inputs(w)
+    x["d"][2, 1] = w.V
+    x["d"][3, 0] = -5
+    g = gpu_verify(x)
+    o = oracle_verify(x)
+    assert g["status"] & lib.STATUS_BAD_DRAFT_ID
+    assert o["status"] & oracle.STATUS_BAD_DRAFT_ID
+    compare(g, o, label="bad ids")
+    assert g["num_accepted"][3] == 0 and g["p_target"][3, 0] == 0
+    # a negative temperature is reported and the row is verified greedily
+    x["tau"][4] = -1.0
+    g = gpu_verify(x)
+    assert g["status"] & lib.STATUS_BAD_PARAM
+    go, gn, _ = oracle.verify_greedy(x["T"][4:5], x["d"][4:5])
+    np.testing.assert_array_equal(g["out"][4], go[0])
+
+
+def test_unaligned_rows():
+    # V odd: rows start at arbitrary 4- or 2-byte offsets
+    for dtype in ("f32", "bf16"):
+        w = Workload(name="odd", B=10, D=3, V=12343, H=8, dtype=dtype, tau=0.9, top_k=64,
+                     top_p=0.92, seed=10, philox_seed=10)
+        x = make_verify_inputs(w)
+        compare(gpu_verify(x), oracle_verify(x), label=f"odd {dtype}")
+
+
+def test_deterministic_and_seed_sensitive():
+    w = WORKLOADS["sample_b8_d3_v152k"]
+    x = make_verify_inputs(w)
+    a, b = gpu_verify(x), gpu_verify(x)
+    for k in ("out", "num_accepted", "p_target", "p_draft"):
+        np.testing.assert_array_equal(a[k], b[k])
+    x2 = dict(x, seed=x["seed"] + 1)
+    c = gpu_verify(x2)
+    compare(c, oracle_verify(x2), label="seed+1")
+
+
+def test_margin_rows_are_rare():
+    # many rows at a moderate vocabulary; the stated budget: rows whose accept margin is
+    # below 1e-5 stay under 1e-4 of the rows.  The other categories are reported.
+    w = Workload(name="many", B=4000, D=3, V=2048, H=8, tau_range=(0.5, 1.2), top_k=200,
+                 top_p=0.9, t_std=3.0, q_noise_range=(0.3, 2.0), seed=12, philox_seed=12)
+    x = make_verify_inputs(w)
+    compare(gpu_verify(x), oracle_verify(x), label="many rows")
+    print("margin accounting:", TOTAL)
+    assert TOTAL["accept_margin_rows"] <= max(1, 1e-4 * TOTAL["rows"]), TOTAL

@@ -190,3 +190,22 @@ def test_draws_take_the_inverse_cdf_in_ascending_id_order():
     for b in range(N):
         us = oracle.uniforms(99, b, 1)[1]
         assert r["out"][b, 1] == kept[int(us * 4)]
+
+
+def test_all_negative_infinity_rows_are_point_masses_on_id_0():
+    V, N = 6, 2000
+    t = np.full(V, -np.inf, np.float32)
+    q = np.array([0.0, 1.0, -1.0, 0.5, -np.inf, 2.0], np.float32)
+    T, Q = _rows(np.stack([t, t]), q[None], N)
+    Qd = oracle.filter_probs(q, 1.0)
+    # draft 0: p(0) = 1 >= q(0), always kept; any other draft: outside p's support
+    r = oracle.verify_sample(T, Q, np.zeros((N, 1), np.int32), np.ones(N, np.float32), seed=1)
+    assert (r["num_accepted"] == 1).all() and (r["out"][:, 1] == 0).all()
+    np.testing.assert_allclose(r["p_draft"][:, 0], Qd[0])
+    r = oracle.verify_sample(T, Q, np.full((N, 1), 3, np.int32), np.ones(N, np.float32), seed=2)
+    assert (r["num_accepted"] == 0).all() and (r["out"][:, 0] == 0).all()
+    # the draft side degenerate: q = point mass on 0, accepted with probability p(0)
+    T2, Q2 = _rows(np.stack([q, q]), t[None], N)
+    r = oracle.verify_sample(T2, Q2, np.zeros((N, 1), np.int32), np.ones(N, np.float32), seed=3)
+    want = oracle.filter_probs(q, 1.0)[0]
+    assert abs((r["num_accepted"] == 1).mean() - want) < 4.5 * np.sqrt(want * (1 - want) / N)

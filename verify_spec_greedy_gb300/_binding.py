@@ -1,0 +1,141 @@
+"""ctypes binding of libmtpspec: argument marshalling only.
+
+Every function has the name of the C entry point it calls (include/libmtpspec.h) and
+takes torch tensors that already live on the GPU; it passes their device pointers,
+sizes and the current CUDA stream to the library and raises MtpSpecError on a non-zero
+status.  All computation happens in the library's CUDA kernels.  There is no fallback:
+if the library has not been built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmtpspec.so")
+
+F32, BF16 = 0, 1
+STATUS_BAD_DRAFT_ID = 0x1
+STATUS_BAD_PARAM = 0x2
+STATUS_TIMEOUT = 0x4
+
+_lib = None
+
+
+class MtpSpecError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn}: {status_string(code)} ({code})")
+
+
+def load():
+    """Load libmtpspec.so (built by verify_spec_greedy_gb300.build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmtpspec is not built ({LIB_PATH} missing); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = C.CDLL(LIB_PATH)
+    p, i64, i32, u64, sz, f32 = (C.c_void_p, C.c_int64, C.c_int32, C.c_uint64, C.c_size_t,
+                                 C.c_float)
+    sigs = {
+        "mtp_draft_input": ([p, p, p, p, p, p, i64, i64, f32, p, sz, p], C.c_int),
+        "mtp_draft_input_workspace_bytes": ([i64, i64], sz),
+        "mtp_greedy_draft": ([p, C.c_int, i64, i64, p, p], C.c_int),
+        "spec_verify_greedy": ([p, C.c_int, p, i64, i32, i64, p, p, p, p], C.c_int),
+        "spec_verify_sample": ([p, p, C.c_int, p, p, p, p, u64, i64, i32, i64, p, p, p, p, p, sz,
+                                p, p], C.c_int),
+        "spec_verify_workspace_bytes": ([i64, i32, i64], sz),
+        "mtpspec_status_string": ([C.c_int], C.c_char_p),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(lib, name, None)
+        if fn is not None:
+            fn.argtypes = args
+            fn.restype = res
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().mtpspec_status_string(int(code)).decode()
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _call(name, *args):
+    rc = getattr(load(), name)(*args)
+    if rc != 0:
+        raise MtpSpecError(name, rc)
+
+
+# ---------------------------------------------------------------- entry points
+
+def mtp_draft_input_workspace_bytes(M: int, H: int) -> int:
+    return int(load().mtp_draft_input_workspace_bytes(int(M), int(H)))
+
+
+def mtp_draft_input(emb_next, hidden, enorm_w, hnorm_w, eh_proj_w, out, eps: float,
+                    workspace=None, stream=None):
+    """out[M, H] = eh_proj_w @ [enorm(emb_next); hnorm(hidden)] (all bf16 on the GPU)."""
+    M, H = emb_next.shape
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _call("mtp_draft_input", _ptr(emb_next), _ptr(hidden), _ptr(enorm_w), _ptr(hnorm_w),
+          _ptr(eh_proj_w), _ptr(out), M, H, float(eps), _ptr(workspace), ws, _stream(stream))
+    return out
+
+
+def mtp_greedy_draft(logits, out_ids, stream=None):
+    """out_ids[M] = argmax of each row of logits[M, V] (lowest id on ties)."""
+    M, V = logits.shape
+    _call("mtp_greedy_draft", _ptr(logits), _dtype_code(logits), M, V, _ptr(out_ids),
+          _stream(stream))
+    return out_ids
+
+
+def spec_verify_greedy(target_logits, draft_ids, out_tokens, num_accepted, status=None,
+                       stream=None):
+    """Greedy verification of draft_ids[B, D] against target_logits[B, D+1, V]."""
+    B, D1, V = target_logits.shape
+    _call("spec_verify_greedy", _ptr(target_logits), _dtype_code(target_logits), _ptr(draft_ids),
+          B, D1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(status), _stream(stream))
+    return out_tokens, num_accepted
+
+
+def spec_verify_workspace_bytes(B: int, D: int, V: int) -> int:
+    return int(load().spec_verify_workspace_bytes(int(B), int(D), int(V)))
+
+
+def spec_verify_sample(target_logits, draft_logits, draft_ids, temperature, top_k, top_p,
+                       seed: int, out_tokens, num_accepted, p_target=None, p_draft=None,
+                       workspace=None, status=None, stream=None):
+    """Speculative-sampling verification (see include/libmtpspec.h)."""
+    B, D1, V = target_logits.shape
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _call("spec_verify_sample", _ptr(target_logits), _ptr(draft_logits),
+          _dtype_code(target_logits), _ptr(draft_ids), _ptr(temperature), _ptr(top_k),
+          _ptr(top_p), int(seed) & 0xFFFFFFFFFFFFFFFF, B, D1 - 1, V, _ptr(out_tokens),
+          _ptr(num_accepted), _ptr(p_target), _ptr(p_draft), _ptr(workspace), ws, _ptr(status),
+          _stream(stream))
+    return out_tokens, num_accepted

@@ -1,0 +1,214 @@
+// The MTP draft head's input stage: y = eh_proj_w @ [enorm(emb_next); hnorm(hidden)]
+// ("14. MTP: speculative decoding with the built-in draft head", "The draft head":
+// fc(cat(norm(e_{t+1}), norm(h_t))) with fc = Linear(2H, H, bias=False); "MPT (MTP,
+// Multi-Token Prediction) 原理详解" section 二.2 steps 2-3: enorm, hnorm, concat with the
+// embedding first, eh_proj).  RMSNorm: v / sqrt(mean(v^2) + eps) * w, rounded to bf16.
+//
+// Two paths, chosen by the token count M:
+//  - small M: one fused kernel.  Each CTA normalises the M tokens into shared memory (bf16,
+//    2H values each), then its warps stream rows of the weight once from HBM with 16-byte
+//    loads and reduce the M dot products per row.  HBM-bound on the weight.
+//  - larger M: a normalisation pass writes the bf16 activations [M, 2H] to the workspace,
+//    then the tcgen05 GEMM (tcgen05_gemm.cu) computes the projection on the tensor cores.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mtpspec {
+namespace di {
+
+constexpr int GEMV_THREADS = 256;
+constexpr int GEMV_WARPS = GEMV_THREADS / 32;
+constexpr int GEMV_UNROLL = 4;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+    __nv_bfloat16 b = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t *>(&b);
+}
+
+// Sum over the block; every thread gets the result.
+template <int NTH>
+__device__ __forceinline__ float block_sum(float v, float *scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    float t = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NTH / 32; ++w) t += scratch[w];
+    return t;
+}
+
+// out[i] = bf16(v[i] * r * w[i]) for one H-vector, r = 1/sqrt(mean(v^2) + eps).  All
+// threads of the block call it.  H % 8 == 0 and 16-byte aligned vectors.
+template <int NTH>
+__device__ __forceinline__ void rmsnorm_row(const uint16_t *__restrict__ v,
+                                            const uint16_t *__restrict__ w, int H, float eps,
+                                            uint16_t *out, float *scratch) {
+    const uint4 *vv = reinterpret_cast<const uint4 *>(v);
+    const int nv = H / 8;
+    float ss = 0.0f;
+    for (int i = threadIdx.x; i < nv; i += NTH) {
+        const uint4 q = vv[i];
+        const uint32_t a[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float x0 = bf16_lo(a[t]), x1 = bf16_hi(a[t]);
+            ss = fmaf(x0, x0, ss);
+            ss = fmaf(x1, x1, ss);
+        }
+    }
+    ss = block_sum<NTH>(ss, scratch);
+    const float r = 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
+    const uint4 *ww = reinterpret_cast<const uint4 *>(w);
+    uint4 *oo = reinterpret_cast<uint4 *>(out);
+    for (int i = threadIdx.x; i < nv; i += NTH) {
+        const uint4 q = vv[i], g = ww[i];
+        const uint32_t a[4] = {q.x, q.y, q.z, q.w}, b[4] = {g.x, g.y, g.z, g.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const uint16_t lo = f32_to_bf16_bits(bf16_lo(a[t]) * r * bf16_lo(b[t]));
+            const uint16_t hi = f32_to_bf16_bits(bf16_hi(a[t]) * r * bf16_hi(b[t]));
+            o[t] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
+        oo[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// Fused norm + GEMV for MT tokens: blockIdx.x owns output rows
+// [blockIdx.x * rows_per_cta, ...), one warp per row at a time.
+template <int MT>
+__global__ void __launch_bounds__(GEMV_THREADS)
+k_draft_gemv(const uint16_t *__restrict__ e, const uint16_t *__restrict__ h,
+             const uint16_t *__restrict__ we, const uint16_t *__restrict__ wh,
+             const uint16_t *__restrict__ W, uint16_t *__restrict__ y, int H, float eps,
+             int rows_per_cta) {
+    extern __shared__ __align__(16) uint16_t xs[];  // [MT][2H] normalised activations
+    __shared__ float scratch[GEMV_WARPS];
+    const int K = 2 * H;
+    for (int t = 0; t < MT; ++t) {
+        rmsnorm_row<GEMV_THREADS>(e + static_cast<size_t>(t) * H, we, H, eps, xs + t * K, scratch);
+        rmsnorm_row<GEMV_THREADS>(h + static_cast<size_t>(t) * H, wh, H, eps, xs + t * K + H,
+                                  scratch);
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nv = K / 8;  // 16-byte vectors per weight row
+    const int r0 = blockIdx.x * rows_per_cta;
+    const int r1 = min(H, r0 + rows_per_cta);
+    for (int o = r0 + warp; o < r1; o += GEMV_WARPS) {
+        const uint4 *wr = reinterpret_cast<const uint4 *>(W + static_cast<size_t>(o) * K);
+        float acc[MT];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
+        for (int v0 = lane; v0 < nv; v0 += 32 * GEMV_UNROLL) {
+            uint4 q[GEMV_UNROLL];
+#pragma unroll
+            for (int u = 0; u < GEMV_UNROLL; ++u) {
+                const int vi = v0 + u * 32;
+                if (vi < nv) q[u] = ld_stream_16B(wr + vi);
+            }
+#pragma unroll
+            for (int u = 0; u < GEMV_UNROLL; ++u) {
+                const int vi = v0 + u * 32;
+                if (vi >= nv) continue;
+                const uint32_t a[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    const uint4 xv = reinterpret_cast<const uint4 *>(xs + t * K)[vi];
+                    const uint32_t b[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        acc[t] = fmaf(bf16_lo(a[c]), bf16_lo(b[c]), acc[t]);
+                        acc[t] = fmaf(bf16_hi(a[c]), bf16_hi(b[c]), acc[t]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            float v = acc[t];
+#pragma unroll
+            for (int s = 16; s > 0; s >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, s);
+            if (lane == 0) y[static_cast<size_t>(t) * H + o] = f32_to_bf16_bits(v);
+        }
+    }
+}
+
+// Normalisation pass of the tensor-core path: one CTA per (token, half).
+__global__ void __launch_bounds__(256)
+k_draft_norm(const uint16_t *__restrict__ e, const uint16_t *__restrict__ h,
+             const uint16_t *__restrict__ we, const uint16_t *__restrict__ wh,
+             uint16_t *__restrict__ xn, int H, float eps) {
+    __shared__ float scratch[8];
+    const int t = blockIdx.x >> 1, half = blockIdx.x & 1;
+    const uint16_t *v = (half ? h : e) + static_cast<size_t>(t) * H;
+    rmsnorm_row<256>(v, half ? wh : we, H, eps, xn + static_cast<size_t>(t) * 2 * H + half * H,
+                     scratch);
+}
+
+}  // namespace di
+
+constexpr int kGemvMaxTokens = 4;
+
+bool draft_input_uses_gemv(int64_t M, int64_t H) {
+    (void)H;
+    return M <= kGemvMaxTokens;
+}
+
+size_t draft_input_workspace_bytes(int64_t M, int64_t H) {
+    if (draft_input_uses_gemv(M, H)) return 0;
+    const size_t xn = static_cast<size_t>(M) * static_cast<size_t>(2 * H) * 2;
+    return ((xn + 1023) & ~static_cast<size_t>(1023)) + gemm_workspace_bytes(M, H);
+}
+
+template <int MT>
+static cudaError_t launch_gemv(const DraftInputArgs &a, cudaStream_t stream) {
+    const int H = static_cast<int>(a.H);
+    const size_t smem = static_cast<size_t>(MT) * 2 * H * 2;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(di::k_draft_gemv<MT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    // enough CTAs for a few waves over 152 SMs, whole warps of rows each
+    int rows = (H + 4 * 152 - 1) / (4 * 152);
+    rows = ((rows + di::GEMV_WARPS - 1) / di::GEMV_WARPS) * di::GEMV_WARPS;
+    const int grid = (H + rows - 1) / rows;
+    di::k_draft_gemv<MT><<<grid, di::GEMV_THREADS, smem, stream>>>(
+        static_cast<const uint16_t *>(a.e), static_cast<const uint16_t *>(a.h),
+        static_cast<const uint16_t *>(a.we), static_cast<const uint16_t *>(a.wh),
+        static_cast<const uint16_t *>(a.W), static_cast<uint16_t *>(a.y), H, a.eps, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t run_draft_input(const DraftInputArgs &a, cudaStream_t stream) {
+    if (draft_input_uses_gemv(a.M, a.H)) {
+        switch (a.M) {
+        case 1: return launch_gemv<1>(a, stream);
+        case 2: return launch_gemv<2>(a, stream);
+        case 3: return launch_gemv<3>(a, stream);
+        default: return launch_gemv<4>(a, stream);
+        }
+    }
+    uint16_t *xn = static_cast<uint16_t *>(a.workspace);
+    const size_t xn_bytes = static_cast<size_t>(a.M) * static_cast<size_t>(2 * a.H) * 2;
+    void *gemm_ws = static_cast<unsigned char *>(a.workspace) + ((xn_bytes + 1023) & ~static_cast<size_t>(1023));
+    di::k_draft_norm<<<static_cast<unsigned>(2 * a.M), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(a.e), static_cast<const uint16_t *>(a.h),
+        static_cast<const uint16_t *>(a.we), static_cast<const uint16_t *>(a.wh), xn,
+        static_cast<int>(a.H), a.eps);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return run_gemm_bf16_nt(a.W, xn, a.y, a.H, a.M, 2 * a.H, gemm_ws, stream);
+}
+
+}  // namespace mtpspec

@@ -1,0 +1,73 @@
+// Host-side launchers of libmtpspec's kernels (called by the C-ABI entry points in
+// api.cu after argument validation).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mtpspec {
+
+cudaError_t run_greedy_draft(const void *logits, int dtype, int64_t M, int64_t V, int32_t *ids,
+                             cudaStream_t stream);
+
+cudaError_t run_verify_greedy(const void *target, int dtype, const int32_t *d, int64_t B,
+                              int32_t D, int64_t V, int32_t *tokens, int32_t *num_accepted,
+                              int32_t *status, cudaStream_t stream);
+
+}  // namespace mtpspec
+
+namespace mtpspec {
+
+struct VerifySampleArgs {
+    const void *target;
+    const void *draft;
+    int dtype;
+    const int32_t *draft_ids;
+    const float *temperature;
+    const int32_t *top_k;
+    const float *top_p;
+    uint64_t seed;
+    int64_t B;
+    int32_t D;
+    int64_t V;
+    int32_t *out_tokens;
+    int32_t *num_accepted;
+    float *p_target;
+    float *p_draft;
+    void *workspace;
+    int32_t *status;
+};
+
+// Bytes of per-unit results the sampling verifier keeps between its two kernels.
+size_t verify_workspace_bytes(int64_t B, int32_t D);
+
+// Whether one cluster's shared memory can hold a row of V logits of this element size.
+bool verify_fits(int64_t V, size_t elem_bytes);
+
+cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream);
+
+}  // namespace mtpspec
+
+namespace mtpspec {
+
+struct DraftInputArgs {
+    const void *e, *h, *we, *wh, *W;
+    void *y;
+    int64_t M, H;
+    float eps;
+    void *workspace;
+};
+
+// Whether (M, H) takes the fused norm + GEMV path (no workspace).
+bool draft_input_uses_gemv(int64_t M, int64_t H);
+size_t draft_input_workspace_bytes(int64_t M, int64_t H);
+cudaError_t run_draft_input(const DraftInputArgs &a, cudaStream_t stream);
+
+// Tensor-core GEMM Y[Mt, H] = B[Mt, K] @ A[H, K]^T (bf16, fp32 accumulate) and its
+// workspace (a flag word and split-K partial sums).
+size_t gemm_workspace_bytes(int64_t Mt, int64_t H);
+cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, int64_t Mt,
+                             int64_t K, void *workspace, cudaStream_t stream);
+
+}  // namespace mtpspec
