@@ -1,0 +1,441 @@
+"""Benchmark of the libmtpspec hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of a synthetic workload:
+  1. mtp_draft_input     the draft head's input stage for the batch's M tokens
+  2. mtp_greedy_draft    greedy drafts of the greedy rows (written into their draft ids)
+  3. spec_verify_sample  verification of every row (greedy rows by the greedy rule)
+The default workload is the batched-serving one: 256 rows x 3 drafts over a 151,936-id
+vocabulary in fp32 (a quarter of the rows greedy, the rest sampled at temperatures
+U[0.5, 1.2] with top-p 0.9), 768 draft-input tokens of hidden size 4096.  Its inputs
+(1.2 GB per step) are larger than L2, so every step reads them from HBM.
+
+Metric: verify rows per second (a row is one (b, j) logit row of V; B*(D+1) per step).
+Prints one JSON line.  `--impl reference` times the CPU oracle instead (a bounded sample
+of the same workload on the host cores).  Multi-GPU: one process per GPU, each running
+an independent replica (the rows of a batch are independent; no collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "verify rows/s (B·(D+1)·V logits) & HBM GB/s vs 8 TB/s roofline; 1×GB300"
+UNIT = "rows/s"
+DEFAULT_WORKLOAD = "serve_b256_d3_v152k"
+L2_BYTES = 129 * 1024 * 1024
+PROFILE_FILE = os.path.join(ROOT, "profiles", "verify_sample_serve_b256_d3_v152k.md")
+KERNEL_SOURCES = ["verify_spec_greedy_gb300/csrc/verify_sample.cu",
+                  "verify_spec_greedy_gb300/csrc/common.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["libmtpspec", "reference"], default="libmtpspec")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-launch-count", action="store_true",
+                    help="skip the CUDA-profiler launch count (needed under ncu)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's row count (profiling on a smaller case)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_init(n):
+    if n <= 1 or "RANK" not in os.environ:
+        return 0, 1, None
+    import torch
+    import torch.distributed as dist
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl")
+    return dist.get_rank(), dist.get_world_size(), dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x, dist):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- workload bytes
+
+def verify_bytes(x):
+    """Algorithmic bytes of one spec_verify_sample call: each target row read once, each
+    draft row of a sampled row read once (greedy rows need no draft logits), plus the
+    per-row inputs and outputs."""
+    B, D, V = x["B"], x["D"], x["V"]
+    es = 4 if x["dtype"] == "f32" else 2
+    n_greedy = int((x["tau"] == 0).sum())
+    t_rows = B * (D + 1)
+    q_rows = (B - n_greedy) * D
+    small = B * D * 4 + B * 4 * 3 + B * (D + 1) * 4 + B * 4 + 2 * B * D * 4
+    return (t_rows + q_rows) * V * es + small
+
+
+def draft_input_bytes(w):
+    return 2 * w.H * 2 * w.H + 2 * w.tokens * w.H * 2 + 2 * w.H * 2 + w.tokens * w.H * 2
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- roofline inputs
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the verify kernel from the committed ncu summary, if it
+    was taken on this workload with the current kernel source; else None."""
+    if not os.path.exists(PROFILE_FILE) or workload != DEFAULT_WORKLOAD:
+        return None
+    src, traffic = None, None
+    for line in open(PROFILE_FILE):
+        if line.startswith("kernel_source_sha256:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            try:
+                traffic = float(line.split(":", 1)[1].strip())
+            except ValueError:
+                traffic = None
+    return traffic if src == kernel_hash() else None
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+
+def oracle_sample(x, di, w, rows):
+    """Time the oracle on a bounded sample: `rows` rows of the verify (the workload's mix
+    of greedy and sampled rows) plus the draft-input tokens of those rows and the greedy
+    drafts of the greedy rows among them, spread over the host cores."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    cores = os.cpu_count() or 1
+    B = x["B"]
+    ng = int((x["tau"] == 0).sum())
+    n_g = max(1, round(rows * ng / B)) if ng else 0
+    sel = list(range(n_g)) + list(range(ng, ng + rows - n_g))
+    tok_per_row = max(1, w.tokens // B)
+    ntok = tok_per_row * len(sel)
+    e, h = di["e"][0][:ntok], di["h"][0][:ntok]
+    chunks = [(i, min(ntok, i + 4)) for i in range(0, ntok, 4)]
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(cores) as ex:
+        futs = [ex.submit(oracle.draft_input, e[a:b], h[a:b], di["we"], di["wh"], di["W"],
+                          di["eps"]) for a, b in chunks]
+        if n_g:
+            futs.append(ex.submit(oracle.greedy_draft,
+                                  x["Q"][:n_g].reshape(-1, x["V"])))
+        for f in futs:
+            f.result()
+    oracle.verify_sample_rows(x["T"], x["Q"], x["d"], x["tau"], x["top_k"], x["top_p"],
+                              x["seed"], rows=sel, threads=cores)
+    dt = time.perf_counter() - t0
+    rows_verified = len(sel) * (x["D"] + 1)
+    sample = (f"{len(sel)} of {B} rows ({n_g} greedy) of {w.name}: their verify, their "
+              f"{ntok} draft-input tokens and the greedy drafts of the greedy rows")
+    return rows_verified / dt, cores, sample, dt
+
+
+# ---------------------------------------------------------------- the GPU arm
+
+def run_gpu(args, rank, world, dist):
+    import torch
+    import verify_spec_greedy_gb300 as lib
+    from verify_spec_greedy_gb300.inputs import WORKLOADS, make_draft_input, make_verify_inputs
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = WORKLOADS[args.workload]
+    if args.batch:
+        w = w.scaled(B=args.batch, M=(w.tokens * args.batch) // w.B if w.M else 0)
+    x = make_verify_inputs(w)
+    di = make_draft_input(w)
+    B, D, V = x["B"], x["D"], x["V"]
+    ng = int((x["tau"] == 0).sum())
+    assert (x["tau"][:ng] == 0).all() and (x["tau"][ng:] > 0).all()
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    step_bytes = verify_bytes(x) + draft_input_bytes(w) + ng * D * V * (4 if x["dtype"] == "f32" else 2)
+    copies = max(1, math.ceil(3 * L2_BYTES / step_bytes))
+    T0, Q0 = to_dev(x["T"]), to_dev(x["Q"])
+    sets = []
+    for c in range(copies):
+        sets.append(dict(
+            T=T0 if c == 0 else T0.clone(), Q=Q0 if c == 0 else Q0.clone(),
+            d=to_dev(x["d"]), e=to_dev(di["e"][0]), h=to_dev(di["h"][0]),
+            W=to_dev(di["W"]) if c == 0 else sets[0]["W"].clone()))
+    tau, top_p = to_dev(x["tau"]), to_dev(x["top_p"])
+    top_k = to_dev(x["top_k"]) if (x["top_k"] > 0).any() else None
+    we, wh = to_dev(di["we"]), to_dev(di["wh"])
+    M, H = w.tokens, w.H
+    y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    ws_di = torch.empty(max(1, lib.mtp_draft_input_workspace_bytes(M, H)), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+    na = torch.empty(B, dtype=torch.int32, device=dev)
+    pt = torch.empty((B, D), dtype=torch.float32, device=dev)
+    pd = torch.empty((B, D), dtype=torch.float32, device=dev)
+    ws_v = torch.empty(lib.spec_verify_workspace_bytes(B, D, V), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    ev_v = []
+
+    def step(i, timed=False):
+        s = sets[i % copies]
+        lib.mtp_draft_input(s["e"], s["h"], we, wh, s["W"], y, di["eps"], ws_di)
+        if ng:
+            lib.mtp_greedy_draft(s["Q"][:ng].view(ng * D, V), s["d"][:ng].view(-1))
+        if timed:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+        lib.spec_verify_sample(s["T"], s["Q"], s["d"], tau, top_k, top_p, x["seed"], out, na,
+                               pt, pd, ws_v, status)
+        if timed:
+            b.record(stream)
+            ev_v.append((a, b))
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"status word {int(status.item())}"
+
+    # launches of this library's kernels in one step, from the CUDA profiler
+    launches_per_step = None
+    try:
+        if args.no_launch_count:
+            raise RuntimeError("launch count skipped")
+        from torch.profiler import ProfilerActivity, profile
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            step(0)
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if e.device_type.name == "CUDA"]
+        ours = [n for n in names if "mtpspec" in n]
+        launches_per_step = len(ours) if ours else None
+    except Exception:
+        launches_per_step = None
+
+    clocks = ClockSampler(dev.index)
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, timed=True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(dist)
+    ms = t_start.elapsed_time(t_end)
+    ms_max = max_over_ranks(ms, dist)
+    verify_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_v)
+    rows_per_step = B * (D + 1)
+    value = world * rows_per_step * args.steps / (ms_max / 1e3)
+
+    # end to end through the C ABI with host buffers: pinned inputs copied in, results out
+    host_in = {k: torch.from_numpy(np.ascontiguousarray(
+        v if v.dtype != np.uint16 else v.view(np.int16))).pin_memory()
+        for k, v in dict(T=x["T"], Q=x["Q"], d=x["d"], e=di["e"][0], h=di["h"][0],
+                         W=di["W"]).items()}
+    host_out = dict(out=torch.empty((B, D + 1), dtype=torch.int32).pin_memory(),
+                    na=torch.empty(B, dtype=torch.int32).pin_memory(),
+                    pt=torch.empty((B, D), dtype=torch.float32).pin_memory(),
+                    pd=torch.empty((B, D), dtype=torch.float32).pin_memory(),
+                    y=torch.empty((M, H), dtype=torch.bfloat16).pin_memory())
+    s0 = sets[0]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for k in ("T", "Q", "d", "e", "h", "W"):
+            dst = s0[k] if s0[k].dtype != torch.bfloat16 else s0[k].view(torch.int16)
+            dst.copy_(host_in[k], non_blocking=True)
+        step(0)
+        host_out["out"].copy_(out, non_blocking=True)
+        host_out["na"].copy_(na, non_blocking=True)
+        host_out["pt"].copy_(pt, non_blocking=True)
+        host_out["pd"].copy_(pd, non_blocking=True)
+        host_out["y"].copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist)
+    e2e_value = world * rows_per_step * args.e2e_steps / (e2e_ms / 1e3)
+
+    peak, peak_kind = measured_peaks()
+    vb = verify_bytes(x)
+    achieved = vb / (verify_ms / 1e3) / 1e9
+    traffic = profiled_traffic(args.workload)
+    roofline = {"bound": "hbm", "kernel": "k_verify_units + k_verify_finalize",
+                "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "algorithmic_bytes_per_launch": vb,
+                "launch_ms": round(verify_ms, 5), "traffic": traffic}
+
+    res = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": max(3, args.warmup),
+           "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": x["dtype"],
+           "data": "synthetic",
+           "config": {"workload": w.name, "B": B, "D": D, "V": V, "H": H, "draft_tokens": M,
+                      "greedy_rows": ng, "top_k": int(w.top_k), "top_p": float(w.top_p),
+                      "logits": x["dtype"], "step": "mtp_draft_input + mtp_greedy_draft + "
+                      "spec_verify_sample", "parallelism": f"replicas x{world}",
+                      "l2": ("inputs larger than L2" if copies == 1 else
+                             f"{copies} rotating input copies, {copies * step_bytes / 1e6:.0f} MB")},
+           "clocks": clk,
+           "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h},
+           "gpu_launches": (launches_per_step * args.steps) if launches_per_step else None,
+           "roofline": roofline}
+    return res, x, di, w
+
+
+def main():
+    args = parse_args()
+    rank, world, dist = dist_init(args.gpus)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args)
+    res, x, di, w = run_gpu(args, rank, world, dist)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            v, cores, sample, dt = oracle_sample(x, di, w, rows=64)
+            res["cpu_baseline"] = {"value": round(v, 2), "unit": UNIT, "cores": cores,
+                                   "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle on this arm's workload, metric and unit; each
+    step a bounded sample of the workload on the host cores."""
+    from verify_spec_greedy_gb300.inputs import WORKLOADS, make_draft_input, make_verify_inputs
+    w = WORKLOADS[args.workload]
+    x = make_verify_inputs(w)
+    di = make_draft_input(w)
+    rows = 16
+    for _ in range(min(args.warmup, 1)):
+        oracle_sample(x, di, w, rows)
+    vals, dts = [], []
+    steps = max(1, min(args.steps, 10))
+    for _ in range(steps):
+        v, cores, sample, dt = oracle_sample(x, di, w, rows)
+        vals.append(v)
+        dts.append(dt)
+    value = len(vals) * rows * (x["D"] + 1) / sum(dts)
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+           "n_gpus": 0, "steps": steps, "warmup": min(args.warmup, 1),
+           "ms_per_step": round(1e3 * sum(dts) / steps, 2), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": w.name, "B": x["B"], "D": x["D"], "V": x["V"], "H": w.H,
+                      "draft_tokens": w.tokens},
+           "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -10,26 +10,31 @@
 // copies its slice of the target row (and, for j < D, of the draft row) into shared memory
 // with bulk asynchronous copies, so every logit is read from HBM exactly once.  Everything
 // after that runs on chip:
-//   pass 1   per-slice max and online softmax sum (argmax for greedy rows) as chunks land
-//   E1       the per-CTA partials meet in every CTA through distributed shared memory
-//   pass 2   (top-k/top-p only) histogram of count and fixed-point softmax weight over
-//            bins of z = (x - max) * log2(e) / tau, R bins per unit of z; reduce-scattered
-//            and re-broadcast across the cluster (E2)
-//   gather   the elements of the bins that hold the top-k / top-p boundary are pushed to
-//            every CTA (E3); each CTA finds the exact thresholds by radix select on their
-//            order-preserving keys.  If the boundary is outside the binned range or its bins
-//            hold too many elements, an exact binary search over keys replaces this step.
+//   pass 1   maximum and online softmax sum (argmax for greedy rows) as the chunks land
+//   E1       per-CTA partials meet in every CTA through distributed shared memory
+//   pass 2   (top-k / top-p) counts over fine bins of z = (x - max) * log2(e) / tau,
+//            R bins per unit of z, only for elements that can hold the boundary; the counts
+//            are reduce-scattered and re-broadcast across the cluster (E2)
+//   plan     the bins that must hold the boundary, from exact counts (top-k) or from
+//            per-bin weight bounds count * 2^(-b/R) (top-p)
+//   gather   elements of those bins are pushed to every CTA with their weights, and the
+//            exact weight of everything above them is summed (E3); each CTA then finds
+//            the thresholds by exact rank / weight-above counts over the candidates.  If
+//            the boundary is outside the binned range or too many elements fall in its
+//            bins, an exact bisection over the 32-bit value keys replaces this step.
 //   accept   p(d), q(d) and U_acc <= p/q (ratio formed with both maxima factored out)
-//   draw     only for a rejected draft or the bonus position: per-warp sums of the draw
-//            weights in id order, CTA sums exchanged (E4), and the CTA holding the target
-//            walks its slice to the token (inverse CDF in ascending id order).
+//   draw     only for a rejected draft or the bonus position: draw weights in fixed point
+//            (2^31 per unit of probability), per-warp sums in id order, CTA sums exchanged
+//            (E4), and the CTA holding the target walks its slice to the token.
 // A per-row finalize kernel then takes the first rejected position.
 //
-// Every decision is computed identically in every CTA of a cluster from exchanged data, so
-// all CTAs run the same sequence of cluster barriers.  Data exchanges are pushes into the
-// peers' shared memory before a barrier; after the last barrier a CTA only reads its own
-// shared memory, so it may exit.  The only wait on an asynchronous event is the bulk-copy
-// barrier, bounded by an iteration limit that raises MTPSPEC_STATUS_TIMEOUT.
+// Weight sums are formed per thread in fp32 over a fixed set of elements, converted once
+// to 64-bit fixed point and reduced as integers, so every sum is deterministic and the same
+// in every CTA of a cluster.  Every decision is computed identically in every CTA from
+// exchanged data, so all CTAs run the same sequence of cluster barriers.  Exchanges are
+// pushes into the peers' shared memory before a barrier; after the last barrier a CTA only
+// reads its own shared memory.  The bulk-copy barrier waits are bounded and raise
+// MTPSPEC_STATUS_TIMEOUT when they give up.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -39,19 +44,27 @@ namespace vs {
 constexpr int NT = 512;          // threads per CTA
 constexpr int NW = NT / 32;      // warps per CTA
 constexpr int MAXC = 16;         // largest cluster
-constexpr int R = 16;            // histogram bins per unit of z (log2 of the softmax weight)
-constexpr int NB = 512;          // binned range: z in (-NB/R, 0] = weights in (2^-32, 1]
-constexpr int NBT = NB + 1;      // + one bin for everything below the range
-constexpr int INCOMING = NBT + MAXC;  // reduce-scatter slots per row (C * ceil(NBT / C))
-constexpr int CAP = 1024;        // boundary candidates per row
+constexpr int R = 64;            // histogram bins per unit of z (log2 of the softmax weight)
+constexpr int ZR = 24;           // binned range: z in (-ZR, 0], weights in (2^-24, 1]
+constexpr int NB = R * ZR;       // bins
+constexpr int INCOMING = NB + MAXC;  // reduce-scatter slots per row (C * ceil(NB / C))
+constexpr int CAP = 512;         // boundary candidates per row
 constexpr int NCH = 4;           // bulk-copy chunks per row
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
+constexpr float FX = 2147483648.0f;  // 2^31: fixed-point scale of weights (weights <= 1)
+constexpr double INV_FX = 1.0 / 2147483648.0;
+constexpr float BOUND_SLACK = 4e-5f;  // relative slack of the per-bin weight bounds
 
 struct UnitResult {
     int32_t flags;  // bit 0: draft accepted
     int32_t token;  // greedy pick, or the draw (residual / bonus) of this unit, or -1
     float pt;       // p_j(d_j)
     float pd;       // q_j(d_j)
+};
+
+struct Cand {
+    float v;       // logit
+    uint32_t idx;  // token id
 };
 
 struct __align__(16) Shared {
@@ -67,37 +80,33 @@ struct __align__(16) Shared {
     int32_t x_i[MAXC][2];
     float x_d[2];  // the draft token's logit in each row, pushed by the CTA that owns it
     // per-row state, identical in every CTA of the cluster
-    float m[2], zall[2], invZ[2], Z[2];
-    uint32_t theta[2];
-    int32_t deg[2];    // row of all -inf: a point mass on id 0
-    int32_t mode[2];   // 0 no filter, 1 candidates, 2 exact search
-    int32_t blo[2], bhi[2];
+    float c2;                 // log2(e) / tau
+    float m[2], Z[2], invZ[2], theta[2], zcut[2];
+    int32_t deg[2];           // a row of all -inf: a point mass on id 0
+    int32_t mode[2];          // 0 no filter, 1 candidates, 2 exact bisection
+    int32_t b1[2], b2[2];
     uint32_t ncand[2];
-    unsigned long long NA[2], MA[2];
-    // histogram (local during pass 2, the cluster-wide histogram after E2)
-    uint32_t hcnt[2][NBT];
-    unsigned long long hmass[2][NBT];
+    unsigned long long tgt[2];
+    // histogram of counts (local during pass 2, cluster-wide after E2)
+    uint32_t hcnt[2][NB];
     // reduce-scatter inbox, reused for the boundary candidates
     union {
+        uint32_t in[2][INCOMING];
         struct {
-            uint32_t cnt[2][INCOMING];
-            unsigned long long mass[2][INCOMING];
-        } in;
-        unsigned long long cand[2][CAP];
+            Cand c[2][CAP];
+            unsigned long long w[2][CAP];
+        } cd;
     } u;
-    uint32_t cand_n[2];  // slot allocator, used in CTA 0
-    // radix select scratch
-    uint32_t s_cnt[256];
-    unsigned long long s_mass[256];
-    unsigned long long s_bcast[4];
-    // exact search exchange (double-buffered by iteration parity)
+    uint32_t cand_n[2];                // slot allocator, used in CTA 0
+    unsigned long long ma_x[MAXC][2];  // per-CTA fixed-point weight above bin b1
+    // exact bisection exchange (double-buffered by iteration parity)
     unsigned long long sx[2][2][MAXC];
     // draws
     unsigned long long dr_R[2][MAXC];  // per draw attempt: each CTA's fixed-point weight
     unsigned long long w_sum[NW];
-    unsigned long long mtot[2];         // exact fixed-point weight of the whole row
     int32_t flags;  // bit 0: a bulk copy timed out
     int32_t pick[4];
+    float fpick[4];
 };
 
 __device__ __forceinline__ float ex2(float z) {
@@ -109,13 +118,17 @@ __device__ __forceinline__ float ex2(float z) {
 __device__ __forceinline__ float zval(float x, float m, float c2) {
     return __fmul_rn(__fsub_rn(x, m), c2);
 }
+// bin of z in (-ZR, 0]; NB below the range (or NaN)
 __device__ __forceinline__ int zbin(float z) {
-    if (!(z > -static_cast<float>(NB / R))) return NB;  // below the range (or NaN)
-    int b = static_cast<int>(__fmul_rn(-z, static_cast<float>(R)));
+    if (!(z > -static_cast<float>(ZR))) return NB;
+    const int b = static_cast<int>(__fmul_rn(-z, static_cast<float>(R)));
     return b < NB ? b : NB - 1;
 }
-__device__ __forceinline__ unsigned long long fixmass(float e, float scale) {
-    return __float2ull_rn(__fmul_rn(e, scale));
+// a weight (<= 1) in fixed point; the float-to-32-bit conversion is a fast instruction
+__device__ __forceinline__ uint32_t fix31(float w) { return __float2uint_rn(__fmul_rn(w, FX)); }
+// a per-thread sum in fixed point: a slow 64-bit conversion, used once per thread
+__device__ __forceinline__ unsigned long long fix_sum(float s) {
+    return __float2ull_rn(__fmul_rn(s, FX));
 }
 
 // ---------------------------------------------------------------- Philox4x32-10
@@ -161,10 +174,21 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
     return v;
 }
-__device__ __forceinline__ float warp_sum_f32(float v) {
+__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
+    return __reduce_add_sync(0xFFFFFFFFu, v);
+}
+
+// Sum of one u64 per thread over the block; every thread gets the result.
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v,
+                                                            unsigned long long *scratch) {
+    v = warp_sum_u64(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    __syncthreads();
+    unsigned long long t = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
+    for (int w = 0; w < NW; ++w) t += scratch[w];
+    return t;
 }
 
 __device__ __forceinline__ void mbar_init(unsigned long long *bar, uint32_t count) {
@@ -207,10 +231,9 @@ __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// ---------------------------------------------------------------- per-element visitors
-
 // Visit every element [0, n) of a shared-memory slice as (value, local index), with
-// 16-byte vector reads for the aligned body, threads strided over vectors.
+// 16-byte vector reads for the aligned body, threads strided over vectors.  Each thread
+// always visits the same elements in the same order.
 template <typename T, typename F>
 __device__ __forceinline__ void for_each_elem(const T *s, int n, F &&f) {
     constexpr int EPV = elems_per_16B<T>::value;
@@ -225,126 +248,85 @@ __device__ __forceinline__ void for_each_elem(const T *s, int n, F &&f) {
     for (int i = nv * EPV + threadIdx.x; i < n; i += NT) f(widen(s[i]), i);
 }
 
-// ---------------------------------------------------------------- radix select
-
-// Among candidates (key << 32 | id) with key >= floor_key, the largest key t such that the
-// count (use_mass = false) or the fixed-point weight (use_mass = true) of candidates with
-// key >= t reaches `need` (need >= 1 and reachable).  All threads call; returns in all.
-__device__ uint32_t radix_select(Shared &sh, const unsigned long long *cand, int n,
-                                 uint32_t floor_key, unsigned long long need, bool use_mass,
-                                 float m, float c2, float scale) {
-    uint32_t prefix = 0, pmask = 0;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += NT) {
-            sh.s_cnt[i] = 0;
-            sh.s_mass[i] = 0;
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < n; i += NT) {
-            const uint32_t key = static_cast<uint32_t>(cand[i] >> 32);
-            if (key < floor_key || (key & pmask) != prefix) continue;
-            const uint32_t dg = (key >> shift) & 255u;
-            if (use_mass) {
-                const float x = key_to_float(key);
-                atomicAdd(&sh.s_mass[dg], fixmass(ex2(zval(x, m, c2)), scale));
-            } else {
-                atomicAdd(&sh.s_cnt[dg], 1u);
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            const int lane = threadIdx.x;
-            // lane l owns digits 255-8l .. 248-8l (descending)
-            unsigned long long v[8], tot = 0;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int dg = 255 - (lane * 8 + t);
-                v[t] = use_mass ? sh.s_mass[dg] : static_cast<unsigned long long>(sh.s_cnt[dg]);
-                tot += v[t];
-            }
-            unsigned long long incl = tot;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const unsigned long long excl = incl - tot;
-            if (excl < need && incl >= need) {
-                unsigned long long acc = excl;
-                int pick = 0;
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    if (acc + v[t] >= need) {
-                        pick = 255 - (lane * 8 + t);
-                        break;
-                    }
-                    acc += v[t];
-                }
-                sh.s_bcast[0] = static_cast<unsigned long long>(pick);
-                sh.s_bcast[1] = need - acc;
-            }
-        }
-        __syncthreads();
-        prefix |= static_cast<uint32_t>(sh.s_bcast[0]) << shift;
-        pmask |= 255u << shift;
-        need = sh.s_bcast[1];
-        __syncthreads();
-    }
-    return prefix;
-}
-
-// Sum of fixed-point weights of candidates with key >= t.
-__device__ unsigned long long cand_mass_from(Shared &sh, const unsigned long long *cand, int n,
-                                             uint32_t t, float m, float c2, float scale) {
-    unsigned long long acc = 0;
-    for (int i = threadIdx.x; i < n; i += NT) {
-        const uint32_t key = static_cast<uint32_t>(cand[i] >> 32);
-        if (key >= t) acc += fixmass(ex2(zval(key_to_float(key), m, c2)), scale);
-    }
-    acc = warp_sum_u64(acc);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) sh.ru[0][threadIdx.x >> 5] = acc;
-    __syncthreads();
-    unsigned long long tot = 0;
-    for (int w = 0; w < NW; ++w) tot += sh.ru[0][w];
-    __syncthreads();
-    return tot;
-}
-
-// First bin b (0..NB-1) whose cumulative value (bins 0..b) reaches `need`; NB if none.
-// One warp; the histogram is the cluster-wide one.  Writes the result to *out.
-__device__ void first_bin_reaching(const uint32_t *cnt, const unsigned long long *mass,
-                                   bool use_mass, unsigned long long need, int32_t *out) {
+// First bin whose cumulative count reaches `need` (NB if none); one warp, lane 0 writes.
+__device__ void count_search(const uint32_t *cnt, uint32_t need, int32_t *out) {
     const int lane = threadIdx.x & 31;
-    constexpr int PER = (NB + 31) / 32;
-    unsigned long long tot = 0;
-    for (int t = 0; t < PER; ++t) {
-        const int b = lane * PER + t;
-        if (b < NB) tot += use_mass ? mass[b] : static_cast<unsigned long long>(cnt[b]);
-    }
-    unsigned long long incl = tot;
+    constexpr int PER = NB / 32;
+    uint32_t own = 0;
+    for (int t = 0; t < PER; ++t) own += cnt[lane * PER + t];
+    uint32_t incl = own;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
+        const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += a;
     }
-    const unsigned long long excl = incl - tot;
-    const unsigned ball = __ballot_sync(0xFFFFFFFFu, excl < need && incl >= need);
+    const unsigned ball = __ballot_sync(0xFFFFFFFFu, incl - own < need && incl >= need);
     if (ball == 0) {
         if (lane == 0) *out = NB;
-        return;
-    }
-    if (lane == __ffs(ball) - 1) {
-        unsigned long long acc = excl;
+    } else if (lane == __ffs(ball) - 1) {
+        uint32_t acc = incl - own;
         for (int t = 0; t < PER; ++t) {
-            const int b = lane * PER + t;
-            acc += use_mass ? mass[b] : static_cast<unsigned long long>(cnt[b]);
+            acc += cnt[lane * PER + t];
             if (acc >= need) {
-                *out = b;
+                *out = lane * PER + t;
                 break;
             }
         }
     }
+    __syncwarp();
+}
+
+// Bins that must hold the top-p boundary: bin b holds weights in [2^-(b+1)/R, 2^-b/R]
+// (relative to the row maximum), so the cumulative weight of bins 0..b lies between two
+// bounds.  *first = the first bin whose upper bound reaches `need`, *last = the first bin
+// whose lower bound reaches it (NB if none).  One warp.
+__device__ void weight_search(const uint32_t *cnt, float need, int32_t *first, int32_t *last) {
+    const int lane = threadIdx.x & 31;
+    constexpr int PER = NB / 32;
+    const float step = ex2(-1.0f / R);
+    const float up = 1.0f + BOUND_SLACK, dn = (1.0f - BOUND_SLACK) * step;
+    float hi = 0.0f, lo = 0.0f;
+    float w = ex2(-static_cast<float>(lane * PER) / R);
+    for (int t = 0; t < PER; ++t) {
+        const float c = static_cast<float>(cnt[lane * PER + t]);
+        hi += c * w * up;
+        lo += c * w * dn;
+        w *= step;
+    }
+    float ihi = hi, ilo = lo;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float a = __shfl_up_sync(0xFFFFFFFFu, ihi, o);
+        const float c = __shfl_up_sync(0xFFFFFFFFu, ilo, o);
+        if (lane >= o) {
+            ihi += a;
+            ilo += c;
+        }
+    }
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const float incl = pass == 0 ? ihi : ilo, own = pass == 0 ? hi : lo;
+        const float f = pass == 0 ? up : dn;
+        int32_t *out = pass == 0 ? first : last;
+        const unsigned ball = __ballot_sync(0xFFFFFFFFu, incl - own < need && incl >= need);
+        if (ball == 0) {
+            if (lane == 0) *out = NB;
+        } else if (lane == __ffs(ball) - 1) {
+            float acc = incl - own;
+            float ww = ex2(-static_cast<float>(lane * PER) / R);
+            int res = lane * PER + PER - 1;
+            for (int t = 0; t < PER; ++t) {
+                acc += static_cast<float>(cnt[lane * PER + t]) * ww * f;
+                ww *= step;
+                if (acc >= need) {
+                    res = lane * PER + t;
+                    break;
+                }
+            }
+            *out = res;
+        }
+    }
+    __syncwarp();
 }
 
 struct Params {
@@ -359,8 +341,6 @@ struct Params {
     int32_t D;
     int64_t V;
     int64_t slice;
-    float scale;      // 2^S, the fixed-point weight scale
-    float inv_scale;  // 2^-S
     UnitResult *res;
     int32_t *status;
 };
@@ -373,9 +353,10 @@ __global__ void __launch_bounds__(NT, 2) k_verify_units(const Params P) {
     Shared &sh = *reinterpret_cast<Shared *>(smem_raw);
     constexpr int EPV = elems_per_16B<T>::value;
     const size_t data_off = (sizeof(Shared) + 127) & ~static_cast<size_t>(127);
-    const size_t row_bytes = ((static_cast<size_t>(P.slice) * sizeof(T)) + 127) & ~static_cast<size_t>(127);
-    T *sdat[2] = {reinterpret_cast<T *>(smem_raw + data_off),
-                  reinterpret_cast<T *>(smem_raw + data_off + row_bytes)};
+    const size_t row_bytes =
+        ((static_cast<size_t>(P.slice) * sizeof(T)) + 127) & ~static_cast<size_t>(127);
+    T *const sd0 = reinterpret_cast<T *>(smem_raw + data_off);
+    T *const sd1 = reinterpret_cast<T *>(smem_raw + data_off + row_bytes);
 
     const uint32_t C = cluster_size();
     const uint32_t rank = cluster_rank();
@@ -395,113 +376,111 @@ __global__ void __launch_bounds__(NT, 2) k_verify_units(const Params P) {
     const int nrows = has_q ? 2 : 1;
     const bool k_on = !greedy && kk >= 1 && static_cast<int64_t>(kk) < V;
     const bool p_on = !greedy && pp < 1.0f;
-    const float c2 = greedy ? 0.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(tau));
 
     const int64_t lo64 = static_cast<int64_t>(rank) * P.slice;
     const int64_t rest = V - lo64;
     const int n = static_cast<int>(rest <= 0 ? 0 : (rest < P.slice ? rest : P.slice));
     const int32_t d = j < D ? P.d[b * D + j] : -1;
     const bool dvalid = d >= 0 && static_cast<int64_t>(d) < V;
-    const bool d_here = dvalid && static_cast<int64_t>(d) >= lo64 && static_cast<int64_t>(d) < lo64 + n;
+    const bool d_here =
+        dvalid && static_cast<int64_t>(d) >= lo64 && static_cast<int64_t>(d) < lo64 + n;
 
-    const T *grow[2];
-    grow[0] = static_cast<const T *>(P.T) + (b * (D + 1) + j) * V + lo64;
-    grow[1] = has_q ? static_cast<const T *>(P.Q) + (b * D + j) * V + lo64 : nullptr;
+    const T *g0 = static_cast<const T *>(P.T) + (b * (D + 1) + j) * V + lo64;
+    const T *g1 = has_q ? static_cast<const T *>(P.Q) + (b * D + j) * V + lo64 : nullptr;
 
-    // ---- set-up: barriers, counters, histogram
+    // ---- set-up: barriers, counters, histogram, the temperature scale
     if (tid == 0) {
         for (int r = 0; r < 2; ++r)
             for (int c = 0; c < NCH; ++c) mbar_init(&sh.bar[r][c], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         sh.cand_n[0] = sh.cand_n[1] = 0;
         sh.flags = 0;
+        sh.fpick[0] = sh.fpick[1] = -INFINITY;
+        sh.c2 = greedy ? 0.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(tau));
     }
-    for (int i = tid; i < 2 * NBT; i += NT) {
-        (&sh.hcnt[0][0])[i] = 0;
-        (&sh.hmass[0][0])[i] = 0;
-    }
+    for (int i = tid; i < 2 * NB; i += NT) (&sh.hcnt[0][0])[i] = 0;
     __syncthreads();
     cluster_arrive_release();  // peers may touch this CTA's shared memory after the wait below
     pdl_launch_dependents();
+    const float c2 = sh.c2;
 
     // ---- loads: bulk copies of the 16-byte-aligned body, plain loads for the rest
     const int nv = n / EPV;
-    bool bulk[2] = {false, false};
-    for (int r = 0; r < nrows; ++r)
-        bulk[r] = nv > 0 && (reinterpret_cast<uintptr_t>(grow[r]) & 15u) == 0;
+    const bool bulk0 = nv > 0 && (reinterpret_cast<uintptr_t>(g0) & 15u) == 0;
+    const bool bulk1 = has_q && nv > 0 && (reinterpret_cast<uintptr_t>(g1) & 15u) == 0;
+    const int per_ch = (nv + NCH - 1) / NCH;
     if (tid == 0) {
         for (int r = 0; r < nrows; ++r) {
-            if (!bulk[r]) continue;
-            const int per = (nv + NCH - 1) / NCH;
+            if (!(r == 0 ? bulk0 : bulk1)) continue;
+            T *dst = r == 0 ? sd0 : sd1;
+            const T *src = r == 0 ? g0 : g1;
             for (int c = 0; c < NCH; ++c) {
-                const int v0 = c * per, v1 = min(nv, v0 + per);
-                if (v1 <= v0) {
-                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sh.bar[r][c])) : "memory");
-                    continue;
-                }
+                const int v0 = c * per_ch, v1 = min(nv, v0 + per_ch);
+                if (v1 <= v0) continue;
                 const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
                 mbar_expect_tx(&sh.bar[r][c], bytes);
-                bulk_copy_g2s(sdat[r] + v0 * EPV, grow[r] + v0 * EPV, bytes, &sh.bar[r][c]);
+                bulk_copy_g2s(dst + v0 * EPV, src + v0 * EPV, bytes, &sh.bar[r][c]);
             }
         }
     }
-    for (int r = 0; r < nrows; ++r) {
-        const int from = bulk[r] ? nv * EPV : 0;
-        for (int i = from + tid; i < n; i += NT) sdat[r][i] = grow[r][i];
-    }
+    for (int i = (bulk0 ? nv * EPV : 0) + tid; i < n; i += NT) sd0[i] = g0[i];
+    if (has_q)
+        for (int i = (bulk1 ? nv * EPV : 0) + tid; i < n; i += NT) sd1[i] = g1[i];
     __syncthreads();
 
-    // ---- pass 1: max (+ online sum when nothing is filtered) or argmax (greedy)
-    const bool online = !greedy && !k_on && !p_on;
+    // ---- pass 1: argmax (greedy) or maximum + online softmax sum, as the chunks land
     float tm[2] = {-INFINITY, -INFINITY}, ts[2] = {0.0f, 0.0f};
     ArgMax am{-INFINITY, -1};
     bool timed_out = false;
-    for (int r = 0; r < nrows; ++r) {
-        const uint4 *vp = reinterpret_cast<const uint4 *>(sdat[r]);
-        const int per = (nv + NCH - 1) / NCH;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        if (r >= nrows) break;
+        const T *s = r == 0 ? sd0 : sd1;
+        const bool bulk = r == 0 ? bulk0 : bulk1;
+        const uint4 *vp = reinterpret_cast<const uint4 *>(s);
         for (int c = 0; c < NCH; ++c) {
-            const int v0 = c * per, v1 = min(nv, v0 + per);
-            if (bulk[r] && v1 > v0 && !mbar_wait_bounded(&sh.bar[r][c])) timed_out = true;
+            const int v0 = c * per_ch, v1 = min(nv, v0 + per_ch);
+            if (bulk && v1 > v0 && !mbar_wait_bounded(&sh.bar[r][c])) timed_out = true;
             for (int i = v0 + tid; i < v1; i += NT) {
                 float x[EPV];
                 unpack(vp[i], x);
                 if (greedy) {
 #pragma unroll
                     for (int e = 0; e < EPV; ++e)
-                        if (x[e] > am.v || am.i < 0) am = {x[e], static_cast<int32_t>(lo64 + i * EPV + e)};
+                        if (x[e] > am.v || am.i < 0)
+                            am = {x[e], static_cast<int32_t>(lo64 + i * EPV + e)};
                 } else {
                     float vm = x[0];
 #pragma unroll
                     for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, x[e]);
                     if (vm > tm[r]) {
-                        ts[r] = ts[r] * ex2(__fmul_rn(tm[r] - vm, c2));
+                        ts[r] *= ex2(__fmul_rn(tm[r] - vm, c2));
                         tm[r] = vm;
                     }
-                    if (online && tm[r] > -INFINITY) {
+                    if (tm[r] > -INFINITY) {
+                        float a = 0.0f;
 #pragma unroll
-                        for (int e = 0; e < EPV; ++e) ts[r] += ex2(__fmul_rn(x[e] - tm[r], c2));
+                        for (int e = 0; e < EPV; ++e) a += ex2(__fmul_rn(x[e] - tm[r], c2));
+                        ts[r] += a;
                     }
                 }
             }
         }
         for (int i = nv * EPV + tid; i < n; i += NT) {
-            const float x = widen(sdat[r][i]);
+            const float x = widen(s[i]);
             if (greedy) {
                 if (x > am.v || am.i < 0) am = {x, static_cast<int32_t>(lo64 + i)};
             } else if (x > -INFINITY) {
-                if (online)
-                    ms_merge(tm[r], ts[r], x, 1.0f, c2);
-                else
-                    tm[r] = fmaxf(tm[r], x);
+                ms_merge(tm[r], ts[r], x, 1.0f, c2);
             }
         }
     }
     if (timed_out) atomicOr(&sh.flags, 1);
-    if (!online)  // only the maxima matter; a sum of 1 marks a non-empty partial for the merge
-        for (int r = 0; r < nrows; ++r) ts[r] = tm[r] > -INFINITY ? 1.0f : 0.0f;
 
     // block reduction of the pass-1 partials
-    for (int r = 0; r < nrows; ++r) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        if (r >= nrows) break;
         if (greedy) {
             am = warp_argmax(am);
             if (lane == 0) {
@@ -537,13 +516,13 @@ __global__ void __launch_bounds__(NT, 2) k_verify_units(const Params P) {
         } else {
             for (int w = 0; w < NW; ++w) ms_merge(mv, sv, sh.rf[r][w], sh.rs[r][w], c2);
         }
+        const float xd =
+            d_here ? widen((r == 0 ? sd0 : sd1)[static_cast<int64_t>(d) - lo64]) : 0.0f;
         for (uint32_t c = 0; c < C; ++c) {
             st_peer_f32(peer_addr(smem_addr(&sh.x_m[rank][r]), c), mv);
             st_peer_f32(peer_addr(smem_addr(&sh.x_s[rank][r]), c), sv);
             st_peer_u32(peer_addr(smem_addr(&sh.x_i[rank][r]), c), static_cast<uint32_t>(iv));
-            if (d_here)
-                st_peer_f32(peer_addr(smem_addr(&sh.x_d[r]), c),
-                            widen(sdat[r][static_cast<int64_t>(d) - lo64]));
+            if (d_here) st_peer_f32(peer_addr(smem_addr(&sh.x_d[r]), c), xd);
         }
     }
     cluster_sync();  // B1
@@ -576,245 +555,236 @@ __global__ void __launch_bounds__(NT, 2) k_verify_units(const Params P) {
         for (uint32_t c = 0; c < C; ++c) ms_merge(mv, sv, sh.x_m[c][r], sh.x_s[c][r], c2);
         float mx = -INFINITY;
         for (uint32_t c = 0; c < C; ++c) mx = fmaxf(mx, sh.x_m[c][r]);
+        if (sv > 0.0f && mv != mx) sv *= ex2(__fmul_rn(mv - mx, c2));
         sh.m[r] = mx;
-        sh.zall[r] = sv;
         sh.deg[r] = !(mx > -INFINITY);
         sh.mode[r] = 0;
-        sh.theta[r] = 0u;
+        sh.theta[r] = -INFINITY;
         sh.Z[r] = sv;
+        // for top-p alone, a kept token weighs at least (1 - p) Z / V: the tokens below
+        // that level weigh less than (1 - p) Z together
+        float zc = -static_cast<float>(ZR);
+        if (!k_on && sv > 0.0f) {
+            const float lvl = __log2f((1.0f - pp) * sv / static_cast<float>(V));
+            zc = fmaxf(zc, lvl - 2.0f / R);
+        }
+        sh.zcut[r] = zc;
     }
     __syncthreads();
 
     const bool need_filter = k_on || p_on;
     if (need_filter) {
-        // ---- pass 2: histogram of count and fixed-point weight over z bins
-        for (int r = 0; r < nrows; ++r) {
-            if (sh.deg[r]) continue;
-            const float m = sh.m[r];
-            uint32_t below = 0;
-            unsigned long long below_w = 0;
-            for_each_elem(sdat[r], n, [&](float x, int) {
+        // ---- pass 2: counts over fine z bins for the elements that can hold the boundary
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            if (r >= nrows || sh.deg[r]) continue;
+            const float m = sh.m[r], zcut = sh.zcut[r];
+            uint32_t *h = sh.hcnt[r];
+            for_each_elem(r == 0 ? sd0 : sd1, n, [&](float x, int) {
                 const float z = zval(x, m, c2);
-                const int bn = zbin(z);
-                const unsigned long long w = fixmass(ex2(z), P.scale);
-                if (bn < NB) {
-                    atomicAdd(&sh.hcnt[r][bn], 1u);
-                    atomicAdd(&sh.hmass[r][bn], w);
-                } else {
-                    ++below;
-                    below_w += w;
-                }
+                if (z > zcut) atomicAdd(&h[zbin(z)], 1u);
             });
-            below = __reduce_add_sync(0xFFFFFFFFu, below);
-            below_w = warp_sum_u64(below_w);
-            if (lane == 0 && below_w) atomicAdd(&sh.hmass[r][NB], below_w);
-            if (lane == 0 && below) atomicAdd(&sh.hcnt[r][NB], below);
         }
         __syncthreads();
         // ---- E2a: reduce-scatter, push local bins to their owner CTA
-        const int RS = (NBT + C - 1) / C;
-        for (int idx = tid; idx < nrows * NBT; idx += NT) {
-            const int r = idx / NBT, bn = idx - r * NBT;
+        const int RS = (NB + C - 1) / C;
+        for (int idx = tid; idx < nrows * NB; idx += NT) {
+            const int r = idx / NB, bn = idx - r * NB;
             const int owner = bn / RS, k = bn - owner * RS;
-            const int slot = static_cast<int>(rank) * RS + k;
-            st_peer_u32(peer_addr(smem_addr(&sh.u.in.cnt[r][slot]), owner), sh.hcnt[r][bn]);
-            st_peer_u64(peer_addr(smem_addr(&sh.u.in.mass[r][slot]), owner), sh.hmass[r][bn]);
+            st_peer_u32(peer_addr(smem_addr(&sh.u.in[r][static_cast<int>(rank) * RS + k]), owner),
+                        sh.hcnt[r][bn]);
         }
         cluster_sync();  // B2a
         // ---- E2b: sum the owned bins and broadcast them
         for (int idx = tid; idx < nrows * RS; idx += NT) {
             const int r = idx / RS, k = idx - r * RS;
             const int bn = static_cast<int>(rank) * RS + k;
-            if (bn >= NBT) continue;
+            if (bn >= NB) continue;
             uint32_t cs = 0;
-            unsigned long long msum = 0;
-            for (uint32_t c = 0; c < C; ++c) {
-                cs += sh.u.in.cnt[r][c * RS + k];
-                msum += sh.u.in.mass[r][c * RS + k];
-            }
-            for (uint32_t c = 0; c < C; ++c) {
+            for (uint32_t c = 0; c < C; ++c) cs += sh.u.in[r][c * RS + k];
+            for (uint32_t c = 0; c < C; ++c)
                 st_peer_u32(peer_addr(smem_addr(&sh.hcnt[r][bn]), c), cs);
-                st_peer_u64(peer_addr(smem_addr(&sh.hmass[r][bn]), c), msum);
-            }
         }
         cluster_sync();  // B2b
 
-        // ---- plan per row: the bin range holding the boundary, or the exact search
+        // ---- plan per row: the bin range that holds the boundary, or the exact search
         if (warp < nrows) {
             const int r = warp;
-            if (sh.deg[r]) {
-                if (lane == 0) sh.mode[r] = 0;
-            } else {
-                int32_t bk = -1, blo = 0, bhi = 0;
+            if (!sh.deg[r]) {
+                int32_t b1 = 0, b2 = 0;
                 bool slow = false;
                 if (k_on) {
-                    first_bin_reaching(sh.hcnt[r], sh.hmass[r], false,
-                                       static_cast<unsigned long long>(kk), &sh.pick[r]);
+                    count_search(sh.hcnt[r], static_cast<uint32_t>(kk), &sh.pick[r]);
+                    const int32_t bk = sh.pick[r];
                     __syncwarp();
-                    bk = sh.pick[r];
+                    slow = bk >= NB;
+                    b1 = 0;  // every bin up to the k-th value; top-p then works inside them
+                    b2 = bk;
+                } else {
+                    weight_search(sh.hcnt[r], pp * sh.Z[r], &sh.pick[r], &sh.pick[2 + r]);
+                    b1 = sh.pick[r];
+                    b2 = sh.pick[2 + r];
                     __syncwarp();
-                    if (bk >= NB) slow = true;
-                    bhi = bk;
-                    blo = bk;
-                    if (!slow && p_on) {
-                        unsigned long long above = 0;  // weight of the bins before bk
-                        for (int t = lane; t < bk; t += 32) above += sh.hmass[r][t];
-                        above = warp_sum_u64(above);
-                        const double tt = static_cast<double>(pp) * static_cast<double>(above);
-                        const unsigned long long need = static_cast<unsigned long long>(ceil(tt));
-                        if (need == 0) {
-                            blo = 0;
-                        } else {
-                            first_bin_reaching(sh.hcnt[r], sh.hmass[r], true, need, &sh.pick[r]);
-                            __syncwarp();
-                            blo = min(sh.pick[r], bk);
-                            __syncwarp();
-                        }
-                    }
-                } else {  // top-p alone
-                    unsigned long long tot = 0;
-                    for (int t = lane; t < NBT; t += 32) tot += sh.hmass[r][t];
-                    tot = warp_sum_u64(tot);
-                    if (lane == 0) sh.mtot[r] = tot;
-                    const double tt = static_cast<double>(pp) * static_cast<double>(tot);
-                    const unsigned long long need = max(1ull, static_cast<unsigned long long>(ceil(tt)));
-                    first_bin_reaching(sh.hcnt[r], sh.hmass[r], true, need, &sh.pick[r]);
-                    __syncwarp();
-                    blo = bhi = sh.pick[r];
-                    __syncwarp();
-                    if (blo >= NB) slow = true;
+                    if (b1 >= NB) slow = true;
+                    if (b2 >= NB) b2 = NB - 1;
                 }
-                unsigned long long na = 0, ma = 0, inr = 0;
-                if (!slow) {
-                    for (int t = lane; t < NB; t += 32) {
-                        if (t < blo) {
-                            na += sh.hcnt[r][t];
-                            ma += sh.hmass[r][t];
-                        } else if (t <= bhi) {
-                            inr += sh.hcnt[r][t];
-                        }
-                    }
-                    na = warp_sum_u64(na);
-                    ma = warp_sum_u64(ma);
-                    inr = warp_sum_u64(inr);
-                    if (inr > static_cast<unsigned long long>(CAP)) slow = true;
-                }
+                uint32_t inr = 0;
+                if (!slow)
+                    for (int t = lane; t < NB; t += 32)
+                        if (t >= b1 && t <= b2) inr += sh.hcnt[r][t];
+                inr = warp_sum_u32(inr);
+                if (inr > static_cast<uint32_t>(CAP)) slow = true;
                 if (lane == 0) {
                     sh.mode[r] = slow ? 2 : 1;
-                    sh.blo[r] = blo;
-                    sh.bhi[r] = bhi;
-                    sh.NA[r] = na;
-                    sh.MA[r] = ma;
-                    sh.ncand[r] = static_cast<uint32_t>(inr);
+                    sh.b1[r] = b1;
+                    sh.b2[r] = b2;
+                    sh.ncand[r] = inr;
                 }
             }
         }
         __syncthreads();
 
-        // ---- gather the boundary candidates into every CTA (E3)
+        // ---- gather the boundary candidates into every CTA, with the exact weight of
+        // everything above them (E3)
         const bool any_fast = sh.mode[0] == 1 || (nrows > 1 && sh.mode[1] == 1);
         if (any_fast) {
-            for (int r = 0; r < nrows; ++r) {
-                if (sh.mode[r] != 1) continue;
-                const float m = sh.m[r];
-                const int blo = sh.blo[r], bhi = sh.bhi[r];
-                const uint32_t cnt_addr0 = peer_addr(smem_addr(&sh.cand_n[r]), 0);
-                // warp-contiguous traversal so that every lane of a warp iterates together
-                const int per_w = (n + NW - 1) / NW;
-                const int w0 = warp * per_w, w1 = min(n, w0 + per_w);
-                for (int base = w0; base < w1; base += 32) {
-                    const int i = base + lane;
-                    bool hit = false;
-                    uint32_t key = 0;
-                    if (i < w1) {
-                        const float x = widen(sdat[r][i]);
-                        const int bn = zbin(zval(x, m, c2));
-                        hit = bn >= blo && bn <= bhi;
-                        key = order_key(x);
-                    }
-                    const unsigned ball = __ballot_sync(0xFFFFFFFFu, hit);
-                    if (ball == 0) continue;
-                    uint32_t slot0 = 0;
-                    if (lane == __ffs(ball) - 1) slot0 = atom_peer_add_u32(cnt_addr0, __popc(ball));
-                    slot0 = __shfl_sync(0xFFFFFFFFu, slot0, __ffs(ball) - 1);
-                    if (hit) {
-                        const uint32_t slot = slot0 + __popc(ball & ((1u << lane) - 1u));
-                        const unsigned long long v = (static_cast<unsigned long long>(key) << 32) |
-                                                     static_cast<uint32_t>(lo64 + i);
-                        if (slot < static_cast<uint32_t>(CAP))
-                            for (uint32_t c = 0; c < C; ++c)
-                                st_peer_u64(peer_addr(smem_addr(&sh.u.cand[r][slot]), c), v);
-                    }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                if (r >= nrows) break;
+                float above = 0.0f;
+                if (sh.mode[r] == 1) {
+                    const float m = sh.m[r];
+                    const int b1 = sh.b1[r], b2 = sh.b2[r];
+                    const uint32_t alloc = peer_addr(smem_addr(&sh.cand_n[r]), 0);
+                    for_each_elem(r == 0 ? sd0 : sd1, n, [&](float x, int i) {
+                        const float z = zval(x, m, c2);
+                        const int bn = zbin(z);
+                        if (bn < b1) {
+                            above += ex2(z);
+                        } else if (bn <= b2) {
+                            const uint32_t slot = atom_peer_add_u32(alloc, 1u);
+                            if (slot < static_cast<uint32_t>(CAP)) {
+                                const uint32_t w = fix31(ex2(z));
+                                const uint32_t gi = static_cast<uint32_t>(lo64 + i);
+                                for (uint32_t c = 0; c < C; ++c) {
+                                    st_peer_f32(peer_addr(smem_addr(&sh.u.cd.c[r][slot].v), c), x);
+                                    st_peer_u32(peer_addr(smem_addr(&sh.u.cd.c[r][slot].idx), c), gi);
+                                    st_peer_u64(peer_addr(smem_addr(&sh.u.cd.w[r][slot]), c), w);
+                                }
+                            }
+                        }
+                    });
                 }
+                const unsigned long long ma = block_sum_u64(fix_sum(above), sh.ru[r]);
+                if (tid == 0)
+                    for (uint32_t c = 0; c < C; ++c)
+                        st_peer_u64(peer_addr(smem_addr(&sh.ma_x[rank][r]), c), ma);
             }
             cluster_sync();  // B3
-            // ---- exact thresholds from the candidates
-            for (int r = 0; r < nrows; ++r) {
-                if (sh.mode[r] != 1) continue;
-                const float m = sh.m[r];
+            // ---- exact thresholds: rank and weight above each candidate
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                if (r >= nrows || sh.mode[r] != 1) continue;
                 const int nc = static_cast<int>(sh.ncand[r]);
-                const unsigned long long *cand = sh.u.cand[r];
-                uint32_t thk = 0;
-                unsigned long long zk = 0;
+                const Cand *cd = sh.u.cd.c[r];
+                const unsigned long long *cw = sh.u.cd.w[r];
+                unsigned long long MA = 0;
+                for (uint32_t c = 0; c < C; ++c) MA += sh.ma_x[c][r];
+                // top-k: the k-th largest value (every bin above the candidates is empty)
+                float thk = -INFINITY;
                 if (k_on) {
-                    const unsigned long long need = static_cast<unsigned long long>(kk) - sh.NA[r];
-                    thk = radix_select(sh, cand, nc, 0u, need, false, m, c2, P.scale);
-                    zk = sh.MA[r] + cand_mass_from(sh, cand, nc, thk, m, c2, P.scale);
+                    for (int i = tid; i < nc; i += NT) {
+                        const float v = cd[i].v;
+                        uint32_t gt = 0, ge = 0;
+                        for (int t = 0; t < nc; ++t) {
+                            gt += cd[t].v > v;
+                            ge += cd[t].v >= v;
+                        }
+                        if (gt < static_cast<uint32_t>(kk) && ge >= static_cast<uint32_t>(kk))
+                            sh.fpick[r] = v;  // every thread that finds it writes the same value
+                    }
+                    __syncthreads();
+                    thk = sh.fpick[r];
                 }
-                uint32_t th = thk;
+                float th = thk;
                 if (p_on) {
-                    double tt;
-                    if (k_on)
-                        tt = static_cast<double>(pp) * static_cast<double>(zk);
-                    else
-                        tt = static_cast<double>(pp) * static_cast<double>(sh.mtot[r]);
-                    unsigned long long need = static_cast<unsigned long long>(ceil(tt));
-                    need = need > sh.MA[r] ? need - sh.MA[r] : 1ull;
-                    th = radix_select(sh, cand, nc, thk, need, true, m, c2, P.scale);
+                    unsigned long long zk = 0;
+                    if (k_on) {
+                        for (int i = tid; i < nc; i += NT)
+                            if (cd[i].v >= thk) zk += cw[i];
+                        zk = MA + block_sum_u64(zk, sh.ru[r]);
+                    }
+                    if (tid == 0) {
+                        const double t = k_on ? static_cast<double>(pp) * static_cast<double>(zk)
+                                              : static_cast<double>(pp) * static_cast<double>(sh.Z[r]) *
+                                                    static_cast<double>(FX);
+                        sh.tgt[r] = static_cast<unsigned long long>(ceil(t));
+                    }
+                    __syncthreads();
+                    const unsigned long long tgt = sh.tgt[r];
+                    // kept iff the weight strictly above is below the target: the threshold
+                    // is the smallest kept value
+                    float lowest = INFINITY;
+                    for (int i = tid; i < nc; i += NT) {
+                        const float v = cd[i].v;
+                        if (v < thk) continue;
+                        unsigned long long ab = MA;
+                        for (int t = 0; t < nc; ++t)
+                            if (cd[t].v > v && cd[t].v >= thk) ab += cw[t];
+                        if (ab < tgt) lowest = fminf(lowest, v);
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        lowest = fminf(lowest, __shfl_xor_sync(0xFFFFFFFFu, lowest, o));
+                    if (lane == 0) sh.rf[r][warp] = lowest;
+                    __syncthreads();
+                    float l = INFINITY;
+                    for (int w = 0; w < NW; ++w) l = fminf(l, sh.rf[r][w]);
+                    th = l;
                 }
-                const unsigned long long zfx = sh.MA[r] + cand_mass_from(sh, cand, nc, th, m, c2, P.scale);
+                unsigned long long zf = 0;
+                for (int i = tid; i < nc; i += NT)
+                    if (cd[i].v >= th) zf += cw[i];
+                zf = MA + block_sum_u64(zf, sh.ru[r]);
                 if (tid == 0) {
                     sh.theta[r] = th;
-                    sh.Z[r] = static_cast<float>(static_cast<double>(zfx) * static_cast<double>(P.inv_scale));
+                    sh.Z[r] = static_cast<float>(static_cast<double>(zf) * INV_FX);
                 }
                 __syncthreads();
             }
         }
 
-        // ---- exact binary search over keys (boundary outside the binned range, or too
+        // ---- exact bisection over value keys (boundary outside the binned range, or too
         // many elements in its bins); both rows advance in lockstep, one barrier a step
         const bool any_slow = sh.mode[0] == 2 || (nrows > 1 && sh.mode[1] == 2);
         if (any_slow) {
             int parity = 0;
-            // F(t) for each row: count (what = 0) or weight (what = 1) of elements with
-            // key >= t and key >= floor; pushed to every CTA; returns the cluster sums
-            auto eval = [&](const uint32_t t[2], const uint32_t fl[2], const int what[2],
+            // F(t) per row: count (wt = 0) or fixed-point weight (wt = 1) of the elements
+            // with key >= max(t, floor); returns the cluster-wide sums
+            auto eval = [&](const uint32_t t[2], const uint32_t fl[2], int wt,
                             unsigned long long out[2]) {
                 unsigned long long acc[2] = {0, 0};
-                for (int r = 0; r < nrows; ++r) {
-                    if (sh.mode[r] != 2) continue;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if (r >= nrows || sh.mode[r] != 2) continue;
                     const float m = sh.m[r];
                     const uint32_t lim = max(t[r], fl[r]);
-                    const int wt = what[r];
-                    unsigned long long a = 0;
-                    for_each_elem(sdat[r], n, [&](float x, int) {
-                        if (order_key(x) >= lim)
-                            a += wt ? fixmass(ex2(zval(x, m, c2)), P.scale) : 1ull;
+                    float a = 0.0f;
+                    uint32_t cnum = 0;
+                    for_each_elem(r == 0 ? sd0 : sd1, n, [&](float x, int) {
+                        if (order_key(x) >= lim) {
+                            if (wt) a += ex2(zval(x, m, c2));
+                            else ++cnum;
+                        }
                     });
-                    acc[r] = warp_sum_u64(a);
+                    acc[r] = wt ? fix_sum(a) : static_cast<unsigned long long>(cnum);
                 }
-                __syncthreads();
-                if (lane == 0) {
-                    sh.ru[0][warp] = acc[0];
-                    sh.ru[1][warp] = acc[1];
-                }
-                __syncthreads();
-                if (tid < 2) {
-                    unsigned long long s = 0;
-                    for (int w = 0; w < NW; ++w) s += sh.ru[tid][w];
+                const unsigned long long s0 = block_sum_u64(acc[0], sh.ru[0]);
+                const unsigned long long s1 = block_sum_u64(acc[1], sh.ru[1]);
+                if (tid < 2)
                     for (uint32_t c = 0; c < C; ++c)
-                        st_peer_u64(peer_addr(smem_addr(&sh.sx[parity][tid][rank]), c), s);
-                }
+                        st_peer_u64(peer_addr(smem_addr(&sh.sx[parity][tid][rank]), c),
+                                    tid == 0 ? s0 : s1);
                 cluster_sync();
                 for (int r = 0; r < 2; ++r) {
                     unsigned long long s = 0;
@@ -823,16 +793,16 @@ __global__ void __launch_bounds__(NT, 2) k_verify_units(const Params P) {
                 }
                 parity ^= 1;
             };
-            // largest t with F(t) >= need, by bisection over the 32-bit key space
-            auto search = [&](const uint32_t fl[2], const int what[2],
-                              const unsigned long long need[2], uint32_t res_t[2]) {
+            // largest key t with F(t) >= need, by bisection over the 32-bit key space
+            auto search = [&](const uint32_t fl[2], int wt, const unsigned long long need[2],
+                              uint32_t res_t[2]) {
                 uint32_t lo[2] = {0u, 0u}, hi[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};
                 for (int it = 0; it < 32; ++it) {
                     uint32_t mid[2];
                     for (int r = 0; r < 2; ++r)
                         mid[r] = lo[r] + static_cast<uint32_t>((static_cast<uint64_t>(hi[r]) - lo[r] + 1) / 2);
                     unsigned long long f[2];
-                    eval(mid, fl, what, f);
+                    eval(mid, fl, wt, f);
                     for (int r = 0; r < 2; ++r) {
                         if (lo[r] >= hi[r]) continue;
                         if (f[r] >= need[r]) lo[r] = mid[r];
@@ -843,30 +813,32 @@ __global__ void __launch_bounds__(NT, 2) k_verify_units(const Params P) {
                 res_t[1] = lo[1];
             };
             uint32_t zero[2] = {0u, 0u}, thk[2] = {0u, 0u}, th[2] = {0u, 0u};
-            int wcnt[2] = {0, 0}, wmass[2] = {1, 1};
-            unsigned long long zk[2] = {0, 0};
             if (k_on) {
-                unsigned long long need[2] = {static_cast<unsigned long long>(kk),
-                                              static_cast<unsigned long long>(kk)};
-                search(zero, wcnt, need, thk);
-                eval(thk, zero, wmass, zk);
+                const unsigned long long need[2] = {static_cast<unsigned long long>(kk),
+                                                    static_cast<unsigned long long>(kk)};
+                search(zero, 0, need, thk);
             }
             th[0] = thk[0];
             th[1] = thk[1];
             if (p_on) {
+                unsigned long long zk[2] = {0, 0};
+                if (k_on) eval(thk, zero, 1, zk);
                 unsigned long long need[2];
                 for (int r = 0; r < 2; ++r) {
-                    double tt = k_on ? static_cast<double>(pp) * static_cast<double>(zk[r])
-                                     : static_cast<double>(pp) * static_cast<double>(sh.mtot[r < nrows ? r : 0]);
-                    need[r] = max(1ull, static_cast<unsigned long long>(ceil(tt)));
+                    const double t = k_on ? static_cast<double>(pp) * static_cast<double>(zk[r])
+                                          : static_cast<double>(pp) *
+                                                static_cast<double>(sh.Z[r < nrows ? r : 0]) *
+                                                static_cast<double>(FX);
+                    need[r] = static_cast<unsigned long long>(ceil(t));
+                    if (need[r] == 0) need[r] = 1;
                 }
-                search(thk, wmass, need, th);
+                search(thk, 1, need, th);
             }
             unsigned long long zf[2];
-            eval(th, zero, wmass, zf);
+            eval(th, zero, 1, zf);
             if (tid < nrows && sh.mode[tid] == 2) {
-                sh.theta[tid] = th[tid];
-                sh.Z[tid] = static_cast<float>(static_cast<double>(zf[tid]) * static_cast<double>(P.inv_scale));
+                sh.theta[tid] = key_to_float(th[tid]);
+                sh.Z[tid] = static_cast<float>(static_cast<double>(zf[tid]) * INV_FX);
             }
             __syncthreads();
         }
@@ -879,55 +851,82 @@ __global__ void __launch_bounds__(NT, 2) k_verify_units(const Params P) {
     philox(uw, static_cast<uint32_t>(P.seed), static_cast<uint32_t>(P.seed >> 32));
     const float u_acc = word_uniform(uw[0]), u_smp = word_uniform(uw[1]);
 
-    auto member = [&](int r, float x, int64_t idx) -> bool {
-        return sh.deg[r] ? idx == 0 : order_key(x) >= sh.theta[r];
+    // membership and probability of a token in the target (0) and draft (1) rows
+    const float m0 = sh.m[0], m1 = sh.m[1], th0 = sh.theta[0], th1 = sh.theta[1];
+    const float iz0 = sh.invZ[0], iz1 = sh.invZ[1];
+    const bool deg0 = sh.deg[0], deg1 = sh.deg[1];
+    auto prob0 = [&](float x, int64_t idx) -> float {
+        if (deg0) return idx == 0 ? 1.0f : 0.0f;
+        return x >= th0 ? ex2(zval(x, m0, c2)) * iz0 : 0.0f;
     };
-    auto prob = [&](int r, float x, int64_t idx) -> float {
-        if (!member(r, x, idx)) return 0.0f;
-        return sh.deg[r] ? 1.0f : ex2(zval(x, sh.m[r], c2)) * sh.invZ[r];
+    auto prob1 = [&](float x, int64_t idx) -> float {
+        if (deg1) return idx == 0 ? 1.0f : 0.0f;
+        return x >= th1 ? ex2(zval(x, m1, c2)) * iz1 : 0.0f;
     };
 
     bool accept = false;
     float pt = 0.0f, pd = 0.0f;
     if (j < D && dvalid) {
         const float xt = sh.x_d[0], xq = sh.x_d[1];
-        const bool in_p = member(0, xt, d), in_q = member(1, xq, d);
-        pt = prob(0, xt, d);
-        pd = prob(1, xq, d);
+        const bool in_p = deg0 ? d == 0 : xt >= th0;
+        const bool in_q = deg1 ? d == 0 : xq >= th1;
+        pt = prob0(xt, d);
+        pd = prob1(xq, d);
         if (!in_p) {
             accept = false;
         } else if (!in_q) {
             accept = true;
         } else {
             float ratio;
-            if (sh.deg[0] || sh.deg[1])
+            if (deg0 || deg1)
                 ratio = pt / pd;
             else
-                ratio = ex2(__fmul_rn((xt - sh.m[0]) - (xq - sh.m[1]), c2)) * (sh.Z[1] / sh.Z[0]);
+                ratio = ex2(__fmul_rn((xt - m0) - (xq - m1), c2)) * (sh.Z[1] / sh.Z[0]);
             accept = u_acc <= ratio;
         }
     }
 
-    // ---- draw (a rejected draft's residual, or the bonus).  Weights are rounded to fixed
-    // point (2^40 per unit of probability) and summed as integers, so the cumulative sums
-    // at every level (lane, warp, CTA, cluster) are exact and agree with one another.
+    // ---- draw (a rejected draft's residual, or the bonus).  Weights in fixed point, summed
+    // as integers: the cumulative sums at every level (lane, warp, CTA, cluster) are exact
+    // and agree with one another.  Each warp owns a contiguous run of vectors; within it a
+    // lane takes consecutive vectors, so (step, lane, element) is ascending id order.
     const bool draw = (j == D) || !accept;
     if (draw) {
         int wmode = (j == D) ? 1 : 0;  // 0: max(0, p - q), 1: p
-        const int per_w = (((n + NW - 1) / NW) + 31) & ~31;
-        const int w0 = min(n, warp * per_w), w1 = min(n, w0 + per_w);
-        auto weight = [&](int i) -> unsigned long long {
-            const int64_t gi = lo64 + i;
-            const float p = prob(0, widen(sdat[0][i]), gi);
-            float w = p;
-            if (wmode == 0) w = fmaxf(p - prob(1, widen(sdat[1][i]), gi), 0.0f);
-            return __float2ull_rn(__fmul_rn(w, 1099511627776.0f));
+        const int nvw = (((n + EPV - 1) / EPV) + NW - 1) / NW;  // vectors per warp
+        const int wv0 = warp * nvw, wv1 = wv0 + nvw;
+        auto weights = [&](int vi, uint32_t (&w)[EPV]) {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) w[e] = 0u;
+            const int i0 = vi * EPV;
+            if (vi >= wv1 || i0 >= n) return;
+            float x[EPV], y[EPV];
+            if (i0 + EPV <= n) {
+                unpack(reinterpret_cast<const uint4 *>(sd0)[vi], x);
+                if (wmode == 0) unpack(reinterpret_cast<const uint4 *>(sd1)[vi], y);
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    x[e] = i0 + e < n ? widen(sd0[i0 + e]) : -INFINITY;
+                    y[e] = (wmode == 0 && i0 + e < n) ? widen(sd1[i0 + e]) : -INFINITY;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+                if (i0 + e >= n) break;
+                const int64_t gi = lo64 + i0 + e;
+                float p = prob0(x[e], gi);
+                if (p > 0.0f && wmode == 0) p = fmaxf(p - prob1(y[e], gi), 0.0f);
+                w[e] = fix31(p);
+            }
         };
         for (int attempt = 0; attempt < 2; ++attempt) {
             unsigned long long acc = 0;
-            for (int base = w0; base < w1; base += 32) {
-                const int i = base + lane;
-                if (i < w1) acc += weight(i);
+            for (int v = wv0 + lane; v < wv1; v += 32) {
+                uint32_t w[EPV];
+                weights(v, w);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) acc += w[e];
             }
             acc = warp_sum_u64(acc);
             if (lane == 0) sh.w_sum[warp] = acc;
@@ -943,13 +942,14 @@ __global__ void __launch_bounds__(NT, 2) k_verify_units(const Params P) {
             unsigned long long Rt = 0;
             for (uint32_t c = 0; c < C; ++c) Rt += dR[c];
             if (Rt > 0 || wmode == 1) {
-                // smallest id whose cumulative weight exceeds u_smp * R: the CTA, then the
-                // warp, then the element
-                const double t = static_cast<double>(u_smp) * static_cast<double>(Rt);
+                // smallest id whose cumulative weight exceeds u_smp * R; a cumulative
+                // integer sum S exceeds u_smp * R exactly when S > floor(u_smp * R)
+                const unsigned long long tt = static_cast<unsigned long long>(
+                    floor(static_cast<double>(u_smp) * static_cast<double>(Rt)));
                 uint32_t cs = C - 1;
                 unsigned long long before = 0;
                 for (uint32_t c = 0; c < C; ++c) {
-                    if (static_cast<double>(before + dR[c]) > t) {
+                    if (before + dR[c] > tt) {
                         cs = c;
                         break;
                     }
@@ -963,7 +963,7 @@ __global__ void __launch_bounds__(NT, 2) k_verify_units(const Params P) {
                     int ws = NW - 1;
                     unsigned long long wb = before;
                     for (int w = 0; w < NW; ++w) {
-                        if (static_cast<double>(wb + sh.w_sum[w]) > t) {
+                        if (wb + sh.w_sum[w] > tt) {
                             ws = w;
                             break;
                         }
@@ -974,23 +974,43 @@ __global__ void __launch_bounds__(NT, 2) k_verify_units(const Params P) {
                         for (int w = 0; w + 1 < NW; ++w) wb += sh.w_sum[w];
                     }
                     if (warp == ws) {
-                        const int v0 = min(n, ws * per_w), v1 = min(n, v0 + per_w);
                         unsigned long long a = wb;
                         int32_t tok = -1, lastpos = -1;
-                        for (int base = v0; base < v1 && tok < 0; base += 32) {
-                            const int i = base + lane;
-                            const unsigned long long wv = i < v1 ? weight(i) : 0ull;
-                            unsigned long long incl = wv;
+                        for (int v0 = wv0; v0 < wv1 && tok < 0; v0 += 32) {
+                            uint32_t w[EPV];
+                            weights(v0 + lane, w);
+                            unsigned long long own = 0;
+#pragma unroll
+                            for (int e = 0; e < EPV; ++e) own += w[e];
+                            unsigned long long incl = own;
 #pragma unroll
                             for (int o = 1; o < 32; o <<= 1) {
                                 const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
                                 if (lane >= o) incl += y;
                             }
-                            const unsigned hitm = __ballot_sync(
-                                0xFFFFFFFFu, wv > 0 && static_cast<double>(a + incl) > t);
-                            const unsigned posm = __ballot_sync(0xFFFFFFFFu, wv > 0);
-                            if (posm) lastpos = base + 31 - __clz(posm);
-                            if (hitm) tok = base + __ffs(hitm) - 1;
+                            const unsigned hitm = __ballot_sync(0xFFFFFFFFu, own > 0 && a + incl > tt);
+                            const unsigned posm = __ballot_sync(0xFFFFFFFFu, own > 0);
+                            // per lane: its first element past the target, its last positive one
+                            int first_e = EPV - 1, last_e = 0;
+                            {
+                                unsigned long long cum = a + incl - own;
+                                int f = -1;
+#pragma unroll
+                                for (int e = 0; e < EPV; ++e) {
+                                    cum += w[e];
+                                    if (w[e] > 0) last_e = e;
+                                    if (f < 0 && w[e] > 0 && cum > tt) f = e;
+                                }
+                                if (f >= 0) first_e = f;
+                            }
+                            if (posm) {
+                                const int ll = 31 - __clz(posm);
+                                lastpos = (v0 + ll) * EPV + __shfl_sync(0xFFFFFFFFu, last_e, ll);
+                            }
+                            if (hitm) {
+                                const int hl = __ffs(hitm) - 1;
+                                tok = (v0 + hl) * EPV + __shfl_sync(0xFFFFFFFFu, first_e, hl);
+                            }
                             a += __shfl_sync(0xFFFFFFFFu, incl, 31);
                         }
                         if (tok < 0) tok = lastpos < 0 ? 0 : lastpos;
@@ -1070,11 +1090,6 @@ static size_t verify_smem_bytes_es(int64_t slice, size_t es) {
     return head + 2 * row;
 }
 
-template <typename T>
-static size_t verify_smem_bytes(int64_t slice) {
-    return verify_smem_bytes_es(slice, sizeof(T));
-}
-
 bool verify_fits(int64_t V, size_t elem_bytes) {
     const int C = verify_cluster_size(V);
     return verify_smem_bytes_es(verify_slice(V, C), elem_bytes) <= 227u * 1024u;
@@ -1082,7 +1097,7 @@ bool verify_fits(int64_t V, size_t elem_bytes) {
 
 template <typename T>
 static cudaError_t launch_verify_sample(const vs::Params &p, int C, cudaStream_t stream) {
-    const size_t smem = verify_smem_bytes<T>(p.slice);
+    const size_t smem = verify_smem_bytes_es(p.slice, sizeof(T));
     cudaError_t e = cudaFuncSetAttribute(vs::k_verify_units<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -1122,11 +1137,6 @@ cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream) {
     p.D = a.D;
     p.V = a.V;
     p.slice = verify_slice(a.V, C);
-    int lg = 0;
-    while ((int64_t{1} << lg) < a.V + 1) ++lg;
-    const int S = max(20, 52 - lg);
-    p.scale = ldexpf(1.0f, S);
-    p.inv_scale = ldexpf(1.0f, -S);
     p.res = static_cast<vs::UnitResult *>(a.workspace);
     p.status = a.status;
     cudaError_t e = a.dtype == MTPSPEC_F32 ? launch_verify_sample<float>(p, C, stream)
