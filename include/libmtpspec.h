@@ -178,6 +178,30 @@ int spec_verify_sample(const void *target_logits, const void *draft_logits, int 
  * for arguments spec_verify_sample would reject. */
 size_t spec_verify_workspace_bytes(int64_t B, int32_t D, int64_t V);
 
+/*
+ * spec_verify_sample_static — spec_verify_sample without a caller-supplied workspace.
+ * The pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory, such as a serving loop whose device memory is owned entirely
+ * by another allocator (a framework's caching pool that must see every allocation), or a
+ * latency-critical decode step that must never risk the device-wide synchronisation an
+ * allocation can cause.  The per-unit scratch lives in a fixed array inside the library
+ * (1 MiB of device memory on every GPU that loads the library, held until the process
+ * exits), so this call allocates nothing.
+ *   Arguments, outputs and status: as spec_verify_sample.
+ *   Limit: B * (D + 1) <= 65536; a larger batch returns MTPSPEC_ERR_SHAPE.
+ *   The first call on a device looks up the array's device address with that device
+ *   current; make that first call before capturing the stream into a CUDA graph.
+ *   All calls on a device share the array and each call overwrites the records it uses:
+ *   two calls whose GPU work can overlap (different streams, or threads without stream
+ *   ordering between them) race on it and give undefined results.
+ */
+int spec_verify_sample_static(const void *target_logits, const void *draft_logits, int dtype,
+                              const int32_t *draft_ids, const float *temperature,
+                              const int32_t *top_k, const float *top_p, uint64_t seed,
+                              int64_t B, int32_t D, int64_t V, int32_t *out_tokens,
+                              int32_t *num_accepted, float *p_target, float *p_draft,
+                              int32_t *status, void *stream);
+
 /* ------------------------------------------------------------------ misc */
 
 /* A static, human-readable name for an mtpspec_status value. */

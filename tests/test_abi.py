@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     assert _declared() == sorted([
         "mtp_draft_input", "mtp_draft_input_workspace_bytes", "mtp_greedy_draft",
         "spec_verify_greedy", "spec_verify_sample", "spec_verify_workspace_bytes",
-        "mtpspec_status_string"])
+        "spec_verify_sample_static", "mtpspec_status_string"])
 
 
 def test_every_declared_symbol_is_exported(so):

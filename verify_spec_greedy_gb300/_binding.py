@@ -47,6 +47,8 @@ def load():
         "spec_verify_sample": ([p, p, C.c_int, p, p, p, p, u64, i64, i32, i64, p, p, p, p, p, sz,
                                 p, p], C.c_int),
         "spec_verify_workspace_bytes": ([i64, i32, i64], sz),
+        "spec_verify_sample_static": ([p, p, C.c_int, p, p, p, p, u64, i64, i32, i64, p, p, p, p,
+                                       p, p], C.c_int),
         "mtpspec_status_string": ([C.c_int], C.c_char_p),
     }
     for name, (args, res) in sigs.items():
@@ -138,4 +140,17 @@ def spec_verify_sample(target_logits, draft_logits, draft_ids, temperature, top_
           _ptr(top_p), int(seed) & 0xFFFFFFFFFFFFFFFF, B, D1 - 1, V, _ptr(out_tokens),
           _ptr(num_accepted), _ptr(p_target), _ptr(p_draft), _ptr(workspace), ws, _ptr(status),
           _stream(stream))
+    return out_tokens, num_accepted
+
+
+def spec_verify_sample_static(target_logits, draft_logits, draft_ids, temperature, top_k, top_p,
+                              seed: int, out_tokens, num_accepted, p_target=None, p_draft=None,
+                              status=None, stream=None):
+    """spec_verify_sample with the library's own fixed scratch instead of a workspace
+    (for callers that cannot allocate device memory; see include/libmtpspec.h)."""
+    B, D1, V = target_logits.shape
+    _call("spec_verify_sample_static", _ptr(target_logits), _ptr(draft_logits),
+          _dtype_code(target_logits), _ptr(draft_ids), _ptr(temperature), _ptr(top_k),
+          _ptr(top_p), int(seed) & 0xFFFFFFFFFFFFFFFF, B, D1 - 1, V, _ptr(out_tokens),
+          _ptr(num_accepted), _ptr(p_target), _ptr(p_draft), _ptr(status), _stream(stream))
     return out_tokens, num_accepted

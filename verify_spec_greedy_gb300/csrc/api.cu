@@ -184,3 +184,48 @@ MTPSPEC_API int mtp_draft_input(const void *emb_next, const void *hidden, const 
     a.workspace = workspace;
     return launched(mtpspec::run_draft_input(a, s));
 }
+
+MTPSPEC_API int spec_verify_sample_static(const void *target_logits, const void *draft_logits,
+                                          int dtype, const int32_t *draft_ids,
+                                          const float *temperature, const int32_t *top_k,
+                                          const float *top_p, uint64_t seed, int64_t B, int32_t D,
+                                          int64_t V, int32_t *out_tokens, int32_t *num_accepted,
+                                          float *p_target, float *p_draft, int32_t *status,
+                                          void *stream) {
+    if (dtype != MTPSPEC_F32 && dtype != MTPSPEC_BF16) return MTPSPEC_ERR_DTYPE;
+    if (B < 0 || D < 1 || D > kMaxD || V < 1 || V > kMaxV || B > kMaxRows) return MTPSPEC_ERR_SHAPE;
+    if (B * (D + 1) > mtpspec::kStaticVerifyUnits) return MTPSPEC_ERR_SHAPE;
+    if (!mtpspec::verify_fits(V, elem_size(dtype))) return MTPSPEC_ERR_SHAPE;
+    if (B == 0) return MTPSPEC_OK;
+    if (!target_logits || !draft_logits || !draft_ids || !temperature || !out_tokens ||
+        !num_accepted)
+        return MTPSPEC_ERR_ARG;
+    const size_t es = elem_size(dtype);
+    if (!aligned(target_logits, es) || !aligned(draft_logits, es) || !aligned(draft_ids, 4) ||
+        !aligned(temperature, 4) || !aligned(top_k, 4) || !aligned(top_p, 4) ||
+        !aligned(out_tokens, 4) || !aligned(num_accepted, 4) || !aligned(p_target, 4) ||
+        !aligned(p_draft, 4) || !aligned(status, 4))
+        return MTPSPEC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = prepare_device(s);
+    if (rc != MTPSPEC_OK) return rc;
+    mtpspec::VerifySampleArgs a;
+    a.target = target_logits;
+    a.draft = draft_logits;
+    a.dtype = dtype;
+    a.draft_ids = draft_ids;
+    a.temperature = temperature;
+    a.top_k = top_k;
+    a.top_p = top_p;
+    a.seed = seed;
+    a.B = B;
+    a.D = D;
+    a.V = V;
+    a.out_tokens = out_tokens;
+    a.num_accepted = num_accepted;
+    a.p_target = p_target;
+    a.p_draft = p_draft;
+    a.workspace = nullptr;
+    a.status = status;
+    return launched(mtpspec::run_verify_sample_static(a, s));
+}

@@ -47,6 +47,11 @@ bool verify_fits(int64_t V, size_t elem_bytes);
 
 cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream);
 
+// The fixed-scratch variant: per-unit records in the library's static device array
+// (a.workspace is ignored).  Units B * (D + 1) must not exceed kStaticVerifyUnits.
+constexpr int64_t kStaticVerifyUnits = 65536;
+cudaError_t run_verify_sample_static(VerifySampleArgs a, cudaStream_t stream);
+
 }  // namespace mtpspec
 
 namespace mtpspec {

@@ -35,6 +35,8 @@
 // pushes into the peers' shared memory before a barrier; after the last barrier a CTA only
 // reads its own shared memory.  The bulk-copy barrier waits are bounded and raise
 // MTPSPEC_STATUS_TIMEOUT when they give up.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -1155,6 +1157,44 @@ cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream) {
     return cudaLaunchKernelEx(&fin, vs::k_verify_finalize,
                               static_cast<const vs::UnitResult *>(a.workspace), a.draft_ids, a.B,
                               a.D, a.out_tokens, a.num_accepted, a.p_target, a.p_draft);
+}
+
+}  // namespace mtpspec
+
+// ---------------------------------------------------------------- fixed-scratch variant
+
+namespace mtpspec {
+
+// Scratch of the fixed-scratch entry point: the per-unit records the two kernels of a
+// sampling verification hand over, for up to kStaticVerifyUnits units (B * (D + 1)).  It
+// lives in the library's own device memory, so that entry point allocates nothing; every
+// GPU that loads the library holds these 1 MiB until the process exits.  All calls on a
+// device share it: each call overwrites every record it reads, so nothing needs clearing,
+// and calls whose work overlaps on the GPU (other streams, other threads) race on it.
+static __device__ __align__(256) unsigned char g_verify_scratch[kStaticVerifyUnits * 16];
+static_assert(sizeof(vs::UnitResult) == 16, "one 16-byte record per unit");
+
+static std::mutex g_scratch_mu;
+static void *g_scratch_ptr[64] = {nullptr};
+
+cudaError_t run_verify_sample_static(VerifySampleArgs a, cudaStream_t stream) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    void *ptr = nullptr;
+    {
+        // once per device, with that device current: the device address of the array
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (!g_scratch_ptr[dev]) {
+            e = cudaGetSymbolAddress(&ptr, g_verify_scratch);
+            if (e != cudaSuccess) return e;
+            g_scratch_ptr[dev] = ptr;
+        }
+        ptr = g_scratch_ptr[dev];
+    }
+    a.workspace = ptr;
+    return run_verify_sample(a, stream);
 }
 
 }  // namespace mtpspec
