@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-launch-count", action="store_true",
-                    help="skip the CUDA-profiler launch count (needed under ncu)")
+                    help="accepted for older command lines; launches are counted by the library")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's row count (profiling on a smaller case)")
     return ap.parse_args()
@@ -286,31 +286,19 @@ def run_gpu(args, rank, world, dist):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"status word {int(status.item())}"
 
-    # launches of this library's kernels in one step, from the CUDA profiler
-    launches_per_step = None
-    try:
-        if args.no_launch_count:
-            raise RuntimeError("launch count skipped")
-        from torch.profiler import ProfilerActivity, profile
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            step(0)
-            torch.cuda.synchronize()
-        names = [e.name for e in prof.events() if e.device_type.name == "CUDA"]
-        ours = [n for n in names if "mtpspec" in n]
-        launches_per_step = len(ours) if ours else None
-    except Exception:
-        launches_per_step = None
-
+    # launches of this library's kernels inside the timed region, counted by the library
     clocks = ClockSampler(dev.index)
     barrier(dist)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = lib.mtpspec_launch_count()
     t_start.record(stream)
     for i in range(args.steps):
         step(i, timed=True)
     t_end.record(stream)
+    launches = lib.mtpspec_launch_count() - launches0
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier(dist)
@@ -382,7 +370,7 @@ def run_gpu(args, rank, world, dist):
            "clocks": clk,
            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                    "d2h_bytes_per_step": d2h},
-           "gpu_launches": (launches_per_step * args.steps) if launches_per_step else None,
+           "gpu_launches": launches,
            "roofline": roofline}
     return res, x, di, w
 

@@ -207,6 +207,10 @@ int spec_verify_sample_static(const void *target_logits, const void *draft_logit
 /* A static, human-readable name for an mtpspec_status value. */
 const char *mtpspec_status_string(int code);
 
+/* Diagnostics (no counterpart in the pages): the number of kernel launches this library
+ * has enqueued, on any stream and device, since it was loaded.  Thread-safe. */
+uint64_t mtpspec_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     assert _declared() == sorted([
         "mtp_draft_input", "mtp_draft_input_workspace_bytes", "mtp_greedy_draft",
         "spec_verify_greedy", "spec_verify_sample", "spec_verify_workspace_bytes",
-        "spec_verify_sample_static", "mtpspec_status_string"])
+        "spec_verify_sample_static", "mtpspec_status_string", "mtpspec_launch_count"])
 
 
 def test_every_declared_symbol_is_exported(so):
@@ -60,3 +60,7 @@ def test_host_side_validation(so):
     assert so.spec_verify_greedy(nul, 0, nul, 0, 3, 10, nul, nul, nul, nul) == 0    # B == 0
     assert so.spec_verify_greedy(nul, 1, nul, 2, 3, 10, nul, nul, nul, nul) == -1
     assert so.spec_verify_greedy(nul, 0, nul, 1, 1, 2**31, nul, nul, nul, nul) == -3
+
+
+def test_launch_count_starts_at_zero_on_the_host(so):
+    assert lib.mtpspec_launch_count() >= 0

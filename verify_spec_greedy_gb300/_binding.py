@@ -50,6 +50,7 @@ def load():
         "spec_verify_sample_static": ([p, p, C.c_int, p, p, p, p, u64, i64, i32, i64, p, p, p, p,
                                        p, p], C.c_int),
         "mtpspec_status_string": ([C.c_int], C.c_char_p),
+        "mtpspec_launch_count": ([], C.c_uint64),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name, None)
@@ -58,6 +59,11 @@ def load():
             fn.restype = res
     _lib = lib
     return lib
+
+
+def mtpspec_launch_count() -> int:
+    """Kernel launches this library has enqueued since it was loaded."""
+    return int(load().mtpspec_launch_count())
 
 
 def status_string(code: int) -> str:

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/libmtpspec.h"
@@ -51,6 +52,15 @@ int prepare_device(cudaStream_t stream) {
 int launched(cudaError_t e) { return e == cudaSuccess ? MTPSPEC_OK : MTPSPEC_ERR_CUDA; }
 
 }  // namespace
+
+namespace mtpspec {
+std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n)); }
+}  // namespace mtpspec
+
+MTPSPEC_API uint64_t mtpspec_launch_count(void) {
+    return static_cast<uint64_t>(mtpspec::g_launches.load());
+}
 
 MTPSPEC_API const char *mtpspec_status_string(int code) {
     switch (code) {

@@ -170,8 +170,11 @@ static cudaError_t launch_argmax(const void *logits, int64_t groups, int P, int6
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_argmax_groups<T>, static_cast<const T *>(logits), V, P,
-                              mode, d, out_a, out_b, status);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_argmax_groups<T>,
+                                             static_cast<const T *>(logits), V, P, mode, d, out_a,
+                                             out_b, status);
+    if (e == cudaSuccess) count_launches(1);
+    return e;
 }
 
 cudaError_t run_greedy_draft(const void *logits, int dtype, int64_t M, int64_t V, int32_t *ids,
@@ -189,6 +192,116 @@ cudaError_t run_verify_greedy(const void *target, int dtype, const int32_t *d, i
                                     stream);
     return launch_argmax<uint16_t>(target, B, D + 1, V, 1, d, tokens, num_accepted, status,
                                    stream);
+}
+
+}  // namespace mtpspec
+
+namespace mtpspec {
+
+// Greedy rows of a sampling verification: one cluster per row, all D + 1 positions.  A row
+// with a positive temperature and a valid top-p belongs to the sampling kernel and is
+// skipped.  For a greedy row the record of position j holds the argmax g_j, the flag
+// d_j == g_j, p_target = [d_j == g_j] and p_draft = [d_j valid].
+template <typename T>
+__global__ void __launch_bounds__(kArgmaxThreads)
+k_argmax_verify_rows(const T *__restrict__ logits, int64_t V, int D,
+                     const float *__restrict__ tau, const float *__restrict__ top_p,
+                     const int32_t *__restrict__ draft_ids, VerifyUnitRecord *__restrict__ rec,
+                     int32_t *__restrict__ status) {
+    __shared__ float red_v[kMaxPositions];
+    __shared__ int32_t red_i[kMaxPositions];
+    __shared__ float warp_v[kArgmaxThreads / 32];
+    __shared__ int32_t warp_i[kArgmaxThreads / 32];
+
+    const int64_t row = cluster_index();
+    const float t = tau[row];
+    const float p = top_p ? top_p[row] : 1.0f;
+    const bool bad = !(t >= 0.0f) || !(p > 0.0f);
+    if (!bad && t != 0.0f) return;  // the whole cluster takes this exit together
+
+    const uint32_t C = cluster_size();
+    const uint32_t rank = cluster_rank();
+    const int P = D + 1;
+    int64_t chunk = (V + C - 1) / C;
+    chunk = (chunk + 15) & ~static_cast<int64_t>(15);
+    const int64_t lo = min(V, static_cast<int64_t>(rank) * chunk);
+    const int64_t hi = min(V, lo + chunk);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int q = 0; q < P; ++q) {
+        ArgMax a = warp_argmax(thread_scan(logits + (row * P + q) * V, lo, hi));
+        if (lane == 0) {
+            warp_v[warp] = a.v;
+            warp_i[warp] = a.i;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            ArgMax b{-INFINITY, -1};
+            if (lane < kArgmaxThreads / 32) b = {warp_v[lane], warp_i[lane]};
+            b = warp_argmax(b);
+            if (lane == 0) {
+                red_v[q] = b.v;
+                red_i[q] = b.i;
+            }
+        }
+        __syncthreads();
+    }
+    cluster_sync();
+    if (rank == 0) {
+        for (int q = threadIdx.x; q < P; q += blockDim.x) {
+            ArgMax best{-INFINITY, -1};
+            for (uint32_t r = 0; r < C; ++r) {
+                ArgMax o;
+                o.v = ld_peer_f32(peer_addr(smem_addr(&red_v[q]), r));
+                o.i = ld_peer_s32(peer_addr(smem_addr(&red_i[q]), r));
+                best = argmax_merge(best, o);
+            }
+            const int32_t g = best.i < 0 ? 0 : best.i;
+            VerifyUnitRecord u;
+            u.token = g;
+            if (q < D) {
+                const int32_t dj = draft_ids[row * D + q];
+                const bool valid = dj >= 0 && static_cast<int64_t>(dj) < V;
+                u.flags = dj == g ? 1 : 0;
+                u.pt = dj == g ? 1.0f : 0.0f;
+                u.pd = valid ? 1.0f : 0.0f;
+                if (!valid && status) atomicOr(status, MTPSPEC_STATUS_BAD_DRAFT_ID);
+            } else {
+                u.flags = 0;
+                u.pt = u.pd = 0.0f;
+            }
+            rec[row * P + q] = u;
+        }
+        if (threadIdx.x == 0 && bad && status) atomicOr(status, MTPSPEC_STATUS_BAD_PARAM);
+    }
+    cluster_sync();
+}
+
+template <typename T>
+static cudaError_t launch_verify_greedy_rows(const VerifySampleArgs &a, cudaStream_t stream) {
+    const int C = argmax_cluster_size(a.V);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B * C), 1, 1);
+    cfg.blockDim = dim3(kArgmaxThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, k_argmax_verify_rows<T>, static_cast<const T *>(a.target), a.V, a.D, a.temperature,
+        a.top_p, a.draft_ids, static_cast<VerifyUnitRecord *>(a.workspace), a.status);
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
+cudaError_t run_verify_greedy_rows(const VerifySampleArgs &a, cudaStream_t stream) {
+    return a.dtype == MTPSPEC_F32 ? launch_verify_greedy_rows<float>(a, stream)
+                                  : launch_verify_greedy_rows<uint16_t>(a, stream);
 }
 
 }  // namespace mtpspec

@@ -187,7 +187,9 @@ static cudaError_t launch_gemv(const DraftInputArgs &a, cudaStream_t stream) {
         static_cast<const uint16_t *>(a.e), static_cast<const uint16_t *>(a.h),
         static_cast<const uint16_t *>(a.we), static_cast<const uint16_t *>(a.wh),
         static_cast<const uint16_t *>(a.W), static_cast<uint16_t *>(a.y), H, a.eps, rows);
-    return cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
 }
 
 cudaError_t run_draft_input(const DraftInputArgs &a, cudaStream_t stream) {
@@ -208,6 +210,7 @@ cudaError_t run_draft_input(const DraftInputArgs &a, cudaStream_t stream) {
         static_cast<int>(a.H), a.eps);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    count_launches(1);
     return run_gemm_bf16_nt(a.W, xn, a.y, a.H, a.M, 2 * a.H, gemm_ws, stream);
 }
 

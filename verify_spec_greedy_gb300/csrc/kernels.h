@@ -8,6 +8,9 @@
 
 namespace mtpspec {
 
+// Adds n to the library's count of kernel launches (read by mtpspec_launch_count).
+void count_launches(int n);
+
 cudaError_t run_greedy_draft(const void *logits, int dtype, int64_t M, int64_t V, int32_t *ids,
                              cudaStream_t stream);
 
@@ -18,6 +21,15 @@ cudaError_t run_verify_greedy(const void *target, int dtype, const int32_t *d, i
 }  // namespace mtpspec
 
 namespace mtpspec {
+
+// Per-unit record handed from the unit kernels of spec_verify_sample to its finalize
+// kernel: one per (row, position).
+struct VerifyUnitRecord {
+    int32_t flags;  // bit 0: draft accepted
+    int32_t token;  // greedy pick, or the draw (residual / bonus) of this unit, or -1
+    float pt;       // p_j(d_j)
+    float pd;       // q_j(d_j)
+};
 
 struct VerifySampleArgs {
     const void *target;
@@ -38,6 +50,12 @@ struct VerifySampleArgs {
     void *workspace;
     int32_t *status;
 };
+
+// Greedy rows of a sampling verification (temperature 0, or a bad sampling parameter):
+// the argmax of each of their positions, written as unit records.  Rows that sample
+// return at once.  Launched as a programmatic dependent of the sampling kernel, so the
+// two run concurrently.
+cudaError_t run_verify_greedy_rows(const VerifySampleArgs &a, cudaStream_t stream);
 
 // Bytes of per-unit results the sampling verifier keeps between its two kernels.
 size_t verify_workspace_bytes(int64_t B, int32_t D);

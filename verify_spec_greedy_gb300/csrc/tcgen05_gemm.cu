@@ -342,7 +342,9 @@ static cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, con
     if (e != cudaSuccess) return e;
     dim3 grid(g.o_tiles, g.t_tiles, g.splits);
     tg::k_gemm<BN, STAGES><<<grid, tg::NTHREADS, smem, stream>>>(ma, mb, p);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
 }
 
 cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, int64_t Mt,
@@ -380,8 +382,10 @@ cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tg::k_split_reduce, static_cast<const float *>(p.part),
-                              static_cast<uint16_t *>(Y), n, g.splits);
+    e = cudaLaunchKernelEx(&cfg, tg::k_split_reduce, static_cast<const float *>(p.part),
+                           static_cast<uint16_t *>(Y), n, g.splits);
+    if (e == cudaSuccess) count_launches(1);
+    return e;
 }
 
 }  // namespace mtpspec
