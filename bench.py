@@ -350,7 +350,7 @@ def run_gpu(args, rank, world, dist):
     vb = verify_bytes(x)
     achieved = vb / (verify_ms / 1e3) / 1e9
     traffic = profiled_traffic(args.workload)
-    roofline = {"bound": "hbm", "kernel": "k_verify_units + k_verify_finalize",
+    roofline = {"bound": "hbm", "kernel": "spec_verify_sample: k_verify_rr + k_argmax_verify_rows + k_verify_finalize",
                 "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "algorithmic_bytes_per_launch": vb,

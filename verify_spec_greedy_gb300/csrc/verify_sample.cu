@@ -6,45 +6,52 @@
 // extra token).
 //
 // Three kernels on the caller's stream:
-//  - k_verify_persistent: the sampled rows.  A persistent grid of thread-block clusters,
-//    as many as can be resident; cluster g takes units g, g + G, ... (a unit is one
-//    (row b, position j) pair of a sampled row).  CTA r of a cluster owns the contiguous
-//    vocabulary slice [r*slice, (r+1)*slice).  Each CTA keeps two shared-memory buffers:
-//    while it works on one unit, bulk asynchronous copies bring the next unit's slices of
-//    the target row (and, for j < D, of the draft row) into the other, so every logit is
-//    read from HBM exactly once and the loads overlap the work.
+//  - k_verify_rr: the sampled rows.  A persistent grid of thread-block clusters, as many
+//    as can be resident; cluster g takes units g, g + G, ... (a unit is one (row b,
+//    position j) pair of a sampled row: the target row T[b, j] and, for j < D, the draft
+//    row Q[b, j]).  CTA r of a cluster owns the contiguous vocabulary slice
+//    [r*slice, (r+1)*slice) of both rows.
+//    Data path: bulk asynchronous copies bring a unit's two slices into shared memory;
+//    the first pass moves them into registers (each thread holds up to MAXV 16-byte
+//    vectors of each row), and the shared-memory buffer is at once refilled with the next
+//    unit's slices.  Every later pass of the unit runs over registers, so every logit is
+//    read from HBM exactly once and the next unit's loads overlap all of this unit's work.
 //  - the greedy rows (temperature 0) go to the streaming argmax kernel
 //    (run_verify_greedy_rows), launched as a programmatic dependent so that it runs beside
 //    the persistent grid.
 //  - k_verify_finalize: one thread per row takes the first rejected position.
 //
-// Work on one unit, all on chip:
-//   pass 1   maximum and online softmax sum as the chunks land
-//   E1       per-CTA partials meet in every CTA through distributed shared memory
-//   pass 2   (top-k / top-p) counts over fine bins of z = (x - max) * log2(e) / tau,
-//            R bins per unit of z, only for elements that can hold the boundary; the counts
-//            are reduce-scattered and re-broadcast across the cluster (E2)
-//   plan     the bins that must hold the boundary, from exact counts (top-k) or from
-//            per-bin weight bounds count * 2^(-b/R) (top-p)
-//   gather   elements of those bins are pushed to every CTA with their weights, and the
-//            exact weight of everything above them is summed (E3); each CTA sorts the
-//            candidates (bitonic) and scans them for the exact thresholds.  If the boundary
-//            is outside the binned range or too many elements fall in its bins, an exact
-//            bisection over the 32-bit value keys replaces this step.
+// Work on one unit:
+//   pass 1   per-thread maximum and softmax sum of z = (x - max) * log2(e) / tau
+//   E1       per-CTA partials (and the draft token's logits) meet in every CTA
+//   pass 2   (top-k / top-p) a histogram over R bins per unit of z, only for elements that
+//            can hold the boundary: counts (top-k) or near-exact weight sums (top-p: each
+//            element adds its weight relative to its bin's upper edge in 2^-S units)
+//   E2       reduce-scatter of the histograms to owner CTAs, then all-gather of the sums
+//   plan     the bins that may hold the boundary: by exact counts (top-k) or by rigorous
+//            bounds on the cumulative weight (top-p)
+//   gather   elements of those bins go to every CTA; the exact weight of everything above
+//            them is summed (E3); every CTA sorts the candidates (bitonic) and scans them
+//            for the exact thresholds.  If the boundary lies outside the binned range or too
+//            many elements fall into its bins, an exact bisection over the 32-bit value
+//            keys replaces this step.
 //   accept   p(d), q(d) and U_acc <= p/q (ratio formed with both maxima factored out)
 //   draw     only for a rejected draft or the bonus position: draw weights in fixed point
 //            (2^31 per unit of probability), per-warp sums in id order, CTA sums exchanged
-//            (E4), and the CTA holding the target walks its slice to the token.
+//            (E4), and the CTA holding the target walks its registers to the token.
+//
+// Exchanges are point to point: a CTA writes its part into every peer's shared memory and
+// then arrives (release, cluster scope) on that peer's mbarrier for the exchange; a CTA
+// waits (acquire) until all C CTAs have arrived.  E1 alternates between two barriers and
+// buffers by unit parity; every other exchange has one buffer, which is safe because a
+// CTA can only write a peer's buffer for unit k + 1 after that peer has arrived at E1 of
+// unit k + 1, i.e. after it finished unit k.  All waits are bounded and raise
+// MTPSPEC_STATUS_TIMEOUT when they give up.
 //
 // Weight sums are formed per thread in fp32 over a fixed set of elements, converted once
 // to 64-bit fixed point and reduced as integers, so every sum is deterministic and the same
 // in every CTA of a cluster.  Every decision is computed identically in every CTA from
-// exchanged data, so all CTAs run the same sequence of cluster barriers.  Exchanges are
-// pushes into the peers' shared memory before a barrier.  Every unit starts with barrier
-// B1 after its first exchange, so later exchanges of a unit cannot overwrite data a slower
-// CTA still reads for the previous unit; the first exchange alternates between two
-// buffers by unit parity.  The bulk-copy waits are bounded and raise
-// MTPSPEC_STATUS_TIMEOUT when they give up.
+// exchanged data, so all CTAs take the same sequence of exchanges.
 #include <mutex>
 
 #include "common.cuh"
@@ -56,83 +63,80 @@ namespace vs {
 constexpr int NT = 512;          // threads per CTA
 constexpr int NW = NT / 32;      // warps per CTA
 constexpr int MAXC = 16;         // largest cluster
-constexpr int R = 64;            // histogram bins per unit of z (log2 of the softmax weight)
+constexpr int MAXV = 10;         // most 16-byte vectors per thread per row in registers (fp32)
+constexpr int MAXV_BF16 = 8;     // the same for bf16 rows
+constexpr int R = 32;            // histogram bins per unit of z (log2 of the softmax weight)
 constexpr int ZR = 24;           // binned range: z in (-ZR, 0], weights in (2^-24, 1]
 constexpr int NB = R * ZR;       // bins
-constexpr int INCOMING = NB + MAXC;  // reduce-scatter slots per row (C * ceil(NB / C))
-constexpr int CAP = 512;         // boundary candidates per row (= NT: one per thread)
+constexpr int RSN = NB + 4 * MAXC;  // reduce-scatter inbox per row (C * RS, RS a multiple of 4)
+constexpr int CAPT = 1024;       // candidate slots per row in a cluster (CAPT / C per CTA)
 constexpr int NCH = 4;           // bulk-copy chunks per row
+constexpr int WPC = NW / NCH;    // warps whose register blocks one chunk covers
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr float FX = 2147483648.0f;  // 2^31: fixed-point scale of weights (weights <= 1)
 constexpr double INV_FX = 1.0 / 2147483648.0;
-constexpr float BOUND_SLACK = 4e-5f;  // relative slack of the per-bin weight bounds
-static_assert(CAP == NT, "the candidate sort keeps one candidate per thread");
+
+// exchange barriers
+constexpr int XB_E1 = 0;   // two, by unit parity
+constexpr int XB_RS = 2;
+constexpr int XB_AG = 3;
+constexpr int XB_E3 = 4;
+constexpr int XB_E4 = 5;   // two, by draw attempt
+constexpr int XB_S = 7;    // two, by exact-search step parity
+constexpr int NXB = 9;
 
 using UnitResult = VerifyUnitRecord;
 
-struct __align__(8) Cand {
-    float v;       // logit
-    uint32_t idx;  // token id
-};
+constexpr int MVMAX = MAXV > MAXV_BF16 ? MAXV : MAXV_BF16;
+constexpr int NSMALL = NT / 2;   // candidates per row ranked by counting (both rows at once)
 
 struct __align__(16) Shared {
-    unsigned long long bar[2][2][NCH];  // [buffer][row][chunk] bulk-copy barriers
-    // block reductions
-    float rf[2][NW];
-    float rs[2][NW];
+    unsigned long long dbar[2][NCH];   // [row][chunk] bulk-copy barriers
+    unsigned long long xbar[NXB];      // exchange barriers (C arrivals each)
+    float4 e1[2][MAXC];                // E1, by unit parity: (m0, s0, m1, s1) per CTA
+    float2 e1d[2];                     // E1, by unit parity: the draft token's logits
+    uint32_t hloc[2][RSN];             // this CTA's histogram (zero past the used bins)
+    uint32_t rsin[2][RSN];             // reduce-scatter inbox [row][source CTA * RS + bin]
+    uint32_t hist[2][RSN];             // cluster-wide histogram
+    uint32_t topfix[NB];               // round(2^(31 - b/R)): the fixed-point scale of bin b
+    unsigned long long cand[2][CAPT];  // candidates: (value bits << 32) | token id
+    uint32_t ccnt[MAXC][2];            // candidates found per CTA
+    unsigned long long cabove[MAXC][2];  // per CTA: fixed-point weight above the candidates
+    unsigned long long sx[2][MAXC][2];   // exact search: per step parity, per CTA
+    unsigned long long dr[2][MAXC];      // draw: per attempt, each CTA's fixed-point weight
+    float rf[2][NW], rs[2][NW];
     unsigned long long ru[2][NW];
     unsigned long long scan[NW];
+    unsigned long long wsum[NW];
+    uint32_t tsum[MVMAX][NT];          // draw: each thread's vector sums
     int32_t scani[NW];
-    // E1, by unit parity: partials of every CTA and the draft token's logit per row
-    float x_m[2][MAXC][2];
-    float x_s[2][MAXC][2];
-    float x_d[2][2];
+    unsigned long long skey[NT];       // sort keys; candidate weights when ranking by counting
+    float sval[NT];                    // sorted values; candidate values when counting
+    float red_v[NW];                   // per-warp reductions of the counting path
+    unsigned long long red_w[NW];
+    unsigned long long psc_lo[NW], psc_hi[NW];  // plan: per-warp totals of the bound scans
+    uint32_t psc_cn[NW];
+    int32_t pb1[2], pb2[2];            // plan: crossing bins found by the scan
+    uint32_t pcc1[2], pcc2[2];         // plan: count bounds before b1 and through b2
+    uint32_t lcnt[2];                  // candidate slot allocator of this CTA
+    float xd[2];                       // the draft token's logits, if this CTA holds it
     // per-row state, identical in every CTA of the cluster
     float m[2], Z[2], invZ[2], theta[2], zcut[2];
-    int32_t deg[2];           // a row of all -inf: a point mass on id 0
-    int32_t mode[2];          // 0 no filter, 1 candidates, 2 exact bisection
-    int32_t b1[2], b2[2];
-    uint32_t ncand[2];
+    float nmc[2];     // -m * c2: z = x * c2 + nmc
+    float tzb[2];     // m * c2 * R: the bin coordinate tz = -z * R = x * (-c2 * R) + tzb
+    int32_t deg[2];   // a row of all -inf: a point mass on id 0
+    int32_t mode[2];  // 0 no filter, 1 candidates, 2 exact bisection
+    int32_t b1[2], b2[2], nbu[2];
     unsigned long long tgt[2];
-    // histogram of counts (local during pass 2, cluster-wide after E2)
-    uint32_t hcnt[2][NB];
-    // reduce-scatter inbox, reused for the boundary candidates
-    union {
-        uint32_t in[2][INCOMING];
-        struct {
-            Cand c[2][CAP];
-            unsigned long long w[2][CAP];
-        } cd;
-    } u;
-    unsigned long long skey[CAP];      // candidate sort keys, then exclusive weight prefix
-    float sval[CAP];                   // sorted candidate values
-    uint32_t cand_n[2];                // slot allocator, used in CTA 0
-    uint32_t lcount[2];                // this CTA's own candidates, then its base slot
-    Cand lc[2][CAP];                   // this CTA's own candidates before the push
-    uint32_t lw[2][CAP];
-    unsigned long long ma_x[MAXC][2];  // per-CTA fixed-point weight above bin b1
-    unsigned long long sx[2][2][MAXC];  // exact bisection exchange, by iteration parity
-    unsigned long long dr_R[2][MAXC];   // per draw attempt: each CTA's fixed-point weight
-    unsigned long long w_sum[NW];
-    int32_t flags;  // bit 0: a bulk copy timed out
-    int32_t pick[4];
-    float fpick[4];
+    int32_t flags;    // bit 0: a bulk copy timed out; bit 1: an exchange timed out
+    int32_t pick[2];
+    float fpick[2];
 };
 
 __device__ __forceinline__ float ex2(float z) {
     float r;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(z));
     return r;
-}
-// z = (x - m) * c2, written so that every pass computes it with the same two roundings
-__device__ __forceinline__ float zval(float x, float m, float c2) {
-    return __fmul_rn(__fsub_rn(x, m), c2);
-}
-// bin of z in (-ZR, 0]; NB below the range (or NaN)
-__device__ __forceinline__ int zbin(float z) {
-    if (!(z > -static_cast<float>(ZR))) return NB;
-    const int b = static_cast<int>(__fmul_rn(-z, static_cast<float>(R)));
-    return b < NB ? b : NB - 1;
 }
 // a weight (<= 1) in fixed point; the float-to-32-bit conversion is a fast instruction
 __device__ __forceinline__ uint32_t fix31(float w) { return __float2uint_rn(__fmul_rn(w, FX)); }
@@ -183,9 +187,6 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
     return v;
-}
-__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
-    return __reduce_add_sync(0xFFFFFFFFu, v);
 }
 
 // Sum of one u64 per thread over the block; every thread gets the result.
@@ -263,6 +264,29 @@ __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, uint3
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+// The same with acquire semantics at cluster scope: the peers' writes released by their
+// arrivals are visible after it returns true.
+__device__ __forceinline__ bool xbar_wait_bounded(unsigned long long *bar, uint32_t parity) {
+    for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+// Arrive on CTA `peer`'s copy of the barrier, releasing this thread's earlier writes (and,
+// through a preceding __syncthreads, the whole CTA's) at cluster scope.
+__device__ __forceinline__ void xarrive(unsigned long long *bar, uint32_t peer) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                     peer_addr(smem_addr(bar), peer))
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
                                               unsigned long long *bar) {
     asm volatile(
@@ -281,105 +305,93 @@ __device__ __forceinline__ void cluster_arrive_release() {
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-
-// Visit every element [0, n) of a shared-memory slice as (value, local index), with
-// 16-byte vector reads for the aligned body, threads strided over vectors.  Each thread
-// always visits the same elements in the same order.
-template <typename T, typename F>
-__device__ __forceinline__ void for_each_elem(const T *s, int n, F &&f) {
-    constexpr int EPV = elems_per_16B<T>::value;
-    const int nv = n / EPV;
-    const uint4 *v = reinterpret_cast<const uint4 *>(s);
-    for (int i = threadIdx.x; i < nv; i += NT) {
-        float x[EPV];
-        unpack(v[i], x);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) f(x[e], i * EPV + e);
-    }
-    for (int i = nv * EPV + threadIdx.x; i < n; i += NT) f(widen(s[i]), i);
+__device__ __forceinline__ void st_peer_v4(uint32_t a, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_peer_u32x4(uint32_t a, uint4 v) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_peer_v2(uint32_t a, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y)
+                 : "memory");
 }
 
-// First bin whose cumulative count reaches `need` (NB if none); one warp.
-__device__ void count_search(const uint32_t *cnt, uint32_t need, int32_t *out) {
-    const int lane = threadIdx.x & 31;
-    constexpr int PER = NB / 32;
-    uint32_t own = 0;
-    for (int t = 0; t < PER; ++t) own += cnt[lane * PER + t];
-    uint32_t incl = own;
+// Every element of a thread's register block of one row: f(x, t, e) for vector t < vpt,
+// element e.  Vector t of thread (warp, lane) is vector warp*32*vpt + t*32 + lane of the
+// CTA's slice, so a warp owns a contiguous run of the slice and, within it, (t, lane, e)
+// is ascending id order.
+template <int EPV, int MV, typename F>
+__device__ __forceinline__ void for_regs(const uint4 (&rv)[MV], int vpt, F &&f) {
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += a;
+    for (int t = 0; t < MV; ++t) {
+        if (t < vpt) {
+            float x[EPV];
+            unpack(rv[t], x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) f(x[e], t, e);
+        }
     }
-    const unsigned ball = __ballot_sync(0xFFFFFFFFu, incl - own < need && incl >= need);
-    if (ball == 0) {
-        if (lane == 0) *out = NB;
-    } else if (lane == __ffs(ball) - 1) {
-        uint32_t acc = incl - own;
-        for (int t = 0; t < PER; ++t) {
-            acc += cnt[lane * PER + t];
-            if (acc >= need) {
-                *out = lane * PER + t;
-                break;
+}
+
+// The same over row r (0 or 1, at run time) of the two rows' blocks: the element code is
+// emitted once for both rows.
+template <int EPV, int MV, typename F>
+__device__ __forceinline__ void for_row(const uint4 (&rv)[2][MV], int r, int vpt, F &&f) {
+#pragma unroll
+    for (int t = 0; t < MV; ++t) {
+        if (t < vpt) {
+            const uint4 v = r ? rv[1][t] : rv[0][t];
+            float x[EPV];
+            unpack(v, x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) f(x[e], t, e);
+        }
+    }
+}
+
+// Replace the elements from `keep` on of one 16-byte vector by -inf.
+template <int EPV>
+__device__ __forceinline__ uint4 mask_tail(uint4 v, int keep) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+        if (e >= keep) {
+            if (EPV == 4) {
+                w[e] = 0xFF800000u;
+            } else {
+                const int q = e >> 1;
+                w[q] = (e & 1) ? ((w[q] & 0x0000FFFFu) | 0xFF800000u) : ((w[q] & 0xFFFF0000u) | 0xFF80u);
             }
         }
     }
-    __syncwarp();
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Bins that must hold the top-p boundary: bin b holds weights in [2^-(b+1)/R, 2^-b/R]
-// (relative to the row maximum), so the cumulative weight of bins 0..b lies between two
-// bounds.  *first = the first bin whose upper bound reaches `need`, *last = the first bin
-// whose lower bound reaches it (NB if none).  One warp.
-__device__ void weight_search(const uint32_t *cnt, float need, int32_t *first, int32_t *last) {
-    const int lane = threadIdx.x & 31;
-    constexpr int PER = NB / 32;
-    const float step = ex2(-1.0f / R);
-    const float up = 1.0f + BOUND_SLACK, dn = (1.0f - BOUND_SLACK) * step;
-    float hi = 0.0f, lo = 0.0f;
-    float w = ex2(-static_cast<float>(lane * PER) / R);
-    for (int t = 0; t < PER; ++t) {
-        const float c = static_cast<float>(cnt[lane * PER + t]);
-        hi += c * w * up;
-        lo += c * w * dn;
-        w *= step;
-    }
-    float ihi = hi, ilo = lo;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float a = __shfl_up_sync(0xFFFFFFFFu, ihi, o);
-        const float c = __shfl_up_sync(0xFFFFFFFFu, ilo, o);
-        if (lane >= o) {
-            ihi += a;
-            ilo += c;
-        }
-    }
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
-        const float incl = pass == 0 ? ihi : ilo, own = pass == 0 ? hi : lo;
-        const float f = pass == 0 ? up : dn;
-        int32_t *out = pass == 0 ? first : last;
-        const unsigned ball = __ballot_sync(0xFFFFFFFFu, incl - own < need && incl >= need);
-        if (ball == 0) {
-            if (lane == 0) *out = NB;
-        } else if (lane == __ffs(ball) - 1) {
-            float acc = incl - own;
-            float ww = ex2(-static_cast<float>(lane * PER) / R);
-            int res = lane * PER + PER - 1;
-            for (int t = 0; t < PER; ++t) {
-                acc += static_cast<float>(cnt[lane * PER + t]) * ww * f;
-                ww *= step;
-                if (acc >= need) {
-                    res = lane * PER + t;
-                    break;
-                }
-            }
-            *out = res;
-        }
-    }
-    __syncwarp();
+// Bounds on the fixed-point weight of bin b of a top-p histogram.  Bin b holds elements
+// with z in (-(b+1)/R, -b/R]; each added q = round(2^(z + b/R) * sq), so the bin's
+// fixed-point weight (2^31 per unit) is q_sum * 2^(31 - b/R) / sq.  Bounds are kept in units
+// of 2^-31 / sq as exact integers: mid = q_sum * topfix[b], widened by the rounding of q
+// (half a unit, times topfix, per element), by the rounding of the fixed-point weights of
+// the final decision (half of 2^-31, i.e. sq / 2, per element), and by 2^-15 of mid for the
+// relative error of the fp32 weights and of the table; an element adds at least qmin, so a
+// bin holds at most q_sum / qmin elements (cnt, rounded up).
+__device__ __forceinline__ void bin_bounds(const uint32_t *q, const uint32_t *topfix, int bn,
+                                           float qmin_inv, uint32_t sq,
+                                           unsigned long long &lo, unsigned long long &hi,
+                                           uint32_t &cnt) {
+    const uint32_t qs = q[bn];
+    const uint32_t tf = topfix[bn];
+    const unsigned long long mid = static_cast<unsigned long long>(qs) * tf;
+    cnt = static_cast<uint32_t>(static_cast<float>(qs) * qmin_inv) + 2u;
+    const unsigned long long err =
+        (mid >> 15) + static_cast<unsigned long long>(cnt) * ((tf >> 1) + 1u + sq);
+    lo = mid > err ? mid - err : 0ull;
+    hi = mid + err;
 }
-
 struct Params {
     const void *T;
     const void *Q;
@@ -391,9 +403,10 @@ struct Params {
     int64_t B;
     int32_t D;
     int64_t V;
-    int64_t slice;
-    int32_t nbuf;  // shared-memory data buffers per CTA: 2 (double-buffered) or 1
-    int32_t G;     // clusters in the persistent grid
+    int64_t slice;  // logits per CTA (a multiple of 16)
+    int32_t vpt;    // 16-byte vectors per thread per row (<= MAXV, MAXV_BF16)
+    int32_t G;      // clusters in the persistent grid
+    uint32_t sq;    // 2^S: scale of the per-element weights of a top-p histogram
     UnitResult *res;
     int32_t *status;
 };
@@ -406,454 +419,739 @@ __device__ __forceinline__ bool row_sampled(const Params &P, int64_t b) {
 
 // ---------------------------------------------------------------- the persistent kernel
 
+// Per-unit parameters of a sampled row, loaded one unit ahead.
+struct UnitParams {
+    int b, j;
+    float tau, pp;
+    int32_t kk, d;
+};
+
 template <typename T>
-__global__ void __launch_bounds__(NT, 1) k_verify_persistent(const Params P) {
+__global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Shared &sh = *reinterpret_cast<Shared *>(smem_raw);
     constexpr int EPV = elems_per_16B<T>::value;
+    constexpr int MV = sizeof(T) == 4 ? MAXV : MAXV_BF16;
+    // -inf in every element of a 32-bit word (one fp32, or two bf16)
+    constexpr uint32_t NEG = sizeof(T) == 4 ? 0xFF800000u : 0xFF80FF80u;
     const size_t data_off = (sizeof(Shared) + 127) & ~static_cast<size_t>(127);
     const size_t row_bytes =
         ((static_cast<size_t>(P.slice) * sizeof(T)) + 127) & ~static_cast<size_t>(127);
-    auto sdat = [&](int buf, int row) -> T * {
-        return reinterpret_cast<T *>(smem_raw + data_off + (2 * buf + row) * row_bytes);
+    auto sdat = [&](int row) -> T * {
+        return reinterpret_cast<T *>(smem_raw + data_off + row * row_bytes);
     };
 
     const uint32_t C = cluster_size();
     const uint32_t rank = cluster_rank();
-    const int64_t g = cluster_index();
+    const int g = static_cast<int>(cluster_index());
     const int D = P.D;
-    const int64_t V = P.V;
-    const int64_t U = P.B * (D + 1);
-    const int64_t G = P.G;
+    const int V = static_cast<int>(P.V);
+    const int U = static_cast<int>(P.B) * (D + 1);
+    const int G = P.G;
+    const int vpt = P.vpt;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t lo64 = static_cast<int64_t>(rank) * P.slice;
-    const int64_t rest = V - lo64;
-    const int n = static_cast<int>(rest <= 0 ? 0 : (rest < P.slice ? rest : P.slice));
-    const int nv = n / EPV;
-    const int per_ch = (nv + NCH - 1) / NCH;
+    const int lo = static_cast<int>(rank) * static_cast<int>(P.slice);
+    const int n = max(0, min(V - lo, static_cast<int>(P.slice)));
+    const int nvb = n / EPV;               // whole vectors (bulk-copied when aligned)
+    const int nvr = (n + EPV - 1) / EPV;   // vectors with the ragged one
+    const int wbase = warp * 32 * vpt;     // first vector of this warp's register block
+    const int blk = WPC * 32 * vpt;        // vectors per chunk
+    const int capc = CAPT / static_cast<int>(C);
 
     // ---- set-up
     if (tid == 0) {
-        for (int bb = 0; bb < 2; ++bb)
-            for (int r = 0; r < 2; ++r)
-                for (int c = 0; c < NCH; ++c) mbar_init(&sh.bar[bb][r][c], 1);
+        for (int r = 0; r < 2; ++r)
+            for (int c = 0; c < NCH; ++c) mbar_init(&sh.dbar[r][c], 1);
+        for (int i = 0; i < NXB; ++i) mbar_init(&sh.xbar[i], C);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         sh.flags = 0;
     }
+    for (int i = tid; i < NB; i += NT)
+        sh.topfix[i] = __float2uint_rn(ex2(31.0f - static_cast<float>(i) * (1.0f / R)));
     __syncthreads();
     cluster_arrive_release();  // peers may touch this CTA's shared memory after the wait below
     pdl_launch_dependents();   // the greedy-row kernel runs beside this grid
 
-    auto row_ptr = [&](int64_t u, int r) -> const T * {
-        const int64_t b = u / (D + 1);
-        const int j = static_cast<int>(u - b * (D + 1));
-        return r == 0 ? static_cast<const T *>(P.T) + (b * (D + 1) + j) * V + lo64
-                      : static_cast<const T *>(P.Q) + (b * D + j) * V + lo64;
+    auto load_params = [&](int u) -> UnitParams {
+        UnitParams q;
+        q.b = u / (D + 1);
+        q.j = u - q.b * (D + 1);
+        q.tau = P.tau[q.b];
+        q.kk = P.topk ? P.topk[q.b] : 0;
+        q.pp = P.topp ? P.topp[q.b] : 1.0f;
+        q.d = q.j < D ? P.d[q.b * D + q.j] : -1;
+        return q;
     };
-    auto next_unit = [&](int64_t u) -> int64_t {
+    auto row_ptr = [&](int b, int j, int r) -> const T * {
+        return r == 0 ? static_cast<const T *>(P.T) + (static_cast<int64_t>(b) * (D + 1) + j) * V + lo
+                      : static_cast<const T *>(P.Q) + (static_cast<int64_t>(b) * D + j) * V + lo;
+    };
+    auto next_unit = [&](int u) -> int {
         for (u += G; u < U; u += G)
             if (row_sampled(P, u / (D + 1))) return u;
         return -1;
     };
-    // thread 0: arm every chunk barrier of buffer `buf` exactly once for unit u, with
-    // bulk copies of the 16-byte-aligned bodies of its rows
-    auto issue = [&](int64_t u, int buf) {
-        const int j = static_cast<int>(u % (D + 1));
+    // lane 0 of warps 0 .. 2 * NCH - 1: arm chunk barrier (warp / NCH, warp % NCH) exactly
+    // once for unit (b, j), with a bulk copy of the 16-byte-aligned body of that chunk
+    auto issue = [&](int b, int j, bool after_reads) {
+        if (lane != 0 || warp >= 2 * NCH) return;
+        const int r = warp / NCH, c = warp % NCH;
         const int nrows = j < D ? 2 : 1;
-        for (int r = 0; r < 2; ++r) {
-            const T *src = r < nrows ? row_ptr(u, r) : nullptr;
-            const bool bulk = r < nrows && nv > 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
-            for (int c = 0; c < NCH; ++c) {
-                const int v0 = c * per_ch, v1 = min(nv, v0 + per_ch);
-                if (bulk && v1 > v0) {
-                    const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
-                    mbar_expect_tx(&sh.bar[buf][r][c], bytes);
-                    bulk_copy_g2s(sdat(buf, r) + v0 * EPV, src + v0 * EPV, bytes, &sh.bar[buf][r][c]);
-                } else {
-                    mbar_arrive(&sh.bar[buf][r][c]);
-                }
-            }
+        const T *src = r < nrows ? row_ptr(b, j, r) : nullptr;
+        const bool bulk = r < nrows && nvb > 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+        const int v0 = min(nvb, c * blk), v1 = min(nvb, (c + 1) * blk);
+        if (bulk && v1 > v0) {
+            if (after_reads) fence_proxy_async_smem();
+            const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
+            mbar_expect_tx(&sh.dbar[r][c], bytes);
+            bulk_copy_g2s(sdat(r) + v0 * EPV, src + v0 * EPV, bytes, &sh.dbar[r][c]);
+        } else {
+            mbar_arrive(&sh.dbar[r][c]);
         }
     };
 
-    int64_t u = -1;
-    if (g < U) u = row_sampled(P, g / (D + 1)) ? g : next_unit(g);
-    if (tid == 0 && u >= 0) {
-        issue(u, 0);
-        if (P.nbuf == 2) {
-            const int64_t u1 = next_unit(u);
-            if (u1 >= 0) issue(u1, 1);
+    uint32_t ph = 0;      // current phase parity of each exchange barrier (bit i)
+    uint32_t sstep = 0;   // exact-search exchanges so far
+    bool xdead = false;   // an exchange wait gave up: skip the remaining waits
+    auto xwait = [&](int i) {
+        const uint32_t par = (ph >> i) & 1u;
+        ph ^= 1u << i;
+        if (xdead) return;
+        if (!xbar_wait_bounded(&sh.xbar[i], par)) {
+            xdead = true;
+            atomicOr(&sh.flags, 2);
         }
+    };
+
+    int u = -1;
+    if (g < U) u = row_sampled(P, g / (D + 1)) ? g : next_unit(g);
+    UnitParams nxt = {0, 0, 1.0f, 1.0f, 0, -1};
+    if (u >= 0) {
+        nxt = load_params(u);
+        issue(nxt.b, nxt.j, false);
     }
     bool started = false;
 
     for (int k = 0; u >= 0; ++k) {
-        const int buf = P.nbuf == 2 ? (k & 1) : 0;
-        const uint32_t par = static_cast<uint32_t>(P.nbuf == 2 ? (k >> 1) & 1 : k & 1);
+        const UnitParams cur = nxt;
+        const int un = next_unit(u);
+        if (un >= 0) nxt = load_params(un);  // in flight while this unit works
+        const uint32_t dpar = static_cast<uint32_t>(k & 1);
         const int ep = k & 1;
-        if (P.nbuf == 1 && k > 0 && tid == 0) issue(u, 0);
-        T *const sd0 = sdat(buf, 0);
-        T *const sd1 = sdat(buf, 1);
-
-        const int64_t b = u / (D + 1);
-        const int j = static_cast<int>(u - b * (D + 1));
-        const float tau = P.tau[b];
-        const int32_t kk = P.topk ? P.topk[b] : 0;
-        const float pp = P.topp ? P.topp[b] : 1.0f;
-        const bool has_q = j < D;
-        const int nrows = has_q ? 2 : 1;
-        const bool k_on = kk >= 1 && static_cast<int64_t>(kk) < V;
+        const int b = cur.b, j = cur.j;
+        const float tau = cur.tau, pp = cur.pp;
+        const int32_t kk = cur.kk, d = cur.d;
+        const int nrows = j < D ? 2 : 1;
+        const bool k_on = kk >= 1 && kk < V;
         const bool p_on = pp < 1.0f;
         const float c2 = __fdiv_rn(1.44269504088896340736f, tau);
-        const int32_t d = j < D ? P.d[b * D + j] : -1;
-        const bool dvalid = d >= 0 && static_cast<int64_t>(d) < V;
-        const bool d_here =
-            dvalid && static_cast<int64_t>(d) >= lo64 && static_cast<int64_t>(d) < lo64 + n;
+        const bool dvalid = d >= 0 && d < V;
+        const bool d_here = dvalid && d >= lo && d < lo + n;
 
         // the parts the bulk copies do not cover: a ragged tail, or a misaligned row
         for (int r = 0; r < nrows; ++r) {
-            const T *src = row_ptr(u, r);
-            const bool bulk = nv > 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
-            T *dst = r == 0 ? sd0 : sd1;
-            for (int i = (bulk ? nv * EPV : 0) + tid; i < n; i += NT) dst[i] = src[i];
+            const T *src = row_ptr(b, j, r);
+            const bool bulk = nvb > 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+            T *dst = sdat(r);
+            for (int i = (bulk ? nvb * EPV : 0) + tid; i < n; i += NT) dst[i] = src[i];
         }
         if (tid == 0) {
-            sh.cand_n[0] = sh.cand_n[1] = 0;
-            sh.lcount[0] = sh.lcount[1] = 0;
+            sh.lcnt[0] = sh.lcnt[1] = 0;
             sh.fpick[0] = sh.fpick[1] = -INFINITY;
         }
-        for (int i = tid; i < 2 * NB; i += NT) (&sh.hcnt[0][0])[i] = 0;
+        if (k_on || p_on)
+            for (int i = tid; i < 2 * RSN; i += NT) (&sh.hloc[0][0])[i] = 0;
         __syncthreads();
 
-        // ---- pass 1: maximum + online softmax sum, as the chunks land
-        bool timed_out = false;
-        auto pass1_row = [&](const T *s, int r, bool active) {
-            float tm = -INFINITY, ts = 0.0f;
-            const uint4 *vp = reinterpret_cast<const uint4 *>(s);
-            for (int c = 0; c < NCH; ++c) {
-                if (!mbar_wait_bounded(&sh.bar[buf][r][c], par)) timed_out = true;
-                if (!active) continue;
-                const int v0 = c * per_ch, v1 = min(nv, v0 + per_ch);
-                for (int i = v0 + tid; i < v1; i += NT) {
-                    float x[EPV];
-                    unpack(vp[i], x);
-                    float vm = x[0];
+        // ---- pass 1a: this warp's register blocks of both rows, as their chunk lands
+        uint4 rv[2][MV];
+        {
+            bool timed_out = false;
+            const int ch = warp / WPC;
 #pragma unroll
-                    for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, x[e]);
-                    if (vm > tm) {
-                        ts *= ex2(__fmul_rn(tm - vm, c2));
-                        tm = vm;
-                    }
-                    if (tm > -INFINITY) {
-                        const float nmc = -tm * c2;
-                        float a = 0.0f;
+            for (int r = 0; r < 2; ++r) {
+                if (!mbar_wait_bounded(&sh.dbar[r][ch], dpar)) timed_out = true;
+                const uint4 *sv = reinterpret_cast<const uint4 *>(sdat(r));
 #pragma unroll
-                        for (int e = 0; e < EPV; ++e) a += ex2(fmaf(x[e], c2, nmc));
-                        ts += a;
+                for (int t = 0; t < MV; ++t) {
+                    const int vi = wbase + t * 32 + lane;
+                    uint4 v = make_uint4(NEG, NEG, NEG, NEG);
+                    if (r < nrows && t < vpt && vi < nvr) {
+                        v = sv[vi];
+                        if (vi >= nvb) v = mask_tail<EPV>(v, n - vi * EPV);
                     }
+                    rv[r][t] = v;
                 }
             }
-            if (active)
-                for (int i = nv * EPV + tid; i < n; i += NT) {
-                    const float x = widen(s[i]);
-                    if (x > -INFINITY) ms_merge(tm, ts, x, 1.0f, c2);
-                }
+            if (d_here && tid == 0) {
+                sh.xd[0] = widen(sdat(0)[d - lo]);
+                sh.xd[1] = widen(sdat(1)[d - lo]);
+            }
+            if (timed_out) atomicOr(&sh.flags, 1);
+        }
+        __syncthreads();
+        // the shared-memory buffer is free: bring in the next unit
+        if (un >= 0) issue(nxt.b, nxt.j, true);
+
+        // ---- pass 1b: per-thread maximum and softmax sum, merged per warp
+#pragma unroll 1
+        for (int r = 0; r < nrows; ++r) {
+            float tm = -INFINITY;
+            for_row<EPV, MV>(rv, r, vpt, [&](float x, int, int) { tm = fmaxf(tm, x); });
+            float ts = 0.0f;
+            if (tm > -INFINITY) {
+                const float nmc = -tm * c2;
+                for_row<EPV, MV>(rv, r, vpt, [&](float x, int, int) { ts += ex2(fmaf(x, c2, nmc)); });
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
                 const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
                 ms_merge(tm, ts, m2, s2, c2);
             }
-            if (active && lane == 0) {
+            if (lane == 0) {
                 sh.rf[r][warp] = tm;
                 sh.rs[r][warp] = ts;
             }
-        };
-        pass1_row(sd0, 0, true);
-        pass1_row(sd1, 1, nrows > 1);
-        if (timed_out) atomicOr(&sh.flags, 1);
+        }
         __syncthreads();
         if (!started) {
-            cluster_wait_acquire();  // every CTA of the cluster has started
+            cluster_wait_acquire();  // every CTA of the cluster has initialised its barriers
             started = true;
         }
 
-        // ---- E1: push this CTA's partials (and the draft's logits) to every CTA
-        if (tid < nrows) {
-            const int r = tid;
-            float mv = -INFINITY, sv = 0.0f;
-            for (int w = 0; w < NW; ++w) ms_merge(mv, sv, sh.rf[r][w], sh.rs[r][w], c2);
-            const float xd =
-                d_here ? widen((r == 0 ? sd0 : sd1)[static_cast<int64_t>(d) - lo64]) : 0.0f;
-            for (uint32_t c = 0; c < C; ++c) {
-                st_peer_f32(peer_addr(smem_addr(&sh.x_m[ep][rank][r]), c), mv);
-                st_peer_f32(peer_addr(smem_addr(&sh.x_s[ep][rank][r]), c), sv);
-                if (d_here) st_peer_f32(peer_addr(smem_addr(&sh.x_d[ep][r]), c), xd);
+        // ---- E1: warp 0 merges the warps' partials (lanes 0-15 row 0, 16-31 row 1) and
+        // sends this CTA's partials (and the draft's logits) to every CTA
+        if (warp == 0) {
+            const int r = lane >> 4;
+            float tm = r < nrows ? sh.rf[r][lane & 15] : -INFINITY;
+            float ts = r < nrows ? sh.rs[r][lane & 15] : 0.0f;
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
+                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
+                ms_merge(tm, ts, m2, s2, c2);
+            }
+            const float4 part = make_float4(__shfl_sync(0xFFFFFFFFu, tm, 0), __shfl_sync(0xFFFFFFFFu, ts, 0),
+                                            __shfl_sync(0xFFFFFFFFu, tm, 16), __shfl_sync(0xFFFFFFFFu, ts, 16));
+            if (lane < static_cast<int>(C)) {
+                st_peer_v4(peer_addr(smem_addr(&sh.e1[ep][rank]), lane), part);
+                if (d_here) st_peer_v2(peer_addr(smem_addr(&sh.e1d[ep]), lane), make_float2(sh.xd[0], sh.xd[1]));
+                xarrive(&sh.xbar[XB_E1 + ep], lane);
             }
         }
-        cluster_sync();  // B1
+        xwait(XB_E1 + ep);
 
-        // ---- row statistics (every CTA, identical)
-        if (tid < nrows) {
-            const int r = tid;
-            float mv = -INFINITY, sv = 0.0f;
-            for (uint32_t c = 0; c < C; ++c) ms_merge(mv, sv, sh.x_m[ep][c][r], sh.x_s[ep][c][r], c2);
-            float mx = -INFINITY;
-            for (uint32_t c = 0; c < C; ++c) mx = fmaxf(mx, sh.x_m[ep][c][r]);
-            if (sv > 0.0f && mv != mx) sv *= ex2(__fmul_rn(mv - mx, c2));
-            sh.m[r] = mx;
-            sh.deg[r] = !(mx > -INFINITY);
-            sh.mode[r] = 0;
-            sh.theta[r] = -INFINITY;
-            sh.Z[r] = sv;
-            // for top-p alone, a kept token weighs at least (1 - p) Z / V: the tokens below
-            // that level weigh less than (1 - p) Z together
-            float zc = -static_cast<float>(ZR);
-            if (!k_on && sv > 0.0f) {
-                const float lvl = __log2f((1.0f - pp) * sv / static_cast<float>(V));
-                zc = fmaxf(zc, lvl - 2.0f / R);
+        // ---- row statistics (every CTA, identical): warp 0 merges the CTAs' partials
+        if (warp == 0) {
+            const int r = lane >> 4, c = lane & 15;
+            float tm = -INFINITY, ts = 0.0f;
+            if (r < nrows && c < static_cast<int>(C)) {
+                const float4 e = sh.e1[ep][c];
+                tm = r == 0 ? e.x : e.z;
+                ts = r == 0 ? e.y : e.w;
             }
-            sh.zcut[r] = zc;
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
+                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
+                ms_merge(tm, ts, m2, s2, c2);
+            }
+            if (c == 0 && r < nrows) {
+                sh.m[r] = tm;
+                sh.nmc[r] = -tm * c2;
+                sh.tzb[r] = tm * (c2 * static_cast<float>(R));
+                sh.deg[r] = !(tm > -INFINITY);
+                sh.mode[r] = 0;
+                sh.theta[r] = -INFINITY;
+                sh.Z[r] = ts;
+                // for top-p alone, a kept token weighs at least (1 - p) Z / V: the tokens
+                // below that level weigh less than (1 - p) Z together
+                float zc = -static_cast<float>(ZR);
+                if (!k_on && ts > 0.0f) {
+                    const float lvl = __log2f((1.0f - pp) * ts / static_cast<float>(V));
+                    zc = fmaxf(zc, lvl - 2.0f / R);
+                }
+                sh.zcut[r] = zc;
+                sh.nbu[r] = k_on ? NB : min(NB, static_cast<int>(-zc * R) + 1);
+            }
         }
         __syncthreads();
 
         if (k_on || p_on) {
-            // ---- pass 2: counts over fine z bins for the elements that can hold the boundary
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                if (r >= nrows || sh.deg[r]) continue;
-                const float m = sh.m[r], zcut = sh.zcut[r];
-                uint32_t *h = sh.hcnt[r];
-                for_each_elem(r == 0 ? sd0 : sd1, n, [&](float x, int) {
-                    const float z = zval(x, m, c2);
-                    if (z > zcut) atomicAdd(&h[zbin(z)], 1u);
+            // ---- pass 2: histogram of the elements that can hold the boundary
+            // top-k counts the elements; top-p adds each element's weight relative to its
+            // bin's upper edge, in units of 1 / sq
+#pragma unroll 1
+            for (int r = 0; r < nrows; ++r) {
+                if (sh.deg[r]) continue;
+                const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
+                const float tzc = -sh.zcut[r] * static_cast<float>(R);
+                const float lsq = static_cast<float>(31 - __clz(P.sq));  // log2(sq)
+                uint32_t *h = sh.hloc[r];
+                for_row<EPV, MV>(rv, r, vpt, [&](float x, int, int) {
+                    const float tz = fmaf(x, tza, tzb);  // -z * R >= 0, bins at its integer part
+                    if (tz < tzc) {
+                        const float tf = truncf(tz);
+                        const uint32_t q =
+                            k_on ? 1u : __float2uint_rn(ex2(fmaf(tf - tz, 1.0f / R, lsq)));
+                        atomicAdd(&h[static_cast<int>(tf)], q);
+                    }
                 });
             }
             __syncthreads();
-            // ---- E2a: reduce-scatter, push local bins to their owner CTA
-            const int RS = (NB + C - 1) / C;
-            for (int idx = tid; idx < nrows * NB; idx += NT) {
-                const int r = idx / NB, bn = idx - r * NB;
-                const int owner = bn / RS, kq = bn - owner * RS;
-                st_peer_u32(peer_addr(smem_addr(&sh.u.in[r][static_cast<int>(rank) * RS + kq]), owner),
-                            sh.hcnt[r][bn]);
-            }
-            cluster_sync();  // B2a
-            // ---- E2b: sum the owned bins and broadcast them
-            for (int idx = tid; idx < nrows * RS; idx += NT) {
-                const int r = idx / RS, kq = idx - r * RS;
-                const int bn = static_cast<int>(rank) * RS + kq;
-                if (bn >= NB) continue;
-                uint32_t cs = 0;
-                for (uint32_t c = 0; c < C; ++c) cs += sh.u.in[r][c * RS + kq];
-                for (uint32_t c = 0; c < C; ++c)
-                    st_peer_u32(peer_addr(smem_addr(&sh.hcnt[r][bn]), c), cs);
-            }
-            cluster_sync();  // B2b
-
-            // ---- plan per row: the bin range that holds the boundary, or the exact search
-            if (warp < nrows) {
-                const int r = warp;
-                if (!sh.deg[r]) {
-                    int32_t b1 = 0, b2 = 0;
-                    bool slow = false;
-                    if (k_on) {
-                        count_search(sh.hcnt[r], static_cast<uint32_t>(kk), &sh.pick[r]);
-                        const int32_t bk = sh.pick[r];
-                        __syncwarp();
-                        slow = bk >= NB;
-                        b1 = 0;  // every bin up to the k-th value; top-p then works inside them
-                        b2 = bk;
-                    } else {
-                        weight_search(sh.hcnt[r], pp * sh.Z[r], &sh.pick[r], &sh.pick[2 + r]);
-                        b1 = sh.pick[r];
-                        b2 = sh.pick[2 + r];
-                        __syncwarp();
-                        if (b1 >= NB) slow = true;
-                        if (b2 >= NB) b2 = NB - 1;
-                    }
-                    uint32_t inr = 0;
-                    if (!slow)
-                        for (int t = lane; t < NB; t += 32)
-                            if (t >= b1 && t <= b2) inr += sh.hcnt[r][t];
-                    inr = warp_sum_u32(inr);
-                    if (inr > static_cast<uint32_t>(CAP)) slow = true;
-                    if (lane == 0) {
-                        sh.mode[r] = slow ? 2 : 1;
-                        sh.b1[r] = b1;
-                        sh.b2[r] = b2;
-                        sh.ncand[r] = inr;
-                    }
-                }
+            // ---- E2a: reduce-scatter in groups of four bins, each CTA's bins to their owner
+            const int nb0 = sh.nbu[0], nb1 = nrows > 1 ? sh.nbu[1] : 0;
+            const int rs0 = (((nb0 + C - 1) / C) + 3) & ~3, rs1 = (((nb1 + C - 1) / C) + 3) & ~3;
+            const int g0 = static_cast<int>(C) * (rs0 >> 2), g1 = static_cast<int>(C) * (rs1 >> 2);
+            for (int idx = tid; idx < g0 + g1; idx += NT) {
+                const int r = idx < g0 ? 0 : 1;
+                const int q4 = r == 0 ? idx : idx - g0;           // group of 4 bins, in bin order
+                const int rsz = r == 0 ? rs0 : rs1;
+                const int owner = (q4 * 4) / rsz, kq = q4 * 4 - owner * rsz;
+                const uint4 v = *reinterpret_cast<const uint4 *>(&sh.hloc[r][q4 * 4]);
+                st_peer_u32x4(peer_addr(smem_addr(&sh.rsin[r][static_cast<int>(rank) * rsz + kq]), owner), v);
             }
             __syncthreads();
+            if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_RS], tid);
+            xwait(XB_RS);
+            // ---- E2b: sum the owned bins and broadcast them
+            for (int idx = tid; idx < ((rs0 + rs1) >> 2); idx += NT) {
+                const int r = idx < (rs0 >> 2) ? 0 : 1;
+                const int kq = (r == 0 ? idx : idx - (rs0 >> 2)) * 4;
+                const int rsz = r == 0 ? rs0 : rs1;
+                uint4 cs = make_uint4(0u, 0u, 0u, 0u);
+                for (uint32_t c = 0; c < C; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(&sh.rsin[r][c * rsz + kq]);
+                    cs.x += v.x;
+                    cs.y += v.y;
+                    cs.z += v.z;
+                    cs.w += v.w;
+                }
+                const uint32_t a = smem_addr(&sh.hist[r][static_cast<int>(rank) * rsz + kq]);
+                for (uint32_t c = 0; c < C; ++c) st_peer_u32x4(peer_addr(a, c), cs);
+            }
+            __syncthreads();
+            if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_AG], tid);
+            xwait(XB_AG);
+
+            // ---- plan per row: the bin range that holds the boundary, or the exact search.
+            // Threads [0, NSMALL) take row 0 and the rest row 1, BPT bins each; block scans of
+            // the per-bin counts (top-k) or weight bounds (top-p) find the crossing bins.
+            {
+                constexpr int BPT = (NB + NSMALL - 1) / NSMALL;
+                const int r = tid / NSMALL, i = tid - r * NSMALL, hw = warp - r * (NW / 2);
+                const bool act = r < nrows && !sh.deg[r];
+                const int nbu = act ? sh.nbu[r] : 0;
+                const float qmin_inv =
+                    1.0f / (floorf(static_cast<float>(P.sq) * ex2(-1.0f / R)) - 1.0f);
+                unsigned long long tgt = 0;
+                if (act && !k_on)
+                    tgt = static_cast<unsigned long long>(ceil(static_cast<double>(pp) *
+                                                               static_cast<double>(sh.Z[r]) * 2147483648.0)) *
+                          P.sq;
+                // bounds of bin bn (0 past the used bins)
+                auto bounds = [&](int bn, unsigned long long &blo, unsigned long long &bhi, uint32_t &bcn) {
+                    blo = bhi = 0;
+                    bcn = 0;
+                    if (bn < nbu) {
+                        if (k_on) bcn = sh.hist[r][bn];
+                        else bin_bounds(sh.hist[r], sh.topfix, bn, qmin_inv, P.sq, blo, bhi, bcn);
+                    }
+                };
+                unsigned long long lo_s = 0, hi_s = 0;
+                uint32_t cn_s = 0;
+                for (int t = 0; t < BPT; ++t) {
+                    unsigned long long blo, bhi;
+                    uint32_t bcn;
+                    bounds(BPT * i + t, blo, bhi, bcn);
+                    lo_s += blo;
+                    hi_s += bhi;
+                    cn_s += bcn;
+                }
+                unsigned long long lo_i = lo_s, hi_i = hi_s;
+                uint32_t cn_i = cn_s;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long a1 = __shfl_up_sync(0xFFFFFFFFu, lo_i, o);
+                    const unsigned long long a2 = __shfl_up_sync(0xFFFFFFFFu, hi_i, o);
+                    const uint32_t a3 = __shfl_up_sync(0xFFFFFFFFu, cn_i, o);
+                    if (lane >= o) {
+                        lo_i += a1;
+                        hi_i += a2;
+                        cn_i += a3;
+                    }
+                }
+                if (lane == 31) {
+                    sh.psc_lo[warp] = lo_i;
+                    sh.psc_hi[warp] = hi_i;
+                    sh.psc_cn[warp] = cn_i;
+                }
+                if (i == 0 && r < nrows) {
+                    sh.pb1[r] = nbu;
+                    sh.pb2[r] = nbu;
+                    sh.pcc1[r] = 0;
+                    sh.pcc2[r] = 0;
+                }
+                __syncthreads();
+                uint32_t cn_tot = 0;
+                for (int wq = 0; wq < NW / 2; ++wq) {
+                    const int wi = r * (NW / 2) + wq;
+                    if (wq < hw) {
+                        lo_i += sh.psc_lo[wi];
+                        hi_i += sh.psc_hi[wi];
+                        cn_i += sh.psc_cn[wi];
+                    }
+                    cn_tot += sh.psc_cn[wi];
+                }
+                if (act) {
+                    if (k_on) {
+                        // the bin holding the k-th largest value; every bin up to it is gathered
+                        const uint32_t need = static_cast<uint32_t>(kk);
+                        if (cn_i - cn_s < need && cn_i >= need) {
+                            uint32_t acc = cn_i - cn_s;
+                            for (int t = 0; t < BPT; ++t) {
+                                unsigned long long blo, bhi;
+                                uint32_t bcn;
+                                bounds(BPT * i + t, blo, bhi, bcn);
+                                acc += bcn;
+                                if (acc >= need) {
+                                    sh.pb2[r] = BPT * i + t;
+                                    sh.pcc2[r] = acc;
+                                    break;
+                                }
+                            }
+                        }
+                    } else {
+                        if (hi_i - hi_s < tgt && hi_i >= tgt) {
+                            unsigned long long acc = hi_i - hi_s;
+                            uint32_t cb = cn_i - cn_s;
+                            for (int t = 0; t < BPT; ++t) {
+                                unsigned long long blo, bhi;
+                                uint32_t bcn;
+                                bounds(BPT * i + t, blo, bhi, bcn);
+                                acc += bhi;
+                                if (acc >= tgt) {
+                                    sh.pb1[r] = BPT * i + t;
+                                    sh.pcc1[r] = cb;
+                                    break;
+                                }
+                                cb += bcn;
+                            }
+                        }
+                        if (lo_i - lo_s < tgt && lo_i >= tgt) {
+                            unsigned long long acc = lo_i - lo_s;
+                            uint32_t cb = cn_i - cn_s;
+                            for (int t = 0; t < BPT; ++t) {
+                                unsigned long long blo, bhi;
+                                uint32_t bcn;
+                                bounds(BPT * i + t, blo, bhi, bcn);
+                                acc += blo;
+                                cb += bcn;
+                                if (acc >= tgt) {
+                                    sh.pb2[r] = BPT * i + t;
+                                    sh.pcc2[r] = cb;
+                                    break;
+                                }
+                            }
+                        }
+                    }
+                }
+                __syncthreads();
+                if (act && i == 0) {
+                    int32_t b1 = 0, b2 = sh.pb2[r];
+                    uint32_t ncand;
+                    bool slow;
+                    if (k_on) {
+                        ncand = sh.pcc2[r];
+                        slow = b2 >= nbu;
+                    } else {
+                        b1 = sh.pb1[r];
+                        slow = b1 >= nbu;
+                        const uint32_t c2b = b2 >= nbu ? cn_tot : sh.pcc2[r];
+                        if (b2 >= nbu) b2 = nbu - 1;
+                        ncand = c2b - sh.pcc1[r];
+                    }
+                    if (ncand > static_cast<uint32_t>(NT) || ncand == 0) slow = true;
+                    sh.mode[r] = slow ? 2 : 1;
+                    sh.b1[r] = b1;
+                    sh.b2[r] = b2;
+                    sh.lcnt[r] = 0;
+                }
+                __syncthreads();
+            }
 
             // ---- gather the boundary candidates into every CTA, with the exact weight of
             // everything above them (E3)
             const bool any_fast = sh.mode[0] == 1 || (nrows > 1 && sh.mode[1] == 1);
             if (any_fast) {
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    if (r >= nrows) break;
+                unsigned long long ma0 = 0ull, ma1 = 0ull;
+#pragma unroll 1
+                for (int r = 0; r < nrows; ++r) {
+                    if (sh.mode[r] != 1) continue;
+                    const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r], nmc = sh.nmc[r];
+                    const float tzc = -sh.zcut[r] * static_cast<float>(R);
+                    const int b1 = sh.b1[r], b2 = sh.b2[r];
                     float above = 0.0f;
-                    if (sh.mode[r] == 1) {
-                        // compact this CTA's candidates locally, then push them as one block
-                        const float m = sh.m[r];
-                        const int b1 = sh.b1[r], b2 = sh.b2[r];
-                        for_each_elem(r == 0 ? sd0 : sd1, n, [&](float x, int i) {
-                            const float z = zval(x, m, c2);
-                            const int bn = zbin(z);
-                            if (bn < b1) {
-                                above += ex2(z);
-                            } else if (bn <= b2) {
-                                const uint32_t slot = atomicAdd(&sh.lcount[r], 1u);
-                                if (slot < static_cast<uint32_t>(CAP)) {
-                                    sh.lc[r][slot].v = x;
-                                    sh.lc[r][slot].idx = static_cast<uint32_t>(lo64 + i);
-                                    sh.lw[r][slot] = fix31(ex2(z));
-                                }
-                            }
-                        });
-                    }
-                    const unsigned long long ma = block_sum_u64(fix_sum(above), sh.ru[r]);
-                    if (sh.mode[r] == 1) {
-                        const uint32_t nl = min(sh.lcount[r], static_cast<uint32_t>(CAP));
-                        __syncthreads();
-                        if (tid == 0)
-                            sh.lcount[r] = nl ? atom_peer_add_u32(peer_addr(smem_addr(&sh.cand_n[r]), 0), nl) : 0u;
-                        __syncthreads();
-                        const uint32_t base = sh.lcount[r];
-                        for (uint32_t q = tid; q < nl * C; q += NT) {
-                            const uint32_t i = q / C, c = q - i * C, slot = base + i;
-                            if (slot < static_cast<uint32_t>(CAP)) {
-                                const Cand cv = sh.lc[r][i];
-                                st_peer_u64(peer_addr(smem_addr(&sh.u.cd.c[r][slot]), c),
-                                            *reinterpret_cast<const unsigned long long *>(&cv));
-                                st_peer_u64(peer_addr(smem_addr(&sh.u.cd.w[r][slot]), c), sh.lw[r][i]);
+                    for_row<EPV, MV>(rv, r, vpt, [&](float x, int t, int e) {
+                        const float tz = fmaf(x, tza, tzb);
+                        const int bn = static_cast<int>(tz);  // saturates for -inf
+                        if (bn < b1) above += ex2(fmaf(x, c2, nmc));
+                        if (bn >= b1 && bn <= b2 && tz < tzc) {
+                            const uint32_t slot = atomicAdd(&sh.lcnt[r], 1u);
+                            if (slot < static_cast<uint32_t>(capc)) {
+                                const int gi = lo + (wbase + t * 32 + lane) * EPV + e;
+                                const unsigned long long pk =
+                                    (static_cast<unsigned long long>(__float_as_uint(x)) << 32) |
+                                    static_cast<uint32_t>(gi);
+                                const uint32_t a = smem_addr(&sh.cand[r][static_cast<int>(rank) * capc + slot]);
+                                for (uint32_t c = 0; c < C; ++c) st_peer_u64(peer_addr(a, c), pk);
                             }
                         }
-                    }
-                    if (tid == 0)
-                        for (uint32_t c = 0; c < C; ++c)
-                            st_peer_u64(peer_addr(smem_addr(&sh.ma_x[rank][r]), c), ma);
+                    });
+                    const unsigned long long ma = block_sum_u64(fix_sum(above), sh.ru[r]);
+                    if (r == 0) ma0 = ma;
+                    else ma1 = ma;
                 }
-                cluster_sync();  // B3
-                // ---- exact thresholds: sort the candidates by value (descending) and scan
+                __syncthreads();
+                if (tid < static_cast<int>(C)) {
+                    for (int r = 0; r < 2; ++r) {
+                        st_peer_u32(peer_addr(smem_addr(&sh.ccnt[rank][r]), tid), sh.lcnt[r]);
+                        st_peer_u64(peer_addr(smem_addr(&sh.cabove[rank][r]), tid), r == 0 ? ma0 : ma1);
+                    }
+                    xarrive(&sh.xbar[XB_E3], tid);
+                }
+                xwait(XB_E3);
+
+                // ---- exact thresholds.  Per row: the candidates' count, the weight above
+                // them, and whether some CTA overflowed its slots (then the exact search)
+                int ncr[2] = {0, 0};
+                unsigned long long MAr[2] = {0ull, 0ull};
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     if (r >= nrows || sh.mode[r] != 1) continue;
-                    const int nc = static_cast<int>(sh.ncand[r]);
-                    const Cand *cd = sh.u.cd.c[r];
-                    const unsigned long long *cw = sh.u.cd.w[r];
-                    unsigned long long MA = 0;
-                    for (uint32_t c = 0; c < C; ++c) MA += sh.ma_x[c][r];
-                    // bitonic sort of (value key, slot), one key per thread; strides below
-                    // 32 exchange through shuffles, wider ones through shared memory
-                    unsigned long long key =
-                        tid < nc ? (static_cast<unsigned long long>(order_key(cd[tid].v)) << 32) |
-                                       static_cast<uint32_t>(tid)
-                                 : 0ull;
-                    for (int kb = 2; kb <= NT; kb <<= 1) {
-                        for (int jb = kb >> 1; jb > 0; jb >>= 1) {
-                            unsigned long long other;
-                            if (jb >= 32) {
-                                __syncthreads();
-                                sh.skey[tid] = key;
-                                __syncthreads();
-                                other = sh.skey[tid ^ jb];
-                            } else {
-                                other = __shfl_xor_sync(0xFFFFFFFFu, key, jb);
+                    bool over = false;
+                    for (uint32_t c = 0; c < C; ++c) {
+                        const int cc = static_cast<int>(sh.ccnt[c][r]);
+                        MAr[r] += sh.cabove[c][r];
+                        if (cc > capc) over = true;
+                        ncr[r] += cc;
+                    }
+                    if (over || ncr[r] > NT || ncr[r] == 0) ncr[r] = -1;
+                }
+                // candidate i of row r, counted over the CTAs' slots in CTA order
+                auto cand_at = [&](int r, int i) -> float {
+                    int c = 0;
+                    while (c + 1 < static_cast<int>(C) && i >= static_cast<int>(sh.ccnt[c][r])) {
+                        i -= static_cast<int>(sh.ccnt[c][r]);
+                        ++c;
+                    }
+                    return __uint_as_float(static_cast<uint32_t>(sh.cand[r][c * capc + i] >> 32));
+                };
+                const bool small = ncr[0] <= NSMALL && (nrows < 2 || ncr[1] <= NSMALL);
+                if (small) {
+                    // ---- rank by counting, both rows at once (threads [0, NSMALL) take row
+                    // 0, the rest row 1): for each candidate, the weight and number of the
+                    // candidates strictly above it; then three block reductions
+                    const int r = tid / NSMALL, i = tid - r * NSMALL;
+                    const int nr = r < nrows ? ncr[r] : -1;
+                    const bool real = nr > 0 && i < nr;
+                    float v = -INFINITY;
+                    uint32_t w = 0u;
+                    if (real) {
+                        v = cand_at(r, i);
+                        w = fix31(ex2(fmaf(v, c2, sh.nmc[r])));
+                        sh.sval[tid] = v;
+                        sh.skey[tid] = w;
+                    }
+                    __syncthreads();
+                    unsigned long long sgt = 0;
+                    int cgt = 0;
+                    if (real) {
+                        const float *cv = sh.sval + r * NSMALL;
+                        const unsigned long long *cw = sh.skey + r * NSMALL;
+#pragma unroll 4
+                        for (int q = 0; q < nr; ++q) {
+                            const float vq = cv[q];
+                            if (vq > v) {
+                                sgt += cw[q];
+                                ++cgt;
                             }
-                            const bool lower = (tid & jb) == 0;
-                            const bool desc = (tid & kb) == 0;
-                            key = (lower == desc) ? max(key, other) : min(key, other);
                         }
                     }
-                    const bool real = tid < nc;
-                    const uint32_t slot = static_cast<uint32_t>(key);
-                    const float v = real ? cd[slot].v : -INFINITY;
-                    const unsigned long long w = real ? cw[slot] : 0ull;
-                    __syncthreads();
-                    sh.sval[tid] = v;
-                    // top-k: the k-th largest value (no element lies above the candidates)
-                    if (k_on && tid == kk - 1) sh.fpick[r] = v;
-                    __syncthreads();
-                    const float thk = k_on ? sh.fpick[r] : -INFINITY;
-                    const unsigned long long wk = (real && v >= thk) ? w : 0ull;
-                    // weight strictly above each value: the exclusive prefix of the weights at
-                    // the first position of its tie group (sorted descending)
-                    const unsigned long long excl = block_excl_scan_u64(wk, sh.scan);
-                    const int32_t headpos = (tid == 0 || sh.sval[tid - 1] != v) ? tid : -1;
-                    const int32_t first = block_incl_max_i32(headpos, sh.scani);
-                    sh.skey[tid] = excl;
-                    const unsigned long long zk = MA + block_sum_u64(wk, sh.ru[r]);
-                    if (tid == 0) {
-                        const double t = k_on ? static_cast<double>(pp) * static_cast<double>(zk)
-                                              : static_cast<double>(pp) * static_cast<double>(sh.Z[r]) *
-                                                    static_cast<double>(FX);
-                        sh.tgt[r] = static_cast<unsigned long long>(ceil(t));
+                    const bool kept_k = real && (!k_on || cgt < kk);
+                    const unsigned long long MA = MAr[r < 2 ? r : 0];
+                    // reduction 1 (top-k with top-p): the weight of the top-k set
+                    unsigned long long tgt = 0;
+                    if (k_on && p_on) {
+                        const unsigned long long ws = warp_sum_u64(kept_k ? static_cast<unsigned long long>(w) : 0ull);
+                        if (lane == 0) sh.red_w[warp] = ws;
+                        __syncthreads();
+                        unsigned long long zk = MA;
+                        for (int wq = 0; wq < NW / 2; ++wq) zk += sh.red_w[r * (NW / 2) + wq];
+                        tgt = static_cast<unsigned long long>(ceil(static_cast<double>(pp) * static_cast<double>(zk)));
+                        __syncthreads();
+                    } else if (p_on) {
+                        tgt = static_cast<unsigned long long>(
+                            ceil(static_cast<double>(pp) * static_cast<double>(sh.Z[r < nrows ? r : 0]) *
+                                 static_cast<double>(FX)));
+                    }
+                    const bool kept = kept_k && (!p_on || MA + sgt < tgt);
+                    // reduction 2: the smallest kept value and the kept weight
+                    float vmin = kept ? v : INFINITY;
+                    unsigned long long wk = kept ? static_cast<unsigned long long>(w) : 0ull;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
+                        wk += __shfl_xor_sync(0xFFFFFFFFu, wk, o);
+                    }
+                    if (lane == 0) {
+                        sh.red_v[warp] = vmin;
+                        sh.red_w[warp] = wk;
                     }
                     __syncthreads();
-                    const unsigned long long above = MA + sh.skey[first];
-                    const bool kept = real && v >= thk && (!p_on || above < sh.tgt[r]);
-                    int32_t lastk = kept ? tid : -1;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-                        lastk = max(lastk, __shfl_xor_sync(0xFFFFFFFFu, lastk, o));
-                    __syncthreads();
-                    if (lane == 0) sh.scani[warp] = lastk;
-                    __syncthreads();
-                    int32_t lk = -1;
-                    for (int wq = 0; wq < NW; ++wq) lk = max(lk, sh.scani[wq]);
-                    const float th = sh.sval[lk < 0 ? 0 : lk];  // the smallest kept value
-                    const unsigned long long zf =
-                        MA + block_sum_u64((real && v >= th) ? wk : 0ull, sh.ru[r]);
-                    if (tid == 0) {
+                    if (i == 0 && nr > 0) {
+                        float th = INFINITY;
+                        unsigned long long zf = MA;
+                        for (int wq = 0; wq < NW / 2; ++wq) {
+                            th = fminf(th, sh.red_v[r * (NW / 2) + wq]);
+                            zf += sh.red_w[r * (NW / 2) + wq];
+                        }
                         sh.theta[r] = th;
                         sh.Z[r] = static_cast<float>(static_cast<double>(zf) * INV_FX);
                     }
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr)
+                        if (rr < nrows && sh.mode[rr] == 1 && ncr[rr] < 0 && tid == 0) sh.mode[rr] = 2;
                     __syncthreads();
+                } else {
+                    // ---- sort the candidates by value (descending) and scan, one row at a time
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        if (r >= nrows || sh.mode[r] != 1) continue;
+                        const int nc = ncr[r];
+                        if (nc < 0) {
+                            __syncthreads();
+                            if (tid == 0) sh.mode[r] = 2;
+                            __syncthreads();
+                            continue;
+                        }
+                        const unsigned long long MA = MAr[r];
+                        int P2 = 1;
+                        while (P2 < nc) P2 <<= 1;
+                        // bitonic sort of (value key, position), one key per thread; strides
+                        // below 32 exchange through shuffles, wider ones through shared memory
+                        unsigned long long key = 0ull;
+                        if (tid < nc)
+                            key = (static_cast<unsigned long long>(order_key(cand_at(r, tid))) << 32) |
+                                  static_cast<uint32_t>(tid);
+                        for (int kb = 2; kb <= P2; kb <<= 1) {
+                            for (int jb = kb >> 1; jb > 0; jb >>= 1) {
+                                unsigned long long other;
+                                if (jb >= 32) {
+                                    __syncthreads();
+                                    sh.skey[tid] = key;
+                                    __syncthreads();
+                                    other = sh.skey[tid ^ jb];
+                                } else {
+                                    other = __shfl_xor_sync(0xFFFFFFFFu, key, jb);
+                                }
+                                const bool lower = (tid & jb) == 0;
+                                const bool desc = (tid & kb) == 0;
+                                key = (lower == desc) ? max(key, other) : min(key, other);
+                            }
+                        }
+                        const bool real = tid < nc;
+                        const float v = real ? key_to_float(static_cast<uint32_t>(key >> 32)) : -INFINITY;
+                        const unsigned long long w =
+                            real ? static_cast<unsigned long long>(fix31(ex2(fmaf(v, c2, sh.nmc[r])))) : 0ull;
+                        __syncthreads();
+                        sh.sval[tid] = v;
+                        // top-k: the k-th largest value (no element lies above the candidates)
+                        if (k_on && tid == kk - 1) sh.fpick[r] = v;
+                        __syncthreads();
+                        const float thk = k_on ? sh.fpick[r] : -INFINITY;
+                        const unsigned long long wk = (real && v >= thk) ? w : 0ull;
+                        // weight strictly above each value: the exclusive prefix of the weights
+                        // at the first position of its tie group (sorted descending)
+                        const unsigned long long excl = block_excl_scan_u64(wk, sh.scan);
+                        const int32_t headpos = (tid == 0 || sh.sval[tid - 1] != v) ? tid : -1;
+                        const int32_t first = block_incl_max_i32(headpos, sh.scani);
+                        sh.skey[tid] = excl;
+                        const unsigned long long zk = MA + block_sum_u64(wk, sh.ru[r]);
+                        if (tid == 0) {
+                            const double t = k_on ? static_cast<double>(pp) * static_cast<double>(zk)
+                                                  : static_cast<double>(pp) * static_cast<double>(sh.Z[r]) *
+                                                        static_cast<double>(FX);
+                            sh.tgt[r] = static_cast<unsigned long long>(ceil(t));
+                        }
+                        __syncthreads();
+                        const unsigned long long above = MA + sh.skey[first];
+                        const bool kept = real && v >= thk && (!p_on || above < sh.tgt[r]);
+                        int32_t lastk = kept ? tid : -1;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1)
+                            lastk = max(lastk, __shfl_xor_sync(0xFFFFFFFFu, lastk, o));
+                        __syncthreads();
+                        if (lane == 0) sh.scani[warp] = lastk;
+                        __syncthreads();
+                        int32_t lk = -1;
+                        for (int wq = 0; wq < NW; ++wq) lk = max(lk, sh.scani[wq]);
+                        const float th = sh.sval[lk < 0 ? 0 : lk];  // the smallest kept value
+                        const unsigned long long zf =
+                            MA + block_sum_u64((real && v >= th) ? wk : 0ull, sh.ru[r]);
+                        if (tid == 0) {
+                            sh.theta[r] = th;
+                            sh.Z[r] = static_cast<float>(static_cast<double>(zf) * INV_FX);
+                        }
+                        __syncthreads();
+                    }
                 }
             }
-
-            // ---- exact bisection over value keys (boundary outside the binned range, or too
-            // many elements in its bins); both rows advance in lockstep, one barrier a step
+            // ---- exact bisection over value keys (boundary outside the binned range, or
+            // too many elements in its bins); both rows advance in lockstep
             const bool any_slow = sh.mode[0] == 2 || (nrows > 1 && sh.mode[1] == 2);
             if (any_slow) {
-                int parity = 0;
+                const int lim_n = n;
                 // F(t) per row: count (wt = 0) or fixed-point weight (wt = 1) of the elements
                 // with key >= max(t, floor); returns the cluster-wide sums
                 auto eval = [&](const uint32_t t[2], const uint32_t fl[2], int wt,
                                 unsigned long long out[2]) {
-                    unsigned long long acc[2] = {0, 0};
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        if (r >= nrows || sh.mode[r] != 2) continue;
-                        const float m = sh.m[r];
+                    unsigned long long acc0 = 0, acc1 = 0;
+#pragma unroll 1
+                    for (int r = 0; r < nrows; ++r) {
+                        if (sh.mode[r] != 2) continue;
+                        const float nmc = sh.nmc[r];
                         const uint32_t lim = max(t[r], fl[r]);
                         float a = 0.0f;
                         uint32_t cnum = 0;
-                        for_each_elem(r == 0 ? sd0 : sd1, n, [&](float x, int) {
-                            if (order_key(x) >= lim) {
-                                if (wt) a += ex2(zval(x, m, c2));
+                        for_row<EPV, MV>(rv, r, vpt, [&](float x, int tt, int e) {
+                            const int li = (wbase + tt * 32 + lane) * EPV + e;
+                            if (li < lim_n && order_key(x) >= lim) {
+                                if (wt) a += ex2(fmaf(x, c2, nmc));
                                 else ++cnum;
                             }
                         });
-                        acc[r] = wt ? fix_sum(a) : static_cast<unsigned long long>(cnum);
+                        const unsigned long long ac = wt ? fix_sum(a) : static_cast<unsigned long long>(cnum);
+                        if (r == 0) acc0 = ac;
+                        else acc1 = ac;
                     }
-                    const unsigned long long s0 = block_sum_u64(acc[0], sh.ru[0]);
-                    const unsigned long long s1 = block_sum_u64(acc[1], sh.ru[1]);
-                    if (tid < 2)
-                        for (uint32_t c = 0; c < C; ++c)
-                            st_peer_u64(peer_addr(smem_addr(&sh.sx[parity][tid][rank]), c),
-                                        tid == 0 ? s0 : s1);
-                    cluster_sync();
+                    const unsigned long long s0 = block_sum_u64(acc0, sh.ru[0]);
+                    const unsigned long long s1 = block_sum_u64(acc1, sh.ru[1]);
+                    const int sp = static_cast<int>(sstep & 1u);
+                    if (tid < static_cast<int>(C)) {
+                        st_peer_u64(peer_addr(smem_addr(&sh.sx[sp][rank][0]), tid), s0);
+                        st_peer_u64(peer_addr(smem_addr(&sh.sx[sp][rank][1]), tid), s1);
+                        xarrive(&sh.xbar[XB_S + sp], tid);
+                    }
+                    xwait(XB_S + sp);
                     for (int r = 0; r < 2; ++r) {
                         unsigned long long sum = 0;
-                        for (uint32_t c = 0; c < C; ++c) sum += sh.sx[parity][r][c];
+                        for (uint32_t c = 0; c < C; ++c) sum += sh.sx[sp][c][r];
                         out[r] = sum;
                     }
-                    parity ^= 1;
+                    ++sstep;
+                    __syncthreads();  // every thread has read this step's sums
                 };
                 // largest key t with F(t) >= need, by bisection over the 32-bit key space
                 auto search = [&](const uint32_t fl[2], int wt, const unsigned long long need[2],
@@ -915,21 +1213,22 @@ __global__ void __launch_bounds__(NT, 1) k_verify_persistent(const Params P) {
 
         // membership and probability of a token in the target (0) and draft (1) rows
         const float m0 = sh.m[0], m1 = sh.m[1], th0 = sh.theta[0], th1 = sh.theta[1];
-        const float iz0 = sh.invZ[0], iz1 = sh.invZ[1];
+        const float iz0 = sh.invZ[0], iz1 = sh.invZ[1], nm0 = sh.nmc[0], nm1 = sh.nmc[1];
         const bool deg0 = sh.deg[0], deg1 = sh.deg[1];
         auto prob0 = [&](float x, int64_t idx) -> float {
             if (deg0) return idx == 0 ? 1.0f : 0.0f;
-            return x >= th0 ? ex2(zval(x, m0, c2)) * iz0 : 0.0f;
+            return x >= th0 ? ex2(fmaf(x, c2, nm0)) * iz0 : 0.0f;
         };
         auto prob1 = [&](float x, int64_t idx) -> float {
             if (deg1) return idx == 0 ? 1.0f : 0.0f;
-            return x >= th1 ? ex2(zval(x, m1, c2)) * iz1 : 0.0f;
+            return x >= th1 ? ex2(fmaf(x, c2, nm1)) * iz1 : 0.0f;
         };
 
         bool accept = false;
         float pt = 0.0f, pd = 0.0f;
         if (j < D && dvalid) {
-            const float xt = sh.x_d[ep][0], xq = sh.x_d[ep][1];
+            const float2 xdv = sh.e1d[ep];
+            const float xt = xdv.x, xq = xdv.y;
             const bool in_p = deg0 ? d == 0 : xt >= th0;
             const bool in_q = deg1 ? d == 0 : xq >= th1;
             pt = prob0(xt, d);
@@ -950,59 +1249,58 @@ __global__ void __launch_bounds__(NT, 1) k_verify_persistent(const Params P) {
 
         // ---- draw (a rejected draft's residual, or the bonus).  Weights in fixed point,
         // summed as integers: the cumulative sums at every level (lane, warp, CTA, cluster)
-        // are exact and agree with one another.  Each warp owns a contiguous run of vectors;
-        // within it a lane takes consecutive vectors, so (step, lane, element) is ascending
-        // id order.
+        // are exact and agree with one another.  A distribution's weights add up to about
+        // 2^31, so sums within a CTA fit 32 bits.  A degenerate target row is a point mass
+        // on id 0, and so is every draw from it (its residual, when not zero, too).
         UnitResult *res = P.res + u;
         const bool draw = (j == D) || !accept;
-        if (draw) {
+        if (draw && deg0) {
+            if (rank == 0 && tid == 0) res->token = 0;
+        } else if (draw) {
             int wmode = (j == D) ? 1 : 0;  // 0: max(0, p - q), 1: p
-            const int nvw = (((n + EPV - 1) / EPV) + NW - 1) / NW;  // vectors per warp
-            const int wv0 = warp * nvw, wv1 = wv0 + nvw;
-            auto weights = [&](int vi, uint32_t (&w)[EPV]) {
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) w[e] = 0u;
-                const int i0 = vi * EPV;
-                if (vi >= wv1 || i0 >= n) return;
-                float x[EPV], y[EPV];
-                if (i0 + EPV <= n) {
-                    unpack(reinterpret_cast<const uint4 *>(sd0)[vi], x);
-                    if (wmode == 0) unpack(reinterpret_cast<const uint4 *>(sd1)[vi], y);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        x[e] = i0 + e < n ? widen(sd0[i0 + e]) : -INFINITY;
-                        y[e] = (wmode == 0 && i0 + e < n) ? widen(sd1[i0 + e]) : -INFINITY;
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    if (i0 + e >= n) break;
-                    const int64_t gi = lo64 + i0 + e;
-                    float p = prob0(x[e], gi);
-                    if (p > 0.0f && wmode == 0) p = fmaxf(p - prob1(y[e], gi), 0.0f);
-                    w[e] = fix31(p);
-                }
+            // a degenerate draft row is a point mass on id 0: q = 0 elsewhere, and at id 0
+            // the residual is p - 1 <= 0
+            const float thq = deg1 ? INFINITY : th1;
+            const bool zero_here = deg1 && lo == 0 && wbase == 0 && lane == 0;
+            auto weight = [&](float xt, float xq) -> uint32_t {
+                if (!(xt >= th0)) return 0u;
+                float p = ex2(fmaf(xt, c2, nm0)) * iz0;
+                if (wmode == 0 && xq >= thq) p = fmaxf(p - ex2(fmaf(xq, c2, nm1)) * iz1, 0.0f);
+                return fix31(p);
             };
-            for (int attempt = 0; attempt < 2; ++attempt) {
-                unsigned long long acc = 0;
-                for (int vq = wv0 + lane; vq < wv1; vq += 32) {
-                    uint32_t w[EPV];
-                    weights(vq, w);
+            // the weight of one of this thread's vectors, or of its element e_only
+            auto vec_weight = [&](const uint4 &a, const uint4 &q, bool first, int e_only) -> uint32_t {
+                float x[EPV], y[EPV];
+                unpack(a, x);
+                unpack(q, y);
+                uint32_t s = 0;
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) acc += w[e];
-                }
-                acc = warp_sum_u64(acc);
-                if (lane == 0) sh.w_sum[warp] = acc;
+                for (int e = 0; e < EPV; ++e)
+                    if (e_only < 0 || e == e_only) s += weight(x[e], y[e]);
+                if (first && zero_here && wmode == 0 && e_only <= 0) s -= weight(x[0], y[0]);
+                return s;
+            };
+#pragma unroll 1
+            for (int attempt = 0; attempt < 2; ++attempt) {
+                uint32_t acc = 0;
+#pragma unroll
+                for (int t = 0; t < MV; ++t)
+                    if (t < vpt) {
+                        const uint32_t vw = vec_weight(rv[0][t], rv[1][t], t == 0, -1);
+                        sh.tsum[t][tid] = vw;
+                        acc += vw;
+                    }
+                acc = __reduce_add_sync(0xFFFFFFFFu, acc);
+                if (lane == 0) sh.wsum[warp] = acc;
                 __syncthreads();
-                if (tid == 0) {
+                if (tid < static_cast<int>(C)) {
                     unsigned long long cs = 0;
-                    for (int wq = 0; wq < NW; ++wq) cs += sh.w_sum[wq];
-                    for (uint32_t c = 0; c < C; ++c)
-                        st_peer_u64(peer_addr(smem_addr(&sh.dr_R[attempt][rank]), c), cs);
+                    for (int wq = 0; wq < NW; ++wq) cs += sh.wsum[wq];
+                    st_peer_u64(peer_addr(smem_addr(&sh.dr[attempt][rank]), tid), cs);
+                    xarrive(&sh.xbar[XB_E4 + attempt], tid);
                 }
-                cluster_sync();  // B4
-                const unsigned long long *dR = sh.dr_R[attempt];
+                xwait(XB_E4 + attempt);
+                const unsigned long long *dR = sh.dr[attempt];
                 unsigned long long Rt = 0;
                 for (uint32_t c = 0; c < C; ++c) Rt += dR[c];
                 if (Rt > 0 || wmode == 1) {
@@ -1027,59 +1325,71 @@ __global__ void __launch_bounds__(NT, 1) k_verify_persistent(const Params P) {
                         int ws = NW - 1;
                         unsigned long long wb = before;
                         for (int wq = 0; wq < NW; ++wq) {
-                            if (wb + sh.w_sum[wq] > tt) {
+                            if (wb + sh.wsum[wq] > tt) {
                                 ws = wq;
                                 break;
                             }
-                            wb += sh.w_sum[wq];
+                            wb += sh.wsum[wq];
                         }
                         if (ws == NW - 1) {
                             wb = before;
-                            for (int wq = 0; wq + 1 < NW; ++wq) wb += sh.w_sum[wq];
+                            for (int wq = 0; wq + 1 < NW; ++wq) wb += sh.wsum[wq];
                         }
                         if (warp == ws) {
-                            unsigned long long a = wb;
-                            int32_t tok = -1, lastpos = -1;
-                            for (int v0 = wv0; v0 < wv1 && tok < 0; v0 += 32) {
-                                uint32_t w[EPV];
-                                weights(v0 + lane, w);
-                                unsigned long long own = 0;
-#pragma unroll
-                                for (int e = 0; e < EPV; ++e) own += w[e];
-                                unsigned long long incl = own;
+                            // the vector (t, lane) that crosses the target, from the vector
+                            // sums; rem = tt - (weight before this warp's run)
+                            uint32_t rem = tt >= wb ? static_cast<uint32_t>(tt - wb) : 0u;
+                            int hit_t = -1, hit_l = 0, pos_t = -1, pos_l = 0;
+                            uint32_t hit_rem = 0;
+                            for (int t = 0; t < vpt && hit_t < 0; ++t) {
+                                const uint32_t own = sh.tsum[t][tid];
+                                uint32_t incl = own;
 #pragma unroll
                                 for (int o = 1; o < 32; o <<= 1) {
-                                    const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                                    if (lane >= o) incl += y;
+                                    const uint32_t yv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                                    if (lane >= o) incl += yv;
                                 }
-                                const unsigned hitm =
-                                    __ballot_sync(0xFFFFFFFFu, own > 0 && a + incl > tt);
+                                const unsigned hitm = __ballot_sync(0xFFFFFFFFu, own > 0 && incl > rem);
                                 const unsigned posm = __ballot_sync(0xFFFFFFFFu, own > 0);
-                                // per lane: its first element past the target, its last positive one
-                                int first_e = EPV - 1, last_e = 0;
-                                {
-                                    unsigned long long cum = a + incl - own;
-                                    int f = -1;
-#pragma unroll
-                                    for (int e = 0; e < EPV; ++e) {
-                                        cum += w[e];
-                                        if (w[e] > 0) last_e = e;
-                                        if (f < 0 && w[e] > 0 && cum > tt) f = e;
-                                    }
-                                    if (f >= 0) first_e = f;
-                                }
-                                if (posm) {
-                                    const int ll = 31 - __clz(posm);
-                                    lastpos = (v0 + ll) * EPV + __shfl_sync(0xFFFFFFFFu, last_e, ll);
-                                }
                                 if (hitm) {
-                                    const int hl = __ffs(hitm) - 1;
-                                    tok = (v0 + hl) * EPV + __shfl_sync(0xFFFFFFFFu, first_e, hl);
+                                    hit_t = t;
+                                    hit_l = __ffs(hitm) - 1;
+                                    // the target relative to the start of that vector
+                                    hit_rem = rem - __shfl_sync(0xFFFFFFFFu, incl - own, hit_l);
+                                } else if (posm) {
+                                    pos_t = t;
+                                    pos_l = 31 - __clz(posm);
                                 }
-                                a += __shfl_sync(0xFFFFFFFFu, incl, 31);
+                                rem -= __shfl_sync(0xFFFFFFFFu, incl, 31);
                             }
-                            if (tok < 0) tok = lastpos < 0 ? 0 : lastpos;
-                            if (lane == 0) res->token = static_cast<int32_t>(lo64 + tok);
+                            // that lane walks the vector's elements (the last positive
+                            // element of the run when rounding left no vector crossing)
+                            const int ft = hit_t >= 0 ? hit_t : pos_t;
+                            const int fl = hit_t >= 0 ? hit_l : pos_l;
+                            if (ft >= 0 && lane == fl) {
+                                int fe = EPV - 1, le = 0;
+                                uint32_t cum = 0;
+                                uint4 va = rv[0][0], vq = rv[1][0];
+#pragma unroll
+                                for (int t = 1; t < MV; ++t)
+                                    if (t == ft) {
+                                        va = rv[0][t];
+                                        vq = rv[1][t];
+                                    }
+                                for (int e = 0; e < EPV; ++e) {
+                                    const uint32_t we = vec_weight(va, vq, ft == 0, e);
+                                    if (we > 0) le = e;
+                                    cum += we;
+                                    if (hit_t >= 0 && we > 0 && cum > hit_rem) {
+                                        fe = e;
+                                        break;
+                                    }
+                                }
+                                const int tok = (wbase + ft * 32 + fl) * EPV + (hit_t >= 0 ? fe : le);
+                                res->token = lo + tok;
+                            } else if (ft < 0 && lane == 0) {
+                                res->token = lo;
+                            }
                         }
                     }
                     break;
@@ -1096,25 +1406,15 @@ __global__ void __launch_bounds__(NT, 1) k_verify_persistent(const Params P) {
             if (!draw) res->token = -1;
             if (P.status && j < D && !dvalid) atomicOr(P.status, MTPSPEC_STATUS_BAD_DRAFT_ID);
         }
-
-        // ---- this buffer is free: bring in the unit after the next one
-        const int64_t un = next_unit(u);
-        __syncthreads();
-        if (P.nbuf == 2 && tid == 0 && un >= 0) {
-            const int64_t un2 = next_unit(un);
-            if (un2 >= 0) {
-                fence_proxy_async_smem();
-                issue(un2, buf);
-            }
-        } else if (P.nbuf == 1 && tid == 0 && un >= 0) {
-            fence_proxy_async_smem();
-        }
+        __syncthreads();  // every thread is done with this unit's shared state
         u = un;
     }
-    if (tid == 0 && (sh.flags & 1) && P.status) atomicOr(P.status, MTPSPEC_STATUS_TIMEOUT);
-    if (!started) {
-        cluster_wait_acquire();  // a cluster with no unit still completes its start barrier
-    }
+    if (!started) cluster_wait_acquire();  // a cluster with no unit still completes its start
+    // no CTA leaves while a peer may still write into its shared memory or arrive on its
+    // barriers
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (tid == 0 && (sh.flags & 3) && P.status) atomicOr(P.status, MTPSPEC_STATUS_TIMEOUT);
 }
 
 // One thread per row: the first rejected position decides what the row emits.
@@ -1143,19 +1443,44 @@ __global__ void k_verify_finalize(const UnitResult *__restrict__ res, const int3
 
 // ---------------------------------------------------------------- host side
 
-static int verify_cluster_size(int64_t V) {
-    if (const char *e = getenv("MTPSPEC_VERIFY_CLUSTER")) {
-        const int c = atoi(e);
-        if (c >= 1 && c <= vs::MAXC) return c;
-    }
-    int C = 1;
-    while (C < 8 && V / (2 * C) >= 2048) C *= 2;
-    return C;
-}
+struct VerifyGeometry {
+    int C;          // CTAs per cluster
+    int64_t slice;  // logits per CTA
+    int vpt;        // 16-byte vectors per thread per row
+};
 
 static int64_t verify_slice(int64_t V, int C) {
-    int64_t s = (V + C - 1) / C;
+    const int64_t s = (V + C - 1) / C;
     return (s + 15) & ~static_cast<int64_t>(15);
+}
+static int verify_vpt(int64_t slice, size_t es) {
+    const int64_t epv = static_cast<int64_t>(16 / es);
+    const int64_t nv = (slice + epv - 1) / epv;
+    return static_cast<int>((nv + vs::NT - 1) / vs::NT);
+}
+
+// The smallest cluster whose slices fit the register blocks; clusters of 16 when there
+// are too few units to spread over clusters of 8.  0 CTAs when nothing fits.
+static VerifyGeometry verify_geometry(int64_t V, size_t es, int64_t units) {
+    VerifyGeometry gm = {0, 0, 0};
+    int Cmin = 0;
+    const int maxv = es == 4 ? vs::MAXV : vs::MAXV_BF16;
+    for (int C = 2; C <= vs::MAXC; C *= 2)
+        if (verify_vpt(verify_slice(V, C), es) <= maxv) {
+            Cmin = C;
+            break;
+        }
+    if (Cmin == 0) return gm;
+    int C = units <= 8 ? 16 : 8;
+    if (C < Cmin) C = Cmin;
+    if (const char *e = getenv("MTPSPEC_VERIFY_CLUSTER")) {
+        const int c = atoi(e);
+        if ((c == 2 || c == 4 || c == 8 || c == 16) && c >= Cmin) C = c;
+    }
+    gm.C = C;
+    gm.slice = verify_slice(V, C);
+    gm.vpt = verify_vpt(gm.slice, es);
+    return gm;
 }
 
 size_t verify_workspace_bytes(int64_t B, int32_t D) {
@@ -1164,15 +1489,15 @@ size_t verify_workspace_bytes(int64_t B, int32_t D) {
 
 constexpr size_t kSmemLimit = 227u * 1024u;
 
-static size_t verify_smem_bytes(int64_t slice, size_t es, int nbuf) {
+static size_t verify_smem_bytes(int64_t slice, size_t es) {
     const size_t head = (sizeof(vs::Shared) + 127) & ~static_cast<size_t>(127);
     const size_t row = ((static_cast<size_t>(slice) * es) + 127) & ~static_cast<size_t>(127);
-    return head + 2 * static_cast<size_t>(nbuf) * row;
+    return head + 2 * row;
 }
 
 bool verify_fits(int64_t V, size_t elem_bytes) {
-    const int C = verify_cluster_size(V);
-    return verify_smem_bytes(verify_slice(V, C), elem_bytes, 1) <= kSmemLimit;
+    const VerifyGeometry gm = verify_geometry(V, elem_bytes, 1 << 20);
+    return gm.C > 0 && verify_smem_bytes(gm.slice, elem_bytes) <= kSmemLimit;
 }
 
 // Resident clusters of the persistent kernel for one configuration (cached).
@@ -1199,7 +1524,7 @@ static int resident_clusters(int C, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, vs::k_verify_persistent<T>, &cfg) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveClusters(&n, vs::k_verify_rr<T>, &cfg) != cudaSuccess || n < 1)
         n = 1;
     for (int i = 0; i < 8; ++i)
         if (dev_of[i] == -1 || i == 7) {
@@ -1213,19 +1538,27 @@ static int resident_clusters(int C, size_t smem) {
 }
 
 template <typename T>
-static cudaError_t launch_verify_persistent(vs::Params p, int C, cudaStream_t stream) {
-    p.nbuf = verify_smem_bytes(p.slice, sizeof(T), 2) <= kSmemLimit ? 2 : 1;
-    const size_t smem = verify_smem_bytes(p.slice, sizeof(T), p.nbuf);
-    cudaError_t e = cudaFuncSetAttribute(vs::k_verify_persistent<T>,
+static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
+    const int64_t units = p.B * (p.D + 1);
+    const VerifyGeometry gm = verify_geometry(p.V, sizeof(T), units);
+    if (gm.C == 0) return cudaErrorInvalidValue;
+    const int C = gm.C;
+    p.slice = gm.slice;
+    p.vpt = gm.vpt;
+    // per-element weights of a top-p histogram in units of 2^-S of the bin's upper edge,
+    // with S so that V of them fit in 32 bits
+    int lg = 0;
+    while ((int64_t{1} << lg) < p.V) ++lg;
+    p.sq = 1u << (31 - lg);
+    const size_t smem = verify_smem_bytes(p.slice, sizeof(T));
+    cudaError_t e = cudaFuncSetAttribute(vs::k_verify_rr<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (C > 8) {
-        e = cudaFuncSetAttribute(vs::k_verify_persistent<T>,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(vs::k_verify_rr<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
-    const int64_t units = p.B * (p.D + 1);
     int64_t G = resident_clusters<T>(C, smem);
     if (G > units) G = units;
     p.G = static_cast<int32_t>(G);
@@ -1241,13 +1574,12 @@ static cudaError_t launch_verify_persistent(vs::Params p, int C, cudaStream_t st
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, vs::k_verify_persistent<T>, p);
+    e = cudaLaunchKernelEx(&cfg, vs::k_verify_rr<T>, p);
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
 
 cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream) {
-    const int C = verify_cluster_size(a.V);
     vs::Params p;
     p.T = a.target;
     p.Q = a.draft;
@@ -1259,14 +1591,15 @@ cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream) {
     p.B = a.B;
     p.D = a.D;
     p.V = a.V;
-    p.slice = verify_slice(a.V, C);
-    p.nbuf = 2;
+    p.slice = 0;
+    p.vpt = 0;
     p.G = 1;
+    p.sq = 1u;
     p.res = static_cast<vs::UnitResult *>(a.workspace);
     p.status = a.status;
     // the sampled rows, then (beside them) the greedy rows, then the per-row finalize
-    cudaError_t e = a.dtype == MTPSPEC_F32 ? launch_verify_persistent<float>(p, C, stream)
-                                           : launch_verify_persistent<uint16_t>(p, C, stream);
+    cudaError_t e = a.dtype == MTPSPEC_F32 ? launch_verify_rr<float>(p, stream)
+                                           : launch_verify_rr<uint16_t>(p, stream);
     if (e != cudaSuccess) return e;
     e = run_verify_greedy_rows(a, stream);
     if (e != cudaSuccess) return e;
