@@ -74,7 +74,6 @@ constexpr int NCH = 4;           // bulk-copy chunks per row
 constexpr int WPC = NW / NCH;    // warps whose register blocks one chunk covers
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr float FX = 2147483648.0f;  // 2^31: fixed-point scale of weights (weights <= 1)
-constexpr double INV_FX = 1.0 / 2147483648.0;
 
 // exchange barriers
 constexpr int XB_E1 = 0;   // two, by unit parity
@@ -95,20 +94,25 @@ struct __align__(16) Shared {
     unsigned long long xbar[NXB];      // exchange barriers (C arrivals each)
     float4 e1[2][MAXC];                // E1, by unit parity: (m0, s0, m1, s1) per CTA
     float2 e1d[2];                     // E1, by unit parity: the draft token's logits
-    uint32_t hloc[2][RSN];             // this CTA's histogram (zero past the used bins)
-    uint32_t rsin[2][RSN];             // reduce-scatter inbox [row][source CTA * RS + bin]
-    uint32_t hist[2][RSN];             // cluster-wide histogram
+    // histograms per row: top-k counts, or top-p weights as 16-bit fixed point relative to
+    // each bin's upper edge
+    uint32_t hloc[2][RSN];             // this CTA's histograms (zero past the used bins)
+    union {
+        struct {
+            uint32_t rsin[2][RSN];     // reduce-scatter inbox [row][source CTA * RS + bin]
+            unsigned long long hist[2][RSN];  // cluster-wide histograms
+        } h;
+        uint32_t tsum[MVMAX][NT];      // draw: each thread's vector sums (histograms are idle)
+    } x;
     uint32_t topfix[NB];               // round(2^(31 - b/R)): the fixed-point scale of bin b
     unsigned long long cand[2][CAPT];  // candidates: (value bits << 32) | token id
     uint32_t ccnt[MAXC][2];            // candidates found per CTA
-    unsigned long long cabove[MAXC][2];  // per CTA: fixed-point weight above the candidates
     unsigned long long sx[2][MAXC][2];   // exact search: per step parity, per CTA
     unsigned long long dr[2][MAXC];      // draw: per attempt, each CTA's fixed-point weight
     float rf[2][NW], rs[2][NW];
     unsigned long long ru[2][NW];
     unsigned long long scan[NW];
     unsigned long long wsum[NW];
-    uint32_t tsum[MVMAX][NT];          // draw: each thread's vector sums
     int32_t scani[NW];
     unsigned long long skey[NT];       // sort keys; candidate weights when ranking by counting
     float sval[NT];                    // sorted values; candidate values when counting
@@ -118,6 +122,7 @@ struct __align__(16) Shared {
     uint32_t psc_cn[NW];
     int32_t pb1[2], pb2[2];            // plan: crossing bins found by the scan
     uint32_t pcc1[2], pcc2[2];         // plan: count bounds before b1 and through b2
+    unsigned long long pma[2];         // plan: fixed-point weight of the bins before b1
     uint32_t lcnt[2];                  // candidate slot allocator of this CTA
     float xd[2];                       // the draft token's logits, if this CTA holds it
     // per-row state, identical in every CTA of the cluster
@@ -143,6 +148,20 @@ __device__ __forceinline__ uint32_t fix31(float w) { return __float2uint_rn(__fm
 // a per-thread sum in fixed point: a slow 64-bit conversion, used once per thread
 __device__ __forceinline__ unsigned long long fix_sum(float s) {
     return __float2ull_rn(__fmul_rn(s, FX));
+}
+
+// ceil(p * Z * 2^31), the fixed-point top-p target of a row whose weights (relative to the
+// row maximum) sum to Z, formed in fp32 (relative error 2^-24, the same in every CTA)
+__device__ __forceinline__ unsigned long long fx_target(float p, float Z) {
+    return __float2ull_ru(__fmul_rn(__fmul_rn(p, Z), FX));
+}
+// the same for a fixed-point sum z
+__device__ __forceinline__ unsigned long long fx_target_fx(float p, unsigned long long z) {
+    return __float2ull_ru(__fmul_rn(p, __ull2float_rn(z)));
+}
+// a fixed-point weight sum as a weight
+__device__ __forceinline__ float fx_to_float(unsigned long long z) {
+    return __fmul_rn(__ull2float_rn(z), 1.0f / FX);
 }
 
 // ---------------------------------------------------------------- Philox4x32-10
@@ -320,25 +339,28 @@ __device__ __forceinline__ void st_peer_v2(uint32_t a, float2 v) {
                  : "memory");
 }
 
-// Every element of a thread's register block of one row: f(x, t, e) for vector t < vpt,
-// element e.  Vector t of thread (warp, lane) is vector warp*32*vpt + t*32 + lane of the
-// CTA's slice, so a warp owns a contiguous run of the slice and, within it, (t, lane, e)
-// is ascending id order.
-template <int EPV, int MV, typename F>
-__device__ __forceinline__ void for_regs(const uint4 (&rv)[MV], int vpt, F &&f) {
-#pragma unroll
-    for (int t = 0; t < MV; ++t) {
-        if (t < vpt) {
-            float x[EPV];
-            unpack(rv[t], x);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) f(x[e], t, e);
-        }
+// Vector k (row k / MV, vector k % MV) of a thread's register blocks, chosen at run time
+// through a jump over statically indexed registers, so the blocks stay in registers.
+template <int MV>
+__device__ __forceinline__ uint4 fetch(const uint4 (&rv)[2][MV], int k) {
+    static_assert(2 * MV <= 20, "fetch covers 20 vectors");
+    switch (k) {
+#define MTPSPEC_FETCH_CASE(i) \
+    case i: return rv[((i) / MV) & 1][(i) % MV];
+        MTPSPEC_FETCH_CASE(0) MTPSPEC_FETCH_CASE(1) MTPSPEC_FETCH_CASE(2) MTPSPEC_FETCH_CASE(3)
+        MTPSPEC_FETCH_CASE(4) MTPSPEC_FETCH_CASE(5) MTPSPEC_FETCH_CASE(6) MTPSPEC_FETCH_CASE(7)
+        MTPSPEC_FETCH_CASE(8) MTPSPEC_FETCH_CASE(9) MTPSPEC_FETCH_CASE(10) MTPSPEC_FETCH_CASE(11)
+        MTPSPEC_FETCH_CASE(12) MTPSPEC_FETCH_CASE(13) MTPSPEC_FETCH_CASE(14) MTPSPEC_FETCH_CASE(15)
+        MTPSPEC_FETCH_CASE(16) MTPSPEC_FETCH_CASE(17) MTPSPEC_FETCH_CASE(18) MTPSPEC_FETCH_CASE(19)
+#undef MTPSPEC_FETCH_CASE
+        default: return rv[0][0];
     }
 }
 
-// The same over row r (0 or 1, at run time) of the two rows' blocks: the element code is
-// emitted once for both rows.
+// Every element of a thread's register block of row r: f(x, t, e) for vector t < vpt and
+// element e.  Vector t of thread (warp, lane) is vector warp*32*vpt + t*32 + lane of the
+// CTA's slice, so a warp owns a contiguous run of the slice and, within it, (t, lane, e)
+// is ascending id order.
 template <int EPV, int MV, typename F>
 __device__ __forceinline__ void for_row(const uint4 (&rv)[2][MV], int r, int vpt, F &&f) {
 #pragma unroll
@@ -353,45 +375,27 @@ __device__ __forceinline__ void for_row(const uint4 (&rv)[2][MV], int r, int vpt
     }
 }
 
-// Replace the elements from `keep` on of one 16-byte vector by -inf.
-template <int EPV>
-__device__ __forceinline__ uint4 mask_tail(uint4 v, int keep) {
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) {
-        if (e >= keep) {
-            if (EPV == 4) {
-                w[e] = 0xFF800000u;
-            } else {
-                const int q = e >> 1;
-                w[q] = (e & 1) ? ((w[q] & 0x0000FFFFu) | 0xFF800000u) : ((w[q] & 0xFFFF0000u) | 0xFF80u);
-            }
-        }
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+// -inf as a stored logit
+template <typename T> __device__ __forceinline__ T neg_inf();
+template <> __device__ __forceinline__ float neg_inf<float>() { return -INFINITY; }
+template <> __device__ __forceinline__ uint16_t neg_inf<uint16_t>() { return 0xFF80u; }
+
+// Bounds on the fixed-point weight (2^31 per unit) of bin b of a top-p histogram.  Bin b
+// holds elements with tz = -z * R in [b, b + 1); each adds q = round(2^(16 - f/R)), f = tz -
+// b, its weight relative to the bin's upper edge 2^(-b/R) in 2^-16 units.  The bin's weight
+// is q_sum * 2^(-16) * topfix[b]: mid, exact but for the truncation of the product (1
+// unit).  The margin err covers the rounding of q and of its polynomial (1 unit of q, i.e.
+// topfix >> 16, per element), the truncation, and 2^-18 of mid for the fp32 error of tz and
+// of the table.  An element adds at least qmin = 2^16 * 2^(-1/R) - 1, so a bin holds at
+// most q_sum / qmin elements (cnt).
+__device__ __forceinline__ void bin_bounds(unsigned long long qs, uint32_t tf,
+                                           unsigned long long &mid, unsigned long long &err,
+                                           uint32_t &cnt) {
+    mid = (qs >> 16) * tf + (((qs & 0xFFFFull) * tf) >> 16);
+    cnt = static_cast<uint32_t>(static_cast<float>(qs) * (1.0f / 64130.0f)) + 2u;
+    err = (mid >> 18) + 2ull + static_cast<unsigned long long>(cnt) * ((tf >> 16) + 2u);
 }
 
-// Bounds on the fixed-point weight of bin b of a top-p histogram.  Bin b holds elements
-// with z in (-(b+1)/R, -b/R]; each added q = round(2^(z + b/R) * sq), so the bin's
-// fixed-point weight (2^31 per unit) is q_sum * 2^(31 - b/R) / sq.  Bounds are kept in units
-// of 2^-31 / sq as exact integers: mid = q_sum * topfix[b], widened by the rounding of q
-// (half a unit, times topfix, per element), by the rounding of the fixed-point weights of
-// the final decision (half of 2^-31, i.e. sq / 2, per element), and by 2^-15 of mid for the
-// relative error of the fp32 weights and of the table; an element adds at least qmin, so a
-// bin holds at most q_sum / qmin elements (cnt, rounded up).
-__device__ __forceinline__ void bin_bounds(const uint32_t *q, const uint32_t *topfix, int bn,
-                                           float qmin_inv, uint32_t sq,
-                                           unsigned long long &lo, unsigned long long &hi,
-                                           uint32_t &cnt) {
-    const uint32_t qs = q[bn];
-    const uint32_t tf = topfix[bn];
-    const unsigned long long mid = static_cast<unsigned long long>(qs) * tf;
-    cnt = static_cast<uint32_t>(static_cast<float>(qs) * qmin_inv) + 2u;
-    const unsigned long long err =
-        (mid >> 15) + static_cast<unsigned long long>(cnt) * ((tf >> 1) + 1u + sq);
-    lo = mid > err ? mid - err : 0ull;
-    hi = mid + err;
-}
 struct Params {
     const void *T;
     const void *Q;
@@ -553,7 +557,8 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
             const T *src = row_ptr(b, j, r);
             const bool bulk = nvb > 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
             T *dst = sdat(r);
-            for (int i = (bulk ? nvb * EPV : 0) + tid; i < n; i += NT) dst[i] = src[i];
+            for (int i = (bulk ? nvb * EPV : 0) + tid; i < nvr * EPV; i += NT)
+                dst[i] = i < n ? src[i] : neg_inf<T>();
         }
         if (tid == 0) {
             sh.lcnt[0] = sh.lcnt[1] = 0;
@@ -576,10 +581,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                 for (int t = 0; t < MV; ++t) {
                     const int vi = wbase + t * 32 + lane;
                     uint4 v = make_uint4(NEG, NEG, NEG, NEG);
-                    if (r < nrows && t < vpt && vi < nvr) {
-                        v = sv[vi];
-                        if (vi >= nvb) v = mask_tail<EPV>(v, n - vi * EPV);
-                    }
+                    if (r < nrows && t < vpt && vi < nvr) v = sv[vi];
                     rv[r][t] = v;
                 }
             }
@@ -681,23 +683,32 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
         if (k_on || p_on) {
             // ---- pass 2: histogram of the elements that can hold the boundary
             // top-k counts the elements; top-p adds each element's weight relative to its
-            // bin's upper edge, in units of 1 / sq
+            // bin's upper edge, 2^(16 - f/R) for f = tz - bin in [0, 1), from the Taylor series
+            // of exp(-a f), a = ln 2 / R, to its f^3 term (remainder below 2^-26).  One shared
+            // atomic per element: each costs an issue slot of the atomic unit whether or not
+            // its lane is selected.
+            {
+                constexpr float A = 0.69314718055994531f / R;
+                constexpr float Q0 = 65536.0f, Q1 = -A * Q0, Q2 = A * A / 2.0f * Q0,
+                                Q3 = -A * A * A / 6.0f * Q0;
 #pragma unroll 1
-            for (int r = 0; r < nrows; ++r) {
-                if (sh.deg[r]) continue;
-                const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
-                const float tzc = -sh.zcut[r] * static_cast<float>(R);
-                const float lsq = static_cast<float>(31 - __clz(P.sq));  // log2(sq)
-                uint32_t *h = sh.hloc[r];
-                for_row<EPV, MV>(rv, r, vpt, [&](float x, int, int) {
-                    const float tz = fmaf(x, tza, tzb);  // -z * R >= 0, bins at its integer part
-                    if (tz < tzc) {
+                for (int r = 0; r < nrows; ++r) {
+                    if (sh.deg[r]) continue;
+                    const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
+                    const float tzc = -sh.zcut[r] * static_cast<float>(R);
+                    uint32_t *hh = sh.hloc[r];
+                    for_row<EPV, MV>(rv, r, vpt, [&](float x, int, int) {
+                        // -z * R >= 0 (clamped: rounding can make it a hair negative at the
+                        // maximum); bins at its integer part
+                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
                         const float tf = truncf(tz);
+                        const float f = tz - tf;
                         const uint32_t q =
-                            k_on ? 1u : __float2uint_rn(ex2(fmaf(tf - tz, 1.0f / R, lsq)));
-                        atomicAdd(&h[static_cast<int>(tf)], q);
-                    }
-                });
+                            k_on ? 1u : __float2uint_rn(fmaf(fmaf(fmaf(Q3, f, Q2), f, Q1), f, Q0));
+                        const int bn = static_cast<int>(tf);
+                        if (tz < tzc) atomicAdd(&hh[bn], q);
+                    });
+                }
             }
             __syncthreads();
             // ---- E2a: reduce-scatter in groups of four bins, each CTA's bins to their owner
@@ -706,30 +717,31 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
             const int g0 = static_cast<int>(C) * (rs0 >> 2), g1 = static_cast<int>(C) * (rs1 >> 2);
             for (int idx = tid; idx < g0 + g1; idx += NT) {
                 const int r = idx < g0 ? 0 : 1;
-                const int q4 = r == 0 ? idx : idx - g0;           // group of 4 bins, in bin order
+                const int q4 = r == 0 ? idx : idx - g0;  // group of 4 bins, in bin order
                 const int rsz = r == 0 ? rs0 : rs1;
                 const int owner = (q4 * 4) / rsz, kq = q4 * 4 - owner * rsz;
                 const uint4 v = *reinterpret_cast<const uint4 *>(&sh.hloc[r][q4 * 4]);
-                st_peer_u32x4(peer_addr(smem_addr(&sh.rsin[r][static_cast<int>(rank) * rsz + kq]), owner), v);
+                st_peer_u32x4(peer_addr(smem_addr(&sh.x.h.rsin[r][static_cast<int>(rank) * rsz + kq]), owner), v);
             }
             __syncthreads();
             if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_RS], tid);
             xwait(XB_RS);
-            // ---- E2b: sum the owned bins and broadcast them
-            for (int idx = tid; idx < ((rs0 + rs1) >> 2); idx += NT) {
-                const int r = idx < (rs0 >> 2) ? 0 : 1;
-                const int kq = (r == 0 ? idx : idx - (rs0 >> 2)) * 4;
+            // ---- E2b: sum the owned bins (in 64 bits: a bin of the whole row can exceed 32)
+            // and broadcast them, two bins per store
+            for (int idx = tid; idx < ((rs0 + rs1) >> 1); idx += NT) {
+                const int r = idx < (rs0 >> 1) ? 0 : 1;
+                const int kq = (r == 0 ? idx : idx - (rs0 >> 1)) * 2;
                 const int rsz = r == 0 ? rs0 : rs1;
-                uint4 cs = make_uint4(0u, 0u, 0u, 0u);
+                unsigned long long c0 = 0, c1 = 0;
                 for (uint32_t c = 0; c < C; ++c) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(&sh.rsin[r][c * rsz + kq]);
-                    cs.x += v.x;
-                    cs.y += v.y;
-                    cs.z += v.z;
-                    cs.w += v.w;
+                    const uint2 v = *reinterpret_cast<const uint2 *>(&sh.x.h.rsin[r][c * rsz + kq]);
+                    c0 += v.x;
+                    c1 += v.y;
                 }
-                const uint32_t a = smem_addr(&sh.hist[r][static_cast<int>(rank) * rsz + kq]);
-                for (uint32_t c = 0; c < C; ++c) st_peer_u32x4(peer_addr(a, c), cs);
+                const uint4 w = make_uint4(static_cast<uint32_t>(c0), static_cast<uint32_t>(c0 >> 32),
+                                           static_cast<uint32_t>(c1), static_cast<uint32_t>(c1 >> 32));
+                const uint32_t a = smem_addr(&sh.x.h.hist[r][static_cast<int>(rank) * rsz + kq]);
+                for (uint32_t c = 0; c < C; ++c) st_peer_u32x4(peer_addr(a, c), w);
             }
             __syncthreads();
             if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_AG], tid);
@@ -737,54 +749,49 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
 
             // ---- plan per row: the bin range that holds the boundary, or the exact search.
             // Threads [0, NSMALL) take row 0 and the rest row 1, BPT bins each; block scans of
-            // the per-bin counts (top-k) or weight bounds (top-p) find the crossing bins.
+            // the per-bin counts (top-k) or weights and their margins (top-p) find the
+            // crossing bins and the exact weight of the bins before them.
             {
                 constexpr int BPT = (NB + NSMALL - 1) / NSMALL;
                 const int r = tid / NSMALL, i = tid - r * NSMALL, hw = warp - r * (NW / 2);
                 const bool act = r < nrows && !sh.deg[r];
                 const int nbu = act ? sh.nbu[r] : 0;
-                const float qmin_inv =
-                    1.0f / (floorf(static_cast<float>(P.sq) * ex2(-1.0f / R)) - 1.0f);
-                unsigned long long tgt = 0;
-                if (act && !k_on)
-                    tgt = static_cast<unsigned long long>(ceil(static_cast<double>(pp) *
-                                                               static_cast<double>(sh.Z[r]) * 2147483648.0)) *
-                          P.sq;
-                // bounds of bin bn (0 past the used bins)
-                auto bounds = [&](int bn, unsigned long long &blo, unsigned long long &bhi, uint32_t &bcn) {
-                    blo = bhi = 0;
-                    bcn = 0;
+                const unsigned long long tgt = act && !k_on ? fx_target(pp, sh.Z[r]) : 0ull;
+                // weight, margin and element-count bound of bin bn (0 past the used bins)
+                auto bounds = [&](int bn, unsigned long long &bm, unsigned long long &be, uint32_t &bc) {
+                    bm = be = 0;
+                    bc = 0;
                     if (bn < nbu) {
-                        if (k_on) bcn = sh.hist[r][bn];
-                        else bin_bounds(sh.hist[r], sh.topfix, bn, qmin_inv, P.sq, blo, bhi, bcn);
+                        if (k_on) bc = static_cast<uint32_t>(sh.x.h.hist[r][bn]);
+                        else bin_bounds(sh.x.h.hist[r][bn], sh.topfix[bn], bm, be, bc);
                     }
                 };
-                unsigned long long lo_s = 0, hi_s = 0;
+                unsigned long long m_s = 0, e_s = 0;
                 uint32_t cn_s = 0;
                 for (int t = 0; t < BPT; ++t) {
-                    unsigned long long blo, bhi;
-                    uint32_t bcn;
-                    bounds(BPT * i + t, blo, bhi, bcn);
-                    lo_s += blo;
-                    hi_s += bhi;
-                    cn_s += bcn;
+                    unsigned long long bm, be;
+                    uint32_t bc;
+                    bounds(BPT * i + t, bm, be, bc);
+                    m_s += bm;
+                    e_s += be;
+                    cn_s += bc;
                 }
-                unsigned long long lo_i = lo_s, hi_i = hi_s;
+                unsigned long long m_i = m_s, e_i = e_s;
                 uint32_t cn_i = cn_s;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned long long a1 = __shfl_up_sync(0xFFFFFFFFu, lo_i, o);
-                    const unsigned long long a2 = __shfl_up_sync(0xFFFFFFFFu, hi_i, o);
+                    const unsigned long long a1 = __shfl_up_sync(0xFFFFFFFFu, m_i, o);
+                    const unsigned long long a2 = __shfl_up_sync(0xFFFFFFFFu, e_i, o);
                     const uint32_t a3 = __shfl_up_sync(0xFFFFFFFFu, cn_i, o);
                     if (lane >= o) {
-                        lo_i += a1;
-                        hi_i += a2;
+                        m_i += a1;
+                        e_i += a2;
                         cn_i += a3;
                     }
                 }
                 if (lane == 31) {
-                    sh.psc_lo[warp] = lo_i;
-                    sh.psc_hi[warp] = hi_i;
+                    sh.psc_lo[warp] = m_i;
+                    sh.psc_hi[warp] = e_i;
                     sh.psc_cn[warp] = cn_i;
                 }
                 if (i == 0 && r < nrows) {
@@ -792,14 +799,15 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                     sh.pb2[r] = nbu;
                     sh.pcc1[r] = 0;
                     sh.pcc2[r] = 0;
+                    sh.pma[r] = 0;
                 }
                 __syncthreads();
                 uint32_t cn_tot = 0;
                 for (int wq = 0; wq < NW / 2; ++wq) {
                     const int wi = r * (NW / 2) + wq;
                     if (wq < hw) {
-                        lo_i += sh.psc_lo[wi];
-                        hi_i += sh.psc_hi[wi];
+                        m_i += sh.psc_lo[wi];
+                        e_i += sh.psc_hi[wi];
                         cn_i += sh.psc_cn[wi];
                     }
                     cn_tot += sh.psc_cn[wi];
@@ -811,10 +819,10 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                         if (cn_i - cn_s < need && cn_i >= need) {
                             uint32_t acc = cn_i - cn_s;
                             for (int t = 0; t < BPT; ++t) {
-                                unsigned long long blo, bhi;
-                                uint32_t bcn;
-                                bounds(BPT * i + t, blo, bhi, bcn);
-                                acc += bcn;
+                                unsigned long long bm, be;
+                                uint32_t bc;
+                                bounds(BPT * i + t, bm, be, bc);
+                                acc += bc;
                                 if (acc >= need) {
                                     sh.pb2[r] = BPT * i + t;
                                     sh.pcc2[r] = acc;
@@ -823,32 +831,40 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                             }
                         }
                     } else {
-                        if (hi_i - hi_s < tgt && hi_i >= tgt) {
-                            unsigned long long acc = hi_i - hi_s;
+                        // b1: the first bin whose upper cumulative bound reaches the target
+                        // (every earlier bin is kept whole); b2: the first whose lower bound
+                        // reaches it (every later bin is dropped)
+                        if (m_i + e_i - (m_s + e_s) < tgt && m_i + e_i >= tgt) {
+                            unsigned long long am = m_i - m_s, ae = e_i - e_s;
                             uint32_t cb = cn_i - cn_s;
                             for (int t = 0; t < BPT; ++t) {
-                                unsigned long long blo, bhi;
-                                uint32_t bcn;
-                                bounds(BPT * i + t, blo, bhi, bcn);
-                                acc += bhi;
-                                if (acc >= tgt) {
+                                unsigned long long bm, be;
+                                uint32_t bc;
+                                bounds(BPT * i + t, bm, be, bc);
+                                if (am + bm + ae + be >= tgt) {
                                     sh.pb1[r] = BPT * i + t;
                                     sh.pcc1[r] = cb;
+                                    sh.pma[r] = am;
                                     break;
                                 }
-                                cb += bcn;
+                                am += bm;
+                                ae += be;
+                                cb += bc;
                             }
                         }
-                        if (lo_i - lo_s < tgt && lo_i >= tgt) {
-                            unsigned long long acc = lo_i - lo_s;
+                        const unsigned long long lo_i = m_i > e_i ? m_i - e_i : 0ull;
+                        const unsigned long long lo_x = (m_i - m_s) > (e_i - e_s) ? (m_i - m_s) - (e_i - e_s) : 0ull;
+                        if (lo_x < tgt && lo_i >= tgt) {
+                            unsigned long long am = m_i - m_s, ae = e_i - e_s;
                             uint32_t cb = cn_i - cn_s;
                             for (int t = 0; t < BPT; ++t) {
-                                unsigned long long blo, bhi;
-                                uint32_t bcn;
-                                bounds(BPT * i + t, blo, bhi, bcn);
-                                acc += blo;
-                                cb += bcn;
-                                if (acc >= tgt) {
+                                unsigned long long bm, be;
+                                uint32_t bc;
+                                bounds(BPT * i + t, bm, be, bc);
+                                am += bm;
+                                ae += be;
+                                cb += bc;
+                                if (am > ae && am - ae >= tgt) {
                                     sh.pb2[r] = BPT * i + t;
                                     sh.pcc2[r] = cb;
                                     break;
@@ -865,6 +881,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                     if (k_on) {
                         ncand = sh.pcc2[r];
                         slow = b2 >= nbu;
+                        sh.pma[r] = 0;
                     } else {
                         b1 = sh.pb1[r];
                         slow = b1 >= nbu;
@@ -881,44 +898,73 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                 __syncthreads();
             }
 
-            // ---- gather the boundary candidates into every CTA, with the exact weight of
-            // everything above them (E3)
+            // ---- gather the boundary candidates into every CTA (E3)
             const bool any_fast = sh.mode[0] == 1 || (nrows > 1 && sh.mode[1] == 1);
             if (any_fast) {
-                unsigned long long ma0 = 0ull, ma1 = 0ull;
 #pragma unroll 1
                 for (int r = 0; r < nrows; ++r) {
                     if (sh.mode[r] != 1) continue;
-                    const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r], nmc = sh.nmc[r];
+                    const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
                     const float tzc = -sh.zcut[r] * static_cast<float>(R);
-                    const int b1 = sh.b1[r], b2 = sh.b2[r];
-                    float above = 0.0f;
-                    for_row<EPV, MV>(rv, r, vpt, [&](float x, int t, int e) {
-                        const float tz = fmaf(x, tza, tzb);
-                        const int bn = static_cast<int>(tz);  // saturates for -inf
-                        if (bn < b1) above += ex2(fmaf(x, c2, nmc));
-                        if (bn >= b1 && bn <= b2 && tz < tzc) {
-                            const uint32_t slot = atomicAdd(&sh.lcnt[r], 1u);
-                            if (slot < static_cast<uint32_t>(capc)) {
-                                const int gi = lo + (wbase + t * 32 + lane) * EPV + e;
-                                const unsigned long long pk =
-                                    (static_cast<unsigned long long>(__float_as_uint(x)) << 32) |
-                                    static_cast<uint32_t>(gi);
-                                const uint32_t a = smem_addr(&sh.cand[r][static_cast<int>(rank) * capc + slot]);
-                                for (uint32_t c = 0; c < C; ++c) st_peer_u64(peer_addr(a, c), pk);
+                    // this thread's number of candidates: elements of bins [b1, b2] that the
+                    // histogram counted (bin bn = trunc(tz): bn >= b1 iff tz >= b1, bn <= b2
+                    // iff tz < b2 + 1)
+                    const float fb1 = static_cast<float>(sh.b1[r]);
+                    const float fb2 = fminf(static_cast<float>(sh.b2[r] + 1), tzc);
+                    auto is_cand = [&](float x) -> bool {
+                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
+                        return tz >= fb1 && tz < fb2;
+                    };
+                    uint32_t nct = 0;
+                    for_row<EPV, MV>(rv, r, vpt, [&](float x, int, int) { nct += is_cand(x) ? 1u : 0u; });
+                    // slots in this CTA's own block: a warp scan and one allocation per warp
+                    uint32_t incl = nct;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    const uint32_t wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+                    uint32_t base = 0;
+                    if (wtot) {
+                        if (lane == 31) base = atomicAdd(&sh.lcnt[r], wtot);
+                        base = __shfl_sync(0xFFFFFFFFu, base, 31);
+                    }
+                    if (nct) {
+                        // the threads that hold candidates write them
+                        uint32_t slot = base + incl - nct;
+                        for_row<EPV, MV>(rv, r, vpt, [&](float x, int t, int e) {
+                            if (is_cand(x)) {
+                                if (slot < static_cast<uint32_t>(capc)) {
+                                    const int gi = lo + (wbase + t * 32 + lane) * EPV + e;
+                                    sh.cand[r][static_cast<int>(rank) * capc + slot] =
+                                        (static_cast<unsigned long long>(__float_as_uint(x)) << 32) |
+                                        static_cast<uint32_t>(gi);
+                                }
+                                ++slot;
                             }
-                        }
-                    });
-                    const unsigned long long ma = block_sum_u64(fix_sum(above), sh.ru[r]);
-                    if (r == 0) ma0 = ma;
-                    else ma1 = ma;
+                        });
+                    }
+                }
+                __syncthreads();
+                // ---- push this CTA's candidates into the other CTAs' copies of its slots
+#pragma unroll 1
+                for (int r = 0; r < nrows; ++r) {
+                    if (sh.mode[r] != 1) continue;
+                    const int nl = min(static_cast<int>(sh.lcnt[r]), capc);
+                    const int np = static_cast<int>(C) - 1;
+                    for (int q = tid; q < nl * np; q += NT) {
+                        const int i = q / np, c0 = q - i * np;
+                        const uint32_t c = c0 >= static_cast<int>(rank) ? static_cast<uint32_t>(c0 + 1)
+                                                                         : static_cast<uint32_t>(c0);
+                        unsigned long long *slot = &sh.cand[r][static_cast<int>(rank) * capc + i];
+                        st_peer_u64(peer_addr(smem_addr(slot), c), *slot);
+                    }
                 }
                 __syncthreads();
                 if (tid < static_cast<int>(C)) {
-                    for (int r = 0; r < 2; ++r) {
+                    for (int r = 0; r < 2; ++r)
                         st_peer_u32(peer_addr(smem_addr(&sh.ccnt[rank][r]), tid), sh.lcnt[r]);
-                        st_peer_u64(peer_addr(smem_addr(&sh.cabove[rank][r]), tid), r == 0 ? ma0 : ma1);
-                    }
                     xarrive(&sh.xbar[XB_E3], tid);
                 }
                 xwait(XB_E3);
@@ -931,9 +977,9 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                 for (int r = 0; r < 2; ++r) {
                     if (r >= nrows || sh.mode[r] != 1) continue;
                     bool over = false;
+                    MAr[r] = sh.pma[r];
                     for (uint32_t c = 0; c < C; ++c) {
                         const int cc = static_cast<int>(sh.ccnt[c][r]);
-                        MAr[r] += sh.cabove[c][r];
                         if (cc > capc) over = true;
                         ncr[r] += cc;
                     }
@@ -952,26 +998,33 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                 if (small) {
                     // ---- rank by counting, both rows at once (threads [0, NSMALL) take row
                     // 0, the rest row 1): for each candidate, the weight and number of the
-                    // candidates strictly above it; then three block reductions
-                    const int r = tid / NSMALL, i = tid - r * NSMALL;
+                    // candidates strictly above it, each counted by S consecutive lanes over
+                    // every S-th candidate; then block reductions
+                    const int r = tid / NSMALL, tt = tid - r * NSMALL;
                     const int nr = r < nrows ? ncr[r] : -1;
+                    int p2 = 1;
+                    while (p2 < nr) p2 <<= 1;
+                    const int S = min(32, NSMALL / p2);
+                    const int i = tt / S, sub = tt - i * S;
                     const bool real = nr > 0 && i < nr;
                     float v = -INFINITY;
                     uint32_t w = 0u;
+                    float *cv = sh.sval + r * NSMALL;
+                    uint32_t *cw = reinterpret_cast<uint32_t *>(sh.skey) + r * NSMALL;
                     if (real) {
                         v = cand_at(r, i);
                         w = fix31(ex2(fmaf(v, c2, sh.nmc[r])));
-                        sh.sval[tid] = v;
-                        sh.skey[tid] = w;
+                        if (sub == 0) {
+                            cv[i] = v;
+                            cw[i] = w;
+                        }
                     }
                     __syncthreads();
                     unsigned long long sgt = 0;
                     int cgt = 0;
                     if (real) {
-                        const float *cv = sh.sval + r * NSMALL;
-                        const unsigned long long *cw = sh.skey + r * NSMALL;
 #pragma unroll 4
-                        for (int q = 0; q < nr; ++q) {
+                        for (int q = sub; q < nr; q += S) {
                             const float vq = cv[q];
                             if (vq > v) {
                                 sgt += cw[q];
@@ -979,7 +1032,12 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                             }
                         }
                     }
-                    const bool kept_k = real && (!k_on || cgt < kk);
+                    for (int o = S >> 1; o > 0; o >>= 1) {
+                        sgt += __shfl_xor_sync(0xFFFFFFFFu, sgt, o);
+                        cgt += __shfl_xor_sync(0xFFFFFFFFu, cgt, o);
+                    }
+                    const bool lead = real && sub == 0;  // one lane per candidate contributes
+                    const bool kept_k = lead && (!k_on || cgt < kk);
                     const unsigned long long MA = MAr[r < 2 ? r : 0];
                     // reduction 1 (top-k with top-p): the weight of the top-k set
                     unsigned long long tgt = 0;
@@ -989,12 +1047,10 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                         __syncthreads();
                         unsigned long long zk = MA;
                         for (int wq = 0; wq < NW / 2; ++wq) zk += sh.red_w[r * (NW / 2) + wq];
-                        tgt = static_cast<unsigned long long>(ceil(static_cast<double>(pp) * static_cast<double>(zk)));
+                        tgt = fx_target_fx(pp, zk);
                         __syncthreads();
                     } else if (p_on) {
-                        tgt = static_cast<unsigned long long>(
-                            ceil(static_cast<double>(pp) * static_cast<double>(sh.Z[r < nrows ? r : 0]) *
-                                 static_cast<double>(FX)));
+                        tgt = fx_target(pp, sh.Z[r < nrows ? r : 0]);
                     }
                     const bool kept = kept_k && (!p_on || MA + sgt < tgt);
                     // reduction 2: the smallest kept value and the kept weight
@@ -1010,7 +1066,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                         sh.red_w[warp] = wk;
                     }
                     __syncthreads();
-                    if (i == 0 && nr > 0) {
+                    if (tt == 0 && nr > 0) {
                         float th = INFINITY;
                         unsigned long long zf = MA;
                         for (int wq = 0; wq < NW / 2; ++wq) {
@@ -1018,7 +1074,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                             zf += sh.red_w[r * (NW / 2) + wq];
                         }
                         sh.theta[r] = th;
-                        sh.Z[r] = static_cast<float>(static_cast<double>(zf) * INV_FX);
+                        sh.Z[r] = fx_to_float(zf);
                     }
 #pragma unroll
                     for (int rr = 0; rr < 2; ++rr)
@@ -1080,10 +1136,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                         sh.skey[tid] = excl;
                         const unsigned long long zk = MA + block_sum_u64(wk, sh.ru[r]);
                         if (tid == 0) {
-                            const double t = k_on ? static_cast<double>(pp) * static_cast<double>(zk)
-                                                  : static_cast<double>(pp) * static_cast<double>(sh.Z[r]) *
-                                                        static_cast<double>(FX);
-                            sh.tgt[r] = static_cast<unsigned long long>(ceil(t));
+                            sh.tgt[r] = k_on ? fx_target_fx(pp, zk) : fx_target(pp, sh.Z[r]);
                         }
                         __syncthreads();
                         const unsigned long long above = MA + sh.skey[first];
@@ -1102,7 +1155,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                             MA + block_sum_u64((real && v >= th) ? wk : 0ull, sh.ru[r]);
                         if (tid == 0) {
                             sh.theta[r] = th;
-                            sh.Z[r] = static_cast<float>(static_cast<double>(zf) * INV_FX);
+                            sh.Z[r] = fx_to_float(zf);
                         }
                         __syncthreads();
                     }
@@ -1185,11 +1238,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                     if (k_on) eval(thk, zero, 1, zk);
                     unsigned long long need[2];
                     for (int r = 0; r < 2; ++r) {
-                        const double t = k_on ? static_cast<double>(pp) * static_cast<double>(zk[r])
-                                              : static_cast<double>(pp) *
-                                                    static_cast<double>(sh.Z[r < nrows ? r : 0]) *
-                                                    static_cast<double>(FX);
-                        need[r] = static_cast<unsigned long long>(ceil(t));
+                        need[r] = k_on ? fx_target_fx(pp, zk[r]) : fx_target(pp, sh.Z[r < nrows ? r : 0]);
                         if (need[r] == 0) need[r] = 1;
                     }
                     search(thk, 1, need, th);
@@ -1198,7 +1247,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                 eval(th, zero, 1, zf);
                 if (tid < nrows && sh.mode[tid] == 2) {
                     sh.theta[tid] = key_to_float(th[tid]);
-                    sh.Z[tid] = static_cast<float>(static_cast<double>(zf[tid]) * INV_FX);
+                    sh.Z[tid] = fx_to_float(zf[tid]);
                 }
                 __syncthreads();
             }
@@ -1287,7 +1336,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                 for (int t = 0; t < MV; ++t)
                     if (t < vpt) {
                         const uint32_t vw = vec_weight(rv[0][t], rv[1][t], t == 0, -1);
-                        sh.tsum[t][tid] = vw;
+                        sh.x.tsum[t][tid] = vw;
                         acc += vw;
                     }
                 acc = __reduce_add_sync(0xFFFFFFFFu, acc);
@@ -1305,9 +1354,10 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                 for (uint32_t c = 0; c < C; ++c) Rt += dR[c];
                 if (Rt > 0 || wmode == 1) {
                     // smallest id whose cumulative weight exceeds u_smp * R; a cumulative
-                    // integer sum S exceeds u_smp * R exactly when S > floor(u_smp * R)
-                    const unsigned long long tt = static_cast<unsigned long long>(
-                        floor(static_cast<double>(u_smp) * static_cast<double>(Rt)));
+                    // integer sum S exceeds u_smp * R exactly when S > floor(u_smp * R), and
+                    // u_smp = k * 2^-24 with k odd, so floor(u_smp * R) = (k * R) >> 24 exactly
+                    const unsigned long long tt =
+                        (static_cast<unsigned long long>(2u * (uw[1] >> 9) + 1u) * Rt) >> 24;
                     uint32_t cs = C - 1;
                     unsigned long long before = 0;
                     for (uint32_t c = 0; c < C; ++c) {
@@ -1342,7 +1392,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                             int hit_t = -1, hit_l = 0, pos_t = -1, pos_l = 0;
                             uint32_t hit_rem = 0;
                             for (int t = 0; t < vpt && hit_t < 0; ++t) {
-                                const uint32_t own = sh.tsum[t][tid];
+                                const uint32_t own = sh.x.tsum[t][tid];
                                 uint32_t incl = own;
 #pragma unroll
                                 for (int o = 1; o < 32; o <<= 1) {
@@ -1369,13 +1419,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                             if (ft >= 0 && lane == fl) {
                                 int fe = EPV - 1, le = 0;
                                 uint32_t cum = 0;
-                                uint4 va = rv[0][0], vq = rv[1][0];
-#pragma unroll
-                                for (int t = 1; t < MV; ++t)
-                                    if (t == ft) {
-                                        va = rv[0][t];
-                                        vq = rv[1][t];
-                                    }
+                                const uint4 va = fetch<MV>(rv, ft), vq = fetch<MV>(rv, MV + ft);
                                 for (int e = 0; e < EPV; ++e) {
                                     const uint32_t we = vec_weight(va, vq, ft == 0, e);
                                     if (we > 0) le = e;
