@@ -60,18 +60,17 @@
 namespace mtpspec {
 namespace vs {
 
-constexpr int NT = 512;          // threads per CTA
+constexpr int NT = 1024;         // threads per CTA
+constexpr int CPS = 1;           // CTAs resident per SM
 constexpr int NW = NT / 32;      // warps per CTA
+static_assert(NW <= 32 && NW % 2 == 0, "one warp merges the warps' partials; rows split the warps in halves");
 constexpr int MAXC = 16;         // largest cluster
-constexpr int MAXV = 10;         // most 16-byte vectors per thread per row in registers (fp32)
-constexpr int MAXV_BF16 = 8;     // the same for bf16 rows
 constexpr int R = 32;            // histogram bins per unit of z (log2 of the softmax weight)
 constexpr int ZR = 24;           // binned range: z in (-ZR, 0], weights in (2^-24, 1]
 constexpr int NB = R * ZR;       // bins
 constexpr int RSN = NB + 4 * MAXC;  // reduce-scatter inbox per row (C * RS, RS a multiple of 4)
 constexpr int CAPT = 1024;       // candidate slots per row in a cluster (CAPT / C per CTA)
 constexpr int NCH = 4;           // bulk-copy chunks per row
-constexpr int WPC = NW / NCH;    // warps whose register blocks one chunk covers
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr float FX = 2147483648.0f;  // 2^31: fixed-point scale of weights (weights <= 1)
 
@@ -86,7 +85,6 @@ constexpr int NXB = 9;
 
 using UnitResult = VerifyUnitRecord;
 
-constexpr int MVMAX = MAXV > MAXV_BF16 ? MAXV : MAXV_BF16;
 constexpr int NSMALL = NT / 2;   // candidates per row ranked by counting (both rows at once)
 
 struct __align__(16) Shared {
@@ -94,18 +92,25 @@ struct __align__(16) Shared {
     unsigned long long xbar[NXB];      // exchange barriers (C arrivals each)
     float4 e1[2][MAXC];                // E1, by unit parity: (m0, s0, m1, s1) per CTA
     float2 e1d[2];                     // E1, by unit parity: the draft token's logits
-    // histograms per row: top-k counts, or top-p weights as 16-bit fixed point relative to
-    // each bin's upper edge
-    uint32_t hloc[2][RSN];             // this CTA's histograms (zero past the used bins)
+    // Buffers whose lifetimes within a unit do not overlap share storage.  The histograms
+    // per row hold top-k counts, or top-p weights as 16-bit fixed point relative to each
+    // bin's upper edge.  Peers write rsin before E2b, hist before the plan and cand after
+    // the plan (once every CTA has passed E2b), so cand can take the place of hloc and rsin,
+    // and the sort scratch, used after E3, the place of hist.
     union {
         struct {
+            uint32_t hloc[2][RSN];     // this CTA's histograms (zero past the used bins)
             uint32_t rsin[2][RSN];     // reduce-scatter inbox [row][source CTA * RS + bin]
-            unsigned long long hist[2][RSN];  // cluster-wide histograms
         } h;
-        uint32_t tsum[MVMAX][NT];      // draw: each thread's vector sums (histograms are idle)
-    } x;
-    uint32_t topfix[NB];               // round(2^(31 - b/R)): the fixed-point scale of bin b
-    unsigned long long cand[2][CAPT];  // candidates: (value bits << 32) | token id
+        unsigned long long cand[2][CAPT];  // candidates: (value bits << 32) | token id
+    } a;
+    union {
+        unsigned long long hist[2][RSN];  // cluster-wide histograms
+        struct {
+            unsigned long long skey[NT];  // sort keys; candidate weights when counting
+            float sval[NT];               // sorted values; candidate values when counting
+        } s;
+    } b;
     uint32_t ccnt[MAXC][2];            // candidates found per CTA
     unsigned long long sx[2][MAXC][2];   // exact search: per step parity, per CTA
     unsigned long long dr[2][MAXC];      // draw: per attempt, each CTA's fixed-point weight
@@ -114,8 +119,6 @@ struct __align__(16) Shared {
     unsigned long long scan[NW];
     unsigned long long wsum[NW];
     int32_t scani[NW];
-    unsigned long long skey[NT];       // sort keys; candidate weights when ranking by counting
-    float sval[NT];                    // sorted values; candidate values when counting
     float red_v[NW];                   // per-warp reductions of the counting path
     unsigned long long red_w[NW];
     unsigned long long psc_lo[NW], psc_hi[NW];  // plan: per-warp totals of the bound scans
@@ -339,39 +342,18 @@ __device__ __forceinline__ void st_peer_v2(uint32_t a, float2 v) {
                  : "memory");
 }
 
-// Vector k (row k / MV, vector k % MV) of a thread's register blocks, chosen at run time
-// through a jump over statically indexed registers, so the blocks stay in registers.
-template <int MV>
-__device__ __forceinline__ uint4 fetch(const uint4 (&rv)[2][MV], int k) {
-    static_assert(2 * MV <= 20, "fetch covers 20 vectors");
-    switch (k) {
-#define MTPSPEC_FETCH_CASE(i) \
-    case i: return rv[((i) / MV) & 1][(i) % MV];
-        MTPSPEC_FETCH_CASE(0) MTPSPEC_FETCH_CASE(1) MTPSPEC_FETCH_CASE(2) MTPSPEC_FETCH_CASE(3)
-        MTPSPEC_FETCH_CASE(4) MTPSPEC_FETCH_CASE(5) MTPSPEC_FETCH_CASE(6) MTPSPEC_FETCH_CASE(7)
-        MTPSPEC_FETCH_CASE(8) MTPSPEC_FETCH_CASE(9) MTPSPEC_FETCH_CASE(10) MTPSPEC_FETCH_CASE(11)
-        MTPSPEC_FETCH_CASE(12) MTPSPEC_FETCH_CASE(13) MTPSPEC_FETCH_CASE(14) MTPSPEC_FETCH_CASE(15)
-        MTPSPEC_FETCH_CASE(16) MTPSPEC_FETCH_CASE(17) MTPSPEC_FETCH_CASE(18) MTPSPEC_FETCH_CASE(19)
-#undef MTPSPEC_FETCH_CASE
-        default: return rv[0][0];
-    }
-}
-
-// Every element of a thread's register block of row r: f(x, t, e) for vector t < vpt and
-// element e.  Vector t of thread (warp, lane) is vector warp*32*vpt + t*32 + lane of the
-// CTA's slice, so a warp owns a contiguous run of the slice and, within it, (t, lane, e)
-// is ascending id order.
-template <int EPV, int MV, typename F>
-__device__ __forceinline__ void for_row(const uint4 (&rv)[2][MV], int r, int vpt, F &&f) {
+// Every element of one row's slice in shared memory: f(x, i) for element i < nv * EPV
+// (16-byte vectors v = tid, tid + NT, ...; the ragged last vector is padded with -inf).
+template <typename T, typename F>
+__device__ __forceinline__ void for_row(const T *s, int nv, F &&f) {
+    constexpr int EPV = elems_per_16B<T>::value;
+    const uint4 *vp = reinterpret_cast<const uint4 *>(s);
+#pragma unroll 2
+    for (int v = threadIdx.x; v < nv; v += NT) {
+        float x[EPV];
+        unpack(vp[v], x);
 #pragma unroll
-    for (int t = 0; t < MV; ++t) {
-        if (t < vpt) {
-            const uint4 v = r ? rv[1][t] : rv[0][t];
-            float x[EPV];
-            unpack(v, x);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) f(x[e], t, e);
-        }
+        for (int e = 0; e < EPV; ++e) f(x[e], v * EPV + e);
     }
 }
 
@@ -383,11 +365,15 @@ template <> __device__ __forceinline__ uint16_t neg_inf<uint16_t>() { return 0xF
 // Bounds on the fixed-point weight (2^31 per unit) of bin b of a top-p histogram.  Bin b
 // holds elements with tz = -z * R in [b, b + 1); each adds q = round(2^(16 - f/R)), f = tz -
 // b, its weight relative to the bin's upper edge 2^(-b/R) in 2^-16 units.  The bin's weight
-// is q_sum * 2^(-16) * topfix[b]: mid, exact but for the truncation of the product (1
+// is q_sum * 2^(-16) * topfix(b): mid, exact but for the truncation of the product (1
 // unit).  The margin err covers the rounding of q and of its polynomial (1 unit of q, i.e.
 // topfix >> 16, per element), the truncation, and 2^-18 of mid for the fp32 error of tz and
 // of the table.  An element adds at least qmin = 2^16 * 2^(-1/R) - 1, so a bin holds at
 // most q_sum / qmin elements (cnt).
+// round(2^(31 - b/R)): the fixed-point weight of bin b's upper edge
+__device__ __forceinline__ uint32_t topfix(int b) {
+    return __float2uint_rn(ex2(31.0f - static_cast<float>(b) * (1.0f / R)));
+}
 __device__ __forceinline__ void bin_bounds(unsigned long long qs, uint32_t tf,
                                            unsigned long long &mid, unsigned long long &err,
                                            uint32_t &cnt) {
@@ -408,7 +394,6 @@ struct Params {
     int32_t D;
     int64_t V;
     int64_t slice;  // logits per CTA (a multiple of 16)
-    int32_t vpt;    // 16-byte vectors per thread per row (<= MAXV, MAXV_BF16)
     int32_t G;      // clusters in the persistent grid
     uint32_t sq;    // 2^S: scale of the per-element weights of a top-p histogram
     UnitResult *res;
@@ -431,13 +416,10 @@ struct UnitParams {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
+__global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Shared &sh = *reinterpret_cast<Shared *>(smem_raw);
     constexpr int EPV = elems_per_16B<T>::value;
-    constexpr int MV = sizeof(T) == 4 ? MAXV : MAXV_BF16;
-    // -inf in every element of a 32-bit word (one fp32, or two bf16)
-    constexpr uint32_t NEG = sizeof(T) == 4 ? 0xFF800000u : 0xFF80FF80u;
     const size_t data_off = (sizeof(Shared) + 127) & ~static_cast<size_t>(127);
     const size_t row_bytes =
         ((static_cast<size_t>(P.slice) * sizeof(T)) + 127) & ~static_cast<size_t>(127);
@@ -452,14 +434,12 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
     const int V = static_cast<int>(P.V);
     const int U = static_cast<int>(P.B) * (D + 1);
     const int G = P.G;
-    const int vpt = P.vpt;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int lo = static_cast<int>(rank) * static_cast<int>(P.slice);
     const int n = max(0, min(V - lo, static_cast<int>(P.slice)));
     const int nvb = n / EPV;               // whole vectors (bulk-copied when aligned)
     const int nvr = (n + EPV - 1) / EPV;   // vectors with the ragged one
-    const int wbase = warp * 32 * vpt;     // first vector of this warp's register block
-    const int blk = WPC * 32 * vpt;        // vectors per chunk
+    const int blk = (nvb + NCH - 1) / NCH;  // whole vectors per bulk-copy chunk
     const int capc = CAPT / static_cast<int>(C);
 
     // ---- set-up
@@ -470,8 +450,6 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         sh.flags = 0;
     }
-    for (int i = tid; i < NB; i += NT)
-        sh.topfix[i] = __float2uint_rn(ex2(31.0f - static_cast<float>(i) * (1.0f / R)));
     __syncthreads();
     cluster_arrive_release();  // peers may touch this CTA's shared memory after the wait below
     pdl_launch_dependents();   // the greedy-row kernel runs beside this grid
@@ -497,6 +475,21 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
     };
     // lane 0 of warps 0 .. 2 * NCH - 1: arm chunk barrier (warp / NCH, warp % NCH) exactly
     // once for unit (b, j), with a bulk copy of the 16-byte-aligned body of that chunk
+    // thread 0: ask L2 to fetch unit (b, j)'s slices ahead of their bulk copies
+    auto prefetch_l2 = [&](int b, int j) {
+        if (tid != 0) return;
+        for (int r = 0; r < (j < D ? 2 : 1); ++r) {
+            const T *src = row_ptr(b, j, r);
+            if (nvb == 0 || (reinterpret_cast<uintptr_t>(src) & 15u) != 0) continue;
+            for (int c = 0; c < NCH; ++c) {
+                const int v0 = min(nvb, c * blk), v1 = min(nvb, (c + 1) * blk);
+                if (v1 > v0)
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + v0 * EPV),
+                                 "r"(static_cast<uint32_t>(v1 - v0) * 16u)
+                                 : "memory");
+            }
+        }
+    };
     auto issue = [&](int b, int j, bool after_reads) {
         if (lane != 0 || warp >= 2 * NCH) return;
         const int r = warp / NCH, c = warp % NCH;
@@ -539,7 +532,10 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
     for (int k = 0; u >= 0; ++k) {
         const UnitParams cur = nxt;
         const int un = next_unit(u);
-        if (un >= 0) nxt = load_params(un);  // in flight while this unit works
+        if (un >= 0) {
+            nxt = load_params(un);  // in flight while this unit works
+            prefetch_l2(nxt.b, nxt.j);
+        }
         const uint32_t dpar = static_cast<uint32_t>(k & 1);
         const int ep = k & 1;
         const int b = cur.b, j = cur.j;
@@ -565,57 +561,68 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
             sh.fpick[0] = sh.fpick[1] = -INFINITY;
         }
         if (k_on || p_on)
-            for (int i = tid; i < 2 * RSN; i += NT) (&sh.hloc[0][0])[i] = 0;
+            for (int i = tid; i < 2 * RSN; i += NT) (&sh.a.h.hloc[0][0])[i] = 0;
         __syncthreads();
 
-        // ---- pass 1a: this warp's register blocks of both rows, as their chunk lands
-        uint4 rv[2][MV];
+        // ---- pass 1: per-thread maximum and online softmax sum of both rows, chunk by chunk
+        // as the bulk copies land (the ragged tail and misaligned rows are already in place)
         {
+            float tm[2] = {-INFINITY, -INFINITY}, ts[2] = {0.0f, 0.0f};
+            auto online = [&](int r, const uint4 &raw) {
+                float x[EPV];
+                unpack(raw, x);
+                float vm = x[0];
+#pragma unroll
+                for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, x[e]);
+                if (vm > tm[r]) {
+                    ts[r] = tm[r] > -INFINITY ? ts[r] * ex2(__fmul_rn(tm[r] - vm, c2)) : 0.0f;
+                    tm[r] = vm;
+                }
+                if (tm[r] > -INFINITY) {
+                    const float nmc = -tm[r] * c2;
+                    float a = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) a += ex2(fmaf(x[e], c2, nmc));
+                    ts[r] += a;
+                }
+            };
             bool timed_out = false;
-            const int ch = warp / WPC;
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                if (!mbar_wait_bounded(&sh.dbar[r][ch], dpar)) timed_out = true;
-                const uint4 *sv = reinterpret_cast<const uint4 *>(sdat(r));
-#pragma unroll
-                for (int t = 0; t < MV; ++t) {
-                    const int vi = wbase + t * 32 + lane;
-                    uint4 v = make_uint4(NEG, NEG, NEG, NEG);
-                    if (r < nrows && t < vpt && vi < nvr) v = sv[vi];
-                    rv[r][t] = v;
+            const uint4 *sv0 = reinterpret_cast<const uint4 *>(sdat(0));
+            const uint4 *sv1 = reinterpret_cast<const uint4 *>(sdat(1));
+            for (int c = 0; c < NCH; ++c) {
+                if (!mbar_wait_bounded(&sh.dbar[0][c], dpar)) timed_out = true;
+                if (!mbar_wait_bounded(&sh.dbar[1][c], dpar)) timed_out = true;
+                const int v1 = min(nvb, (c + 1) * blk);
+                for (int v = c * blk + tid; v < v1; v += NT) {
+                    online(0, sv0[v]);
+                    if (nrows > 1) online(1, sv1[v]);
                 }
             }
-            if (d_here && tid == 0) {
+            for (int v = nvb + tid; v < nvr; v += NT) {
+                online(0, sv0[v]);
+                if (nrows > 1) online(1, sv1[v]);
+            }
+            if (timed_out) atomicOr(&sh.flags, 1);
+            if (d_here && tid == 0) {  // every chunk has landed for this thread
                 sh.xd[0] = widen(sdat(0)[d - lo]);
                 sh.xd[1] = widen(sdat(1)[d - lo]);
             }
-            if (timed_out) atomicOr(&sh.flags, 1);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                float m = tm[r], sm = ts[r];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+                    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sm, o);
+                    ms_merge(m, sm, m2, s2, c2);
+                }
+                if (lane == 0) {
+                    sh.rf[r][warp] = m;
+                    sh.rs[r][warp] = sm;
+                }
+            }
         }
         __syncthreads();
-        // the shared-memory buffer is free: bring in the next unit
-        if (un >= 0) issue(nxt.b, nxt.j, true);
-
-        // ---- pass 1b: per-thread maximum and softmax sum, merged per warp
-#pragma unroll 1
-        for (int r = 0; r < nrows; ++r) {
-            float tm = -INFINITY;
-            for_row<EPV, MV>(rv, r, vpt, [&](float x, int, int) { tm = fmaxf(tm, x); });
-            float ts = 0.0f;
-            if (tm > -INFINITY) {
-                const float nmc = -tm * c2;
-                for_row<EPV, MV>(rv, r, vpt, [&](float x, int, int) { ts += ex2(fmaf(x, c2, nmc)); });
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
-                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
-                ms_merge(tm, ts, m2, s2, c2);
-            }
-            if (lane == 0) {
-                sh.rf[r][warp] = tm;
-                sh.rs[r][warp] = ts;
-            }
-        }
         __syncthreads();
         if (!started) {
             cluster_wait_acquire();  // every CTA of the cluster has initialised its barriers
@@ -625,17 +632,21 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
         // ---- E1: warp 0 merges the warps' partials (lanes 0-15 row 0, 16-31 row 1) and
         // sends this CTA's partials (and the draft's logits) to every CTA
         if (warp == 0) {
-            const int r = lane >> 4;
-            float tm = r < nrows ? sh.rf[r][lane & 15] : -INFINITY;
-            float ts = r < nrows ? sh.rs[r][lane & 15] : 0.0f;
+            float pm[2], ps[2];
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {
-                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
-                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
-                ms_merge(tm, ts, m2, s2, c2);
+            for (int r = 0; r < 2; ++r) {
+                float tm = r < nrows && lane < NW ? sh.rf[r][lane] : -INFINITY;
+                float ts = r < nrows && lane < NW ? sh.rs[r][lane] : 0.0f;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
+                    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
+                    ms_merge(tm, ts, m2, s2, c2);
+                }
+                pm[r] = tm;
+                ps[r] = ts;
             }
-            const float4 part = make_float4(__shfl_sync(0xFFFFFFFFu, tm, 0), __shfl_sync(0xFFFFFFFFu, ts, 0),
-                                            __shfl_sync(0xFFFFFFFFu, tm, 16), __shfl_sync(0xFFFFFFFFu, ts, 16));
+            const float4 part = make_float4(pm[0], ps[0], pm[1], ps[1]);
             if (lane < static_cast<int>(C)) {
                 st_peer_v4(peer_addr(smem_addr(&sh.e1[ep][rank]), lane), part);
                 if (d_here) st_peer_v2(peer_addr(smem_addr(&sh.e1d[ep]), lane), make_float2(sh.xd[0], sh.xd[1]));
@@ -672,7 +683,9 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                 float zc = -static_cast<float>(ZR);
                 if (!k_on && ts > 0.0f) {
                     const float lvl = __log2f((1.0f - pp) * ts / static_cast<float>(V));
-                    zc = fmaxf(zc, lvl - 2.0f / R);
+                    // Z <= V keeps the level below 0; the clamps keep at least one bin for
+                    // any input (NaN included)
+                    zc = fminf(fmaxf(zc, lvl - 2.0f / R), -1.0f / R);
                 }
                 sh.zcut[r] = zc;
                 sh.nbu[r] = k_on ? NB : min(NB, static_cast<int>(-zc * R) + 1);
@@ -696,8 +709,8 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                     if (sh.deg[r]) continue;
                     const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
                     const float tzc = -sh.zcut[r] * static_cast<float>(R);
-                    uint32_t *hh = sh.hloc[r];
-                    for_row<EPV, MV>(rv, r, vpt, [&](float x, int, int) {
+                    uint32_t *hh = sh.a.h.hloc[r];
+                    for_row(sdat(r), nvr, [&](float x, int) {
                         // -z * R >= 0 (clamped: rounding can make it a hair negative at the
                         // maximum); bins at its integer part
                         const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
@@ -712,7 +725,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
             }
             __syncthreads();
             // ---- E2a: reduce-scatter in groups of four bins, each CTA's bins to their owner
-            const int nb0 = sh.nbu[0], nb1 = nrows > 1 ? sh.nbu[1] : 0;
+            const int nb0 = max(sh.nbu[0], 0), nb1 = nrows > 1 ? max(sh.nbu[1], 0) : 0;
             const int rs0 = (((nb0 + C - 1) / C) + 3) & ~3, rs1 = (((nb1 + C - 1) / C) + 3) & ~3;
             const int g0 = static_cast<int>(C) * (rs0 >> 2), g1 = static_cast<int>(C) * (rs1 >> 2);
             for (int idx = tid; idx < g0 + g1; idx += NT) {
@@ -720,8 +733,8 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                 const int q4 = r == 0 ? idx : idx - g0;  // group of 4 bins, in bin order
                 const int rsz = r == 0 ? rs0 : rs1;
                 const int owner = (q4 * 4) / rsz, kq = q4 * 4 - owner * rsz;
-                const uint4 v = *reinterpret_cast<const uint4 *>(&sh.hloc[r][q4 * 4]);
-                st_peer_u32x4(peer_addr(smem_addr(&sh.x.h.rsin[r][static_cast<int>(rank) * rsz + kq]), owner), v);
+                const uint4 v = *reinterpret_cast<const uint4 *>(&sh.a.h.hloc[r][q4 * 4]);
+                st_peer_u32x4(peer_addr(smem_addr(&sh.a.h.rsin[r][static_cast<int>(rank) * rsz + kq]), owner), v);
             }
             __syncthreads();
             if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_RS], tid);
@@ -734,13 +747,13 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                 const int rsz = r == 0 ? rs0 : rs1;
                 unsigned long long c0 = 0, c1 = 0;
                 for (uint32_t c = 0; c < C; ++c) {
-                    const uint2 v = *reinterpret_cast<const uint2 *>(&sh.x.h.rsin[r][c * rsz + kq]);
+                    const uint2 v = *reinterpret_cast<const uint2 *>(&sh.a.h.rsin[r][c * rsz + kq]);
                     c0 += v.x;
                     c1 += v.y;
                 }
                 const uint4 w = make_uint4(static_cast<uint32_t>(c0), static_cast<uint32_t>(c0 >> 32),
                                            static_cast<uint32_t>(c1), static_cast<uint32_t>(c1 >> 32));
-                const uint32_t a = smem_addr(&sh.x.h.hist[r][static_cast<int>(rank) * rsz + kq]);
+                const uint32_t a = smem_addr(&sh.b.hist[r][static_cast<int>(rank) * rsz + kq]);
                 for (uint32_t c = 0; c < C; ++c) st_peer_u32x4(peer_addr(a, c), w);
             }
             __syncthreads();
@@ -762,8 +775,8 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                     bm = be = 0;
                     bc = 0;
                     if (bn < nbu) {
-                        if (k_on) bc = static_cast<uint32_t>(sh.x.h.hist[r][bn]);
-                        else bin_bounds(sh.x.h.hist[r][bn], sh.topfix[bn], bm, be, bc);
+                        if (k_on) bc = static_cast<uint32_t>(sh.b.hist[r][bn]);
+                        else bin_bounds(sh.b.hist[r][bn], topfix(bn), bm, be, bc);
                     }
                 };
                 unsigned long long m_s = 0, e_s = 0;
@@ -916,7 +929,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                         return tz >= fb1 && tz < fb2;
                     };
                     uint32_t nct = 0;
-                    for_row<EPV, MV>(rv, r, vpt, [&](float x, int, int) { nct += is_cand(x) ? 1u : 0u; });
+                    for_row(sdat(r), nvr, [&](float x, int) { nct += is_cand(x) ? 1u : 0u; });
                     // slots in this CTA's own block: a warp scan and one allocation per warp
                     uint32_t incl = nct;
 #pragma unroll
@@ -933,11 +946,11 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                     if (nct) {
                         // the threads that hold candidates write them
                         uint32_t slot = base + incl - nct;
-                        for_row<EPV, MV>(rv, r, vpt, [&](float x, int t, int e) {
+                        for_row(sdat(r), nvr, [&](float x, int li) {
                             if (is_cand(x)) {
                                 if (slot < static_cast<uint32_t>(capc)) {
-                                    const int gi = lo + (wbase + t * 32 + lane) * EPV + e;
-                                    sh.cand[r][static_cast<int>(rank) * capc + slot] =
+                                    const int gi = lo + li;
+                                    sh.a.cand[r][static_cast<int>(rank) * capc + slot] =
                                         (static_cast<unsigned long long>(__float_as_uint(x)) << 32) |
                                         static_cast<uint32_t>(gi);
                                 }
@@ -957,7 +970,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                         const int i = q / np, c0 = q - i * np;
                         const uint32_t c = c0 >= static_cast<int>(rank) ? static_cast<uint32_t>(c0 + 1)
                                                                          : static_cast<uint32_t>(c0);
-                        unsigned long long *slot = &sh.cand[r][static_cast<int>(rank) * capc + i];
+                        unsigned long long *slot = &sh.a.cand[r][static_cast<int>(rank) * capc + i];
                         st_peer_u64(peer_addr(smem_addr(slot), c), *slot);
                     }
                 }
@@ -992,7 +1005,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                         i -= static_cast<int>(sh.ccnt[c][r]);
                         ++c;
                     }
-                    return __uint_as_float(static_cast<uint32_t>(sh.cand[r][c * capc + i] >> 32));
+                    return __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][c * capc + i] >> 32));
                 };
                 const bool small = ncr[0] <= NSMALL && (nrows < 2 || ncr[1] <= NSMALL);
                 if (small) {
@@ -1009,8 +1022,8 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                     const bool real = nr > 0 && i < nr;
                     float v = -INFINITY;
                     uint32_t w = 0u;
-                    float *cv = sh.sval + r * NSMALL;
-                    uint32_t *cw = reinterpret_cast<uint32_t *>(sh.skey) + r * NSMALL;
+                    float *cv = sh.b.s.sval + r * NSMALL;
+                    uint32_t *cw = reinterpret_cast<uint32_t *>(sh.b.s.skey) + r * NSMALL;
                     if (real) {
                         v = cand_at(r, i);
                         w = fix31(ex2(fmaf(v, c2, sh.nmc[r])));
@@ -1106,9 +1119,9 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                                 unsigned long long other;
                                 if (jb >= 32) {
                                     __syncthreads();
-                                    sh.skey[tid] = key;
+                                    sh.b.s.skey[tid] = key;
                                     __syncthreads();
-                                    other = sh.skey[tid ^ jb];
+                                    other = sh.b.s.skey[tid ^ jb];
                                 } else {
                                     other = __shfl_xor_sync(0xFFFFFFFFu, key, jb);
                                 }
@@ -1122,7 +1135,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                         const unsigned long long w =
                             real ? static_cast<unsigned long long>(fix31(ex2(fmaf(v, c2, sh.nmc[r])))) : 0ull;
                         __syncthreads();
-                        sh.sval[tid] = v;
+                        sh.b.s.sval[tid] = v;
                         // top-k: the k-th largest value (no element lies above the candidates)
                         if (k_on && tid == kk - 1) sh.fpick[r] = v;
                         __syncthreads();
@@ -1131,15 +1144,15 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                         // weight strictly above each value: the exclusive prefix of the weights
                         // at the first position of its tie group (sorted descending)
                         const unsigned long long excl = block_excl_scan_u64(wk, sh.scan);
-                        const int32_t headpos = (tid == 0 || sh.sval[tid - 1] != v) ? tid : -1;
+                        const int32_t headpos = (tid == 0 || sh.b.s.sval[tid - 1] != v) ? tid : -1;
                         const int32_t first = block_incl_max_i32(headpos, sh.scani);
-                        sh.skey[tid] = excl;
+                        sh.b.s.skey[tid] = excl;
                         const unsigned long long zk = MA + block_sum_u64(wk, sh.ru[r]);
                         if (tid == 0) {
                             sh.tgt[r] = k_on ? fx_target_fx(pp, zk) : fx_target(pp, sh.Z[r]);
                         }
                         __syncthreads();
-                        const unsigned long long above = MA + sh.skey[first];
+                        const unsigned long long above = MA + sh.b.s.skey[first];
                         const bool kept = real && v >= thk && (!p_on || above < sh.tgt[r]);
                         int32_t lastk = kept ? tid : -1;
 #pragma unroll
@@ -1150,7 +1163,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                         __syncthreads();
                         int32_t lk = -1;
                         for (int wq = 0; wq < NW; ++wq) lk = max(lk, sh.scani[wq]);
-                        const float th = sh.sval[lk < 0 ? 0 : lk];  // the smallest kept value
+                        const float th = sh.b.s.sval[lk < 0 ? 0 : lk];  // the smallest kept value
                         const unsigned long long zf =
                             MA + block_sum_u64((real && v >= th) ? wk : 0ull, sh.ru[r]);
                         if (tid == 0) {
@@ -1178,8 +1191,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                         const uint32_t lim = max(t[r], fl[r]);
                         float a = 0.0f;
                         uint32_t cnum = 0;
-                        for_row<EPV, MV>(rv, r, vpt, [&](float x, int tt, int e) {
-                            const int li = (wbase + tt * 32 + lane) * EPV + e;
+                        for_row(sdat(r), nvr, [&](float x, int li) {
                             if (li < lim_n && order_key(x) >= lim) {
                                 if (wt) a += ex2(fmaf(x, c2, nmc));
                                 else ++cnum;
@@ -1296,13 +1308,16 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
             }
         }
 
+        // the slice buffer is free unless a draw reads it: bring in the next unit now
+        const bool draw = (j == D) || !accept;
+        if (!draw && un >= 0) issue(nxt.b, nxt.j, true);
+
         // ---- draw (a rejected draft's residual, or the bonus).  Weights in fixed point,
         // summed as integers: the cumulative sums at every level (lane, warp, CTA, cluster)
         // are exact and agree with one another.  A distribution's weights add up to about
         // 2^31, so sums within a CTA fit 32 bits.  A degenerate target row is a point mass
         // on id 0, and so is every draw from it (its residual, when not zero, too).
         UnitResult *res = P.res + u;
-        const bool draw = (j == D) || !accept;
         if (draw && deg0) {
             if (rank == 0 && tid == 0) res->token = 0;
         } else if (draw) {
@@ -1310,35 +1325,33 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
             // a degenerate draft row is a point mass on id 0: q = 0 elsewhere, and at id 0
             // the residual is p - 1 <= 0
             const float thq = deg1 ? INFINITY : th1;
-            const bool zero_here = deg1 && lo == 0 && wbase == 0 && lane == 0;
             auto weight = [&](float xt, float xq) -> uint32_t {
                 if (!(xt >= th0)) return 0u;
                 float p = ex2(fmaf(xt, c2, nm0)) * iz0;
                 if (wmode == 0 && xq >= thq) p = fmaxf(p - ex2(fmaf(xq, c2, nm1)) * iz1, 0.0f);
                 return fix31(p);
             };
-            // the weight of one of this thread's vectors, or of its element e_only
-            auto vec_weight = [&](const uint4 &a, const uint4 &q, bool first, int e_only) -> uint32_t {
+            // the weight of vector v of the slice (of its element e_only alone when >= 0)
+            const uint4 *sv0 = reinterpret_cast<const uint4 *>(sdat(0));
+            const uint4 *sv1 = reinterpret_cast<const uint4 *>(sdat(1));
+            auto vec_weight = [&](int v, int e_only) -> uint32_t {
                 float x[EPV], y[EPV];
-                unpack(a, x);
-                unpack(q, y);
+                unpack(sv0[v], x);
+                unpack(sv1[v], y);
                 uint32_t s = 0;
 #pragma unroll
                 for (int e = 0; e < EPV; ++e)
                     if (e_only < 0 || e == e_only) s += weight(x[e], y[e]);
-                if (first && zero_here && wmode == 0 && e_only <= 0) s -= weight(x[0], y[0]);
+                // id 0 of a degenerate draft row carries no residual weight
+                if (deg1 && wmode == 0 && lo == 0 && v == 0 && e_only <= 0) s -= weight(x[0], y[0]);
                 return s;
             };
+            const int nvw = (nvr + NW - 1) / NW;  // vectors per warp
+            const int w0 = warp * nvw, w1 = min(nvr, w0 + nvw);
 #pragma unroll 1
             for (int attempt = 0; attempt < 2; ++attempt) {
                 uint32_t acc = 0;
-#pragma unroll
-                for (int t = 0; t < MV; ++t)
-                    if (t < vpt) {
-                        const uint32_t vw = vec_weight(rv[0][t], rv[1][t], t == 0, -1);
-                        sh.x.tsum[t][tid] = vw;
-                        acc += vw;
-                    }
+                for (int v = w0 + lane; v < w1; v += 32) acc += vec_weight(v, -1);
                 acc = __reduce_add_sync(0xFFFFFFFFu, acc);
                 if (lane == 0) sh.wsum[warp] = acc;
                 __syncthreads();
@@ -1386,13 +1399,14 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                             for (int wq = 0; wq + 1 < NW; ++wq) wb += sh.wsum[wq];
                         }
                         if (warp == ws) {
-                            // the vector (t, lane) that crosses the target, from the vector
-                            // sums; rem = tt - (weight before this warp's run)
+                            // the vector that crosses the target, walking the warp's run in id
+                            // order; rem = tt - (weight before this warp's run)
                             uint32_t rem = tt >= wb ? static_cast<uint32_t>(tt - wb) : 0u;
-                            int hit_t = -1, hit_l = 0, pos_t = -1, pos_l = 0;
+                            int hit_v = -1, pos_v = -1;
                             uint32_t hit_rem = 0;
-                            for (int t = 0; t < vpt && hit_t < 0; ++t) {
-                                const uint32_t own = sh.x.tsum[t][tid];
+                            for (int v0 = w0; v0 < w1 && hit_v < 0; v0 += 32) {
+                                const int v = v0 + lane;
+                                const uint32_t own = v < w1 ? vec_weight(v, -1) : 0u;
                                 uint32_t incl = own;
 #pragma unroll
                                 for (int o = 1; o < 32; o <<= 1) {
@@ -1402,37 +1416,34 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
                                 const unsigned hitm = __ballot_sync(0xFFFFFFFFu, own > 0 && incl > rem);
                                 const unsigned posm = __ballot_sync(0xFFFFFFFFu, own > 0);
                                 if (hitm) {
-                                    hit_t = t;
-                                    hit_l = __ffs(hitm) - 1;
-                                    // the target relative to the start of that vector
-                                    hit_rem = rem - __shfl_sync(0xFFFFFFFFu, incl - own, hit_l);
+                                    const int hl = __ffs(hitm) - 1;
+                                    hit_v = v0 + hl;
+                                    hit_rem = rem - __shfl_sync(0xFFFFFFFFu, incl - own, hl);
                                 } else if (posm) {
-                                    pos_t = t;
-                                    pos_l = 31 - __clz(posm);
+                                    pos_v = v0 + 31 - __clz(posm);
                                 }
                                 rem -= __shfl_sync(0xFFFFFFFFu, incl, 31);
                             }
-                            // that lane walks the vector's elements (the last positive
-                            // element of the run when rounding left no vector crossing)
-                            const int ft = hit_t >= 0 ? hit_t : pos_t;
-                            const int fl = hit_t >= 0 ? hit_l : pos_l;
-                            if (ft >= 0 && lane == fl) {
-                                int fe = EPV - 1, le = 0;
-                                uint32_t cum = 0;
-                                const uint4 va = fetch<MV>(rv, ft), vq = fetch<MV>(rv, MV + ft);
-                                for (int e = 0; e < EPV; ++e) {
-                                    const uint32_t we = vec_weight(va, vq, ft == 0, e);
-                                    if (we > 0) le = e;
-                                    cum += we;
-                                    if (hit_t >= 0 && we > 0 && cum > hit_rem) {
-                                        fe = e;
-                                        break;
+                            // one lane walks that vector's elements (the last positive element
+                            // of the run when rounding left no vector crossing)
+                            if (lane == 0) {
+                                const int fv = hit_v >= 0 ? hit_v : pos_v;
+                                if (fv >= 0) {
+                                    int fe = EPV - 1, le = 0;
+                                    uint32_t cum = 0;
+                                    for (int e = 0; e < EPV; ++e) {
+                                        const uint32_t we = vec_weight(fv, e);
+                                        if (we > 0) le = e;
+                                        cum += we;
+                                        if (hit_v >= 0 && we > 0 && cum > hit_rem) {
+                                            fe = e;
+                                            break;
+                                        }
                                     }
+                                    res->token = lo + fv * EPV + (hit_v >= 0 ? fe : le);
+                                } else {
+                                    res->token = lo;
                                 }
-                                const int tok = (wbase + ft * 32 + fl) * EPV + (hit_t >= 0 ? fe : le);
-                                res->token = lo + tok;
-                            } else if (ft < 0 && lane == 0) {
-                                res->token = lo;
                             }
                         }
                     }
@@ -1451,6 +1462,7 @@ __global__ void __launch_bounds__(NT, 1) k_verify_rr(const Params P) {
             if (P.status && j < D && !dvalid) atomicOr(P.status, MTPSPEC_STATUS_BAD_DRAFT_ID);
         }
         __syncthreads();  // every thread is done with this unit's shared state
+        if (draw && un >= 0) issue(nxt.b, nxt.j, true);
         u = un;
     }
     if (!started) cluster_wait_acquire();  // a cluster with no unit still completes its start
@@ -1490,45 +1502,11 @@ __global__ void k_verify_finalize(const UnitResult *__restrict__ res, const int3
 struct VerifyGeometry {
     int C;          // CTAs per cluster
     int64_t slice;  // logits per CTA
-    int vpt;        // 16-byte vectors per thread per row
 };
 
 static int64_t verify_slice(int64_t V, int C) {
     const int64_t s = (V + C - 1) / C;
     return (s + 15) & ~static_cast<int64_t>(15);
-}
-static int verify_vpt(int64_t slice, size_t es) {
-    const int64_t epv = static_cast<int64_t>(16 / es);
-    const int64_t nv = (slice + epv - 1) / epv;
-    return static_cast<int>((nv + vs::NT - 1) / vs::NT);
-}
-
-// The smallest cluster whose slices fit the register blocks; clusters of 16 when there
-// are too few units to spread over clusters of 8.  0 CTAs when nothing fits.
-static VerifyGeometry verify_geometry(int64_t V, size_t es, int64_t units) {
-    VerifyGeometry gm = {0, 0, 0};
-    int Cmin = 0;
-    const int maxv = es == 4 ? vs::MAXV : vs::MAXV_BF16;
-    for (int C = 2; C <= vs::MAXC; C *= 2)
-        if (verify_vpt(verify_slice(V, C), es) <= maxv) {
-            Cmin = C;
-            break;
-        }
-    if (Cmin == 0) return gm;
-    int C = units <= 8 ? 16 : 8;
-    if (C < Cmin) C = Cmin;
-    if (const char *e = getenv("MTPSPEC_VERIFY_CLUSTER")) {
-        const int c = atoi(e);
-        if ((c == 2 || c == 4 || c == 8 || c == 16) && c >= Cmin) C = c;
-    }
-    gm.C = C;
-    gm.slice = verify_slice(V, C);
-    gm.vpt = verify_vpt(gm.slice, es);
-    return gm;
-}
-
-size_t verify_workspace_bytes(int64_t B, int32_t D) {
-    return static_cast<size_t>(B) * static_cast<size_t>(D + 1) * sizeof(vs::UnitResult);
 }
 
 constexpr size_t kSmemLimit = 227u * 1024u;
@@ -1539,9 +1517,42 @@ static size_t verify_smem_bytes(int64_t slice, size_t es) {
     return head + 2 * row;
 }
 
+// Shared memory per CTA when two CTAs (of different clusters) share an SM, so that one unit's
+// waits overlap the other's work.
+constexpr size_t kSmemHalf = 113u * 1024u;
+
+// Clusters of 8 CTAs (16 when there are too few units to spread over clusters of 8; 16 too
+// when CTAs share an SM and that lets them fit); larger clusters when a CTA's slices of a
+// target and a draft row would not fit its shared memory otherwise.  0 CTAs when nothing fits.
+static VerifyGeometry verify_geometry(int64_t V, size_t es, int64_t units) {
+    VerifyGeometry gm = {0, 0};
+    int Cmin = 0;
+    for (int C = 2; C <= vs::MAXC; C *= 2)
+        if (verify_smem_bytes(verify_slice(V, C), es) <= kSmemLimit) {
+            Cmin = C;
+            break;
+        }
+    if (Cmin == 0) return gm;
+    int C = units <= 8 ? 16 : 8;
+    if (C < Cmin) C = Cmin;
+    if (vs::CPS > 1 && C < vs::MAXC && verify_smem_bytes(verify_slice(V, C), es) > kSmemHalf &&
+        verify_smem_bytes(verify_slice(V, vs::MAXC), es) <= kSmemHalf)
+        C = vs::MAXC;
+    if (const char *e = getenv("MTPSPEC_VERIFY_CLUSTER")) {
+        const int c = atoi(e);
+        if ((c == 2 || c == 4 || c == 8 || c == 16) && c >= Cmin) C = c;
+    }
+    gm.C = C;
+    gm.slice = verify_slice(V, C);
+    return gm;
+}
+
+size_t verify_workspace_bytes(int64_t B, int32_t D) {
+    return static_cast<size_t>(B) * static_cast<size_t>(D + 1) * sizeof(vs::UnitResult);
+}
+
 bool verify_fits(int64_t V, size_t elem_bytes) {
-    const VerifyGeometry gm = verify_geometry(V, elem_bytes, 1 << 20);
-    return gm.C > 0 && verify_smem_bytes(gm.slice, elem_bytes) <= kSmemLimit;
+    return verify_geometry(V, elem_bytes, 1 << 20).C > 0;
 }
 
 // Resident clusters of the persistent kernel for one configuration (cached).
@@ -1588,7 +1599,6 @@ static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     if (gm.C == 0) return cudaErrorInvalidValue;
     const int C = gm.C;
     p.slice = gm.slice;
-    p.vpt = gm.vpt;
     // per-element weights of a top-p histogram in units of 2^-S of the bin's upper edge,
     // with S so that V of them fit in 32 bits
     int lg = 0;
@@ -1598,6 +1608,9 @@ static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(vs::k_verify_rr<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(vs::k_verify_rr<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (e != cudaSuccess) return e;
     if (C > 8) {
         e = cudaFuncSetAttribute(vs::k_verify_rr<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1636,7 +1649,6 @@ cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream) {
     p.D = a.D;
     p.V = a.V;
     p.slice = 0;
-    p.vpt = 0;
     p.G = 1;
     p.sq = 1u;
     p.res = static_cast<vs::UnitResult *>(a.workspace);
