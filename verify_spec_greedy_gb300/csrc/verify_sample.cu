@@ -65,9 +65,13 @@ constexpr int CPS = 1;           // CTAs resident per SM
 constexpr int NW = NT / 32;      // warps per CTA
 static_assert(NW <= 32 && NW % 2 == 0, "one warp merges the warps' partials; rows split the warps in halves");
 constexpr int MAXC = 16;         // largest cluster
-constexpr int R = 32;            // histogram bins per unit of z (log2 of the softmax weight)
-constexpr int ZR = 24;           // binned range: z in (-ZR, 0], weights in (2^-24, 1]
+// Histogram bins follow the bits of a weight w = 2^z in (0, 1] (relative to the row maximum):
+// key = bits(w) >> 18 is its exponent and 5 leading significand bits, monotone in w, so 32
+// bins per octave.  Bin b holds key = KMAX - b (bin 0: w = 1, the maximum).
+constexpr int R = 32;            // bins per octave
+constexpr int ZR = 24;           // binned range: 24 octaves, weights above about 2^-24
 constexpr int NB = R * ZR;       // bins
+constexpr int KMAX = 127 * 32;   // key of w = 1
 constexpr int RSN = NB + 4 * MAXC;  // reduce-scatter inbox per row (C * RS, RS a multiple of 4)
 constexpr int CAPT = 1024;       // candidate slots per row in a cluster (CAPT / C per CTA)
 constexpr int NCH = 4;           // bulk-copy chunks per row
@@ -87,11 +91,19 @@ using UnitResult = VerifyUnitRecord;
 
 constexpr int NSMALL = NT / 2;   // candidates per row ranked by counting (both rows at once)
 
+// Per-unit parameters of a sampled row.
+struct UnitParams {
+    int b, j;
+    float tau, pp;
+    int32_t kk, d;
+};
+
 struct __align__(16) Shared {
     unsigned long long dbar[2][NCH];   // [row][chunk] bulk-copy barriers
     unsigned long long xbar[NXB];      // exchange barriers (C arrivals each)
     float4 e1[2][MAXC];                // E1, by unit parity: (m0, s0, m1, s1) per CTA
     float2 e1d[2];                     // E1, by unit parity: the draft token's logits
+    float2 e2z[MAXC];                  // E2a: each CTA's softmax sums (rows 0, 1)
     // Buffers whose lifetimes within a unit do not overlap share storage.  The histograms
     // per row hold top-k counts, or top-p weights as 16-bit fixed point relative to each
     // bin's upper edge.  Peers write rsin before E2b, hist before the plan and cand after
@@ -129,7 +141,7 @@ struct __align__(16) Shared {
     uint32_t lcnt[2];                  // candidate slot allocator of this CTA
     float xd[2];                       // the draft token's logits, if this CTA holds it
     // per-row state, identical in every CTA of the cluster
-    float m[2], Z[2], invZ[2], theta[2], zcut[2];
+    float m[2], Z[2], invZ[2], theta[2];
     float nmc[2];     // -m * c2: z = x * c2 + nmc
     float tzb[2];     // m * c2 * R: the bin coordinate tz = -z * R = x * (-c2 * R) + tzb
     int32_t deg[2];   // a row of all -inf: a point mass on id 0
@@ -139,6 +151,10 @@ struct __align__(16) Shared {
     int32_t flags;    // bit 0: a bulk copy timed out; bit 1: an exchange timed out
     int32_t pick[2];
     float fpick[2];
+    // the unit after the next one (-1: none) and its parameters, found by one warp while
+    // the current unit works
+    int32_t su;
+    UnitParams sp;
 };
 
 __device__ __forceinline__ float ex2(float z) {
@@ -357,30 +373,65 @@ __device__ __forceinline__ void for_row(const T *s, int nv, F &&f) {
     }
 }
 
+// Maximum of a 16-byte vector of logits.
+template <typename T>
+__device__ __forceinline__ float vec_max(const uint4 &raw) {
+    constexpr int EPV = elems_per_16B<T>::value;
+    float x[EPV];
+    unpack(raw, x);
+#pragma unroll
+    for (int w = 1; w < EPV; w <<= 1)
+#pragma unroll
+        for (int e = 0; e + w < EPV; e += 2 * w) x[e] = fmaxf(x[e], x[e + w]);
+    return x[0];
+}
+// Sum of 2^(x * c2 + nm) over a 16-byte vector of logits.
+template <typename T>
+__device__ __forceinline__ float vec_sum_ex2(const uint4 &raw, float c2, float nm) {
+    constexpr int EPV = elems_per_16B<T>::value;
+    float x[EPV];
+    unpack(raw, x);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) x[e] = ex2(fmaf(x[e], c2, nm));
+#pragma unroll
+    for (int w = 1; w < EPV; w <<= 1)
+#pragma unroll
+        for (int e = 0; e + w < EPV; e += 2 * w) x[e] += x[e + w];
+    return x[0];
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum_f32(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
 // -inf as a stored logit
 template <typename T> __device__ __forceinline__ T neg_inf();
 template <> __device__ __forceinline__ float neg_inf<float>() { return -INFINITY; }
 template <> __device__ __forceinline__ uint16_t neg_inf<uint16_t>() { return 0xFF80u; }
 
-// Bounds on the fixed-point weight (2^31 per unit) of bin b of a top-p histogram.  Bin b
-// holds elements with tz = -z * R in [b, b + 1); each adds q = round(2^(16 - f/R)), f = tz -
-// b, its weight relative to the bin's upper edge 2^(-b/R) in 2^-16 units.  The bin's weight
-// is q_sum * 2^(-16) * topfix(b): mid, exact but for the truncation of the product (1
-// unit).  The margin err covers the rounding of q and of its polynomial (1 unit of q, i.e.
-// topfix >> 16, per element), the truncation, and 2^-18 of mid for the fp32 error of tz and
-// of the table.  An element adds at least qmin = 2^16 * 2^(-1/R) - 1, so a bin holds at
-// most q_sum / qmin elements (cnt).
-// round(2^(31 - b/R)): the fixed-point weight of bin b's upper edge
-__device__ __forceinline__ uint32_t topfix(int b) {
-    return __float2uint_rn(ex2(31.0f - static_cast<float>(b) * (1.0f / R)));
+// Bounds on the fixed-point weight (2^31 per unit) of bin b of a top-p histogram.  Each
+// element of the bin adds q, its significand rounded to 16 bits (2^15 <= q <= 2^16, w = q *
+// 2^(E - 142) to half a unit of q, E the biased exponent of the bin's key); the bin's weight
+// is q_sum * 2^(E - 111): mid, exact but for the truncation of a right shift.  The margin
+// err covers half a unit of q per element, the truncation, and 2^-18 of mid for the fp32
+// error of the weights.  An element adds at least 2^15, so a bin holds at most
+// q_sum / 2^15 elements (cnt).
+__device__ __forceinline__ void bin_bounds(unsigned long long qs, int b, unsigned long long &mid,
+                                           unsigned long long &err, uint32_t &cnt) {
+    const int sh = ((KMAX - b) >> 5) - 111;
+    mid = sh >= 0 ? qs << sh : qs >> (-sh);
+    cnt = static_cast<uint32_t>(qs >> 15) + 1u;
+    err = (mid >> 18) + 2ull + (sh >= 1 ? static_cast<unsigned long long>(cnt) << (sh - 1)
+                                        : static_cast<unsigned long long>(cnt));
 }
-__device__ __forceinline__ void bin_bounds(unsigned long long qs, uint32_t tf,
-                                           unsigned long long &mid, unsigned long long &err,
-                                           uint32_t &cnt) {
-    mid = (qs >> 16) * tf + (((qs & 0xFFFFull) * tf) >> 16);
-    cnt = static_cast<uint32_t>(static_cast<float>(qs) * (1.0f / 64130.0f)) + 2u;
-    err = (mid >> 18) + 2ull + static_cast<unsigned long long>(cnt) * ((tf >> 16) + 2u);
-}
+// The bits of a weight, capped at those of 1 (the maximum's weight can round a hair above it)
+__device__ __forceinline__ uint32_t wbits(float w) { return min(__float_as_uint(w), 0x3F800000u); }
 
 struct Params {
     const void *T;
@@ -407,13 +458,6 @@ __device__ __forceinline__ bool row_sampled(const Params &P, int64_t b) {
 }
 
 // ---------------------------------------------------------------- the persistent kernel
-
-// Per-unit parameters of a sampled row, loaded one unit ahead.
-struct UnitParams {
-    int b, j;
-    float tau, pp;
-    int32_t kk, d;
-};
 
 template <typename T>
 __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
@@ -463,6 +507,24 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         q.pp = P.topp ? P.topp[q.b] : 1.0f;
         q.d = q.j < D ? P.d[q.b * D + q.j] : -1;
         return q;
+    };
+    // one whole warp: the first sampled unit after unit `from` in this cluster's sequence,
+    // with its parameters, into sh.su / sh.sp.  Each lane loads a candidate's parameters, so
+    // 32 candidates cost one round of loads.
+    auto find_next = [&](int from) {
+        int found = -1;
+        for (int base = from + G; from >= 0 && base < U && found < 0; base += 32 * G) {
+            const int cand = base + lane * G;
+            UnitParams q = {0, 0, 0.0f, 1.0f, 0, -1};
+            if (cand < U) q = load_params(cand);
+            const unsigned msk = __ballot_sync(0xFFFFFFFFu, cand < U && q.tau > 0.0f && q.pp > 0.0f);
+            if (msk) {
+                const int l = __ffs(msk) - 1;
+                found = __shfl_sync(0xFFFFFFFFu, cand, l);
+                if (lane == l) sh.sp = q;
+            }
+        }
+        if (lane == 0) sh.su = found;
     };
     auto row_ptr = [&](int b, int j, int r) -> const T * {
         return r == 0 ? static_cast<const T *>(P.T) + (static_cast<int64_t>(b) * (D + 1) + j) * V + lo
@@ -522,20 +584,20 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
 
     int u = -1;
     if (g < U) u = row_sampled(P, g / (D + 1)) ? g : next_unit(g);
-    UnitParams nxt = {0, 0, 1.0f, 1.0f, 0, -1};
+    UnitParams cnx = {0, 0, 1.0f, 1.0f, 0, -1};  // this unit's parameters
+    UnitParams nxt = {0, 0, 1.0f, 1.0f, 0, -1};  // the next unit's
+    int un = -1;
     if (u >= 0) {
-        nxt = load_params(u);
-        issue(nxt.b, nxt.j, false);
+        cnx = load_params(u);
+        issue(cnx.b, cnx.j, false);
+        un = next_unit(u);
+        if (un >= 0) nxt = load_params(un);
     }
     bool started = false;
 
     for (int k = 0; u >= 0; ++k) {
-        const UnitParams cur = nxt;
-        const int un = next_unit(u);
-        if (un >= 0) {
-            nxt = load_params(un);  // in flight while this unit works
-            prefetch_l2(nxt.b, nxt.j);
-        }
+        const UnitParams cur = cnx;
+        if (un >= 0) prefetch_l2(nxt.b, nxt.j);
         const uint32_t dpar = static_cast<uint32_t>(k & 1);
         const int ep = k & 1;
         const int b = cur.b, j = cur.j;
@@ -564,98 +626,85 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             for (int i = tid; i < 2 * RSN; i += NT) (&sh.a.h.hloc[0][0])[i] = 0;
         __syncthreads();
 
-        // ---- pass 1: per-thread maximum and online softmax sum of both rows, chunk by chunk
-        // as the bulk copies land (the ragged tail and misaligned rows are already in place)
+        // ---- pass 1: the maxima of both rows' slices, chunk by chunk as the bulk copies land
+        // (the ragged tail and misaligned rows are already in place).  An unfiltered unit also
+        // sums its softmax weights relative to this CTA's maxima here; a filtered one does so
+        // in pass 2, relative to the rows' maxima, together with its histograms.
+        const bool filt = k_on || p_on;
+        const uint4 *sv0 = reinterpret_cast<const uint4 *>(sdat(0));
+        const uint4 *sv1 = reinterpret_cast<const uint4 *>(sdat(1));
+        float cm0, cm1, cs0 = 0.0f, cs1 = 0.0f;
         {
-            float tm[2] = {-INFINITY, -INFINITY}, ts[2] = {0.0f, 0.0f};
-            auto online = [&](int r, const uint4 &raw) {
-                float x[EPV];
-                unpack(raw, x);
-                float vm = x[0];
-#pragma unroll
-                for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, x[e]);
-                if (vm > tm[r]) {
-                    ts[r] = tm[r] > -INFINITY ? ts[r] * ex2(__fmul_rn(tm[r] - vm, c2)) : 0.0f;
-                    tm[r] = vm;
-                }
-                if (tm[r] > -INFINITY) {
-                    const float nmc = -tm[r] * c2;
-                    float a = 0.0f;
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) a += ex2(fmaf(x[e], c2, nmc));
-                    ts[r] += a;
-                }
-            };
+            float mx0 = -INFINITY, mx1 = -INFINITY;
             bool timed_out = false;
-            const uint4 *sv0 = reinterpret_cast<const uint4 *>(sdat(0));
-            const uint4 *sv1 = reinterpret_cast<const uint4 *>(sdat(1));
             for (int c = 0; c < NCH; ++c) {
                 if (!mbar_wait_bounded(&sh.dbar[0][c], dpar)) timed_out = true;
                 if (!mbar_wait_bounded(&sh.dbar[1][c], dpar)) timed_out = true;
                 const int v1 = min(nvb, (c + 1) * blk);
+#pragma unroll 2
                 for (int v = c * blk + tid; v < v1; v += NT) {
-                    online(0, sv0[v]);
-                    if (nrows > 1) online(1, sv1[v]);
+                    mx0 = fmaxf(mx0, vec_max<T>(sv0[v]));
+                    if (nrows > 1) mx1 = fmaxf(mx1, vec_max<T>(sv1[v]));
                 }
             }
             for (int v = nvb + tid; v < nvr; v += NT) {
-                online(0, sv0[v]);
-                if (nrows > 1) online(1, sv1[v]);
+                mx0 = fmaxf(mx0, vec_max<T>(sv0[v]));
+                if (nrows > 1) mx1 = fmaxf(mx1, vec_max<T>(sv1[v]));
             }
             if (timed_out) atomicOr(&sh.flags, 1);
             if (d_here && tid == 0) {  // every chunk has landed for this thread
                 sh.xd[0] = widen(sdat(0)[d - lo]);
                 sh.xd[1] = widen(sdat(1)[d - lo]);
             }
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                float m = tm[r], sm = ts[r];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-                    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sm, o);
-                    ms_merge(m, sm, m2, s2, c2);
+            mx0 = warp_max(mx0);
+            mx1 = warp_max(mx1);
+            if (lane == 0) {
+                sh.rf[0][warp] = mx0;
+                sh.rf[1][warp] = mx1;
+            }
+            __syncthreads();
+            // every warp reduces the warps' maxima the same way
+            cm0 = warp_max(lane < NW ? sh.rf[0][lane] : -INFINITY);
+            cm1 = warp_max(lane < NW ? sh.rf[1][lane] : -INFINITY);
+            if (!filt) {
+                // z = x * c2 + nm, nm = -cm * c2 (0 for a slice of -inf alone, whose sum is 0)
+                const float nm0 = cm0 > -INFINITY ? -cm0 * c2 : 0.0f;
+                const float nm1 = cm1 > -INFINITY ? -cm1 * c2 : 0.0f;
+                float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll 2
+                for (int v = tid; v < nvr; v += NT) {
+                    a0 += vec_sum_ex2<T>(sv0[v], c2, nm0);
+                    if (nrows > 1) a1 += vec_sum_ex2<T>(sv1[v], c2, nm1);
                 }
+                a0 = warp_sum_f32(a0);
+                a1 = warp_sum_f32(a1);
                 if (lane == 0) {
-                    sh.rf[r][warp] = m;
-                    sh.rs[r][warp] = sm;
+                    sh.rs[0][warp] = a0;
+                    sh.rs[1][warp] = a1;
                 }
+                __syncthreads();
+                cs0 = warp_sum_f32(lane < NW ? sh.rs[0][lane] : 0.0f);
+                cs1 = warp_sum_f32(lane < NW ? sh.rs[1][lane] : 0.0f);
             }
         }
-        __syncthreads();
-        __syncthreads();
         if (!started) {
             cluster_wait_acquire();  // every CTA of the cluster has initialised its barriers
             started = true;
         }
 
-        // ---- E1: warp 0 merges the warps' partials (lanes 0-15 row 0, 16-31 row 1) and
-        // sends this CTA's partials (and the draft's logits) to every CTA
-        if (warp == 0) {
-            float pm[2], ps[2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                float tm = r < nrows && lane < NW ? sh.rf[r][lane] : -INFINITY;
-                float ts = r < nrows && lane < NW ? sh.rs[r][lane] : 0.0f;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
-                    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
-                    ms_merge(tm, ts, m2, s2, c2);
-                }
-                pm[r] = tm;
-                ps[r] = ts;
-            }
-            const float4 part = make_float4(pm[0], ps[0], pm[1], ps[1]);
-            if (lane < static_cast<int>(C)) {
-                st_peer_v4(peer_addr(smem_addr(&sh.e1[ep][rank]), lane), part);
-                if (d_here) st_peer_v2(peer_addr(smem_addr(&sh.e1d[ep]), lane), make_float2(sh.xd[0], sh.xd[1]));
-                xarrive(&sh.xbar[XB_E1 + ep], lane);
-            }
+        // ---- E1: warp 0 sends this CTA's maxima (and sums), and the draft token's logits, to
+        // every CTA
+        if (warp == 0 && lane < static_cast<int>(C)) {
+            const float4 part = make_float4(cm0, cs0, cm1, cs1);  // row 1: (-inf, 0) when absent
+            st_peer_v4(peer_addr(smem_addr(&sh.e1[ep][rank]), lane), part);
+            if (d_here) st_peer_v2(peer_addr(smem_addr(&sh.e1d[ep]), lane), make_float2(sh.xd[0], sh.xd[1]));
+            xarrive(&sh.xbar[XB_E1 + ep], lane);
         }
+        if (warp == NW - 1) find_next(un);  // its loads overlap the wait
         xwait(XB_E1 + ep);
 
-        // ---- row statistics (every CTA, identical): warp 0 merges the CTAs' partials
+        // ---- row statistics (every CTA, identical): warp 0 merges the CTAs' maxima (and,
+        // unfiltered, their sums)
         if (warp == 0) {
             const int r = lane >> 4, c = lane & 15;
             float tm = -INFINITY, ts = 0.0f;
@@ -664,87 +713,110 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 tm = r == 0 ? e.x : e.z;
                 ts = r == 0 ? e.y : e.w;
             }
+            if (filt) {
+                tm = fmaxf(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, 8));
+                tm = fmaxf(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, 4));
+                tm = fmaxf(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, 2));
+                tm = fmaxf(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, 1));
+            } else {
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {
-                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
-                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
-                ms_merge(tm, ts, m2, s2, c2);
+                for (int o = 8; o > 0; o >>= 1) {
+                    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
+                    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
+                    ms_merge(tm, ts, m2, s2, c2);
+                }
             }
             if (c == 0 && r < nrows) {
                 sh.m[r] = tm;
-                sh.nmc[r] = -tm * c2;
+                sh.nmc[r] = tm > -INFINITY ? -tm * c2 : 0.0f;
                 sh.tzb[r] = tm * (c2 * static_cast<float>(R));
                 sh.deg[r] = !(tm > -INFINITY);
                 sh.mode[r] = 0;
                 sh.theta[r] = -INFINITY;
                 sh.Z[r] = ts;
-                // for top-p alone, a kept token weighs at least (1 - p) Z / V: the tokens
-                // below that level weigh less than (1 - p) Z together
-                float zc = -static_cast<float>(ZR);
-                if (!k_on && ts > 0.0f) {
-                    const float lvl = __log2f((1.0f - pp) * ts / static_cast<float>(V));
-                    // Z <= V keeps the level below 0; the clamps keep at least one bin for
-                    // any input (NaN included)
-                    zc = fminf(fmaxf(zc, lvl - 2.0f / R), -1.0f / R);
-                }
-                sh.zcut[r] = zc;
-                sh.nbu[r] = k_on ? NB : min(NB, static_cast<int>(-zc * R) + 1);
+                sh.nbu[r] = NB;
             }
         }
         __syncthreads();
 
-        if (k_on || p_on) {
-            // ---- pass 2: histogram of the elements that can hold the boundary
-            // top-k counts the elements; top-p adds each element's weight relative to its
-            // bin's upper edge, 2^(16 - f/R) for f = tz - bin in [0, 1), from the Taylor series
-            // of exp(-a f), a = ln 2 / R, to its f^3 term (remainder below 2^-26).  One shared
-            // atomic per element: each costs an issue slot of the atomic unit whether or not
-            // its lane is selected.
+        if (filt) {
+            // ---- pass 2: the softmax sums relative to the rows' maxima, and a histogram of
+            // every weight within ZR octaves of the maximum's, binned by its bits.  Top-k
+            // counts the elements; top-p adds each element's significand rounded to 16 bits.
+            // One shared atomic per element: each costs an issue slot of the atomic unit
+            // whether or not its lane is selected.
             {
-                constexpr float A = 0.69314718055994531f / R;
-                constexpr float Q0 = 65536.0f, Q1 = -A * Q0, Q2 = A * A / 2.0f * Q0,
-                                Q3 = -A * A * A / 6.0f * Q0;
+                float acc[2] = {0.0f, 0.0f};
 #pragma unroll 1
                 for (int r = 0; r < nrows; ++r) {
                     if (sh.deg[r]) continue;
-                    const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
-                    const float tzc = -sh.zcut[r] * static_cast<float>(R);
+                    const float nm = sh.nmc[r];
                     uint32_t *hh = sh.a.h.hloc[r];
+                    float a = 0.0f;
                     for_row(sdat(r), nvr, [&](float x, int) {
-                        // -z * R >= 0 (clamped: rounding can make it a hair negative at the
-                        // maximum); bins at its integer part
-                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
-                        const float tf = truncf(tz);
-                        const float f = tz - tf;
-                        const uint32_t q =
-                            k_on ? 1u : __float2uint_rn(fmaf(fmaf(fmaf(Q3, f, Q2), f, Q1), f, Q0));
-                        const int bn = static_cast<int>(tf);
-                        if (tz < tzc) atomicAdd(&hh[bn], q);
+                        const float w = ex2(fmaf(x, c2, nm));
+                        a += w;
+                        const uint32_t ub = wbits(w);
+                        const uint32_t bn = static_cast<uint32_t>(KMAX) - (ub >> 18);
+                        // the significand with its leading bit, rounded to 16 bits
+                        const uint32_t q = k_on ? 1u : ((ub & 0x7FFFFFu) + 0x800080u) >> 8;
+                        if (bn < static_cast<uint32_t>(NB)) atomicAdd(&hh[bn], q);
                     });
+                    acc[r] = a;
+                }
+                float a0 = warp_sum_f32(acc[0]), a1 = warp_sum_f32(acc[1]);
+                if (lane == 0) {
+                    sh.rs[0][warp] = a0;
+                    sh.rs[1][warp] = a1;
                 }
             }
             __syncthreads();
-            // ---- E2a: reduce-scatter in groups of four bins, each CTA's bins to their owner
-            const int nb0 = max(sh.nbu[0], 0), nb1 = nrows > 1 ? max(sh.nbu[1], 0) : 0;
-            const int rs0 = (((nb0 + C - 1) / C) + 3) & ~3, rs1 = (((nb1 + C - 1) / C) + 3) & ~3;
-            const int g0 = static_cast<int>(C) * (rs0 >> 2), g1 = static_cast<int>(C) * (rs1 >> 2);
-            for (int idx = tid; idx < g0 + g1; idx += NT) {
-                const int r = idx < g0 ? 0 : 1;
-                const int q4 = r == 0 ? idx : idx - g0;  // group of 4 bins, in bin order
-                const int rsz = r == 0 ? rs0 : rs1;
+            cs0 = warp_sum_f32(lane < NW ? sh.rs[0][lane] : 0.0f);
+            cs1 = warp_sum_f32(lane < NW ? sh.rs[1][lane] : 0.0f);
+            // ---- E2a: reduce-scatter in groups of four bins, each CTA's bins to their owner;
+            // the CTAs' sums to every CTA
+            const int rsz = (((NB + static_cast<int>(C) - 1) / static_cast<int>(C)) + 3) & ~3;
+            const int gq = static_cast<int>(C) * (rsz >> 2);  // groups of four bins per row
+            for (int idx = tid; idx < nrows * gq; idx += NT) {
+                const int r = idx < gq ? 0 : 1;
+                const int q4 = idx - r * gq;  // group of 4 bins, in bin order
                 const int owner = (q4 * 4) / rsz, kq = q4 * 4 - owner * rsz;
                 const uint4 v = *reinterpret_cast<const uint4 *>(&sh.a.h.hloc[r][q4 * 4]);
                 st_peer_u32x4(peer_addr(smem_addr(&sh.a.h.rsin[r][static_cast<int>(rank) * rsz + kq]), owner), v);
             }
+            if (tid < static_cast<int>(C)) st_peer_v2(peer_addr(smem_addr(&sh.e2z[rank]), tid), make_float2(cs0, cs1));
             __syncthreads();
             if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_RS], tid);
             xwait(XB_RS);
-            // ---- E2b: sum the owned bins (in 64 bits: a bin of the whole row can exceed 32)
-            // and broadcast them, two bins per store
-            for (int idx = tid; idx < ((rs0 + rs1) >> 1); idx += NT) {
-                const int r = idx < (rs0 >> 1) ? 0 : 1;
-                const int kq = (r == 0 ? idx : idx - (rs0 >> 1)) * 2;
-                const int rsz = r == 0 ? rs0 : rs1;
+            // the rows' sums (every warp adds the CTAs' parts in the same order), and the bins
+            // that can hold a top-p boundary: a kept token weighs at least (1 - p) Z / V, since
+            // the tokens below that level weigh less than (1 - p) Z together
+            int nbu2[2] = {NB, NB};
+            {
+                const float2 e = lane < static_cast<int>(C) ? sh.e2z[lane] : make_float2(0.0f, 0.0f);
+                const float Zr[2] = {warp_sum_f32(e.x), warp_sum_f32(e.y)};
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    nbu2[r] = NB;
+                    if (!k_on && Zr[r] > 0.0f) {
+                        // the level, less 10% for rounding; Z <= V keeps it below 1, and the
+                        // clamps keep at least one bin for any input (NaN included)
+                        const float lvl = (1.0f - pp) * Zr[r] / static_cast<float>(V) * 0.9f;
+                        const int kl = static_cast<int>(__float_as_uint(lvl) >> 18);
+                        nbu2[r] = min(NB, max(1, KMAX - kl + 1));
+                    }
+                    if (tid == 0 && r < nrows) {
+                        sh.Z[r] = Zr[r];
+                        sh.nbu[r] = nbu2[r];
+                    }
+                }
+            }
+            // ---- E2b: sum the owned bins below the used range's end (in 64 bits: a bin of
+            // the whole row can exceed 32) and broadcast them, two bins per store
+            for (int idx = tid; idx < nrows * (rsz >> 1); idx += NT) {
+                const int r = idx < (rsz >> 1) ? 0 : 1;
+                const int kq = (idx - r * (rsz >> 1)) * 2;
+                if (static_cast<int>(rank) * rsz + kq >= nbu2[r]) continue;
                 unsigned long long c0 = 0, c1 = 0;
                 for (uint32_t c = 0; c < C; ++c) {
                     const uint2 v = *reinterpret_cast<const uint2 *>(&sh.a.h.rsin[r][c * rsz + kq]);
@@ -776,7 +848,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                     bc = 0;
                     if (bn < nbu) {
                         if (k_on) bc = static_cast<uint32_t>(sh.b.hist[r][bn]);
-                        else bin_bounds(sh.b.hist[r][bn], topfix(bn), bm, be, bc);
+                        else bin_bounds(sh.b.hist[r][bn], bn, bm, be, bc);
                     }
                 };
                 unsigned long long m_s = 0, e_s = 0;
@@ -917,16 +989,13 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
 #pragma unroll 1
                 for (int r = 0; r < nrows; ++r) {
                     if (sh.mode[r] != 1) continue;
-                    const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
-                    const float tzc = -sh.zcut[r] * static_cast<float>(R);
-                    // this thread's number of candidates: elements of bins [b1, b2] that the
-                    // histogram counted (bin bn = trunc(tz): bn >= b1 iff tz >= b1, bn <= b2
-                    // iff tz < b2 + 1)
-                    const float fb1 = static_cast<float>(sh.b1[r]);
-                    const float fb2 = fminf(static_cast<float>(sh.b2[r] + 1), tzc);
+                    // this thread's number of candidates: elements of bins [b1, b2], i.e. whose
+                    // weight's capped bits lie in [(KMAX - b2) << 18, (KMAX - b1 + 1) << 18)
+                    const float nm = sh.nmc[r];
+                    const uint32_t ulo = static_cast<uint32_t>(KMAX - sh.b2[r]) << 18;
+                    const uint32_t uw = (static_cast<uint32_t>(KMAX - sh.b1[r] + 1) << 18) - ulo;
                     auto is_cand = [&](float x) -> bool {
-                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
-                        return tz >= fb1 && tz < fb2;
+                        return wbits(ex2(fmaf(x, c2, nm))) - ulo < uw;
                     };
                     uint32_t nct = 0;
                     for_row(sdat(r), nvr, [&](float x, int) { nct += is_cand(x) ? 1u : 0u; });
@@ -1464,6 +1533,9 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         __syncthreads();  // every thread is done with this unit's shared state
         if (draw && un >= 0) issue(nxt.b, nxt.j, true);
         u = un;
+        cnx = nxt;
+        un = sh.su;  // written during this unit, before E1; rewritten only after the next set-up
+        nxt = sh.sp;
     }
     if (!started) cluster_wait_acquire();  // a cluster with no unit still completes its start
     // no CTA leaves while a peer may still write into its shared memory or arrive on its
