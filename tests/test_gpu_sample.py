@@ -242,3 +242,16 @@ def test_margin_rows_are_rare():
     compare(gpu_verify(x), oracle_verify(x), label="many rows")
     print("margin accounting:", TOTAL)
     assert TOTAL["accept_margin_rows"] <= max(1, 1e-4 * TOTAL["rows"]), TOTAL
+
+
+@pytest.mark.parametrize("C", [2, 3, 5, 6, 7, 9, 10, 11, 16])
+def test_cluster_sizes(C, monkeypatch):
+    # every cluster size the launch can choose (odd ones split the candidate slots unevenly
+    # and leave slices ragged) gives the oracle's results
+    monkeypatch.setenv("MTPSPEC_VERIFY_CLUSTER", str(C))
+    for dtype, k in (("f32", 0), ("bf16", 50)):
+        w = Workload(name="cl", B=12, D=3, V=20011, H=8, dtype=dtype, tau_range=(0.5, 1.2),
+                     top_k=k, top_p=0.9, t_std=3.0, q_noise_range=(0.3, 2.0), seed=20 + C,
+                     philox_seed=20 + C)
+        x = make_verify_inputs(w)
+        compare(gpu_verify(x), oracle_verify(x), label=f"C={C} {dtype}")

@@ -11,34 +11,35 @@
 //    position j) pair of a sampled row: the target row T[b, j] and, for j < D, the draft
 //    row Q[b, j]).  CTA r of a cluster owns the contiguous vocabulary slice
 //    [r*slice, (r+1)*slice) of both rows.
-//    Data path: bulk asynchronous copies bring a unit's two slices into shared memory;
-//    the first pass moves them into registers (each thread holds up to MAXV 16-byte
-//    vectors of each row), and the shared-memory buffer is at once refilled with the next
-//    unit's slices.  Every later pass of the unit runs over registers, so every logit is
-//    read from HBM exactly once and the next unit's loads overlap all of this unit's work.
+//    Data path: bulk asynchronous copies (four chunks per row, each on its own mbarrier)
+//    bring a unit's two slices into shared memory, where every pass of the unit reads
+//    them, so every logit is read from HBM once.  While a unit works, one thread asks L2
+//    to prefetch the next unit's slices; their copies are issued as soon as this unit no
+//    longer needs its buffer (after the accept test, or after the draw).
 //  - the greedy rows (temperature 0) go to the streaming argmax kernel
 //    (run_verify_greedy_rows), launched as a programmatic dependent so that it runs beside
 //    the persistent grid.
 //  - k_verify_finalize: one thread per row takes the first rejected position.
 //
 // Work on one unit:
-//   pass 1   per-thread maximum and softmax sum of z = (x - max) * log2(e) / tau
-//   E1       per-CTA partials (and the draft token's logits) meet in every CTA
+//   pass 1   the slices' maxima (as the chunks land), then the softmax sums of
+//            z = (x - max) * log2(e) / tau relative to them
+//   E1       per-CTA maxima and sums (and the draft token's logits) meet in every CTA
 //   pass 2   (top-k / top-p) a histogram over R bins per unit of z, only for elements that
-//            can hold the boundary: counts (top-k) or near-exact weight sums (top-p: each
-//            element adds its weight relative to its bin's upper edge in 2^-S units)
+//            can hold the boundary: counts (top-k) or near-exact weights (top-p: each
+//            element adds its weight scaled by its bin's octave, rounded to an integer)
 //   E2       reduce-scatter of the histograms to owner CTAs, then all-gather of the sums
 //   plan     the bins that may hold the boundary: by exact counts (top-k) or by rigorous
 //            bounds on the cumulative weight (top-p)
-//   gather   elements of those bins go to every CTA; the exact weight of everything above
-//            them is summed (E3); every CTA sorts the candidates (bitonic) and scans them
+//   gather   elements of those bins go to every CTA (E3); the candidates, compacted with
+//            their exact weights, are ranked by counting (or sorted, when there are many)
 //            for the exact thresholds.  If the boundary lies outside the binned range or too
 //            many elements fall into its bins, an exact bisection over the 32-bit value
 //            keys replaces this step.
 //   accept   p(d), q(d) and U_acc <= p/q (ratio formed with both maxima factored out)
 //   draw     only for a rejected draft or the bonus position: draw weights in fixed point
 //            (2^31 per unit of probability), per-warp sums in id order, CTA sums exchanged
-//            (E4), and the CTA holding the target walks its registers to the token.
+//            (E4), and the warp holding the target walks its run to the token.
 //
 // Exchanges are point to point: a CTA writes its part into every peer's shared memory and
 // then arrives (release, cluster scope) on that peer's mbarrier for the exchange; a CTA
@@ -47,6 +48,12 @@
 // CTA can only write a peer's buffer for unit k + 1 after that peer has arrived at E1 of
 // unit k + 1, i.e. after it finished unit k.  All waits are bounded and raise
 // MTPSPEC_STATUS_TIMEOUT when they give up.
+//
+// The kernel is bound by instruction issue rather than by memory: each phase is written
+// for few instructions per element (no per-element branch, bins and weights leave fp32
+// through exponent arithmetic, not conversions), and the latency-bound bookkeeping
+// (scheduling the next unit, its L2 prefetch, the Philox words) runs in one warp while the
+// others wait for E1.
 //
 // Weight sums are formed per thread in fp32 over a fixed set of elements, converted once
 // to 64-bit fixed point and reduced as integers, so every sum is deterministic and the same
@@ -65,15 +72,16 @@ constexpr int CPS = 1;           // CTAs resident per SM
 constexpr int NW = NT / 32;      // warps per CTA
 static_assert(NW <= 32 && NW % 2 == 0, "one warp merges the warps' partials; rows split the warps in halves");
 constexpr int MAXC = 16;         // largest cluster
-// Histogram bins follow the bits of a weight w = 2^z in (0, 1] (relative to the row maximum):
-// key = bits(w) >> 18 is its exponent and 5 leading significand bits, monotone in w, so 32
-// bins per octave.  Bin b holds key = KMAX - b (bin 0: w = 1, the maximum).
+// Histogram bins are R per unit of z = log2 of the softmax weight w = 2^z relative to the row
+// maximum: bin b holds tz = -z * R in [b, b + 1), tz an affine function of the logit, so that
+// a bin's members are a value interval.
 constexpr int R = 32;            // bins per octave
-constexpr int ZR = 24;           // binned range: 24 octaves, weights above about 2^-24
+constexpr int ZR = 24;           // binned range: z in (-ZR, 0], weights in (2^-24, 1]
 constexpr int NB = R * ZR;       // bins
-constexpr int KMAX = 127 * 32;   // key of w = 1
-constexpr int RSN = NB + 4 * MAXC;  // reduce-scatter inbox per row (C * RS, RS a multiple of 4)
-constexpr int CAPT = 1024;       // candidate slots per row in a cluster (CAPT / C per CTA)
+// reduce-scatter inbox per row: C * RS bins, RS = ceil(NB / C) rounded up to a multiple of 4,
+// at most NB + 32 for any C <= 16 (the most, 800, at C = 10)
+constexpr int RSN = NB + 32;
+constexpr int CAPT = 512;        // candidate slots per row in a cluster (CAPT / C per CTA)
 constexpr int NCH = 4;           // bulk-copy chunks per row
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr float FX = 2147483648.0f;  // 2^31: fixed-point scale of weights (weights <= 1)
@@ -103,7 +111,6 @@ struct __align__(16) Shared {
     unsigned long long xbar[NXB];      // exchange barriers (C arrivals each)
     float4 e1[2][MAXC];                // E1, by unit parity: (m0, s0, m1, s1) per CTA
     float2 e1d[2];                     // E1, by unit parity: the draft token's logits
-    float2 e2z[MAXC];                  // E2a: each CTA's softmax sums (rows 0, 1)
     // Buffers whose lifetimes within a unit do not overlap share storage.  The histograms
     // per row hold top-k counts, or top-p weights as 16-bit fixed point relative to each
     // bin's upper edge.  Peers write rsin before E2b, hist before the plan and cand after
@@ -124,17 +131,30 @@ struct __align__(16) Shared {
         } s;
     } b;
     uint32_t ccnt[MAXC][2];            // candidates found per CTA
+    uint32_t cpre[2][MAXC];            // per row, each CTA's offset in the row's candidate list
+    int32_t ncr[2];                    // per row, the candidates' count (-1: exact search)
     unsigned long long sx[2][MAXC][2];   // exact search: per step parity, per CTA
     unsigned long long dr[2][MAXC];      // draw: per attempt, each CTA's fixed-point weight
-    float rf[2][NW], rs[2][NW];
-    unsigned long long ru[2][NW];
-    unsigned long long scan[NW];
-    unsigned long long wsum[NW];
-    int32_t scani[NW];
-    float red_v[NW];                   // per-warp reductions of the counting path
-    unsigned long long red_w[NW];
-    unsigned long long psc_lo[NW], psc_hi[NW];  // plan: per-warp totals of the bound scans
-    uint32_t psc_cn[NW];
+    // per-warp scratch of phases that barriers separate
+    union {
+        struct {
+            float rf[2][NW], rs[2][NW];    // pass 1: maxima and sums
+        } p1;
+        struct {
+            unsigned long long lo[NW], hi[NW];  // plan: totals of the bound scans
+            uint32_t cn[NW];
+        } pl;
+        struct {
+            float v[NW];                   // counting: reductions
+            unsigned long long w[NW];
+        } ct;
+        struct {
+            unsigned long long scan[NW];   // sort and exact search: block scans and sums
+            int32_t scani[NW];
+            unsigned long long ru[2][NW];
+        } so;
+        unsigned long long wsum[NW];       // draw: each warp's weight
+    } w;
     int32_t pb1[2], pb2[2];            // plan: crossing bins found by the scan
     uint32_t pcc1[2], pcc2[2];         // plan: count bounds before b1 and through b2
     unsigned long long pma[2];         // plan: fixed-point weight of the bins before b1
@@ -142,8 +162,9 @@ struct __align__(16) Shared {
     float xd[2];                       // the draft token's logits, if this CTA holds it
     // per-row state, identical in every CTA of the cluster
     float m[2], Z[2], invZ[2], theta[2];
-    float nmc[2];     // -m * c2: z = x * c2 + nmc
     float tzb[2];     // m * c2 * R: the bin coordinate tz = -z * R = x * (-c2 * R) + tzb
+    uint32_t uwd[2];  // the unit's two Philox words (accept test, draw)
+    float nmc[2];     // -m * c2: z = x * c2 + nmc
     int32_t deg[2];   // a row of all -inf: a point mass on id 0
     int32_t mode[2];  // 0 no filter, 1 candidates, 2 exact bisection
     int32_t b1[2], b2[2], nbu[2];
@@ -416,22 +437,19 @@ template <> __device__ __forceinline__ float neg_inf<float>() { return -INFINITY
 template <> __device__ __forceinline__ uint16_t neg_inf<uint16_t>() { return 0xFF80u; }
 
 // Bounds on the fixed-point weight (2^31 per unit) of bin b of a top-p histogram.  Each
-// element of the bin adds q, its significand rounded to 16 bits (2^15 <= q <= 2^16, w = q *
-// 2^(E - 142) to half a unit of q, E the biased exponent of the bin's key); the bin's weight
-// is q_sum * 2^(E - 111): mid, exact but for the truncation of a right shift.  The margin
-// err covers half a unit of q per element, the truncation, and 2^-18 of mid for the fp32
-// error of the weights.  An element adds at least 2^15, so a bin holds at most
-// q_sum / 2^15 elements (cnt).
+// element of the bin adds q = round(w * 2^(16 + o)), o = b / R its octave, so that
+// 2^15 <= q <= 2^16 up to rounding; the bin's weight is q_sum * 2^(15 - o): mid, exact but
+// for the truncation of a right shift.  The margin err covers half a unit of q per element,
+// the truncation, and 2^-18 of mid for the fp32 error of the weights.  An element adds at
+// least 2^15 less rounding, so a bin holds at most q_sum / 32256 elements (cnt).
 __device__ __forceinline__ void bin_bounds(unsigned long long qs, int b, unsigned long long &mid,
                                            unsigned long long &err, uint32_t &cnt) {
-    const int sh = ((KMAX - b) >> 5) - 111;
-    mid = sh >= 0 ? qs << sh : qs >> (-sh);
-    cnt = static_cast<uint32_t>(qs >> 15) + 1u;
-    err = (mid >> 18) + 2ull + (sh >= 1 ? static_cast<unsigned long long>(cnt) << (sh - 1)
-                                        : static_cast<unsigned long long>(cnt));
+    const int sft = 15 - b / R;
+    mid = sft >= 0 ? qs << sft : qs >> (-sft);
+    cnt = static_cast<uint32_t>((qs >> 15) + (qs >> 21)) + 2u;
+    err = (mid >> 18) + 2ull + (sft >= 1 ? static_cast<unsigned long long>(cnt) << (sft - 1)
+                                         : static_cast<unsigned long long>(cnt));
 }
-// The bits of a weight, capped at those of 1 (the maximum's weight can round a hair above it)
-__device__ __forceinline__ uint32_t wbits(float w) { return min(__float_as_uint(w), 0x3F800000u); }
 
 struct Params {
     const void *T;
@@ -446,7 +464,6 @@ struct Params {
     int64_t V;
     int64_t slice;  // logits per CTA (a multiple of 16)
     int32_t G;      // clusters in the persistent grid
-    uint32_t sq;    // 2^S: scale of the per-element weights of a top-p histogram
     UnitResult *res;
     int32_t *status;
 };
@@ -537,9 +554,8 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     };
     // lane 0 of warps 0 .. 2 * NCH - 1: arm chunk barrier (warp / NCH, warp % NCH) exactly
     // once for unit (b, j), with a bulk copy of the 16-byte-aligned body of that chunk
-    // thread 0: ask L2 to fetch unit (b, j)'s slices ahead of their bulk copies
+    // one thread: ask L2 to fetch unit (b, j)'s slices ahead of their bulk copies
     auto prefetch_l2 = [&](int b, int j) {
-        if (tid != 0) return;
         for (int r = 0; r < (j < D ? 2 : 1); ++r) {
             const T *src = row_ptr(b, j, r);
             if (nvb == 0 || (reinterpret_cast<uintptr_t>(src) & 15u) != 0) continue;
@@ -597,7 +613,6 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
 
     for (int k = 0; u >= 0; ++k) {
         const UnitParams cur = cnx;
-        if (un >= 0) prefetch_l2(nxt.b, nxt.j);
         const uint32_t dpar = static_cast<uint32_t>(k & 1);
         const int ep = k & 1;
         const int b = cur.b, j = cur.j;
@@ -627,13 +642,12 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         __syncthreads();
 
         // ---- pass 1: the maxima of both rows' slices, chunk by chunk as the bulk copies land
-        // (the ragged tail and misaligned rows are already in place).  An unfiltered unit also
-        // sums its softmax weights relative to this CTA's maxima here; a filtered one does so
-        // in pass 2, relative to the rows' maxima, together with its histograms.
+        // (the ragged tail and misaligned rows are already in place), then the softmax sums
+        // relative to this CTA's maxima.  Two plain sweeps: no per-element branch.
         const bool filt = k_on || p_on;
         const uint4 *sv0 = reinterpret_cast<const uint4 *>(sdat(0));
         const uint4 *sv1 = reinterpret_cast<const uint4 *>(sdat(1));
-        float cm0, cm1, cs0 = 0.0f, cs1 = 0.0f;
+        float cm0, cm1, cs0, cs1;
         {
             float mx0 = -INFINITY, mx1 = -INFINITY;
             bool timed_out = false;
@@ -659,40 +673,38 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             mx0 = warp_max(mx0);
             mx1 = warp_max(mx1);
             if (lane == 0) {
-                sh.rf[0][warp] = mx0;
-                sh.rf[1][warp] = mx1;
+                sh.w.p1.rf[0][warp] = mx0;
+                sh.w.p1.rf[1][warp] = mx1;
             }
             __syncthreads();
             // every warp reduces the warps' maxima the same way
-            cm0 = warp_max(lane < NW ? sh.rf[0][lane] : -INFINITY);
-            cm1 = warp_max(lane < NW ? sh.rf[1][lane] : -INFINITY);
-            if (!filt) {
-                // z = x * c2 + nm, nm = -cm * c2 (0 for a slice of -inf alone, whose sum is 0)
-                const float nm0 = cm0 > -INFINITY ? -cm0 * c2 : 0.0f;
-                const float nm1 = cm1 > -INFINITY ? -cm1 * c2 : 0.0f;
-                float a0 = 0.0f, a1 = 0.0f;
+            cm0 = warp_max(lane < NW ? sh.w.p1.rf[0][lane] : -INFINITY);
+            cm1 = warp_max(lane < NW ? sh.w.p1.rf[1][lane] : -INFINITY);
+            // z = x * c2 + nm, nm = -cm * c2 (0 for a slice of -inf alone, whose sum is 0)
+            const float nm0 = cm0 > -INFINITY ? -cm0 * c2 : 0.0f;
+            const float nm1 = cm1 > -INFINITY ? -cm1 * c2 : 0.0f;
+            float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll 2
-                for (int v = tid; v < nvr; v += NT) {
-                    a0 += vec_sum_ex2<T>(sv0[v], c2, nm0);
-                    if (nrows > 1) a1 += vec_sum_ex2<T>(sv1[v], c2, nm1);
-                }
-                a0 = warp_sum_f32(a0);
-                a1 = warp_sum_f32(a1);
-                if (lane == 0) {
-                    sh.rs[0][warp] = a0;
-                    sh.rs[1][warp] = a1;
-                }
-                __syncthreads();
-                cs0 = warp_sum_f32(lane < NW ? sh.rs[0][lane] : 0.0f);
-                cs1 = warp_sum_f32(lane < NW ? sh.rs[1][lane] : 0.0f);
+            for (int v = tid; v < nvr; v += NT) {
+                a0 += vec_sum_ex2<T>(sv0[v], c2, nm0);
+                if (nrows > 1) a1 += vec_sum_ex2<T>(sv1[v], c2, nm1);
             }
+            a0 = warp_sum_f32(a0);
+            a1 = warp_sum_f32(a1);
+            if (lane == 0) {
+                sh.w.p1.rs[0][warp] = a0;
+                sh.w.p1.rs[1][warp] = a1;
+            }
+            __syncthreads();
+            cs0 = warp_sum_f32(lane < NW ? sh.w.p1.rs[0][lane] : 0.0f);
+            cs1 = warp_sum_f32(lane < NW ? sh.w.p1.rs[1][lane] : 0.0f);
         }
         if (!started) {
             cluster_wait_acquire();  // every CTA of the cluster has initialised its barriers
             started = true;
         }
 
-        // ---- E1: warp 0 sends this CTA's maxima (and sums), and the draft token's logits, to
+        // ---- E1: warp 0 sends this CTA's maxima and sums, and the draft token's logits, to
         // every CTA
         if (warp == 0 && lane < static_cast<int>(C)) {
             const float4 part = make_float4(cm0, cs0, cm1, cs1);  // row 1: (-inf, 0) when absent
@@ -700,11 +712,19 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             if (d_here) st_peer_v2(peer_addr(smem_addr(&sh.e1d[ep]), lane), make_float2(sh.xd[0], sh.xd[1]));
             xarrive(&sh.xbar[XB_E1 + ep], lane);
         }
-        if (warp == NW - 1) find_next(un);  // its loads overlap the wait
+        if (warp == NW - 1) {  // work whose latency the wait hides
+            if (lane == 0) {
+                if (un >= 0) prefetch_l2(nxt.b, nxt.j);
+                uint32_t c4[4] = {static_cast<uint32_t>(b), static_cast<uint32_t>(j), 0u, 0u};
+                philox(c4, static_cast<uint32_t>(P.seed), static_cast<uint32_t>(P.seed >> 32));
+                sh.uwd[0] = c4[0];
+                sh.uwd[1] = c4[1];
+            }
+            find_next(un);
+        }
         xwait(XB_E1 + ep);
 
-        // ---- row statistics (every CTA, identical): warp 0 merges the CTAs' maxima (and,
-        // unfiltered, their sums)
+        // ---- row statistics (every CTA, identical): warp 0 merges the CTAs' partials
         if (warp == 0) {
             const int r = lane >> 4, c = lane & 15;
             float tm = -INFINITY, ts = 0.0f;
@@ -713,18 +733,11 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 tm = r == 0 ? e.x : e.z;
                 ts = r == 0 ? e.y : e.w;
             }
-            if (filt) {
-                tm = fmaxf(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, 8));
-                tm = fmaxf(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, 4));
-                tm = fmaxf(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, 2));
-                tm = fmaxf(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, 1));
-            } else {
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1) {
-                    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
-                    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
-                    ms_merge(tm, ts, m2, s2, c2);
-                }
+            for (int o = 8; o > 0; o >>= 1) {
+                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
+                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
+                ms_merge(tm, ts, m2, s2, c2);
             }
             if (c == 0 && r < nrows) {
                 sh.m[r] = tm;
@@ -734,89 +747,77 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 sh.mode[r] = 0;
                 sh.theta[r] = -INFINITY;
                 sh.Z[r] = ts;
-                sh.nbu[r] = NB;
+                // the bins that can hold a top-p boundary: a kept token weighs at least
+                // (1 - p) Z / V, since the tokens below that level weigh less than (1 - p) Z
+                // together
+                float zc = -static_cast<float>(ZR);
+                if (!k_on && ts > 0.0f) {
+                    const float lvl = __log2f((1.0f - pp) * ts / static_cast<float>(V));
+                    // Z <= V keeps the level below 0; the clamps keep at least one bin for
+                    // any input (NaN included)
+                    zc = fminf(fmaxf(zc, lvl - 2.0f / R), -1.0f / R);
+                }
+                sh.nbu[r] = k_on ? NB : min(NB, static_cast<int>(-zc * R) + 1);
             }
         }
         __syncthreads();
 
         if (filt) {
-            // ---- pass 2: the softmax sums relative to the rows' maxima, and a histogram of
-            // every weight within ZR octaves of the maximum's, binned by its bits.  Top-k
-            // counts the elements; top-p adds each element's significand rounded to 16 bits.
-            // One shared atomic per element: each costs an issue slot of the atomic unit
-            // whether or not its lane is selected.
-            {
-                float acc[2] = {0.0f, 0.0f};
+            // ---- pass 2: histogram of the elements in the bins that can hold the boundary.
+            // Top-k counts them; top-p adds each element's weight scaled by its bin's octave,
+            // round(w * 2^(16 + o)): an exponent add, then rounding by the sum with 2^23.  Bin
+            // and weight leave fp32 without conversion instructions.  One shared atomic per
+            // element: its cost grows with the lanes it serves, which the bins' range keeps
+            // few.
+            constexpr float MAG = 8388608.0f;  // 2^23
 #pragma unroll 1
-                for (int r = 0; r < nrows; ++r) {
-                    if (sh.deg[r]) continue;
-                    const float nm = sh.nmc[r];
-                    uint32_t *hh = sh.a.h.hloc[r];
-                    float a = 0.0f;
+            for (int r = 0; r < nrows; ++r) {
+                if (sh.deg[r]) continue;
+                const float nm = sh.nmc[r], tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
+                const float fnb = static_cast<float>(sh.nbu[r]);
+                uint32_t *hh = sh.a.h.hloc[r];
+                if (k_on) {
                     for_row(sdat(r), nvr, [&](float x, int) {
-                        const float w = ex2(fmaf(x, c2, nm));
-                        a += w;
-                        const uint32_t ub = wbits(w);
-                        const uint32_t bn = static_cast<uint32_t>(KMAX) - (ub >> 18);
-                        // the significand with its leading bit, rounded to 16 bits
-                        const uint32_t q = k_on ? 1u : ((ub & 0x7FFFFFu) + 0x800080u) >> 8;
-                        if (bn < static_cast<uint32_t>(NB)) atomicAdd(&hh[bn], q);
+                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
+                        const float tb = __fadd_rz(tz, MAG);  // 2^23 + trunc(tz) below 2^23
+                        if (tz < fnb) atomicAdd(&hh[__float_as_int(tb) - 0x4B000000], 1u);
                     });
-                    acc[r] = a;
-                }
-                float a0 = warp_sum_f32(acc[0]), a1 = warp_sum_f32(acc[1]);
-                if (lane == 0) {
-                    sh.rs[0][warp] = a0;
-                    sh.rs[1][warp] = a1;
+                } else {
+                    for_row(sdat(r), nvr, [&](float x, int) {
+                        // -z * R >= 0 (clamped: rounding can make it a hair negative at the
+                        // maximum); bins at its integer part
+                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
+                        const float tb = __fadd_rz(tz, MAG);
+                        const int bn = __float_as_int(tb) - 0x4B000000;
+                        const float ws = __uint_as_float(__float_as_uint(ex2(fmaf(x, c2, nm))) +
+                                                         (static_cast<uint32_t>((bn >> 5) + 16) << 23));
+                        const uint32_t q = __float_as_uint(ws + MAG) - 0x4B000000u;
+                        if (tz < fnb) atomicAdd(&hh[bn], q);
+                    });
                 }
             }
             __syncthreads();
-            cs0 = warp_sum_f32(lane < NW ? sh.rs[0][lane] : 0.0f);
-            cs1 = warp_sum_f32(lane < NW ? sh.rs[1][lane] : 0.0f);
-            // ---- E2a: reduce-scatter in groups of four bins, each CTA's bins to their owner;
-            // the CTAs' sums to every CTA
-            const int rsz = (((NB + static_cast<int>(C) - 1) / static_cast<int>(C)) + 3) & ~3;
-            const int gq = static_cast<int>(C) * (rsz >> 2);  // groups of four bins per row
-            for (int idx = tid; idx < nrows * gq; idx += NT) {
-                const int r = idx < gq ? 0 : 1;
-                const int q4 = idx - r * gq;  // group of 4 bins, in bin order
+            // ---- E2a: reduce-scatter in groups of four bins, each CTA's bins to their owner
+            const int nb0 = sh.nbu[0], nb1 = nrows > 1 ? sh.nbu[1] : 0;
+            const int rs0 = (((nb0 + C - 1) / C) + 3) & ~3, rs1 = (((nb1 + C - 1) / C) + 3) & ~3;
+            const int g0 = static_cast<int>(C) * (rs0 >> 2), g1 = static_cast<int>(C) * (rs1 >> 2);
+            for (int idx = tid; idx < g0 + g1; idx += NT) {
+                const int r = idx < g0 ? 0 : 1;
+                const int q4 = r == 0 ? idx : idx - g0;  // group of 4 bins, in bin order
+                const int rsz = r == 0 ? rs0 : rs1;
                 const int owner = (q4 * 4) / rsz, kq = q4 * 4 - owner * rsz;
                 const uint4 v = *reinterpret_cast<const uint4 *>(&sh.a.h.hloc[r][q4 * 4]);
                 st_peer_u32x4(peer_addr(smem_addr(&sh.a.h.rsin[r][static_cast<int>(rank) * rsz + kq]), owner), v);
             }
-            if (tid < static_cast<int>(C)) st_peer_v2(peer_addr(smem_addr(&sh.e2z[rank]), tid), make_float2(cs0, cs1));
             __syncthreads();
             if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_RS], tid);
             xwait(XB_RS);
-            // the rows' sums (every warp adds the CTAs' parts in the same order), and the bins
-            // that can hold a top-p boundary: a kept token weighs at least (1 - p) Z / V, since
-            // the tokens below that level weigh less than (1 - p) Z together
-            int nbu2[2] = {NB, NB};
-            {
-                const float2 e = lane < static_cast<int>(C) ? sh.e2z[lane] : make_float2(0.0f, 0.0f);
-                const float Zr[2] = {warp_sum_f32(e.x), warp_sum_f32(e.y)};
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    nbu2[r] = NB;
-                    if (!k_on && Zr[r] > 0.0f) {
-                        // the level, less 10% for rounding; Z <= V keeps it below 1, and the
-                        // clamps keep at least one bin for any input (NaN included)
-                        const float lvl = (1.0f - pp) * Zr[r] / static_cast<float>(V) * 0.9f;
-                        const int kl = static_cast<int>(__float_as_uint(lvl) >> 18);
-                        nbu2[r] = min(NB, max(1, KMAX - kl + 1));
-                    }
-                    if (tid == 0 && r < nrows) {
-                        sh.Z[r] = Zr[r];
-                        sh.nbu[r] = nbu2[r];
-                    }
-                }
-            }
-            // ---- E2b: sum the owned bins below the used range's end (in 64 bits: a bin of
-            // the whole row can exceed 32) and broadcast them, two bins per store
-            for (int idx = tid; idx < nrows * (rsz >> 1); idx += NT) {
-                const int r = idx < (rsz >> 1) ? 0 : 1;
-                const int kq = (idx - r * (rsz >> 1)) * 2;
-                if (static_cast<int>(rank) * rsz + kq >= nbu2[r]) continue;
+            // ---- E2b: sum the owned bins (in 64 bits: a bin of the whole row can exceed 32)
+            // and broadcast them, two bins per store
+            for (int idx = tid; idx < ((rs0 + rs1) >> 1); idx += NT) {
+                const int r = idx < (rs0 >> 1) ? 0 : 1;
+                const int kq = (r == 0 ? idx : idx - (rs0 >> 1)) * 2;
+                const int rsz = r == 0 ? rs0 : rs1;
                 unsigned long long c0 = 0, c1 = 0;
                 for (uint32_t c = 0; c < C; ++c) {
                     const uint2 v = *reinterpret_cast<const uint2 *>(&sh.a.h.rsin[r][c * rsz + kq]);
@@ -875,9 +876,9 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                     }
                 }
                 if (lane == 31) {
-                    sh.psc_lo[warp] = m_i;
-                    sh.psc_hi[warp] = e_i;
-                    sh.psc_cn[warp] = cn_i;
+                    sh.w.pl.lo[warp] = m_i;
+                    sh.w.pl.hi[warp] = e_i;
+                    sh.w.pl.cn[warp] = cn_i;
                 }
                 if (i == 0 && r < nrows) {
                     sh.pb1[r] = nbu;
@@ -887,15 +888,37 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                     sh.pma[r] = 0;
                 }
                 __syncthreads();
-                uint32_t cn_tot = 0;
-                for (int wq = 0; wq < NW / 2; ++wq) {
-                    const int wi = r * (NW / 2) + wq;
-                    if (wq < hw) {
-                        m_i += sh.psc_lo[wi];
-                        e_i += sh.psc_hi[wi];
-                        cn_i += sh.psc_cn[wi];
+                // the row's warp totals, scanned across its NW / 2 warps by every warp
+                uint32_t cn_tot;
+                {
+                    unsigned long long pm = 0, pe = 0;
+                    uint32_t pc = 0;
+                    if (lane < NW / 2) {
+                        pm = sh.w.pl.lo[r * (NW / 2) + lane];
+                        pe = sh.w.pl.hi[r * (NW / 2) + lane];
+                        pc = sh.w.pl.cn[r * (NW / 2) + lane];
                     }
-                    cn_tot += sh.psc_cn[wi];
+#pragma unroll
+                    for (int o = 1; o < NW / 2; o <<= 1) {
+                        const unsigned long long a1 = __shfl_up_sync(0xFFFFFFFFu, pm, o);
+                        const unsigned long long a2 = __shfl_up_sync(0xFFFFFFFFu, pe, o);
+                        const uint32_t a3 = __shfl_up_sync(0xFFFFFFFFu, pc, o);
+                        if (lane >= o) {
+                            pm += a1;
+                            pe += a2;
+                            pc += a3;
+                        }
+                    }
+                    const int src = hw > 0 ? hw - 1 : 0;
+                    const unsigned long long xm = __shfl_sync(0xFFFFFFFFu, pm, src);
+                    const unsigned long long xe = __shfl_sync(0xFFFFFFFFu, pe, src);
+                    const uint32_t xc = __shfl_sync(0xFFFFFFFFu, pc, src);
+                    cn_tot = __shfl_sync(0xFFFFFFFFu, pc, NW / 2 - 1);
+                    if (hw > 0) {
+                        m_i += xm;
+                        e_i += xe;
+                        cn_i += xc;
+                    }
                 }
                 if (act) {
                     if (k_on) {
@@ -989,43 +1012,36 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
 #pragma unroll 1
                 for (int r = 0; r < nrows; ++r) {
                     if (sh.mode[r] != 1) continue;
-                    // this thread's number of candidates: elements of bins [b1, b2], i.e. whose
-                    // weight's capped bits lie in [(KMAX - b2) << 18, (KMAX - b1 + 1) << 18)
-                    const float nm = sh.nmc[r];
-                    const uint32_t ulo = static_cast<uint32_t>(KMAX - sh.b2[r]) << 18;
-                    const uint32_t uw = (static_cast<uint32_t>(KMAX - sh.b1[r] + 1) << 18) - ulo;
+                    // the candidates: elements of bins [b1, b2] (bin bn = trunc(tz): bn >= b1 iff
+                    // tz >= b1, bn <= b2 iff tz < b2 + 1)
+                    const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
+                    const float fb1 = static_cast<float>(sh.b1[r]);
+                    const float fb2 = static_cast<float>(sh.b2[r] + 1);
                     auto is_cand = [&](float x) -> bool {
-                        return wbits(ex2(fmaf(x, c2, nm))) - ulo < uw;
+                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
+                        return tz >= fb1 && tz < fb2;
                     };
-                    uint32_t nct = 0;
-                    for_row(sdat(r), nvr, [&](float x, int) { nct += is_cand(x) ? 1u : 0u; });
-                    // slots in this CTA's own block: a warp scan and one allocation per warp
-                    uint32_t incl = nct;
+                    // one sweep; a vector that holds candidates claims their slots at once (the
+                    // order of the slots does not matter: every later step depends on values)
+                    const uint4 *vp = reinterpret_cast<const uint4 *>(sdat(r));
+                    unsigned long long *cr = &sh.a.cand[r][static_cast<int>(rank) * capc];
+#pragma unroll 2
+                    for (int v = tid; v < nvr; v += NT) {
+                        float x[EPV];
+                        unpack(vp[v], x);
+                        uint32_t msk = 0;
 #pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                        if (lane >= o) incl += y;
-                    }
-                    const uint32_t wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-                    uint32_t base = 0;
-                    if (wtot) {
-                        if (lane == 31) base = atomicAdd(&sh.lcnt[r], wtot);
-                        base = __shfl_sync(0xFFFFFFFFu, base, 31);
-                    }
-                    if (nct) {
-                        // the threads that hold candidates write them
-                        uint32_t slot = base + incl - nct;
-                        for_row(sdat(r), nvr, [&](float x, int li) {
-                            if (is_cand(x)) {
-                                if (slot < static_cast<uint32_t>(capc)) {
-                                    const int gi = lo + li;
-                                    sh.a.cand[r][static_cast<int>(rank) * capc + slot] =
-                                        (static_cast<unsigned long long>(__float_as_uint(x)) << 32) |
-                                        static_cast<uint32_t>(gi);
-                                }
-                                ++slot;
+                        for (int e = 0; e < EPV; ++e) msk |= is_cand(x[e]) ? (1u << e) : 0u;
+                        if (msk) {
+                            uint32_t slot = atomicAdd(&sh.lcnt[r], static_cast<uint32_t>(__popc(msk)));
+#pragma unroll
+                            for (int e = 0; e < EPV; ++e) {
+                                if (((msk >> e) & 1u) && slot < static_cast<uint32_t>(capc))
+                                    cr[slot] = (static_cast<unsigned long long>(__float_as_uint(x[e])) << 32) |
+                                               static_cast<uint32_t>(lo + v * EPV + e);
+                                slot += (msk >> e) & 1u;
                             }
-                        });
+                        }
                     }
                 }
                 __syncthreads();
@@ -1051,33 +1067,51 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 }
                 xwait(XB_E3);
 
-                // ---- exact thresholds.  Per row: the candidates' count, the weight above
-                // them, and whether some CTA overflowed its slots (then the exact search)
-                int ncr[2] = {0, 0};
-                unsigned long long MAr[2] = {0ull, 0ull};
+                // ---- exact thresholds.  Warp 0, per row: the candidates' count (-1 when some
+                // CTA overflowed its slots, or with too many or none: then the exact search)
+                // and each CTA's offset in the row's list in CTA order
+                if (warp == 0) {
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    if (r >= nrows || sh.mode[r] != 1) continue;
-                    bool over = false;
-                    MAr[r] = sh.pma[r];
-                    for (uint32_t c = 0; c < C; ++c) {
-                        const int cc = static_cast<int>(sh.ccnt[c][r]);
-                        if (cc > capc) over = true;
-                        ncr[r] += cc;
+                    for (int r = 0; r < 2; ++r) {
+                        const bool on = r < nrows && sh.mode[r] == 1;
+                        const uint32_t cc = on && lane < static_cast<int>(C) ? sh.ccnt[lane][r] : 0u;
+                        const bool over = __any_sync(0xFFFFFFFFu, cc > static_cast<uint32_t>(capc));
+                        uint32_t incl = cc;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                            if (lane >= o) incl += y;
+                        }
+                        if (lane < static_cast<int>(C)) sh.cpre[r][lane] = incl - cc;
+                        if (lane == 31)
+                            sh.ncr[r] = !on ? 0 : (over || incl > static_cast<uint32_t>(NT) || incl == 0) ? -1
+                                                                                                    : static_cast<int>(incl);
                     }
-                    if (over || ncr[r] > NT || ncr[r] == 0) ncr[r] = -1;
                 }
+                __syncthreads();
+                const int ncr[2] = {sh.ncr[0], sh.ncr[1]};
+                const unsigned long long MAr[2] = {sh.mode[0] == 1 ? sh.pma[0] : 0ull,
+                                                   nrows > 1 && sh.mode[1] == 1 ? sh.pma[1] : 0ull};
                 // candidate i of row r, counted over the CTAs' slots in CTA order
                 auto cand_at = [&](int r, int i) -> float {
                     int c = 0;
-                    while (c + 1 < static_cast<int>(C) && i >= static_cast<int>(sh.ccnt[c][r])) {
-                        i -= static_cast<int>(sh.ccnt[c][r]);
-                        ++c;
-                    }
-                    return __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][c * capc + i] >> 32));
+                    while (c + 1 < static_cast<int>(C) && i >= static_cast<int>(sh.cpre[r][c + 1])) ++c;
+                    return __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][c * capc + i - static_cast<int>(sh.cpre[r][c])] >> 32));
                 };
                 const bool small = ncr[0] <= NSMALL && (nrows < 2 || ncr[1] <= NSMALL);
                 if (small) {
+                    // both rows' candidates into contiguous lists, with their fixed-point weights
+                    for (int t = tid; t < 2 * CAPT; t += NT) {
+                        const int r = t >= CAPT ? 1 : 0, slot = t - r * CAPT;
+                        const int c = slot / capc, i = slot - c * capc;
+                        if (ncr[r] > 0 && c < static_cast<int>(C) && i < static_cast<int>(sh.ccnt[c][r])) {
+                            const int pos = r * NSMALL + static_cast<int>(sh.cpre[r][c]) + i;
+                            const float v = __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][slot] >> 32));
+                            sh.b.s.sval[pos] = v;
+                            reinterpret_cast<uint32_t *>(sh.b.s.skey)[pos] = fix31(ex2(fmaf(v, c2, sh.nmc[r])));
+                        }
+                    }
+                    __syncthreads();
                     // ---- rank by counting, both rows at once (threads [0, NSMALL) take row
                     // 0, the rest row 1): for each candidate, the weight and number of the
                     // candidates strictly above it, each counted by S consecutive lanes over
@@ -1089,19 +1123,10 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                     const int S = min(32, NSMALL / p2);
                     const int i = tt / S, sub = tt - i * S;
                     const bool real = nr > 0 && i < nr;
-                    float v = -INFINITY;
-                    uint32_t w = 0u;
-                    float *cv = sh.b.s.sval + r * NSMALL;
-                    uint32_t *cw = reinterpret_cast<uint32_t *>(sh.b.s.skey) + r * NSMALL;
-                    if (real) {
-                        v = cand_at(r, i);
-                        w = fix31(ex2(fmaf(v, c2, sh.nmc[r])));
-                        if (sub == 0) {
-                            cv[i] = v;
-                            cw[i] = w;
-                        }
-                    }
-                    __syncthreads();
+                    const float *cv = sh.b.s.sval + r * NSMALL;
+                    const uint32_t *cw = reinterpret_cast<const uint32_t *>(sh.b.s.skey) + r * NSMALL;
+                    const float v = real ? cv[i] : -INFINITY;
+                    const uint32_t w = real ? cw[i] : 0u;
                     unsigned long long sgt = 0;
                     int cgt = 0;
                     if (real) {
@@ -1125,10 +1150,10 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                     unsigned long long tgt = 0;
                     if (k_on && p_on) {
                         const unsigned long long ws = warp_sum_u64(kept_k ? static_cast<unsigned long long>(w) : 0ull);
-                        if (lane == 0) sh.red_w[warp] = ws;
+                        if (lane == 0) sh.w.ct.w[warp] = ws;
                         __syncthreads();
                         unsigned long long zk = MA;
-                        for (int wq = 0; wq < NW / 2; ++wq) zk += sh.red_w[r * (NW / 2) + wq];
+                        for (int wq = 0; wq < NW / 2; ++wq) zk += sh.w.ct.w[r * (NW / 2) + wq];
                         tgt = fx_target_fx(pp, zk);
                         __syncthreads();
                     } else if (p_on) {
@@ -1144,16 +1169,16 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                         wk += __shfl_xor_sync(0xFFFFFFFFu, wk, o);
                     }
                     if (lane == 0) {
-                        sh.red_v[warp] = vmin;
-                        sh.red_w[warp] = wk;
+                        sh.w.ct.v[warp] = vmin;
+                        sh.w.ct.w[warp] = wk;
                     }
                     __syncthreads();
                     if (tt == 0 && nr > 0) {
                         float th = INFINITY;
                         unsigned long long zf = MA;
                         for (int wq = 0; wq < NW / 2; ++wq) {
-                            th = fminf(th, sh.red_v[r * (NW / 2) + wq]);
-                            zf += sh.red_w[r * (NW / 2) + wq];
+                            th = fminf(th, sh.w.ct.v[r * (NW / 2) + wq]);
+                            zf += sh.w.ct.w[r * (NW / 2) + wq];
                         }
                         sh.theta[r] = th;
                         sh.Z[r] = fx_to_float(zf);
@@ -1212,11 +1237,11 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                         const unsigned long long wk = (real && v >= thk) ? w : 0ull;
                         // weight strictly above each value: the exclusive prefix of the weights
                         // at the first position of its tie group (sorted descending)
-                        const unsigned long long excl = block_excl_scan_u64(wk, sh.scan);
+                        const unsigned long long excl = block_excl_scan_u64(wk, sh.w.so.scan);
                         const int32_t headpos = (tid == 0 || sh.b.s.sval[tid - 1] != v) ? tid : -1;
-                        const int32_t first = block_incl_max_i32(headpos, sh.scani);
+                        const int32_t first = block_incl_max_i32(headpos, sh.w.so.scani);
                         sh.b.s.skey[tid] = excl;
-                        const unsigned long long zk = MA + block_sum_u64(wk, sh.ru[r]);
+                        const unsigned long long zk = MA + block_sum_u64(wk, sh.w.so.ru[r]);
                         if (tid == 0) {
                             sh.tgt[r] = k_on ? fx_target_fx(pp, zk) : fx_target(pp, sh.Z[r]);
                         }
@@ -1228,13 +1253,13 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                         for (int o = 16; o > 0; o >>= 1)
                             lastk = max(lastk, __shfl_xor_sync(0xFFFFFFFFu, lastk, o));
                         __syncthreads();
-                        if (lane == 0) sh.scani[warp] = lastk;
+                        if (lane == 0) sh.w.so.scani[warp] = lastk;
                         __syncthreads();
                         int32_t lk = -1;
-                        for (int wq = 0; wq < NW; ++wq) lk = max(lk, sh.scani[wq]);
+                        for (int wq = 0; wq < NW; ++wq) lk = max(lk, sh.w.so.scani[wq]);
                         const float th = sh.b.s.sval[lk < 0 ? 0 : lk];  // the smallest kept value
                         const unsigned long long zf =
-                            MA + block_sum_u64((real && v >= th) ? wk : 0ull, sh.ru[r]);
+                            MA + block_sum_u64((real && v >= th) ? wk : 0ull, sh.w.so.ru[r]);
                         if (tid == 0) {
                             sh.theta[r] = th;
                             sh.Z[r] = fx_to_float(zf);
@@ -1270,8 +1295,8 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                         if (r == 0) acc0 = ac;
                         else acc1 = ac;
                     }
-                    const unsigned long long s0 = block_sum_u64(acc0, sh.ru[0]);
-                    const unsigned long long s1 = block_sum_u64(acc1, sh.ru[1]);
+                    const unsigned long long s0 = block_sum_u64(acc0, sh.w.so.ru[0]);
+                    const unsigned long long s1 = block_sum_u64(acc1, sh.w.so.ru[1]);
                     const int sp = static_cast<int>(sstep & 1u);
                     if (tid < static_cast<int>(C)) {
                         st_peer_u64(peer_addr(smem_addr(&sh.sx[sp][rank][0]), tid), s0);
@@ -1337,9 +1362,8 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         __syncthreads();
 
         // ---- accept test
-        uint32_t uw[4] = {static_cast<uint32_t>(b), static_cast<uint32_t>(j), 0u, 0u};
-        philox(uw, static_cast<uint32_t>(P.seed), static_cast<uint32_t>(P.seed >> 32));
-        const float u_acc = word_uniform(uw[0]), u_smp = word_uniform(uw[1]);
+        const uint32_t uw1 = sh.uwd[1];  // the unit's Philox words, (b, j, 0, 0) under the seed
+        const float u_acc = word_uniform(sh.uwd[0]), u_smp = word_uniform(uw1);
 
         // membership and probability of a token in the target (0) and draft (1) rows
         const float m0 = sh.m[0], m1 = sh.m[1], th0 = sh.theta[0], th1 = sh.theta[1];
@@ -1406,6 +1430,10 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             auto vec_weight = [&](int v, int e_only) -> uint32_t {
                 float x[EPV], y[EPV];
                 unpack(sv0[v], x);
+                float xm = x[0];
+#pragma unroll
+                for (int e = 1; e < EPV; ++e) xm = fmaxf(xm, x[e]);
+                if (!(xm >= th0)) return 0u;  // no target logit of the vector is kept
                 unpack(sv1[v], y);
                 uint32_t s = 0;
 #pragma unroll
@@ -1422,11 +1450,11 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 uint32_t acc = 0;
                 for (int v = w0 + lane; v < w1; v += 32) acc += vec_weight(v, -1);
                 acc = __reduce_add_sync(0xFFFFFFFFu, acc);
-                if (lane == 0) sh.wsum[warp] = acc;
+                if (lane == 0) sh.w.wsum[warp] = acc;
                 __syncthreads();
                 if (tid < static_cast<int>(C)) {
                     unsigned long long cs = 0;
-                    for (int wq = 0; wq < NW; ++wq) cs += sh.wsum[wq];
+                    for (int wq = 0; wq < NW; ++wq) cs += sh.w.wsum[wq];
                     st_peer_u64(peer_addr(smem_addr(&sh.dr[attempt][rank]), tid), cs);
                     xarrive(&sh.xbar[XB_E4 + attempt], tid);
                 }
@@ -1439,7 +1467,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                     // integer sum S exceeds u_smp * R exactly when S > floor(u_smp * R), and
                     // u_smp = k * 2^-24 with k odd, so floor(u_smp * R) = (k * R) >> 24 exactly
                     const unsigned long long tt =
-                        (static_cast<unsigned long long>(2u * (uw[1] >> 9) + 1u) * Rt) >> 24;
+                        (static_cast<unsigned long long>(2u * (uw1 >> 9) + 1u) * Rt) >> 24;
                     uint32_t cs = C - 1;
                     unsigned long long before = 0;
                     for (uint32_t c = 0; c < C; ++c) {
@@ -1457,15 +1485,15 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                         int ws = NW - 1;
                         unsigned long long wb = before;
                         for (int wq = 0; wq < NW; ++wq) {
-                            if (wb + sh.wsum[wq] > tt) {
+                            if (wb + sh.w.wsum[wq] > tt) {
                                 ws = wq;
                                 break;
                             }
-                            wb += sh.wsum[wq];
+                            wb += sh.w.wsum[wq];
                         }
                         if (ws == NW - 1) {
                             wb = before;
-                            for (int wq = 0; wq + 1 < NW; ++wq) wb += sh.wsum[wq];
+                            for (int wq = 0; wq + 1 < NW; ++wq) wb += sh.w.wsum[wq];
                         }
                         if (warp == ws) {
                             // the vector that crosses the target, walking the warp's run in id
@@ -1493,15 +1521,20 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                                 }
                                 rem -= __shfl_sync(0xFFFFFFFFu, incl, 31);
                             }
-                            // one lane walks that vector's elements (the last positive element
-                            // of the run when rounding left no vector crossing)
+                            // one lane walks that vector's elements, each weight once (the last
+                            // positive element of the run when rounding left no vector crossing)
                             if (lane == 0) {
                                 const int fv = hit_v >= 0 ? hit_v : pos_v;
                                 if (fv >= 0) {
+                                    float x[EPV], y[EPV];
+                                    unpack(sv0[fv], x);
+                                    unpack(sv1[fv], y);
                                     int fe = EPV - 1, le = 0;
                                     uint32_t cum = 0;
                                     for (int e = 0; e < EPV; ++e) {
-                                        const uint32_t we = vec_weight(fv, e);
+                                        uint32_t we = weight(x[e], y[e]);
+                                        // id 0 of a degenerate draft row carries no residual weight
+                                        if (deg1 && wmode == 0 && lo == 0 && fv == 0 && e == 0) we = 0u;
                                         if (we > 0) le = e;
                                         cum += we;
                                         if (hit_v >= 0 && we > 0 && cum > hit_rem) {
@@ -1583,61 +1616,39 @@ static int64_t verify_slice(int64_t V, int C) {
 
 constexpr size_t kSmemLimit = 227u * 1024u;
 
+// Shared memory of a CTA for a slice of `slice` logits.
 static size_t verify_smem_bytes(int64_t slice, size_t es) {
     const size_t head = (sizeof(vs::Shared) + 127) & ~static_cast<size_t>(127);
     const size_t row = ((static_cast<size_t>(slice) * es) + 127) & ~static_cast<size_t>(127);
     return head + 2 * row;
 }
 
-// Shared memory per CTA when two CTAs (of different clusters) share an SM, so that one unit's
-// waits overlap the other's work.
-constexpr size_t kSmemHalf = 113u * 1024u;
-
-// Clusters of 8 CTAs (16 when there are too few units to spread over clusters of 8; 16 too
-// when CTAs share an SM and that lets them fit); larger clusters when a CTA's slices of a
-// target and a draft row would not fit its shared memory otherwise.  0 CTAs when nothing fits.
-static VerifyGeometry verify_geometry(int64_t V, size_t es, int64_t units) {
-    VerifyGeometry gm = {0, 0};
-    int Cmin = 0;
-    for (int C = 2; C <= vs::MAXC; C *= 2)
-        if (verify_smem_bytes(verify_slice(V, C), es) <= kSmemLimit) {
-            Cmin = C;
-            break;
-        }
-    if (Cmin == 0) return gm;
-    int C = units <= 8 ? 16 : 8;
-    if (C < Cmin) C = Cmin;
-    if (vs::CPS > 1 && C < vs::MAXC && verify_smem_bytes(verify_slice(V, C), es) > kSmemHalf &&
-        verify_smem_bytes(verify_slice(V, vs::MAXC), es) <= kSmemHalf)
-        C = vs::MAXC;
-    if (const char *e = getenv("MTPSPEC_VERIFY_CLUSTER")) {
-        const int c = atoi(e);
-        if ((c == 2 || c == 4 || c == 8 || c == 16) && c >= Cmin) C = c;
-    }
-    gm.C = C;
-    gm.slice = verify_slice(V, C);
-    return gm;
+// Smallest cluster size whose CTAs fit their slices of a target and a draft row in shared
+// memory (0: none up to MAXC).
+static int verify_cmin(int64_t V, size_t es) {
+    for (int C = 2; C <= vs::MAXC; ++C)
+        if (verify_smem_bytes(verify_slice(V, C), es) <= kSmemLimit) return C;
+    return 0;
 }
 
 size_t verify_workspace_bytes(int64_t B, int32_t D) {
     return static_cast<size_t>(B) * static_cast<size_t>(D + 1) * sizeof(vs::UnitResult);
 }
 
-bool verify_fits(int64_t V, size_t elem_bytes) {
-    return verify_geometry(V, elem_bytes, 1 << 20).C > 0;
-}
+bool verify_fits(int64_t V, size_t elem_bytes) { return verify_cmin(V, elem_bytes) > 0; }
 
 // Resident clusters of the persistent kernel for one configuration (cached).
 template <typename T>
 static int resident_clusters(int C, size_t smem) {
+    constexpr int NC = 64;
     static std::mutex mu;
-    static int cache_c[8] = {0}, cache_v[8] = {0};
-    static size_t cache_s[8] = {0};
-    static int dev_of[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+    static int cache_c[NC] = {0}, cache_v[NC] = {0}, dev_of[NC] = {0};
+    static size_t cache_s[NC] = {0};
+    static int used = 0;
     int dev = 0;
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < used; ++i)
         if (dev_of[i] == dev && cache_c[i] == C && cache_s[i] == smem) return cache_v[i];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(C), 1, 1);
@@ -1653,41 +1664,70 @@ static int resident_clusters(int C, size_t smem) {
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, vs::k_verify_rr<T>, &cfg) != cudaSuccess || n < 1)
         n = 1;
-    for (int i = 0; i < 8; ++i)
-        if (dev_of[i] == -1 || i == 7) {
-            dev_of[i] = dev;
-            cache_c[i] = C;
-            cache_s[i] = smem;
-            cache_v[i] = n;
-            break;
-        }
+    const int i = used < NC ? used++ : NC - 1;
+    dev_of[i] = dev;
+    cache_c[i] = C;
+    cache_s[i] = smem;
+    cache_v[i] = n;
     return n;
+}
+
+// Fixed cost of a unit, in logits of a CTA's slice: the exchanges and the work that does not
+// scale with the slice take about as long as the passes over a slice of this length (fitted
+// to timings of the 256-row serving verify over a 151,936-id vocabulary, fp32 and bf16).
+constexpr int64_t kUnitFixedLogits = 5000;
+
+// The cluster size of a launch.  Clusters are placed within GPCs, so the resident clusters
+// (and the SMs they use) depend on the size; among the sizes whose slices fit, take the one
+// that finishes the most units per unit time by a simple model: min(resident clusters,
+// units) units in flight, each taking time in proportion to kUnitFixedLogits + slice.
+// MTPSPEC_VERIFY_CLUSTER forces a size (any that fits, 2 to MAXC).
+template <typename T>
+static VerifyGeometry verify_geometry(int64_t V, int64_t units) {
+    VerifyGeometry gm = {0, 0};
+    const int Cmin = verify_cmin(V, sizeof(T));
+    if (Cmin == 0) return gm;
+    int best = 0;
+    double best_score = -1.0;
+    for (int C = Cmin; C <= vs::MAXC; ++C) {
+        const int64_t sl = verify_slice(V, C);
+        const size_t smem = verify_smem_bytes(sl, sizeof(T));
+        if (smem > kSmemLimit) continue;
+        const int64_t a = std::min<int64_t>(resident_clusters<T>(C, smem), units);
+        const double score = static_cast<double>(a) / static_cast<double>(kUnitFixedLogits + sl);
+        if (score > best_score) {
+            best_score = score;
+            best = C;
+        }
+    }
+    if (const char *e = getenv("MTPSPEC_VERIFY_CLUSTER")) {
+        const int c = atoi(e);
+        if (c >= Cmin && c <= vs::MAXC) best = c;
+    }
+    gm.C = best;
+    gm.slice = verify_slice(V, best);
+    return gm;
 }
 
 template <typename T>
 static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     const int64_t units = p.B * (p.D + 1);
-    const VerifyGeometry gm = verify_geometry(p.V, sizeof(T), units);
-    if (gm.C == 0) return cudaErrorInvalidValue;
-    const int C = gm.C;
-    p.slice = gm.slice;
-    // per-element weights of a top-p histogram in units of 2^-S of the bin's upper edge,
-    // with S so that V of them fit in 32 bits
-    int lg = 0;
-    while ((int64_t{1} << lg) < p.V) ++lg;
-    p.sq = 1u << (31 - lg);
-    const size_t smem = verify_smem_bytes(p.slice, sizeof(T));
+    // the kernel may take the largest shared memory and clusters up to MAXC (the occupancy
+    // queries of the geometry need both)
     cudaError_t e = cudaFuncSetAttribute(vs::k_verify_rr<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+                                         static_cast<int>(kSmemLimit));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(vs::k_verify_rr<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (e != cudaSuccess) return e;
-    if (C > 8) {
-        e = cudaFuncSetAttribute(vs::k_verify_rr<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
+    e = cudaFuncSetAttribute(vs::k_verify_rr<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    const VerifyGeometry gm = verify_geometry<T>(p.V, units);
+    if (gm.C == 0) return cudaErrorInvalidValue;
+    const int C = gm.C;
+    p.slice = gm.slice;
+    const size_t smem = verify_smem_bytes(p.slice, sizeof(T));
     int64_t G = resident_clusters<T>(C, smem);
     if (G > units) G = units;
     p.G = static_cast<int32_t>(G);
@@ -1722,7 +1762,6 @@ cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream) {
     p.V = a.V;
     p.slice = 0;
     p.G = 1;
-    p.sq = 1u;
     p.res = static_cast<vs::UnitResult *>(a.workspace);
     p.status = a.status;
     // the sampled rows, then (beside them) the greedy rows, then the per-row finalize
