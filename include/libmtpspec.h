@@ -165,7 +165,9 @@ int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draf
  *   workspace      >= spec_verify_workspace_bytes(B, D, V) bytes, 256-byte aligned;
  *                  no initial contents are needed
  *   status         int32 [1] or NULL
- *   B >= 0, 1 <= D <= 64, 1 <= V <= 2^31 - 1.
+ *   B >= 0, 1 <= D <= 64, 1 <= V <= 407,552 (fp32) or 815,104 (bf16): a CTA of a cluster
+ *   of at most 16 holds its slices of a target and a draft row in shared memory; a larger
+ *   V returns MTPSPEC_ERR_SHAPE.
  */
 int spec_verify_sample(const void *target_logits, const void *draft_logits, int dtype,
                        const int32_t *draft_ids, const float *temperature, const int32_t *top_k,
@@ -175,7 +177,8 @@ int spec_verify_sample(const void *target_logits, const void *draft_logits, int 
                        void *stream);
 
 /* Bytes of device workspace spec_verify_sample needs for (B, D, V); 0 for B == 0 or
- * for arguments spec_verify_sample would reject. */
+ * for arguments spec_verify_sample rejects whatever the logit type (V above the bf16
+ * limit included). */
 size_t spec_verify_workspace_bytes(int64_t B, int32_t D, int64_t V);
 
 /*

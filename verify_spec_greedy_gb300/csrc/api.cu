@@ -108,6 +108,7 @@ MTPSPEC_API int spec_verify_greedy(const void *target_logits, int dtype, const i
 
 MTPSPEC_API size_t spec_verify_workspace_bytes(int64_t B, int32_t D, int64_t V) {
     if (B <= 0 || D < 1 || D > kMaxD || V < 1 || V > kMaxV || B > kMaxRows) return 0;
+    if (!mtpspec::verify_fits(V, 2)) return 0;  // too large for either logit type
     return mtpspec::verify_workspace_bytes(B, D);
 }
 
