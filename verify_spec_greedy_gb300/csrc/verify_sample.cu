@@ -81,7 +81,8 @@ constexpr int NB = R * ZR;       // bins
 // reduce-scatter inbox per row: C * RS bins, RS = ceil(NB / C) rounded up to a multiple of 4,
 // at most NB + 32 for any C <= 16 (the most, 800, at C = 10)
 constexpr int RSN = NB + 32;
-constexpr int CAPT = 512;        // candidate slots per row in a cluster (CAPT / C per CTA)
+constexpr int CAPT = RSN;        // candidate slots per row in a cluster (CAPT / C per CTA):
+                                 // as many as the histograms they share storage with
 constexpr int NCH = 4;           // bulk-copy chunks per row
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr float FX = 2147483648.0f;  // 2^31: fixed-point scale of weights (weights <= 1)
