@@ -99,6 +99,10 @@ constexpr int NXB = 9;
 using UnitResult = VerifyUnitRecord;
 
 constexpr int NSMALL = NT / 2;   // candidates per row ranked by counting (both rows at once)
+constexpr int PW = 8;            // plan: warps per row
+constexpr int PL = PW * 32;      // plan: lanes per row
+constexpr int BPL = NB / PL;     // plan: bins per lane
+static_assert(NB % PL == 0 && 2 * PW <= NW, "the plan's groups tile the bins and fit the CTA");
 
 // Per-unit parameters of a sampled row.
 struct UnitParams {
@@ -293,6 +297,13 @@ __device__ __forceinline__ int32_t block_incl_max_i32(int32_t v, int32_t *scratc
     int32_t before = -1;
     for (int w = 0; w < warp; ++w) before = max(before, scratch[w]);
     return max(before, incl);
+}
+
+// The plan's barrier of row r's group (hardware barriers 1 and 2; 0 is __syncthreads).
+template <int N>
+__device__ __forceinline__ void group_barrier(int r) {
+    if (r == 0) asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
+    else asm volatile("bar.sync 2, %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void mbar_init(unsigned long long *bar, uint32_t count) {
@@ -748,6 +759,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 sh.mode[r] = 0;
                 sh.theta[r] = -INFINITY;
                 sh.Z[r] = ts;
+                sh.tgt[r] = fx_target(pp, ts);  // the fixed-point top-p target of the plan
                 // the bins that can hold a top-p boundary: a kept token weighs at least
                 // (1 - p) Z / V, since the tokens below that level weigh less than (1 - p) Z
                 // together
@@ -825,115 +837,102 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                     c0 += v.x;
                     c1 += v.y;
                 }
-                const uint4 w = make_uint4(static_cast<uint32_t>(c0), static_cast<uint32_t>(c0 >> 32),
-                                           static_cast<uint32_t>(c1), static_cast<uint32_t>(c1 >> 32));
-                const uint32_t a = smem_addr(&sh.b.hist[r][static_cast<int>(rank) * rsz + kq]);
-                for (uint32_t c = 0; c < C; ++c) st_peer_u32x4(peer_addr(a, c), w);
+                // bin b goes to [b % BPL][b / BPL] (bins past NB lie past every used range)
+                const int b0 = static_cast<int>(rank) * rsz + kq;
+                const uint32_t a0 = smem_addr(&sh.b.hist[r][(b0 % BPL) * PL + b0 / BPL]);
+                const uint32_t a1 = smem_addr(&sh.b.hist[r][((b0 + 1) % BPL) * PL + (b0 + 1) / BPL]);
+                for (uint32_t c = 0; c < C; ++c) {
+                    if (b0 < NB) st_peer_u64(peer_addr(a0, c), c0);
+                    if (b0 + 1 < NB) st_peer_u64(peer_addr(a1, c), c1);
+                }
             }
             __syncthreads();
             if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_AG], tid);
             xwait(XB_AG);
 
             // ---- plan per row: the bin range that holds the boundary, or the exact search.
-            // Threads [0, NSMALL) take row 0 and the rest row 1, BPT bins each; block scans of
-            // the per-bin counts (top-k) or weights and their margins (top-p) find the
-            // crossing bins and the exact weight of the bins before them.
+            // The PW warps of group r take row r, BPL bins a lane (the gathered histogram is
+            // stored transposed, bin b at [b % BPL][b / BPL], so that these loads are free of
+            // bank conflicts); scans of the per-bin counts (top-k) or weights and their
+            // margins (top-p) over the group's lanes find the crossing bins and the exact
+            // weight of the bins before them.  The other warps go on to the barrier.
             {
-                constexpr int BPT = (NB + NSMALL - 1) / NSMALL;
-                const int r = tid / NSMALL, i = tid - r * NSMALL, hw = warp - r * (NW / 2);
-                const bool act = r < nrows && !sh.deg[r];
-                const int nbu = act ? sh.nbu[r] : 0;
-                const unsigned long long tgt = act && !k_on ? fx_target(pp, sh.Z[r]) : 0ull;
-                // weight, margin and element-count bound of bin bn (0 past the used bins)
-                auto bounds = [&](int bn, unsigned long long &bm, unsigned long long &be, uint32_t &bc) {
-                    bm = be = 0;
-                    bc = 0;
-                    if (bn < nbu) {
-                        if (k_on) bc = static_cast<uint32_t>(sh.b.hist[r][bn]);
-                        else bin_bounds(sh.b.hist[r][bn], bn, bm, be, bc);
-                    }
-                };
-                unsigned long long m_s = 0, e_s = 0;
-                uint32_t cn_s = 0;
-                for (int t = 0; t < BPT; ++t) {
-                    unsigned long long bm, be;
-                    uint32_t bc;
-                    bounds(BPT * i + t, bm, be, bc);
-                    m_s += bm;
-                    e_s += be;
-                    cn_s += bc;
-                }
-                unsigned long long m_i = m_s, e_i = e_s;
-                uint32_t cn_i = cn_s;
+                const int r = warp / PW, j = tid - r * PL, hw = warp - r * PW;
+                if (r < nrows && !sh.deg[r]) {
+                    const int nbu = sh.nbu[r];
+                    const unsigned long long tgt = k_on ? 0ull : sh.tgt[r];
+                    const unsigned long long *hr = sh.b.hist[r];
+                    // weight, margin and element-count bound of bin bn (0 past the used bins)
+                    auto bounds = [&](int bn, unsigned long long &bm, unsigned long long &be, uint32_t &bc) {
+                        bm = be = 0;
+                        bc = 0;
+                        if (bn < nbu) {
+                            const unsigned long long qs = hr[(bn % BPL) * PL + bn / BPL];
+                            if (k_on) bc = static_cast<uint32_t>(qs);
+                            else bin_bounds(qs, bn, bm, be, bc);
+                        }
+                    };
+                    unsigned long long m_s = 0, e_s = 0;
+                    uint32_t cn_s = 0;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned long long a1 = __shfl_up_sync(0xFFFFFFFFu, m_i, o);
-                    const unsigned long long a2 = __shfl_up_sync(0xFFFFFFFFu, e_i, o);
-                    const uint32_t a3 = __shfl_up_sync(0xFFFFFFFFu, cn_i, o);
-                    if (lane >= o) {
-                        m_i += a1;
-                        e_i += a2;
-                        cn_i += a3;
+                    for (int t = 0; t < BPL; ++t) {
+                        unsigned long long bm, be;
+                        uint32_t bc;
+                        bounds(BPL * j + t, bm, be, bc);
+                        m_s += bm;
+                        e_s += be;
+                        cn_s += bc;
                     }
-                }
-                if (lane == 31) {
-                    sh.w.pl.lo[warp] = m_i;
-                    sh.w.pl.hi[warp] = e_i;
-                    sh.w.pl.cn[warp] = cn_i;
-                }
-                if (i == 0 && r < nrows) {
-                    sh.pb1[r] = nbu;
-                    sh.pb2[r] = nbu;
-                    sh.pcc1[r] = 0;
-                    sh.pcc2[r] = 0;
-                    sh.pma[r] = 0;
-                }
-                __syncthreads();
-                // the row's warp totals, scanned across its NW / 2 warps by every warp
-                uint32_t cn_tot;
-                {
-                    unsigned long long pm = 0, pe = 0;
-                    uint32_t pc = 0;
-                    if (lane < NW / 2) {
-                        pm = sh.w.pl.lo[r * (NW / 2) + lane];
-                        pe = sh.w.pl.hi[r * (NW / 2) + lane];
-                        pc = sh.w.pl.cn[r * (NW / 2) + lane];
-                    }
+                    unsigned long long m_i = m_s, e_i = e_s;
+                    uint32_t cn_i = cn_s;
 #pragma unroll
-                    for (int o = 1; o < NW / 2; o <<= 1) {
-                        const unsigned long long a1 = __shfl_up_sync(0xFFFFFFFFu, pm, o);
-                        const unsigned long long a2 = __shfl_up_sync(0xFFFFFFFFu, pe, o);
-                        const uint32_t a3 = __shfl_up_sync(0xFFFFFFFFu, pc, o);
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned long long a1 = __shfl_up_sync(0xFFFFFFFFu, m_i, o);
+                        const unsigned long long a2 = __shfl_up_sync(0xFFFFFFFFu, e_i, o);
+                        const uint32_t a3 = __shfl_up_sync(0xFFFFFFFFu, cn_i, o);
                         if (lane >= o) {
-                            pm += a1;
-                            pe += a2;
-                            pc += a3;
+                            m_i += a1;
+                            e_i += a2;
+                            cn_i += a3;
                         }
                     }
-                    const int src = hw > 0 ? hw - 1 : 0;
-                    const unsigned long long xm = __shfl_sync(0xFFFFFFFFu, pm, src);
-                    const unsigned long long xe = __shfl_sync(0xFFFFFFFFu, pe, src);
-                    const uint32_t xc = __shfl_sync(0xFFFFFFFFu, pc, src);
-                    cn_tot = __shfl_sync(0xFFFFFFFFu, pc, NW / 2 - 1);
-                    if (hw > 0) {
-                        m_i += xm;
-                        e_i += xe;
-                        cn_i += xc;
+                    if (lane == 31) {
+                        sh.w.pl.lo[warp] = m_i;
+                        sh.w.pl.hi[warp] = e_i;
+                        sh.w.pl.cn[warp] = cn_i;
                     }
-                }
-                if (act) {
+                    if (j == 0) {
+                        sh.pb1[r] = nbu;
+                        sh.pb2[r] = nbu;
+                        sh.pcc1[r] = 0;
+                        sh.pcc2[r] = 0;
+                        sh.pma[r] = 0;
+                    }
+                    group_barrier<PL>(r);
+                    // the group's earlier warps, and the row's total count
+                    uint32_t cn_tot = 0;
+#pragma unroll
+                    for (int q = 0; q < PW; ++q) {
+                        const int wi = r * PW + q;
+                        if (q < hw) {
+                            m_i += sh.w.pl.lo[wi];
+                            e_i += sh.w.pl.hi[wi];
+                            cn_i += sh.w.pl.cn[wi];
+                        }
+                        cn_tot += sh.w.pl.cn[wi];
+                    }
                     if (k_on) {
                         // the bin holding the k-th largest value; every bin up to it is gathered
                         const uint32_t need = static_cast<uint32_t>(kk);
                         if (cn_i - cn_s < need && cn_i >= need) {
                             uint32_t acc = cn_i - cn_s;
-                            for (int t = 0; t < BPT; ++t) {
+                            for (int t = 0; t < BPL; ++t) {
                                 unsigned long long bm, be;
                                 uint32_t bc;
-                                bounds(BPT * i + t, bm, be, bc);
+                                bounds(BPL * j + t, bm, be, bc);
                                 acc += bc;
                                 if (acc >= need) {
-                                    sh.pb2[r] = BPT * i + t;
+                                    sh.pb2[r] = BPL * j + t;
                                     sh.pcc2[r] = acc;
                                     break;
                                 }
@@ -946,12 +945,12 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                         if (m_i + e_i - (m_s + e_s) < tgt && m_i + e_i >= tgt) {
                             unsigned long long am = m_i - m_s, ae = e_i - e_s;
                             uint32_t cb = cn_i - cn_s;
-                            for (int t = 0; t < BPT; ++t) {
+                            for (int t = 0; t < BPL; ++t) {
                                 unsigned long long bm, be;
                                 uint32_t bc;
-                                bounds(BPT * i + t, bm, be, bc);
+                                bounds(BPL * j + t, bm, be, bc);
                                 if (am + bm + ae + be >= tgt) {
-                                    sh.pb1[r] = BPT * i + t;
+                                    sh.pb1[r] = BPL * j + t;
                                     sh.pcc1[r] = cb;
                                     sh.pma[r] = am;
                                     break;
@@ -966,43 +965,43 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                         if (lo_x < tgt && lo_i >= tgt) {
                             unsigned long long am = m_i - m_s, ae = e_i - e_s;
                             uint32_t cb = cn_i - cn_s;
-                            for (int t = 0; t < BPT; ++t) {
+                            for (int t = 0; t < BPL; ++t) {
                                 unsigned long long bm, be;
                                 uint32_t bc;
-                                bounds(BPT * i + t, bm, be, bc);
+                                bounds(BPL * j + t, bm, be, bc);
                                 am += bm;
                                 ae += be;
                                 cb += bc;
                                 if (am > ae && am - ae >= tgt) {
-                                    sh.pb2[r] = BPT * i + t;
+                                    sh.pb2[r] = BPL * j + t;
                                     sh.pcc2[r] = cb;
                                     break;
                                 }
                             }
                         }
                     }
-                }
-                __syncthreads();
-                if (act && i == 0) {
-                    int32_t b1 = 0, b2 = sh.pb2[r];
-                    uint32_t ncand;
-                    bool slow;
-                    if (k_on) {
-                        ncand = sh.pcc2[r];
-                        slow = b2 >= nbu;
-                        sh.pma[r] = 0;
-                    } else {
-                        b1 = sh.pb1[r];
-                        slow = b1 >= nbu;
-                        const uint32_t c2b = b2 >= nbu ? cn_tot : sh.pcc2[r];
-                        if (b2 >= nbu) b2 = nbu - 1;
-                        ncand = c2b - sh.pcc1[r];
+                    group_barrier<PL>(r);
+                    if (j == 0) {
+                        int32_t b1 = 0, b2 = sh.pb2[r];
+                        uint32_t ncand;
+                        bool slow;
+                        if (k_on) {
+                            ncand = sh.pcc2[r];
+                            slow = b2 >= nbu;
+                            sh.pma[r] = 0;
+                        } else {
+                            b1 = sh.pb1[r];
+                            slow = b1 >= nbu;
+                            const uint32_t c2b = b2 >= nbu ? cn_tot : sh.pcc2[r];
+                            if (b2 >= nbu) b2 = nbu - 1;
+                            ncand = c2b - sh.pcc1[r];
+                        }
+                        if (ncand > static_cast<uint32_t>(NT) || ncand == 0) slow = true;
+                        sh.mode[r] = slow ? 2 : 1;
+                        sh.b1[r] = b1;
+                        sh.b2[r] = b2;
+                        sh.lcnt[r] = 0;
                     }
-                    if (ncand > static_cast<uint32_t>(NT) || ncand == 0) slow = true;
-                    sh.mode[r] = slow ? 2 : 1;
-                    sh.b1[r] = b1;
-                    sh.b2[r] = b2;
-                    sh.lcnt[r] = 0;
                 }
                 __syncthreads();
             }
