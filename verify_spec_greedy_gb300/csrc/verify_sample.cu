@@ -1445,10 +1445,20 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             };
             const int nvw = (nvr + NW - 1) / NW;  // vectors per warp
             const int w0 = warp * nvw, w1 = min(nvr, w0 + nvw);
+            // the vectors' weights, in the candidate and histogram storage (free by now)
+            uint32_t *wvec = reinterpret_cast<uint32_t *>(&sh.a);
+            static_assert(offsetof(Shared, b) == offsetof(Shared, a) + sizeof(Shared::a) &&
+                              sizeof(Shared::a) + sizeof(Shared::b) >= 4 * 6400,
+                          "the draw keeps up to 6400 vector weights in the storage of a and b");
 #pragma unroll 1
             for (int attempt = 0; attempt < 2; ++attempt) {
+                // each vector's weight is kept for the walk below
                 uint32_t acc = 0;
-                for (int v = w0 + lane; v < w1; v += 32) acc += vec_weight(v, -1);
+                for (int v = w0 + lane; v < w1; v += 32) {
+                    const uint32_t wvv = vec_weight(v, -1);
+                    wvec[v] = wvv;
+                    acc += wvv;
+                }
                 acc = __reduce_add_sync(0xFFFFFFFFu, acc);
                 if (lane == 0) sh.w.wsum[warp] = acc;
                 __syncthreads();
@@ -1496,56 +1506,71 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                             for (int wq = 0; wq + 1 < NW; ++wq) wb += sh.w.wsum[wq];
                         }
                         if (warp == ws) {
-                            // the vector that crosses the target, walking the warp's run in id
-                            // order; rem = tt - (weight before this warp's run)
+                            // the vector that crosses the target: each lane sums a stretch of
+                            // the warp's run (in id order) from the kept vector weights, a
+                            // scan finds the stretch, and its lane walks it; rem = tt - (weight
+                            // before this warp's run)
                             uint32_t rem = tt >= wb ? static_cast<uint32_t>(tt - wb) : 0u;
-                            int hit_v = -1, pos_v = -1;
-                            uint32_t hit_rem = 0;
-                            for (int v0 = w0; v0 < w1 && hit_v < 0; v0 += 32) {
-                                const int v = v0 + lane;
-                                const uint32_t own = v < w1 ? vec_weight(v, -1) : 0u;
-                                uint32_t incl = own;
+                            const int kq = (w1 - w0 + 31) / 32;
+                            const int a0 = min(w1, w0 + lane * kq), a1 = min(w1, a0 + kq);
+                            uint32_t sl = 0;
+                            for (int v = a0; v < a1; ++v) sl += wvec[v];
+                            uint32_t incl = sl;
 #pragma unroll
-                                for (int o = 1; o < 32; o <<= 1) {
-                                    const uint32_t yv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                                    if (lane >= o) incl += yv;
-                                }
-                                const unsigned hitm = __ballot_sync(0xFFFFFFFFu, own > 0 && incl > rem);
-                                const unsigned posm = __ballot_sync(0xFFFFFFFFu, own > 0);
-                                if (hitm) {
-                                    const int hl = __ffs(hitm) - 1;
-                                    hit_v = v0 + hl;
-                                    hit_rem = rem - __shfl_sync(0xFFFFFFFFu, incl - own, hl);
-                                } else if (posm) {
-                                    pos_v = v0 + 31 - __clz(posm);
-                                }
-                                rem -= __shfl_sync(0xFFFFFFFFu, incl, 31);
+                            for (int o = 1; o < 32; o <<= 1) {
+                                const uint32_t yv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                                if (lane >= o) incl += yv;
                             }
-                            // one lane walks that vector's elements, each weight once (the last
-                            // positive element of the run when rounding left no vector crossing)
-                            if (lane == 0) {
-                                const int fv = hit_v >= 0 ? hit_v : pos_v;
-                                if (fv >= 0) {
+                            const unsigned hitm = __ballot_sync(0xFFFFFFFFu, incl > rem);
+                            const unsigned posm = __ballot_sync(0xFFFFFFFFu, sl > 0);
+                            // the vector and the weight before it within the vector's stretch
+                            int fv = -1;
+                            uint32_t hit_rem = 0;
+                            const bool hit = hitm != 0;
+                            const int hl = hit ? __ffs(hitm) - 1 : (posm ? 31 - __clz(posm) : -1);
+                            if (hl >= 0 && lane == hl) {
+                                uint32_t cum = incl - sl;
+                                for (int v = a0; v < a1; ++v) {
+                                    const uint32_t wvv = wvec[v];
+                                    if (hit && cum + wvv > rem) {
+                                        fv = v;
+                                        hit_rem = rem - cum;
+                                        break;
+                                    }
+                                    if (wvv > 0) fv = v;  // the last positive vector
+                                    cum += wvv;
+                                }
+                            }
+                            if (hl >= 0) {
+                                fv = __shfl_sync(0xFFFFFFFFu, fv, hl);
+                                hit_rem = __shfl_sync(0xFFFFFFFFu, hit_rem, hl);
+                            }
+                            // its elements, one per lane: the first whose cumulative weight
+                            // exceeds hit_rem (the last positive one when nothing crossed)
+                            if (fv >= 0) {
+                                uint32_t we = 0;
+                                if (lane < EPV) {
                                     float x[EPV], y[EPV];
                                     unpack(sv0[fv], x);
                                     unpack(sv1[fv], y);
-                                    int fe = EPV - 1, le = 0;
-                                    uint32_t cum = 0;
-                                    for (int e = 0; e < EPV; ++e) {
-                                        uint32_t we = weight(x[e], y[e]);
-                                        // id 0 of a degenerate draft row carries no residual weight
-                                        if (deg1 && wmode == 0 && lo == 0 && fv == 0 && e == 0) we = 0u;
-                                        if (we > 0) le = e;
-                                        cum += we;
-                                        if (hit_v >= 0 && we > 0 && cum > hit_rem) {
-                                            fe = e;
-                                            break;
-                                        }
-                                    }
-                                    res->token = lo + fv * EPV + (hit_v >= 0 ? fe : le);
-                                } else {
-                                    res->token = lo;
+#pragma unroll
+                                    for (int e = 0; e < EPV; ++e)
+                                        if (e == lane) we = weight(x[e], y[e]);
+                                    // id 0 of a degenerate draft row carries no residual weight
+                                    if (deg1 && wmode == 0 && lo == 0 && fv == 0 && lane == 0) we = 0u;
                                 }
+                                uint32_t ce = we;
+#pragma unroll
+                                for (int o = 1; o < EPV; o <<= 1) {
+                                    const uint32_t yv = __shfl_up_sync(0xFFFFFFFFu, ce, o);
+                                    if (lane >= o) ce += yv;
+                                }
+                                const unsigned em = __ballot_sync(0xFFFFFFFFu, lane < EPV && we > 0 && ce > hit_rem);
+                                const unsigned pm = __ballot_sync(0xFFFFFFFFu, lane < EPV && we > 0);
+                                const int fe = (hit && em) ? __ffs(em) - 1 : (pm ? 31 - __clz(pm) : 0);
+                                if (lane == 0) res->token = lo + fv * EPV + fe;
+                            } else if (lane == 0) {
+                                res->token = lo;
                             }
                         }
                     }
@@ -1616,8 +1641,10 @@ static int64_t verify_slice(int64_t V, int C) {
 
 constexpr size_t kSmemLimit = 227u * 1024u;
 
-// Shared memory of a CTA for a slice of `slice` logits.
+// Shared memory of a CTA for a slice of `slice` logits (SIZE_MAX past the 6400 16-byte
+// vectors whose weights the draw keeps).
 static size_t verify_smem_bytes(int64_t slice, size_t es) {
+    if ((static_cast<size_t>(slice) * es + 15) / 16 > 6400u) return SIZE_MAX;
     const size_t head = (sizeof(vs::Shared) + 127) & ~static_cast<size_t>(127);
     const size_t row = ((static_cast<size_t>(slice) * es) + 127) & ~static_cast<size_t>(127);
     return head + 2 * row;
