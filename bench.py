@@ -53,6 +53,9 @@ def parse_args():
                     help="accepted for older command lines; launches are counted by the library")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's row count (profiling on a smaller case)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the verify and the draft-input calls alone on every workload "
+                         "(one JSON line each) instead of the benchmark step")
     return ap.parse_args()
 
 
@@ -382,8 +385,97 @@ def run_gpu(args, rank, world, dist):
     return res, x, di, w
 
 
+def run_sweep(args):
+    """Per workload: one verify call (spec_verify_greedy for a greedy workload, else
+    spec_verify_sample) and one mtp_draft_input call of its draft-token count, each timed
+    alone with CUDA events after an L2 flush (a write of twice the L2), median of the
+    launches; rows/s, tokens/s and the fraction of the roofline that bounds each."""
+    import numpy as np
+    import torch
+    import verify_spec_greedy_gb300 as lib
+    from verify_spec_greedy_gb300.inputs import WORKLOADS, make_draft_input, make_verify_inputs
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hbm, hbm_kind = measured_peaks()
+    tflops = 1881.1
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        tflops = float(json.load(open(pk)).get("bf16_tflops", tflops))
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(n):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    for name, w in WORKLOADS.items():
+        x = make_verify_inputs(w)
+        di = make_draft_input(w)
+        B, D, V = x["B"], x["D"], x["V"]
+        T, Q, d = to_dev(x["T"]), to_dev(x["Q"]), to_dev(x["d"])
+        out = torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+        na = torch.empty(B, dtype=torch.int32, device=dev)
+        if w.mode == "greedy":
+            vfn = lambda: lib.spec_verify_greedy(T, d, out, na)
+            vbytes = B * (D + 1) * V * (4 if x["dtype"] == "f32" else 2)
+            vcall = "spec_verify_greedy"
+        else:
+            tau, top_p = to_dev(x["tau"]), to_dev(x["top_p"])
+            top_k = to_dev(x["top_k"]) if (x["top_k"] > 0).any() else None
+            ws = torch.empty(lib.spec_verify_workspace_bytes(B, D, V), dtype=torch.uint8, device=dev)
+            vfn = lambda: lib.spec_verify_sample(T, Q, d, tau, top_k, top_p, x["seed"], out, na,
+                                                 None, None, ws)
+            vbytes = verify_bytes(x)
+            vcall = "spec_verify_sample"
+        vms = timed(vfn, 20)
+        M, H = w.tokens, w.H  # tokens of one draft-input call
+        e, h = to_dev(di["e"][0][:M]), to_dev(di["h"][0][:M])
+        we, wh, W = to_dev(di["we"]), to_dev(di["wh"]), to_dev(di["W"])
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        wsd = torch.empty(max(1, lib.mtp_draft_input_workspace_bytes(M, H)), dtype=torch.uint8, device=dev)
+        dms = timed(lambda: lib.mtp_draft_input(e, h, we, wh, W, y, di["eps"], wsd), 20)
+        dbytes = 2 * H * 2 * H + 2 * M * H * 2 + 2 * H * 2 + M * H * 2
+        dflop = 2.0 * M * H * 2 * H
+        tensor = dflop / dbytes > tflops * 1e12 / (hbm * 1e9)
+        if tensor:
+            droof = {"bound": "tensor", "achieved": round(dflop / (dms / 1e3) / 1e12, 1),
+                     "peak": tflops, "unit": "TFLOP/s"}
+        else:
+            droof = {"bound": "hbm", "achieved": round(dbytes / (dms / 1e3) / 1e9, 1),
+                     "peak": hbm, "unit": "GB/s"}
+        droof["frac"] = round(droof["achieved"] / droof["peak"], 4)
+        vach = vbytes / (vms / 1e3) / 1e9
+        print(json.dumps({
+            "sweep": name, "dtype": x["dtype"], "B": B, "D": D, "V": V, "H": H,
+            "verify": {"call": vcall, "ms": round(vms, 4),
+                       "rows_per_s": round(B * (D + 1) / (vms / 1e3), 1),
+                       "roofline": {"bound": "hbm", "achieved": round(vach, 1), "peak": hbm,
+                                    "unit": "GB/s", "frac": round(vach / hbm, 4),
+                                    "bytes": vbytes}},
+            "draft_input": {"M": M, "calls_per_step": w.draft_steps, "ms": round(dms, 4),
+                            "tokens_per_s": round(M / (dms / 1e3), 1), "roofline": droof},
+            "peaks": hbm_kind}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        return run_sweep(args)
     rank, world, dist = dist_init(args.gpus)
     if args.impl == "reference":
         if rank != 0:
