@@ -11,6 +11,8 @@
 // warps read the accumulator with tcgen05.ld and store bf16 (or fp32 partial sums when the
 // K range is split across CTAs, reduced by a second kernel).  Every mbarrier wait is
 // bounded; a wait that gives up sets a flag word in the workspace and the CTA drains out.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -312,16 +314,35 @@ struct GemmPlan {
     int BN, splits, kb_per_split, kb_total, o_tiles, t_tiles;
 };
 
+// SMs of a GB300; the plan depends on the sizes alone, so that the workspace query (which
+// needs no GPU) and the launch agree.
+constexpr int kPlanSMs = 152;
+
+// Tile widths and K splits.  Up to 256 tokens, one token tile (the narrowest width that
+// holds them): the weight, the bulk of the bytes, is streamed once.  Beyond, the width of
+// 128, 192 or 256 whose tiles fill the SMs in the fewest waves of the least work (waves x
+// width).  Then K is split so that the grid fills one wave, keeping >= 8 K-blocks a split.
 static GemmPlan plan_gemm(int64_t H, int64_t Mt, int64_t K) {
     GemmPlan g;
-    g.BN = Mt <= 16 ? 16 : (Mt <= 32 ? 32 : (Mt <= 64 ? 64 : (Mt <= 128 ? 128 : 256)));
     g.o_tiles = static_cast<int>((H + tg::BM - 1) / tg::BM);
-    g.t_tiles = static_cast<int>((Mt + g.BN - 1) / g.BN);
     g.kb_total = static_cast<int>((K + tg::BK - 1) / tg::BK);
+    if (Mt <= 256) {
+        g.BN = Mt <= 16 ? 16 : (Mt <= 32 ? 32 : (Mt <= 64 ? 64 : (Mt <= 128 ? 128 : (Mt <= 192 ? 192 : 256))));
+    } else {
+        int64_t best = -1;
+        for (int bn : {256, 192, 128}) {
+            const int64_t tiles = g.o_tiles * ((Mt + bn - 1) / bn);
+            const int64_t cost = ((tiles + kPlanSMs - 1) / kPlanSMs) * bn;
+            if (best < 0 || cost < best) {
+                best = cost;
+                g.BN = bn;
+            }
+        }
+    }
+    g.t_tiles = static_cast<int>((Mt + g.BN - 1) / g.BN);
     const int tiles = g.o_tiles * g.t_tiles;
-    int splits = 1;
-    // split K until the grid covers the 148+ SMs, keeping >= 8 K-blocks per split
-    while (tiles * splits < 148 && g.kb_total / (splits * 2) >= 8) splits *= 2;
+    int splits = tiles >= kPlanSMs ? 1 : kPlanSMs / tiles;
+    splits = std::max(1, std::min(splits, g.kb_total / 8));
     g.kb_per_split = (g.kb_total + splits - 1) / splits;
     g.splits = (g.kb_total + g.kb_per_split - 1) / g.kb_per_split;
     return g;
@@ -369,6 +390,7 @@ cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, i
     case 32: e = launch_gemm<32, 8>(ma, mb, p, g, stream); break;
     case 64: e = launch_gemm<64, 6>(ma, mb, p, g, stream); break;
     case 128: e = launch_gemm<128, 5>(ma, mb, p, g, stream); break;
+    case 192: e = launch_gemm<192, 5>(ma, mb, p, g, stream); break;
     default: e = launch_gemm<256, 4>(ma, mb, p, g, stream); break;
     }
     if (e != cudaSuccess || g.splits == 1) return e;
