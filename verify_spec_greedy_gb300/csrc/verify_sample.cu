@@ -1492,19 +1492,20 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                         for (uint32_t c = 0; c + 1 < C; ++c) before += dR[c];
                     }
                     if (rank == cs) {
-                        int ws = NW - 1;
-                        unsigned long long wb = before;
-                        for (int wq = 0; wq < NW; ++wq) {
-                            if (wb + sh.w.wsum[wq] > tt) {
-                                ws = wq;
-                                break;
-                            }
-                            wb += sh.w.wsum[wq];
+                        // the warp holding it (the last one when rounding left none crossing)
+                        // and the weight before its run: every warp scans the warps' sums,
+                        // lane w holding warp w's
+                        const unsigned long long dw = lane < NW ? sh.w.wsum[lane] : 0ull;
+                        unsigned long long iw = dw;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, iw, o);
+                            if (lane >= o) iw += y;
                         }
-                        if (ws == NW - 1) {
-                            wb = before;
-                            for (int wq = 0; wq + 1 < NW; ++wq) wb += sh.w.wsum[wq];
-                        }
+                        iw += before;
+                        const unsigned wm = __ballot_sync(0xFFFFFFFFu, lane < NW && iw > tt);
+                        const int ws = wm ? __ffs(wm) - 1 : NW - 1;
+                        const unsigned long long wb = __shfl_sync(0xFFFFFFFFu, iw - dw, ws);
                         if (warp == ws) {
                             // the vector that crosses the target: each lane sums a stretch of
                             // the warp's run (in id order) from the kept vector weights, a
