@@ -164,16 +164,19 @@ def filter_probs(x, tau: float, k: int = 0, p: float = 1.0, with_margin: bool = 
 def verify_sample(T, Q, d, tau, top_k=None, top_p=None, seed: int = 0, row0: int = 0):
     """Speculative-sampling verification of B rows.
 
-    T [B, D+1, V], Q [B, D, V] (fp32, or bf16 bits as uint16), d [B, D] int32,
+    T [B, D+1, V], Q [B, D, V] (fp32, or bf16 bits as uint16) or None (a one-hot draft:
+    the drafter's distribution is the point mass on its token), d [B, D] int32,
     tau [B] float32, top_k [B] int32 or None, top_p [B] float32 or None.
     Returns a dict: out, num_accepted, p_target, p_draft, status, margins [B, D+1, 4].
     """
     x, dt = _logits(T)
-    q, dq = _logits(Q)
-    assert dt == dq
     B, D1, V = x.shape
     D = D1 - 1
-    assert q.shape == (B, D, V)
+    q = None
+    if Q is not None:
+        q, dq = _logits(Q)
+        assert dt == dq
+        assert q.shape == (B, D, V)
     d = np.ascontiguousarray(d, dtype=np.int32).reshape(B, D)
     tau = np.ascontiguousarray(tau, dtype=np.float32).reshape(B)
     tk = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32).reshape(B)
@@ -202,7 +205,7 @@ def verify_sample_rows(T, Q, d, tau, top_k=None, top_p=None, seed: int = 0, rows
     tau = np.asarray(tau, dtype=np.float32)
 
     def one(r):
-        return verify_sample(T[r:r + 1], Q[r:r + 1], d[r:r + 1], tau[r:r + 1],
+        return verify_sample(T[r:r + 1], None if Q is None else Q[r:r + 1], d[r:r + 1], tau[r:r + 1],
                              None if tk is None else tk[r:r + 1],
                              None if tp is None else tp[r:r + 1], seed=seed, row0=r)
 

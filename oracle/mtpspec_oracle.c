@@ -409,7 +409,9 @@ static int64_t orc_inverse_cdf(const double *w, int64_t V, double u, double *mar
  *          (from p_a when that residual is identically 0);
  *   a = D: the bonus token is drawn from p_D with U_smp(b, D).
  * tau_b = 0 makes row b greedy (orc_verify_greedy's rule).  top_k / top_p may be NULL
- * (off).  row0 offsets the Philox row counter (the rows passed are rows row0.. of a
+ * (off).  Q may be NULL: a one-hot draft, q_j the point mass on d_j (a greedy drafter),
+ * so that d_j is accepted iff U_acc <= p_j(d_j), q_j(d_j) = 1, and the residual is p_a
+ * with d_a removed.  row0 offsets the Philox row counter (the rows passed are rows row0.. of a
  * larger batch).  out[B, D+1] (-1 padded), num_accepted[B]; p_target / p_draft [B, D]
  * receive p_j(d_j), q_j(d_j).  margins (optional) [B, D+1, 4] receive per unit:
  * |U_acc - p/q|, the top-p margin of T, of Q, and the draw's inverse-CDF margin
@@ -425,7 +427,7 @@ int orc_verify_sample(const void *T, const void *Q, int dt, const int32_t *d, co
         return ORC_ERR_ARG;
     if (B == 0)
         return ORC_OK;
-    if (!T || !Q || !d || !tau || !out || !num_accepted)
+    if (!T || !d || !tau || !out || !num_accepted)
         return ORC_ERR_ARG;
     size_t es = dt == ORC_F32 ? 4 : 2;
     double *wp = (double *)malloc((size_t)V * sizeof(double) * 3);
@@ -442,7 +444,7 @@ int orc_verify_sample(const void *T, const void *Q, int dt, const int32_t *d, co
 
     for (int64_t b = 0; b < B && rc == ORC_OK; ++b) {
         const char *rowT = (const char *)T + (size_t)b * (size_t)(D + 1) * (size_t)V * es;
-        const char *rowQ = (const char *)Q + (size_t)b * (size_t)D * (size_t)V * es;
+        const char *rowQ = Q ? (const char *)Q + (size_t)b * (size_t)D * (size_t)V * es : NULL;
         double tb = (double)tau[b];
         int32_t kb = top_k ? top_k[b] : 0;
         double pb = top_p ? (double)top_p[b] : 1.0;
@@ -499,13 +501,26 @@ int orc_verify_sample(const void *T, const void *Q, int dt, const int32_t *d, co
             double Zp, Zq, mp, mq, xp, xq;
             rc = orc_filter_weights(rowT + (size_t)j * (size_t)V * es, dt, V, tb, kb, pb, wp, inp,
                                     &Zp, &xp, &mp);
-            if (rc == ORC_OK)
+            if (rc == ORC_OK && Q)
                 rc = orc_filter_weights(rowQ + (size_t)j * (size_t)V * es, dt, V, tb, kb, pb, wq,
                                         inq, &Zq, &xq, &mq);
             if (rc != ORC_OK)
                 break;
             int32_t dj = d[b * D + j];
             int valid = dj >= 0 && (int64_t)dj < V;
+            if (!Q) { /* one-hot draft: q_j = 1 at d_j, 0 elsewhere */
+                for (int64_t i = 0; i < V; ++i) {
+                    wq[i] = 0.0;
+                    inq[i] = 0;
+                }
+                if (valid) {
+                    wq[dj] = 1.0;
+                    inq[dj] = 1;
+                }
+                Zq = 1.0;
+                xq = 0.0;
+                mq = INFINITY;
+            }
             double pt = valid ? wp[dj] / Zp : 0.0;
             double pd = valid ? wq[dj] / Zq : 0.0;
             if (p_target)
@@ -524,7 +539,7 @@ int orc_verify_sample(const void *T, const void *Q, int dt, const int32_t *d, co
                  * underflow when both probabilities are tiny; a row of all -inf is a
                  * point mass, whose probability is exact */
                 double ratio;
-                if (xp == -INFINITY || xq == -INFINITY) {
+                if (!Q || xp == -INFINITY || xq == -INFINITY) {
                     ratio = pt / pd;
                 } else {
                     double xt = logit_at(rowT + (size_t)j * (size_t)V * es, dt, dj);

@@ -209,3 +209,53 @@ def test_all_negative_infinity_rows_are_point_masses_on_id_0():
     r = oracle.verify_sample(T2, Q2, np.zeros((N, 1), np.int32), np.ones(N, np.float32), seed=3)
     want = oracle.filter_probs(q, 1.0)[0]
     assert abs((r["num_accepted"] == 1).mean() - want) < 4.5 * np.sqrt(want * (1 - want) / N)
+
+
+def test_one_hot_mode_equals_point_mass_draft_rows():
+    # without draft logits the drafter's distribution is the point mass on its token: the
+    # same verification as draft rows of -inf but 0 at the token (same uniforms, same
+    # expressions), and q(d) = 1
+    rng = np.random.default_rng(21)
+    B, D, V = 40, 3, 300
+    T = (rng.standard_normal((B, D + 1, V)) * 2.0).astype(np.float32)
+    d = rng.integers(0, V, (B, D)).astype(np.int32)
+    # half the drafts are the target's argmax, so that some are held
+    am = T[:, :D, :].argmax(-1).astype(np.int32)
+    d = np.where(rng.random((B, D)) < 0.5, am, d).astype(np.int32)
+    Q = np.full((B, D, V), -np.inf, np.float32)
+    np.put_along_axis(Q, d[:, :, None], 0.0, axis=2)
+    tau = rng.uniform(0.5, 1.5, B).astype(np.float32)
+    tk = rng.choice([0, 5, 40], B).astype(np.int32)
+    tp = rng.choice([1.0, 0.9, 0.6], B).astype(np.float32)
+    a = oracle.verify_sample(T, Q, d, tau, tk, tp, seed=3)
+    b = oracle.verify_sample(T, None, d, tau, tk, tp, seed=3)
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["num_accepted"], b["num_accepted"])
+    np.testing.assert_array_equal(a["p_target"], b["p_target"])
+    np.testing.assert_array_equal(b["p_draft"], np.ones((B, D)))
+    assert 0 < (b["num_accepted"] > 0).sum() < B
+
+
+def test_one_hot_mode_lossless_and_acceptance():
+    # a fixed drafted token x: kept with probability p(x); the first emitted token follows
+    # p whatever x is (chi-square over 20,000 trials)
+    V, N = 16, 20000
+    rng = np.random.default_rng(31)
+    t = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    tau, k, p = float(np.float32(0.9)), 10, float(np.float32(0.9))  # as the verify sees them
+    P = oracle.filter_probs(t, tau, k, p)
+    x = int(np.argsort(-P)[1])    # a likely but not the likeliest token
+    T = np.ascontiguousarray(np.broadcast_to(np.stack([t, t]), (N, 2, V)))
+    r = oracle.verify_sample(T, None, np.full((N, 1), x, np.int32), np.full(N, tau, np.float32),
+                             np.full(N, k, np.int32), np.full(N, p, np.float32), seed=17)
+    acc = r["num_accepted"] == 1
+    assert abs(acc.mean() - P[x]) <= 4.5 * np.sqrt(P[x] * (1 - P[x]) / N)
+    assert _chi2_ok(np.bincount(r["out"][:, 0], minlength=V), P)
+    np.testing.assert_allclose(r["p_target"][:, 0], P[x], rtol=1e-12)
+    # an id outside the vocabulary is rejected and flagged; the token then follows p
+    r = oracle.verify_sample(T[:4000], None, np.full((4000, 1), V, np.int32),
+                             np.full(4000, tau, np.float32), np.full(4000, k, np.int32),
+                             np.full(4000, p, np.float32), seed=18)
+    assert r["status"] & oracle.STATUS_BAD_DRAFT_ID
+    assert (r["num_accepted"] == 0).all() and (r["p_draft"] == 0).all()
+    assert _chi2_ok(np.bincount(r["out"][:, 0], minlength=V), P)
