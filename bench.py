@@ -441,6 +441,15 @@ def run_sweep(args):
                                                  None, None, ws)
             vbytes = verify_bytes(x)
             vcall = "spec_verify_sample"
+            # the same rows with a one-hot draft (no draft logits are read)
+            ofn = lambda: lib.spec_verify_sample(T, None, d, tau, top_k, top_p, x["seed"], out,
+                                                 na, None, None, ws)
+            ob = vbytes - (B - int((x["tau"] == 0).sum())) * D * V * (4 if x["dtype"] == "f32" else 2)
+            oms = timed(ofn, 20)
+            oach = ob / (oms / 1e3) / 1e9
+            one_hot = {"ms": round(oms, 4), "rows_per_s": round(B * (D + 1) / (oms / 1e3), 1),
+                       "roofline": {"bound": "hbm", "achieved": round(oach, 1), "peak": hbm,
+                                    "unit": "GB/s", "frac": round(oach / hbm, 4), "bytes": ob}}
         vms = timed(vfn, 20)
         M, H = w.tokens, w.H  # tokens of one draft-input call
         e, h = to_dev(di["e"][0][:M]), to_dev(di["h"][0][:M])
@@ -466,6 +475,7 @@ def run_sweep(args):
                        "roofline": {"bound": "hbm", "achieved": round(vach, 1), "peak": hbm,
                                     "unit": "GB/s", "frac": round(vach / hbm, 4),
                                     "bytes": vbytes}},
+            "verify_one_hot": None if w.mode == "greedy" else one_hot,
             "draft_input": {"M": M, "calls_per_step": w.draft_steps, "ms": round(dms, 4),
                             "tokens_per_s": round(M / (dms / 1e3), 1), "roofline": droof},
             "peaks": hbm_kind}), flush=True)

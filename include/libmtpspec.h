@@ -153,8 +153,14 @@ int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draf
  * (b, j, 0, 0), each mapped to (2 * (word >> 9) + 1) * 2^-24.  A row with tau_b = 0 is
  * verified greedily as in spec_verify_greedy (reported p_target = [d_j == argmax],
  * p_draft = 1).
+ * draft_logits may be NULL: a one-hot draft, q_j the point mass on d_j (greedy guesses,
+ * [DL] "MTP speculative decoding" items 1 and 3: a guess is kept with its probability
+ * under p_j, otherwise the token is drawn from the other candidates).  Then d_j is
+ * accepted when it is in the support of p_j and U_acc(b, j) <= p_j(d_j), the residual is
+ * p_a with d_a removed, p_draft reports 1 (0 for an id outside [0, V)), and only the
+ * target logits are read.
  *
- *   target_logits  [B, D+1, V]     draft_logits [B, D, V] (same dtype)
+ *   target_logits  [B, D+1, V]     draft_logits [B, D, V] (same dtype) or NULL
  *   draft_ids      int32 [B, D]
  *   temperature    float [B]       0 => greedy row
  *   top_k          int32 [B] or NULL   <= 0 or >= V => off
@@ -165,9 +171,9 @@ int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draf
  *   workspace      >= spec_verify_workspace_bytes(B, D, V) bytes, 256-byte aligned;
  *                  no initial contents are needed
  *   status         int32 [1] or NULL
- *   B >= 0, 1 <= D <= 64, 1 <= V <= 407,552 (fp32) or 815,104 (bf16): a CTA of a cluster
- *   of at most 16 holds its slices of a target and a draft row in shared memory; a larger
- *   V returns MTPSPEC_ERR_SHAPE.
+ *   B >= 0, 1 <= D <= 64, 1 <= V <= 407,552 (fp32) or 815,104 (bf16), or with a one-hot
+ *   draft 652,288 (fp32) or 1,304,576 (bf16): a CTA of a cluster of at most 16 holds its
+ *   slices of the staged rows in shared memory; a larger V returns MTPSPEC_ERR_SHAPE.
  */
 int spec_verify_sample(const void *target_logits, const void *draft_logits, int dtype,
                        const int32_t *draft_ids, const float *temperature, const int32_t *top_k,

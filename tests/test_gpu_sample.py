@@ -35,10 +35,10 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
-def gpu_verify(x, T_dev=None, Q_dev=None):
+def gpu_verify(x, T_dev=None, Q_dev=None, one_hot=False):
     B, D = x["d"].shape
     T = _dev(x["T"]) if T_dev is None else T_dev
-    Q = _dev(x["Q"]) if Q_dev is None else Q_dev
+    Q = None if one_hot else (_dev(x["Q"]) if Q_dev is None else Q_dev)
     out = torch.full((B, D + 1), -9, dtype=torch.int32, device=DEV)
     na = torch.full((B,), -9, dtype=torch.int32, device=DEV)
     pt = torch.full((B, D), -1.0, dtype=torch.float32, device=DEV)
@@ -53,9 +53,9 @@ def gpu_verify(x, T_dev=None, Q_dev=None):
                 p_draft=pd.cpu().numpy(), status=int(st.item()))
 
 
-def oracle_verify(x, rows=None):
-    return oracle.verify_sample_rows(x["T"], x["Q"], x["d"], x["tau"], x.get("top_k"),
-                                     x.get("top_p"), x["seed"], rows=rows)
+def oracle_verify(x, rows=None, one_hot=False):
+    return oracle.verify_sample_rows(x["T"], None if one_hot else x["Q"], x["d"], x["tau"],
+                                     x.get("top_k"), x.get("top_p"), x["seed"], rows=rows)
 
 
 def compare(g, o, rows=None, label=""):
@@ -255,3 +255,40 @@ def test_cluster_sizes(C, monkeypatch):
                      philox_seed=20 + C)
         x = make_verify_inputs(w)
         compare(gpu_verify(x), oracle_verify(x), label=f"C={C} {dtype}")
+
+
+# ---------------------------------------------------------------- one-hot drafts
+
+def _greedy_half(x, rng):
+    """Half the drafts become the target's argmax, so that some of them are held."""
+    am = x["T"][:, :-1, :]
+    if am.dtype == np.uint16:
+        am = (am.astype(np.uint32) << 16).view(np.float32)
+    am = am.argmax(-1).astype(np.int32)
+    x["d"] = np.where(rng.random(x["d"].shape) < 0.5, am, x["d"]).astype(np.int32)
+    return x
+
+
+@pytest.mark.parametrize("V,D,dtype,tau,k,p", [
+    (17, 2, "f32", 0.7, 5, 0.9),
+    (4099, 3, "bf16", 0.9, 100, 0.6),
+    (40001, 4, "f32", 0.8, 2000, 0.9),
+    (151936, 3, "f32", 1.0, 0, 0.9),
+    (262147, 2, "bf16", 1.0, 64, 0.95),
+])
+def test_one_hot_draft_mode(V, D, dtype, tau, k, p):
+    # no draft logits: each draft is the point mass on its token
+    w = Workload(name="oh", B=8 if V > 60000 else 24, D=D, V=V, H=8, dtype=dtype, tau=tau,
+                 top_k=k, top_p=p, t_std=3.0, q_noise=1.0, seed=V + 7, philox_seed=V + 1)
+    x = _greedy_half(make_verify_inputs(w), np.random.default_rng(V))
+    g, o = gpu_verify(x, one_hot=True), oracle_verify(x, one_hot=True)
+    assert g["status"] == o["status"] == 0
+    compare(g, o, label=f"one-hot V={V} {dtype} k={k} p={p}")
+    if V < 60000:  # (over the large vocabularies even the argmax holds only a few percent)
+        assert (g["num_accepted"] > 0).any()
+
+
+def test_one_hot_draft_serving_mix():
+    w = WORKLOADS["serve_b256_d3_v152k"].scaled(B=64, seed=41, philox_seed=43)
+    x = _greedy_half(make_verify_inputs(w), np.random.default_rng(41))
+    compare(gpu_verify(x, one_hot=True), oracle_verify(x, one_hot=True), label="one-hot serve")

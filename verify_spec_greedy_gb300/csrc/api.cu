@@ -108,7 +108,7 @@ MTPSPEC_API int spec_verify_greedy(const void *target_logits, int dtype, const i
 
 MTPSPEC_API size_t spec_verify_workspace_bytes(int64_t B, int32_t D, int64_t V) {
     if (B <= 0 || D < 1 || D > kMaxD || V < 1 || V > kMaxV || B > kMaxRows) return 0;
-    if (!mtpspec::verify_fits(V, 2)) return 0;  // too large for either logit type
+    if (!mtpspec::verify_fits(V, 2, true)) return 0;  // too large for any logit type and mode
     return mtpspec::verify_workspace_bytes(B, D);
 }
 
@@ -121,10 +121,9 @@ MTPSPEC_API int spec_verify_sample(const void *target_logits, const void *draft_
                                    void *stream) {
     if (dtype != MTPSPEC_F32 && dtype != MTPSPEC_BF16) return MTPSPEC_ERR_DTYPE;
     if (B < 0 || D < 1 || D > kMaxD || V < 1 || V > kMaxV || B > kMaxRows) return MTPSPEC_ERR_SHAPE;
-    if (!mtpspec::verify_fits(V, elem_size(dtype))) return MTPSPEC_ERR_SHAPE;
+    if (!mtpspec::verify_fits(V, elem_size(dtype), draft_logits == nullptr)) return MTPSPEC_ERR_SHAPE;
     if (B == 0) return MTPSPEC_OK;
-    if (!target_logits || !draft_logits || !draft_ids || !temperature || !out_tokens ||
-        !num_accepted)
+    if (!target_logits || !draft_ids || !temperature || !out_tokens || !num_accepted)
         return MTPSPEC_ERR_ARG;
     const size_t es = elem_size(dtype);
     if (!aligned(target_logits, es) || !aligned(draft_logits, es) || !aligned(draft_ids, 4) ||
@@ -206,10 +205,9 @@ MTPSPEC_API int spec_verify_sample_static(const void *target_logits, const void 
     if (dtype != MTPSPEC_F32 && dtype != MTPSPEC_BF16) return MTPSPEC_ERR_DTYPE;
     if (B < 0 || D < 1 || D > kMaxD || V < 1 || V > kMaxV || B > kMaxRows) return MTPSPEC_ERR_SHAPE;
     if (B * (D + 1) > mtpspec::kStaticVerifyUnits) return MTPSPEC_ERR_SHAPE;
-    if (!mtpspec::verify_fits(V, elem_size(dtype))) return MTPSPEC_ERR_SHAPE;
+    if (!mtpspec::verify_fits(V, elem_size(dtype), draft_logits == nullptr)) return MTPSPEC_ERR_SHAPE;
     if (B == 0) return MTPSPEC_OK;
-    if (!target_logits || !draft_logits || !draft_ids || !temperature || !out_tokens ||
-        !num_accepted)
+    if (!target_logits || !draft_ids || !temperature || !out_tokens || !num_accepted)
         return MTPSPEC_ERR_ARG;
     const size_t es = elem_size(dtype);
     if (!aligned(target_logits, es) || !aligned(draft_logits, es) || !aligned(draft_ids, 4) ||

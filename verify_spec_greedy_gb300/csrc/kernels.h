@@ -61,7 +61,7 @@ cudaError_t run_verify_greedy_rows(const VerifySampleArgs &a, cudaStream_t strea
 size_t verify_workspace_bytes(int64_t B, int32_t D);
 
 // Whether one cluster's shared memory can hold a row of V logits of this element size.
-bool verify_fits(int64_t V, size_t elem_bytes);
+bool verify_fits(int64_t V, size_t elem_bytes, bool one_hot);
 
 cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream);
 

@@ -84,6 +84,7 @@ constexpr int RSN = NB + 32;
 constexpr int CAPT = RSN;        // candidate slots per row in a cluster (CAPT / C per CTA):
                                  // as many as the histograms they share storage with
 constexpr int NCH = 4;           // bulk-copy chunks per row
+constexpr int WVEC_SHARED = 6400;  // draw: vector weights kept in the shared state's storage
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr float FX = 2147483648.0f;  // 2^31: fixed-point scale of weights (weights <= 1)
 
@@ -496,8 +497,11 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     const size_t data_off = (sizeof(Shared) + 127) & ~static_cast<size_t>(127);
     const size_t row_bytes =
         ((static_cast<size_t>(P.slice) * sizeof(T)) + 127) & ~static_cast<size_t>(127);
+    // without draft logits (a one-hot draft) only the target row is staged; the draft row's
+    // slice then aliases it, so that reads of it stay in bounds (their values go unused)
+    const bool one_hot = P.Q == nullptr;
     auto sdat = [&](int row) -> T * {
-        return reinterpret_cast<T *>(smem_raw + data_off + row * row_bytes);
+        return reinterpret_cast<T *>(smem_raw + data_off + (one_hot ? 0 : row * row_bytes));
     };
 
     const uint32_t C = cluster_size();
@@ -568,7 +572,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     // once for unit (b, j), with a bulk copy of the 16-byte-aligned body of that chunk
     // one thread: ask L2 to fetch unit (b, j)'s slices ahead of their bulk copies
     auto prefetch_l2 = [&](int b, int j) {
-        for (int r = 0; r < (j < D ? 2 : 1); ++r) {
+        for (int r = 0; r < (j < D && !one_hot ? 2 : 1); ++r) {
             const T *src = row_ptr(b, j, r);
             if (nvb == 0 || (reinterpret_cast<uintptr_t>(src) & 15u) != 0) continue;
             for (int c = 0; c < NCH; ++c) {
@@ -583,7 +587,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     auto issue = [&](int b, int j, bool after_reads) {
         if (lane != 0 || warp >= 2 * NCH) return;
         const int r = warp / NCH, c = warp % NCH;
-        const int nrows = j < D ? 2 : 1;
+        const int nrows = j < D && !one_hot ? 2 : 1;
         const T *src = r < nrows ? row_ptr(b, j, r) : nullptr;
         const bool bulk = r < nrows && nvb > 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
         const int v0 = min(nvb, c * blk), v1 = min(nvb, (c + 1) * blk);
@@ -630,7 +634,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         const int b = cur.b, j = cur.j;
         const float tau = cur.tau, pp = cur.pp;
         const int32_t kk = cur.kk, d = cur.d;
-        const int nrows = j < D ? 2 : 1;
+        const int nrows = j < D && !one_hot ? 2 : 1;
         const bool k_on = kk >= 1 && kk < V;
         const bool p_on = pp < 1.0f;
         const float c2 = __fdiv_rn(1.44269504088896340736f, tau);
@@ -1380,7 +1384,14 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
 
         bool accept = false;
         float pt = 0.0f, pd = 0.0f;
-        if (j < D && dvalid) {
+        if (j < D && dvalid && one_hot) {
+            // the draft is the point mass on d: q(d) = 1, held iff U_acc <= p(d)
+            const float xt = sh.e1d[ep].x;
+            const bool in_p = deg0 ? d == 0 : xt >= th0;
+            pt = prob0(xt, d);
+            pd = 1.0f;
+            accept = in_p && u_acc <= pt;
+        } else if (j < D && dvalid) {
             const float2 xdv = sh.e1d[ep];
             const float xt = xdv.x, xq = xdv.y;
             const bool in_p = deg0 ? d == 0 : xt >= th0;
@@ -1415,9 +1426,13 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             if (rank == 0 && tid == 0) res->token = 0;
         } else if (draw) {
             int wmode = (j == D) ? 1 : 0;  // 0: max(0, p - q), 1: p
-            // a degenerate draft row is a point mass on id 0: q = 0 elsewhere, and at id 0
-            // the residual is p - 1 <= 0
-            const float thq = deg1 ? INFINITY : th1;
+            // a point-mass draft (a one-hot draft on d, or a degenerate draft row on id 0):
+            // q = 0 elsewhere, and at its id the residual is p - 1 <= 0
+            const bool qpoint = one_hot || deg1;
+            const float thq = qpoint ? INFINITY : th1;
+            const int pm = one_hot ? d : 0;  // the point's id
+            const bool pm_here = qpoint && pm >= lo && pm < lo + n;
+            const int pv = pm_here ? (pm - lo) / EPV : -1, pe = pm_here ? (pm - lo) - pv * EPV : 0;
             auto weight = [&](float xt, float xq) -> uint32_t {
                 if (!(xt >= th0)) return 0u;
                 float p = ex2(fmaf(xt, c2, nm0)) * iz0;
@@ -1439,17 +1454,25 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
 #pragma unroll
                 for (int e = 0; e < EPV; ++e)
                     if (e_only < 0 || e == e_only) s += weight(x[e], y[e]);
-                // id 0 of a degenerate draft row carries no residual weight
-                if (deg1 && wmode == 0 && lo == 0 && v == 0 && e_only <= 0) s -= weight(x[0], y[0]);
+                // the draft point's id carries no residual weight
+                if (wmode == 0 && v == pv && e_only < 0) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e)
+                        if (e == pe) s -= weight(x[e], y[e]);
+                }
                 return s;
             };
             const int nvw = (nvr + NW - 1) / NW;  // vectors per warp
             const int w0 = warp * nvw, w1 = min(nvr, w0 + nvw);
-            // the vectors' weights, in the candidate and histogram storage (free by now)
-            uint32_t *wvec = reinterpret_cast<uint32_t *>(&sh.a);
+            // the vectors' weights, in the candidate and histogram storage (free by now), or
+            // past the staged rows for larger slices
+            const int svecs = static_cast<int>((P.slice * static_cast<int64_t>(sizeof(T)) + 15) / 16);
+            uint32_t *wvec = svecs <= WVEC_SHARED
+                                 ? reinterpret_cast<uint32_t *>(&sh.a)
+                                 : reinterpret_cast<uint32_t *>(smem_raw + data_off + (one_hot ? 1 : 2) * row_bytes);
             static_assert(offsetof(Shared, b) == offsetof(Shared, a) + sizeof(Shared::a) &&
-                              sizeof(Shared::a) + sizeof(Shared::b) >= 4 * 6400,
-                          "the draw keeps up to 6400 vector weights in the storage of a and b");
+                              sizeof(Shared::a) + sizeof(Shared::b) >= 4 * WVEC_SHARED,
+                          "the draw keeps up to WVEC_SHARED vector weights in the storage of a and b");
 #pragma unroll 1
             for (int attempt = 0; attempt < 2; ++attempt) {
                 // each vector's weight is kept for the walk below
@@ -1557,8 +1580,8 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
 #pragma unroll
                                     for (int e = 0; e < EPV; ++e)
                                         if (e == lane) we = weight(x[e], y[e]);
-                                    // id 0 of a degenerate draft row carries no residual weight
-                                    if (deg1 && wmode == 0 && lo == 0 && fv == 0 && lane == 0) we = 0u;
+                                    // the draft point's id carries no residual weight
+                                    if (wmode == 0 && fv == pv && lane == pe) we = 0u;
                                 }
                                 uint32_t ce = we;
 #pragma unroll
@@ -1642,20 +1665,22 @@ static int64_t verify_slice(int64_t V, int C) {
 
 constexpr size_t kSmemLimit = 227u * 1024u;
 
-// Shared memory of a CTA for a slice of `slice` logits (SIZE_MAX past the 6400 16-byte
-// vectors whose weights the draw keeps).
-static size_t verify_smem_bytes(int64_t slice, size_t es) {
-    if ((static_cast<size_t>(slice) * es + 15) / 16 > 6400u) return SIZE_MAX;
+// Shared memory of a CTA for slices of `slice` logits of `rows` rows (2: target and draft;
+// 1: the target alone, for a one-hot draft), plus, past vs::WVEC_SHARED 16-byte vectors,
+// a region for the draw's vector weights (they fit the shared state below that).
+static size_t verify_smem_bytes(int64_t slice, size_t es, int rows) {
+    const size_t vecs = (static_cast<size_t>(slice) * es + 15) / 16;
     const size_t head = (sizeof(vs::Shared) + 127) & ~static_cast<size_t>(127);
     const size_t row = ((static_cast<size_t>(slice) * es) + 127) & ~static_cast<size_t>(127);
-    return head + 2 * row;
+    const size_t extra = vecs > static_cast<size_t>(vs::WVEC_SHARED) ? ((vecs * 4 + 127) & ~static_cast<size_t>(127)) : 0;
+    return head + static_cast<size_t>(rows) * row + extra;
 }
 
-// Smallest cluster size whose CTAs fit their slices of a target and a draft row in shared
-// memory (0: none up to MAXC).
-static int verify_cmin(int64_t V, size_t es) {
+// Smallest cluster size whose CTAs fit their slices of the staged rows in shared memory (0:
+// none up to MAXC).
+static int verify_cmin(int64_t V, size_t es, int rows) {
     for (int C = 2; C <= vs::MAXC; ++C)
-        if (verify_smem_bytes(verify_slice(V, C), es) <= kSmemLimit) return C;
+        if (verify_smem_bytes(verify_slice(V, C), es, rows) <= kSmemLimit) return C;
     return 0;
 }
 
@@ -1663,7 +1688,9 @@ size_t verify_workspace_bytes(int64_t B, int32_t D) {
     return static_cast<size_t>(B) * static_cast<size_t>(D + 1) * sizeof(vs::UnitResult);
 }
 
-bool verify_fits(int64_t V, size_t elem_bytes) { return verify_cmin(V, elem_bytes) > 0; }
+bool verify_fits(int64_t V, size_t elem_bytes, bool one_hot) {
+    return verify_cmin(V, elem_bytes, one_hot ? 1 : 2) > 0;
+}
 
 // Resident clusters of the persistent kernel for one configuration (cached).
 template <typename T>
@@ -1711,15 +1738,15 @@ constexpr int64_t kUnitFixedLogits = 5000;
 // units) units in flight, each taking time in proportion to kUnitFixedLogits + slice.
 // MTPSPEC_VERIFY_CLUSTER forces a size (any that fits, 2 to MAXC).
 template <typename T>
-static VerifyGeometry verify_geometry(int64_t V, int64_t units) {
+static VerifyGeometry verify_geometry(int64_t V, int64_t units, int rows) {
     VerifyGeometry gm = {0, 0};
-    const int Cmin = verify_cmin(V, sizeof(T));
+    const int Cmin = verify_cmin(V, sizeof(T), rows);
     if (Cmin == 0) return gm;
     int best = 0;
     double best_score = -1.0;
     for (int C = Cmin; C <= vs::MAXC; ++C) {
         const int64_t sl = verify_slice(V, C);
-        const size_t smem = verify_smem_bytes(sl, sizeof(T));
+        const size_t smem = verify_smem_bytes(sl, sizeof(T), rows);
         if (smem > kSmemLimit) continue;
         const int64_t a = std::min<int64_t>(resident_clusters<T>(C, smem), units);
         const double score = static_cast<double>(a) / static_cast<double>(kUnitFixedLogits + sl);
@@ -1751,11 +1778,12 @@ static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(vs::k_verify_rr<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    const VerifyGeometry gm = verify_geometry<T>(p.V, units);
+    const int rows = p.Q ? 2 : 1;
+    const VerifyGeometry gm = verify_geometry<T>(p.V, units, rows);
     if (gm.C == 0) return cudaErrorInvalidValue;
     const int C = gm.C;
     p.slice = gm.slice;
-    const size_t smem = verify_smem_bytes(p.slice, sizeof(T));
+    const size_t smem = verify_smem_bytes(p.slice, sizeof(T), rows);
     int64_t G = resident_clusters<T>(C, smem);
     if (G > units) G = units;
     p.G = static_cast<int32_t>(G);
