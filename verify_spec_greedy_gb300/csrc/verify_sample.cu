@@ -176,7 +176,6 @@ struct __align__(16) Shared {
     int32_t b1[2], b2[2], nbu[2];
     unsigned long long tgt[2];
     int32_t flags;    // bit 0: a bulk copy timed out; bit 1: an exchange timed out
-    int32_t pick[2];
     float fpick[2];
     // the unit after the next one (-1: none) and its parameters, found by one warp while
     // the current unit works
@@ -1071,204 +1070,319 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 }
                 xwait(XB_E3);
 
-                // ---- exact thresholds.  Warp 0, per row: the candidates' count (-1 when some
-                // CTA overflowed its slots, or with too many or none: then the exact search)
-                // and each CTA's offset in the row's list in CTA order
-                if (warp == 0) {
+                // ---- exact thresholds.  Every warp, per row (lane c holding CTA c's count):
+                // the candidates' number, the CTAs' offsets in the row's list, and whether
+                // the row can be ranked by its plan group (1 to PL candidates, no CTA over its
+                // slots)
+                uint32_t ccl[2], cpl[2];
+                int ncnt[2];
+                bool grp = true;
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const bool on = r < nrows && sh.mode[r] == 1;
-                        const uint32_t cc = on && lane < static_cast<int>(C) ? sh.ccnt[lane][r] : 0u;
-                        const bool over = __any_sync(0xFFFFFFFFu, cc > static_cast<uint32_t>(capc));
-                        uint32_t incl = cc;
+                for (int r = 0; r < 2; ++r) {
+                    const bool on = r < nrows && sh.mode[r] == 1;
+                    const uint32_t cc = on && lane < static_cast<int>(C) ? sh.ccnt[lane][r] : 0u;
+                    const bool over = __any_sync(0xFFFFFFFFu, cc > static_cast<uint32_t>(capc));
+                    uint32_t incl = cc;
 #pragma unroll
-                        for (int o = 1; o < 32; o <<= 1) {
-                            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                            if (lane >= o) incl += y;
-                        }
-                        if (lane < static_cast<int>(C)) sh.cpre[r][lane] = incl - cc;
-                        if (lane == 31)
-                            sh.ncr[r] = !on ? 0 : (over || incl > static_cast<uint32_t>(NT) || incl == 0) ? -1
-                                                                                                    : static_cast<int>(incl);
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                        if (lane >= o) incl += y;
                     }
+                    ccl[r] = cc;
+                    cpl[r] = incl - cc;
+                    ncnt[r] = static_cast<int>(__shfl_sync(0xFFFFFFFFu, incl, 31));
+                    if (on && (over || ncnt[r] == 0 || ncnt[r] > PL)) grp = false;
                 }
-                __syncthreads();
-                const int ncr[2] = {sh.ncr[0], sh.ncr[1]};
-                const unsigned long long MAr[2] = {sh.mode[0] == 1 ? sh.pma[0] : 0ull,
-                                                   nrows > 1 && sh.mode[1] == 1 ? sh.pma[1] : 0ull};
-                // candidate i of row r, counted over the CTAs' slots in CTA order
-                auto cand_at = [&](int r, int i) -> float {
-                    int c = 0;
-                    while (c + 1 < static_cast<int>(C) && i >= static_cast<int>(sh.cpre[r][c + 1])) ++c;
-                    return __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][c * capc + i - static_cast<int>(sh.cpre[r][c])] >> 32));
-                };
-                const bool small = ncr[0] <= NSMALL && (nrows < 2 || ncr[1] <= NSMALL);
-                if (small) {
-                    // both rows' candidates into contiguous lists, with their fixed-point weights
-                    for (int t = tid; t < 2 * CAPT; t += NT) {
-                        const int r = t >= CAPT ? 1 : 0, slot = t - r * CAPT;
-                        const int c = slot / capc, i = slot - c * capc;
-                        if (ncr[r] > 0 && c < static_cast<int>(C) && i < static_cast<int>(sh.ccnt[c][r])) {
-                            const int pos = r * NSMALL + static_cast<int>(sh.cpre[r][c]) + i;
-                            const float v = __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][slot] >> 32));
-                            sh.b.s.sval[pos] = v;
-                            reinterpret_cast<uint32_t *>(sh.b.s.skey)[pos] = fix31(ex2(fmaf(v, c2, sh.nmc[r])));
+                if (grp) {
+                    // ---- rank by counting in the plan's groups (PW warps a row): lane jj
+                    // fetches candidate jj and its fixed-point weight; then S lanes a
+                    // candidate sum the weight and number of the candidates strictly above
+                    // it; the row's reductions go through its group barrier
+                    const int r = warp / PW, jj = tid - r * PL;
+                    if (warp < 2 * PW && r < nrows && sh.mode[r] == 1) {
+                        const int nr = ncnt[r];
+                        const uint32_t cpr = r == 0 ? cpl[0] : cpl[1], ccr = r == 0 ? ccl[0] : ccl[1];
+                        // candidate jj's CTA: the last with candidates whose offset is <= jj
+                        int c = 0;
+                        for (int k = 1; k < static_cast<int>(C); ++k) {
+                            const uint32_t pk = __shfl_sync(0xFFFFFFFFu, cpr, k);
+                            const uint32_t ck = __shfl_sync(0xFFFFFFFFu, ccr, k);
+                            if (static_cast<uint32_t>(jj) >= pk && ck > 0u) c = k;
                         }
-                    }
-                    __syncthreads();
-                    // ---- rank by counting, both rows at once (threads [0, NSMALL) take row
-                    // 0, the rest row 1): for each candidate, the weight and number of the
-                    // candidates strictly above it, each counted by S consecutive lanes over
-                    // every S-th candidate; then block reductions
-                    const int r = tid / NSMALL, tt = tid - r * NSMALL;
-                    const int nr = r < nrows ? ncr[r] : -1;
-                    int p2 = 1;
-                    while (p2 < nr) p2 <<= 1;
-                    const int S = min(32, NSMALL / p2);
-                    const int i = tt / S, sub = tt - i * S;
-                    const bool real = nr > 0 && i < nr;
-                    const float *cv = sh.b.s.sval + r * NSMALL;
-                    const uint32_t *cw = reinterpret_cast<const uint32_t *>(sh.b.s.skey) + r * NSMALL;
-                    const float v = real ? cv[i] : -INFINITY;
-                    const uint32_t w = real ? cw[i] : 0u;
-                    unsigned long long sgt = 0;
-                    int cgt = 0;
-                    if (real) {
+                        const uint32_t pre_c = __shfl_sync(0xFFFFFFFFu, cpr, c);
+                        float *cv = sh.b.s.sval + r * PL;
+                        uint32_t *cw = reinterpret_cast<uint32_t *>(sh.b.s.skey) + r * PL;
+                        if (jj < nr) {
+                            const float vj = __uint_as_float(static_cast<uint32_t>(
+                                sh.a.cand[r][c * capc + jj - static_cast<int>(pre_c)] >> 32));
+                            cv[jj] = vj;
+                            cw[jj] = fix31(ex2(fmaf(vj, c2, sh.nmc[r])));
+                        }
+                        group_barrier<PL>(r);
+                        int p2 = 1;
+                        while (p2 < nr) p2 <<= 1;
+                        const int S = min(32, PL / p2);
+                        const int i = jj / S, sub = jj - i * S;
+                        const bool real = i < nr;
+                        const float v = real ? cv[i] : -INFINITY;
+                        const uint32_t w = real ? cw[i] : 0u;
+                        unsigned long long sgt = 0;
+                        int cgt = 0;
+                        if (real) {
 #pragma unroll 4
-                        for (int q = sub; q < nr; q += S) {
-                            const float vq = cv[q];
-                            if (vq > v) {
-                                sgt += cw[q];
-                                ++cgt;
-                            }
-                        }
-                    }
-                    for (int o = S >> 1; o > 0; o >>= 1) {
-                        sgt += __shfl_xor_sync(0xFFFFFFFFu, sgt, o);
-                        cgt += __shfl_xor_sync(0xFFFFFFFFu, cgt, o);
-                    }
-                    const bool lead = real && sub == 0;  // one lane per candidate contributes
-                    const bool kept_k = lead && (!k_on || cgt < kk);
-                    const unsigned long long MA = MAr[r < 2 ? r : 0];
-                    // reduction 1 (top-k with top-p): the weight of the top-k set
-                    unsigned long long tgt = 0;
-                    if (k_on && p_on) {
-                        const unsigned long long ws = warp_sum_u64(kept_k ? static_cast<unsigned long long>(w) : 0ull);
-                        if (lane == 0) sh.w.ct.w[warp] = ws;
-                        __syncthreads();
-                        unsigned long long zk = MA;
-                        for (int wq = 0; wq < NW / 2; ++wq) zk += sh.w.ct.w[r * (NW / 2) + wq];
-                        tgt = fx_target_fx(pp, zk);
-                        __syncthreads();
-                    } else if (p_on) {
-                        tgt = fx_target(pp, sh.Z[r < nrows ? r : 0]);
-                    }
-                    const bool kept = kept_k && (!p_on || MA + sgt < tgt);
-                    // reduction 2: the smallest kept value and the kept weight
-                    float vmin = kept ? v : INFINITY;
-                    unsigned long long wk = kept ? static_cast<unsigned long long>(w) : 0ull;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
-                        wk += __shfl_xor_sync(0xFFFFFFFFu, wk, o);
-                    }
-                    if (lane == 0) {
-                        sh.w.ct.v[warp] = vmin;
-                        sh.w.ct.w[warp] = wk;
-                    }
-                    __syncthreads();
-                    if (tt == 0 && nr > 0) {
-                        float th = INFINITY;
-                        unsigned long long zf = MA;
-                        for (int wq = 0; wq < NW / 2; ++wq) {
-                            th = fminf(th, sh.w.ct.v[r * (NW / 2) + wq]);
-                            zf += sh.w.ct.w[r * (NW / 2) + wq];
-                        }
-                        sh.theta[r] = th;
-                        sh.Z[r] = fx_to_float(zf);
-                    }
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr)
-                        if (rr < nrows && sh.mode[rr] == 1 && ncr[rr] < 0 && tid == 0) sh.mode[rr] = 2;
-                    __syncthreads();
-                } else {
-                    // ---- sort the candidates by value (descending) and scan, one row at a time
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        if (r >= nrows || sh.mode[r] != 1) continue;
-                        const int nc = ncr[r];
-                        if (nc < 0) {
-                            __syncthreads();
-                            if (tid == 0) sh.mode[r] = 2;
-                            __syncthreads();
-                            continue;
-                        }
-                        const unsigned long long MA = MAr[r];
-                        int P2 = 1;
-                        while (P2 < nc) P2 <<= 1;
-                        // bitonic sort of (value key, position), one key per thread; strides
-                        // below 32 exchange through shuffles, wider ones through shared memory
-                        unsigned long long key = 0ull;
-                        if (tid < nc)
-                            key = (static_cast<unsigned long long>(order_key(cand_at(r, tid))) << 32) |
-                                  static_cast<uint32_t>(tid);
-                        for (int kb = 2; kb <= P2; kb <<= 1) {
-                            for (int jb = kb >> 1; jb > 0; jb >>= 1) {
-                                unsigned long long other;
-                                if (jb >= 32) {
-                                    __syncthreads();
-                                    sh.b.s.skey[tid] = key;
-                                    __syncthreads();
-                                    other = sh.b.s.skey[tid ^ jb];
-                                } else {
-                                    other = __shfl_xor_sync(0xFFFFFFFFu, key, jb);
+                            for (int q = sub; q < nr; q += S) {
+                                if (cv[q] > v) {
+                                    sgt += cw[q];
+                                    ++cgt;
                                 }
-                                const bool lower = (tid & jb) == 0;
-                                const bool desc = (tid & kb) == 0;
-                                key = (lower == desc) ? max(key, other) : min(key, other);
                             }
                         }
-                        const bool real = tid < nc;
-                        const float v = real ? key_to_float(static_cast<uint32_t>(key >> 32)) : -INFINITY;
-                        const unsigned long long w =
-                            real ? static_cast<unsigned long long>(fix31(ex2(fmaf(v, c2, sh.nmc[r])))) : 0ull;
-                        __syncthreads();
-                        sh.b.s.sval[tid] = v;
-                        // top-k: the k-th largest value (no element lies above the candidates)
-                        if (k_on && tid == kk - 1) sh.fpick[r] = v;
-                        __syncthreads();
-                        const float thk = k_on ? sh.fpick[r] : -INFINITY;
-                        const unsigned long long wk = (real && v >= thk) ? w : 0ull;
-                        // weight strictly above each value: the exclusive prefix of the weights
-                        // at the first position of its tie group (sorted descending)
-                        const unsigned long long excl = block_excl_scan_u64(wk, sh.w.so.scan);
-                        const int32_t headpos = (tid == 0 || sh.b.s.sval[tid - 1] != v) ? tid : -1;
-                        const int32_t first = block_incl_max_i32(headpos, sh.w.so.scani);
-                        sh.b.s.skey[tid] = excl;
-                        const unsigned long long zk = MA + block_sum_u64(wk, sh.w.so.ru[r]);
-                        if (tid == 0) {
-                            sh.tgt[r] = k_on ? fx_target_fx(pp, zk) : fx_target(pp, sh.Z[r]);
+                        for (int o = S >> 1; o > 0; o >>= 1) {
+                            sgt += __shfl_xor_sync(0xFFFFFFFFu, sgt, o);
+                            cgt += __shfl_xor_sync(0xFFFFFFFFu, cgt, o);
                         }
-                        __syncthreads();
-                        const unsigned long long above = MA + sh.b.s.skey[first];
-                        const bool kept = real && v >= thk && (!p_on || above < sh.tgt[r]);
-                        int32_t lastk = kept ? tid : -1;
+                        const bool lead = real && sub == 0;  // one lane per candidate contributes
+                        const bool kept_k = lead && (!k_on || cgt < kk);
+                        const unsigned long long MA = sh.pma[r];
+                        unsigned long long tgt = 0;
+                        if (k_on && p_on) {
+                            // the top-p target within the top-k set
+                            const unsigned long long ws = warp_sum_u64(kept_k ? static_cast<unsigned long long>(w) : 0ull);
+                            if (lane == 0) sh.w.ct.w[warp] = ws;
+                            group_barrier<PL>(r);
+                            unsigned long long zk = MA;
+                            for (int q = 0; q < PW; ++q) zk += sh.w.ct.w[r * PW + q];
+                            tgt = fx_target_fx(pp, zk);
+                            group_barrier<PL>(r);
+                        } else if (p_on) {
+                            tgt = sh.tgt[r];
+                        }
+                        const bool kept = kept_k && (!p_on || MA + sgt < tgt);
+                        // the smallest kept value and the kept weight
+                        float vmin = kept ? v : INFINITY;
+                        unsigned long long wk = kept ? static_cast<unsigned long long>(w) : 0ull;
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1)
-                            lastk = max(lastk, __shfl_xor_sync(0xFFFFFFFFu, lastk, o));
-                        __syncthreads();
-                        if (lane == 0) sh.w.so.scani[warp] = lastk;
-                        __syncthreads();
-                        int32_t lk = -1;
-                        for (int wq = 0; wq < NW; ++wq) lk = max(lk, sh.w.so.scani[wq]);
-                        const float th = sh.b.s.sval[lk < 0 ? 0 : lk];  // the smallest kept value
-                        const unsigned long long zf =
-                            MA + block_sum_u64((real && v >= th) ? wk : 0ull, sh.w.so.ru[r]);
-                        if (tid == 0) {
+                        for (int o = 16; o > 0; o >>= 1) {
+                            vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
+                            wk += __shfl_xor_sync(0xFFFFFFFFu, wk, o);
+                        }
+                        if (lane == 0) {
+                            sh.w.ct.v[warp] = vmin;
+                            sh.w.ct.w[warp] = wk;
+                        }
+                        group_barrier<PL>(r);
+                        if (jj == 0) {
+                            float th = INFINITY;
+                            unsigned long long zf = MA;
+                            for (int q = 0; q < PW; ++q) {
+                                th = fminf(th, sh.w.ct.v[r * PW + q]);
+                                zf += sh.w.ct.w[r * PW + q];
+                            }
                             sh.theta[r] = th;
                             sh.Z[r] = fx_to_float(zf);
                         }
+                    }
+                    __syncthreads();
+                } else {
+                    // ---- exact thresholds.  Warp 0, per row: the candidates' count (-1 when some
+                    // CTA overflowed its slots, or with too many or none: then the exact search)
+                    // and each CTA's offset in the row's list in CTA order
+                    if (warp == 0) {
+    #pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            const bool on = r < nrows && sh.mode[r] == 1;
+                            const uint32_t cc = on && lane < static_cast<int>(C) ? sh.ccnt[lane][r] : 0u;
+                            const bool over = __any_sync(0xFFFFFFFFu, cc > static_cast<uint32_t>(capc));
+                            uint32_t incl = cc;
+    #pragma unroll
+                            for (int o = 1; o < 32; o <<= 1) {
+                                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                                if (lane >= o) incl += y;
+                            }
+                            if (lane < static_cast<int>(C)) sh.cpre[r][lane] = incl - cc;
+                            if (lane == 31)
+                                sh.ncr[r] = !on ? 0 : (over || incl > static_cast<uint32_t>(NT) || incl == 0) ? -1
+                                                                                                        : static_cast<int>(incl);
+                        }
+                    }
+                    __syncthreads();
+                    const int ncr[2] = {sh.ncr[0], sh.ncr[1]};
+                    const unsigned long long MAr[2] = {sh.mode[0] == 1 ? sh.pma[0] : 0ull,
+                                                       nrows > 1 && sh.mode[1] == 1 ? sh.pma[1] : 0ull};
+                    // candidate i of row r, counted over the CTAs' slots in CTA order
+                    auto cand_at = [&](int r, int i) -> float {
+                        int c = 0;
+                        while (c + 1 < static_cast<int>(C) && i >= static_cast<int>(sh.cpre[r][c + 1])) ++c;
+                        return __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][c * capc + i - static_cast<int>(sh.cpre[r][c])] >> 32));
+                    };
+                    const bool small = ncr[0] <= NSMALL && (nrows < 2 || ncr[1] <= NSMALL);
+                    if (small) {
+                        // both rows' candidates into contiguous lists, with their fixed-point weights
+                        for (int t = tid; t < 2 * CAPT; t += NT) {
+                            const int r = t >= CAPT ? 1 : 0, slot = t - r * CAPT;
+                            const int c = slot / capc, i = slot - c * capc;
+                            if (ncr[r] > 0 && c < static_cast<int>(C) && i < static_cast<int>(sh.ccnt[c][r])) {
+                                const int pos = r * NSMALL + static_cast<int>(sh.cpre[r][c]) + i;
+                                const float v = __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][slot] >> 32));
+                                sh.b.s.sval[pos] = v;
+                                reinterpret_cast<uint32_t *>(sh.b.s.skey)[pos] = fix31(ex2(fmaf(v, c2, sh.nmc[r])));
+                            }
+                        }
                         __syncthreads();
+                        // ---- rank by counting, both rows at once (threads [0, NSMALL) take row
+                        // 0, the rest row 1): for each candidate, the weight and number of the
+                        // candidates strictly above it, each counted by S consecutive lanes over
+                        // every S-th candidate; then block reductions
+                        const int r = tid / NSMALL, tt = tid - r * NSMALL;
+                        const int nr = r < nrows ? ncr[r] : -1;
+                        int p2 = 1;
+                        while (p2 < nr) p2 <<= 1;
+                        const int S = min(32, NSMALL / p2);
+                        const int i = tt / S, sub = tt - i * S;
+                        const bool real = nr > 0 && i < nr;
+                        const float *cv = sh.b.s.sval + r * NSMALL;
+                        const uint32_t *cw = reinterpret_cast<const uint32_t *>(sh.b.s.skey) + r * NSMALL;
+                        const float v = real ? cv[i] : -INFINITY;
+                        const uint32_t w = real ? cw[i] : 0u;
+                        unsigned long long sgt = 0;
+                        int cgt = 0;
+                        if (real) {
+    #pragma unroll 4
+                            for (int q = sub; q < nr; q += S) {
+                                const float vq = cv[q];
+                                if (vq > v) {
+                                    sgt += cw[q];
+                                    ++cgt;
+                                }
+                            }
+                        }
+                        for (int o = S >> 1; o > 0; o >>= 1) {
+                            sgt += __shfl_xor_sync(0xFFFFFFFFu, sgt, o);
+                            cgt += __shfl_xor_sync(0xFFFFFFFFu, cgt, o);
+                        }
+                        const bool lead = real && sub == 0;  // one lane per candidate contributes
+                        const bool kept_k = lead && (!k_on || cgt < kk);
+                        const unsigned long long MA = MAr[r < 2 ? r : 0];
+                        // reduction 1 (top-k with top-p): the weight of the top-k set
+                        unsigned long long tgt = 0;
+                        if (k_on && p_on) {
+                            const unsigned long long ws = warp_sum_u64(kept_k ? static_cast<unsigned long long>(w) : 0ull);
+                            if (lane == 0) sh.w.ct.w[warp] = ws;
+                            __syncthreads();
+                            unsigned long long zk = MA;
+                            for (int wq = 0; wq < NW / 2; ++wq) zk += sh.w.ct.w[r * (NW / 2) + wq];
+                            tgt = fx_target_fx(pp, zk);
+                            __syncthreads();
+                        } else if (p_on) {
+                            tgt = fx_target(pp, sh.Z[r < nrows ? r : 0]);
+                        }
+                        const bool kept = kept_k && (!p_on || MA + sgt < tgt);
+                        // reduction 2: the smallest kept value and the kept weight
+                        float vmin = kept ? v : INFINITY;
+                        unsigned long long wk = kept ? static_cast<unsigned long long>(w) : 0ull;
+    #pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
+                            wk += __shfl_xor_sync(0xFFFFFFFFu, wk, o);
+                        }
+                        if (lane == 0) {
+                            sh.w.ct.v[warp] = vmin;
+                            sh.w.ct.w[warp] = wk;
+                        }
+                        __syncthreads();
+                        if (tt == 0 && nr > 0) {
+                            float th = INFINITY;
+                            unsigned long long zf = MA;
+                            for (int wq = 0; wq < NW / 2; ++wq) {
+                                th = fminf(th, sh.w.ct.v[r * (NW / 2) + wq]);
+                                zf += sh.w.ct.w[r * (NW / 2) + wq];
+                            }
+                            sh.theta[r] = th;
+                            sh.Z[r] = fx_to_float(zf);
+                        }
+    #pragma unroll
+                        for (int rr = 0; rr < 2; ++rr)
+                            if (rr < nrows && sh.mode[rr] == 1 && ncr[rr] < 0 && tid == 0) sh.mode[rr] = 2;
+                        __syncthreads();
+                    } else {
+                        // ---- sort the candidates by value (descending) and scan, one row at a time
+    #pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            if (r >= nrows || sh.mode[r] != 1) continue;
+                            const int nc = ncr[r];
+                            if (nc < 0) {
+                                __syncthreads();
+                                if (tid == 0) sh.mode[r] = 2;
+                                __syncthreads();
+                                continue;
+                            }
+                            const unsigned long long MA = MAr[r];
+                            int P2 = 1;
+                            while (P2 < nc) P2 <<= 1;
+                            // bitonic sort of (value key, position), one key per thread; strides
+                            // below 32 exchange through shuffles, wider ones through shared memory
+                            unsigned long long key = 0ull;
+                            if (tid < nc)
+                                key = (static_cast<unsigned long long>(order_key(cand_at(r, tid))) << 32) |
+                                      static_cast<uint32_t>(tid);
+                            for (int kb = 2; kb <= P2; kb <<= 1) {
+                                for (int jb = kb >> 1; jb > 0; jb >>= 1) {
+                                    unsigned long long other;
+                                    if (jb >= 32) {
+                                        __syncthreads();
+                                        sh.b.s.skey[tid] = key;
+                                        __syncthreads();
+                                        other = sh.b.s.skey[tid ^ jb];
+                                    } else {
+                                        other = __shfl_xor_sync(0xFFFFFFFFu, key, jb);
+                                    }
+                                    const bool lower = (tid & jb) == 0;
+                                    const bool desc = (tid & kb) == 0;
+                                    key = (lower == desc) ? max(key, other) : min(key, other);
+                                }
+                            }
+                            const bool real = tid < nc;
+                            const float v = real ? key_to_float(static_cast<uint32_t>(key >> 32)) : -INFINITY;
+                            const unsigned long long w =
+                                real ? static_cast<unsigned long long>(fix31(ex2(fmaf(v, c2, sh.nmc[r])))) : 0ull;
+                            __syncthreads();
+                            sh.b.s.sval[tid] = v;
+                            // top-k: the k-th largest value (no element lies above the candidates)
+                            if (k_on && tid == kk - 1) sh.fpick[r] = v;
+                            __syncthreads();
+                            const float thk = k_on ? sh.fpick[r] : -INFINITY;
+                            const unsigned long long wk = (real && v >= thk) ? w : 0ull;
+                            // weight strictly above each value: the exclusive prefix of the weights
+                            // at the first position of its tie group (sorted descending)
+                            const unsigned long long excl = block_excl_scan_u64(wk, sh.w.so.scan);
+                            const int32_t headpos = (tid == 0 || sh.b.s.sval[tid - 1] != v) ? tid : -1;
+                            const int32_t first = block_incl_max_i32(headpos, sh.w.so.scani);
+                            sh.b.s.skey[tid] = excl;
+                            const unsigned long long zk = MA + block_sum_u64(wk, sh.w.so.ru[r]);
+                            if (tid == 0) {
+                                sh.tgt[r] = k_on ? fx_target_fx(pp, zk) : fx_target(pp, sh.Z[r]);
+                            }
+                            __syncthreads();
+                            const unsigned long long above = MA + sh.b.s.skey[first];
+                            const bool kept = real && v >= thk && (!p_on || above < sh.tgt[r]);
+                            int32_t lastk = kept ? tid : -1;
+    #pragma unroll
+                            for (int o = 16; o > 0; o >>= 1)
+                                lastk = max(lastk, __shfl_xor_sync(0xFFFFFFFFu, lastk, o));
+                            __syncthreads();
+                            if (lane == 0) sh.w.so.scani[warp] = lastk;
+                            __syncthreads();
+                            int32_t lk = -1;
+                            for (int wq = 0; wq < NW; ++wq) lk = max(lk, sh.w.so.scani[wq]);
+                            const float th = sh.b.s.sval[lk < 0 ? 0 : lk];  // the smallest kept value
+                            const unsigned long long zf =
+                                MA + block_sum_u64((real && v >= th) ? wk : 0ull, sh.w.so.ru[r]);
+                            if (tid == 0) {
+                                sh.theta[r] = th;
+                                sh.Z[r] = fx_to_float(zf);
+                            }
+                            __syncthreads();
+                        }
                     }
                 }
             }
@@ -1439,10 +1553,10 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 if (wmode == 0 && xq >= thq) p = fmaxf(p - ex2(fmaf(xq, c2, nm1)) * iz1, 0.0f);
                 return fix31(p);
             };
-            // the weight of vector v of the slice (of its element e_only alone when >= 0)
+            // the weight of vector v of the slice
             const uint4 *sv0 = reinterpret_cast<const uint4 *>(sdat(0));
             const uint4 *sv1 = reinterpret_cast<const uint4 *>(sdat(1));
-            auto vec_weight = [&](int v, int e_only) -> uint32_t {
+            auto vec_weight = [&](int v) -> uint32_t {
                 float x[EPV], y[EPV];
                 unpack(sv0[v], x);
                 float xm = x[0];
@@ -1453,9 +1567,9 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 uint32_t s = 0;
 #pragma unroll
                 for (int e = 0; e < EPV; ++e)
-                    if (e_only < 0 || e == e_only) s += weight(x[e], y[e]);
+                    s += weight(x[e], y[e]);
                 // the draft point's id carries no residual weight
-                if (wmode == 0 && v == pv && e_only < 0) {
+                if (wmode == 0 && v == pv) {
 #pragma unroll
                     for (int e = 0; e < EPV; ++e)
                         if (e == pe) s -= weight(x[e], y[e]);
@@ -1478,7 +1592,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 // each vector's weight is kept for the walk below
                 uint32_t acc = 0;
                 for (int v = w0 + lane; v < w1; v += 32) {
-                    const uint32_t wvv = vec_weight(v, -1);
+                    const uint32_t wvv = vec_weight(v);
                     wvec[v] = wvv;
                     acc += wvv;
                 }
