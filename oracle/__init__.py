@@ -71,6 +71,10 @@ def _load():
         lib.orc_draft_input.restype = C.c_int
         lib.orc_draft_input_at.argtypes = [p, p, p, p, p, i64, i64, dbl, p, p, i64, p]
         lib.orc_draft_input_at.restype = C.c_int
+        lib.orc_lm_head_logits.argtypes = [p, p, dbl, p, i64, i64, i64, p, i64, p, p]
+        lib.orc_lm_head_logits.restype = C.c_int
+        lib.orc_lm_head_greedy.argtypes = [p, p, dbl, p, i64, i64, i64, p, p]
+        lib.orc_lm_head_greedy.restype = C.c_int
         _lib = lib
         return lib
 
@@ -250,3 +254,40 @@ def draft_input_at(e, h, we, wh, W, eps: float, tok, col):
                                       float(eps), _ptr(tok), _ptr(col), tok.size, _ptr(y)),
            "draft_input_at")
     return y
+
+
+# ---------------------------------------------------------------- draft output layer
+
+def lm_head_logits(hidden, W, tok, norm_w=None, eps: float = 0.0, with_absdot: bool = False):
+    """Logits [len(tok), V] (float64) of the draft head's output layer for tokens `tok`:
+    hidden [M, H] and W [V, H] bf16 bits, norm_w [H] bf16 bits or None (no normalisation).
+    With `with_absdot`, also sum_k |W[v, k] x_k| per logit."""
+    hidden = np.ascontiguousarray(hidden, dtype=np.uint16)
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    nw = None if norm_w is None else np.ascontiguousarray(norm_w, dtype=np.uint16)
+    M, H = hidden.shape
+    V = W.shape[0]
+    if W.shape[1] != H:
+        raise ValueError("W must be [V, H]")
+    tok = np.ascontiguousarray(tok, dtype=np.int64)
+    lg = np.zeros((tok.size, V), np.float64)
+    ad = np.zeros((tok.size, V), np.float64) if with_absdot else None
+    _check(_load().orc_lm_head_logits(_ptr(hidden), _ptr(nw), float(eps), _ptr(W), M, H, V,
+                                      _ptr(tok), tok.size, _ptr(lg), _ptr(ad)), "lm_head_logits")
+    return (lg, ad) if with_absdot else lg
+
+
+def lm_head_greedy(hidden, W, norm_w=None, eps: float = 0.0):
+    """(ids int32 [M], max logit float64 [M]) of the greedy draft from the output layer."""
+    hidden = np.ascontiguousarray(hidden, dtype=np.uint16)
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    nw = None if norm_w is None else np.ascontiguousarray(norm_w, dtype=np.uint16)
+    M, H = hidden.shape
+    V = W.shape[0]
+    if W.shape[1] != H:
+        raise ValueError("W must be [V, H]")
+    ids = np.zeros(M, np.int32)
+    mx = np.zeros(M, np.float64)
+    _check(_load().orc_lm_head_greedy(_ptr(hidden), _ptr(nw), float(eps), _ptr(W), M, H, V,
+                                      _ptr(ids), _ptr(mx)), "lm_head_greedy")
+    return ids, mx

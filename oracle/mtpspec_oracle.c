@@ -687,3 +687,81 @@ int orc_draft_input_at(const uint16_t *e, const uint16_t *h, const uint16_t *we,
     free(x);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------ draft output layer [HB][ZH] */
+
+/* Logits of the draft head's output layer for selected tokens ([HB] "The draft head": the
+ * block's output goes through a normalisation and the output layer shared with the main
+ * model; [ZH] 二.1 shared_head shares the main model's lm_head, 三 stage 1
+ * compute_logits).  For token t = tok[i]: x = hidden[t] (bf16 [H]), replaced by its
+ * RMSNorm with norm_w (bf16 result, the input stage's rule) when norm_w is given;
+ * logits[i, v] = sum_k W[v, k] x_k in double for W [V, H] row-major (out x in, no bias).
+ * absdot (optional) [n, V] receives sum_k |W[v, k] x_k|, the scale of the rounding error
+ * a lower-precision sum of the same products can make. */
+int orc_lm_head_logits(const uint16_t *hidden, const uint16_t *norm_w, double eps,
+                       const uint16_t *W, int64_t M, int64_t H, int64_t V, const int64_t *tok,
+                       int64_t n, double *logits, double *absdot)
+{
+    if (M < 0 || H < 1 || V < 1 || n < 0 || !(eps >= 0.0) || (n > 0 && (!hidden || !W || !tok || !logits)))
+        return ORC_ERR_ARG;
+    double *x = (double *)malloc((size_t)H * sizeof(double));
+    if (!x)
+        return ORC_ERR_NOMEM;
+    for (int64_t i = 0; i < n; ++i) {
+        if (tok[i] < 0 || tok[i] >= M) {
+            free(x);
+            return ORC_ERR_ARG;
+        }
+        const uint16_t *h = hidden + tok[i] * H;
+        if (norm_w)
+            orc_rmsnorm_bf16(h, norm_w, H, eps, x);
+        else
+            for (int64_t k = 0; k < H; ++k)
+                x[k] = bf16_bits_to_double(h[k]);
+        for (int64_t v = 0; v < V; ++v) {
+            const uint16_t *wrow = W + v * H;
+            double acc = 0.0, aacc = 0.0;
+            for (int64_t k = 0; k < H; ++k) {
+                double pr = bf16_bits_to_double(wrow[k]) * x[k];
+                acc += pr;
+                aacc += fabs(pr);
+            }
+            logits[i * V + v] = acc;
+            if (absdot)
+                absdot[i * V + v] = aacc;
+        }
+    }
+    free(x);
+    return ORC_OK;
+}
+
+/* The greedy draft from the output layer ([HB] "The draft head" and the greedy loop: the
+ * draft is the argmax of the draft logits; [DL] "Why a hand-written decoding loop": argmax
+ * takes the lower id on ties; [ZH] 三 stage 1 greedy sample): ids[t] = the lowest v with
+ * the largest logit of token t, for every token; maxv (optional) = that logit. */
+int orc_lm_head_greedy(const uint16_t *hidden, const uint16_t *norm_w, double eps,
+                       const uint16_t *W, int64_t M, int64_t H, int64_t V, int32_t *ids,
+                       double *maxv)
+{
+    if (M < 0 || H < 1 || V < 1 || V > 2147483647 || (M > 0 && !ids))
+        return ORC_ERR_ARG;
+    double *lg = (double *)malloc((size_t)V * sizeof(double));
+    if (!lg)
+        return ORC_ERR_NOMEM;
+    for (int64_t t = 0; t < M; ++t) {
+        int rc = orc_lm_head_logits(hidden, norm_w, eps, W, M, H, V, &t, 1, lg, NULL);
+        if (rc != ORC_OK) {
+            free(lg);
+            return rc;
+        }
+        int64_t best = 0;
+        for (int64_t v = 1; v < V; ++v)
+            if (lg[v] > lg[best])
+                best = v;
+        ids[t] = (int32_t)best;
+        if (maxv)
+            maxv[t] = lg[best];
+    }
+    free(lg);
+    return ORC_OK;
+}

@@ -184,3 +184,19 @@ def make_greedy_draft_logits(w: Workload, rows: int | None = None) -> np.ndarray
     rng = np.random.default_rng(w.seed + 2000)
     rows = w.tokens if rows is None else rows
     return _store(_normal(rng, (rows, w.V), w.t_std), w.dtype)
+
+
+def make_lm_head_input(M: int, H: int, V: int, seed: int, w_std: float = 0.02,
+                       hidden_std: float = 1.0, norm_w_std: float = 0.1) -> dict:
+    """The draft head's output layer: hidden states [M, H] ~ N(0, hidden_std), the final
+    norm weight [H] ~ 1 + N(0, norm_w_std) and the output-layer weight [V, H] ~ N(0, w_std),
+    all as bf16 bits (random stand-ins for the shared lm_head)."""
+    rng = np.random.default_rng(seed)
+    hidden = f32_to_bf16_bits(_normal(rng, (M, H), hidden_std))
+    norm_w = f32_to_bf16_bits(1.0 + _normal(rng, (H,), norm_w_std))
+    W = np.empty((V, H), np.uint16)
+    step = max(1, (1 << 24) // max(H, 1))  # rows per chunk: bounded temporaries
+    for v0 in range(0, V, step):
+        v1 = min(V, v0 + step)
+        W[v0:v1] = f32_to_bf16_bits(_normal(rng, (v1 - v0, H), w_std))
+    return dict(hidden=hidden, norm_w=norm_w, W=W, M=M, H=H, V=V, eps=1e-6)
