@@ -107,6 +107,41 @@ size_t mtp_draft_input_workspace_bytes(int64_t M, int64_t H);
 int mtp_greedy_draft(const void *logits, int dtype, int64_t M, int64_t V, int32_t *out_ids,
                      void *stream);
 
+/*
+ * mtp_lm_head_greedy — the greedy draft straight from the draft head's output layer,
+ * without writing the [M, V] logits ([HB] "The draft head": the block's output passes a
+ * normalisation and the output layer shared with the main model, and the draft is the
+ * argmax of those logits; [ZH] 二.1 shared_head = the main model's lm_head, 三 stage 1
+ * compute_logits then greedy sample).  For each of M tokens:
+ *     x        = hidden[t], or rmsnorm(hidden[t]) * norm_w rounded to bf16 when norm_w
+ *                is given (rmsnorm as in mtp_draft_input)
+ *     logits_v = sum_k lm_head_w[v, k] * x_k       (bf16 products, fp32 accumulation)
+ *     out_ids[t]   = the LOWEST v among the largest logits_v ([DL] "Why a hand-written
+ *                    decoding loop": argmax takes the lower id)
+ *     out_logit[t] = that largest logit (fp32), when out_logit is not NULL.
+ * The pick is made on the fp32 sums: where the two largest exact logits lie within the
+ * fp32 rounding of the sum, either id may come back.
+ *
+ *   hidden       bf16 [M, H]    the draft block's output (before the final norm when
+ *                               norm_w is given)
+ *   norm_w       bf16 [H] or NULL   final RMSNorm weight; eps >= 0 its epsilon
+ *   lm_head_w    bf16 [V, H]    row-major (vocabulary x hidden), as nn.Linear(H, V)
+ *   out_ids      int32 [M]      out_logit float [M] or NULL
+ *   workspace    >= mtp_lm_head_greedy_workspace_bytes(M, H, V) bytes, 256-byte aligned
+ *   status       int32 [1] or NULL   MTPSPEC_STATUS_TIMEOUT is OR-ed in if a wait of the
+ *                                    GEMM gave up (its ids are then unspecified)
+ *   M >= 0 (<= 2^20), 8 <= H <= 65536 with H % 8 == 0, 1 <= V <= 8,388,480.  hidden,
+ *   norm_w and lm_head_w 16-byte aligned.  Returns MTPSPEC_OK (also for M == 0, with
+ *   nothing enqueued) or an error as above.
+ */
+int mtp_lm_head_greedy(const void *hidden, const void *norm_w, float eps, const void *lm_head_w,
+                       int64_t M, int64_t H, int64_t V, int32_t *out_ids, float *out_logit,
+                       void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
+
+/* Bytes of device workspace mtp_lm_head_greedy needs for (M, H, V); 0 for arguments it
+ * would reject. */
+size_t mtp_lm_head_greedy_workspace_bytes(int64_t M, int64_t H, int64_t V);
+
 /* ------------------------------------------------------------------ greedy verification */
 
 /*

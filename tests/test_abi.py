@@ -33,6 +33,7 @@ def _declared():
 def test_header_declares_the_boundary():
     assert _declared() == sorted([
         "mtp_draft_input", "mtp_draft_input_workspace_bytes", "mtp_greedy_draft",
+        "mtp_lm_head_greedy", "mtp_lm_head_greedy_workspace_bytes",
         "spec_verify_greedy", "spec_verify_sample", "spec_verify_workspace_bytes",
         "spec_verify_sample_static", "mtpspec_status_string", "mtpspec_launch_count"])
 
@@ -77,6 +78,36 @@ def test_sampling_vocabulary_limit(so):
     # combination accepts
     assert so.spec_verify_workspace_bytes(1, 1, 1304576) > 0
     assert so.spec_verify_workspace_bytes(1, 1, 1304577) == 0
+
+
+def test_lm_head_greedy_host_checks(so):
+    nul = None
+    f = so.mtp_lm_head_greedy
+    ok = (C.c_void_p(256), nul, 1e-6, C.c_void_p(512), 4, 64, 1000, C.c_void_p(1024), nul,
+          C.c_void_p(4096), 1 << 20, nul, nul)
+    def call(**kw):
+        names = ["hidden", "norm_w", "eps", "W", "M", "H", "V", "ids", "logit", "ws", "wsb",
+                 "status", "stream"]
+        a = dict(zip(names, ok))
+        a.update(kw)
+        return f(*[a[n] for n in names])
+    assert call(H=12) == -3                      # H % 8
+    assert call(H=0) == -3
+    assert call(V=0) == -3
+    assert call(V=65535 * 128 + 1) == -3         # past the vocabulary tiles of one grid
+    assert call(M=-1) == -3
+    assert call(eps=-1.0) == -1
+    assert call(M=0) == 0                        # nothing to do
+    assert call(hidden=nul) == -1
+    assert call(W=C.c_void_p(520)) == -1         # not 16-byte aligned
+    assert call(ids=C.c_void_p(1026)) == -1
+    assert call(ws=nul) == -4
+    assert call(wsb=100) == -4
+    assert call(ws=C.c_void_p(4100)) == -4       # not 256-byte aligned
+    need = so.mtp_lm_head_greedy_workspace_bytes(4, 64, 1000)
+    assert need == 256 + 1024 + 4 * 8 * 8
+    assert so.mtp_lm_head_greedy_workspace_bytes(4, 12, 1000) == 0
+    assert so.mtp_lm_head_greedy_workspace_bytes(0, 64, 1000) == 0
 
 
 def test_launch_count_starts_at_zero_on_the_host(so):

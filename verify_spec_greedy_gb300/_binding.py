@@ -49,6 +49,8 @@ def load():
         "spec_verify_workspace_bytes": ([i64, i32, i64], sz),
         "spec_verify_sample_static": ([p, p, C.c_int, p, p, p, p, u64, i64, i32, i64, p, p, p, p,
                                        p, p], C.c_int),
+        "mtp_lm_head_greedy": ([p, p, f32, p, i64, i64, i64, p, p, p, sz, p, p], C.c_int),
+        "mtp_lm_head_greedy_workspace_bytes": ([i64, i64, i64], sz),
         "mtpspec_status_string": ([C.c_int], C.c_char_p),
         "mtpspec_launch_count": ([], C.c_uint64),
     }
@@ -119,6 +121,22 @@ def mtp_greedy_draft(logits, out_ids, stream=None):
     M, V = logits.shape
     _call("mtp_greedy_draft", _ptr(logits), _dtype_code(logits), M, V, _ptr(out_ids),
           _stream(stream))
+    return out_ids
+
+
+def mtp_lm_head_greedy_workspace_bytes(M: int, H: int, V: int) -> int:
+    return int(load().mtp_lm_head_greedy_workspace_bytes(int(M), int(H), int(V)))
+
+
+def mtp_lm_head_greedy(hidden, lm_head_w, out_ids, norm_w=None, eps: float = 0.0,
+                       out_logit=None, workspace=None, status=None, stream=None):
+    """out_ids[M] = argmax_v (lm_head_w @ x_t)_v, x_t = hidden[t] or its RMSNorm with norm_w
+    (bf16 hidden [M, H] and lm_head_w [V, H] on the GPU; lowest id on ties)."""
+    M, H = hidden.shape
+    V = lm_head_w.shape[0]
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _call("mtp_lm_head_greedy", _ptr(hidden), _ptr(norm_w), float(eps), _ptr(lm_head_w), M, H,
+          V, _ptr(out_ids), _ptr(out_logit), _ptr(workspace), ws, _ptr(status), _stream(stream))
     return out_ids
 
 

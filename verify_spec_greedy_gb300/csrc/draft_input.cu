@@ -154,7 +154,26 @@ k_draft_norm(const uint16_t *__restrict__ e, const uint16_t *__restrict__ h,
                      scratch);
 }
 
+// The output layer's normalisation: one CTA per token.
+__global__ void __launch_bounds__(256)
+k_head_norm(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w,
+            uint16_t *__restrict__ out, int H, float eps) {
+    __shared__ float scratch[8];
+    const size_t t = blockIdx.x;
+    rmsnorm_row<256>(x + t * H, w, H, eps, out + t * H, scratch);
+}
+
 }  // namespace di
+
+cudaError_t run_head_norm(const void *x, const void *w, void *out, int64_t M, int64_t H, float eps,
+                          cudaStream_t stream) {
+    di::k_head_norm<<<static_cast<unsigned>(M), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(w),
+        static_cast<uint16_t *>(out), static_cast<int>(H), eps);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
 
 constexpr int kGemvMaxTokens = 4;
 

@@ -94,3 +94,31 @@ cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, i
                              int64_t K, void *workspace, cudaStream_t stream);
 
 }  // namespace mtpspec
+
+namespace mtpspec {
+
+// The draft head's output layer with the greedy pick (lm_head.cu).
+struct LmHeadArgs {
+    const void *hidden;   // bf16 [M, H]
+    const void *norm_w;   // bf16 [H] or nullptr
+    float eps;
+    const void *W;        // bf16 [V, H]
+    int64_t M, H, V;
+    int32_t *ids;         // [M]
+    float *logit;         // [M] or nullptr
+    void *workspace;
+    int32_t *status;      // or nullptr
+};
+size_t lm_head_workspace_bytes(int64_t M, int64_t H, int64_t V);
+cudaError_t run_lm_head_greedy(const LmHeadArgs &a, cudaStream_t stream);
+
+// Pieces it is made of: the RMSNorm of each token's hidden state (draft_input.cu) and the
+// tcgen05 GEMM with the argmax epilogue (tcgen05_gemm.cu), which leaves one key
+// (order key << 32 | ~id) per (token, 128-row block of the vocabulary) in keys [Mt, o_tiles].
+cudaError_t run_head_norm(const void *x, const void *w, void *out, int64_t M, int64_t H, float eps,
+                          cudaStream_t stream);
+int lm_head_o_tiles(int64_t V);
+cudaError_t run_gemm_argmax(const void *W, const void *X, int64_t V, int64_t Mt, int64_t K,
+                            unsigned long long *keys, unsigned *err, cudaStream_t stream);
+
+}  // namespace mtpspec

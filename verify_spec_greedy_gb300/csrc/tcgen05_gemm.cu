@@ -11,6 +11,11 @@
 // warps read the accumulator with tcgen05.ld and store bf16 (or fp32 partial sums when the
 // K range is split across CTAs, reduced by a second kernel).  Every mbarrier wait is
 // bounded; a wait that gives up sets a flag word in the workspace and the CTA drains out.
+//
+// The same kernel with the argmax epilogue is the draft head's output layer with the
+// greedy pick: A = the output-layer weight [V, H], B = the tokens' hidden states [M, H];
+// the epilogue reduces each token's column of the 128 x BN logit tile to its largest
+// value and lowest id, so the logits never leave the SM.
 #include <algorithm>
 
 #include <cuda.h>
@@ -32,9 +37,10 @@ constexpr int A_BYTES = BM * BK * 2;
 struct Params {
     uint16_t *y;       // [Mt, H] bf16, when splits == 1
     float *part;       // [splits, Mt, H] fp32 partial sums, when splits > 1
-    unsigned *err;     // workspace flag word
-    int H, Mt, K;
-    int kb_total, kb_per_split, splits;
+    unsigned long long *keys;  // argmax epilogue: [Mt, o_tiles] (order key << 32 | ~id)
+    unsigned *err;     // flag word
+    int H, Mt, K;      // H: rows of A (output features, or the vocabulary)
+    int kb_total, kb_per_split, splits, o_tiles;
 };
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -125,7 +131,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool AM>
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
        const Params p) {
@@ -140,7 +146,10 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
     uint8_t *ring = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int o0 = blockIdx.x * BM, t0 = blockIdx.y * BN, split = blockIdx.z;
+    // the argmax grid runs the token tiles of one weight tile side by side (x fastest), so
+    // that the weight tile is read from HBM once and from L2 by the others
+    const int ob = AM ? blockIdx.y : blockIdx.x;
+    const int o0 = ob * BM, t0 = (AM ? blockIdx.x : blockIdx.y) * BN, split = blockIdx.z;
     const int kb0 = split * p.kb_per_split;
     const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
     const int nkb = max(0, kb1 - kb0);
@@ -210,7 +219,41 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
         }
         (void)ok;
         mma_commit(&accb);  // arrives once every MMA issued above has completed
-    } else if (warp >= 2) {
+    } else if (AM && warp >= 2) {
+        // ---- argmax epilogue: per token column, the warp's largest order key over its 32
+        // rows (redux max), then the lowest id holding it (redux min); the four warps'
+        // results meet in shared memory.  Rows past the vocabulary take key 0, below every
+        // value's key.
+        __shared__ unsigned long long red[4][BN];
+        const int q = warp & 3;
+        const bool ready = mbar_wait(&accb, 0);
+        tc_fence_after();
+        if (!ready) atomicOr(&abort_flag, 1);
+        const int o = o0 + q * 32 + lane;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        for (int c = 0; c < BN; c += 8) {
+            float v[8];
+            tmem_ld8(trow + c, v);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t key = (o < p.H && ready && nkb > 0) ? order_key(v[u]) : 0u;
+                const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, key);
+                const uint32_t omin =
+                    __reduce_min_sync(0xFFFFFFFFu, key == kmax ? static_cast<uint32_t>(o) : 0xFFFFFFFFu);
+                if (lane == u)
+                    red[q][c + u] = (static_cast<unsigned long long>(kmax) << 32) | (0xFFFFFFFFu - omin);
+            }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+        for (int c = threadIdx.x - 64; c < BN; c += 128) {
+            const int t = t0 + c;
+            if (t < p.Mt) {
+                const unsigned long long k =
+                    max(max(red[0][c], red[1][c]), max(red[2][c], red[3][c]));
+                p.keys[static_cast<size_t>(t) * p.o_tiles + ob] = k;
+            }
+        }
+    } else if (!AM && warp >= 2) {
         // ---- epilogue: TMEM lanes 32*(warp % 4) .. +31 are rows of this warp
         const int q = warp & 3;
         const bool ready = mbar_wait(&accb, 0);
@@ -354,15 +397,15 @@ size_t gemm_workspace_bytes(int64_t Mt, int64_t H) {
     return 256 + part;  // flag word, then the partial sums
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool AM = false>
 static cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const tg::Params &p,
                                const GemmPlan &g, cudaStream_t stream) {
     constexpr int smem = STAGES * (tg::A_BYTES + BN * tg::BK * 2) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(tg::k_gemm<BN, STAGES>,
+    cudaError_t e = cudaFuncSetAttribute(tg::k_gemm<BN, STAGES, AM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(g.o_tiles, g.t_tiles, g.splits);
-    tg::k_gemm<BN, STAGES><<<grid, tg::NTHREADS, smem, stream>>>(ma, mb, p);
+    const dim3 grid = AM ? dim3(g.t_tiles, g.o_tiles, 1) : dim3(g.o_tiles, g.t_tiles, g.splits);
+    tg::k_gemm<BN, STAGES, AM><<<grid, tg::NTHREADS, smem, stream>>>(ma, mb, p);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
@@ -374,7 +417,7 @@ cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, i
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, H, K, tg::BM) || !make_map(&mb, B, Mt, K, g.BN))
         return cudaErrorInvalidValue;
-    tg::Params p;
+    tg::Params p = {};
     p.y = static_cast<uint16_t *>(Y);
     p.err = static_cast<unsigned *>(workspace);
     p.part = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + 256);
@@ -408,6 +451,44 @@ cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, i
                            static_cast<uint16_t *>(Y), n, g.splits);
     if (e == cudaSuccess) count_launches(1);
     return e;
+}
+
+// The output layer's logits tile by tile with the argmax epilogue: keys [Mt, o_tiles], one
+// per (token, 128-row block of the vocabulary).  Up to 256 tokens, one token tile of the
+// narrowest width that holds them (the weight is streamed once); beyond, tiles of 256
+// tokens whose CTAs for one weight tile run side by side.  No K split.
+int lm_head_o_tiles(int64_t V) { return static_cast<int>((V + tg::BM - 1) / tg::BM); }
+
+cudaError_t run_gemm_argmax(const void *W, const void *X, int64_t V, int64_t Mt, int64_t K,
+                            unsigned long long *keys, unsigned *err, cudaStream_t stream) {
+    GemmPlan g;
+    g.o_tiles = lm_head_o_tiles(V);
+    g.kb_total = static_cast<int>((K + tg::BK - 1) / tg::BK);
+    g.BN = Mt <= 16 ? 16 : (Mt <= 32 ? 32 : (Mt <= 64 ? 64 : (Mt <= 128 ? 128 : (Mt <= 192 ? 192 : 256))));
+    g.t_tiles = static_cast<int>((Mt + g.BN - 1) / g.BN);
+    g.splits = 1;
+    g.kb_per_split = g.kb_total;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, W, V, K, tg::BM) || !make_map(&mb, X, Mt, K, g.BN))
+        return cudaErrorInvalidValue;
+    tg::Params p = {};
+    p.keys = keys;
+    p.err = err;
+    p.H = static_cast<int>(V);
+    p.Mt = static_cast<int>(Mt);
+    p.K = static_cast<int>(K);
+    p.kb_total = g.kb_total;
+    p.kb_per_split = g.kb_per_split;
+    p.splits = 1;
+    p.o_tiles = g.o_tiles;
+    switch (g.BN) {
+    case 16: return launch_gemm<16, 12, true>(ma, mb, p, g, stream);
+    case 32: return launch_gemm<32, 10, true>(ma, mb, p, g, stream);
+    case 64: return launch_gemm<64, 8, true>(ma, mb, p, g, stream);
+    case 128: return launch_gemm<128, 5, true>(ma, mb, p, g, stream);
+    case 192: return launch_gemm<192, 4, true>(ma, mb, p, g, stream);
+    default: return launch_gemm<256, 4, true>(ma, mb, p, g, stream);
+    }
 }
 
 }  // namespace mtpspec
