@@ -294,6 +294,175 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
     }
 }
 
+// OR of a predicate over the four epilogue warps (named barrier 1, 128 threads), which all
+// of them reach once per tile.
+__device__ __forceinline__ bool epi_vote_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v))
+        : "memory");
+    return r != 0;
+}
+
+// The argmax GEMM as a persistent kernel: CTA c takes tiles c, c + G, c + 2G, ... (tile i
+// = token tile i % t_tiles of vocabulary tile i / t_tiles, so the CTAs that share a weight
+// tile run together and read it from HBM once).  The accumulator is double-buffered in
+// tensor memory (2 x BN columns): the epilogue warps reduce tile j from one buffer while
+// the MMA warp accumulates tile j + 1 into the other, and the producer streams the next
+// tile's stages without a gap.  Barriers: the stage ring (full / empty, as in k_gemm),
+// accf[b] (MMA -> epilogue: buffer b holds a finished tile) and acce[b] (epilogue -> MMA:
+// buffer b has been read).  Every wait is bounded; a wait that gives up raises the CTA's
+// abort flag and every role leaves its loop.
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(NTHREADS, 1)
+k_gemm_argmax(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const Params p, int t_tiles, int n_tiles) {
+    constexpr int B_BYTES = BN * BK * 2;
+    constexpr int STAGE = A_BYTES + B_BYTES;
+    constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+    extern __shared__ uint8_t smem_dyn[];
+    __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], accf[2], acce[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int abort_flag;
+    __shared__ unsigned long long red[4][BN];
+
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x;
+    const int nkb = p.kb_total;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 4);  // lane 0 of each epilogue warp
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_map(&tmA);
+        prefetch_map(&tmB);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(&tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ---- producer: every tile's K-blocks through the ring, one global stage counter
+        int it = 0;
+        for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += G) {
+            const int o0 = (tile / t_tiles) * BM, t0 = (tile % t_tiles) * BN;
+            for (int i = 0; i < nkb; ++i, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u)) abort_flag = 1;
+                if (abort_flag) break;
+                uint8_t *a = ring + s * STAGE;
+                mbar_expect_tx(&full[s], STAGE);
+                tma_load_2d(a, &tmA, i * BK, o0, &full[s]);
+                tma_load_2d(a + A_BYTES, &tmB, i * BK, t0, &full[s]);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer: tile j accumulates into buffer j & 1 once the epilogue has read it
+        constexpr uint32_t idesc = instr_desc(BM, BN);
+        int it = 0, j = 0;
+        for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += G, ++j) {
+            const int b = j & 1;
+            if (!mbar_wait(&acce[b], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u)) {
+                abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t acc = tmem + static_cast<uint32_t>(b * BN);
+            for (int i = 0; i < nkb; ++i, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
+                if (!mbar_wait(&full[s], ph)) abort_flag = 1;
+                if (abort_flag) break;
+                tc_fence_after();
+                const uint32_t a = smem_addr(ring + s * STAGE);
+                const uint32_t bb = a + A_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / UK; ++k)
+                    mma_bf16(acc, smem_desc_sw128(a + k * 32), smem_desc_sw128(bb + k * 32), idesc,
+                             (i > 0 || k > 0) ? 1u : 0u);
+                mma_commit(&empty[s]);
+            }
+            if (abort_flag) break;
+            mma_commit(&accf[b]);  // arrives when this tile's MMAs have completed
+        }
+    } else if (warp >= 2) {
+        // ---- epilogue: per token column the largest order key over the tile's 128 rows and
+        // the lowest id holding it (redux in each warp, then across the four warps)
+        const int q = warp & 3;
+        int j = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += G, ++j) {
+            const int b = j & 1;
+            const int ob = tile / t_tiles, o0 = ob * BM, t0 = (tile % t_tiles) * BN;
+            // the four warps leave together or not at all (a named barrier would otherwise
+            // wait for a warp that has left); the vote is also the point after which the
+            // previous tile's red[] has been read
+            const bool bad = abort_flag || !mbar_wait(&accf[b], static_cast<uint32_t>(j >> 1) & 1u);
+            if (epi_vote_any(bad)) {
+                abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const int o = o0 + q * 32 + lane;
+            const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
+            for (int c = 0; c < BN; c += 8) {
+                float v[8];
+                tmem_ld8(trow + c, v);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t key = o < p.H ? order_key(v[u]) : 0u;
+                    const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, key);
+                    const uint32_t omin = __reduce_min_sync(
+                        0xFFFFFFFFu, key == kmax ? static_cast<uint32_t>(o) : 0xFFFFFFFFu);
+                    if (lane == u)
+                        red[q][c + u] = (static_cast<unsigned long long>(kmax) << 32) | (0xFFFFFFFFu - omin);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&acce[b])) : "memory");
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // red[] complete
+            for (int c = threadIdx.x - 64; c < BN; c += 128) {
+                const int t = t0 + c;
+                if (t < p.Mt)
+                    p.keys[static_cast<size_t>(t) * p.o_tiles + ob] =
+                        max(max(red[0][c], red[1][c]), max(red[2][c], red[3][c]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && abort_flag) atomicOr(p.err, MTPSPEC_STATUS_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
 // y = bf16(sum over splits of the fp32 partials), 4 outputs per thread.
 __global__ void k_split_reduce(const float *__restrict__ part, uint16_t *__restrict__ y,
                                int64_t n, int splits) {
@@ -453,6 +622,21 @@ cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, i
     return e;
 }
 
+template <int BN, int STAGES>
+static cudaError_t launch_gemm_argmax(const CUtensorMap &ma, const CUtensorMap &mb,
+                                      const tg::Params &p, int t_tiles, int n_tiles,
+                                      cudaStream_t stream) {
+    constexpr int smem = STAGES * (tg::A_BYTES + BN * tg::BK * 2) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(tg::k_gemm_argmax<BN, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = n_tiles < kPlanSMs ? n_tiles : kPlanSMs;  // persistent: one CTA per SM
+    tg::k_gemm_argmax<BN, STAGES><<<grid, tg::NTHREADS, smem, stream>>>(ma, mb, p, t_tiles, n_tiles);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
 // The output layer's logits tile by tile with the argmax epilogue: keys [Mt, o_tiles], one
 // per (token, 128-row block of the vocabulary).  Up to 256 tokens, one token tile of the
 // narrowest width that holds them (the weight is streamed once); beyond, tiles of 256
@@ -481,13 +665,14 @@ cudaError_t run_gemm_argmax(const void *W, const void *X, int64_t V, int64_t Mt,
     p.kb_per_split = g.kb_per_split;
     p.splits = 1;
     p.o_tiles = g.o_tiles;
+    const int n_tiles = g.o_tiles * g.t_tiles;
     switch (g.BN) {
-    case 16: return launch_gemm<16, 12, true>(ma, mb, p, g, stream);
-    case 32: return launch_gemm<32, 10, true>(ma, mb, p, g, stream);
-    case 64: return launch_gemm<64, 8, true>(ma, mb, p, g, stream);
-    case 128: return launch_gemm<128, 5, true>(ma, mb, p, g, stream);
-    case 192: return launch_gemm<192, 4, true>(ma, mb, p, g, stream);
-    default: return launch_gemm<256, 4, true>(ma, mb, p, g, stream);
+    case 16: return launch_gemm_argmax<16, 12>(ma, mb, p, g.t_tiles, n_tiles, stream);
+    case 32: return launch_gemm_argmax<32, 10>(ma, mb, p, g.t_tiles, n_tiles, stream);
+    case 64: return launch_gemm_argmax<64, 8>(ma, mb, p, g.t_tiles, n_tiles, stream);
+    case 128: return launch_gemm_argmax<128, 5>(ma, mb, p, g.t_tiles, n_tiles, stream);
+    case 192: return launch_gemm_argmax<192, 4>(ma, mb, p, g.t_tiles, n_tiles, stream);
+    default: return launch_gemm_argmax<256, 4>(ma, mb, p, g.t_tiles, n_tiles, stream);
     }
 }
 
