@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="time the verify and the draft-input calls alone on every workload "
                          "(one JSON line each) instead of the benchmark step")
+    ap.add_argument("--lm-head", type=int, nargs=3, metavar=("M", "H", "V"), default=None,
+                    help="time mtp_lm_head_greedy alone on seeded random inputs of this size "
+                         "(--warmup, then --steps calls, each after an L2 flush)")
     return ap.parse_args()
 
 
@@ -387,7 +390,8 @@ def run_gpu(args, rank, world, dist):
 
 def run_sweep(args):
     """Per workload: one verify call (spec_verify_greedy for a greedy workload, else
-    spec_verify_sample) and one mtp_draft_input call of its draft-token count, each timed
+    spec_verify_sample), one mtp_draft_input call of its draft-token count and one
+    mtp_lm_head_greedy call of one token per row, each timed
     alone with CUDA events after an L2 flush (a write of twice the L2), median of the
     launches; rows/s, tokens/s and the fraction of the roofline that bounds each."""
     import numpy as np
@@ -467,6 +471,34 @@ def run_sweep(args):
             droof = {"bound": "hbm", "achieved": round(dbytes / (dms / 1e3) / 1e9, 1),
                      "peak": hbm, "unit": "GB/s"}
         droof["frac"] = round(droof["achieved"] / droof["peak"], 4)
+        # the draft step's output layer with the greedy pick: one token per row, the
+        # workload's hidden size and vocabulary (seeded random stand-ins for the weights);
+        # beside it, the same pick through a cuBLAS product and torch.argmax, for context
+        Ml, Hl = B, H
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(w.seed + 77)
+        hl = torch.randn((Ml, Hl), device=dev, generator=gen).to(torch.bfloat16)
+        Wl = (torch.randn((V, Hl), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+        nl = (1.0 + 0.1 * torch.randn((Hl,), device=dev, generator=gen)).to(torch.bfloat16)
+        idl = torch.empty(Ml, dtype=torch.int32, device=dev)
+        wsl = torch.empty(lib.mtp_lm_head_greedy_workspace_bytes(Ml, Hl, V), dtype=torch.uint8, device=dev)
+        lms = timed(lambda: lib.mtp_lm_head_greedy(hl, Wl, idl, norm_w=nl, eps=1e-6, workspace=wsl), 20)
+
+        def lib_pick():
+            xf = hl.float()
+            xn = (xf * torch.rsqrt((xf * xf).mean(-1, keepdim=True) + 1e-6) * nl.float()).to(torch.bfloat16)
+            return torch.argmax(xn @ Wl.t(), dim=-1)
+        cms = timed(lib_pick, 10)
+        del Wl
+        lbytes = V * Hl * 2 + 2 * Ml * Hl * 2 + Hl * 2 + Ml * 4
+        lflop = 2.0 * Ml * Hl * V
+        if lflop / (tflops * 1e12) > lbytes / (hbm * 1e9):
+            lroof = {"bound": "tensor", "achieved": round(lflop / (lms / 1e3) / 1e12, 1),
+                     "peak": tflops, "unit": "TFLOP/s"}
+        else:
+            lroof = {"bound": "hbm", "achieved": round(lbytes / (lms / 1e3) / 1e9, 1),
+                     "peak": hbm, "unit": "GB/s"}
+        lroof["frac"] = round(lroof["achieved"] / lroof["peak"], 4)
         vach = vbytes / (vms / 1e3) / 1e9
         print(json.dumps({
             "sweep": name, "dtype": x["dtype"], "B": B, "D": D, "V": V, "H": H,
@@ -478,7 +510,49 @@ def run_sweep(args):
             "verify_one_hot": None if w.mode == "greedy" else one_hot,
             "draft_input": {"M": M, "calls_per_step": w.draft_steps, "ms": round(dms, 4),
                             "tokens_per_s": round(M / (dms / 1e3), 1), "roofline": droof},
+            "lm_head_greedy": {"M": Ml, "ms": round(lms, 4),
+                               "tokens_per_s": round(Ml / (lms / 1e3), 1), "roofline": lroof,
+                               "cublas_matmul_argmax_ms": round(cms, 4)},
             "peaks": hbm_kind}), flush=True)
+    return 0
+
+
+def run_lm_head(args):
+    """mtp_lm_head_greedy alone at (M, H, V): seeded random bf16 hidden states, final-norm
+    and output-layer weights; prints one JSON line with the median time per call."""
+    import numpy as np
+    import torch
+    import verify_spec_greedy_gb300 as lib
+    M, H, V = args.lm_head
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hbm, hbm_kind = measured_peaks()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+    h = torch.randn((M, H), device=dev, generator=gen).to(torch.bfloat16)
+    W = (torch.randn((V, H), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+    nw = (1.0 + 0.1 * torch.randn((H,), device=dev, generator=gen)).to(torch.bfloat16)
+    ids = torch.empty(M, dtype=torch.int32, device=dev)
+    ws = torch.empty(lib.mtp_lm_head_greedy_workspace_bytes(M, H, V), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(1, args.warmup)):
+        lib.mtp_lm_head_greedy(h, W, ids, norm_w=nw, eps=1e-6, workspace=ws)
+    ts = []
+    for _ in range(max(1, args.steps)):
+        flush.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        lib.mtp_lm_head_greedy(h, W, ids, norm_w=nw, eps=1e-6, workspace=ws)
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = float(np.median(ts))
+    nbytes = V * H * 2 + 2 * M * H * 2 + H * 2 + M * 4
+    print(json.dumps({"lm_head_greedy": {"M": M, "H": H, "V": V}, "ms": round(ms, 4),
+                      "tokens_per_s": round(M / (ms / 1e3), 1),
+                      "hbm_gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "hbm_peak": hbm,
+                      "tflops": round(2.0 * M * H * V / (ms / 1e3) / 1e12, 1),
+                      "peaks": hbm_kind}), flush=True)
     return 0
 
 
@@ -486,6 +560,8 @@ def main():
     args = parse_args()
     if args.sweep:
         return run_sweep(args)
+    if args.lm_head:
+        return run_lm_head(args)
     rank, world, dist = dist_init(args.gpus)
     if args.impl == "reference":
         if rank != 0:
