@@ -75,6 +75,10 @@ def _load():
         lib.orc_lm_head_logits.restype = C.c_int
         lib.orc_lm_head_greedy.argtypes = [p, p, dbl, p, i64, i64, i64, p, p]
         lib.orc_lm_head_greedy.restype = C.c_int
+        lib.orc_state_snapshot.argtypes = [p, p, i64, i64]
+        lib.orc_state_snapshot.restype = C.c_int
+        lib.orc_state_fixup.argtypes = [p, i32, p, p, p, p, i64, i64, p, p, p]
+        lib.orc_state_fixup.restype = C.c_int
         _lib = lib
         return lib
 
@@ -291,3 +295,36 @@ def lm_head_greedy(hidden, W, norm_w=None, eps: float = 0.0):
     _check(_load().orc_lm_head_greedy(_ptr(hidden), _ptr(nw), float(eps), _ptr(W), M, H, V,
                                       _ptr(ids), _ptr(mx)), "lm_head_greedy")
     return ids, mx
+
+
+# ---------------------------------------------------------------- post-verify state
+
+def state_snapshot(state):
+    """backup = a copy of state [B, row_bytes] (uint8)."""
+    state = np.ascontiguousarray(state, dtype=np.uint8)
+    B, rb = state.shape
+    backup = np.zeros_like(state)
+    _check(_load().orc_state_snapshot(_ptr(state), _ptr(backup), B, rb), "state_snapshot")
+    return backup
+
+
+def state_fixup(num_accepted, D: int, kv_before, state=None, backup=None, draft_kv_len=None):
+    """The post-verify fix-up of each row.  Returns (kv_len, recompute, state after,
+    draft_kv_len after, status); state/backup are uint8 [B, row_bytes] or None (no
+    recurrent state)."""
+    na = np.ascontiguousarray(num_accepted, dtype=np.int32)
+    B = na.size
+    kvb = np.ascontiguousarray(kv_before, dtype=np.int32)
+    if state is None:
+        st_arr, bk, rb = None, None, 0
+    else:
+        st_arr = np.array(state, dtype=np.uint8, copy=True, order="C")
+        bk = np.ascontiguousarray(backup, dtype=np.uint8)
+        rb = st_arr.shape[1]
+    dk = None if draft_kv_len is None else np.array(draft_kv_len, dtype=np.int32, copy=True)
+    kv = np.zeros(B, np.int32)
+    rc = np.zeros(B, np.int32)
+    status = np.zeros(1, np.int32)
+    _check(_load().orc_state_fixup(_ptr(na), int(D), _ptr(kvb), _ptr(kv), _ptr(st_arr), _ptr(bk),
+                                   B, rb, _ptr(dk), _ptr(rc), _ptr(status)), "state_fixup")
+    return kv, rc, st_arr, dk, int(status[0])

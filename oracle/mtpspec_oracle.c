@@ -765,3 +765,72 @@ int orc_lm_head_greedy(const uint16_t *hidden, const uint16_t *norm_w, double ep
     free(lg);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------ post-verify state [HB] */
+
+/* Snapshot before verification ([HB] "Rolling back" and the snapshot step of the decoding
+ * loop: a KV cache only needs its length, which the caller keeps; the linear attention's
+ * memory tables and convolution windows are copied): backup[b] = state[b] for each of B
+ * rows of row_bytes bytes. */
+int orc_state_snapshot(const uint8_t *state, uint8_t *backup, int64_t B, int64_t row_bytes)
+{
+    if (B < 0 || row_bytes < 0 || (B > 0 && row_bytes > 0 && (!state || !backup)))
+        return ORC_ERR_ARG;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t i = 0; i < row_bytes; ++i)
+            backup[b * row_bytes + i] = state[b * row_bytes + i];
+    return ORC_OK;
+}
+
+/* Fix-up after verification ([HB] "Rolling back" and the loop's hit / miss branches; [ZH]
+ * 三 stage 4; the accepted count a comes from the verifier).  The verify forward appended
+ * D + 1 positions (the carried-in token and the D drafts) after kv_before[b] positions.
+ *  - a == D (hit): every appended position stays: kv_len = kv_before + D + 1, the state is
+ *    kept, nothing is recomputed.
+ *  - a < D (miss), with a recurrent state (row_bytes > 0): the memory tables have absorbed
+ *    rejected drafts and cannot be undone, so the row goes back to its snapshot: state =
+ *    backup, kv_len = kv_before (a truncation), and the carried-in token and the a
+ *    accepted drafts (recompute = 1 + a) must pass the model again.
+ *  - a < D without a recurrent state (row_bytes == 0): attention keys of kept positions do
+ *    not depend on later ones, so kv_len = kv_before + 1 + a and nothing is recomputed.
+ *  - on a miss, the draft head's own KV length is cut to the main model's:
+ *    draft_kv_len = min(draft_kv_len, kv_len).
+ * A row with a outside [0, D] is left untouched and sets ORC_STATUS_BAD_PARAM (2). */
+int orc_state_fixup(const int32_t *num_accepted, int32_t D, const int32_t *kv_before,
+                    int32_t *kv_len, uint8_t *state, const uint8_t *backup, int64_t B,
+                    int64_t row_bytes, int32_t *draft_kv_len, int32_t *recompute,
+                    int32_t *status)
+{
+    if (B < 0 || D < 1 || row_bytes < 0)
+        return ORC_ERR_ARG;
+    if (B > 0 && (!num_accepted || !kv_before || !kv_len || (row_bytes > 0 && (!state || !backup))))
+        return ORC_ERR_ARG;
+    int32_t st = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        const int32_t a = num_accepted[b];
+        if (a < 0 || a > D) {
+            st |= 2;
+            continue;
+        }
+        const int miss = a < D;
+        int32_t kv, rc = 0;
+        if (!miss) {
+            kv = kv_before[b] + D + 1;
+        } else if (row_bytes > 0) {
+            for (int64_t i = 0; i < row_bytes; ++i)
+                state[b * row_bytes + i] = backup[b * row_bytes + i];
+            kv = kv_before[b];
+            rc = 1 + a;
+        } else {
+            kv = kv_before[b] + 1 + a;
+        }
+        kv_len[b] = kv;
+        if (recompute)
+            recompute[b] = rc;
+        if (draft_kv_len && miss && draft_kv_len[b] > kv)
+            draft_kv_len[b] = kv;
+    }
+    if (status)
+        *status |= st;
+    return ORC_OK;
+}
