@@ -500,6 +500,27 @@ def run_sweep(args):
                      "peak": hbm, "unit": "GB/s"}
         lroof["frac"] = round(lroof["achieved"] / lroof["peak"], 4)
         vach = vbytes / (vms / 1e3) / 1e9
+        # the state around the verification: a snapshot of each row's recurrent state (the
+        # pages' 19 MiB of memory tables and convolution windows) and the fix-up with this
+        # workload's accepted counts (misses copy their row back)
+        rb = 19 << 20
+        S = torch.empty((B, rb), dtype=torch.uint8, device=dev)
+        S.fill_(7)
+        Sb = torch.empty_like(S)
+        kv0 = torch.zeros(B, dtype=torch.int32, device=dev)
+        kv1 = torch.empty_like(kv0)
+        sms = timed(lambda: lib.mtp_state_snapshot(S, Sb), 10)
+        fms = timed(lambda: lib.mtp_state_fixup(na, D, kv0, kv1, S, Sb), 10)
+        nmiss = int((na < D).sum().item())
+        del S, Sb
+        sbytes, fbytes = 2 * B * rb, 2 * nmiss * rb + B * 12
+        state = {"row_bytes": rb,
+                 "snapshot": {"ms": round(sms, 4), "roofline": {
+                     "bound": "hbm", "achieved": round(sbytes / (sms / 1e3) / 1e9, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(sbytes / (sms / 1e3) / 1e9 / hbm, 4), "bytes": sbytes}},
+                 "fixup": {"ms": round(fms, 4), "rows_restored": nmiss, "roofline": {
+                     "bound": "hbm", "achieved": round(fbytes / (fms / 1e3) / 1e9, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(fbytes / (fms / 1e3) / 1e9 / hbm, 4), "bytes": fbytes}}}
         print(json.dumps({
             "sweep": name, "dtype": x["dtype"], "B": B, "D": D, "V": V, "H": H,
             "verify": {"call": vcall, "ms": round(vms, 4),
@@ -513,6 +534,7 @@ def run_sweep(args):
             "lm_head_greedy": {"M": Ml, "ms": round(lms, 4),
                                "tokens_per_s": round(Ml / (lms / 1e3), 1), "roofline": lroof,
                                "cublas_matmul_argmax_ms": round(cms, 4)},
+            "state": state,
             "peaks": hbm_kind}), flush=True)
     return 0
 

@@ -246,6 +246,47 @@ int spec_verify_sample_static(const void *target_logits, const void *draft_logit
                               int32_t *num_accepted, float *p_target, float *p_draft,
                               int32_t *status, void *stream);
 
+/* ------------------------------------------------------------------ state around a verification */
+
+/*
+ * mtp_state_snapshot — the copy taken before a verification ([HB] the decoding loop's
+ * snapshot and "Rolling back": a KV cache needs only its length, which the caller keeps;
+ * the linear attention's memory tables and convolution windows are copied):
+ *     backup[b] = state[b]   for each of B rows of row_bytes bytes.
+ *   state, backup   device [B, row_bytes], 16-byte aligned, not overlapping
+ *   B >= 0 (<= 2^24), row_bytes >= 0 with row_bytes % 16 == 0.
+ * Returns MTPSPEC_OK (nothing enqueued when there is nothing to copy) or an error.
+ */
+int mtp_state_snapshot(const void *state, void *backup, int64_t B, int64_t row_bytes,
+                       void *stream);
+
+/*
+ * mtp_state_fixup — the model state after a verification, from the verifier's accepted
+ * counts ([HB] the decoding loop's hit / miss branches and "Rolling back"; [ZH] 三 stage
+ * 4).  The verify forward appended D + 1 positions (the carried-in token and the D
+ * drafts) after kv_len_before[b].  With a = num_accepted[b]:
+ *   a == D (hit):   kv_len = kv_len_before + D + 1; the state is kept; recompute = 0.
+ *   a <  D (miss), row_bytes > 0 (a recurrent state):  state[b] = backup[b] (the memory
+ *                   tables absorbed rejected drafts and cannot be undone), kv_len =
+ *                   kv_len_before (truncated), recompute = 1 + a: the carried-in token and
+ *                   the accepted drafts must pass the model again.
+ *   a <  D, row_bytes == 0 (attention only):  kv_len = kv_len_before + 1 + a (the kept
+ *                   keys do not depend on later positions); recompute = 0.
+ *   on a miss, draft_kv_len (the draft head's own cache) = min(draft_kv_len, kv_len).
+ * A row with a outside [0, D] is left untouched and ORs MTPSPEC_STATUS_BAD_PARAM into
+ * *status.
+ *   num_accepted, kv_len_before  int32 [B]      kv_len  int32 [B] (may be kv_len_before)
+ *   state   device [B, row_bytes] (in/out)   backup  device [B, row_bytes] from
+ *           mtp_state_snapshot; both 16-byte aligned and not overlapping; unused when
+ *           row_bytes == 0
+ *   draft_kv_len, recompute  int32 [B] or NULL   status  int32 [1] or NULL
+ *   B >= 0 (<= 2^24), 1 <= D <= 64, row_bytes >= 0 with row_bytes % 16 == 0.
+ */
+int mtp_state_fixup(const int32_t *num_accepted, int32_t D, const int32_t *kv_len_before,
+                    int32_t *kv_len, void *state, const void *backup, int64_t B,
+                    int64_t row_bytes, int32_t *draft_kv_len, int32_t *recompute,
+                    int32_t *status, void *stream);
+
 /* ------------------------------------------------------------------ misc */
 
 /* A static, human-readable name for an mtpspec_status value. */

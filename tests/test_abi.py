@@ -34,6 +34,7 @@ def test_header_declares_the_boundary():
     assert _declared() == sorted([
         "mtp_draft_input", "mtp_draft_input_workspace_bytes", "mtp_greedy_draft",
         "mtp_lm_head_greedy", "mtp_lm_head_greedy_workspace_bytes",
+        "mtp_state_snapshot", "mtp_state_fixup",
         "spec_verify_greedy", "spec_verify_sample", "spec_verify_workspace_bytes",
         "spec_verify_sample_static", "mtpspec_status_string", "mtpspec_launch_count"])
 
@@ -108,6 +109,27 @@ def test_lm_head_greedy_host_checks(so):
     assert need == 256 + 1024 + 4 * 8 * 8
     assert so.mtp_lm_head_greedy_workspace_bytes(4, 12, 1000) == 0
     assert so.mtp_lm_head_greedy_workspace_bytes(0, 64, 1000) == 0
+
+
+def test_state_host_checks(so):
+    nul, p16, q16 = None, C.c_void_p(4096), C.c_void_p(1 << 20)
+    snap = so.mtp_state_snapshot
+    assert snap(p16, q16, 2, 24, nul) == -3          # row_bytes % 16
+    assert snap(p16, q16, -1, 32, nul) == -3
+    assert snap(nul, nul, 0, 32, nul) == 0           # nothing to copy
+    assert snap(nul, nul, 3, 0, nul) == 0
+    assert snap(nul, q16, 2, 32, nul) == -1
+    assert snap(C.c_void_p(4100), q16, 2, 32, nul) == -1   # misaligned
+    assert snap(p16, C.c_void_p(4096 + 32), 2, 32, nul) == -1  # overlapping
+    fix = so.mtp_state_fixup
+    i4 = C.c_void_p(256)
+    assert fix(i4, 0, i4, i4, nul, nul, 1, 0, nul, nul, nul, nul) == -3    # D < 1
+    assert fix(i4, 65, i4, i4, nul, nul, 1, 0, nul, nul, nul, nul) == -3   # D > 64
+    assert fix(i4, 3, i4, i4, p16, q16, 1, 40, nul, nul, nul, nul) == -3   # row_bytes % 16
+    assert fix(nul, 3, nul, nul, nul, nul, 0, 0, nul, nul, nul, nul) == 0  # B == 0
+    assert fix(nul, 3, i4, i4, nul, nul, 2, 0, nul, nul, nul, nul) == -1   # no counts
+    assert fix(i4, 3, i4, i4, nul, q16, 2, 32, nul, nul, nul, nul) == -1   # state missing
+    assert fix(i4, 3, i4, C.c_void_p(258), nul, nul, 2, 0, nul, nul, nul, nul) == -1
 
 
 def test_launch_count_starts_at_zero_on_the_host(so):

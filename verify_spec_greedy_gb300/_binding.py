@@ -51,6 +51,8 @@ def load():
                                        p, p], C.c_int),
         "mtp_lm_head_greedy": ([p, p, f32, p, i64, i64, i64, p, p, p, sz, p, p], C.c_int),
         "mtp_lm_head_greedy_workspace_bytes": ([i64, i64, i64], sz),
+        "mtp_state_snapshot": ([p, p, i64, i64, p], C.c_int),
+        "mtp_state_fixup": ([p, i32, p, p, p, p, i64, i64, p, p, p, p], C.c_int),
         "mtpspec_status_string": ([C.c_int], C.c_char_p),
         "mtpspec_launch_count": ([], C.c_uint64),
     }
@@ -138,6 +140,26 @@ def mtp_lm_head_greedy(hidden, lm_head_w, out_ids, norm_w=None, eps: float = 0.0
     _call("mtp_lm_head_greedy", _ptr(hidden), _ptr(norm_w), float(eps), _ptr(lm_head_w), M, H,
           V, _ptr(out_ids), _ptr(out_logit), _ptr(workspace), ws, _ptr(status), _stream(stream))
     return out_ids
+
+
+def mtp_state_snapshot(state, backup, stream=None):
+    """backup[b] = state[b] for device tensors of B rows (any dtype, same shape)."""
+    B = state.shape[0]
+    rb = state[0].numel() * state.element_size() if B else 0
+    _call("mtp_state_snapshot", _ptr(state), _ptr(backup), B, rb, _stream(stream))
+    return backup
+
+
+def mtp_state_fixup(num_accepted, D: int, kv_len_before, kv_len, state=None, backup=None,
+                    draft_kv_len=None, recompute=None, status=None, stream=None):
+    """The post-verify fix-up of each row (see include/libmtpspec.h); state/backup are
+    device tensors of B rows, or None for a model without recurrent state."""
+    B = num_accepted.shape[0]
+    rb = 0 if state is None else state[0].numel() * state.element_size()
+    _call("mtp_state_fixup", _ptr(num_accepted), int(D), _ptr(kv_len_before), _ptr(kv_len),
+          _ptr(state), _ptr(backup), B, rb, _ptr(draft_kv_len), _ptr(recompute), _ptr(status),
+          _stream(stream))
+    return kv_len
 
 
 def spec_verify_greedy(target_logits, draft_ids, out_tokens, num_accepted, status=None,

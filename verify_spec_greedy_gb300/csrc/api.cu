@@ -236,6 +236,46 @@ MTPSPEC_API int mtp_lm_head_greedy(const void *hidden, const void *norm_w, float
     return launched(mtpspec::run_lm_head_greedy(a, s));
 }
 
+constexpr int64_t kMaxStateRows = 1LL << 24;
+
+MTPSPEC_API int mtp_state_snapshot(const void *state, void *backup, int64_t B, int64_t row_bytes,
+                                   void *stream) {
+    if (B < 0 || B > kMaxStateRows || row_bytes < 0 || (row_bytes % 16) != 0) return MTPSPEC_ERR_SHAPE;
+    if (B == 0 || row_bytes == 0) return MTPSPEC_OK;
+    if (!state || !backup || !aligned(state, 16) || !aligned(backup, 16)) return MTPSPEC_ERR_ARG;
+    const char *s0 = static_cast<const char *>(state), *b0 = static_cast<const char *>(backup);
+    const int64_t n = B * row_bytes;
+    if (s0 < b0 + n && b0 < s0 + n) return MTPSPEC_ERR_ARG;  // overlapping
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = prepare_device(s);
+    if (rc != MTPSPEC_OK) return rc;
+    return launched(mtpspec::run_state_snapshot(state, backup, B, row_bytes, s));
+}
+
+MTPSPEC_API int mtp_state_fixup(const int32_t *num_accepted, int32_t D, const int32_t *kv_len_before,
+                                int32_t *kv_len, void *state, const void *backup, int64_t B,
+                                int64_t row_bytes, int32_t *draft_kv_len, int32_t *recompute,
+                                int32_t *status, void *stream) {
+    if (B < 0 || B > kMaxStateRows || D < 1 || D > kMaxD || row_bytes < 0 || (row_bytes % 16) != 0)
+        return MTPSPEC_ERR_SHAPE;
+    if (B == 0) return MTPSPEC_OK;
+    if (!num_accepted || !kv_len_before || !kv_len) return MTPSPEC_ERR_ARG;
+    if (!aligned(num_accepted, 4) || !aligned(kv_len_before, 4) || !aligned(kv_len, 4) ||
+        !aligned(draft_kv_len, 4) || !aligned(recompute, 4) || !aligned(status, 4))
+        return MTPSPEC_ERR_ARG;
+    if (row_bytes > 0) {
+        if (!state || !backup || !aligned(state, 16) || !aligned(backup, 16)) return MTPSPEC_ERR_ARG;
+        const char *s0 = static_cast<const char *>(state), *b0 = static_cast<const char *>(backup);
+        const int64_t n = B * row_bytes;
+        if (s0 < b0 + n && b0 < s0 + n) return MTPSPEC_ERR_ARG;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = prepare_device(s);
+    if (rc != MTPSPEC_OK) return rc;
+    return launched(mtpspec::run_state_fixup(num_accepted, D, kv_len_before, kv_len, state, backup,
+                                             B, row_bytes, draft_kv_len, recompute, status, s));
+}
+
 MTPSPEC_API int spec_verify_sample_static(const void *target_logits, const void *draft_logits,
                                           int dtype, const int32_t *draft_ids,
                                           const float *temperature, const int32_t *top_k,

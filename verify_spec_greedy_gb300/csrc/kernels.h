@@ -122,3 +122,15 @@ cudaError_t run_gemm_argmax(const void *W, const void *X, int64_t V, int64_t Mt,
                             unsigned long long *keys, unsigned *err, cudaStream_t stream);
 
 }  // namespace mtpspec
+
+namespace mtpspec {
+
+// The model state around a verification (state.cu).
+cudaError_t run_state_snapshot(const void *state, void *backup, int64_t B, int64_t row_bytes,
+                               cudaStream_t stream);
+cudaError_t run_state_fixup(const int32_t *num_accepted, int32_t D, const int32_t *kv_before,
+                            int32_t *kv_len, void *state, const void *backup, int64_t B,
+                            int64_t row_bytes, int32_t *draft_kv_len, int32_t *recompute,
+                            int32_t *status, cudaStream_t stream);
+
+}  // namespace mtpspec
