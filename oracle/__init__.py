@@ -79,6 +79,8 @@ def _load():
         lib.orc_state_snapshot.restype = C.c_int
         lib.orc_state_fixup.argtypes = [p, i32, p, p, p, p, i64, i64, p, p, p]
         lib.orc_state_fixup.restype = C.c_int
+        lib.orc_draft_steps.argtypes = [p, p, p, p, p, p, p, p, p, dbl, i64, i64, i64, i32, p, p, p]
+        lib.orc_draft_steps.restype = C.c_int
         _lib = lib
         return lib
 
@@ -328,3 +330,27 @@ def state_fixup(num_accepted, D: int, kv_before, state=None, backup=None, draft_
     _check(_load().orc_state_fixup(_ptr(na), int(D), _ptr(kvb), _ptr(kv), _ptr(st_arr), _ptr(bk),
                                    B, rb, _ptr(dk), _ptr(rc), _ptr(status)), "state_fixup")
     return kv, rc, st_arr, dk, int(status[0])
+
+
+# ---------------------------------------------------------------- draft steps
+
+def draft_steps(embed, next_ids, hidden, enorm_w, hnorm_w, eh_proj_w, lm_head_w, D: int,
+                eps: float, norm_w=None, positions=None):
+    """D serial greedy draft steps with a stub block.  Returns (draft_ids int32 [M, D],
+    hidden_out bf16 bits [D, M, H], status)."""
+    u16 = lambda a: np.ascontiguousarray(a, dtype=np.uint16)
+    embed, hidden, enorm_w, hnorm_w = u16(embed), u16(hidden), u16(enorm_w), u16(hnorm_w)
+    eh_proj_w, lm_head_w = u16(eh_proj_w), u16(lm_head_w)
+    nw = None if norm_w is None else u16(norm_w)
+    ids = np.ascontiguousarray(next_ids, dtype=np.int32)
+    pos = None if positions is None else np.ascontiguousarray(positions, dtype=np.int32)
+    M, H = hidden.shape
+    V = embed.shape[0]
+    out = np.zeros((M, D), np.int32)
+    hout = np.zeros((D, M, H), np.uint16)
+    status = np.zeros(1, np.int32)
+    _check(_load().orc_draft_steps(_ptr(embed), _ptr(ids), _ptr(pos), _ptr(hidden), _ptr(enorm_w),
+                                   _ptr(hnorm_w), _ptr(eh_proj_w), _ptr(nw), _ptr(lm_head_w),
+                                   float(eps), M, H, V, int(D), _ptr(out), _ptr(hout),
+                                   _ptr(status)), "draft_steps")
+    return out, hout, int(status[0])

@@ -834,3 +834,68 @@ int orc_state_fixup(const int32_t *num_accepted, int32_t D, const int32_t *kv_be
         *status |= st;
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------ draft steps [ZH][HB] */
+
+/* D serial draft steps of the draft head ([ZH] 三 stage 1 and stage 2: the bonus token and
+ * the main model's hidden state start the chain; each step embeds the previous token,
+ * runs the head and greedy-samples the next draft, and feeds that token and the head's
+ * hidden state to the next step; 二.2 step 1: the input embedding at position 0 is zeroed;
+ * [HB] "The draft head").  The head's decoder block is not modelled: its output is its
+ * input (a stub), so a step is
+ *     e   = embed[ids] (a zero row where positions[t] + step == 0)
+ *     y   = bf16(eh_proj(cat(enorm(e), hnorm(h))))     (orc_draft_input, then rounded)
+ *     ids = argmax over v of lm_head(norm(y))          (orc_lm_head_greedy's rule)
+ *     h   = y
+ * embed [V, H] and lm_head_w [V, H] bf16; positions may be NULL (no mask); norm_w may be
+ * NULL (no final norm).  draft_ids [M, D]; hidden_out (optional) [D, M, H] bf16 bits of
+ * each step's y.  An id outside [0, V) embeds as a zero row and sets status bit 1. */
+int orc_draft_steps(const uint16_t *embed, const int32_t *next_ids, const int32_t *positions,
+                    const uint16_t *hidden, const uint16_t *enorm_w, const uint16_t *hnorm_w,
+                    const uint16_t *eh_proj_w, const uint16_t *norm_w, const uint16_t *lm_head_w,
+                    double eps, int64_t M, int64_t H, int64_t V, int32_t D, int32_t *draft_ids,
+                    uint16_t *hidden_out, int32_t *status)
+{
+    if (M < 0 || H < 1 || V < 1 || D < 1 || !(eps >= 0.0))
+        return ORC_ERR_ARG;
+    if (M == 0)
+        return ORC_OK;
+    if (!embed || !next_ids || !hidden || !enorm_w || !hnorm_w || !eh_proj_w || !lm_head_w || !draft_ids)
+        return ORC_ERR_ARG;
+    uint16_t *e = (uint16_t *)calloc((size_t)(M * H), sizeof(uint16_t));
+    uint16_t *h = (uint16_t *)malloc((size_t)(M * H) * sizeof(uint16_t));
+    int32_t *ids = (int32_t *)malloc((size_t)M * sizeof(int32_t));
+    double *y = (double *)malloc((size_t)(M * H) * sizeof(double));
+    if (!e || !h || !ids || !y) {
+        free(e); free(h); free(ids); free(y);
+        return ORC_ERR_NOMEM;
+    }
+    memcpy(h, hidden, (size_t)(M * H) * sizeof(uint16_t));
+    memcpy(ids, next_ids, (size_t)M * sizeof(int32_t));
+    int32_t st = 0;
+    int rc = ORC_OK;
+    for (int32_t k = 0; k < D && rc == ORC_OK; ++k) {
+        for (int64_t t = 0; t < M; ++t) {
+            const int masked = positions && (int64_t)positions[t] + k == 0;
+            const int bad = ids[t] < 0 || ids[t] >= V;
+            if (bad)
+                st |= 1;
+            for (int64_t i = 0; i < H; ++i)
+                e[t * H + i] = (masked || bad) ? 0 : embed[(int64_t)ids[t] * H + i];
+        }
+        rc = orc_draft_input(e, h, enorm_w, hnorm_w, eh_proj_w, M, H, eps, y, NULL);
+        if (rc != ORC_OK)
+            break;
+        for (int64_t i = 0; i < M * H; ++i)
+            h[i] = orc_double_to_bf16(y[i]);
+        if (hidden_out)
+            memcpy(hidden_out + (int64_t)k * M * H, h, (size_t)(M * H) * sizeof(uint16_t));
+        rc = orc_lm_head_greedy(h, norm_w, eps, lm_head_w, M, H, V, ids, NULL);
+        for (int64_t t = 0; t < M && rc == ORC_OK; ++t)
+            draft_ids[t * D + k] = ids[t];
+    }
+    free(e); free(h); free(ids); free(y);
+    if (status)
+        *status |= st;
+    return rc;
+}
