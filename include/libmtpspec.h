@@ -142,6 +142,45 @@ int mtp_lm_head_greedy(const void *hidden, const void *norm_w, float eps, const 
  * would reject. */
 size_t mtp_lm_head_greedy_workspace_bytes(int64_t M, int64_t H, int64_t V);
 
+/*
+ * mtp_draft_steps — D serial greedy draft steps of the draft head ([ZH] 三 stages 1-2: the
+ * bonus token and the main model's hidden state start the chain; each step embeds the
+ * previous token, runs the head, greedy-samples the next draft and passes the token and
+ * the head's hidden state to the next step; 二.2 step 1: the input embedding at position 0
+ * is zeroed; [HB] "The draft head").  The head's decoder block is not part of this
+ * library: its output is taken to be its input.  Step k = 0 .. D-1, with ids = next_ids
+ * and h = hidden before step 0:
+ *     e   = embed_w[ids[t]], or a zero row where positions[t] + k == 0 (or the id lies
+ *           outside [0, V): then MTPSPEC_STATUS_BAD_DRAFT_ID is OR-ed into *status)
+ *     y   = mtp_draft_input(e, h)                      (bf16 [M, H])
+ *     ids = mtp_lm_head_greedy(y, norm_w, lm_head_w)   -> draft_ids[:, k]
+ *     h   = y
+ * Every step is one embedding gather, the input stage and the output layer; nothing is
+ * allocated or synchronised, so the call can be captured into a CUDA graph.
+ *
+ *   embed_w     bf16 [V, H]   token embeddings (shared with the main model)
+ *   next_ids    int32 [M]     the token after each row's last verified position
+ *   positions   int32 [M] or NULL   that token's position (no mask when NULL)
+ *   hidden      bf16 [M, H]   the main model's hidden state at the previous position
+ *   enorm_w, hnorm_w, eh_proj_w   as in mtp_draft_input
+ *   norm_w      bf16 [H] or NULL, lm_head_w bf16 [V, H]   as in mtp_lm_head_greedy
+ *   draft_ids   int32 [M, D]  hidden_out bf16 [D, M, H] or NULL (every step's y)
+ *   workspace   >= mtp_draft_steps_workspace_bytes(M, H, V) bytes, 256-byte aligned
+ *   status      int32 [1] or NULL
+ *   M >= 0 (<= 2^20), 8 <= H <= 65536 with H % 8 == 0, 1 <= V <= 8,388,480, 1 <= D <= 64.
+ *   Matrices, norm weights and hidden_out 16-byte aligned.
+ */
+int mtp_draft_steps(const void *embed_w, const int32_t *next_ids, const int32_t *positions,
+                    const void *hidden, const void *enorm_w, const void *hnorm_w,
+                    const void *eh_proj_w, const void *norm_w, const void *lm_head_w, float eps,
+                    int64_t M, int64_t H, int64_t V, int32_t D, int32_t *draft_ids,
+                    void *hidden_out, void *workspace, size_t workspace_bytes, int32_t *status,
+                    void *stream);
+
+/* Bytes of device workspace mtp_draft_steps needs for (M, H, V); 0 for arguments it would
+ * reject. */
+size_t mtp_draft_steps_workspace_bytes(int64_t M, int64_t H, int64_t V);
+
 /* ------------------------------------------------------------------ greedy verification */
 
 /*

@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
     assert _declared() == sorted([
         "mtp_draft_input", "mtp_draft_input_workspace_bytes", "mtp_greedy_draft",
         "mtp_lm_head_greedy", "mtp_lm_head_greedy_workspace_bytes",
-        "mtp_state_snapshot", "mtp_state_fixup",
+        "mtp_state_snapshot", "mtp_state_fixup", "mtp_draft_steps",
+        "mtp_draft_steps_workspace_bytes",
         "spec_verify_greedy", "spec_verify_sample", "spec_verify_workspace_bytes",
         "spec_verify_sample_static", "mtpspec_status_string", "mtpspec_launch_count"])
 
@@ -130,6 +131,32 @@ def test_state_host_checks(so):
     assert fix(nul, 3, i4, i4, nul, nul, 2, 0, nul, nul, nul, nul) == -1   # no counts
     assert fix(i4, 3, i4, i4, nul, q16, 2, 32, nul, nul, nul, nul) == -1   # state missing
     assert fix(i4, 3, i4, C.c_void_p(258), nul, nul, 2, 0, nul, nul, nul, nul) == -1
+
+
+def test_draft_steps_host_checks(so):
+    nul, p = None, C.c_void_p(4096)
+    f = so.mtp_draft_steps
+    names = ["E", "ids", "pos", "h", "we", "wh", "W", "nw", "L", "eps", "M", "H", "V", "D",
+             "out", "hout", "ws", "wsb", "status", "stream"]
+    ok = dict(E=p, ids=p, pos=nul, h=p, we=p, wh=p, W=p, nw=nul, L=p, eps=1e-6, M=4, H=64,
+              V=100, D=3, out=p, hout=nul, ws=p, wsb=1 << 30, status=nul, stream=nul)
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(*[a[n] for n in names])
+    assert call(D=0) == -3
+    assert call(D=65) == -3
+    assert call(H=20) == -3
+    assert call(V=0) == -3
+    assert call(eps=-1.0) == -1
+    assert call(M=0) == 0
+    assert call(E=nul) == -1
+    assert call(L=C.c_void_p(4104)) == -1
+    assert call(out=C.c_void_p(4098)) == -1
+    assert call(ws=nul) == -4
+    assert call(wsb=16) == -4
+    assert so.mtp_draft_steps_workspace_bytes(4, 64, 100) > 0
+    assert so.mtp_draft_steps_workspace_bytes(4, 60, 100) == 0
 
 
 def test_launch_count_starts_at_zero_on_the_host(so):

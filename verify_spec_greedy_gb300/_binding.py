@@ -53,6 +53,9 @@ def load():
         "mtp_lm_head_greedy_workspace_bytes": ([i64, i64, i64], sz),
         "mtp_state_snapshot": ([p, p, i64, i64, p], C.c_int),
         "mtp_state_fixup": ([p, i32, p, p, p, p, i64, i64, p, p, p, p], C.c_int),
+        "mtp_draft_steps": ([p, p, p, p, p, p, p, p, p, f32, i64, i64, i64, i32, p, p, p, sz, p, p],
+                            C.c_int),
+        "mtp_draft_steps_workspace_bytes": ([i64, i64, i64], sz),
         "mtpspec_status_string": ([C.c_int], C.c_char_p),
         "mtpspec_launch_count": ([], C.c_uint64),
     }
@@ -160,6 +163,25 @@ def mtp_state_fixup(num_accepted, D: int, kv_len_before, kv_len, state=None, bac
           _ptr(state), _ptr(backup), B, rb, _ptr(draft_kv_len), _ptr(recompute), _ptr(status),
           _stream(stream))
     return kv_len
+
+
+def mtp_draft_steps_workspace_bytes(M: int, H: int, V: int) -> int:
+    return int(load().mtp_draft_steps_workspace_bytes(int(M), int(H), int(V)))
+
+
+def mtp_draft_steps(embed_w, next_ids, hidden, enorm_w, hnorm_w, eh_proj_w, lm_head_w,
+                    draft_ids, eps: float, norm_w=None, positions=None, hidden_out=None,
+                    workspace=None, status=None, stream=None):
+    """draft_ids[M, D] from D serial greedy steps of the draft head (stub block)."""
+    M, H = hidden.shape
+    V = embed_w.shape[0]
+    D = draft_ids.shape[1]
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _call("mtp_draft_steps", _ptr(embed_w), _ptr(next_ids), _ptr(positions), _ptr(hidden),
+          _ptr(enorm_w), _ptr(hnorm_w), _ptr(eh_proj_w), _ptr(norm_w), _ptr(lm_head_w),
+          float(eps), M, H, V, D, _ptr(draft_ids), _ptr(hidden_out), _ptr(workspace), ws,
+          _ptr(status), _stream(stream))
+    return draft_ids
 
 
 def spec_verify_greedy(target_logits, draft_ids, out_tokens, num_accepted, status=None,

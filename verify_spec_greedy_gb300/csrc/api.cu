@@ -24,10 +24,14 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 size_t elem_size(int dtype) { return dtype == MTPSPEC_F32 ? 4 : 2; }
 
 // Make the stream's device current for this library's runtime and check that it is an
-// sm_103 part.  Called only after every host-side check has passed.
+// sm_103 part.  Called only after every host-side check has passed.  A stream that is
+// being captured into a graph must not be asked for its device (the query invalidates
+// the capture); the capturing thread's current device is used then.
 int prepare_device(cudaStream_t stream) {
     int dev = -1;
-    if (stream != nullptr) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (stream != nullptr && cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return MTPSPEC_ERR_CUDA;
+    if (stream != nullptr && cs == cudaStreamCaptureStatusNone) {
         if (cudaStreamGetDevice(stream, &dev) != cudaSuccess) return MTPSPEC_ERR_CUDA;
         int cur = -1;
         if (cudaGetDevice(&cur) != cudaSuccess) return MTPSPEC_ERR_CUDA;
@@ -230,10 +234,64 @@ MTPSPEC_API int mtp_lm_head_greedy(const void *hidden, const void *norm_w, float
     a.H = H;
     a.V = V;
     a.ids = out_ids;
+    a.ids_stride = 1;
     a.logit = out_logit;
     a.workspace = workspace;
     a.status = status;
     return launched(mtpspec::run_lm_head_greedy(a, s));
+}
+
+MTPSPEC_API size_t mtp_draft_steps_workspace_bytes(int64_t M, int64_t H, int64_t V) {
+    if (M <= 0 || H < 8 || H > kMaxH || (H % 8) != 0 || M > kMaxTokens || V < 1 || V > kMaxLmHeadV)
+        return 0;
+    return mtpspec::draft_steps_workspace_bytes(M, H, V);
+}
+
+MTPSPEC_API int mtp_draft_steps(const void *embed_w, const int32_t *next_ids, const int32_t *positions,
+                                const void *hidden, const void *enorm_w, const void *hnorm_w,
+                                const void *eh_proj_w, const void *norm_w, const void *lm_head_w,
+                                float eps, int64_t M, int64_t H, int64_t V, int32_t D,
+                                int32_t *draft_ids, void *hidden_out, void *workspace,
+                                size_t workspace_bytes, int32_t *status, void *stream) {
+    if (M < 0 || H < 8 || H > kMaxH || (H % 8) != 0 || M > kMaxTokens || V < 1 || V > kMaxLmHeadV ||
+        D < 1 || D > kMaxD)
+        return MTPSPEC_ERR_SHAPE;
+    if (!(eps >= 0.0f)) return MTPSPEC_ERR_ARG;
+    if (M == 0) return MTPSPEC_OK;
+    if (!embed_w || !next_ids || !hidden || !enorm_w || !hnorm_w || !eh_proj_w || !lm_head_w ||
+        !draft_ids)
+        return MTPSPEC_ERR_ARG;
+    if (!aligned(embed_w, 16) || !aligned(hidden, 16) || !aligned(enorm_w, 16) ||
+        !aligned(hnorm_w, 16) || !aligned(eh_proj_w, 16) || !aligned(norm_w, 16) ||
+        !aligned(lm_head_w, 16) || !aligned(hidden_out, 16) || !aligned(next_ids, 4) ||
+        !aligned(positions, 4) || !aligned(draft_ids, 4) || !aligned(status, 4))
+        return MTPSPEC_ERR_ARG;
+    if (!workspace || !aligned(workspace, 256) ||
+        workspace_bytes < mtpspec::draft_steps_workspace_bytes(M, H, V))
+        return MTPSPEC_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = prepare_device(s);
+    if (rc != MTPSPEC_OK) return rc;
+    mtpspec::DraftStepsArgs a;
+    a.embed = embed_w;
+    a.next_ids = next_ids;
+    a.positions = positions;
+    a.hidden = hidden;
+    a.enorm_w = enorm_w;
+    a.hnorm_w = hnorm_w;
+    a.eh_proj_w = eh_proj_w;
+    a.norm_w = norm_w;
+    a.lm_head_w = lm_head_w;
+    a.eps = eps;
+    a.M = M;
+    a.H = H;
+    a.V = V;
+    a.D = D;
+    a.draft_ids = draft_ids;
+    a.hidden_out = hidden_out;
+    a.workspace = workspace;
+    a.status = status;
+    return launched(mtpspec::run_draft_steps(a, s));
 }
 
 constexpr int64_t kMaxStateRows = 1LL << 24;

@@ -193,9 +193,9 @@ static cudaError_t launch_gemv(const DraftInputArgs &a, cudaStream_t stream) {
     const int H = static_cast<int>(a.H);
     const size_t smem = static_cast<size_t>(MT) * 2 * H * 2;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(di::k_draft_gemv<MT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        static AttrCache attr;
+        cudaError_t e = ensure_attr(di::k_draft_gemv<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem), attr);
         if (e != cudaSuccess) return e;
     }
     // enough CTAs for a few waves over 152 SMs, whole warps of rows each

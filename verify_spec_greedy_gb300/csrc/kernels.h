@@ -6,10 +6,28 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace mtpspec {
 
 // Adds n to the library's count of kernel launches (read by mtpspec_launch_count).
 void count_launches(int n);
+
+// Function attributes persist, so each is set once per device (and the shared-memory
+// limit again only when a larger one is asked for): launches recorded by a stream
+// capture then make no attribute call.
+struct AttrCache {
+    std::atomic<int> v[64];
+};
+template <typename F>
+cudaError_t ensure_attr(F kernel, cudaFuncAttribute attr, int value, AttrCache &c) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (c.v[dev].load() >= value) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, attr, value);
+    if (e == cudaSuccess) c.v[dev].store(value);
+    return e;
+}
 
 cudaError_t run_greedy_draft(const void *logits, int dtype, int64_t M, int64_t V, int32_t *ids,
                              cudaStream_t stream);
@@ -104,7 +122,8 @@ struct LmHeadArgs {
     float eps;
     const void *W;        // bf16 [V, H]
     int64_t M, H, V;
-    int32_t *ids;         // [M]
+    int32_t *ids;         // ids[t * ids_stride]
+    int64_t ids_stride;
     float *logit;         // [M] or nullptr
     void *workspace;
     int32_t *status;      // or nullptr
@@ -132,5 +151,29 @@ cudaError_t run_state_fixup(const int32_t *num_accepted, int32_t D, const int32_
                             int32_t *kv_len, void *state, const void *backup, int64_t B,
                             int64_t row_bytes, int32_t *draft_kv_len, int32_t *recompute,
                             int32_t *status, cudaStream_t stream);
+
+}  // namespace mtpspec
+
+namespace mtpspec {
+
+// Serial greedy draft steps (draft_steps.cu).
+struct DraftStepsArgs {
+    const void *embed;       // bf16 [V, H]
+    const int32_t *next_ids; // [M]
+    const int32_t *positions;  // [M] or nullptr
+    const void *hidden;      // bf16 [M, H]
+    const void *enorm_w, *hnorm_w, *eh_proj_w;  // bf16 [H], [H], [H, 2H]
+    const void *norm_w;      // bf16 [H] or nullptr
+    const void *lm_head_w;   // bf16 [V, H]
+    float eps;
+    int64_t M, H, V;
+    int32_t D;
+    int32_t *draft_ids;      // [M, D]
+    void *hidden_out;        // bf16 [D, M, H] or nullptr
+    void *workspace;
+    int32_t *status;
+};
+size_t draft_steps_workspace_bytes(int64_t M, int64_t H, int64_t V);
+cudaError_t run_draft_steps(const DraftStepsArgs &a, cudaStream_t stream);
 
 }  // namespace mtpspec

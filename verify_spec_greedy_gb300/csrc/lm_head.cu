@@ -23,7 +23,7 @@ constexpr int PICK_THREADS = 256;
 // One warp per token: the largest of its o_tiles keys.
 __global__ void __launch_bounds__(PICK_THREADS)
 k_lm_head_pick(const unsigned long long *__restrict__ keys, int o_tiles, int64_t M,
-               int32_t *__restrict__ ids, float *__restrict__ logit) {
+               int32_t *__restrict__ ids, int64_t ids_stride, float *__restrict__ logit) {
     pdl_wait_primary();
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (PICK_THREADS / 32) + (threadIdx.x >> 5);
@@ -34,7 +34,7 @@ k_lm_head_pick(const unsigned long long *__restrict__ keys, int o_tiles, int64_t
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
     if (lane == 0) {
-        ids[t] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(best));
+        ids[t * ids_stride] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(best));
         if (logit) logit[t] = key_to_float(static_cast<uint32_t>(best >> 32));
     }
 }
@@ -77,7 +77,7 @@ cudaError_t run_lm_head_greedy(const LmHeadArgs &a, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, lh::k_lm_head_pick, static_cast<const unsigned long long *>(keys),
-                           o_tiles, a.M, a.ids, a.logit);
+                           o_tiles, a.M, a.ids, a.ids_stride, a.logit);
     if (e == cudaSuccess) count_launches(1);
     return e;
 }

@@ -570,8 +570,9 @@ template <int BN, int STAGES, bool AM = false>
 static cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const tg::Params &p,
                                const GemmPlan &g, cudaStream_t stream) {
     constexpr int smem = STAGES * (tg::A_BYTES + BN * tg::BK * 2) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(tg::k_gemm<BN, STAGES, AM>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static AttrCache attr;
+    cudaError_t e = ensure_attr(tg::k_gemm<BN, STAGES, AM>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem, attr);
     if (e != cudaSuccess) return e;
     const dim3 grid = AM ? dim3(g.t_tiles, g.o_tiles, 1) : dim3(g.o_tiles, g.t_tiles, g.splits);
     tg::k_gemm<BN, STAGES, AM><<<grid, tg::NTHREADS, smem, stream>>>(ma, mb, p);
@@ -627,8 +628,9 @@ static cudaError_t launch_gemm_argmax(const CUtensorMap &ma, const CUtensorMap &
                                       const tg::Params &p, int t_tiles, int n_tiles,
                                       cudaStream_t stream) {
     constexpr int smem = STAGES * (tg::A_BYTES + BN * tg::BK * 2) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(tg::k_gemm_argmax<BN, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static AttrCache attr;
+    cudaError_t e = ensure_attr(tg::k_gemm_argmax<BN, STAGES>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem, attr);
     if (e != cudaSuccess) return e;
     const int grid = n_tiles < kPlanSMs ? n_tiles : kPlanSMs;  // persistent: one CTA per SM
     tg::k_gemm_argmax<BN, STAGES><<<grid, tg::NTHREADS, smem, stream>>>(ma, mb, p, t_tiles, n_tiles);
