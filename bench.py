@@ -391,7 +391,8 @@ def run_gpu(args, rank, world, dist):
 def run_sweep(args):
     """Per workload: one verify call (spec_verify_greedy for a greedy workload, else
     spec_verify_sample), one mtp_draft_input call of its draft-token count and one
-    mtp_lm_head_greedy call of one token per row, each timed
+    mtp_lm_head_greedy call of one token per row, the state snapshot and fix-up, and
+    mtp_draft_steps (D steps, replayed from a CUDA graph), each timed
     alone with CUDA events after an L2 flush (a write of twice the L2), median of the
     launches; rows/s, tokens/s and the fraction of the roofline that bounds each."""
     import numpy as np
@@ -489,7 +490,36 @@ def run_sweep(args):
             xn = (xf * torch.rsqrt((xf * xf).mean(-1, keepdim=True) + 1e-6) * nl.float()).to(torch.bfloat16)
             return torch.argmax(xn @ Wl.t(), dim=-1)
         cms = timed(lib_pick, 10)
-        del Wl
+        # the serial draft loop: D steps of one token per row (embedding gather with the
+        # position-0 mask, input stage, stub block, output-layer pick), replayed from one
+        # CUDA graph
+        El = (torch.randn((V, Hl), device=dev, generator=gen) * 0.5).to(torch.bfloat16)
+        ids0 = torch.randint(0, V, (Ml,), dtype=torch.int32, device=dev, generator=gen)
+        pos0 = torch.randint(0, 4, (Ml,), dtype=torch.int32, device=dev, generator=gen)
+        dids = torch.empty((Ml, D), dtype=torch.int32, device=dev)
+        wss = torch.empty(lib.mtp_draft_steps_workspace_bytes(Ml, Hl, V), dtype=torch.uint8, device=dev)
+        we_s, wh_s = to_dev(di["we"]), to_dev(di["wh"])
+        Wp_s = to_dev(di["W"])
+        steps_call = lambda: lib.mtp_draft_steps(El, ids0, hl, we_s, wh_s, Wp_s, Wl, dids, 1e-6,
+                                                 norm_w=nl, positions=pos0, workspace=wss)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            steps_call()
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            steps_call()
+        graph.replay()
+        torch.cuda.synchronize()
+        sms_ = timed(graph.replay, 10)
+        sbytes_ = D * (V * Hl * 2 + 2 * Hl * 2 * Hl * 2 + 6 * Ml * Hl * 2)
+        steps = {"M": Ml, "D": D, "ms": round(sms_, 4),
+                 "draft_tokens_per_s": round(Ml * D / (sms_ / 1e3), 1), "graph": True,
+                 "roofline": {"bound": "hbm", "achieved": round(sbytes_ / (sms_ / 1e3) / 1e9, 1),
+                              "peak": hbm, "unit": "GB/s",
+                              "frac": round(sbytes_ / (sms_ / 1e3) / 1e9 / hbm, 4), "bytes": sbytes_}}
+        del Wl, El, graph
         lbytes = V * Hl * 2 + 2 * Ml * Hl * 2 + Hl * 2 + Ml * 4
         lflop = 2.0 * Ml * Hl * V
         if lflop / (tflops * 1e12) > lbytes / (hbm * 1e9):
@@ -535,6 +565,7 @@ def run_sweep(args):
                                "tokens_per_s": round(Ml / (lms / 1e3), 1), "roofline": lroof,
                                "cublas_matmul_argmax_ms": round(cms, 4)},
             "state": state,
+            "draft_steps": steps,
             "peaks": hbm_kind}), flush=True)
     return 0
 

@@ -174,7 +174,6 @@ struct __align__(16) Shared {
     int32_t deg[2];   // a row of all -inf: a point mass on id 0
     int32_t mode[2];  // 0 no filter, 1 candidates, 2 exact bisection
     int32_t b1[2], b2[2], nbu[2];
-    float xc[2][2];   // the candidates' values x lie in (xc[r][1], xc[r][0]]
     unsigned long long tgt[2];
     int32_t flags;    // bit 0: a bulk copy timed out; bit 1: an exchange timed out
     float fpick[2];
@@ -298,25 +297,6 @@ __device__ __forceinline__ int32_t block_incl_max_i32(int32_t v, int32_t *scratc
     int32_t before = -1;
     for (int w = 0; w < warp; ++w) before = max(before, scratch[w]);
     return max(before, incl);
-}
-
-// X(t): the largest non-NaN x with fmaf(x, a, b) >= t, for a < 0 and finite b (f falls as x
-// grows, so the x that pass form a prefix in value order).  A 32-way search over the order
-// keys by one warp (every lane calls it with the same arguments): each round tests 32
-// evenly spaced keys, so the 2^32 keys take at most 7 rounds.
-__device__ __forceinline__ float x_level(float a, float b, float t, int lane) {
-    unsigned long long lo = 0x007FFFFFull;  // key of -inf: f = +inf >= t
-    unsigned long long hi = 0xFF800000ull;  // key of +inf: f = -inf < t
-#pragma unroll 1
-    for (int it = 0; it < 8 && hi - lo > 1; ++it) {
-        const unsigned long long step = (hi - lo + 31) / 32;
-        const unsigned long long k = lo + static_cast<unsigned long long>(lane + 1) * step;
-        const bool pass = k < hi && fmaf(key_to_float(static_cast<uint32_t>(k)), a, b) >= t;
-        const unsigned long long n = static_cast<unsigned long long>(__popc(__ballot_sync(0xFFFFFFFFu, pass)));
-        hi = min(hi, lo + (n + 1) * step);
-        lo += n * step;
-    }
-    return key_to_float(static_cast<uint32_t>(lo));
 }
 
 // The plan's barrier of row r's group (hardware barriers 1 and 2; 0 is __syncthreads).
@@ -1004,9 +984,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                         }
                     }
                     group_barrier<PL>(r);
-                    if (hw < 2) {
-                        // the group's warps 0 and 1: the bins to gather and the mode, then the
-                        // gathered bins' range in value (warp 0 its top, warp 1 its bottom)
+                    if (j == 0) {
                         int32_t b1 = 0, b2 = sh.pb2[r];
                         uint32_t ncand;
                         bool slow;
@@ -1022,22 +1000,10 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                             ncand = c2b - sh.pcc1[r];
                         }
                         if (ncand > static_cast<uint32_t>(NT) || ncand == 0) slow = true;
-                        if (j == 0) {
-                            sh.mode[r] = slow ? 2 : 1;
-                            sh.b1[r] = b1;
-                            sh.b2[r] = b2;
-                            sh.lcnt[r] = 0;
-                        }
-                        if (!slow) {
-                            // tz = max(f(x), 0) with f(x) = fmaf(x, -c2 R, tzb), which falls as x
-                            // grows: tz >= b1 iff x <= X(b1) when b1 > 0 (always when b1 = 0),
-                            // and tz < b2 + 1 iff x > X(b2 + 1)
-                            float xl = INFINITY;
-                            if (hw == 1 || b1 > 0)
-                                xl = x_level(-c2 * static_cast<float>(R), sh.tzb[r],
-                                             static_cast<float>(hw == 0 ? b1 : b2 + 1), lane);
-                            if (lane == 0) sh.xc[r][hw] = xl;
-                        }
+                        sh.mode[r] = slow ? 2 : 1;
+                        sh.b1[r] = b1;
+                        sh.b2[r] = b2;
+                        sh.lcnt[r] = 0;
                     }
                 }
                 __syncthreads();
@@ -1050,9 +1016,14 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 for (int r = 0; r < nrows; ++r) {
                     if (sh.mode[r] != 1) continue;
                     // the candidates: elements of bins [b1, b2] (bin bn = trunc(tz): bn >= b1 iff
-                    // tz >= b1, bn <= b2 iff tz < b2 + 1), i.e. the values in the plan's range
-                    const float xtop = sh.xc[r][0], xbot = sh.xc[r][1];
-                    auto is_cand = [&](float x) -> bool { return x <= xtop && x > xbot; };
+                    // tz >= b1, bn <= b2 iff tz < b2 + 1)
+                    const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
+                    const float fb1 = static_cast<float>(sh.b1[r]);
+                    const float fb2 = static_cast<float>(sh.b2[r] + 1);
+                    auto is_cand = [&](float x) -> bool {
+                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
+                        return tz >= fb1 && tz < fb2;
+                    };
                     // one sweep; a vector that holds candidates claims their slots at once (the
                     // order of the slots does not matter: every later step depends on values)
                     const uint4 *vp = reinterpret_cast<const uint4 *>(sdat(r));
