@@ -84,9 +84,16 @@ def max_over_ranks(x, dist):
     if dist is None:
         return x
     import torch
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_value(units_per_step, steps, world, ms_max):
+    """Units per second of the whole job: every rank runs its own replica of the step, so
+    the job processes world x units_per_step x steps units in the slowest rank's time."""
+    return world * units_per_step * steps / (ms_max / 1e3)
 
 
 # ---------------------------------------------------------------- workload bytes
@@ -319,7 +326,7 @@ def run_gpu(args, rank, world, dist):
     ms_max = max_over_ranks(ms, dist)
     verify_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_v)
     rows_per_step = B * (D + 1)
-    value = world * rows_per_step * args.steps / (ms_max / 1e3)
+    value = whole_job_value(rows_per_step, args.steps, world, ms_max)
 
     # end to end through the C ABI with host buffers: pinned inputs copied in, results out
     host_in = {k: torch.from_numpy(np.ascontiguousarray(
@@ -357,7 +364,7 @@ def run_gpu(args, rank, world, dist):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist)
-    e2e_value = world * rows_per_step * args.e2e_steps / (e2e_ms / 1e3)
+    e2e_value = whole_job_value(rows_per_step, args.e2e_steps, world, e2e_ms)
 
     peak, peak_kind = measured_peaks()
     vb = verify_bytes(x)
