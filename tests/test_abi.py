@@ -107,7 +107,7 @@ def test_lm_head_greedy_host_checks(so):
     assert call(wsb=100) == -4
     assert call(ws=C.c_void_p(4100)) == -4       # not 256-byte aligned
     need = so.mtp_lm_head_greedy_workspace_bytes(4, 64, 1000)
-    assert need == 256 + 1024 + 4 * 8 * 8
+    assert need == 256 + 1024 + 4 * 4 * 8   # keys: 4 tokens x 4 blocks of 256 ids
     assert so.mtp_lm_head_greedy_workspace_bytes(4, 12, 1000) == 0
     assert so.mtp_lm_head_greedy_workspace_bytes(0, 64, 1000) == 0
 

@@ -12,10 +12,10 @@
 // K range is split across CTAs, reduced by a second kernel).  Every mbarrier wait is
 // bounded; a wait that gives up sets a flag word in the workspace and the CTA drains out.
 //
-// The same kernel with the argmax epilogue is the draft head's output layer with the
-// greedy pick: A = the output-layer weight [V, H], B = the tokens' hidden states [M, H];
-// the epilogue reduces each token's column of the 128 x BN logit tile to its largest
-// value and lowest id, so the logits never leave the SM.
+// k_head_argmax below is the draft head's output layer with the greedy pick: the same
+// pipeline with the tokens as the 128-row operand and 256 vocabulary rows as the N side,
+// persistent, with an epilogue that keeps each token's largest logit and its lowest id, so
+// the logits never leave the SM.
 #include <algorithm>
 
 #include <cuda.h>
@@ -37,7 +37,7 @@ constexpr int A_BYTES = BM * BK * 2;
 struct Params {
     uint16_t *y;       // [Mt, H] bf16, when splits == 1
     float *part;       // [splits, Mt, H] fp32 partial sums, when splits > 1
-    unsigned long long *keys;  // argmax epilogue: [Mt, o_tiles] (order key << 32 | ~id)
+    unsigned long long *keys;  // k_head_argmax: [Mt, o_tiles] (order key << 32 | ~id)
     unsigned *err;     // flag word
     int H, Mt, K;      // H: rows of A (output features, or the vocabulary)
     int kb_total, kb_per_split, splits, o_tiles;
@@ -131,7 +131,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int BN, int STAGES, bool AM>
+template <int BN, int STAGES>
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
        const Params p) {
@@ -146,10 +146,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
     uint8_t *ring = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // the argmax grid runs the token tiles of one weight tile side by side (x fastest), so
-    // that the weight tile is read from HBM once and from L2 by the others
-    const int ob = AM ? blockIdx.y : blockIdx.x;
-    const int o0 = ob * BM, t0 = (AM ? blockIdx.x : blockIdx.y) * BN, split = blockIdx.z;
+    const int o0 = blockIdx.x * BM, t0 = blockIdx.y * BN, split = blockIdx.z;
     const int kb0 = split * p.kb_per_split;
     const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
     const int nkb = max(0, kb1 - kb0);
@@ -219,41 +216,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
         }
         (void)ok;
         mma_commit(&accb);  // arrives once every MMA issued above has completed
-    } else if (AM && warp >= 2) {
-        // ---- argmax epilogue: per token column, the warp's largest order key over its 32
-        // rows (redux max), then the lowest id holding it (redux min); the four warps'
-        // results meet in shared memory.  Rows past the vocabulary take key 0, below every
-        // value's key.
-        __shared__ unsigned long long red[4][BN];
-        const int q = warp & 3;
-        const bool ready = mbar_wait(&accb, 0);
-        tc_fence_after();
-        if (!ready) atomicOr(&abort_flag, 1);
-        const int o = o0 + q * 32 + lane;
-        const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
-        for (int c = 0; c < BN; c += 8) {
-            float v[8];
-            tmem_ld8(trow + c, v);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const uint32_t key = (o < p.H && ready && nkb > 0) ? order_key(v[u]) : 0u;
-                const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, key);
-                const uint32_t omin =
-                    __reduce_min_sync(0xFFFFFFFFu, key == kmax ? static_cast<uint32_t>(o) : 0xFFFFFFFFu);
-                if (lane == u)
-                    red[q][c + u] = (static_cast<unsigned long long>(kmax) << 32) | (0xFFFFFFFFu - omin);
-            }
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
-        for (int c = threadIdx.x - 64; c < BN; c += 128) {
-            const int t = t0 + c;
-            if (t < p.Mt) {
-                const unsigned long long k =
-                    max(max(red[0][c], red[1][c]), max(red[2][c], red[3][c]));
-                p.keys[static_cast<size_t>(t) * p.o_tiles + ob] = k;
-            }
-        }
-    } else if (!AM && warp >= 2) {
+    } else if (warp >= 2) {
         // ---- epilogue: TMEM lanes 32*(warp % 4) .. +31 are rows of this warp
         const int q = warp & 3;
         const bool ready = mbar_wait(&accb, 0);
@@ -294,42 +257,34 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
     }
 }
 
-// OR of a predicate over the four epilogue warps (named barrier 1, 128 threads), which all
-// of them reach once per tile.
-__device__ __forceinline__ bool epi_vote_any(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, 1, 128, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v))
-        : "memory");
-    return r != 0;
-}
+// The output layer's argmax GEMM, persistent: logits[t, v] = sum_k X[t, k] W[v, k] with the
+// tokens as the 128-row MMA operand and HV = 256 vocabulary rows as the N side.  A tile is
+// (token tile, vocabulary tile); CTA c takes tiles c, c + G, ... with the token tiles of one
+// vocabulary tile side by side, so the CTAs that share a weight tile run together and it
+// leaves HBM once.  Each stage carries 32 KB of weight (and 16 KB of tokens), so four
+// stages keep 128 KB of weight in flight per SM.  The accumulator is double-buffered in
+// tensor memory (2 x 256 columns): the epilogue of tile j reads one buffer while tile j + 1
+// accumulates into the other.  In the epilogue each thread owns one token's row of the
+// tile: it scans its 256 logits in id order and keeps the largest order key and the first
+// id holding it, then writes one key (order key << 32 | ~id) per (token, vocabulary tile).
+// Barriers: the stage ring (full / empty), accf[b] (MMA -> epilogue) and acce[b] (epilogue
+// -> MMA).  Every wait is bounded; a wait that gives up raises the CTA's abort flag and
+// every role leaves its loop.
+constexpr int HT = 128;  // tokens per tile (MMA M)
+constexpr int HV = 256;  // vocabulary rows per tile (MMA N)
 
-// The argmax GEMM as a persistent kernel: CTA c takes tiles c, c + G, c + 2G, ... (tile i
-// = token tile i % t_tiles of vocabulary tile i / t_tiles, so the CTAs that share a weight
-// tile run together and read it from HBM once).  The accumulator is double-buffered in
-// tensor memory (2 x BN columns): the epilogue warps reduce tile j from one buffer while
-// the MMA warp accumulates tile j + 1 into the other, and the producer streams the next
-// tile's stages without a gap.  Barriers: the stage ring (full / empty, as in k_gemm),
-// accf[b] (MMA -> epilogue: buffer b holds a finished tile) and acce[b] (epilogue -> MMA:
-// buffer b has been read).  Every wait is bounded; a wait that gives up raises the CTA's
-// abort flag and every role leaves its loop.
-template <int BN, int STAGES>
+template <int STAGES>
 __global__ void __launch_bounds__(NTHREADS, 1)
-k_gemm_argmax(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+k_head_argmax(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
               const Params p, int t_tiles, int n_tiles) {
-    constexpr int B_BYTES = BN * BK * 2;
-    constexpr int STAGE = A_BYTES + B_BYTES;
-    constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+    constexpr int X_BYTES = HT * BK * 2;
+    constexpr int W_BYTES = HV * BK * 2;
+    constexpr int STAGE = X_BYTES + W_BYTES;
+    constexpr uint32_t TMEM_COLS = 2 * HV;
     extern __shared__ uint8_t smem_dyn[];
     __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], accf[2], acce[2];
     __shared__ uint32_t tmem_base;
     __shared__ volatile int abort_flag;
-    __shared__ unsigned long long red[4][BN];
 
     uint8_t *ring = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -348,8 +303,8 @@ k_gemm_argmax(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         }
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        prefetch_map(&tmA);
-        prefetch_map(&tmB);
+        prefetch_map(&tmX);
+        prefetch_map(&tmW);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -367,7 +322,7 @@ k_gemm_argmax(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         // ---- producer: every tile's K-blocks through the ring, one global stage counter
         int it = 0;
         for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += G) {
-            const int o0 = (tile / t_tiles) * BM, t0 = (tile % t_tiles) * BN;
+            const int t0 = (tile % t_tiles) * HT, v0 = (tile / t_tiles) * HV;
             for (int i = 0; i < nkb; ++i, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
@@ -375,13 +330,13 @@ k_gemm_argmax(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 if (abort_flag) break;
                 uint8_t *a = ring + s * STAGE;
                 mbar_expect_tx(&full[s], STAGE);
-                tma_load_2d(a, &tmA, i * BK, o0, &full[s]);
-                tma_load_2d(a + A_BYTES, &tmB, i * BK, t0, &full[s]);
+                tma_load_2d(a, &tmX, i * BK, t0, &full[s]);
+                tma_load_2d(a + X_BYTES, &tmW, i * BK, v0, &full[s]);
             }
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer: tile j accumulates into buffer j & 1 once the epilogue has read it
-        constexpr uint32_t idesc = instr_desc(BM, BN);
+        constexpr uint32_t idesc = instr_desc(HT, HV);
         int it = 0, j = 0;
         for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += G, ++j) {
             const int b = j & 1;
@@ -390,7 +345,7 @@ k_gemm_argmax(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 break;
             }
             tc_fence_after();
-            const uint32_t acc = tmem + static_cast<uint32_t>(b * BN);
+            const uint32_t acc = tmem + static_cast<uint32_t>(b * HV);
             for (int i = 0; i < nkb; ++i, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
@@ -398,10 +353,10 @@ k_gemm_argmax(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 if (abort_flag) break;
                 tc_fence_after();
                 const uint32_t a = smem_addr(ring + s * STAGE);
-                const uint32_t bb = a + A_BYTES;
+                const uint32_t w = a + X_BYTES;
 #pragma unroll
                 for (int k = 0; k < BK / UK; ++k)
-                    mma_bf16(acc, smem_desc_sw128(a + k * 32), smem_desc_sw128(bb + k * 32), idesc,
+                    mma_bf16(acc, smem_desc_sw128(a + k * 32), smem_desc_sw128(w + k * 32), idesc,
                              (i > 0 || k > 0) ? 1u : 0u);
                 mma_commit(&empty[s]);
             }
@@ -409,47 +364,40 @@ k_gemm_argmax(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             mma_commit(&accf[b]);  // arrives when this tile's MMAs have completed
         }
     } else if (warp >= 2) {
-        // ---- epilogue: per token column the largest order key over the tile's 128 rows and
-        // the lowest id holding it (redux in each warp, then across the four warps)
+        // ---- epilogue: TMEM lane 32 (warp % 4) + lane is this thread's token
         const int q = warp & 3;
         int j = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += G, ++j) {
             const int b = j & 1;
-            const int ob = tile / t_tiles, o0 = ob * BM, t0 = (tile % t_tiles) * BN;
-            // the four warps leave together or not at all (a named barrier would otherwise
-            // wait for a warp that has left); the vote is also the point after which the
-            // previous tile's red[] has been read
-            const bool bad = abort_flag || !mbar_wait(&accf[b], static_cast<uint32_t>(j >> 1) & 1u);
-            if (epi_vote_any(bad)) {
+            const int vt = tile / t_tiles, v0 = vt * HV;
+            const int t = (tile % t_tiles) * HT + q * 32 + lane;
+            if (abort_flag || !mbar_wait(&accf[b], static_cast<uint32_t>(j >> 1) & 1u)) {
                 abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            const int o = o0 + q * 32 + lane;
-            const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
-            for (int c = 0; c < BN; c += 8) {
+            const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * HV);
+            const int nv = min(HV, p.H - v0);  // vocabulary rows of this tile
+            uint32_t best = 0;                 // below every value's order key
+            int bv = v0;
+            for (int c = 0; c < HV; c += 8) {
                 float v[8];
                 tmem_ld8(trow + c, v);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const uint32_t key = o < p.H ? order_key(v[u]) : 0u;
-                    const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, key);
-                    const uint32_t omin = __reduce_min_sync(
-                        0xFFFFFFFFu, key == kmax ? static_cast<uint32_t>(o) : 0xFFFFFFFFu);
-                    if (lane == u)
-                        red[q][c + u] = (static_cast<unsigned long long>(kmax) << 32) | (0xFFFFFFFFu - omin);
+                    const uint32_t key = c + u < nv ? order_key(v[u]) : 0u;
+                    if (key > best) {  // strictly larger: the first id keeps a tie
+                        best = key;
+                        bv = v0 + c + u;
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&acce[b])) : "memory");
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // red[] complete
-            for (int c = threadIdx.x - 64; c < BN; c += 128) {
-                const int t = t0 + c;
-                if (t < p.Mt)
-                    p.keys[static_cast<size_t>(t) * p.o_tiles + ob] =
-                        max(max(red[0][c], red[1][c]), max(red[2][c], red[3][c]));
-            }
+            if (t < p.Mt)
+                p.keys[static_cast<size_t>(t) * p.o_tiles + vt] =
+                    (static_cast<unsigned long long>(best) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(bv));
         }
     }
     tc_fence_before();
@@ -566,16 +514,16 @@ size_t gemm_workspace_bytes(int64_t Mt, int64_t H) {
     return 256 + part;  // flag word, then the partial sums
 }
 
-template <int BN, int STAGES, bool AM = false>
+template <int BN, int STAGES>
 static cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const tg::Params &p,
                                const GemmPlan &g, cudaStream_t stream) {
     constexpr int smem = STAGES * (tg::A_BYTES + BN * tg::BK * 2) + 1024;
     static AttrCache attr;
-    cudaError_t e = ensure_attr(tg::k_gemm<BN, STAGES, AM>,
+    cudaError_t e = ensure_attr(tg::k_gemm<BN, STAGES>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem, attr);
     if (e != cudaSuccess) return e;
-    const dim3 grid = AM ? dim3(g.t_tiles, g.o_tiles, 1) : dim3(g.o_tiles, g.t_tiles, g.splits);
-    tg::k_gemm<BN, STAGES, AM><<<grid, tg::NTHREADS, smem, stream>>>(ma, mb, p);
+    const dim3 grid(g.o_tiles, g.t_tiles, g.splits);
+    tg::k_gemm<BN, STAGES><<<grid, tg::NTHREADS, smem, stream>>>(ma, mb, p);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
@@ -623,39 +571,19 @@ cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, i
     return e;
 }
 
-template <int BN, int STAGES>
-static cudaError_t launch_gemm_argmax(const CUtensorMap &ma, const CUtensorMap &mb,
-                                      const tg::Params &p, int t_tiles, int n_tiles,
-                                      cudaStream_t stream) {
-    constexpr int smem = STAGES * (tg::A_BYTES + BN * tg::BK * 2) + 1024;
-    static AttrCache attr;
-    cudaError_t e = ensure_attr(tg::k_gemm_argmax<BN, STAGES>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem, attr);
-    if (e != cudaSuccess) return e;
-    const int grid = n_tiles < kPlanSMs ? n_tiles : kPlanSMs;  // persistent: one CTA per SM
-    tg::k_gemm_argmax<BN, STAGES><<<grid, tg::NTHREADS, smem, stream>>>(ma, mb, p, t_tiles, n_tiles);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) count_launches(1);
-    return e;
-}
-
 // The output layer's logits tile by tile with the argmax epilogue: keys [Mt, o_tiles], one
-// per (token, 128-row block of the vocabulary).  Up to 256 tokens, one token tile of the
-// narrowest width that holds them (the weight is streamed once); beyond, tiles of 256
-// tokens whose CTAs for one weight tile run side by side.  No K split.
-int lm_head_o_tiles(int64_t V) { return static_cast<int>((V + tg::BM - 1) / tg::BM); }
+// per (token, block of 256 vocabulary rows).  Token tiles of 128; the persistent grid has
+// one CTA per SM (fewer when there are fewer tiles).  No K split.
+int lm_head_o_tiles(int64_t V) { return static_cast<int>((V + tg::HV - 1) / tg::HV); }
 
 cudaError_t run_gemm_argmax(const void *W, const void *X, int64_t V, int64_t Mt, int64_t K,
                             unsigned long long *keys, unsigned *err, cudaStream_t stream) {
-    GemmPlan g;
-    g.o_tiles = lm_head_o_tiles(V);
-    g.kb_total = static_cast<int>((K + tg::BK - 1) / tg::BK);
-    g.BN = Mt <= 16 ? 16 : (Mt <= 32 ? 32 : (Mt <= 64 ? 64 : (Mt <= 128 ? 128 : (Mt <= 192 ? 192 : 256))));
-    g.t_tiles = static_cast<int>((Mt + g.BN - 1) / g.BN);
-    g.splits = 1;
-    g.kb_per_split = g.kb_total;
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, W, V, K, tg::BM) || !make_map(&mb, X, Mt, K, g.BN))
+    constexpr int STAGES = 4;
+    const int t_tiles = static_cast<int>((Mt + tg::HT - 1) / tg::HT);
+    const int v_tiles = lm_head_o_tiles(V);
+    const int n_tiles = t_tiles * v_tiles;
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, X, Mt, K, tg::HT) || !make_map(&mw, W, V, K, tg::HV))
         return cudaErrorInvalidValue;
     tg::Params p = {};
     p.keys = keys;
@@ -663,19 +591,20 @@ cudaError_t run_gemm_argmax(const void *W, const void *X, int64_t V, int64_t Mt,
     p.H = static_cast<int>(V);
     p.Mt = static_cast<int>(Mt);
     p.K = static_cast<int>(K);
-    p.kb_total = g.kb_total;
-    p.kb_per_split = g.kb_per_split;
+    p.kb_total = static_cast<int>((K + tg::BK - 1) / tg::BK);
+    p.kb_per_split = p.kb_total;
     p.splits = 1;
-    p.o_tiles = g.o_tiles;
-    const int n_tiles = g.o_tiles * g.t_tiles;
-    switch (g.BN) {
-    case 16: return launch_gemm_argmax<16, 12>(ma, mb, p, g.t_tiles, n_tiles, stream);
-    case 32: return launch_gemm_argmax<32, 10>(ma, mb, p, g.t_tiles, n_tiles, stream);
-    case 64: return launch_gemm_argmax<64, 8>(ma, mb, p, g.t_tiles, n_tiles, stream);
-    case 128: return launch_gemm_argmax<128, 5>(ma, mb, p, g.t_tiles, n_tiles, stream);
-    case 192: return launch_gemm_argmax<192, 4>(ma, mb, p, g.t_tiles, n_tiles, stream);
-    default: return launch_gemm_argmax<256, 4>(ma, mb, p, g.t_tiles, n_tiles, stream);
-    }
+    p.o_tiles = v_tiles;
+    constexpr int smem = STAGES * (tg::HT + tg::HV) * tg::BK * 2 + 1024;
+    static AttrCache attr;
+    cudaError_t e = ensure_attr(tg::k_head_argmax<STAGES>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem, attr);
+    if (e != cudaSuccess) return e;
+    const int grid = n_tiles < kPlanSMs ? n_tiles : kPlanSMs;  // persistent: one CTA per SM
+    tg::k_head_argmax<STAGES><<<grid, tg::NTHREADS, smem, stream>>>(mx, mw, p, t_tiles, n_tiles);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
 }
 
 }  // namespace mtpspec
