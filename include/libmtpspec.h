@@ -245,8 +245,8 @@ int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draf
  *   workspace      >= spec_verify_workspace_bytes(B, D, V) bytes, 256-byte aligned;
  *                  no initial contents are needed
  *   status         int32 [1] or NULL
- *   B >= 0, 1 <= D <= 64, 1 <= V <= 408,064 (fp32) or 816,128 (bf16), or with a one-hot
- *   draft 652,800 (fp32) or 1,305,600 (bf16): a CTA of a cluster of at most 16 holds its
+ *   B >= 0, 1 <= D <= 64, 1 <= V <= 407,552 (fp32) or 815,104 (bf16), or with a one-hot
+ *   draft 652,288 (fp32) or 1,304,576 (bf16): a CTA of a cluster of at most 16 holds its
  *   slices of the staged rows in shared memory; a larger V returns MTPSPEC_ERR_SHAPE.
  */
 int spec_verify_sample(const void *target_logits, const void *draft_logits, int dtype,

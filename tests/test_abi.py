@@ -70,16 +70,16 @@ def test_sampling_vocabulary_limit(so):
     # fit a CTA's shared memory at 16 CTAs per cluster; an empty batch (B = 0) passes every
     # check that does not touch device memory
     nul, draft = None, C.c_void_p(256)
-    for dq, dtype, vmax in ((draft, 0, 408064), (draft, 1, 816128), (nul, 0, 652800),
-                            (nul, 1, 1305600)):
+    for dq, dtype, vmax in ((draft, 0, 407552), (draft, 1, 815104), (nul, 0, 652288),
+                            (nul, 1, 1304576)):
         args = lambda V: (nul, dq, dtype, nul, nul, nul, nul, 0, 0, 1, V, nul, nul, nul, nul,
                           nul, 0, nul, nul)
         assert so.spec_verify_sample(*args(vmax)) == 0
         assert so.spec_verify_sample(*args(vmax + 1)) == -3
     # the workspace query knows neither the logit type nor the mode: it refuses what no
     # combination accepts
-    assert so.spec_verify_workspace_bytes(1, 1, 1305600) > 0
-    assert so.spec_verify_workspace_bytes(1, 1, 1305601) == 0
+    assert so.spec_verify_workspace_bytes(1, 1, 1304576) > 0
+    assert so.spec_verify_workspace_bytes(1, 1, 1304577) == 0
 
 
 def test_lm_head_greedy_host_checks(so):

@@ -117,6 +117,7 @@ struct __align__(16) Shared {
     unsigned long long xbar[NXB];      // exchange barriers (C arrivals each)
     float4 e1[2][MAXC];                // E1, by unit parity: (m0, s0, m1, s1) per CTA
     float2 e1d[2];                     // E1, by unit parity: the draft token's logits
+    uint32_t e1k[2][MAXC];             // E1, by unit parity: each CTA's view of the row's first rejection
     // Buffers whose lifetimes within a unit do not overlap share storage.  The histograms
     // per row hold top-k counts, or top-p weights as 16-bit fixed point relative to each
     // bin's upper edge.  Peers write rsin before E2b, hist before the plan and cand after
@@ -478,6 +479,9 @@ struct Params {
     int32_t G;      // clusters in the persistent grid
     UnitResult *res;
     int32_t *status;
+    // per row, the first position found rejected so far (0xFFFFFFFF: none), or nullptr: a
+    // unit behind a rejected position of its row skips its draw, which no output reads
+    uint32_t *dead;
 };
 
 __device__ __forceinline__ bool row_sampled(const Params &P, int64_t b) {
@@ -530,10 +534,13 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     cluster_arrive_release();  // peers may touch this CTA's shared memory after the wait below
     pdl_launch_dependents();   // the greedy-row kernel runs beside this grid
 
+    // units run position-major (u = j * B + b), so that a row's earlier positions are
+    // usually decided before its later ones start
+    const int Bi = static_cast<int>(P.B);
     auto load_params = [&](int u) -> UnitParams {
         UnitParams q;
-        q.b = u / (D + 1);
-        q.j = u - q.b * (D + 1);
+        q.j = u / Bi;
+        q.b = u - q.j * Bi;
         q.tau = P.tau[q.b];
         q.kk = P.topk ? P.topk[q.b] : 0;
         q.pp = P.topp ? P.topp[q.b] : 1.0f;
@@ -564,7 +571,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     };
     auto next_unit = [&](int u) -> int {
         for (u += G; u < U; u += G)
-            if (row_sampled(P, u / (D + 1))) return u;
+            if (row_sampled(P, u % Bi)) return u;
         return -1;
     };
     // lane 0 of warps 0 .. 2 * NCH - 1: arm chunk barrier (warp / NCH, warp % NCH) exactly
@@ -614,7 +621,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     };
 
     int u = -1;
-    if (g < U) u = row_sampled(P, g / (D + 1)) ? g : next_unit(g);
+    if (g < U) u = row_sampled(P, g % Bi) ? g : next_unit(g);
     UnitParams cnx = {0, 0, 1.0f, 1.0f, 0, -1};  // this unit's parameters
     UnitParams nxt = {0, 0, 1.0f, 1.0f, 0, -1};  // the next unit's
     int un = -1;
@@ -724,6 +731,8 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         if (warp == 0 && lane < static_cast<int>(C)) {
             const float4 part = make_float4(cm0, cs0, cm1, cs1);  // row 1: (-inf, 0) when absent
             st_peer_v4(peer_addr(smem_addr(&sh.e1[ep][rank]), lane), part);
+            const uint32_t dk = P.dead ? *reinterpret_cast<volatile const uint32_t *>(P.dead + b) : 0xFFFFFFFFu;
+            st_peer_u32(peer_addr(smem_addr(&sh.e1k[ep][rank]), lane), dk);
             if (d_here) st_peer_v2(peer_addr(smem_addr(&sh.e1d[ep]), lane), make_float2(sh.xd[0], sh.xd[1]));
             xarrive(&sh.xbar[XB_E1 + ep], lane);
         }
@@ -1526,8 +1535,13 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             }
         }
 
+        // a rejection is published for the row's later positions; a unit behind a position
+        // every CTA's view agrees was rejected earlier draws nothing (no output reads it)
+        if (P.dead && rank == 0 && tid == 0 && j < D && !accept) atomicMin(P.dead + b, static_cast<uint32_t>(j));
+        uint32_t dkmin = 0xFFFFFFFFu;
+        for (uint32_t c = 0; c < C; ++c) dkmin = min(dkmin, sh.e1k[ep][c]);
         // the slice buffer is free unless a draw reads it: bring in the next unit now
-        const bool draw = (j == D) || !accept;
+        const bool draw = ((j == D) || !accept) && !(dkmin < static_cast<uint32_t>(j));
         if (!draw && un >= 0) issue(nxt.b, nxt.j, true);
 
         // ---- draw (a rejected draft's residual, or the bonus).  Weights in fixed point,
@@ -1535,7 +1549,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         // are exact and agree with one another.  A distribution's weights add up to about
         // 2^31, so sums within a CTA fit 32 bits.  A degenerate target row is a point mass
         // on id 0, and so is every draw from it (its residual, when not zero, too).
-        UnitResult *res = P.res + u;
+        UnitResult *res = P.res + (static_cast<int64_t>(b) * (D + 1) + j);
         if (draw && deg0) {
             if (rank == 0 && tid == 0) res->token = 0;
         } else if (draw) {
@@ -1798,8 +1812,12 @@ static int verify_cmin(int64_t V, size_t es, int rows) {
     return 0;
 }
 
-size_t verify_workspace_bytes(int64_t B, int32_t D) {
+// Per-unit records, then each row's first rejected position (for skipping draws).
+static size_t verify_records_bytes(int64_t B, int32_t D) {
     return static_cast<size_t>(B) * static_cast<size_t>(D + 1) * sizeof(vs::UnitResult);
+}
+size_t verify_workspace_bytes(int64_t B, int32_t D) {
+    return verify_records_bytes(B, D) + ((static_cast<size_t>(B) * 4 + 15) & ~static_cast<size_t>(15));
 }
 
 bool verify_fits(int64_t V, size_t elem_bytes, bool one_hot) {
@@ -1918,7 +1936,8 @@ static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     return e;
 }
 
-cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream) {
+static cudaError_t run_verify_sample_impl(const VerifySampleArgs &a, bool row_flags,
+                                          cudaStream_t stream) {
     vs::Params p;
     p.T = a.target;
     p.Q = a.draft;
@@ -1934,6 +1953,13 @@ cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream) {
     p.G = 1;
     p.res = static_cast<vs::UnitResult *>(a.workspace);
     p.status = a.status;
+    p.dead = nullptr;
+    if (row_flags) {
+        p.dead = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(a.workspace) +
+                                              verify_records_bytes(a.B, a.D));
+        const cudaError_t e0 = cudaMemsetAsync(p.dead, 0xFF, static_cast<size_t>(a.B) * 4, stream);
+        if (e0 != cudaSuccess) return e0;
+    }
     // the sampled rows, then (beside them) the greedy rows, then the per-row finalize
     cudaError_t e = a.dtype == MTPSPEC_F32 ? launch_verify_rr<float>(p, stream)
                                            : launch_verify_rr<uint16_t>(p, stream);
@@ -1946,6 +1972,10 @@ cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
+}
+
+cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream) {
+    return run_verify_sample_impl(a, true, stream);
 }
 
 }  // namespace mtpspec
@@ -1983,7 +2013,7 @@ cudaError_t run_verify_sample_static(VerifySampleArgs a, cudaStream_t stream) {
         ptr = g_scratch_ptr[dev];
     }
     a.workspace = ptr;
-    return run_verify_sample(a, stream);
+    return run_verify_sample_impl(a, false, stream);  // no row flags: every rejection draws
 }
 
 }  // namespace mtpspec
