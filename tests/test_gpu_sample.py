@@ -257,6 +257,23 @@ def test_cluster_sizes(C, monkeypatch):
         compare(gpu_verify(x), oracle_verify(x), label=f"C={C} {dtype}")
 
 
+@pytest.mark.parametrize("order", ["row", "position"])
+@pytest.mark.parametrize("one_hot", [False, True])
+def test_unit_orders(order, one_hot, monkeypatch):
+    # both unit orders (row-major; position-major with the draws behind a rejected position
+    # skipped) give the oracle's results, and the same outputs as each other
+    monkeypatch.setenv("MTPSPEC_VERIFY_ORDER", order)
+    w = Workload(name="ord", B=40, D=4, V=20011, H=8, tau_range=(0.5, 1.2), top_p=0.9,
+                 t_std=3.0, q_noise_range=(0.3, 2.0), seed=31, philox_seed=31, greedy_frac=0.2)
+    x = make_verify_inputs(w)
+    got = gpu_verify(x, one_hot=one_hot)
+    compare(got, oracle_verify(x, one_hot=one_hot), label=f"{order} one_hot={one_hot}")
+    monkeypatch.setenv("MTPSPEC_VERIFY_ORDER", "row" if order == "position" else "position")
+    other = gpu_verify(x, one_hot=one_hot)
+    for key in got:
+        np.testing.assert_array_equal(np.asarray(got[key]), np.asarray(other[key]), err_msg=key)
+
+
 # ---------------------------------------------------------------- one-hot drafts
 
 def _greedy_half(x, rng):

@@ -482,6 +482,7 @@ struct Params {
     // per row, the first position found rejected so far (0xFFFFFFFF: none), or nullptr: a
     // unit behind a rejected position of its row skips its draw, which no output reads
     uint32_t *dead;
+    int32_t pmajor;  // units position-major (u = j B + b) rather than row-major (u = b (D+1) + j)
 };
 
 __device__ __forceinline__ bool row_sampled(const Params &P, int64_t b) {
@@ -534,13 +535,15 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     cluster_arrive_release();  // peers may touch this CTA's shared memory after the wait below
     pdl_launch_dependents();   // the greedy-row kernel runs beside this grid
 
-    // units run position-major (u = j * B + b), so that a row's earlier positions are
-    // usually decided before its later ones start
+    // many units run position-major (u = j * B + b), so that a row's earlier positions are
+    // usually decided before its later ones start; a few run row-major (u = b * (D + 1) + j)
     const int Bi = static_cast<int>(P.B);
+    const bool pmajor = P.pmajor != 0;
+    auto unit_row = [&](int u) -> int { return pmajor ? u % Bi : u / (D + 1); };
     auto load_params = [&](int u) -> UnitParams {
         UnitParams q;
-        q.j = u / Bi;
-        q.b = u - q.j * Bi;
+        q.b = unit_row(u);
+        q.j = pmajor ? u / Bi : u - q.b * (D + 1);
         q.tau = P.tau[q.b];
         q.kk = P.topk ? P.topk[q.b] : 0;
         q.pp = P.topp ? P.topp[q.b] : 1.0f;
@@ -571,7 +574,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     };
     auto next_unit = [&](int u) -> int {
         for (u += G; u < U; u += G)
-            if (row_sampled(P, u % Bi)) return u;
+            if (row_sampled(P, unit_row(u))) return u;
         return -1;
     };
     // lane 0 of warps 0 .. 2 * NCH - 1: arm chunk barrier (warp / NCH, warp % NCH) exactly
@@ -621,7 +624,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     };
 
     int u = -1;
-    if (g < U) u = row_sampled(P, g % Bi) ? g : next_unit(g);
+    if (g < U) u = row_sampled(P, unit_row(g)) ? g : next_unit(g);
     UnitParams cnx = {0, 0, 1.0f, 1.0f, 0, -1};  // this unit's parameters
     UnitParams nxt = {0, 0, 1.0f, 1.0f, 0, -1};  // the next unit's
     int un = -1;
@@ -662,6 +665,10 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         if (k_on || p_on)
             for (int i = tid; i < 2 * RSN; i += NT) (&sh.a.h.hloc[0][0])[i] = 0;
         __syncthreads();
+        // this CTA's view of the row's first rejection, sent with E1 (only this CTA writes its
+        // own slot): the load's latency hides in pass 1's wait for the unit's data
+        if (tid == 0)
+            sh.e1k[ep][rank] = P.dead ? *reinterpret_cast<volatile const uint32_t *>(P.dead + b) : 0xFFFFFFFFu;
 
         // ---- pass 1: the maxima of both rows' slices, chunk by chunk as the bulk copies land
         // (the ragged tail and misaligned rows are already in place), then the softmax sums
@@ -731,8 +738,8 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         if (warp == 0 && lane < static_cast<int>(C)) {
             const float4 part = make_float4(cm0, cs0, cm1, cs1);  // row 1: (-inf, 0) when absent
             st_peer_v4(peer_addr(smem_addr(&sh.e1[ep][rank]), lane), part);
-            const uint32_t dk = P.dead ? *reinterpret_cast<volatile const uint32_t *>(P.dead + b) : 0xFFFFFFFFu;
-            st_peer_u32(peer_addr(smem_addr(&sh.e1k[ep][rank]), lane), dk);
+            if (lane != static_cast<int>(rank))
+                st_peer_u32(peer_addr(smem_addr(&sh.e1k[ep][rank]), lane), sh.e1k[ep][rank]);
             if (d_here) st_peer_v2(peer_addr(smem_addr(&sh.e1d[ep]), lane), make_float2(sh.xd[0], sh.xd[1]));
             xarrive(&sh.xbar[XB_E1 + ep], lane);
         }
@@ -1919,6 +1926,18 @@ static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     int64_t G = resident_clusters<T>(C, smem);
     if (G > units) G = units;
     p.G = static_cast<int32_t>(G);
+    // position-major order and draw skipping pay once each cluster runs many units, or
+    // with a one-hot draft, whose units are short beside their draws (with two staged rows
+    // and a few rounds of units they cost a few per cent: measured on 32 and 128 units)
+    p.pmajor = (!p.Q || units >= 8 * G) ? 1 : 0;
+    if (const char *o = getenv("MTPSPEC_VERIFY_ORDER"))  // "row" or "position" forces the order
+        p.pmajor = o[0] == 'p' ? 1 : (o[0] == 'r' ? 0 : p.pmajor);
+    if (!p.pmajor) {
+        p.dead = nullptr;
+    } else if (p.dead) {
+        e = cudaMemsetAsync(p.dead, 0xFF, static_cast<size_t>(p.B) * 4, stream);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(G * C), 1, 1);
     cfg.blockDim = dim3(vs::NT, 1, 1);
@@ -1953,13 +1972,10 @@ static cudaError_t run_verify_sample_impl(const VerifySampleArgs &a, bool row_fl
     p.G = 1;
     p.res = static_cast<vs::UnitResult *>(a.workspace);
     p.status = a.status;
-    p.dead = nullptr;
-    if (row_flags) {
-        p.dead = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(a.workspace) +
-                                              verify_records_bytes(a.B, a.D));
-        const cudaError_t e0 = cudaMemsetAsync(p.dead, 0xFF, static_cast<size_t>(a.B) * 4, stream);
-        if (e0 != cudaSuccess) return e0;
-    }
+    p.pmajor = 0;
+    p.dead = row_flags ? reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(a.workspace) +
+                                                      verify_records_bytes(a.B, a.D))
+                       : nullptr;  // reset (and used) by the launch when the order is position-major
     // the sampled rows, then (beside them) the greedy rows, then the per-row finalize
     cudaError_t e = a.dtype == MTPSPEC_F32 ? launch_verify_rr<float>(p, stream)
                                            : launch_verify_rr<uint16_t>(p, stream);
