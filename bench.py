@@ -287,8 +287,7 @@ def run_gpu(args, rank, world, dist):
     stream = torch.cuda.current_stream()
     ev_v = []
 
-    def step(i, timed=False):
-        s = sets[i % copies]
+    def run_step(s, timed=False):
         lib.mtp_draft_input(s["e"], s["h"], we, wh, s["W"], y, di["eps"], ws_di)
         if ng:
             lib.mtp_greedy_draft(s["Q"][:ng].view(ng * D, V), s["d"][:ng].view(-1))
@@ -300,6 +299,9 @@ def run_gpu(args, rank, world, dist):
         if timed:
             b.record(stream)
             ev_v.append((a, b))
+
+    def step(i, timed=False):
+        run_step(sets[i % copies], timed)
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -338,29 +340,45 @@ def run_gpu(args, rank, world, dist):
                     pt=torch.empty((B, D), dtype=torch.float32).pin_memory(),
                     pd=torch.empty((B, D), dtype=torch.float32).pin_memory(),
                     y=torch.empty((M, H), dtype=torch.bfloat16).pin_memory())
-    s0 = sets[0]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    # two device input sets: step i's inputs are copied in on a side stream while step i - 1
+    # computes on the other set (the copies run at the host link's rate, the compute on
+    # the GPU: each step waits for its own copy, each copy for the step that last read
+    # its set); the results go back on the compute stream after their step
+    e2e_sets = [sets[0], {k: v.clone() for k, v in sets[0].items()}]
+    copy_stream = torch.cuda.Stream()
+    ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_free = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def e2e_step():
-        for k in ("T", "Q", "d", "e", "h", "W"):
-            dst = s0[k] if s0[k].dtype != torch.bfloat16 else s0[k].view(torch.int16)
-            dst.copy_(host_in[k], non_blocking=True)
-        step(0)
+    def e2e_step(i):
+        s = e2e_sets[i % 2]
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_free[i % 2])
+            for k in ("T", "Q", "d", "e", "h", "W"):
+                dst = s[k] if s[k].dtype != torch.bfloat16 else s[k].view(torch.int16)
+                dst.copy_(host_in[k], non_blocking=True)
+            ev_in[i % 2].record(copy_stream)
+        stream.wait_event(ev_in[i % 2])
+        run_step(s)
+        ev_free[i % 2].record(stream)
         host_out["out"].copy_(out, non_blocking=True)
         host_out["na"].copy_(na, non_blocking=True)
         host_out["pt"].copy_(pt, non_blocking=True)
         host_out["pd"].copy_(pd, non_blocking=True)
         host_out["y"].copy_(y, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
+    for i in range(2):
+        ev_free[i].record(stream)
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier(dist)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    copy_stream.wait_event(e0)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist)
