@@ -199,7 +199,7 @@ MTPSPEC_API int mtp_draft_input(const void *emb_next, const void *hidden, const 
     return launched(mtpspec::run_draft_input(a, s));
 }
 
-constexpr int64_t kMaxLmHeadV = 65535LL * 128;  // 128-row vocabulary tiles on grid y
+constexpr int64_t kMaxLmHeadV = 65535LL * 128;  // ids stay well inside int32 tile arithmetic
 
 MTPSPEC_API size_t mtp_lm_head_greedy_workspace_bytes(int64_t M, int64_t H, int64_t V) {
     if (M <= 0 || H < 8 || H > kMaxH || (H % 8) != 0 || M > kMaxTokens || V < 1 || V > kMaxLmHeadV)

@@ -133,7 +133,7 @@ cudaError_t run_lm_head_greedy(const LmHeadArgs &a, cudaStream_t stream);
 
 // Pieces it is made of: the RMSNorm of each token's hidden state (draft_input.cu) and the
 // tcgen05 GEMM with the argmax epilogue (tcgen05_gemm.cu), which leaves one key
-// (order key << 32 | ~id) per (token, 128-row block of the vocabulary) in keys [Mt, o_tiles].
+// (order key << 32 | ~id) per (token, 256-id block of the vocabulary) in keys [Mt, o_tiles].
 cudaError_t run_head_norm(const void *x, const void *w, void *out, int64_t M, int64_t H, float eps,
                           cudaStream_t stream);
 int lm_head_o_tiles(int64_t V);

@@ -8,9 +8,9 @@
 //
 // Three launches: the optional RMSNorm of the hidden states into the workspace (bf16, as
 // the input stage rounds its activations), the tcgen05 GEMM whose epilogue reduces each
-// token's column of a 128 x BN logit tile to one key (order key of the largest logit << 32
-// | ~its lowest id), and the pick below, which takes the largest key of each token over
-// the V / 128 tiles.  A larger key is a larger logit, or the same logit at a lower id.
+// token's row of a 128-token x 256-id logit tile to one key (order key of the largest logit
+// << 32 | ~its lowest id), and the pick below, which takes the largest key of each token
+// over the V / 256 tiles.  A larger key is a larger logit, or the same logit at a lower id.
 #include "common.cuh"
 #include "kernels.h"
 #include "../../include/libmtpspec.h"
