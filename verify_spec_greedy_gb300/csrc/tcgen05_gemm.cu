@@ -261,8 +261,11 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
 // tokens as the 128-row MMA operand and HV = 256 vocabulary rows as the N side.  A tile is
 // (token tile, vocabulary tile); CTA c takes tiles c, c + G, ... with the token tiles of one
 // vocabulary tile side by side, so the CTAs that share a weight tile run together and it
-// leaves HBM once.  Each stage carries 32 KB of weight (and 16 KB of tokens), so four
-// stages keep 128 KB of weight in flight per SM.  The accumulator is double-buffered in
+// leaves HBM once.  Each stage carries 32 KB of weight and the tokens' tile, so four
+// stages keep 128 KB of weight in flight per SM.  With at most 64 tokens only their 64
+// rows are staged (8 KB): the MMA's rows 64 to 127 then read the start of the weight tile,
+// which gives rows of the accumulator that no thread keeps, and five stages fit (160 KB
+// of weight in flight).  The accumulator is double-buffered in
 // tensor memory (2 x 256 columns): the epilogue of tile j reads one buffer while tile j + 1
 // accumulates into the other.  In the epilogue each thread owns one token's row of the
 // tile: it scans its 256 logits in id order and keeps the largest order key and the first
@@ -273,11 +276,13 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
 constexpr int HT = 128;  // tokens per tile (MMA M)
 constexpr int HV = 256;  // vocabulary rows per tile (MMA N)
 
-template <int STAGES>
+template <int STAGES, int XROWS>
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_head_argmax(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
               const Params p, int t_tiles, int n_tiles) {
-    constexpr int X_BYTES = HT * BK * 2;
+    static_assert(XROWS == HT || (XROWS == 64 && XROWS * BK * 2 <= HV * BK * 2),
+                  "a short token tile is followed by at least as many bytes of weight");
+    constexpr int X_BYTES = XROWS * BK * 2;
     constexpr int W_BYTES = HV * BK * 2;
     constexpr int STAGE = X_BYTES + W_BYTES;
     constexpr uint32_t TMEM_COLS = 2 * HV;
@@ -576,14 +581,30 @@ cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, i
 // one CTA per SM (fewer when there are fewer tiles).  No K split.
 int lm_head_o_tiles(int64_t V) { return static_cast<int>((V + tg::HV - 1) / tg::HV); }
 
+template <int STAGES, int XROWS>
+static cudaError_t launch_head_argmax(const CUtensorMap &mx, const CUtensorMap &mw,
+                                      const tg::Params &p, int t_tiles, int n_tiles,
+                                      cudaStream_t stream) {
+    constexpr int smem = STAGES * (XROWS + tg::HV) * tg::BK * 2 + 1024;
+    static AttrCache attr;
+    cudaError_t e = ensure_attr(tg::k_head_argmax<STAGES, XROWS>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem, attr);
+    if (e != cudaSuccess) return e;
+    const int grid = n_tiles < kPlanSMs ? n_tiles : kPlanSMs;  // persistent: one CTA per SM
+    tg::k_head_argmax<STAGES, XROWS><<<grid, tg::NTHREADS, smem, stream>>>(mx, mw, p, t_tiles, n_tiles);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
 cudaError_t run_gemm_argmax(const void *W, const void *X, int64_t V, int64_t Mt, int64_t K,
                             unsigned long long *keys, unsigned *err, cudaStream_t stream) {
-    constexpr int STAGES = 4;
+    const bool short_x = Mt <= 64;
     const int t_tiles = static_cast<int>((Mt + tg::HT - 1) / tg::HT);
     const int v_tiles = lm_head_o_tiles(V);
     const int n_tiles = t_tiles * v_tiles;
     CUtensorMap mx, mw;
-    if (!make_map(&mx, X, Mt, K, tg::HT) || !make_map(&mw, W, V, K, tg::HV))
+    if (!make_map(&mx, X, Mt, K, short_x ? 64 : tg::HT) || !make_map(&mw, W, V, K, tg::HV))
         return cudaErrorInvalidValue;
     tg::Params p = {};
     p.keys = keys;
@@ -595,16 +616,8 @@ cudaError_t run_gemm_argmax(const void *W, const void *X, int64_t V, int64_t Mt,
     p.kb_per_split = p.kb_total;
     p.splits = 1;
     p.o_tiles = v_tiles;
-    constexpr int smem = STAGES * (tg::HT + tg::HV) * tg::BK * 2 + 1024;
-    static AttrCache attr;
-    cudaError_t e = ensure_attr(tg::k_head_argmax<STAGES>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem, attr);
-    if (e != cudaSuccess) return e;
-    const int grid = n_tiles < kPlanSMs ? n_tiles : kPlanSMs;  // persistent: one CTA per SM
-    tg::k_head_argmax<STAGES><<<grid, tg::NTHREADS, smem, stream>>>(mx, mw, p, t_tiles, n_tiles);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) count_launches(1);
-    return e;
+    return short_x ? launch_head_argmax<5, 64>(mx, mw, p, t_tiles, n_tiles, stream)
+                   : launch_head_argmax<4, tg::HT>(mx, mw, p, t_tiles, n_tiles, stream);
 }
 
 }  // namespace mtpspec
