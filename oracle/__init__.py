@@ -81,6 +81,8 @@ def _load():
         lib.orc_state_fixup.restype = C.c_int
         lib.orc_draft_steps.argtypes = [p, p, p, p, p, p, p, p, p, dbl, i64, i64, i64, i32, p, p, p]
         lib.orc_draft_steps.restype = C.c_int
+        lib.orc_lm_head_topk.argtypes = [p, p, dbl, p, i64, i64, i64, i32, p, p]
+        lib.orc_lm_head_topk.restype = C.c_int
         _lib = lib
         return lib
 
@@ -297,6 +299,23 @@ def lm_head_greedy(hidden, W, norm_w=None, eps: float = 0.0):
     _check(_load().orc_lm_head_greedy(_ptr(hidden), _ptr(nw), float(eps), _ptr(W), M, H, V,
                                       _ptr(ids), _ptr(mx)), "lm_head_greedy")
     return ids, mx
+
+
+def lm_head_topk(hidden, W, k: int, norm_w=None, eps: float = 0.0):
+    """(ids int32 [M, k], logits float64 [M, k]): the k largest logits of each token in
+    decreasing order, equal logits by increasing id."""
+    hidden = np.ascontiguousarray(hidden, dtype=np.uint16)
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    nw = None if norm_w is None else np.ascontiguousarray(norm_w, dtype=np.uint16)
+    M, H = hidden.shape
+    V = W.shape[0]
+    if W.shape[1] != H:
+        raise ValueError("W must be [V, H]")
+    ids = np.zeros((M, k), np.int32)
+    vals = np.zeros((M, k), np.float64)
+    _check(_load().orc_lm_head_topk(_ptr(hidden), _ptr(nw), float(eps), _ptr(W), M, H, V, int(k),
+                                    _ptr(ids), _ptr(vals)), "lm_head_topk")
+    return ids, vals
 
 
 # ---------------------------------------------------------------- post-verify state

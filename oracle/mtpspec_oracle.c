@@ -899,3 +899,45 @@ int orc_draft_steps(const uint16_t *embed, const int32_t *next_ids, const int32_
         *status |= st;
     return rc;
 }
+
+/* The k largest logits of the draft output layer, for a drafter that proposes several
+ * candidates ([HB] "The draft head" and [ZH] 三 stage 1: the output layer's logits; [DL]
+ * "Why a hand-written decoding loop": top-k keeps the k largest, and a tie goes to the
+ * lower id).  For each token t, ids[t, 0..k-1] lists the ids of the k largest logits in
+ * decreasing order, equal logits in increasing id order; vals (optional) their logits. */
+int orc_lm_head_topk(const uint16_t *hidden, const uint16_t *norm_w, double eps,
+                     const uint16_t *W, int64_t M, int64_t H, int64_t V, int32_t k, int32_t *ids,
+                     double *vals)
+{
+    if (M < 0 || H < 1 || V < 1 || V > 2147483647 || k < 1 || k > V || (M > 0 && !ids))
+        return ORC_ERR_ARG;
+    double *lg = (double *)malloc((size_t)V * sizeof(double));
+    unsigned char *taken = (unsigned char *)malloc((size_t)V);
+    if (!lg || !taken) {
+        free(lg);
+        free(taken);
+        return ORC_ERR_NOMEM;
+    }
+    for (int64_t t = 0; t < M; ++t) {
+        int rc = orc_lm_head_logits(hidden, norm_w, eps, W, M, H, V, &t, 1, lg, NULL);
+        if (rc != ORC_OK) {
+            free(lg);
+            free(taken);
+            return rc;
+        }
+        memset(taken, 0, (size_t)V);
+        for (int32_t r = 0; r < k; ++r) {  /* k selections of the largest remaining logit */
+            int64_t best = -1;
+            for (int64_t v = 0; v < V; ++v)
+                if (!taken[v] && (best < 0 || lg[v] > lg[best]))
+                    best = v;
+            taken[best] = 1;
+            ids[t * k + r] = (int32_t)best;
+            if (vals)
+                vals[t * k + r] = lg[best];
+        }
+    }
+    free(lg);
+    free(taken);
+    return ORC_OK;
+}

@@ -98,3 +98,32 @@ def test_shapes_are_checked():
     x = make_lm_head_input(2, 16, 20, seed=3)
     with pytest.raises(ValueError):
         oracle.lm_head_greedy(x["hidden"], x["W"][:, :8])
+
+
+def test_topk_is_a_stable_sort_of_the_logits():
+    # the k largest of a float64 product, ordered by value then id (numpy's stable sort of
+    # the negated logits), with planted ties
+    M, H, V, k = 4, 64, 300, 8
+    x = make_lm_head_input(M, H, V, seed=12)
+    W = x["W"].copy()
+    W[17] = W[250]                                   # equal logits at 17 and 250
+    W[5] = W[250]
+    ids, vals = oracle.lm_head_topk(x["hidden"], W, k)
+    ref = _f(x["hidden"]) @ _f(W).T
+    for t in range(M):
+        want = np.argsort(-ref[t], kind="stable")[:k]
+        np.testing.assert_array_equal(ids[t], want)
+        np.testing.assert_array_equal(vals[t], ref[t, want])
+    # k = 1 is the greedy pick
+    ids1, _ = oracle.lm_head_topk(x["hidden"], W, 1)
+    g, _ = oracle.lm_head_greedy(x["hidden"], W)
+    np.testing.assert_array_equal(ids1[:, 0], g)
+
+
+def test_topk_of_a_one_hot_hidden_is_a_sorted_column():
+    x = make_lm_head_input(1, 32, 100, seed=13)
+    h = np.zeros((1, 32), np.uint16)
+    h[0, 9] = f32_to_bf16_bits(np.array([1.0], np.float32))[0]
+    ids, vals = oracle.lm_head_topk(h, x["W"], 5)
+    col = _f(x["W"][:, 9])
+    np.testing.assert_array_equal(ids[0], np.argsort(-col, kind="stable")[:5])
