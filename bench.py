@@ -515,6 +515,10 @@ def run_sweep(args):
             xn = (xf * torch.rsqrt((xf * xf).mean(-1, keepdim=True) + 1e-6) * nl.float()).to(torch.bfloat16)
             return torch.argmax(xn @ Wl.t(), dim=-1)
         cms = timed(lib_pick, 10)
+        # the k = 8 largest logits of each token from the same layer
+        idk = torch.empty((Ml, 8), dtype=torch.int32, device=dev)
+        wsk = torch.empty(lib.mtp_lm_head_topk_workspace_bytes(Ml, Hl, V), dtype=torch.uint8, device=dev)
+        kms = timed(lambda: lib.mtp_lm_head_topk(hl, Wl, idk, norm_w=nl, eps=1e-6, workspace=wsk), 20)
         # the serial draft loop: D steps of one token per row (embedding gather with the
         # position-0 mask, input stage, stub block, output-layer pick), replayed from one
         # CUDA graph
@@ -588,7 +592,8 @@ def run_sweep(args):
                             "tokens_per_s": round(M / (dms / 1e3), 1), "roofline": droof},
             "lm_head_greedy": {"M": Ml, "ms": round(lms, 4),
                                "tokens_per_s": round(Ml / (lms / 1e3), 1), "roofline": lroof,
-                               "cublas_matmul_argmax_ms": round(cms, 4)},
+                               "cublas_matmul_argmax_ms": round(cms, 4),
+                               "top8_ms": round(kms, 4)},
             "state": state,
             "draft_steps": steps,
             "peaks": hbm_kind}), flush=True)

@@ -181,6 +181,29 @@ int mtp_draft_steps(const void *embed_w, const int32_t *next_ids, const int32_t 
  * reject. */
 size_t mtp_draft_steps_workspace_bytes(int64_t M, int64_t H, int64_t V);
 
+/*
+ * mtp_lm_head_topk — the k largest logits of the draft output layer, for a drafter that
+ * proposes several candidates per position, again without writing the [M, V] logits
+ * ([HB] "The draft head" and [ZH] 三 stage 1: the output layer's logits; [DL] "Why a
+ * hand-written decoding loop": top-k keeps the k largest, and a tie goes to the lower id).
+ * The logits are those of mtp_lm_head_greedy.
+ *   out_ids     int32 [M, k]   the ids of the k largest logits of each token, in
+ *                              decreasing order, equal logits by increasing id
+ *   out_logits  float [M, k] or NULL   their fp32 logits
+ *   1 <= k <= 8 and k <= V; workspace >= mtp_lm_head_topk_workspace_bytes(M, H, V).
+ * Other arguments, limits and errors as mtp_lm_head_greedy.  As there, the order is taken
+ * on the fp32 sums: ids whose exact logits lie within the fp32 rounding of each other may
+ * come back in either order (or, at the k-th place, either may be listed).
+ */
+int mtp_lm_head_topk(const void *hidden, const void *norm_w, float eps, const void *lm_head_w,
+                     int64_t M, int64_t H, int64_t V, int32_t k, int32_t *out_ids,
+                     float *out_logits, void *workspace, size_t workspace_bytes, int32_t *status,
+                     void *stream);
+
+/* Bytes of device workspace mtp_lm_head_topk needs for (M, H, V) (any k); 0 for
+ * arguments it would reject. */
+size_t mtp_lm_head_topk_workspace_bytes(int64_t M, int64_t H, int64_t V);
+
 /* ------------------------------------------------------------------ greedy verification */
 
 /*

@@ -33,7 +33,8 @@ def _declared():
 def test_header_declares_the_boundary():
     assert _declared() == sorted([
         "mtp_draft_input", "mtp_draft_input_workspace_bytes", "mtp_greedy_draft",
-        "mtp_lm_head_greedy", "mtp_lm_head_greedy_workspace_bytes",
+        "mtp_lm_head_greedy", "mtp_lm_head_greedy_workspace_bytes", "mtp_lm_head_topk",
+        "mtp_lm_head_topk_workspace_bytes",
         "mtp_state_snapshot", "mtp_state_fixup", "mtp_draft_steps",
         "mtp_draft_steps_workspace_bytes",
         "spec_verify_greedy", "spec_verify_sample", "spec_verify_workspace_bytes",
@@ -110,6 +111,23 @@ def test_lm_head_greedy_host_checks(so):
     assert need == 256 + 1024 + 4 * 4 * 8   # keys: 4 tokens x 4 blocks of 256 ids
     assert so.mtp_lm_head_greedy_workspace_bytes(4, 12, 1000) == 0
     assert so.mtp_lm_head_greedy_workspace_bytes(0, 64, 1000) == 0
+
+
+def test_lm_head_topk_host_checks(so):
+    nul, p = None, C.c_void_p(4096)
+    f = so.mtp_lm_head_topk
+    args = lambda **kw: [kw.get(n, d) for n, d in (("h", p), ("nw", nul), ("eps", 1e-6), ("W", p),
+                                                   ("M", 4), ("H", 64), ("V", 1000), ("k", 4),
+                                                   ("ids", p), ("lg", nul), ("ws", p),
+                                                   ("wsb", 1 << 30), ("st", nul), ("s", nul))]
+    assert f(*args(k=0)) == -3
+    assert f(*args(k=9)) == -3                   # at most 8
+    assert f(*args(k=4, V=3)) == -3              # k <= V
+    assert f(*args(M=0)) == 0
+    assert f(*args(ids=nul)) == -1
+    assert f(*args(wsb=64)) == -4
+    assert so.mtp_lm_head_topk_workspace_bytes(4, 64, 1000) == 256 + 1024 + 4 * 4 * 8 * 8
+    assert so.mtp_lm_head_topk_workspace_bytes(4, 60, 1000) == 0
 
 
 def test_state_host_checks(so):

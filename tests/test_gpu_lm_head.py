@@ -111,3 +111,93 @@ def test_parity_full_size_sampled_tokens(M, H, V):
     assert ((ids >= 0) & (ids < V)).all()
     toks = np.unique(np.linspace(0, M - 1, 5).astype(np.int64))
     check(x, ids, lg, toks)
+
+
+def gpu_topk(x, k, norm=True):
+    M, H, V = x["M"], x["H"], x["V"]
+    ids = torch.full((M, k), -7, dtype=torch.int32, device=DEV)
+    lg = torch.full((M, k), float("nan"), dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(lib.mtp_lm_head_topk_workspace_bytes(M, H, V), dtype=torch.uint8, device=DEV)
+    lib.mtp_lm_head_topk(_bf(x["hidden"]), _bf(x["W"]), ids, norm_w=_bf(x["norm_w"]) if norm else None,
+                         eps=x["eps"], out_logits=lg, workspace=ws, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return ids.cpu().numpy(), lg.cpu().numpy()
+
+
+def check_topk(x, ids, lg, toks, k, norm=True):
+    """The GPU's k ids of each token against the exact logits: distinct and valid, each
+    logit within its bound E, the order decreasing up to the bounds, every id that must be
+    in the top k present and none that cannot be; exact equality where the oracle's k
+    largest are separated by more than the bounds."""
+    H = x["H"]
+    exact, ad = oracle.lm_head_logits(x["hidden"], x["W"], toks,
+                                      norm_w=x["norm_w"] if norm else None, eps=x["eps"],
+                                      with_absdot=True)
+    E = H * 2.0 ** -23 * ad
+    strict = 0
+    for i, t in enumerate(toks):
+        e, b, g = exact[i], E[i], ids[t]
+        assert len(set(g.tolist())) == k and ((g >= 0) & (g < x["V"])).all(), (t, g)
+        assert (np.abs(lg[t].astype(np.float64) - e[g]) <= b[g] + 1e-30).all(), t
+        for r in range(k - 1):
+            assert e[g[r]] >= e[g[r + 1]] - b[g[r]] - b[g[r + 1]], (t, r)
+        order = np.argsort(-e, kind="stable")          # the oracle's order: value, then id
+        o = order[:k]
+        kth = e[o[-1]]
+        bmax = b.max()
+        if k < e.size:
+            nxt = order[k]
+            must = o[e[o] > e[nxt] + b[o] + b[nxt]]
+            assert set(must.tolist()) <= set(g.tolist()), (t, must, g)
+        assert (e[g] >= kth - b[g] - bmax).all(), t
+        vals = e[order[:min(k + 1, e.size)]]
+        if np.all(np.diff(vals) < -2 * bmax):
+            assert (g == o).all(), (t, g, o)
+            strict += 1
+    return strict
+
+
+@pytest.mark.parametrize("M,H,V,k,norm", [
+    (1, 64, 1000, 1, False), (2, 8, 300, 8, True), (5, 128, 4099, 8, True),
+    (17, 136, 3000, 3, True), (33, 256, 20000, 5, False), (64, 512, 9000, 8, True),
+    (130, 256, 5000, 8, False), (300, 256, 10000, 2, True), (3, 64, 8, 8, True)])
+def test_topk_parity(M, H, V, k, norm):
+    x = make_lm_head_input(M, H, V, seed=M * 7 + k + V)
+    ids, lg = gpu_topk(x, k, norm)
+    strict = check_topk(x, ids, lg, np.arange(M), k, norm)
+    assert strict >= 0.3 * M
+    # the oracle's own top k agrees with the order used above
+    oi, _ = oracle.lm_head_topk(x["hidden"][:2], x["W"], k, norm_w=x["norm_w"] if norm else None,
+                                eps=x["eps"])
+    assert oi.shape == (min(2, M), k)
+
+
+def test_topk_one_is_the_greedy_pick():
+    x = make_lm_head_input(40, 256, 6000, seed=77)
+    ids1, lg1 = gpu_topk(x, 1)
+    g, lg = gpu_lm_head(x)
+    np.testing.assert_array_equal(ids1[:, 0], g)
+    np.testing.assert_array_equal(lg1[:, 0], lg)
+
+
+def test_topk_ties_by_id():
+    # copies of the top row at higher and lower ids in other tiles: equal logits, listed by id
+    M, H, V, k = 4, 256, 3000, 4
+    x = make_lm_head_input(M, H, V, seed=5)
+    g, _ = gpu_lm_head(x, norm=False)
+    a = int(g[1])
+    W = x["W"].copy()
+    c1, c2 = (a + 700) % V, (a + 1900) % V
+    W[c1] = W[a]
+    W[c2] = W[a]
+    ids, _ = gpu_topk(dict(x, W=W), k, norm=False)
+    assert ids[1, :3].tolist() == sorted([a, c1, c2])
+
+
+def test_topk_serving_size_sampled_tokens():
+    M, H, V, k = 256, 4096, 151936, 8
+    x = make_lm_head_input(M, H, V, seed=H + V, w_std=0.02)
+    ids, lg = gpu_topk(x, k)
+    check_topk(x, ids, lg, np.array([0, 100, 255]), k)

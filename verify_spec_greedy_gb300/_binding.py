@@ -53,6 +53,8 @@ def load():
         "mtp_lm_head_greedy_workspace_bytes": ([i64, i64, i64], sz),
         "mtp_state_snapshot": ([p, p, i64, i64, p], C.c_int),
         "mtp_state_fixup": ([p, i32, p, p, p, p, i64, i64, p, p, p, p], C.c_int),
+        "mtp_lm_head_topk": ([p, p, f32, p, i64, i64, i64, i32, p, p, p, sz, p, p], C.c_int),
+        "mtp_lm_head_topk_workspace_bytes": ([i64, i64, i64], sz),
         "mtp_draft_steps": ([p, p, p, p, p, p, p, p, p, f32, i64, i64, i64, i32, p, p, p, sz, p, p],
                             C.c_int),
         "mtp_draft_steps_workspace_bytes": ([i64, i64, i64], sz),
@@ -163,6 +165,22 @@ def mtp_state_fixup(num_accepted, D: int, kv_len_before, kv_len, state=None, bac
           _ptr(state), _ptr(backup), B, rb, _ptr(draft_kv_len), _ptr(recompute), _ptr(status),
           _stream(stream))
     return kv_len
+
+
+def mtp_lm_head_topk_workspace_bytes(M: int, H: int, V: int) -> int:
+    return int(load().mtp_lm_head_topk_workspace_bytes(int(M), int(H), int(V)))
+
+
+def mtp_lm_head_topk(hidden, lm_head_w, out_ids, norm_w=None, eps: float = 0.0,
+                     out_logits=None, workspace=None, status=None, stream=None):
+    """out_ids[M, k]: the k largest logits' ids of each token (decreasing; ties by id)."""
+    M, H = hidden.shape
+    V = lm_head_w.shape[0]
+    k = out_ids.shape[1]
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _call("mtp_lm_head_topk", _ptr(hidden), _ptr(norm_w), float(eps), _ptr(lm_head_w), M, H, V,
+          k, _ptr(out_ids), _ptr(out_logits), _ptr(workspace), ws, _ptr(status), _stream(stream))
+    return out_ids
 
 
 def mtp_draft_steps_workspace_bytes(M: int, H: int, V: int) -> int:

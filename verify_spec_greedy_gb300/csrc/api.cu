@@ -236,6 +236,7 @@ MTPSPEC_API int mtp_lm_head_greedy(const void *hidden, const void *norm_w, float
     a.ids = out_ids;
     a.ids_stride = 1;
     a.logit = out_logit;
+    a.k = 1;
     a.workspace = workspace;
     a.status = status;
     return launched(mtpspec::run_lm_head_greedy(a, s));
@@ -292,6 +293,48 @@ MTPSPEC_API int mtp_draft_steps(const void *embed_w, const int32_t *next_ids, co
     a.workspace = workspace;
     a.status = status;
     return launched(mtpspec::run_draft_steps(a, s));
+}
+
+MTPSPEC_API size_t mtp_lm_head_topk_workspace_bytes(int64_t M, int64_t H, int64_t V) {
+    if (M <= 0 || H < 8 || H > kMaxH || (H % 8) != 0 || M > kMaxTokens || V < 1 || V > kMaxLmHeadV)
+        return 0;
+    return mtpspec::lm_head_workspace_bytes(M, H, V, mtpspec::kLmHeadTopK);
+}
+
+MTPSPEC_API int mtp_lm_head_topk(const void *hidden, const void *norm_w, float eps,
+                                 const void *lm_head_w, int64_t M, int64_t H, int64_t V, int32_t k,
+                                 int32_t *out_ids, float *out_logits, void *workspace,
+                                 size_t workspace_bytes, int32_t *status, void *stream) {
+    if (M < 0 || H < 8 || H > kMaxH || (H % 8) != 0 || M > kMaxTokens || V < 1 || V > kMaxLmHeadV)
+        return MTPSPEC_ERR_SHAPE;
+    if (k < 1 || k > mtpspec::kLmHeadTopK || k > V) return MTPSPEC_ERR_SHAPE;
+    if (!(eps >= 0.0f)) return MTPSPEC_ERR_ARG;
+    if (M == 0) return MTPSPEC_OK;
+    if (!hidden || !lm_head_w || !out_ids) return MTPSPEC_ERR_ARG;
+    if (!aligned(hidden, 16) || !aligned(norm_w, 16) || !aligned(lm_head_w, 16) ||
+        !aligned(out_ids, 4) || !aligned(out_logits, 4) || !aligned(status, 4))
+        return MTPSPEC_ERR_ARG;
+    if (!workspace || !aligned(workspace, 256) ||
+        workspace_bytes < mtpspec::lm_head_workspace_bytes(M, H, V, mtpspec::kLmHeadTopK))
+        return MTPSPEC_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = prepare_device(s);
+    if (rc != MTPSPEC_OK) return rc;
+    mtpspec::LmHeadArgs a;
+    a.hidden = hidden;
+    a.norm_w = norm_w;
+    a.eps = eps;
+    a.W = lm_head_w;
+    a.M = M;
+    a.H = H;
+    a.V = V;
+    a.ids = out_ids;
+    a.ids_stride = k;
+    a.logit = out_logits;
+    a.k = k;  // k = 1 is the greedy pick, with the same layout of ids and logits
+    a.workspace = workspace;
+    a.status = status;
+    return launched(mtpspec::run_lm_head_greedy(a, s));
 }
 
 constexpr int64_t kMaxStateRows = 1LL << 24;

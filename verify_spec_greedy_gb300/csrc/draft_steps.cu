@@ -100,6 +100,7 @@ cudaError_t run_draft_steps(const DraftStepsArgs &a, cudaStream_t stream) {
         lh.ids = a.draft_ids + k;
         lh.ids_stride = a.D;
         lh.logit = nullptr;
+        lh.k = 1;
         lh.workspace = lm_ws;
         lh.status = a.status;
         err = run_lm_head_greedy(lh, stream);

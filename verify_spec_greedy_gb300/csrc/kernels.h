@@ -122,13 +122,15 @@ struct LmHeadArgs {
     float eps;
     const void *W;        // bf16 [V, H]
     int64_t M, H, V;
-    int32_t *ids;         // ids[t * ids_stride]
+    int32_t *ids;         // ids[t * ids_stride], or [M, k] for the top k
     int64_t ids_stride;
-    float *logit;         // [M] or nullptr
+    float *logit;         // [M] (or [M, k]) or nullptr
+    int32_t k;            // 1: the greedy pick; 2 .. kLmHeadTopK: the k largest
     void *workspace;
     int32_t *status;      // or nullptr
 };
-size_t lm_head_workspace_bytes(int64_t M, int64_t H, int64_t V);
+size_t lm_head_workspace_bytes(int64_t M, int64_t H, int64_t V, int32_t k = 1);
+constexpr int kLmHeadTopK = 8;  // the largest k of the top-k output
 cudaError_t run_lm_head_greedy(const LmHeadArgs &a, cudaStream_t stream);
 
 // Pieces it is made of: the RMSNorm of each token's hidden state (draft_input.cu) and the
@@ -138,7 +140,7 @@ cudaError_t run_head_norm(const void *x, const void *w, void *out, int64_t M, in
                           cudaStream_t stream);
 int lm_head_o_tiles(int64_t V);
 cudaError_t run_gemm_argmax(const void *W, const void *X, int64_t V, int64_t Mt, int64_t K,
-                            unsigned long long *keys, unsigned *err, cudaStream_t stream);
+                            unsigned long long *keys, unsigned *err, int topk, cudaStream_t stream);
 
 }  // namespace mtpspec
 

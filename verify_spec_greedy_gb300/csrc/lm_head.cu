@@ -39,16 +39,65 @@ k_lm_head_pick(const unsigned long long *__restrict__ keys, int o_tiles, int64_t
     }
 }
 
+// One warp per token: the k largest of its o_tiles x TOPK keys.  Each lane keeps the TOPK
+// largest of the keys it reads (sorted); then k rounds take the warp's largest head and
+// pop it from its lane (keys are distinct: each carries its id).
+template <int TOPK>
+__global__ void __launch_bounds__(PICK_THREADS)
+k_lm_head_pick_topk(const unsigned long long *__restrict__ keys, int o_tiles, int64_t M, int k,
+                    int32_t *__restrict__ ids, float *__restrict__ logit) {
+    pdl_wait_primary();
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * (PICK_THREADS / 32) + (threadIdx.x >> 5);
+    if (t >= M) return;
+    const unsigned long long *kr = keys + t * o_tiles * TOPK;
+    const int n = o_tiles * TOPK;
+    unsigned long long lst[TOPK];
+#pragma unroll
+    for (int i = 0; i < TOPK; ++i) lst[i] = 0ull;
+    for (int i = lane; i < n; i += 32) {
+        const unsigned long long key = kr[i];
+        if (key > lst[TOPK - 1]) {
+            lst[TOPK - 1] = key;
+#pragma unroll
+            for (int q = TOPK - 1; q > 0; --q) {
+                if (lst[q] > lst[q - 1]) {
+                    const unsigned long long tmp = lst[q];
+                    lst[q] = lst[q - 1];
+                    lst[q - 1] = tmp;
+                }
+            }
+        }
+    }
+    for (int r = 0; r < k; ++r) {
+        unsigned long long m = lst[0];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const unsigned own = __ballot_sync(0xFFFFFFFFu, m != 0ull && lst[0] == m);
+        if (own && lane == __ffs(own) - 1) {
+#pragma unroll
+            for (int q = 0; q + 1 < TOPK; ++q) lst[q] = lst[q + 1];
+            lst[TOPK - 1] = 0ull;
+        }
+        if (lane == 0) {
+            ids[t * k + r] = m ? static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(m)) : -1;
+            if (logit) logit[t * k + r] = key_to_float(static_cast<uint32_t>(m >> 32));
+        }
+    }
+}
+
 }  // namespace lh
 
 // Workspace: a flag word (256 bytes), the normalised hidden states when a norm weight is
-// given (M x H bf16, counted always), then the keys [M, o_tiles].
+// given (M x H bf16, counted always), then the keys [M, o_tiles] (x kLmHeadTopK for a top
+// k).
 static size_t lm_head_xn_bytes(int64_t M, int64_t H) {
     return (static_cast<size_t>(M) * static_cast<size_t>(H) * 2 + 1023) & ~static_cast<size_t>(1023);
 }
 
-size_t lm_head_workspace_bytes(int64_t M, int64_t H, int64_t V) {
-    return 256 + lm_head_xn_bytes(M, H) + static_cast<size_t>(M) * lm_head_o_tiles(V) * 8;
+size_t lm_head_workspace_bytes(int64_t M, int64_t H, int64_t V, int32_t k) {
+    const size_t per = k > 1 ? kLmHeadTopK : 1;  // keys per (token, tile)
+    return 256 + lm_head_xn_bytes(M, H) + static_cast<size_t>(M) * lm_head_o_tiles(V) * per * 8;
 }
 
 cudaError_t run_lm_head_greedy(const LmHeadArgs &a, cudaStream_t stream) {
@@ -63,7 +112,7 @@ cudaError_t run_lm_head_greedy(const LmHeadArgs &a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         X = xn;
     }
-    e = run_gemm_argmax(a.W, X, a.V, a.M, a.H, keys, flag, stream);
+    e = run_gemm_argmax(a.W, X, a.V, a.M, a.H, keys, flag, a.k > 1 ? kLmHeadTopK : 1, stream);
     if (e != cudaSuccess) return e;
     const int o_tiles = lm_head_o_tiles(a.V);
     const int per = lh::PICK_THREADS / 32;
@@ -76,8 +125,13 @@ cudaError_t run_lm_head_greedy(const LmHeadArgs &a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, lh::k_lm_head_pick, static_cast<const unsigned long long *>(keys),
-                           o_tiles, a.M, a.ids, a.ids_stride, a.logit);
+    if (a.k > 1)
+        e = cudaLaunchKernelEx(&cfg, lh::k_lm_head_pick_topk<kLmHeadTopK>,
+                               static_cast<const unsigned long long *>(keys), o_tiles, a.M,
+                               static_cast<int>(a.k), a.ids, a.logit);
+    else
+        e = cudaLaunchKernelEx(&cfg, lh::k_lm_head_pick, static_cast<const unsigned long long *>(keys),
+                               o_tiles, a.M, a.ids, a.ids_stride, a.logit);
     if (e == cudaSuccess) count_launches(1);
     return e;
 }

@@ -276,7 +276,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
 constexpr int HT = 128;  // tokens per tile (MMA M)
 constexpr int HV = 256;  // vocabulary rows per tile (MMA N)
 
-template <int STAGES, int XROWS>
+template <int STAGES, int XROWS, int TOPK>
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_head_argmax(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
               const Params p, int t_tiles, int n_tiles) {
@@ -383,26 +383,64 @@ k_head_argmax(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             tc_fence_after();
             const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * HV);
             const int nv = min(HV, p.H - v0);  // vocabulary rows of this tile
-            uint32_t best = 0;                 // below every value's order key
-            int bv = v0;
-            for (int c = 0; c < HV; c += 8) {
-                float v[8];
-                tmem_ld8(trow + c, v);
+            if constexpr (TOPK == 1) {
+                uint32_t best = 0;  // below every value's order key
+                int bv = v0;
+                for (int c = 0; c < HV; c += 8) {
+                    float v[8];
+                    tmem_ld8(trow + c, v);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint32_t key = c + u < nv ? order_key(v[u]) : 0u;
-                    if (key > best) {  // strictly larger: the first id keeps a tie
-                        best = key;
-                        bv = v0 + c + u;
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t key = c + u < nv ? order_key(v[u]) : 0u;
+                        if (key > best) {  // strictly larger: the first id keeps a tie
+                            best = key;
+                            bv = v0 + c + u;
+                        }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&acce[b])) : "memory");
+                if (t < p.Mt)
+                    p.keys[static_cast<size_t>(t) * p.o_tiles + vt] =
+                        (static_cast<unsigned long long>(best) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(bv));
+            } else {
+                // the TOPK largest (order key << 32 | ~id), kept sorted in decreasing order:
+                // a key that beats the last one replaces it and bubbles up
+                unsigned long long lst[TOPK];
+#pragma unroll
+                for (int i = 0; i < TOPK; ++i) lst[i] = 0ull;
+                for (int c = 0; c < HV; c += 8) {
+                    float v[8];
+                    tmem_ld8(trow + c, v);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const unsigned long long key =
+                            c + u < nv ? (static_cast<unsigned long long>(order_key(v[u])) << 32) |
+                                             (0xFFFFFFFFu - static_cast<uint32_t>(v0 + c + u))
+                                       : 0ull;
+                        if (key > lst[TOPK - 1]) {
+                            lst[TOPK - 1] = key;
+#pragma unroll
+                            for (int i = TOPK - 1; i > 0; --i) {
+                                if (lst[i] > lst[i - 1]) {
+                                    const unsigned long long tmp = lst[i];
+                                    lst[i] = lst[i - 1];
+                                    lst[i - 1] = tmp;
+                                }
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&acce[b])) : "memory");
+                if (t < p.Mt) {
+                    unsigned long long *kd = p.keys + (static_cast<size_t>(t) * p.o_tiles + vt) * TOPK;
+#pragma unroll
+                    for (int i = 0; i < TOPK; ++i) kd[i] = lst[i];
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&acce[b])) : "memory");
-            if (t < p.Mt)
-                p.keys[static_cast<size_t>(t) * p.o_tiles + vt] =
-                    (static_cast<unsigned long long>(best) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(bv));
         }
     }
     tc_fence_before();
@@ -581,24 +619,24 @@ cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, i
 // one CTA per SM (fewer when there are fewer tiles).  No K split.
 int lm_head_o_tiles(int64_t V) { return static_cast<int>((V + tg::HV - 1) / tg::HV); }
 
-template <int STAGES, int XROWS>
+template <int STAGES, int XROWS, int TOPK>
 static cudaError_t launch_head_argmax(const CUtensorMap &mx, const CUtensorMap &mw,
                                       const tg::Params &p, int t_tiles, int n_tiles,
                                       cudaStream_t stream) {
     constexpr int smem = STAGES * (XROWS + tg::HV) * tg::BK * 2 + 1024;
     static AttrCache attr;
-    cudaError_t e = ensure_attr(tg::k_head_argmax<STAGES, XROWS>,
+    cudaError_t e = ensure_attr(tg::k_head_argmax<STAGES, XROWS, TOPK>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem, attr);
     if (e != cudaSuccess) return e;
     const int grid = n_tiles < kPlanSMs ? n_tiles : kPlanSMs;  // persistent: one CTA per SM
-    tg::k_head_argmax<STAGES, XROWS><<<grid, tg::NTHREADS, smem, stream>>>(mx, mw, p, t_tiles, n_tiles);
+    tg::k_head_argmax<STAGES, XROWS, TOPK><<<grid, tg::NTHREADS, smem, stream>>>(mx, mw, p, t_tiles, n_tiles);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
 
 cudaError_t run_gemm_argmax(const void *W, const void *X, int64_t V, int64_t Mt, int64_t K,
-                            unsigned long long *keys, unsigned *err, cudaStream_t stream) {
+                            unsigned long long *keys, unsigned *err, int topk, cudaStream_t stream) {
     const bool short_x = Mt <= 64;
     const int t_tiles = static_cast<int>((Mt + tg::HT - 1) / tg::HT);
     const int v_tiles = lm_head_o_tiles(V);
@@ -616,8 +654,11 @@ cudaError_t run_gemm_argmax(const void *W, const void *X, int64_t V, int64_t Mt,
     p.kb_per_split = p.kb_total;
     p.splits = 1;
     p.o_tiles = v_tiles;
-    return short_x ? launch_head_argmax<5, 64>(mx, mw, p, t_tiles, n_tiles, stream)
-                   : launch_head_argmax<4, tg::HT>(mx, mw, p, t_tiles, n_tiles, stream);
+    if (topk > 1)
+        return short_x ? launch_head_argmax<5, 64, kLmHeadTopK>(mx, mw, p, t_tiles, n_tiles, stream)
+                       : launch_head_argmax<4, tg::HT, kLmHeadTopK>(mx, mw, p, t_tiles, n_tiles, stream);
+    return short_x ? launch_head_argmax<5, 64, 1>(mx, mw, p, t_tiles, n_tiles, stream)
+                   : launch_head_argmax<4, tg::HT, 1>(mx, mw, p, t_tiles, n_tiles, stream);
 }
 
 }  // namespace mtpspec
