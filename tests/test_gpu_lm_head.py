@@ -59,7 +59,8 @@ def check(x, ids, lg, toks, norm=True):
     (1, 64, 1000, False), (2, 8, 300, True), (5, 128, 4099, True), (16, 256, 32768, False),
     (17, 136, 3000, True), (33, 512, 20000, True), (64, 1024, 12345, False),
     (100, 384, 9000, True), (129, 256, 5000, False), (200, 1024, 50000, False),
-    (256, 512, 7000, True), (300, 256, 10000, True), (700, 128, 2000, False)])
+    (256, 512, 7000, True), (300, 256, 10000, True), (700, 128, 2000, False),
+    (3, 64, 1000003, True)])
 def test_parity_small(M, H, V, norm):
     x = make_lm_head_input(M, H, V, seed=M * 131 + H + V)
     ids, lg = gpu_lm_head(x, norm)
@@ -162,7 +163,8 @@ def check_topk(x, ids, lg, toks, k, norm=True):
 @pytest.mark.parametrize("M,H,V,k,norm", [
     (1, 64, 1000, 1, False), (2, 8, 300, 8, True), (5, 128, 4099, 8, True),
     (17, 136, 3000, 3, True), (33, 256, 20000, 5, False), (64, 512, 9000, 8, True),
-    (130, 256, 5000, 8, False), (300, 256, 10000, 2, True), (3, 64, 8, 8, True)])
+    (130, 256, 5000, 8, False), (300, 256, 10000, 2, True), (3, 64, 8, 8, True),
+    (2, 64, 1000003, 8, True)])
 def test_topk_parity(M, H, V, k, norm):
     x = make_lm_head_input(M, H, V, seed=M * 7 + k + V)
     ids, lg = gpu_topk(x, k, norm)

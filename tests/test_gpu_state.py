@@ -18,7 +18,8 @@ def _t(a):
 
 
 @pytest.mark.parametrize("B,D,row_bytes", [(1, 1, 16), (5, 3, 0), (37, 3, 4112), (64, 6, 65536),
-                                           (300, 2, 1040), (3, 64, 1 << 20)])
+                                           (300, 2, 1040), (3, 64, 1 << 20), (70000, 2, 16),
+                                           (70000, 3, 0)])
 def test_fixup_parity(B, D, row_bytes):
     rng = np.random.default_rng(B * 7 + D + row_bytes)
     a = rng.integers(0, D + 1, B).astype(np.int32)
