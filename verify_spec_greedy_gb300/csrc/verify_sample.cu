@@ -802,30 +802,59 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             // element: its cost grows with the lanes it serves, which the bins' range keeps
             // few.
             constexpr float MAG = 8388608.0f;  // 2^23
+            const float tza = -c2 * static_cast<float>(R);
+            if (nrows > 1 && !sh.deg[0] && !sh.deg[1] && !k_on) {
+                // both rows in one sweep: twice the independent work per iteration
+                const float nmA = sh.nmc[0], tzbA = sh.tzb[0], fnbA = static_cast<float>(sh.nbu[0]);
+                const float nmB = sh.nmc[1], tzbB = sh.tzb[1], fnbB = static_cast<float>(sh.nbu[1]);
+                uint32_t *hA = sh.a.h.hloc[0];
+                uint32_t *hB = sh.a.h.hloc[1];
+                auto bin_w = [&](float x, float nm, float tzb, float fnb, uint32_t *hh) {
+                    const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
+                    const float tb = __fadd_rz(tz, MAG);
+                    const int bn = __float_as_int(tb) - 0x4B000000;
+                    const float ws = __uint_as_float(__float_as_uint(ex2(fmaf(x, c2, nm))) +
+                                                     (static_cast<uint32_t>((bn >> 5) + 16) << 23));
+                    const uint32_t q = __float_as_uint(ws + MAG) - 0x4B000000u;
+                    if (tz < fnb) atomicAdd(&hh[bn], q);
+                };
+#pragma unroll 2
+                for (int v = tid; v < nvr; v += NT) {
+                    float xa[EPV], xb[EPV];
+                    unpack(sv0[v], xa);
+                    unpack(sv1[v], xb);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        bin_w(xa[e], nmA, tzbA, fnbA, hA);
+                        bin_w(xb[e], nmB, tzbB, fnbB, hB);
+                    }
+                }
+            } else {
 #pragma unroll 1
-            for (int r = 0; r < nrows; ++r) {
-                if (sh.deg[r]) continue;
-                const float nm = sh.nmc[r], tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
-                const float fnb = static_cast<float>(sh.nbu[r]);
-                uint32_t *hh = sh.a.h.hloc[r];
-                if (k_on) {
-                    for_row(sdat(r), nvr, [&](float x, int) {
-                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
-                        const float tb = __fadd_rz(tz, MAG);  // 2^23 + trunc(tz) below 2^23
-                        if (tz < fnb) atomicAdd(&hh[__float_as_int(tb) - 0x4B000000], 1u);
-                    });
-                } else {
-                    for_row(sdat(r), nvr, [&](float x, int) {
-                        // -z * R >= 0 (clamped: rounding can make it a hair negative at the
-                        // maximum); bins at its integer part
-                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
-                        const float tb = __fadd_rz(tz, MAG);
-                        const int bn = __float_as_int(tb) - 0x4B000000;
-                        const float ws = __uint_as_float(__float_as_uint(ex2(fmaf(x, c2, nm))) +
-                                                         (static_cast<uint32_t>((bn >> 5) + 16) << 23));
-                        const uint32_t q = __float_as_uint(ws + MAG) - 0x4B000000u;
-                        if (tz < fnb) atomicAdd(&hh[bn], q);
-                    });
+                for (int r = 0; r < nrows; ++r) {
+                    if (sh.deg[r]) continue;
+                    const float nm = sh.nmc[r], tzb = sh.tzb[r];
+                    const float fnb = static_cast<float>(sh.nbu[r]);
+                    uint32_t *hh = sh.a.h.hloc[r];
+                    if (k_on) {
+                        for_row(sdat(r), nvr, [&](float x, int) {
+                            const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
+                            const float tb = __fadd_rz(tz, MAG);  // 2^23 + trunc(tz) below 2^23
+                            if (tz < fnb) atomicAdd(&hh[__float_as_int(tb) - 0x4B000000], 1u);
+                        });
+                    } else {
+                        for_row(sdat(r), nvr, [&](float x, int) {
+                            // -z * R >= 0 (clamped: rounding can make it a hair negative at the
+                            // maximum); bins at its integer part
+                            const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
+                            const float tb = __fadd_rz(tz, MAG);
+                            const int bn = __float_as_int(tb) - 0x4B000000;
+                            const float ws = __uint_as_float(__float_as_uint(ex2(fmaf(x, c2, nm))) +
+                                                             (static_cast<uint32_t>((bn >> 5) + 16) << 23));
+                            const uint32_t q = __float_as_uint(ws + MAG) - 0x4B000000u;
+                            if (tz < fnb) atomicAdd(&hh[bn], q);
+                        });
+                    }
                 }
             }
             __syncthreads();
