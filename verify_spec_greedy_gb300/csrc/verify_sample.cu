@@ -1057,38 +1057,55 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             // ---- gather the boundary candidates into every CTA (E3)
             const bool any_fast = sh.mode[0] == 1 || (nrows > 1 && sh.mode[1] == 1);
             if (any_fast) {
-#pragma unroll 1
-                for (int r = 0; r < nrows; ++r) {
-                    if (sh.mode[r] != 1) continue;
-                    // the candidates: elements of bins [b1, b2] (bin bn = trunc(tz): bn >= b1 iff
-                    // tz >= b1, bn <= b2 iff tz < b2 + 1)
-                    const float tza = -c2 * static_cast<float>(R), tzb = sh.tzb[r];
-                    const float fb1 = static_cast<float>(sh.b1[r]);
-                    const float fb2 = static_cast<float>(sh.b2[r] + 1);
-                    auto is_cand = [&](float x) -> bool {
-                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
-                        return tz >= fb1 && tz < fb2;
-                    };
-                    // one sweep; a vector that holds candidates claims their slots at once (the
-                    // order of the slots does not matter: every later step depends on values)
-                    const uint4 *vp = reinterpret_cast<const uint4 *>(sdat(r));
-                    unsigned long long *cr = &sh.a.cand[r][static_cast<int>(rank) * capc];
+                // the candidates of row r: elements of bins [b1, b2] (bin bn = trunc(tz):
+                // bn >= b1 iff tz >= b1, bn <= b2 iff tz < b2 + 1); a vector that holds
+                // candidates claims their slots at once (the order of the slots does not
+                // matter: every later step depends on values)
+                const float tza = -c2 * static_cast<float>(R);
+                auto gather_vec = [&](int r, int v, const float (&x)[EPV], float tzb, float fb1,
+                                      float fb2) {
+                    uint32_t msk = 0;
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        const float tz = fmaxf(fmaf(x[e], tza, tzb), 0.0f);
+                        msk |= (tz >= fb1 && tz < fb2) ? (1u << e) : 0u;
+                    }
+                    if (msk) {
+                        unsigned long long *cr = &sh.a.cand[r][static_cast<int>(rank) * capc];
+                        uint32_t slot = atomicAdd(&sh.lcnt[r], static_cast<uint32_t>(__popc(msk)));
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) {
+                            if (((msk >> e) & 1u) && slot < static_cast<uint32_t>(capc))
+                                cr[slot] = (static_cast<unsigned long long>(__float_as_uint(x[e])) << 32) |
+                                           static_cast<uint32_t>(lo + v * EPV + e);
+                            slot += (msk >> e) & 1u;
+                        }
+                    }
+                };
+                if (nrows > 1 && sh.mode[0] == 1 && sh.mode[1] == 1) {
+                    // both rows in one sweep
+                    const float tzbA = sh.tzb[0], f1A = static_cast<float>(sh.b1[0]), f2A = static_cast<float>(sh.b2[0] + 1);
+                    const float tzbB = sh.tzb[1], f1B = static_cast<float>(sh.b1[1]), f2B = static_cast<float>(sh.b2[1] + 1);
 #pragma unroll 2
                     for (int v = tid; v < nvr; v += NT) {
-                        float x[EPV];
-                        unpack(vp[v], x);
-                        uint32_t msk = 0;
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e) msk |= is_cand(x[e]) ? (1u << e) : 0u;
-                        if (msk) {
-                            uint32_t slot = atomicAdd(&sh.lcnt[r], static_cast<uint32_t>(__popc(msk)));
-#pragma unroll
-                            for (int e = 0; e < EPV; ++e) {
-                                if (((msk >> e) & 1u) && slot < static_cast<uint32_t>(capc))
-                                    cr[slot] = (static_cast<unsigned long long>(__float_as_uint(x[e])) << 32) |
-                                               static_cast<uint32_t>(lo + v * EPV + e);
-                                slot += (msk >> e) & 1u;
-                            }
+                        float xa[EPV], xb[EPV];
+                        unpack(sv0[v], xa);
+                        unpack(sv1[v], xb);
+                        gather_vec(0, v, xa, tzbA, f1A, f2A);
+                        gather_vec(1, v, xb, tzbB, f1B, f2B);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int r = 0; r < nrows; ++r) {
+                        if (sh.mode[r] != 1) continue;
+                        const float tzb = sh.tzb[r];
+                        const float fb1 = static_cast<float>(sh.b1[r]), fb2 = static_cast<float>(sh.b2[r] + 1);
+                        const uint4 *vp = reinterpret_cast<const uint4 *>(sdat(r));
+#pragma unroll 2
+                        for (int v = tid; v < nvr; v += NT) {
+                            float x[EPV];
+                            unpack(vp[v], x);
+                            gather_vec(r, v, x, tzb, fb1, fb2);
                         }
                     }
                 }
