@@ -10,7 +10,11 @@
 //    as can be resident; cluster g takes units g, g + G, ... (a unit is one (row b,
 //    position j) pair of a sampled row: the target row T[b, j] and, for j < D, the draft
 //    row Q[b, j]).  CTA r of a cluster owns the contiguous vocabulary slice
-//    [r*slice, (r+1)*slice) of both rows.
+//    [r*slice, (r+1)*slice) of both rows.  Large batches (and one-hot drafts) number the
+//    units position-major, so that a row's earlier positions are usually decided before its
+//    later ones start; a unit behind a position of its row that was already rejected skips
+//    its draw, which no output reads (a per-row flag in the workspace, agreed on by the
+//    cluster at its first exchange).
 //    Data path: bulk asynchronous copies (four chunks per row, each on its own mbarrier)
 //    bring a unit's two slices into shared memory, where every pass of the unit reads
 //    them, so every logit is read from HBM once.  While a unit works, one thread asks L2
