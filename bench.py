@@ -670,7 +670,8 @@ def run_reference(args):
     x = make_verify_inputs(w)
     di = make_draft_input(w)
     rows = 16
-    for _ in range(min(args.warmup, 1)):
+    warm = max(1, min(args.warmup, 5))  # about a second each on the host cores
+    for _ in range(warm):
         oracle_sample(x, di, w, rows)
     vals, dts = [], []
     steps = max(1, min(args.steps, 10))
@@ -680,7 +681,7 @@ def run_reference(args):
         dts.append(dt)
     value = len(vals) * rows * (x["D"] + 1) / sum(dts)
     res = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
-           "n_gpus": 0, "steps": steps, "warmup": min(args.warmup, 1),
+           "n_gpus": 0, "steps": steps, "warmup": warm,
            "ms_per_step": round(1e3 * sum(dts) / steps, 2), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": w.name, "B": x["B"], "D": x["D"], "V": x["V"], "H": w.H,
