@@ -670,7 +670,7 @@ def run_reference(args):
     x = make_verify_inputs(w)
     di = make_draft_input(w)
     rows = 16
-    warm = max(1, min(args.warmup, 5))  # about a second each on the host cores
+    warm = max(3, min(args.warmup, 5))  # about a second each on the host cores
     for _ in range(warm):
         oracle_sample(x, di, w, rows)
     vals, dts = [], []
