@@ -43,7 +43,7 @@ KERNEL_SOURCES = ["verify_spec_greedy_gb300/csrc/verify_sample.cu",
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["libmtpspec", "reference"], default="libmtpspec")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -131,7 +131,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -201,18 +201,28 @@ def profiled_traffic(workload):
 
 # ---------------------------------------------------------------- CPU oracle baseline
 
-def oracle_sample(x, di, w, rows, min_seconds=0.0):
+def sample_rows(x, rows):
+    """`rows` rows of the verify with the workload's mix of greedy rows (temperature 0,
+    the first ones of the batch) and sampled rows."""
+    B = x["B"]
+    ng = int((x["tau"] == 0).sum())
+    n_g = max(1, round(rows * ng / B)) if ng else 0
+    return list(range(n_g)) + list(range(ng, ng + rows - n_g))
+
+
+def oracle_sample(x, di, w, rows, min_seconds=0.0, sel=None):
     """Time the oracle on a bounded sample: `rows` rows of the verify (the workload's mix
-    of greedy and sampled rows) plus the draft-input tokens of those rows and the greedy
-    drafts of the greedy rows among them, spread over the host cores; the sample is
-    repeated until at least `min_seconds` have passed."""
+    of greedy and sampled rows; or the rows `sel`) plus the draft-input tokens of those
+    rows and the greedy drafts of the greedy rows among them, spread over the host cores;
+    the sample is repeated until at least `min_seconds` have passed."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     cores = os.cpu_count() or 1
     B = x["B"]
-    ng = int((x["tau"] == 0).sum())
-    n_g = max(1, round(rows * ng / B)) if ng else 0
-    sel = list(range(n_g)) + list(range(ng, ng + rows - n_g))
+    if sel is None:
+        sel = sample_rows(x, rows)
+    greedy = [r for r in sel if x["tau"][r] == 0]
+    n_g = len(greedy)
     tok_per_row = max(1, w.tokens // B)
     ntok = tok_per_row * len(sel)
     e, h = di["e"][0][:ntok], di["h"][0][:ntok]
@@ -225,7 +235,7 @@ def oracle_sample(x, di, w, rows, min_seconds=0.0):
                               di["eps"]) for a, b in chunks]
             if n_g:
                 futs.append(ex.submit(oracle.greedy_draft,
-                                      x["Q"][:n_g].reshape(-1, x["V"])))
+                                      x["Q"][greedy].reshape(-1, x["V"])))
             for f in futs:
                 f.result()
         oracle.verify_sample_rows(x["T"], x["Q"], x["d"], x["tau"], x["top_k"], x["top_p"],
@@ -669,20 +679,44 @@ def run_reference(args):
     w = WORKLOADS[args.workload]
     x = make_verify_inputs(w)
     di = make_draft_input(w)
-    rows = 16
-    warm = max(3, min(args.warmup, 5))  # about a second each on the host cores
+    # a pool of 16 rows in the workload's mix; warm-up steps verify all of it, and the
+    # timed steps take turns through it, as many rows a step as keep the K steps near
+    # two minutes on the host cores
+    mixed = sample_rows(x, 16)
+    g = [r for r in mixed if x["tau"][r] == 0]
+    sp = [r for r in mixed if x["tau"][r] != 0]
+    # interleaved, so that any run of consecutive rows keeps the mix
+    pool = sorted(mixed, key=lambda r: (g.index(r) * len(mixed) / len(g)) if r in g
+                  else (sp.index(r) + 0.5) * len(mixed) / len(sp))
+    warm = max(3, min(args.warmup, 5))
+    t_warm = []
     for _ in range(warm):
-        oracle_sample(x, di, w, rows)
-    vals, dts = [], []
-    steps = max(1, min(args.steps, 10))
+        t_warm.append(oracle_sample(x, di, w, len(pool), sel=pool)[3])
+    steps = max(1, args.steps)
+    per_row = min(t_warm) / len(pool)
+    rows = int(min(len(pool), max(1, 120.0 / (steps * per_row))))
+    # small samples use fewer cores: check the size with untimed steps and shrink it
+    for _ in range(3):
+        t_try = min(oracle_sample(x, di, w, rows, sel=pool[:rows])[3] for _ in range(2))
+        if rows == 1 or steps * t_try <= 150.0:
+            break
+        rows = max(1, int(rows * 120.0 / (steps * t_try)))
+    total_rows, t_sum, at = 0, 0.0, 0
     for _ in range(steps):
-        v, cores, sample, dt = oracle_sample(x, di, w, rows)
-        vals.append(v)
-        dts.append(dt)
-    value = len(vals) * rows * (x["D"] + 1) / sum(dts)
+        sel = [pool[(at + i) % len(pool)] for i in range(rows)]
+        at = (at + rows) % len(pool)
+        v, cores, _, dt = oracle_sample(x, di, w, rows, sel=sel)
+        total_rows += rows
+        t_sum += dt
+    value = total_rows * (x["D"] + 1) / t_sum
+    n_greedy = sum(1 for r in pool if x["tau"][r] == 0)
+    sample = (f"{rows} row(s) a step, taken in turn from {len(pool)} of {x['B']} rows "
+              f"({n_greedy} greedy) of {w.name}: their verify, their draft-input tokens "
+              f"and the greedy drafts of the greedy rows")
     res = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
-           "n_gpus": 0, "steps": steps, "warmup": warm,
-           "ms_per_step": round(1e3 * sum(dts) / steps, 2), "higher_is_better": True,
+           "n_gpus": max(1, args.gpus), "device": "host cores", "steps": steps,
+           "warmup": warm,
+           "ms_per_step": round(1e3 * t_sum / steps, 2), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": w.name, "B": x["B"], "D": x["D"], "V": x["V"], "H": w.H,
                       "draft_tokens": w.tokens},
