@@ -276,12 +276,17 @@ def test_unit_orders(order, one_hot, monkeypatch):
 
 # ---------------------------------------------------------------- one-hot drafts
 
-def _greedy_half(x, rng):
-    """Half the drafts become the target's argmax, so that some of them are held."""
+def _argmax_drafts(x):
+    """The target's argmax at every draft position."""
     am = x["T"][:, :-1, :]
     if am.dtype == np.uint16:
         am = (am.astype(np.uint32) << 16).view(np.float32)
-    am = am.argmax(-1).astype(np.int32)
+    return am.argmax(-1).astype(np.int32)
+
+
+def _greedy_half(x, rng):
+    """Half the drafts become the target's argmax, so that some of them are held."""
+    am = _argmax_drafts(x)
     x["d"] = np.where(rng.random(x["d"].shape) < 0.5, am, x["d"]).astype(np.int32)
     return x
 
@@ -309,3 +314,35 @@ def test_one_hot_draft_serving_mix():
     w = WORKLOADS["serve_b256_d3_v152k"].scaled(B=64, seed=41, philox_seed=43)
     x = _greedy_half(make_verify_inputs(w), np.random.default_rng(41))
     compare(gpu_verify(x, one_hot=True), oracle_verify(x, one_hot=True), label="one-hot serve")
+
+
+# ---------------------------------------------------------------- limits
+
+@pytest.mark.parametrize("dtype,one_hot,V,k", [
+    ("f32", False, 407552, 0),      # the largest vocabularies the call accepts
+    ("bf16", False, 815104, 50),
+    ("f32", True, 652288, 50),
+    ("bf16", True, 1304576, 0),
+])
+def test_maximum_vocabulary(dtype, one_hot, V, k):
+    w = Workload(name="vmax", B=2, D=2, V=V, H=8, dtype=dtype, tau=1.0, top_k=k, top_p=0.9,
+                 t_std=3.0, q_noise=1.0, seed=V % 1000, philox_seed=V)
+    x = _greedy_half(make_verify_inputs(w), np.random.default_rng(V))
+    g, o = gpu_verify(x, one_hot=one_hot), oracle_verify(x, one_hot=one_hot)
+    assert g["status"] == o["status"] == 0
+    compare(g, o, label=f"V={V} {dtype} one-hot={one_hot} k={k}")
+
+
+@pytest.mark.parametrize("V,D,dtype", [(1000, 64, "f32"), (4099, 16, "bf16"),
+                                       (151936, 16, "f32")])
+def test_long_drafts(V, D, dtype):
+    # peaked targets, and every draft of rows 0-1 (half of those of rows 2-3) the target's
+    # argmax, so that long accepted prefixes occur (40 of 64 in one row at V = 1000)
+    w = Workload(name="long", B=4, D=D, V=V, H=8, dtype=dtype, tau=0.5, top_k=0, top_p=0.95,
+                 t_std=8.0, q_noise=1.0, seed=D + V, philox_seed=D)
+    x = _greedy_half(make_verify_inputs(w), np.random.default_rng(D))
+    x["d"][:2] = _argmax_drafts(x)[:2]
+    g, o = gpu_verify(x), oracle_verify(x)
+    assert o["num_accepted"].max() >= min(D, 9)
+    assert g["status"] == o["status"] == 0
+    compare(g, o, label=f"V={V} D={D} {dtype}")
