@@ -75,7 +75,8 @@ def check_steps(x, out, hout, toks):
 
 
 @pytest.mark.parametrize("M,H,V,D", [(1, 64, 500, 1), (3, 64, 500, 3), (4, 128, 1000, 2),
-                                     (20, 256, 3001, 4), (33, 136, 2000, 3), (256, 512, 20000, 2)])
+                                     (20, 256, 3001, 4), (33, 136, 2000, 3), (256, 512, 20000, 2),
+                                     (2, 64, 500, 64)])
 def test_steps_parity(M, H, V, D):
     x = _inputs(M, H, V, seed=M + H + D)
     out, hout, st = gpu_steps(x, D)
