@@ -60,7 +60,7 @@ def check(x, ids, lg, toks, norm=True):
     (17, 136, 3000, True), (33, 512, 20000, True), (64, 1024, 12345, False),
     (100, 384, 9000, True), (129, 256, 5000, False), (200, 1024, 50000, False),
     (256, 512, 7000, True), (300, 256, 10000, True), (700, 128, 2000, False),
-    (3, 64, 1000003, True)])
+    (3, 64, 1000003, True), (2, 64, 8388480, True)])
 def test_parity_small(M, H, V, norm):
     x = make_lm_head_input(M, H, V, seed=M * 131 + H + V)
     ids, lg = gpu_lm_head(x, norm)
