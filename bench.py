@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="time the verify and the draft-input calls alone on every workload "
                          "(one JSON line each) instead of the benchmark step")
+    ap.add_argument("--graph-batch", action="store_true",
+                    help="time the verify call of each small workload as a CUDA graph of 20 "
+                         "back-to-back calls on distinct input copies (one JSON line each)")
     ap.add_argument("--lm-head", type=int, nargs=3, metavar=("M", "H", "V"), default=None,
                     help="time mtp_lm_head_greedy alone on seeded random inputs of this size "
                          "(--warmup, then --steps calls, each after an L2 flush)")
@@ -649,10 +652,94 @@ def run_lm_head(args):
     return 0
 
 
+def run_graph_batch(args):
+    """The verify call of each workload small enough to be bound by launch latency, as a
+    CUDA graph of NB back-to-back calls, each on its own copy of the inputs (so that after
+    an L2 flush every call reads its logits from HBM); per-call time = replay time / NB,
+    median of 10 replays."""
+    import numpy as np
+    import torch
+    import verify_spec_greedy_gb300 as lib
+    from verify_spec_greedy_gb300.inputs import WORKLOADS, make_verify_inputs
+    NB = 20
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hbm, hbm_kind = measured_peaks()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    for name in ("greedy_b1_d1_v32k", "sample_b8_d3_v152k", "sample_b1_d6_v262k_bf16"):
+        w = WORKLOADS[name]
+        x = make_verify_inputs(w)
+        B, D, V = x["B"], x["D"], x["V"]
+        greedy = w.mode == "greedy"
+        Ts = [to_dev(x["T"]) for _ in range(NB)]
+        Qs = None if greedy else [to_dev(x["Q"]) for _ in range(NB)]
+        d = to_dev(x["d"])
+        outs = [torch.empty((B, D + 1), dtype=torch.int32, device=dev) for _ in range(NB)]
+        nas = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(NB)]
+        if greedy:
+            calls = [lambda i=i: lib.spec_verify_greedy(Ts[i], d, outs[i], nas[i])
+                     for i in range(NB)]
+            vbytes = B * (D + 1) * V * (4 if x["dtype"] == "f32" else 2)
+        else:
+            tau, top_p = to_dev(x["tau"]), to_dev(x["top_p"])
+            top_k = to_dev(x["top_k"]) if (x["top_k"] > 0).any() else None
+            ws = torch.empty(lib.spec_verify_workspace_bytes(B, D, V), dtype=torch.uint8,
+                             device=dev)
+            calls = [lambda i=i: lib.spec_verify_sample(Ts[i], Qs[i], d, tau, top_k, top_p,
+                                                        x["seed"], outs[i], nas[i], None, None,
+                                                        ws)
+                     for i in range(NB)]
+            vbytes = verify_bytes(x)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for c in calls:
+                c()
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for c in calls:
+                c()
+        for _ in range(3):
+            graph.replay()
+        ts = []
+        for _ in range(10):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts) / NB
+        ach = vbytes / (ms / 1e3) / 1e9
+        # the outputs of the last replay equal those of a plain call
+        ref_out = outs[0].clone()
+        calls[0]()
+        torch.cuda.synchronize()
+        same = bool(all(torch.equal(o, ref_out) for o in outs))
+        print(json.dumps({"graph_batch": name, "calls": NB, "ms_per_call": round(ms, 5),
+                          "rows_per_s": round(B * (D + 1) / (ms / 1e3), 1),
+                          "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
+                                       "unit": "GB/s", "frac": round(ach / hbm, 4),
+                                       "bytes": vbytes, "peak_kind": hbm_kind},
+                          "outputs_equal": same}), flush=True)
+        del Ts, Qs, graph
+    return 0
+
+
 def main():
     args = parse_args()
     if args.sweep:
         return run_sweep(args)
+    if args.graph_batch:
+        return run_graph_batch(args)
     if args.lm_head:
         return run_lm_head(args)
     rank, world, dist = dist_init(args.gpus)
