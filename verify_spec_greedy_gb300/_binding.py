@@ -88,8 +88,53 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _ptr(t):
-    return None if t is None else t.data_ptr()
+# Argument checks.  The library reads and writes through raw device pointers with the
+# sizes it is given, so a host tensor, a strided view, the wrong element type or a short
+# buffer would be read or written out of bounds on the GPU; they are refused here.
+_I32, _F32, _HALF = "int32", "float32", "16-bit"
+_KINDS = None
+
+
+def _kinds():
+    """The accepted torch dtypes of each kind (built on first use: torch loads lazily)."""
+    global _KINDS
+    if _KINDS is None:
+        import torch
+        half = {torch.bfloat16, torch.float16, torch.int16}
+        if hasattr(torch, "uint16"):
+            half.add(torch.uint16)
+        _KINDS = {_I32: frozenset([torch.int32]), _F32: frozenset([torch.float32]),
+                  _HALF: frozenset(half), "tensor": torch.Tensor}
+    return _KINDS
+
+
+def _arg(t, name, kind=None, numel=0, optional=False):
+    """Device pointer of tensor `t` after checking that it lives on a CUDA device, is
+    contiguous, has the element type `kind` (int32, float32, or any 16-bit type for bf16
+    bit patterns) and holds at least `numel` elements; None when `t` is None and allowed."""
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    kinds = _kinds()
+    if not isinstance(t, kinds["tensor"]):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if kind is not None and t.dtype not in kinds[kind]:
+        raise TypeError(f"{name} must hold {kind} values, got {t.dtype}")
+    if numel and t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements; {numel} are needed")
+    return t.data_ptr()
+
+
+def _ws(workspace):
+    """(pointer, bytes) of an optional workspace tensor."""
+    if workspace is None:
+        return None, 0
+    return _arg(workspace, "workspace"), workspace.numel() * workspace.element_size()
 
 
 def _dtype_code(t):
@@ -117,17 +162,19 @@ def mtp_draft_input(emb_next, hidden, enorm_w, hnorm_w, eh_proj_w, out, eps: flo
                     workspace=None, stream=None):
     """out[M, H] = eh_proj_w @ [enorm(emb_next); hnorm(hidden)] (all bf16 on the GPU)."""
     M, H = emb_next.shape
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _call("mtp_draft_input", _ptr(emb_next), _ptr(hidden), _ptr(enorm_w), _ptr(hnorm_w),
-          _ptr(eh_proj_w), _ptr(out), M, H, float(eps), _ptr(workspace), ws, _stream(stream))
+    wp, ws = _ws(workspace)
+    _call("mtp_draft_input", _arg(emb_next, "emb_next", _HALF, M * H),
+          _arg(hidden, "hidden", _HALF, M * H), _arg(enorm_w, "enorm_w", _HALF, H),
+          _arg(hnorm_w, "hnorm_w", _HALF, H), _arg(eh_proj_w, "eh_proj_w", _HALF, 2 * H * H),
+          _arg(out, "out", _HALF, M * H), M, H, float(eps), wp, ws, _stream(stream))
     return out
 
 
 def mtp_greedy_draft(logits, out_ids, stream=None):
     """out_ids[M] = argmax of each row of logits[M, V] (lowest id on ties)."""
     M, V = logits.shape
-    _call("mtp_greedy_draft", _ptr(logits), _dtype_code(logits), M, V, _ptr(out_ids),
-          _stream(stream))
+    _call("mtp_greedy_draft", _arg(logits, "logits", numel=M * V), _dtype_code(logits), M, V,
+          _arg(out_ids, "out_ids", _I32, M), _stream(stream))
     return out_ids
 
 
@@ -141,9 +188,12 @@ def mtp_lm_head_greedy(hidden, lm_head_w, out_ids, norm_w=None, eps: float = 0.0
     (bf16 hidden [M, H] and lm_head_w [V, H] on the GPU; lowest id on ties)."""
     M, H = hidden.shape
     V = lm_head_w.shape[0]
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _call("mtp_lm_head_greedy", _ptr(hidden), _ptr(norm_w), float(eps), _ptr(lm_head_w), M, H,
-          V, _ptr(out_ids), _ptr(out_logit), _ptr(workspace), ws, _ptr(status), _stream(stream))
+    wp, ws = _ws(workspace)
+    _call("mtp_lm_head_greedy", _arg(hidden, "hidden", _HALF, M * H),
+          _arg(norm_w, "norm_w", _HALF, H, optional=True), float(eps),
+          _arg(lm_head_w, "lm_head_w", _HALF, V * H), M, H, V,
+          _arg(out_ids, "out_ids", _I32, M), _arg(out_logit, "out_logit", _F32, M, optional=True),
+          wp, ws, _arg(status, "status", _I32, 1, optional=True), _stream(stream))
     return out_ids
 
 
@@ -151,7 +201,11 @@ def mtp_state_snapshot(state, backup, stream=None):
     """backup[b] = state[b] for device tensors of B rows (any dtype, same shape)."""
     B = state.shape[0]
     rb = state[0].numel() * state.element_size() if B else 0
-    _call("mtp_state_snapshot", _ptr(state), _ptr(backup), B, rb, _stream(stream))
+    ps = _arg(state, "state")
+    pb = _arg(backup, "backup")
+    if backup.numel() * backup.element_size() < B * rb:
+        raise ValueError("backup is smaller than state")
+    _call("mtp_state_snapshot", ps, pb, B, rb, _stream(stream))
     return backup
 
 
@@ -161,9 +215,16 @@ def mtp_state_fixup(num_accepted, D: int, kv_len_before, kv_len, state=None, bac
     device tensors of B rows, or None for a model without recurrent state."""
     B = num_accepted.shape[0]
     rb = 0 if state is None else state[0].numel() * state.element_size()
-    _call("mtp_state_fixup", _ptr(num_accepted), int(D), _ptr(kv_len_before), _ptr(kv_len),
-          _ptr(state), _ptr(backup), B, rb, _ptr(draft_kv_len), _ptr(recompute), _ptr(status),
-          _stream(stream))
+    ps = _arg(state, "state", optional=True)
+    pb = _arg(backup, "backup", optional=True)
+    for t, n in ((state, "state"), (backup, "backup")):
+        if t is not None and t.numel() * t.element_size() < B * rb:
+            raise ValueError(f"{n} holds fewer than {B} rows of {rb} bytes")
+    _call("mtp_state_fixup", _arg(num_accepted, "num_accepted", _I32, B), int(D),
+          _arg(kv_len_before, "kv_len_before", _I32, B), _arg(kv_len, "kv_len", _I32, B),
+          ps, pb, B, rb, _arg(draft_kv_len, "draft_kv_len", _I32, B, optional=True),
+          _arg(recompute, "recompute", _I32, B, optional=True),
+          _arg(status, "status", _I32, 1, optional=True), _stream(stream))
     return kv_len
 
 
@@ -177,9 +238,13 @@ def mtp_lm_head_topk(hidden, lm_head_w, out_ids, norm_w=None, eps: float = 0.0,
     M, H = hidden.shape
     V = lm_head_w.shape[0]
     k = out_ids.shape[1]
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _call("mtp_lm_head_topk", _ptr(hidden), _ptr(norm_w), float(eps), _ptr(lm_head_w), M, H, V,
-          k, _ptr(out_ids), _ptr(out_logits), _ptr(workspace), ws, _ptr(status), _stream(stream))
+    wp, ws = _ws(workspace)
+    _call("mtp_lm_head_topk", _arg(hidden, "hidden", _HALF, M * H),
+          _arg(norm_w, "norm_w", _HALF, H, optional=True), float(eps),
+          _arg(lm_head_w, "lm_head_w", _HALF, V * H), M, H, V, k,
+          _arg(out_ids, "out_ids", _I32, M * k),
+          _arg(out_logits, "out_logits", _F32, M * k, optional=True), wp, ws,
+          _arg(status, "status", _I32, 1, optional=True), _stream(stream))
     return out_ids
 
 
@@ -194,11 +259,17 @@ def mtp_draft_steps(embed_w, next_ids, hidden, enorm_w, hnorm_w, eh_proj_w, lm_h
     M, H = hidden.shape
     V = embed_w.shape[0]
     D = draft_ids.shape[1]
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _call("mtp_draft_steps", _ptr(embed_w), _ptr(next_ids), _ptr(positions), _ptr(hidden),
-          _ptr(enorm_w), _ptr(hnorm_w), _ptr(eh_proj_w), _ptr(norm_w), _ptr(lm_head_w),
-          float(eps), M, H, V, D, _ptr(draft_ids), _ptr(hidden_out), _ptr(workspace), ws,
-          _ptr(status), _stream(stream))
+    wp, ws = _ws(workspace)
+    _call("mtp_draft_steps", _arg(embed_w, "embed_w", _HALF, V * H),
+          _arg(next_ids, "next_ids", _I32, M),
+          _arg(positions, "positions", _I32, M, optional=True),
+          _arg(hidden, "hidden", _HALF, M * H), _arg(enorm_w, "enorm_w", _HALF, H),
+          _arg(hnorm_w, "hnorm_w", _HALF, H), _arg(eh_proj_w, "eh_proj_w", _HALF, 2 * H * H),
+          _arg(norm_w, "norm_w", _HALF, H, optional=True),
+          _arg(lm_head_w, "lm_head_w", _HALF, V * H), float(eps), M, H, V, D,
+          _arg(draft_ids, "draft_ids", _I32, M * D),
+          _arg(hidden_out, "hidden_out", _HALF, D * M * H, optional=True), wp, ws,
+          _arg(status, "status", _I32, 1, optional=True), _stream(stream))
     return draft_ids
 
 
@@ -206,8 +277,12 @@ def spec_verify_greedy(target_logits, draft_ids, out_tokens, num_accepted, statu
                        stream=None):
     """Greedy verification of draft_ids[B, D] against target_logits[B, D+1, V]."""
     B, D1, V = target_logits.shape
-    _call("spec_verify_greedy", _ptr(target_logits), _dtype_code(target_logits), _ptr(draft_ids),
-          B, D1 - 1, V, _ptr(out_tokens), _ptr(num_accepted), _ptr(status), _stream(stream))
+    D = D1 - 1
+    _call("spec_verify_greedy", _arg(target_logits, "target_logits", numel=B * D1 * V),
+          _dtype_code(target_logits), _arg(draft_ids, "draft_ids", _I32, B * D), B, D, V,
+          _arg(out_tokens, "out_tokens", _I32, B * D1),
+          _arg(num_accepted, "num_accepted", _I32, B),
+          _arg(status, "status", _I32, 1, optional=True), _stream(stream))
     return out_tokens, num_accepted
 
 
@@ -215,17 +290,40 @@ def spec_verify_workspace_bytes(B: int, D: int, V: int) -> int:
     return int(load().spec_verify_workspace_bytes(int(B), int(D), int(V)))
 
 
+def _verify_sample_args(target_logits, draft_logits, draft_ids, temperature, top_k, top_p,
+                        seed, out_tokens, num_accepted, p_target, p_draft):
+    """The checked arguments the two sampling entry points share, in their order: the
+    logits, draft ids, per-row parameters, seed and sizes, then the outputs."""
+    B, D1, V = target_logits.shape
+    D = D1 - 1
+    if draft_logits is not None and (draft_logits.dtype != target_logits.dtype or
+                                     tuple(draft_logits.shape) != (B, D, V)):
+        raise ValueError(f"draft_logits must be {target_logits.dtype} of shape {(B, D, V)}, "
+                         f"got {draft_logits.dtype} {tuple(draft_logits.shape)}")
+    head = (_arg(target_logits, "target_logits", numel=B * D1 * V),
+            _arg(draft_logits, "draft_logits", numel=B * D * V, optional=True),
+            _dtype_code(target_logits), _arg(draft_ids, "draft_ids", _I32, B * D),
+            _arg(temperature, "temperature", _F32, B),
+            _arg(top_k, "top_k", _I32, B, optional=True),
+            _arg(top_p, "top_p", _F32, B, optional=True), int(seed) & 0xFFFFFFFFFFFFFFFF,
+            B, D, V)
+    tail = (_arg(out_tokens, "out_tokens", _I32, B * D1),
+            _arg(num_accepted, "num_accepted", _I32, B),
+            _arg(p_target, "p_target", _F32, B * D, optional=True),
+            _arg(p_draft, "p_draft", _F32, B * D, optional=True))
+    return head, tail
+
+
 def spec_verify_sample(target_logits, draft_logits, draft_ids, temperature, top_k, top_p,
                        seed: int, out_tokens, num_accepted, p_target=None, p_draft=None,
                        workspace=None, status=None, stream=None):
     """Speculative-sampling verification (see include/libmtpspec.h)."""
-    B, D1, V = target_logits.shape
-    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _call("spec_verify_sample", _ptr(target_logits), _ptr(draft_logits),
-          _dtype_code(target_logits), _ptr(draft_ids), _ptr(temperature), _ptr(top_k),
-          _ptr(top_p), int(seed) & 0xFFFFFFFFFFFFFFFF, B, D1 - 1, V, _ptr(out_tokens),
-          _ptr(num_accepted), _ptr(p_target), _ptr(p_draft), _ptr(workspace), ws, _ptr(status),
-          _stream(stream))
+    head, tail = _verify_sample_args(target_logits, draft_logits, draft_ids, temperature,
+                                     top_k, top_p, seed, out_tokens, num_accepted, p_target,
+                                     p_draft)
+    wp, ws = _ws(workspace)
+    _call("spec_verify_sample", *head, *tail, wp, ws,
+          _arg(status, "status", _I32, 1, optional=True), _stream(stream))
     return out_tokens, num_accepted
 
 
@@ -234,9 +332,9 @@ def spec_verify_sample_static(target_logits, draft_logits, draft_ids, temperatur
                               status=None, stream=None):
     """spec_verify_sample with the library's own fixed scratch instead of a workspace
     (for callers that cannot allocate device memory; see include/libmtpspec.h)."""
-    B, D1, V = target_logits.shape
-    _call("spec_verify_sample_static", _ptr(target_logits), _ptr(draft_logits),
-          _dtype_code(target_logits), _ptr(draft_ids), _ptr(temperature), _ptr(top_k),
-          _ptr(top_p), int(seed) & 0xFFFFFFFFFFFFFFFF, B, D1 - 1, V, _ptr(out_tokens),
-          _ptr(num_accepted), _ptr(p_target), _ptr(p_draft), _ptr(status), _stream(stream))
+    head, tail = _verify_sample_args(target_logits, draft_logits, draft_ids, temperature,
+                                     top_k, top_p, seed, out_tokens, num_accepted, p_target,
+                                     p_draft)
+    _call("spec_verify_sample_static", *head, *tail,
+          _arg(status, "status", _I32, 1, optional=True), _stream(stream))
     return out_tokens, num_accepted
