@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 namespace mtpspec {
 
@@ -16,16 +17,21 @@ void count_launches(int n);
 // Function attributes persist, so each is set once per device (and the shared-memory
 // limit again only when a larger one is asked for): launches recorded by a stream
 // capture then make no attribute call.
+// Host threads that miss the cache set the attribute one at a time, so the value set on
+// the device only grows and the cache never claims more than the device holds.
 struct AttrCache {
     std::atomic<int> v[64];
+    std::mutex mu;
 };
 template <typename F>
 cudaError_t ensure_attr(F kernel, cudaFuncAttribute attr, int value, AttrCache &c) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (c.v[dev].load() >= value) return cudaSuccess;
+    if (c.v[dev].load(std::memory_order_acquire) >= value) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(c.mu);
+    if (c.v[dev].load(std::memory_order_relaxed) >= value) return cudaSuccess;
     const cudaError_t e = cudaFuncSetAttribute(kernel, attr, value);
-    if (e == cudaSuccess) c.v[dev].store(value);
+    if (e == cudaSuccess) c.v[dev].store(value, std::memory_order_release);
     return e;
 }
 
