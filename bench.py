@@ -742,11 +742,13 @@ def main():
         return run_graph_batch(args)
     if args.lm_head:
         return run_lm_head(args)
-    rank, world, dist = dist_init(args.gpus)
     if args.impl == "reference":
-        if rank != 0:
+        # host cores only: rank 0 runs the oracle, the other ranks exit without work (no
+        # process group, so no GPU is touched)
+        if int(os.environ.get("RANK", "0")) != 0:
             return 0
         return run_reference(args)
+    rank, world, dist = dist_init(args.gpus)
     res, x, di, w = run_gpu(args, rank, world, dist)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
