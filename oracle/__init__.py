@@ -4,7 +4,7 @@ The arithmetic lives in ``mtpspec_oracle.c`` (plain C, double precision); this m
 compiles it with gcc and exposes it to Python through ctypes with numpy arrays.
 
 Only the test suite, the package's ``smoke()`` check and the benchmark's CPU-baseline
-leg may import this package.  The product library (``verify_spec_greedy_gb300``) never
+leg and reference arm may import this package.  The product library (``verify_spec_greedy_gb300``) never
 imports it and shares no code with it.
 """
 from __future__ import annotations

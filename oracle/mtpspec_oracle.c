@@ -3,8 +3,9 @@
  * speculative-decoding hot path computes.
  *
  * TEST INFRASTRUCTURE ONLY.  It is loaded by the test suite, by the package's smoke
- * check and by the benchmark's CPU-baseline leg; the product library never links,
- * loads or calls it, and the two share no code (no headers, helpers or tables).
+ * check and by the benchmark's CPU-baseline leg and reference arm; the product library
+ * never links, loads or calls it, and the two share no code (no headers, helpers or
+ * tables).
  *
  * Sources, cited by page title and section:
  *  [HB] "14. MTP: speculative decoding with the built-in draft head" (Transformer by
