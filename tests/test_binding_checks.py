@@ -172,3 +172,16 @@ def test_state(lib):
         b.mtp_state_fixup(dev(B, dtype=torch.int64), 3, kv0, kv)
     with pytest.raises(ValueError):
         b.mtp_state_fixup(a, 3, kv0, dev(B - 1, dtype=I32))
+
+
+def test_a_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # no fallback: without the built library every entry point raises
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "libmtpspec.so"))
+    with pytest.raises(ImportError):
+        b.load()
+    a = verify_args()
+    with pytest.raises(ImportError):
+        b.spec_verify_sample(**a)
+    with pytest.raises(ImportError):
+        b.spec_verify_workspace_bytes(1, 1, 10)
