@@ -177,6 +177,7 @@ def test_state(lib):
 def test_a_missing_library_fails_loudly(monkeypatch, tmp_path):
     # no fallback: without the built library every entry point raises
     monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "_stream", lambda s: 0)       # no CUDA stream on this host
     monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "libmtpspec.so"))
     with pytest.raises(ImportError):
         b.load()
