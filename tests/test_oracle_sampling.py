@@ -10,7 +10,9 @@ speculative decoding" item 3).
 - special cases: a one-hot draft distribution is kept with probability p(x) and otherwise
   replaced by a draw from p without x; k = 1 and a vanishing temperature reduce to the
   greedy rule;
-- every verification emits 1 to D+1 tokens.
+- every verification emits 1 to D+1 tokens;
+- a decoding loop of repeated verifications (D = 3, drafts drawn from q) against a
+  stationary target emits independent draws from p: non-overlapping pairs follow p x p.
 """
 import numpy as np
 import pytest
@@ -259,3 +261,37 @@ def test_one_hot_mode_lossless_and_acceptance():
     assert r["status"] & oracle.STATUS_BAD_DRAFT_ID
     assert (r["num_accepted"] == 0).all() and (r["p_draft"] == 0).all()
     assert _chi2_ok(np.bincount(r["out"][:, 0], minlength=V), P)
+
+
+def test_emitted_stream_is_iid_from_the_target():
+    # a stationary target (every position has the same filtered distribution p) and a
+    # drafter that draws each guess from q: a decoding loop that verifies again and again
+    # must emit a stream of independent draws from p.  Non-overlapping pairs of the stream
+    # are checked against p x p, which a wrong residual or bonus at any position, or a
+    # uniform shared between positions, would fail.  top-k 4 leaves p > 0 on an id that q
+    # never proposes, so the residual must supply it.
+    V, D, B, calls = 5, 3, 400, 40
+    rng = np.random.default_rng(21)
+    t = np.array([1.0, 0.3, -0.4, 0.6, -1.0], np.float32)
+    q = np.array([0.2, 0.9, -0.1, -0.3, 0.5], np.float32)
+    tau, k, p = 1.0, 4, 1.0
+    P = oracle.filter_probs(t, tau, k, p)
+    Qd = oracle.filter_probs(q, tau, k, p)
+    assert P[3] > 0 and Qd[3] == 0
+    T, Q = _rows(np.stack([t] * (D + 1)), np.stack([q] * D), B)
+    streams = [[] for _ in range(B)]
+    for c in range(calls):
+        d = rng.choice(V, size=(B, D), p=Qd).astype(np.int32)
+        r = oracle.verify_sample(T, Q, d, np.full(B, tau, np.float32), np.full(B, k, np.int32),
+                                 np.full(B, p, np.float32), seed=1000 + c)
+        for b in range(B):
+            streams[b].extend(int(x) for x in r["out"][b] if x >= 0)
+    marg = np.zeros(V, np.int64)
+    pairs = np.zeros((V, V), np.int64)
+    for s in streams:
+        a = np.array(s[: len(s) // 2 * 2])
+        marg += np.bincount(a, minlength=V)
+        np.add.at(pairs, (a[0::2], a[1::2]), 1)
+    assert pairs.sum() > 12000
+    assert _chi2_ok(marg, P)
+    assert _chi2_ok(pairs.ravel(), np.outer(P, P).ravel())
