@@ -1,0 +1,78 @@
+"""The oracle's pins catch plausible mistakes.  Each case copies the oracle, the tests and
+the input generator into a temporary directory, plants one mistake in the oracle's C
+source (a dropped term, a wrong sign, index or word, a transposed operand, an off-by-one),
+and runs the oracle's pin tests there: they must fail.  The product library is neither
+built nor touched."""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# (name, text in oracle/mtpspec_oracle.c, the planted mistake)
+MUTATIONS = [
+    ("top-p boundary not strict", "if (S < p) {", "if (S <= p) {"),
+    ("hidden half first in the concatenation",
+     "orc_rmsnorm_bf16(e + t * H, we, H, eps, x);\n        orc_rmsnorm_bf16(h + t * H, wh, H, eps, x + H);",
+     "orc_rmsnorm_bf16(h + t * H, wh, H, eps, x);\n        orc_rmsnorm_bf16(e + t * H, we, H, eps, x + H);"),
+    ("argmax ties to the highest id", "if (v > bv) {", "if (v >= bv) {"),
+    ("residual q - p", "double r = wp[i] / Zp - wq[i] / Zq;", "double r = wq[i] / Zq - wp[i] / Zp;"),
+    ("accept test flipped", "accept = ua <= ratio;", "accept = ua >= ratio;"),
+    ("top-k threshold off by one", "theta = s[k - 1].v;", "theta = s[k].v;"),
+    ("Philox round word", "uint32_t n0 = hi1 ^ c1 ^ k0;", "uint32_t n0 = lo1 ^ c1 ^ k0;"),
+    ("bonus drawn at position D-1",
+     "rc = orc_filter_weights(rowT + (size_t)D * (size_t)V * es, dt, V, tb, kb, pb, wp, inp,",
+     "rc = orc_filter_weights(rowT + (size_t)(D - 1) * (size_t)V * es, dt, V, tb, kb, pb, wp, inp,"),
+    ("RMSNorm of the sum, not the mean", "double r = 1.0 / sqrt(ss / (double)H + eps);",
+     "double r = 1.0 / sqrt(ss + eps);"),
+    ("temperature dropped", "double wi = exp((s[kept].v - m) / tau);",
+     "double wi = exp((s[kept].v - m));"),
+    ("accept uniform from another word", "*u_acc = word_to_uniform(o[0]);",
+     "*u_acc = word_to_uniform(o[2]);"),
+    ("accept and draw share a word", "*u_smp = word_to_uniform(o[1]);",
+     "*u_smp = word_to_uniform(o[0]);"),
+    ("normalised activations not rounded to bf16",
+     "out[i] = bf16_bits_to_double(orc_double_to_bf16(y));", "out[i] = y;"),
+    ("draft outside q's support not accepted", "} else if (!inq[dj]) {", "} else if (0) {"),
+    ("rejection draws from p, not the residual", "tok = orc_inverse_cdf(wr, V, us, &dm);",
+     "tok = orc_inverse_cdf(wp, V, us, &dm);"),
+    ("inverse CDF from the top id",
+     "for (int64_t i = 0; i < V; ++i) {\n        double prev = c;",
+     "for (int64_t i = V - 1; i >= 0; --i) {\n        double prev = c;"),
+]
+
+
+def _copy(dst):
+    ignore = shutil.ignore_patterns("_build", "__pycache__", "*.so", "*.o")
+    for d in ("oracle", "tests", "verify_spec_greedy_gb300"):
+        shutil.copytree(os.path.join(ROOT, d), os.path.join(dst, d), ignore=ignore)
+    for f in ("pytest.ini", "bench.py"):
+        if os.path.exists(os.path.join(ROOT, f)):
+            shutil.copy(os.path.join(ROOT, f), dst)
+
+
+@pytest.mark.parametrize("name,text,mistake", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_a_planted_mistake_fails_a_pin(tmp_path, name, text, mistake):
+    _copy(str(tmp_path))
+    src = tmp_path / "oracle" / "mtpspec_oracle.c"
+    s = src.read_text()
+    assert s.count(text) == 1, f"the text to change is not unique in the oracle: {name}"
+    src.write_text(s.replace(text, mistake))
+    tests = sorted(str(p.relative_to(tmp_path)) for p in (tmp_path / "tests").glob("test_oracle_*.py")
+                   if p.name != "test_oracle_mutations.py")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        *tests], cwd=str(tmp_path), capture_output=True, text=True, timeout=600)
+    assert r.returncode == 1, f"{name}: no pin failed\n{r.stdout[-2000:]}"
+
+
+def test_the_copy_without_a_mistake_passes(tmp_path):
+    # the control: the same copy and command, unchanged, pass
+    _copy(str(tmp_path))
+    tests = sorted(str(p.relative_to(tmp_path)) for p in (tmp_path / "tests").glob("test_oracle_*.py")
+                   if p.name != "test_oracle_mutations.py")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        *tests], cwd=str(tmp_path), capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:]
