@@ -127,3 +127,21 @@ def test_topk_of_a_one_hot_hidden_is_a_sorted_column():
     ids, vals = oracle.lm_head_topk(h, x["W"], 5)
     col = _f(x["W"][:, 9])
     np.testing.assert_array_equal(ids[0], np.argsort(-col, kind="stable")[:5])
+
+
+def test_topk_lists_equal_logits_by_id():
+    # each token's largest row copied to a lower and a higher id: the three equal logits
+    # head the list in increasing id order, the next one follows
+    M, H, V, k = 3, 96, 500, 5
+    x = make_lm_head_input(M, H, V, seed=14)
+    ids0, _ = oracle.lm_head_topk(x["hidden"], x["W"], k)
+    for t in range(M):
+        a = int(ids0[t, 0])
+        lo, hi = (a + 7) % 3, V - 1 - (a % 2)          # two other ids, below and above a
+        assert lo < a < hi
+        W = x["W"].copy()
+        W[lo] = W[a]
+        W[hi] = W[a]
+        ids, vals = oracle.lm_head_topk(x["hidden"][t:t + 1], W, k)
+        np.testing.assert_array_equal(ids[0, :3], sorted([lo, a, hi]))
+        assert vals[0, 0] == vals[0, 1] == vals[0, 2] > vals[0, 3]

@@ -42,6 +42,22 @@ MUTATIONS = [
     ("inverse CDF from the top id",
      "for (int64_t i = 0; i < V; ++i) {\n        double prev = c;",
      "for (int64_t i = V - 1; i >= 0; --i) {\n        double prev = c;"),
+    ("output layer without its final norm",
+     "if (norm_w)\n            orc_rmsnorm_bf16(h, norm_w, H, eps, x);",
+     "if (0)\n            orc_rmsnorm_bf16(h, norm_w, H, eps, x);"),
+    ("output-layer pick ties to the highest id", "if (lg[v] > lg[best])", "if (lg[v] >= lg[best])"),
+    ("output-layer sum drops the last element",
+     "for (int64_t k = 0; k < H; ++k) {\n                double pr",
+     "for (int64_t k = 0; k < H - 1; ++k) {\n                double pr"),
+    ("top-k of the output layer ties to the highest id", "(best < 0 || lg[v] > lg[best])",
+     "(best < 0 || lg[v] >= lg[best])"),
+    ("a hit keeps D positions", "kv = kv_before[b] + D + 1;", "kv = kv_before[b] + D;"),
+    ("recompute omits the carried-in token", "rc = 1 + a;", "rc = a;"),
+    ("a miss without recurrent state keeps a positions", "kv = kv_before[b] + 1 + a;",
+     "kv = kv_before[b] + a;"),
+    ("the draft head's KV is not cut on a miss",
+     "if (draft_kv_len && miss && draft_kv_len[b] > kv)", "if (0)"),
+    ("position-0 mask at every step", "positions[t] + k == 0", "positions[t] == 0"),
 ]
 
 
