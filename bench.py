@@ -213,14 +213,26 @@ def sample_rows(x, rows):
     return list(range(n_g)) + list(range(ng, ng + rows - n_g))
 
 
-def oracle_sample(x, di, w, rows, min_seconds=0.0, sel=None):
+def cpu_model():
+    """The host CPU's model name (lscpu), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+    except (OSError, subprocess.SubprocessError):
+        return None
+    for line in out.splitlines():
+        if line.strip().lower().startswith("model name:"):
+            return line.split(":", 1)[1].strip()
+    return None
+
+
+def oracle_sample(x, di, w, rows, min_seconds=0.0, sel=None, threads=None):
     """Time the oracle on a bounded sample: `rows` rows of the verify (the workload's mix
     of greedy and sampled rows; or the rows `sel`) plus the draft-input tokens of those
     rows and the greedy drafts of the greedy rows among them, spread over the host cores;
     the sample is repeated until at least `min_seconds` have passed."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
-    cores = os.cpu_count() or 1
+    cores = threads or os.cpu_count() or 1
     B = x["B"]
     if sel is None:
         sel = sample_rows(x, rows)
@@ -754,7 +766,12 @@ def main():
         if world == 1 and not args.no_cpu_baseline:
             v, cores, sample, dt = oracle_sample(x, di, w, rows=x["B"], min_seconds=10.0)
             res["cpu_baseline"] = {"value": round(v, 2), "unit": UNIT, "cores": cores,
-                                   "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+                                   "kind": "oracle", "sample": sample, "seconds": round(dt, 2),
+                                   "cpu_model": cpu_model()}
+            # the same oracle on one core, over a smaller sample of the same mix
+            v1, _, sample1, dt1 = oracle_sample(x, di, w, rows=8, min_seconds=2.0, threads=1)
+            res["cpu_baseline"]["single_thread"] = {"value": round(v1, 2), "unit": UNIT,
+                                                    "sample": sample1, "seconds": round(dt1, 2)}
         print(json.dumps(res), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -810,7 +827,7 @@ def run_reference(args):
            "config": {"workload": w.name, "B": x["B"], "D": x["D"], "V": x["V"], "H": w.H,
                       "draft_tokens": w.tokens},
            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores,
-                            "kind": "oracle", "sample": sample},
+                            "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)

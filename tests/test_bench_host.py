@@ -87,3 +87,31 @@ def test_clock_samples_give_the_median_and_the_active_reasons():
     # unreadable lines are skipped; no samples at all is reported as such
     assert _sampler(["garbage", ok])["samples"] == 1
     assert _sampler(["garbage"])["reasons"] == ["no samples"]
+
+
+def test_oracle_sample_on_one_core(serve):
+    from verify_spec_greedy_gb300.inputs import make_draft_input
+    w, x = serve
+    v, cores, sample, dt = bench.oracle_sample(x, make_draft_input(w), w, rows=4, threads=1)
+    assert cores == 1 and v > 0 and dt > 0
+    assert sample.startswith("4 of 256 rows (1 greedy)")
+    m = bench.cpu_model()
+    assert m is None or (isinstance(m, str) and m)
+
+
+def test_main_adds_the_cpu_baseline_after_the_gpu_step(monkeypatch, capsys):
+    # the GPU step replaced by a stub: what main() does after it (the oracle on all host
+    # cores and on one, the CPU model) runs as on a GPU machine
+    import json
+    import sys
+    from verify_spec_greedy_gb300.inputs import make_draft_input
+    w = WORKLOADS["sample_b8_d3_v152k"]
+    x = make_verify_inputs(w)
+    di = make_draft_input(w)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", w.name])
+    monkeypatch.setattr(bench, "run_gpu", lambda args, rank, world, dist: ({"metric": "m"}, x, di, w))
+    assert bench.main() == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["seconds"] >= 10.0
+    assert cb["single_thread"]["value"] > 0 and "cpu_model" in cb
