@@ -421,8 +421,8 @@ def run_gpu(args, rank, world, dist):
 
     res = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": max(3, args.warmup),
-           "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": x["dtype"],
+           "ms_per_step": round(ms_max / args.steps, 5), "logits_per_s": round(value * V, 1),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": x["dtype"],
            "data": "synthetic",
            "config": {"workload": w.name, "B": B, "D": D, "V": V, "H": H, "draft_tokens": M,
                       "greedy_rows": ng, "top_k": int(w.top_k), "top_p": float(w.top_p),
@@ -822,7 +822,8 @@ def run_reference(args):
     res = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
            "n_gpus": max(1, args.gpus), "device": "host cores", "steps": steps,
            "warmup": warm,
-           "ms_per_step": round(1e3 * t_sum / steps, 2), "higher_is_better": True,
+           "ms_per_step": round(1e3 * t_sum / steps, 2),
+           "logits_per_s": round(value * x["V"], 1), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": w.name, "B": x["B"], "D": x["D"], "V": x["V"], "H": w.H,
                       "draft_tokens": w.tokens},
