@@ -58,6 +58,8 @@ MUTATIONS = [
     ("the draft head's KV is not cut on a miss",
      "if (draft_kv_len && miss && draft_kv_len[b] > kv)", "if (0)"),
     ("position-0 mask at every step", "positions[t] + k == 0", "positions[t] == 0"),
+    ("a draft step's output not passed on as the next hidden state",
+     "            h[i] = orc_double_to_bf16(y[i]);", "            (void)y[i];"),
 ]
 
 
