@@ -72,25 +72,50 @@ def _copy(dst):
             shutil.copy(os.path.join(ROOT, f), dst)
 
 
-@pytest.mark.parametrize("name,text,mistake", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_a_planted_mistake_fails_a_pin(tmp_path, name, text, mistake):
-    _copy(str(tmp_path))
-    src = tmp_path / "oracle" / "mtpspec_oracle.c"
-    s = src.read_text()
-    assert s.count(text) == 1, f"the text to change is not unique in the oracle: {name}"
-    src.write_text(s.replace(text, mistake))
-    tests = sorted(str(p.relative_to(tmp_path)) for p in (tmp_path / "tests").glob("test_oracle_*.py")
-                   if p.name != "test_oracle_mutations.py")
+def _pin_run(dst, text=None, mistake=None):
+    """Copy into dst, plant the mistake (if any), run the oracle's pin tests there; returns
+    (exit code, the last lines of their output) or raises when the text is not unique."""
+    _copy(dst)
+    if text is not None:
+        src = os.path.join(dst, "oracle", "mtpspec_oracle.c")
+        s = open(src).read()
+        if s.count(text) != 1:
+            raise AssertionError("the text to change is not unique in the oracle")
+        open(src, "w").write(s.replace(text, mistake))
+    tests = sorted(os.path.join("tests", f) for f in os.listdir(os.path.join(dst, "tests"))
+                   if f.startswith("test_oracle_") and f.endswith(".py")
+                   and f != "test_oracle_mutations.py")
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        *tests], cwd=str(tmp_path), capture_output=True, text=True, timeout=600)
-    assert r.returncode == 1, f"{name}: no pin failed\n{r.stdout[-2000:]}"
+                        *tests], cwd=dst, capture_output=True, text=True, timeout=900)
+    return r.returncode, r.stdout[-2000:]
 
 
-def test_the_copy_without_a_mistake_passes(tmp_path):
+@pytest.fixture(scope="module")
+def outcomes(tmp_path_factory):
+    """Every case (and the unchanged control) run at once, one process each, spread over
+    the host cores."""
+    from concurrent.futures import ThreadPoolExecutor
+    jobs = {None: (None, None)}
+    jobs.update({name: (text, mistake) for name, text, mistake in MUTATIONS})
+    base = tmp_path_factory.mktemp("pins")
+
+    def run(item):
+        i, (name, (text, mistake)) = item
+        try:
+            return name, _pin_run(str(base / f"case{i}"), text, mistake)
+        except AssertionError as e:
+            return name, (None, str(e))
+    with ThreadPoolExecutor(max(1, min(8, os.cpu_count() or 1))) as ex:
+        return dict(ex.map(run, enumerate(jobs.items())))
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTATIONS])
+def test_a_planted_mistake_fails_a_pin(outcomes, name):
+    code, out = outcomes[name]
+    assert code == 1, f"{name}: no pin failed (exit code {code})\n{out}"
+
+
+def test_the_copy_without_a_mistake_passes(outcomes):
     # the control: the same copy and command, unchanged, pass
-    _copy(str(tmp_path))
-    tests = sorted(str(p.relative_to(tmp_path)) for p in (tmp_path / "tests").glob("test_oracle_*.py")
-                   if p.name != "test_oracle_mutations.py")
-    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        *tests], cwd=str(tmp_path), capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stdout[-2000:]
+    code, out = outcomes[None]
+    assert code == 0, out
