@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload timings added to the JSON line")
     ap.add_argument("--no-launch-count", action="store_true",
                     help="accepted for older command lines; launches are counted by the library")
     ap.add_argument("--batch", type=int, default=0,
@@ -416,6 +418,7 @@ def run_gpu(args, rank, world, dist):
     roofline = {"bound": "hbm", "kernel": "spec_verify_sample: k_verify_rr + k_argmax_verify_rows + k_verify_finalize",
                 "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "frac_vs_nominal_8tbs": round(achieved / 8000.0, 4),
                 "algorithmic_bytes_per_launch": vb,
                 "launch_ms": round(verify_ms, 5), "traffic": traffic}
 
@@ -436,6 +439,133 @@ def run_gpu(args, rank, world, dist):
            "gpu_launches": launches,
            "roofline": roofline}
     return res, x, di, w
+
+
+def measure_per_config(dev, cached=None, graph_calls=20, reps=15):
+    """Every workload's verify and draft-input calls, timed in this run: each call alone
+    after an L2 flush (a write of twice the L2; median of `reps` launches), the verify call
+    of the three small workloads also as a CUDA graph of `graph_calls` back-to-back calls on
+    distinct copies of the inputs (after a flush; per-call time = replay / calls), and the
+    sampled workloads' verify once more with one-hot drafts.  Fractions are of the measured
+    peaks (HBM copy bandwidth, or bf16 tensor throughput for a contraction whose
+    arithmetic intensity is above the ridge).  `cached` maps a workload name to inputs
+    already made (x, di)."""
+    import torch
+    import verify_spec_greedy_gb300 as lib
+    from verify_spec_greedy_gb300.inputs import WORKLOADS, make_draft_input, make_verify_inputs
+    hbm, _ = measured_peaks()
+    tflops = 1881.1
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        tflops = float(json.load(open(pk)).get("bf16_tflops", tflops))
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    cached = cached or {}
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def roof(nbytes, ms):
+        ach = nbytes / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "bytes": int(nbytes)}
+
+    res = {}
+    for name, w in WORKLOADS.items():
+        x, di = cached.get(name) or (make_verify_inputs(w), make_draft_input(w))
+        B, D, V = x["B"], x["D"], x["V"]
+        es = 4 if x["dtype"] == "f32" else 2
+        T, d = to_dev(x["T"]), to_dev(x["d"])
+        Q = None if w.mode == "greedy" else to_dev(x["Q"])
+        out = torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+        na = torch.empty(B, dtype=torch.int32, device=dev)
+        entry = {"B": B, "D": D, "V": V, "H": w.H, "logits": x["dtype"]}
+        if w.mode == "greedy":
+            def call(Ti=T, Qi=None, o=out, n=na, one_hot=False):
+                lib.spec_verify_greedy(Ti, d, o, n)
+            vbytes = B * (D + 1) * V * es
+            entry["verify_call"] = "spec_verify_greedy"
+        else:
+            tau, top_p = to_dev(x["tau"]), to_dev(x["top_p"])
+            top_k = to_dev(x["top_k"]) if (x["top_k"] > 0).any() else None
+            ws = torch.empty(lib.spec_verify_workspace_bytes(B, D, V), dtype=torch.uint8,
+                             device=dev)
+
+            def call(Ti=T, Qi=Q, o=out, n=na, one_hot=False):
+                lib.spec_verify_sample(Ti, None if one_hot else Qi, d, tau, top_k, top_p,
+                                       x["seed"], o, n, None, None, ws)
+            vbytes = verify_bytes(x)
+            entry["verify_call"] = "spec_verify_sample"
+        vms = timed(call)
+        entry["verify_us"] = round(vms * 1e3, 2)
+        entry["verify_rows_per_s"] = round(B * (D + 1) / (vms / 1e3), 1)
+        entry["verify_roofline"] = roof(vbytes, vms)
+        if vbytes < L2_BYTES:
+            # back-to-back calls as a decode loop issues them: a CUDA graph of calls, each on
+            # its own copy of the logits
+            Ts = [T] + [T.clone() for _ in range(graph_calls - 1)]
+            Qs = None if Q is None else [Q] + [Q.clone() for _ in range(graph_calls - 1)]
+            outs = [torch.empty_like(out) for _ in range(graph_calls)]
+            nas = [torch.empty_like(na) for _ in range(graph_calls)]
+            calls = [lambda i=i: call(Ts[i], None if Qs is None else Qs[i], outs[i], nas[i])
+                     for i in range(graph_calls)]
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                for c in calls:
+                    c()
+            stream.wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for c in calls:
+                    c()
+            gms = timed(graph.replay) / graph_calls
+            entry["verify_graph_batch"] = {"calls": graph_calls, "us_per_call": round(gms * 1e3, 2),
+                                           "rows_per_s": round(B * (D + 1) / (gms / 1e3), 1),
+                                           "roofline": roof(vbytes, gms)}
+            del graph, Ts, Qs
+        if w.mode != "greedy":
+            oms = timed(lambda: call(one_hot=True))
+            ob = vbytes - (B - int((x["tau"] == 0).sum())) * D * V * es
+            entry["one_hot_verify"] = {"us": round(oms * 1e3, 2),
+                                       "rows_per_s": round(B * (D + 1) / (oms / 1e3), 1),
+                                       "roofline": roof(ob, oms)}
+        M, H = w.tokens, w.H
+        e, h = to_dev(di["e"][0][:M]), to_dev(di["h"][0][:M])
+        we, wh, W = to_dev(di["we"]), to_dev(di["wh"]), to_dev(di["W"])
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        wsd = torch.empty(max(1, lib.mtp_draft_input_workspace_bytes(M, H)), dtype=torch.uint8,
+                          device=dev)
+        dms = timed(lambda: lib.mtp_draft_input(e, h, we, wh, W, y, di["eps"], wsd))
+        dbytes = draft_input_bytes(w)
+        dflop = 2.0 * M * H * 2 * H
+        if dflop / dbytes > tflops * 1e12 / (hbm * 1e9):
+            ach = dflop / (dms / 1e3) / 1e12
+            droof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tflops,
+                     "unit": "TFLOP/s", "frac": round(ach / tflops, 4), "flop": dflop}
+        else:
+            droof = roof(dbytes, dms)
+        entry["draft_input"] = {"tokens": M, "us": round(dms * 1e3, 2),
+                                "tokens_per_s": round(M / (dms / 1e3), 1), "roofline": droof}
+        res[name] = entry
+        del T, Q
+    return res
 
 
 def run_sweep(args):
@@ -762,6 +892,10 @@ def main():
         return run_reference(args)
     rank, world, dist = dist_init(args.gpus)
     res, x, di, w = run_gpu(args, rank, world, dist)
+    if rank == 0 and not args.no_per_config and not args.batch:
+        import torch
+        res["per_config"] = measure_per_config(torch.device("cuda", torch.cuda.current_device()),
+                                               cached={w.name: (x, di)})
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             v, cores, sample, dt = oracle_sample(x, di, w, rows=x["B"], min_seconds=10.0)

@@ -67,6 +67,9 @@ def _load():
         lib.orc_verify_sample.argtypes = [p, p, C.c_int, p, p, p, p, u64, i64, i64, i32, i64,
                                           p, p, p, p, p, p]
         lib.orc_verify_sample.restype = C.c_int
+        lib.orc_verify_unit.argtypes = [p, p, C.c_int, i64, i32, dbl, i32, dbl, dbl, dbl, i32, i32,
+                                        i64, i64, dbl, p, p, p, p]
+        lib.orc_verify_unit.restype = C.c_int
         lib.orc_draft_input.argtypes = [p, p, p, p, p, i64, i64, dbl, p, p]
         lib.orc_draft_input.restype = C.c_int
         lib.orc_draft_input_at.argtypes = [p, p, p, p, p, i64, i64, dbl, p, p, i64, p]
@@ -203,6 +206,41 @@ def verify_sample(T, Q, d, tau, top_k=None, top_p=None, seed: int = 0, row0: int
                                      int(seed), int(row0), B, D, V, _ptr(out), _ptr(na), _ptr(pt),
                                      _ptr(pd), _ptr(st), _ptr(mg)), "verify_sample")
     return dict(out=out, num_accepted=na, p_target=pt, p_draft=pd, status=int(st[0]), margins=mg)
+
+
+def verify_unit(t_row, q_row, d: int, tau: float, k: int = 0, p: float = 1.0,
+                u_acc: float = 0.5, u_smp: float = 0.5, bonus: bool = False, draw: bool = True,
+                gt: int = -1, gq: int = -1, delta: float = 0.0, with_weights: bool = False):
+    """One verification unit with explicit uniforms (see orc_verify_unit).
+
+    t_row [V] (and q_row [V], or None for a one-hot draft) fp32 or bf16 bits; bonus: the
+    position after the last draft (a draw from p, no accept test).  gt / gq force the
+    number of top-p groups kept in the target / draft row (-1: the rule); delta is the
+    window of the reported alternative counts.  Returns a dict: accept, pt, pd, ratio,
+    acc_margin, margin_t, margin_q, cdf_margin, token (-1 when nothing was drawn),
+    cdf_lo / cdf_hi (the draw's distances to its cell's edges, relative to the total),
+    tok_prev / tok_next (the neighbouring ids with positive draw weight, -1 if none),
+    cut_t / cut_q = (groups the rule keeps, fewest, most within delta), w_draw [V] or None.
+    """
+    x, dt = _logits(t_row)
+    V = x.size
+    q = None
+    if q_row is not None:
+        q, dq = _logits(q_row)
+        assert dq == dt and q.size == V
+    dres = np.zeros(8, np.float64)
+    dnb = np.zeros(4, np.float64)
+    ires = np.zeros(7, np.int64)
+    w = np.zeros(V, np.float64) if with_weights else None
+    _check(_load().orc_verify_unit(_ptr(x), _ptr(q), dt, V, int(d), float(tau), int(k), float(p),
+                                   float(u_acc), float(u_smp), int(bool(bonus)), int(bool(draw)),
+                                   int(gt), int(gq), float(delta), _ptr(dres), _ptr(dnb),
+                                   _ptr(ires), _ptr(w)), "verify_unit")
+    return dict(accept=bool(dres[0]), pt=dres[1], pd=dres[2], ratio=dres[3], acc_margin=dres[4],
+                margin_t=dres[5], margin_q=dres[6], cdf_margin=dres[7], token=int(ires[0]),
+                cdf_lo=dnb[0], cdf_hi=dnb[1], tok_prev=int(dnb[2]), tok_next=int(dnb[3]),
+                cut_t=tuple(int(v) for v in ires[1:4]), cut_q=tuple(int(v) for v in ires[4:7]),
+                w_draw=w)
 
 
 def verify_sample_rows(T, Q, d, tau, top_k=None, top_p=None, seed: int = 0, rows=None,

@@ -254,14 +254,25 @@ static int orc_vi_desc(const void *pa, const void *pb)
  * Writes the unnormalised kept weights to w[V], support membership to in[V] (a kept
  * token whose weight underflows is still in the support), their sum to *Z and the row
  * maximum to *mx.  A row whose logits are all -inf is a point mass on id 0, its
- * argmax.  *margin_p (if given)
- * receives the distance from p of the two masses that decide the top-p boundary
- * (+inf when top-p is off). */
-static int orc_filter_weights(const void *x, int dt, int64_t V, double tau, int32_t k, double p,
-                              double *w, unsigned char *in, double *Z, double *mx, double *margin_p)
+ * argmax.  *margin_p (if given) receives the distance from p of the two masses that
+ * decide the top-p boundary (+inf when top-p is off).
+ *
+ * For the parity checker: the top-p rule walks groups of equal logits from the top, and
+ * group g (1-based) stays when the mass S_g strictly above it is < p.  force_groups >= 1
+ * keeps exactly the first force_groups groups of the top-k set instead (as a computation
+ * whose masses are off by less than delta might); cuts (if given) receives the number of
+ * groups the rule keeps and the smallest and largest counts that such a computation can
+ * reach: g with S_g < p + delta and S_{g+1} >= p - delta (S of one past the last group
+ * is 1).  With top-p off all three are the group count. */
+static int orc_filter_weights_cut(const void *x, int dt, int64_t V, double tau, int32_t k,
+                                  double p, int64_t force_groups, double delta, double *w,
+                                  unsigned char *in, double *Z, double *mx, double *margin_p,
+                                  int64_t *cuts)
 {
     if (margin_p)
         *margin_p = INFINITY;
+    if (cuts)
+        cuts[0] = cuts[1] = cuts[2] = 1;
     orc_vi *s = (orc_vi *)malloc((size_t)V * sizeof(orc_vi));
     if (!s)
         return ORC_ERR_NOMEM;
@@ -308,7 +319,7 @@ static int orc_filter_weights(const void *x, int dt, int64_t V, double tau, int3
     if (p < 1.0) {
         /* walk groups of equal logits from the top; S = normalised mass strictly above */
         double above = 0.0;
-        int64_t g = 0;
+        int64_t g = 0, gi = 0, cut = -1, rule = 1, glo = -1, ghi = 1;
         while (g < kept) {
             int64_t h = g;
             double gm = 0.0;
@@ -316,32 +327,65 @@ static int orc_filter_weights(const void *x, int dt, int64_t V, double tau, int3
                 gm += w[s[h].i];
                 ++h;
             }
+            ++gi;
             double S = above / z;
-            if (S < p) {
+            if (S < p + delta)
+                ghi = gi;
+            if (glo < 0 && ((above + gm) / z >= p - delta || h == kept))
+                glo = gi;
+            int keep = S < p;
+            if (keep)
+                rule = gi;
+            if (force_groups >= 1)
+                keep = gi <= force_groups;
+            if (keep && cut < 0) {
                 above += gm;
-                if (margin_p) {
+                if (margin_p && force_groups < 1) {
                     double mk = p - S; /* how far the kept group was from dropping */
                     double md = fabs(above / z - p); /* mass that the next group would see */
                     double mm = mk < md ? mk : md;
                     *margin_p = mm;
                 }
-                g = h;
             } else {
-                for (int64_t t = g; t < kept; ++t) {
-                    w[s[t].i] = 0.0;
-                    in[s[t].i] = 0;
-                }
-                kept = g;
-                break;
+                if (cut < 0)
+                    cut = g;
+                above += gm;
             }
+            g = h;
+            if (cut >= 0 && S >= p && above / z >= p + delta && glo >= 0)
+                break;
+        }
+        if (cuts) {
+            cuts[0] = rule;
+            cuts[1] = glo;
+            cuts[2] = ghi;
+        }
+        if (cut >= 0) {
+            for (int64_t t = cut; t < kept; ++t) {
+                w[s[t].i] = 0.0;
+                in[s[t].i] = 0;
+            }
+            kept = cut;
         }
         z = 0.0;
         for (int64_t t = 0; t < kept; ++t)
             z += w[s[t].i];
+    } else if (cuts) {
+        int64_t ng = 0;
+        for (int64_t t = 0; t < kept; ++t)
+            if (t == 0 || s[t].v != s[t - 1].v)
+                ++ng;
+        cuts[0] = cuts[1] = cuts[2] = ng;
     }
     *Z = z;
     free(s);
     return ORC_OK;
+}
+
+static int orc_filter_weights(const void *x, int dt, int64_t V, double tau, int32_t k, double p,
+                              double *w, unsigned char *in, double *Z, double *mx, double *margin_p)
+{
+    return orc_filter_weights_cut(x, dt, V, tau, k, p, -1, 0.0, w, in, Z, mx, margin_p, NULL);
 }
 
 /* Normalised filtered probabilities of one row (see orc_filter_weights). */
@@ -369,34 +413,232 @@ int orc_filter(const void *x, int dt, int64_t V, double tau, int32_t k, double p
 
 /* Inverse-CDF draw over non-negative weights in ascending id order: the smallest i with
  * C(i) = sum_{y <= i} w_y > u * sum(w); if rounding leaves none, the largest i with
- * w_i > 0.  *margin receives min(u*S - C(i-1), C(i) - u*S) / S. */
-static int64_t orc_inverse_cdf(const double *w, int64_t V, double u, double *margin)
+ * w_i > 0.  *margin receives min(u*S - C(i-1), C(i) - u*S) / S.  For the parity checker
+ * nb (if given) receives those two distances apart, (u*S - C(i-1)) / S and
+ * (C(i) - u*S) / S, and the nearest ids below and above i with positive weight (-1 if
+ * none): the tokens a draw whose sums are off by less than the distance would give. */
+static int64_t orc_inverse_cdf_nb(const double *w, int64_t V, double u, double *margin,
+                                  double *nb)
 {
     double S = 0.0;
     for (int64_t i = 0; i < V; ++i)
         S += w[i];
     double t = u * S;
     double c = 0.0;
+    int64_t tok = -1;
+    double lo = 0.0, hi = 0.0;
     for (int64_t i = 0; i < V; ++i) {
         double prev = c;
         c += w[i];
         if (c > t) {
-            if (margin) {
-                double a = (t - prev) / S, b = (c - t) / S;
+            double a = (t - prev) / S, b = (c - t) / S;
+            if (margin)
                 *margin = a < b ? a : b;
-            }
-            return i;
+            lo = a;
+            hi = b;
+            tok = i;
+            break;
         }
     }
-    if (margin)
-        *margin = 0.0;
-    for (int64_t i = V - 1; i >= 0; --i)
-        if (w[i] > 0.0)
-            return i;
-    return 0;
+    if (tok < 0) {
+        if (margin)
+            *margin = 0.0;
+        for (int64_t i = V - 1; i >= 0; --i)
+            if (w[i] > 0.0) {
+                tok = i;
+                break;
+            }
+        if (tok < 0)
+            tok = 0;
+    }
+    if (nb) {
+        int64_t pv = -1, nx = -1;
+        for (int64_t i = tok - 1; i >= 0; --i)
+            if (w[i] > 0.0) {
+                pv = i;
+                break;
+            }
+        for (int64_t i = tok + 1; i < V; ++i)
+            if (w[i] > 0.0) {
+                nx = i;
+                break;
+            }
+        nb[0] = lo;
+        nb[1] = hi;
+        nb[2] = (double)pv;
+        nb[3] = (double)nx;
+    }
+    return tok;
 }
 
 /* ------------------------------------------------------------------ sampling verify */
+
+/* Everything one verification unit (row b, position j) decides, given its uniforms. */
+typedef struct {
+    int32_t accept;      /* position j < D: the draft held */
+    double pt, pd;       /* p_j(d_j), q_j(d_j) */
+    double ratio;        /* p/q of the accept test (NAN when the test needs no ratio) */
+    double acc_margin;   /* |U_acc - p/q| (+inf when no ratio is formed) */
+    double mp_t, mp_q;   /* top-p margins of the target and draft rows */
+    int64_t token;       /* the draw (at a rejection or at the bonus position), or -1 */
+    double cdf_margin;   /* its inverse-CDF margin */
+    double nb[4];        /* its distances to the neighbouring cells and their ids */
+    int64_t cut_t[3], cut_q[3]; /* top-p group counts: the rule's, the smallest, the largest */
+} orc_unit_result;
+
+/* One unit of speculative-sampling verification ([ZH] 三 stage 3 "rejection sampling";
+ * [DL] "MTP speculative decoding" items 2-3).  rowT / rowQ are T[b, j] and Q[b, j] (rowQ
+ * NULL: a one-hot draft, q_j the point mass on d_j).  is_bonus: position D, whose token is
+ * drawn from p_D.  Otherwise the accept test of d_j, and, if the draft is rejected and
+ * want_draw is set, the draw from normalize(max(0, p_j - q_j)) (from p_j when that
+ * residual is identically 0).  gt / gq force the top-p group counts of the two rows (-1:
+ * the rule); delta is the window of the reported alternative counts.  w_draw (if given,
+ * [V]) receives the unnormalised weights of the draw. */
+static int orc_unit(const char *rowT, const char *rowQ, int dt, int64_t V, int32_t dj, double tb,
+                    int32_t kb, double pb, double ua, double us, int is_bonus, int want_draw,
+                    int64_t gt, int64_t gq, double delta, double *wp, double *wq, double *wr,
+                    unsigned char *inp, unsigned char *inq, double *w_draw, orc_unit_result *o)
+{
+    double Zp, Zq, mp, mq, xp, xq;
+    o->accept = 0;
+    o->pt = o->pd = 0.0;
+    o->ratio = NAN;
+    o->acc_margin = INFINITY;
+    o->mp_t = o->mp_q = INFINITY;
+    o->token = -1;
+    o->cdf_margin = INFINITY;
+    for (int t = 0; t < 4; ++t)
+        o->nb[t] = t < 2 ? INFINITY : -1.0;
+    for (int t = 0; t < 3; ++t)
+        o->cut_t[t] = o->cut_q[t] = 0;
+    int rc = orc_filter_weights_cut(rowT, dt, V, tb, kb, pb, gt, delta, wp, inp, &Zp, &xp, &mp,
+                                    o->cut_t);
+    if (rc != ORC_OK)
+        return rc;
+    o->mp_t = mp;
+    if (is_bonus) {
+        double dm;
+        o->token = orc_inverse_cdf_nb(wp, V, us, &dm, o->nb);
+        o->cdf_margin = dm;
+        if (w_draw)
+            memcpy(w_draw, wp, (size_t)V * sizeof(double));
+        return ORC_OK;
+    }
+    if (rowQ) {
+        rc = orc_filter_weights_cut(rowQ, dt, V, tb, kb, pb, gq, delta, wq, inq, &Zq, &xq, &mq,
+                                    o->cut_q);
+        if (rc != ORC_OK)
+            return rc;
+        o->mp_q = mq;
+    } else { /* one-hot draft: q_j = 1 at d_j, 0 elsewhere */
+        for (int64_t i = 0; i < V; ++i) {
+            wq[i] = 0.0;
+            inq[i] = 0;
+        }
+        if (dj >= 0 && (int64_t)dj < V) {
+            wq[dj] = 1.0;
+            inq[dj] = 1;
+        }
+        Zq = 1.0;
+        xq = 0.0;
+    }
+    int valid = dj >= 0 && (int64_t)dj < V;
+    double pt = valid ? wp[dj] / Zp : 0.0;
+    double pd = valid ? wq[dj] / Zq : 0.0;
+    o->pt = pt;
+    o->pd = pd;
+    int accept;
+    if (!valid || !inp[dj]) {
+        accept = 0;
+    } else if (!inq[dj]) {
+        accept = 1;
+    } else {
+        /* p/q written with both row maxima factored out, so that it does not
+         * underflow when both probabilities are tiny; a row of all -inf is a
+         * point mass, whose probability is exact */
+        double ratio;
+        if (!rowQ || xp == -INFINITY || xq == -INFINITY) {
+            ratio = pt / pd;
+        } else {
+            double xt = logit_at(rowT, dt, dj);
+            double xd = logit_at(rowQ, dt, dj);
+            ratio = exp(((xt - xp) - (xd - xq)) / tb) * (Zq / Zp);
+        }
+        accept = ua <= ratio;
+        o->ratio = ratio;
+        o->acc_margin = fabs(ua - ratio);
+    }
+    o->accept = accept;
+    if (!accept && want_draw) {
+        /* residual draw at the first rejection */
+        double R = 0.0;
+        for (int64_t i = 0; i < V; ++i) {
+            double r = wp[i] / Zp - wq[i] / Zq;
+            wr[i] = r > 0.0 ? r : 0.0;
+            R += wr[i];
+        }
+        double dm;
+        int64_t tok;
+        if (R > 0.0)
+            tok = orc_inverse_cdf_nb(wr, V, us, &dm, o->nb);
+        else
+            tok = orc_inverse_cdf_nb(wp, V, us, &dm, o->nb);
+        o->token = tok;
+        o->cdf_margin = dm;
+        if (w_draw)
+            memcpy(w_draw, R > 0.0 ? wr : wp, (size_t)V * sizeof(double));
+    }
+    return ORC_OK;
+}
+
+/* One unit with explicit uniforms, for the tests: the exact-enumeration pin integrates
+ * over (u_acc, u_smp), and the parity checker evaluates the alternatives a computation off
+ * by less than delta could take (gt / gq: forced top-p group counts, -1 for the rule).
+ * Outputs: dres[8] = accept, p, q, ratio, |U_acc - ratio|, top-p margin of T, of Q, the
+ * draw's inverse-CDF margin; dnb[4] = the draw's distances to its cell's edges and the
+ * neighbouring ids; ires[7] = token (-1: no draw), the cut counts of T (rule, lowest,
+ * highest) and of Q; w_draw [V] (optional) = the draw's unnormalised weights. */
+int orc_verify_unit(const void *Trow, const void *Qrow, int dt, int64_t V, int32_t dj, double tau,
+                    int32_t k, double p, double ua, double us, int32_t is_bonus, int32_t want_draw,
+                    int64_t gt, int64_t gq, double delta, double *dres, double *dnb, int64_t *ires,
+                    double *w_draw)
+{
+    if (dt != ORC_F32 && dt != ORC_BF16)
+        return ORC_ERR_DTYPE;
+    if (V < 1 || !Trow || !(tau > 0.0) || !(p > 0.0) || !dres || !dnb || !ires)
+        return ORC_ERR_ARG;
+    double *wp = (double *)malloc((size_t)V * sizeof(double) * 3);
+    unsigned char *inp = (unsigned char *)malloc((size_t)V * 2);
+    if (!wp || !inp) {
+        free(wp);
+        free(inp);
+        return ORC_ERR_NOMEM;
+    }
+    orc_unit_result o;
+    int rc = orc_unit((const char *)Trow, (const char *)Qrow, dt, V, dj, tau, k, p, ua, us,
+                      is_bonus, want_draw, gt, gq, delta, wp, wp + V, wp + 2 * V, inp, inp + V,
+                      w_draw, &o);
+    free(wp);
+    free(inp);
+    if (rc != ORC_OK)
+        return rc;
+    dres[0] = o.accept;
+    dres[1] = o.pt;
+    dres[2] = o.pd;
+    dres[3] = o.ratio;
+    dres[4] = o.acc_margin;
+    dres[5] = o.mp_t;
+    dres[6] = o.mp_q;
+    dres[7] = o.cdf_margin;
+    for (int t = 0; t < 4; ++t)
+        dnb[t] = o.nb[t];
+    ires[0] = o.token;
+    for (int t = 0; t < 3; ++t) {
+        ires[1 + t] = o.cut_t[t];
+        ires[4 + t] = o.cut_q[t];
+    }
+    return ORC_OK;
+}
 
 /* Speculative-sampling verification ([ZH] 三 stage 3 "rejection sampling", stage 4;
  * [DL] "MTP speculative decoding" items 2-3).  For row b with temperature tau_b > 0
@@ -496,107 +738,57 @@ int orc_verify_sample(const void *T, const void *Q, int dt, const int32_t *d, co
             continue;
         }
 
-        /* sampling row: accept tests at every position j < D */
+        /* sampling row: accept tests at every position j < D; the draw at the first
+         * rejection */
         int32_t a = D;
         for (int32_t j = 0; j < D && rc == ORC_OK; ++j) {
-            double Zp, Zq, mp, mq, xp, xq;
-            rc = orc_filter_weights(rowT + (size_t)j * (size_t)V * es, dt, V, tb, kb, pb, wp, inp,
-                                    &Zp, &xp, &mp);
-            if (rc == ORC_OK && Q)
-                rc = orc_filter_weights(rowQ + (size_t)j * (size_t)V * es, dt, V, tb, kb, pb, wq,
-                                        inq, &Zq, &xq, &mq);
-            if (rc != ORC_OK)
-                break;
-            int32_t dj = d[b * D + j];
-            int valid = dj >= 0 && (int64_t)dj < V;
-            if (!Q) { /* one-hot draft: q_j = 1 at d_j, 0 elsewhere */
-                for (int64_t i = 0; i < V; ++i) {
-                    wq[i] = 0.0;
-                    inq[i] = 0;
-                }
-                if (valid) {
-                    wq[dj] = 1.0;
-                    inq[dj] = 1;
-                }
-                Zq = 1.0;
-                xq = 0.0;
-                mq = INFINITY;
-            }
-            double pt = valid ? wp[dj] / Zp : 0.0;
-            double pd = valid ? wq[dj] / Zq : 0.0;
-            if (p_target)
-                p_target[b * D + j] = pt;
-            if (p_draft)
-                p_draft[b * D + j] = pd;
             double ua, us;
             orc_uniforms(seed, (uint64_t)(row0 + b), (uint32_t)j, &ua, &us);
-            int accept;
-            if (!valid || !inp[dj]) {
-                accept = 0;
-            } else if (!inq[dj]) {
-                accept = 1;
-            } else {
-                /* p/q written with both row maxima factored out, so that it does not
-                 * underflow when both probabilities are tiny; a row of all -inf is a
-                 * point mass, whose probability is exact */
-                double ratio;
-                if (!Q || xp == -INFINITY || xq == -INFINITY) {
-                    ratio = pt / pd;
-                } else {
-                    double xt = logit_at(rowT + (size_t)j * (size_t)V * es, dt, dj);
-                    double xd = logit_at(rowQ + (size_t)j * (size_t)V * es, dt, dj);
-                    ratio = exp(((xt - xp) - (xd - xq)) / tb) * (Zq / Zp);
-                }
-                accept = ua <= ratio;
-                if (mg)
-                    mg[j * 4 + 0] = fabs(ua - ratio);
-            }
+            orc_unit_result o;
+            rc = orc_unit(rowT + (size_t)j * (size_t)V * es,
+                          rowQ ? rowQ + (size_t)j * (size_t)V * es : NULL, dt, V, d[b * D + j],
+                          tb, kb, pb, ua, us, 0, a == D, -1, -1, 0.0, wp, wq, wr, inp, inq, NULL,
+                          &o);
+            if (rc != ORC_OK)
+                break;
+            if (p_target)
+                p_target[b * D + j] = o.pt;
+            if (p_draft)
+                p_draft[b * D + j] = o.pd;
             if (mg) {
-                mg[j * 4 + 1] = mp;
-                mg[j * 4 + 2] = mq;
+                mg[j * 4 + 0] = o.acc_margin;
+                mg[j * 4 + 1] = o.mp_t;
+                mg[j * 4 + 2] = o.mp_q;
             }
-            if (!accept && a == D) {
+            if (!o.accept && a == D) {
                 a = j;
-                /* residual draw at the first rejection */
-                double R = 0.0;
-                for (int64_t i = 0; i < V; ++i) {
-                    double r = wp[i] / Zp - wq[i] / Zq;
-                    wr[i] = r > 0.0 ? r : 0.0;
-                    R += wr[i];
-                }
-                double dm;
-                int64_t tok;
-                if (R > 0.0)
-                    tok = orc_inverse_cdf(wr, V, us, &dm);
-                else
-                    tok = orc_inverse_cdf(wp, V, us, &dm);
                 if (mg)
-                    mg[j * 4 + 3] = dm;
+                    mg[j * 4 + 3] = o.cdf_margin;
                 for (int32_t t = 0; t <= D; ++t)
                     out[b * (D + 1) + t] = -1;
                 for (int32_t t = 0; t < a; ++t)
                     out[b * (D + 1) + t] = d[b * D + t];
-                out[b * (D + 1) + a] = (int32_t)tok;
+                out[b * (D + 1) + a] = (int32_t)o.token;
                 num_accepted[b] = a;
             }
         }
         if (rc != ORC_OK)
             break;
         if (a == D) { /* every draft held: bonus token from position D */
-            double Zp, mp, xp, ua, us, dm;
-            rc = orc_filter_weights(rowT + (size_t)D * (size_t)V * es, dt, V, tb, kb, pb, wp, inp,
-                                    &Zp, &xp, &mp);
+            double ua, us;
+            orc_uniforms(seed, (uint64_t)(row0 + b), (uint32_t)D, &ua, &us);
+            orc_unit_result o;
+            rc = orc_unit(rowT + (size_t)D * (size_t)V * es, NULL, dt, V, -1, tb, kb, pb, ua, us,
+                          1, 1, -1, -1, 0.0, wp, wq, wr, inp, inq, NULL, &o);
             if (rc != ORC_OK)
                 break;
-            orc_uniforms(seed, (uint64_t)(row0 + b), (uint32_t)D, &ua, &us);
-            int64_t tok = orc_inverse_cdf(wp, V, us, &dm);
             if (mg) {
-                mg[D * 4 + 1] = mp;
-                mg[D * 4 + 3] = dm;
+                mg[D * 4 + 1] = o.mp_t;
+                mg[D * 4 + 3] = o.cdf_margin;
             }
             for (int32_t t = 0; t < D; ++t)
                 out[b * (D + 1) + t] = d[b * D + t];
-            out[b * (D + 1) + D] = (int32_t)tok;
+            out[b * (D + 1) + D] = (int32_t)o.token;
             num_accepted[b] = D;
         }
     }

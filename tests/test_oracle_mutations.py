@@ -14,7 +14,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # (name, text in oracle/mtpspec_oracle.c, the planted mistake)
 MUTATIONS = [
-    ("top-p boundary not strict", "if (S < p) {", "if (S <= p) {"),
+    ("top-p boundary not strict", "int keep = S < p;", "int keep = S <= p;"),
     ("hidden half first in the concatenation",
      "orc_rmsnorm_bf16(e + t * H, we, H, eps, x);\n        orc_rmsnorm_bf16(h + t * H, wh, H, eps, x + H);",
      "orc_rmsnorm_bf16(h + t * H, wh, H, eps, x);\n        orc_rmsnorm_bf16(e + t * H, we, H, eps, x + H);"),
@@ -24,8 +24,8 @@ MUTATIONS = [
     ("top-k threshold off by one", "theta = s[k - 1].v;", "theta = s[k].v;"),
     ("Philox round word", "uint32_t n0 = hi1 ^ c1 ^ k0;", "uint32_t n0 = lo1 ^ c1 ^ k0;"),
     ("bonus drawn at position D-1",
-     "rc = orc_filter_weights(rowT + (size_t)D * (size_t)V * es, dt, V, tb, kb, pb, wp, inp,",
-     "rc = orc_filter_weights(rowT + (size_t)(D - 1) * (size_t)V * es, dt, V, tb, kb, pb, wp, inp,"),
+     "rc = orc_unit(rowT + (size_t)D * (size_t)V * es, NULL,",
+     "rc = orc_unit(rowT + (size_t)(D - 1) * (size_t)V * es, NULL,"),
     ("RMSNorm of the sum, not the mean", "double r = 1.0 / sqrt(ss / (double)H + eps);",
      "double r = 1.0 / sqrt(ss + eps);"),
     ("temperature dropped", "double wi = exp((s[kept].v - m) / tau);",
@@ -37,8 +37,8 @@ MUTATIONS = [
     ("normalised activations not rounded to bf16",
      "out[i] = bf16_bits_to_double(orc_double_to_bf16(y));", "out[i] = y;"),
     ("draft outside q's support not accepted", "} else if (!inq[dj]) {", "} else if (0) {"),
-    ("rejection draws from p, not the residual", "tok = orc_inverse_cdf(wr, V, us, &dm);",
-     "tok = orc_inverse_cdf(wp, V, us, &dm);"),
+    ("rejection draws from p, not the residual", "tok = orc_inverse_cdf_nb(wr, V, us, &dm, o->nb);",
+     "tok = orc_inverse_cdf_nb(wp, V, us, &dm, o->nb);"),
     ("inverse CDF from the top id",
      "for (int64_t i = 0; i < V; ++i) {\n        double prev = c;",
      "for (int64_t i = V - 1; i >= 0; --i) {\n        double prev = c;"),
@@ -60,6 +60,13 @@ MUTATIONS = [
     ("position-0 mask at every step", "positions[t] + k == 0", "positions[t] == 0"),
     ("a draft step's output not passed on as the next hidden state",
      "            h[i] = orc_double_to_bf16(y[i]);", "            (void)y[i];"),
+    ("top-p alternatives: the upper end of the window on the wrong side",
+     "if (S < p + delta)\n                ghi = gi;", "if (S < p - delta)\n                ghi = gi;"),
+    ("top-p alternatives: a forced cut ignored", "keep = gi <= force_groups;", "keep = keep;"),
+    ("draw neighbours: the next id skips one",
+     "for (int64_t i = tok + 1; i < V; ++i)", "for (int64_t i = tok + 2; i < V; ++i)"),
+    ("draw margins: the distances swapped", "lo = a;\n            hi = b;",
+     "lo = b;\n            hi = a;"),
 ]
 
 

@@ -1,16 +1,23 @@
 """spec_verify_sample_static: sampling verification for callers that cannot allocate device
 memory (a decode loop whose device memory belongs entirely to another allocator, or one
 that must never risk the synchronisation an allocation can cause).  It keeps its scratch
-in a fixed array inside the library, so this test passes no workspace.  Its results must
-equal those of spec_verify_sample with a caller workspace, on two calls in a row with
-different inputs (the second call must not see the first call's leftovers).  This file is
-collected last so that a run stopping at its first failure has already run the rest."""
+in a fixed array inside the library, so this test passes no workspace.
+
+Its results must equal those of spec_verify_sample with a caller workspace, and pass the
+oracle's parity rule, on two calls in a row with different inputs (the second call must
+not see the first call's leftovers).  A call leaves the device's free memory and torch's
+allocator untouched.  At the largest batch the array holds, rows near its end are checked
+against the oracle.  This file is collected last so that a run stopping at its first
+failure has already run the rest."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import verify_spec_greedy_gb300 as lib
 from verify_spec_greedy_gb300.inputs import WORKLOADS, Workload, make_verify_inputs
+
+from sample_parity import check
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -31,33 +38,65 @@ def _outputs(B, D):
             torch.zeros(1, dtype=torch.int32, device=DEV))
 
 
+def _args(x):
+    B, D = x["d"].shape
+    return (_dev(x["T"]), _dev(x["Q"]), _dev(x["d"]), _dev(x["tau"]), _dev(x.get("top_k")),
+            _dev(x.get("top_p")), x["seed"]), _outputs(B, D)
+
+
 def _run(x, static):
     B, D = x["d"].shape
-    T, Q = _dev(x["T"]), _dev(x["Q"])
-    out, na, pt, pd, st = _outputs(B, D)
-    args = (T, Q, _dev(x["d"]), _dev(x["tau"]), _dev(x["top_k"]), _dev(x["top_p"]), x["seed"],
-            out, na, pt, pd)
+    ins, (out, na, pt, pd, st) = _args(x)
     if static:
-        lib.spec_verify_sample_static(*args, status=st)
+        lib.spec_verify_sample_static(*ins, out, na, pt, pd, status=st)
     else:
-        ws = torch.empty(lib.spec_verify_workspace_bytes(B, D, T.shape[-1]), dtype=torch.uint8,
-                         device=DEV)
-        lib.spec_verify_sample(*args, workspace=ws, status=st)
+        ws = torch.empty(lib.spec_verify_workspace_bytes(B, D, ins[0].shape[-1]),
+                         dtype=torch.uint8, device=DEV)
+        lib.spec_verify_sample(*ins, out, na, pt, pd, workspace=ws, status=st)
     torch.cuda.synchronize()
     return [t.cpu().numpy() for t in (out, na, pt, pd, st)]
 
 
-def test_matches_workspace_entry_point_on_two_calls():
+def _as_dict(res):
+    return dict(out=res[0], num_accepted=res[1], p_target=res[2], p_draft=res[3],
+                status=int(res[4][0]))
+
+
+def _oracle(x, rows=None):
+    return oracle.verify_sample_rows(x["T"], x["Q"], x["d"], x["tau"], x.get("top_k"),
+                                     x.get("top_p"), x["seed"], rows=rows)
+
+
+def test_matches_workspace_entry_point_and_oracle_on_two_calls():
     first = make_verify_inputs(WORKLOADS["sample_b8_d3_v152k"])
     second = make_verify_inputs(Workload(
         name="second", B=40, D=2, V=30011, H=8, tau_range=(0.5, 1.2), greedy_frac=0.25,
         top_k=40, top_p=0.9, seed=21, philox_seed=22))
-    for x in (first, second):
+    for label, x in (("first call", first), ("second call", second)):
         got = _run(x, static=True)
         want = _run(x, static=False)
         for g, w in zip(got, want):
             np.testing.assert_array_equal(g, w)   # same kernels, deterministic: exact
-        assert (got[1] >= 0).all()
+        assert got[4][0] == 0
+        check(_as_dict(got), _oracle(x), x, label=f"static {label}")
+
+
+def test_a_call_allocates_nothing():
+    x = make_verify_inputs(Workload(name="alloc", B=24, D=3, V=20011, H=8, tau=0.8, top_p=0.9,
+                                    seed=5, philox_seed=5))
+    ins, (out, na, pt, pd, st) = _args(x)
+    lib.spec_verify_sample_static(*ins, out, na, pt, pd, status=st)  # set-up on this device
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    stats0 = torch.cuda.memory_stats()
+    for _ in range(3):
+        lib.spec_verify_sample_static(*ins, out, na, pt, pd, status=st)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    stats1 = torch.cuda.memory_stats()
+    assert free1 == free0
+    for key in ("allocation.all.allocated", "segment.all.allocated", "allocated_bytes.all.current"):
+        assert stats1.get(key, 0) == stats0.get(key, 0), key
 
 
 def test_rejects_batches_beyond_the_fixed_scratch():
@@ -71,9 +110,13 @@ def test_rejects_batches_beyond_the_fixed_scratch():
     with pytest.raises(lib.MtpSpecError) as e:
         lib.spec_verify_sample_static(T, Q, d, tau, None, None, 0, out, na, pt, pd, st)
     assert e.value.code == -3
-    # one row fewer fits
-    B = 16384
-    res = _run(dict(T=np.zeros((B, D + 1, V), np.float32), Q=np.zeros((B, D, V), np.float32),
-                    d=np.zeros((B, D), np.int32), tau=np.ones(B, np.float32), top_k=None,
-                    top_p=None, seed=0), static=True)
-    assert (res[1] == D).all()  # uniform p == q: every draft is kept
+    # one row fewer fits: random rows fill every record of the array; rows at its end and a
+    # seeded sample of the rest match the oracle
+    x = make_verify_inputs(Workload(name="full", B=16384, D=3, V=64, H=8, tau_range=(0.5, 1.2),
+                                    top_k=20, top_p=0.9, t_std=2.0, q_noise=1.0, seed=3,
+                                    philox_seed=4))
+    got = _as_dict(_run(x, static=True))
+    assert got["status"] == 0
+    rows = sorted(set(range(16384 - 64, 16384)) |
+                  set(np.random.default_rng(0).choice(16384, 64, replace=False).tolist()))
+    check(got, _oracle(x, rows=rows), x, rows=rows, label="static, 65536 units")

@@ -2063,15 +2063,36 @@ static std::mutex g_scratch_mu;
 static void *g_scratch_ptr[64] = {nullptr};
 
 cudaError_t run_verify_sample_static(VerifySampleArgs a, cudaStream_t stream) {
+    // The array's address is looked up for the device the work runs on: the stream's
+    // device (made current by the entry point before this call), or, for the legacy
+    // default stream, the current device.  A stream being captured cannot be asked for its
+    // device without invalidating the capture, so then the current device is taken to be
+    // the stream's (the header states this rule), and its address must already be known.
     int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaSuccess;
+    if (stream != nullptr) {
+        e = cudaStreamIsCapturing(stream, &cs);
+        if (e != cudaSuccess) return e;
+    }
+    if (stream != nullptr && cs == cudaStreamCaptureStatusNone) {
+        e = cudaStreamGetDevice(stream, &dev);
+        if (e != cudaSuccess) return e;
+        int cur = -1;
+        e = cudaGetDevice(&cur);
+        if (e != cudaSuccess) return e;
+        if (cur != dev) return cudaErrorInvalidDevice;  // the set-up needs the device current
+    } else {
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+    }
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     void *ptr = nullptr;
     {
         // once per device, with that device current: the device address of the array
         std::lock_guard<std::mutex> lock(g_scratch_mu);
         if (!g_scratch_ptr[dev]) {
+            if (cs != cudaStreamCaptureStatusNone) return cudaErrorStreamCaptureUnsupported;
             e = cudaGetSymbolAddress(&ptr, g_verify_scratch);
             if (e != cudaSuccess) return e;
             g_scratch_ptr[dev] = ptr;
