@@ -441,6 +441,11 @@ def run_gpu(args, rank, world, dist):
     return res, x, di, w
 
 
+def _current_device():
+    import torch
+    return torch.device("cuda", torch.cuda.current_device())
+
+
 def measure_per_config(dev, cached=None, graph_calls=20, reps=15):
     """Every workload's verify and draft-input calls, timed in this run: each call alone
     after an L2 flush (a write of twice the L2; median of `reps` launches), the verify call
@@ -893,9 +898,7 @@ def main():
     rank, world, dist = dist_init(args.gpus)
     res, x, di, w = run_gpu(args, rank, world, dist)
     if rank == 0 and not args.no_per_config and not args.batch:
-        import torch
-        res["per_config"] = measure_per_config(torch.device("cuda", torch.cuda.current_device()),
-                                               cached={w.name: (x, di)})
+        res["per_config"] = measure_per_config(_current_device(), cached={w.name: (x, di)})
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             v, cores, sample, dt = oracle_sample(x, di, w, rows=x["B"], min_seconds=10.0)

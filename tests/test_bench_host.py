@@ -110,8 +110,11 @@ def test_main_adds_the_cpu_baseline_after_the_gpu_step(monkeypatch, capsys):
     di = make_draft_input(w)
     monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", w.name])
     monkeypatch.setattr(bench, "run_gpu", lambda args, rank, world, dist: ({"metric": "m"}, x, di, w))
+    monkeypatch.setattr(bench, "measure_per_config", lambda dev, cached=None: {"stub": {}})
+    monkeypatch.setattr(bench, "_current_device", lambda: None)
     assert bench.main() == 0
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["per_config"] == {"stub": {}}
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["seconds"] >= 10.0
     assert cb["single_thread"]["value"] > 0 and "cpu_model" in cb
