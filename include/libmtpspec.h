@@ -268,9 +268,16 @@ int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draf
  *   workspace      >= spec_verify_workspace_bytes(B, D, V) bytes, 256-byte aligned;
  *                  no initial contents are needed
  *   status         int32 [1] or NULL
- *   B >= 0, 1 <= D <= 64, 1 <= V <= 407,552 (fp32) or 815,104 (bf16), or with a one-hot
- *   draft 652,288 (fp32) or 1,304,576 (bf16): a CTA of a cluster of at most 16 holds its
- *   slices of the staged rows in shared memory; a larger V returns MTPSPEC_ERR_SHAPE.
+ *   B >= 0, 1 <= D <= 64, 1 <= V <= 2,097,152 (fp32) or 4,194,304 (bf16); a larger V
+ *   returns MTPSPEC_ERR_SHAPE.
+ *   Two verifiers compute these results.  Up to V = 407,552 (fp32) or 815,104 (bf16) with
+ *   draft logits, 652,288 or 1,304,576 with a one-hot draft, a cluster of at most 16 CTAs
+ *   stages a unit's rows in shared memory and verifies the unit alone.  Past those limits
+ *   (or with the environment variable MTPSPEC_VERIFY_IMPL=chunks) the chunked verifier
+ *   cuts each unit's rows into up to 256 chunks of 32 KB of logits, spread over the CTAs
+ *   resident on the GPU, which combine their chunks' statistics through the workspace.
+ *   Both follow the rule above; the outputs of one verifier are deterministic, those of
+ *   the two agree except where a decision sits within rounding of its boundary.
  */
 int spec_verify_sample(const void *target_logits, const void *draft_logits, int dtype,
                        const int32_t *draft_ids, const float *temperature, const int32_t *top_k,
@@ -281,7 +288,11 @@ int spec_verify_sample(const void *target_logits, const void *draft_logits, int 
 
 /* Bytes of device workspace spec_verify_sample needs for (B, D, V); 0 for B == 0 or
  * for arguments spec_verify_sample rejects whatever the logit type (V above the bf16
- * limit included). */
+ * limit included).  Up to the cluster limit for fp32 with draft logits (V <= 407,552)
+ * this is 16 bytes per unit plus 4 per row; beyond it, or with MTPSPEC_VERIFY_IMPL=chunks
+ * set when both calls are made, it adds the chunked verifier's coordination slots: up
+ * to 128 slots, each about 80 KB plus 12 bytes per nucleus entry (V / 3 entries, at
+ * least 8,192 and at most 65,536). */
 size_t spec_verify_workspace_bytes(int64_t B, int32_t D, int64_t V);
 
 /*

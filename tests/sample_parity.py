@@ -51,12 +51,54 @@ def _row_params(x, b):
     return tau, k, p
 
 
-def _alternatives(t_row, q_row, d, tau, k, p, ua, us):
-    """(gt, gq, result) for every top-p cut pair within DELTA, the rule's first."""
+def _match_cut(fn, lo, hi, want):
+    """Cut counts g in [lo, hi] whose probability fn(g) matches want: fn is 0 below the group
+    of the draft token and decreasing from it, so a bisection finds the group's first cut
+    and another the matching value; returns up to three candidates around the match."""
+    if hi - lo <= 4:
+        return [g for g in range(lo, hi + 1) if _close(want, fn(g))]
+    if want == 0.0:
+        return [lo] if _close(0.0, fn(lo)) else []
+    a, b = lo, hi   # first cut keeping the draft token
+    if fn(b) == 0.0:
+        return []
+    while a < b:
+        m = (a + b) // 2
+        if fn(m) > 0.0:
+            b = m
+        else:
+            a = m + 1
+    a, b = a, hi    # decreasing from here: the last cut whose value is >= want
+    while a < b:
+        m = (a + b + 1) // 2
+        if fn(m) >= want * (1 - P_RTOL):
+            a = m
+        else:
+            b = m - 1
+    return [g for g in (a - 1, a, a + 1) if lo <= g <= hi and _close(want, fn(g))]
+
+
+def _alternatives(t_row, q_row, d, tau, k, p, ua, us, gpt=None, gpd=None):
+    """(gt, gq, result) for the top-p cuts within DELTA, the rule's first; when the window
+    holds many cuts (p near 1), only those whose probabilities match the GPU's."""
     base = oracle.verify_unit(t_row, q_row, d, tau, k, p, ua, us, draw=False, delta=DELTA)
-    out = [(base["cut_t"][0], base["cut_q"][0] if q_row is not None else -1, base)]
-    gts = range(base["cut_t"][1], base["cut_t"][2] + 1)
-    gqs = range(base["cut_q"][1], base["cut_q"][2] + 1) if q_row is not None else [-1]
+    rule_t = base["cut_t"][0]
+    rule_q = base["cut_q"][0] if q_row is not None else -1
+    out = [(rule_t, rule_q, base)]
+    gts = list(range(base["cut_t"][1], base["cut_t"][2] + 1))
+    gqs = list(range(base["cut_q"][1], base["cut_q"][2] + 1)) if q_row is not None else [-1]
+    if gpt is not None and (len(gts) > 5 or len(gqs) > 5):
+        cache = {}
+
+        def unit(gt, gq):
+            if (gt, gq) not in cache:
+                cache[(gt, gq)] = oracle.verify_unit(t_row, q_row, d, tau, k, p, ua, us,
+                                                     draw=False, gt=gt, gq=gq)
+            return cache[(gt, gq)]
+        if len(gts) > 5:
+            gts = _match_cut(lambda g: unit(g, rule_q)["pt"], gts[0], gts[-1], float(gpt))
+        if len(gqs) > 5 and q_row is not None:
+            gqs = _match_cut(lambda g: unit(rule_t, g)["pd"], gqs[0], gqs[-1], float(gpd))
     for gt in gts:
         for gq in gqs:
             if gt == out[0][0] and gq == out[0][1]:
@@ -88,7 +130,8 @@ def _check_row(gout, gna, gpt, gpd, x, b, one_hot):
     matched = []
     for j in range(D):
         ua, us = oracle.uniforms(seed, b, j)
-        alts = _alternatives(T[j], None if Q is None else Q[j], int(d[j]), tau, k, p, ua, us)
+        alts = _alternatives(T[j], None if Q is None else Q[j], int(d[j]), tau, k, p, ua, us,
+                             gpt[j], gpd[j])
         m = [a for a in alts if _close(gpt[j], a[2]["pt"]) and _close(gpd[j], a[2]["pd"])]
         if not m:
             return (f"position {j}: p_target {gpt[j]:.9g} / p_draft {gpd[j]:.9g} match no top-p "
@@ -127,8 +170,13 @@ def _check_row(gout, gna, gpt, gpd, x, b, one_hot):
         base = oracle.verify_unit(T[D], None, -1, tau, k, p, ua, us, bonus=True, delta=DELTA)
         exact_tok = base["token"]
         toks = _allowed_tokens(base)
-        for gt in range(base["cut_t"][1], base["cut_t"][2] + 1):
-            if gt != base["cut_t"][0]:
+        lo_, hi_ = base["cut_t"][1], base["cut_t"][2]
+        # the bonus has no probability to match: every cut of a narrow window, else the
+        # window's ends and the rule's neighbours
+        cuts = range(lo_, hi_ + 1) if hi_ - lo_ <= 8 else sorted(
+            {lo_, lo_ + 1, hi_ - 1, hi_, base["cut_t"][0] - 1, base["cut_t"][0] + 1})
+        for gt in cuts:
+            if gt != base["cut_t"][0] and lo_ <= gt <= hi_:
                 toks |= _allowed_tokens(oracle.verify_unit(T[D], None, -1, tau, k, p, ua, us,
                                                            bonus=True, gt=gt))
     tok = int(gout[a])

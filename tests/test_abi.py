@@ -67,20 +67,24 @@ def test_host_side_validation(so):
 
 
 def test_sampling_vocabulary_limit(so):
-    # the staged rows' slices (target and draft; the target alone for a one-hot draft) must
-    # fit a CTA's shared memory at 16 CTAs per cluster; an empty batch (B = 0) passes every
-    # check that does not touch device memory
+    # a cluster stages V up to 407,552 (fp32) or 815,104 (bf16) with draft logits, 652,288
+    # or 1,304,576 one-hot; beyond that the chunked verifier takes V up to 256 chunks of
+    # 32 KB of logits (2,097,152 fp32, 4,194,304 bf16) in either mode.  An empty batch
+    # (B = 0) passes every check that does not touch device memory
     nul, draft = None, C.c_void_p(256)
-    for dq, dtype, vmax in ((draft, 0, 407552), (draft, 1, 815104), (nul, 0, 652288),
-                            (nul, 1, 1304576)):
+    for dq, dtype, vmax in ((draft, 0, 2097152), (draft, 1, 4194304), (nul, 0, 2097152),
+                            (nul, 1, 4194304)):
         args = lambda V: (nul, dq, dtype, nul, nul, nul, nul, 0, 0, 1, V, nul, nul, nul, nul,
                           nul, 0, nul, nul)
+        assert so.spec_verify_sample(*args(407553)) == 0
         assert so.spec_verify_sample(*args(vmax)) == 0
         assert so.spec_verify_sample(*args(vmax + 1)) == -3
     # the workspace query knows neither the logit type nor the mode: it refuses what no
-    # combination accepts
-    assert so.spec_verify_workspace_bytes(1, 1, 1304576) > 0
-    assert so.spec_verify_workspace_bytes(1, 1, 1304577) == 0
+    # combination accepts, and past the cluster limits it counts the chunked verifier's
+    # coordination slots
+    assert so.spec_verify_workspace_bytes(1, 1, 4194304) > 0
+    assert so.spec_verify_workspace_bytes(1, 1, 4194305) == 0
+    assert so.spec_verify_workspace_bytes(8, 3, 407553) > so.spec_verify_workspace_bytes(8, 3, 407552)
 
 
 def test_lm_head_greedy_host_checks(so):

@@ -280,7 +280,7 @@ def test_one_hot_draft_serving_mix():
 # ---------------------------------------------------------------- limits
 
 @pytest.mark.parametrize("dtype,one_hot,V,k", [
-    ("f32", False, 407552, 0),      # the largest vocabularies the call accepts
+    ("f32", False, 407552, 0),      # the largest vocabularies a cluster stages
     ("bf16", False, 815104, 50),
     ("f32", True, 652288, 50),
     ("bf16", True, 1304576, 0),

@@ -112,8 +112,8 @@ MTPSPEC_API int spec_verify_greedy(const void *target_logits, int dtype, const i
 
 MTPSPEC_API size_t spec_verify_workspace_bytes(int64_t B, int32_t D, int64_t V) {
     if (B <= 0 || D < 1 || D > kMaxD || V < 1 || V > kMaxV || B > kMaxRows) return 0;
-    if (!mtpspec::verify_fits(V, 2, true)) return 0;  // too large for any logit type and mode
-    return mtpspec::verify_workspace_bytes(B, D);
+    if (!mtpspec::verify_sample_fits(V, 2, true)) return 0;  // too large for any type and mode
+    return mtpspec::verify_workspace_bytes(B, D, V);
 }
 
 MTPSPEC_API int spec_verify_sample(const void *target_logits, const void *draft_logits, int dtype,
@@ -125,7 +125,8 @@ MTPSPEC_API int spec_verify_sample(const void *target_logits, const void *draft_
                                    void *stream) {
     if (dtype != MTPSPEC_F32 && dtype != MTPSPEC_BF16) return MTPSPEC_ERR_DTYPE;
     if (B < 0 || D < 1 || D > kMaxD || V < 1 || V > kMaxV || B > kMaxRows) return MTPSPEC_ERR_SHAPE;
-    if (!mtpspec::verify_fits(V, elem_size(dtype), draft_logits == nullptr)) return MTPSPEC_ERR_SHAPE;
+    if (!mtpspec::verify_sample_fits(V, elem_size(dtype), draft_logits == nullptr))
+        return MTPSPEC_ERR_SHAPE;
     if (B == 0) return MTPSPEC_OK;
     if (!target_logits || !draft_ids || !temperature || !out_tokens || !num_accepted)
         return MTPSPEC_ERR_ARG;
@@ -136,7 +137,7 @@ MTPSPEC_API int spec_verify_sample(const void *target_logits, const void *draft_
         !aligned(p_draft, 4) || !aligned(status, 4))
         return MTPSPEC_ERR_ARG;
     if (!workspace || !aligned(workspace, 16) ||
-        workspace_bytes < mtpspec::verify_workspace_bytes(B, D))
+        workspace_bytes < mtpspec::verify_workspace_bytes(B, D, V))
         return MTPSPEC_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int rc = prepare_device(s);

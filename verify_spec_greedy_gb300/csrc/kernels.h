@@ -81,13 +81,26 @@ struct VerifySampleArgs {
 // two run concurrently.
 cudaError_t run_verify_greedy_rows(const VerifySampleArgs &a, cudaStream_t stream);
 
-// Bytes of per-unit results the sampling verifier keeps between its two kernels.
-size_t verify_workspace_bytes(int64_t B, int32_t D);
+// Bytes of workspace a sampling verification of these sizes needs, whichever verifier
+// run_verify_sample picks for any logit type and mode.
+size_t verify_workspace_bytes(int64_t B, int32_t D, int64_t V);
 
 // Whether one cluster's shared memory can hold a row of V logits of this element size.
 bool verify_fits(int64_t V, size_t elem_bytes, bool one_hot);
+// Whether either verifier takes V (the cluster kernel, else the chunked one).
+bool verify_sample_fits(int64_t V, size_t elem_bytes, bool one_hot);
 
 cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream);
+
+// The per-row finalize over the unit records rec [B, D + 1] (verify_sample.cu).
+cudaError_t launch_verify_finalize(const VerifyUnitRecord *rec, const VerifySampleArgs &a,
+                                   cudaStream_t stream);
+
+// The chunked verifier (verify_chunked.cu): units cut into vocabulary chunks, several CTAs
+// per SM, chunks of a unit coordinated through the workspace.
+size_t verify_chunks_workspace_bytes(int64_t B, int32_t D, int64_t V);
+bool verify_chunks_fits(int64_t V, size_t elem_bytes);
+cudaError_t run_verify_chunks(const VerifySampleArgs &a, cudaStream_t stream);
 
 // The fixed-scratch variant: per-unit records in the library's static device array
 // (a.workspace is ignored).  Units B * (D + 1) must not exceed kStaticVerifyUnits.

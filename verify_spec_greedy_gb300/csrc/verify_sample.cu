@@ -64,9 +64,12 @@
 // in every CTA of a cluster.  Every decision is computed identically in every CTA from
 // exchanged data, so all CTAs take the same sequence of exchanges.
 #include <mutex>
+#include <stdlib.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "philox.cuh"
 
 namespace mtpspec {
 namespace vs {
@@ -212,30 +215,6 @@ __device__ __forceinline__ unsigned long long fx_target_fx(float p, unsigned lon
 // a fixed-point weight sum as a weight
 __device__ __forceinline__ float fx_to_float(unsigned long long z) {
     return __fmul_rn(__ull2float_rn(z), 1.0f / FX);
-}
-
-// ---------------------------------------------------------------- Philox4x32-10
-
-// Philox4x32-10 (Salmon et al., SC'11): ten rounds of two 32x32->64 multiplications with
-// the round multipliers, half swaps and key mixing; the key advances by the two Weyl
-// increments after each round.
-__device__ __forceinline__ void philox(uint32_t c[4], uint32_t k0, uint32_t k1) {
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        const uint32_t lo0 = 0xD2511F53u * c[0], hi0 = __umulhi(0xD2511F53u, c[0]);
-        const uint32_t lo1 = 0xCD9E8D57u * c[2], hi1 = __umulhi(0xCD9E8D57u, c[2]);
-        const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
-        c[0] = n0;
-        c[1] = lo1;
-        c[2] = n2;
-        c[3] = lo0;
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
-    }
-}
-// odd multiple of 2^-24 in (0, 1), exact in fp32
-__device__ __forceinline__ float word_uniform(uint32_t w) {
-    return __uint2float_rn(2u * (w >> 9) + 1u) * 5.9604644775390625e-08f;
 }
 
 // ---------------------------------------------------------------- small helpers
@@ -1873,8 +1852,22 @@ static int verify_cmin(int64_t V, size_t es, int rows) {
 static size_t verify_records_bytes(int64_t B, int32_t D) {
     return static_cast<size_t>(B) * static_cast<size_t>(D + 1) * sizeof(vs::UnitResult);
 }
-size_t verify_workspace_bytes(int64_t B, int32_t D) {
-    return verify_records_bytes(B, D) + ((static_cast<size_t>(B) * 4 + 15) & ~static_cast<size_t>(15));
+// The chunked verifier is asked for by MTPSPEC_VERIFY_IMPL=chunks (where its limits allow).
+static bool chunks_requested() {
+    const char *s = getenv("MTPSPEC_VERIFY_IMPL");
+    return s && strcmp(s, "chunks") == 0;
+}
+
+size_t verify_workspace_bytes(int64_t B, int32_t D, int64_t V) {
+    const size_t cl = verify_records_bytes(B, D) + ((static_cast<size_t>(B) * 4 + 15) & ~static_cast<size_t>(15));
+    // V that every logit type and mode stages in a cluster: the cluster kernel's records
+    if (!chunks_requested() && verify_cmin(V, 4, 2) > 0) return cl;
+    const size_t ch = verify_chunks_workspace_bytes(B, D, V);
+    return cl > ch ? cl : ch;
+}
+
+bool verify_sample_fits(int64_t V, size_t elem_bytes, bool one_hot) {
+    return verify_cmin(V, elem_bytes, one_hot ? 1 : 2) > 0 || verify_chunks_fits(V, elem_bytes);
 }
 
 bool verify_fits(int64_t V, size_t elem_bytes, bool one_hot) {
@@ -2040,7 +2033,22 @@ static cudaError_t run_verify_sample_impl(const VerifySampleArgs &a, bool row_fl
     return e;
 }
 
+cudaError_t launch_verify_finalize(const VerifyUnitRecord *rec, const VerifySampleArgs &a,
+                                   cudaStream_t stream) {
+    vs::k_verify_finalize<<<static_cast<unsigned>((a.B + 127) / 128), 128, 0, stream>>>(
+        rec, a.draft_ids, a.B, a.D, a.out_tokens, a.num_accepted, a.p_target, a.p_draft);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
+// The cluster kernel wherever a cluster stages the unit's rows; beyond that (or when asked
+// for) the chunked verifier, whose shared memory does not grow with V.
 cudaError_t run_verify_sample(const VerifySampleArgs &a, cudaStream_t stream) {
+    const size_t es = a.dtype == MTPSPEC_F32 ? 4 : 2;
+    const bool one_hot = a.draft == nullptr;
+    if ((chunks_requested() || !verify_fits(a.V, es, one_hot)) && verify_chunks_fits(a.V, es))
+        return run_verify_chunks(a, stream);
     return run_verify_sample_impl(a, true, stream);
 }
 
