@@ -116,6 +116,15 @@ def verify_bytes(x):
     return (t_rows + q_rows) * V * es + small
 
 
+def l2_flush(buf):
+    """Evict L2: write a buffer of twice its size, then read it back.  The read writes the
+    flush's own dirty lines back to HBM before the timed region, so that the kernel timed
+    next starts on a clean L2 that holds none of its inputs (as after another kernel's
+    reads), instead of paying for a full L2 of write-backs."""
+    buf.fill_(1.0)
+    buf.sum()
+
+
 def draft_input_bytes(w):
     return 2 * w.H * 2 * w.H + 2 * w.tokens * w.H * 2 + 2 * w.H * 2 + w.tokens * w.H * 2
 
@@ -448,10 +457,11 @@ def _current_device():
 
 def measure_per_config(dev, cached=None, graph_calls=20, reps=15):
     """Every workload's verify and draft-input calls, timed in this run: each call alone
-    after an L2 flush (a write of twice the L2; median of `reps` launches), the verify call
-    of the three small workloads also as a CUDA graph of `graph_calls` back-to-back calls on
-    distinct copies of the inputs (after a flush; per-call time = replay / calls), and the
-    sampled workloads' verify once more with one-hot drafts.  Fractions are of the measured
+    after an L2 flush (`l2_flush`: a write and a read of twice the L2), replayed from a CUDA
+    graph of that one call (median of `reps` replays); the calls whose inputs fit L2 also as
+    a CUDA graph of `graph_calls` back-to-back calls on distinct copies of the inputs (after
+    a flush; per-call time = replay / calls); and the sampled workloads' verify once more
+    with one-hot drafts.  Fractions are of the measured
     peaks (HBM copy bandwidth, or bf16 tensor throughput for a contraction whose
     arithmetic intensity is above the ridge).  `cached` maps a workload name to inputs
     already made (x, di)."""
@@ -477,7 +487,7 @@ def measure_per_config(dev, cached=None, graph_calls=20, reps=15):
             fn()
         ts = []
         for _ in range(reps):
-            flush.fill_(1.0)
+            l2_flush(flush)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
@@ -485,6 +495,23 @@ def measure_per_config(dev, cached=None, graph_calls=20, reps=15):
             b.synchronize()
             ts.append(a.elapsed_time(b))
         return statistics.median(ts)
+
+    def timed_call(fn):
+        # one call captured in a CUDA graph and replayed: the device time of the call's
+        # kernels without the host's argument marshalling, which a single small call would
+        # otherwise expose (the GPU idles while the launch is prepared)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                fn()
+        stream.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        ms = timed(g.replay)
+        del g
+        return ms
 
     def roof(nbytes, ms):
         ach = nbytes / (ms / 1e3) / 1e9
@@ -517,7 +544,7 @@ def measure_per_config(dev, cached=None, graph_calls=20, reps=15):
                                        x["seed"], o, n, None, None, ws)
             vbytes = verify_bytes(x)
             entry["verify_call"] = "spec_verify_sample"
-        vms = timed(call)
+        vms = timed_call(call)
         entry["verify_us"] = round(vms * 1e3, 2)
         entry["verify_rows_per_s"] = round(B * (D + 1) / (vms / 1e3), 1)
         entry["verify_roofline"] = roof(vbytes, vms)
@@ -546,7 +573,7 @@ def measure_per_config(dev, cached=None, graph_calls=20, reps=15):
                                            "roofline": roof(vbytes, gms)}
             del graph, Ts, Qs
         if w.mode != "greedy":
-            oms = timed(lambda: call(one_hot=True))
+            oms = timed_call(lambda: call(one_hot=True))
             ob = vbytes - (B - int((x["tau"] == 0).sum())) * D * V * es
             entry["one_hot_verify"] = {"us": round(oms * 1e3, 2),
                                        "rows_per_s": round(B * (D + 1) / (oms / 1e3), 1),
@@ -557,7 +584,7 @@ def measure_per_config(dev, cached=None, graph_calls=20, reps=15):
         y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
         wsd = torch.empty(max(1, lib.mtp_draft_input_workspace_bytes(M, H)), dtype=torch.uint8,
                           device=dev)
-        dms = timed(lambda: lib.mtp_draft_input(e, h, we, wh, W, y, di["eps"], wsd))
+        dms = timed_call(lambda: lib.mtp_draft_input(e, h, we, wh, W, y, di["eps"], wsd))
         dbytes = draft_input_bytes(w)
         dflop = 2.0 * M * H * 2 * H
         if dflop / dbytes > tflops * 1e12 / (hbm * 1e9):
@@ -568,6 +595,30 @@ def measure_per_config(dev, cached=None, graph_calls=20, reps=15):
             droof = roof(dbytes, dms)
         entry["draft_input"] = {"tokens": M, "us": round(dms * 1e3, 2),
                                 "tokens_per_s": round(M / (dms / 1e3), 1), "roofline": droof}
+        if droof["bound"] == "hbm" and dbytes < L2_BYTES:
+            # back-to-back calls in a CUDA graph, each on its own copy of the weight (read
+            # from HBM: the copies together exceed what one call leaves in L2 and the replay
+            # starts after a flush)
+            Ws = [W] + [W.clone() for _ in range(graph_calls - 1)]
+            ys = [torch.empty_like(y) for _ in range(graph_calls)]
+            wss = [torch.empty_like(wsd) for _ in range(graph_calls)]
+            dcalls = [lambda i=i: lib.mtp_draft_input(e, h, we, wh, Ws[i], ys[i], di["eps"], wss[i])
+                      for i in range(graph_calls)]
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                for c in dcalls:
+                    c()
+            stream.wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for c in dcalls:
+                    c()
+            gms = timed(graph.replay) / graph_calls
+            entry["draft_input"]["graph_batch"] = {
+                "calls": graph_calls, "us_per_call": round(gms * 1e3, 2),
+                "tokens_per_s": round(M / (gms / 1e3), 1), "roofline": roof(dbytes, gms)}
+            del graph, Ws
         res[name] = entry
         del T, Q
     return res
@@ -578,7 +629,7 @@ def run_sweep(args):
     spec_verify_sample), one mtp_draft_input call of its draft-token count and one
     mtp_lm_head_greedy call of one token per row, the state snapshot and fix-up, and
     mtp_draft_steps (D steps, replayed from a CUDA graph), each timed
-    alone with CUDA events after an L2 flush (a write of twice the L2), median of the
+    alone with CUDA events after an L2 flush (`l2_flush`), median of the
     launches; rows/s, tokens/s and the fraction of the roofline that bounds each."""
     import numpy as np
     import torch
@@ -603,7 +654,7 @@ def run_sweep(args):
             fn()
         ts = []
         for _ in range(n):
-            flush.fill_(1.0)
+            l2_flush(flush)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
@@ -782,7 +833,7 @@ def run_lm_head(args):
         lib.mtp_lm_head_greedy(h, W, ids, norm_w=nw, eps=1e-6, workspace=ws)
     ts = []
     for _ in range(max(1, args.steps)):
-        flush.fill_(1.0)
+        l2_flush(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         lib.mtp_lm_head_greedy(h, W, ids, norm_w=nw, eps=1e-6, workspace=ws)
@@ -857,7 +908,7 @@ def run_graph_batch(args):
             graph.replay()
         ts = []
         for _ in range(10):
-            flush.fill_(1.0)
+            l2_flush(flush)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             graph.replay()

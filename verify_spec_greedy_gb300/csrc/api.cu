@@ -185,7 +185,6 @@ MTPSPEC_API int mtp_draft_input(const void *emb_next, const void *hidden, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int rc = prepare_device(s);
     if (rc != MTPSPEC_OK) return rc;
-    if (need > 0 && cudaMemsetAsync(workspace, 0, 256, s) != cudaSuccess) return MTPSPEC_ERR_CUDA;
     mtpspec::DraftInputArgs a;
     a.e = emb_next;
     a.h = hidden;

@@ -59,10 +59,6 @@ cudaError_t run_draft_steps(const DraftStepsArgs &a, cudaStream_t stream) {
     uint16_t *ping[2] = {reinterpret_cast<uint16_t *>(ws + mh), reinterpret_cast<uint16_t *>(ws + 2 * mh)};
     void *di_ws = ws + 3 * mh;
     void *lm_ws = ws + 3 * mh + ds_di(a.M, a.H);
-    if (draft_input_workspace_bytes(a.M, a.H) > 0) {
-        cudaError_t e0 = cudaMemsetAsync(di_ws, 0, 256, stream);
-        if (e0 != cudaSuccess) return e0;
-    }
     const int32_t *ids_in = a.next_ids;
     int64_t ids_stride = 1;
     const void *h_in = a.hidden;

@@ -124,11 +124,15 @@ bool draft_input_uses_gemv(int64_t M, int64_t H);
 size_t draft_input_workspace_bytes(int64_t M, int64_t H);
 cudaError_t run_draft_input(const DraftInputArgs &a, cudaStream_t stream);
 
-// Tensor-core GEMM Y[Mt, H] = B[Mt, K] @ A[H, K]^T (bf16, fp32 accumulate) and its
-// workspace (a flag word and split-K partial sums).
+// Tensor-core GEMM Y[Mt, H] = B[Mt, K] @ A[H, K]^T (bf16, fp32 accumulate, K = 2H) and its
+// workspace (a flag word, then split-K partial sums).  The first gemm_zero_bytes(Mt, H)
+// bytes of the workspace must be zeroed before the launch; with pdl the GEMM starts as the
+// programmatic dependent of the kernel launched just before it on the stream (its weight
+// loads overlap that kernel) and reads B only once that kernel has completed.
 size_t gemm_workspace_bytes(int64_t Mt, int64_t H);
+size_t gemm_zero_bytes(int64_t Mt, int64_t H);
 cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, int64_t Mt,
-                             int64_t K, void *workspace, cudaStream_t stream);
+                             int64_t K, void *workspace, bool pdl, cudaStream_t stream);
 
 }  // namespace mtpspec
 

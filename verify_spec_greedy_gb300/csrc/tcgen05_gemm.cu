@@ -9,8 +9,12 @@
 // mbarriers; one thread of the MMA warp issues tcgen05.mma (kind::f16, bf16 inputs, fp32
 // accumulator in tensor memory) and releases each stage with tcgen05.commit; four epilogue
 // warps read the accumulator with tcgen05.ld and store bf16 (or fp32 partial sums when the
-// K range is split across CTAs, reduced by a second kernel).  Every mbarrier wait is
-// bounded; a wait that gives up sets a flag word in the workspace and the CTA drains out.
+// K range is split across CTAs, reduced by a second kernel).  Launched as the programmatic
+// dependent of the kernel that writes the activations, the producer loads the weight tiles
+// of the first stages, then waits for that kernel, then loads the activation tiles, so the
+// weight stream starts while the activations are being written.  Every mbarrier wait is
+// bounded; a wait that gives up sets a flag word in the workspace, and the CTA lets its
+// copies and MMAs in flight complete before it leaves.
 //
 // k_head_argmax below is the draft head's output layer with the greedy pick: the same
 // pipeline with the tokens as the 128-row operand and 256 vocabulary rows as the N side,
@@ -41,6 +45,7 @@ struct Params {
     unsigned *err;     // flag word
     int H, Mt, K;      // H: rows of A (output features, or the vocabulary)
     int kb_total, kb_per_split, splits, o_tiles;
+    int pdl;           // k_gemm: B is written by the preceding kernel on the stream
 };
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -142,6 +147,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
     __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], accb;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
+    __shared__ int n_issued, n_consumed;  // stage fills sent and consumed (for an abort)
 
     uint8_t *ring = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -158,6 +164,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
         }
         mbar_init(&accb, 1);
         abort_flag = 0;
+        n_issued = 0;
+        n_consumed = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_map(&tmA);
         prefetch_map(&tmB);
@@ -175,32 +183,41 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
     const uint32_t tmem = tmem_base;
 
     if (warp == 0 && lane == 0) {
-        // ---- producer
+        // ---- producer: the weight tiles of the first stages, then (once the activations
+        // are written) the activation tiles, then both for every later stage
+        const int pre = nkb < STAGES ? nkb : STAGES;
+        for (int i = 0; i < pre; ++i) {
+            mbar_expect_tx(&full[i], STAGE);
+            tma_load_2d(ring + i * STAGE, &tmA, (kb0 + i) * BK, o0, &full[i]);
+        }
+        if (p.pdl) pdl_wait_primary();
+        int issued = 0;
         for (int i = 0; i < nkb; ++i) {
             const int s = i % STAGES;
             const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
-            if (!mbar_wait(&empty[s], ph ^ 1u)) {
-                atomicOr(&abort_flag, 1);
-                break;
-            }
-            if (abort_flag) break;
             uint8_t *a = ring + s * STAGE;
-            uint8_t *b = a + A_BYTES;
-            mbar_expect_tx(&full[s], STAGE);
             const int kx = (kb0 + i) * BK;
-            tma_load_2d(a, &tmA, kx, o0, &full[s]);
-            tma_load_2d(b, &tmB, kx, t0, &full[s]);
+            if (i >= pre) {
+                if (!mbar_wait(&empty[s], ph ^ 1u)) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+                if (abort_flag) break;
+                mbar_expect_tx(&full[s], STAGE);
+                tma_load_2d(a, &tmA, kx, o0, &full[s]);
+            }
+            tma_load_2d(a + A_BYTES, &tmB, kx, t0, &full[s]);
+            issued = i + 1;
         }
+        n_issued = issued;
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
         constexpr uint32_t idesc = instr_desc(BM, BN);
-        bool ok = true;
         for (int i = 0; i < nkb; ++i) {
             const int s = i % STAGES;
             const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
             if (!mbar_wait(&full[s], ph)) {
                 atomicOr(&abort_flag, 1);
-                ok = false;
                 break;
             }
             tc_fence_after();
@@ -213,8 +230,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
                          (i > 0 || k > 0) ? 1u : 0u);
             }
             mma_commit(&empty[s]);
+            n_consumed = i + 1;
         }
-        (void)ok;
         mma_commit(&accb);  // arrives once every MMA issued above has completed
     } else if (warp >= 2) {
         // ---- epilogue: TMEM lanes 32*(warp % 4) .. +31 are rows of this warp
@@ -248,7 +265,15 @@ k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensor
     }
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0 && abort_flag) atomicOr(p.err, MTPSPEC_STATUS_TIMEOUT);
+    if (threadIdx.x == 0 && abort_flag) {
+        atomicOr(p.err, MTPSPEC_STATUS_TIMEOUT);
+        // let the copies still in flight land, and the MMAs issued complete, before the
+        // CTA's shared and tensor memory are released
+        for (int i = n_consumed; i < n_issued; ++i)
+            if (!mbar_wait(&full[i % STAGES], static_cast<uint32_t>(i / STAGES) & 1u)) break;
+        mbar_wait(&accb, 0);
+    }
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -556,24 +581,37 @@ size_t gemm_workspace_bytes(int64_t Mt, int64_t H) {
     const size_t part = g.splits > 1 ? static_cast<size_t>(g.splits) * Mt * H * 4 : 0;
     return 256 + part;  // flag word, then the partial sums
 }
+size_t gemm_zero_bytes(int64_t Mt, int64_t H) {
+    (void)Mt;
+    (void)H;
+    return 256;  // the flag word's block
+}
 
 template <int BN, int STAGES>
 static cudaError_t launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const tg::Params &p,
-                               const GemmPlan &g, cudaStream_t stream) {
+                               const GemmPlan &g, bool pdl, cudaStream_t stream) {
     constexpr int smem = STAGES * (tg::A_BYTES + BN * tg::BK * 2) + 1024;
     static AttrCache attr;
     cudaError_t e = ensure_attr(tg::k_gemm<BN, STAGES>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem, attr);
     if (e != cudaSuccess) return e;
-    const dim3 grid(g.o_tiles, g.t_tiles, g.splits);
-    tg::k_gemm<BN, STAGES><<<grid, tg::NTHREADS, smem, stream>>>(ma, mb, p);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g.o_tiles, g.t_tiles, g.splits);
+    cfg.blockDim = dim3(tg::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, tg::k_gemm<BN, STAGES>, ma, mb, p);
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
 
 cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, int64_t Mt,
-                             int64_t K, void *workspace, cudaStream_t stream) {
+                             int64_t K, void *workspace, bool pdl, cudaStream_t stream) {
     const GemmPlan g = plan_gemm(H, Mt, K);
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, H, K, tg::BM) || !make_map(&mb, B, Mt, K, g.BN))
@@ -588,14 +626,15 @@ cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, i
     p.kb_total = g.kb_total;
     p.kb_per_split = g.kb_per_split;
     p.splits = g.splits;
+    p.pdl = pdl ? 1 : 0;
     cudaError_t e;
     switch (g.BN) {
-    case 16: e = launch_gemm<16, 8>(ma, mb, p, g, stream); break;
-    case 32: e = launch_gemm<32, 8>(ma, mb, p, g, stream); break;
-    case 64: e = launch_gemm<64, 6>(ma, mb, p, g, stream); break;
-    case 128: e = launch_gemm<128, 5>(ma, mb, p, g, stream); break;
-    case 192: e = launch_gemm<192, 5>(ma, mb, p, g, stream); break;
-    default: e = launch_gemm<256, 4>(ma, mb, p, g, stream); break;
+    case 16: e = launch_gemm<16, 10>(ma, mb, p, g, pdl, stream); break;
+    case 32: e = launch_gemm<32, 10>(ma, mb, p, g, pdl, stream); break;
+    case 64: e = launch_gemm<64, 8>(ma, mb, p, g, pdl, stream); break;
+    case 128: e = launch_gemm<128, 6>(ma, mb, p, g, pdl, stream); break;
+    case 192: e = launch_gemm<192, 5>(ma, mb, p, g, pdl, stream); break;
+    default: e = launch_gemm<256, 4>(ma, mb, p, g, pdl, stream); break;
     }
     if (e != cudaSuccess || g.splits == 1) return e;
     const int64_t n = Mt * H;
