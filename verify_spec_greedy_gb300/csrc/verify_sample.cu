@@ -13,8 +13,8 @@
 //    [r*slice, (r+1)*slice) of both rows.  Large batches (and one-hot drafts) number the
 //    units position-major, so that a row's earlier positions are usually decided before its
 //    later ones start; a unit behind a position of its row that was already rejected skips
-//    its draw, which no output reads (a per-row flag in the workspace, agreed on by the
-//    cluster at its first exchange).
+//    its draw, which no output reads, and a bonus unit behind one skips its filters as well
+//    (a per-row flag in the workspace, agreed on by the cluster at its first exchange).
 //    Data path: bulk asynchronous copies (four chunks per row, each on its own mbarrier)
 //    bring a unit's two slices into shared memory, where every pass of the unit reads
 //    them, so every logit is read from HBM once.  While a unit works, one thread asks L2
@@ -777,7 +777,13 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         }
         __syncthreads();
 
-        if (filt) {
+        // A row's bonus unit is read only when every draft of the row is accepted.  When the
+        // cluster's agreed view of the row (exchanged at E1) already holds a rejection, the
+        // unit's filters are not computed, and its draw is skipped below.
+        uint32_t dk1 = 0xFFFFFFFFu;
+        for (uint32_t c = 0; c < C; ++c) dk1 = min(dk1, sh.e1k[ep][c]);
+        const bool dead_bonus = j == D && dk1 < static_cast<uint32_t>(D);
+        if (filt && !dead_bonus) {
             // ---- pass 2: histogram of the elements in the bins that can hold the boundary.
             // Top-k counts them; top-p adds each element's weight scaled by its bin's octave,
             // round(w * 2^(16 + o)): an exponent add, then rounding by the sum with 2^23.  Bin
