@@ -307,11 +307,11 @@ size_t spec_verify_workspace_bytes(int64_t B, int32_t D, int64_t V);
  *   Arguments, outputs and status: as spec_verify_sample.
  *   Limit: B * (D + 1) <= 65536; a larger batch returns MTPSPEC_ERR_SHAPE.
  *   Device: the scratch used is the one on the stream's device (the call makes that
- *   device current, as every entry point does).  The first call on a device looks up
- *   the array's device address with that device current; make that first call before
- *   capturing any stream into a CUDA graph.  While a stream is being captured its device
- *   cannot be queried, so the caller's current device must then be the stream's; a
- *   first call on a device made inside a capture returns MTPSPEC_ERR_CUDA.
+ *   device current, as every entry point does).  The first call on a device does the
+ *   set-up: it looks up the array's device address, with that device current.  Make
+ *   that first call before any stream capture begins.  While its stream is being
+ *   captured, the call does not ask the stream for its device; it takes the current
+ *   device, which must then be the stream's.
  *   The looked-up address is kept for the life of the process: after cudaDeviceReset
  *   (or anything else that destroys the device's primary context) this entry point
  *   must not be called again on that device.
