@@ -156,5 +156,17 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait_primary() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+// The launch attribute that makes a kernel the programmatic dependent of the previous
+// kernel on the stream (it must call pdl_wait_primary before it touches that kernel's
+// data or anything the earlier work may still use).
+inline cudaLaunchAttribute *pdl_attr() {
+    static cudaLaunchAttribute a = [] {
+        cudaLaunchAttribute x = {};
+        x.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        x.val.programmaticStreamSerializationAllowed = 1;
+        return x;
+    }();
+    return &a;
+}
 
 }  // namespace mtpspec

@@ -99,14 +99,19 @@ k_draft_gemv(const uint16_t *__restrict__ e, const uint16_t *__restrict__ h,
     const int K = 2 * H;
     const int r0 = blockIdx.x * rows_per_cta;
     const int r1 = min(H, r0 + rows_per_cta);
+    pdl_launch_dependents();  // a programmatic dependent may start its own prologue
     if (threadIdx.x == 0 && r1 > r0) {
-        // the first 64 KB of this CTA's rows (contiguous) on their way to L2 during the norm
+        // the first 64 KB of this CTA's rows (contiguous) on their way to L2 during the wait
+        // for the previous kernel and the norm
         const size_t slab = static_cast<size_t>(r1 - r0) * K * 2;
         const uint32_t n = static_cast<uint32_t>(slab < 65536 ? slab : 65536);  // K * 2 % 16 == 0
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W + static_cast<size_t>(r0) * K),
                      "r"(n)
                      : "memory");
     }
+    // launched as a programmatic dependent: the tokens (and the output buffer) belong to
+    // the previous kernel on the stream until it has completed
+    pdl_wait_primary();
     for (int t = 0; t < MT; ++t) {
         rmsnorm_row<GEMV_THREADS>(e + static_cast<size_t>(t) * H, we, H, eps, xs + t * K, scratch);
         rmsnorm_row<GEMV_THREADS>(h + static_cast<size_t>(t) * H, wh, H, eps, xs + t * K + H,
@@ -166,6 +171,7 @@ k_draft_norm_reg(const uint16_t *__restrict__ e, const uint16_t *__restrict__ h,
                  int nzero) {
     __shared__ float2 scratch[8];
     pdl_launch_dependents();  // the GEMM may start its prologue and weight loads
+    pdl_wait_primary();       // the tokens and the workspace belong to the previous kernel until then
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < nzero; i += 256) zero[i] = 0u;
     const size_t t = blockIdx.x;
@@ -247,6 +253,7 @@ k_draft_norm(const uint16_t *__restrict__ e, const uint16_t *__restrict__ h,
              uint16_t *__restrict__ xn, int H, float eps, unsigned *__restrict__ zero, int nzero) {
     __shared__ float scratch[8];
     pdl_launch_dependents();  // the GEMM may start its prologue and weight loads
+    pdl_wait_primary();       // the tokens and the workspace belong to the previous kernel until then
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < nzero; i += 256) zero[i] = 0u;
     const int t = blockIdx.x >> 1, half = blockIdx.x & 1;
@@ -306,11 +313,17 @@ static cudaError_t launch_gemv(const DraftInputArgs &a, cudaStream_t stream) {
     // one CTA per SM, an equal share of the rows each (a warp per row at a time)
     const int rows = (H + 151) / 152;
     const int grid = (H + rows - 1) / rows;
-    di::k_draft_gemv<MT><<<grid, di::GEMV_THREADS, smem, stream>>>(
-        static_cast<const uint16_t *>(a.e), static_cast<const uint16_t *>(a.h),
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(di::GEMV_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = pdl_attr();
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, di::k_draft_gemv<MT>, static_cast<const uint16_t *>(a.e), static_cast<const uint16_t *>(a.h),
         static_cast<const uint16_t *>(a.we), static_cast<const uint16_t *>(a.wh),
         static_cast<const uint16_t *>(a.W), static_cast<uint16_t *>(a.y), H, a.eps, rows);
-    const cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
@@ -332,15 +345,23 @@ cudaError_t run_draft_input(const DraftInputArgs &a, cudaStream_t stream) {
     unsigned *zero = static_cast<unsigned *>(gemm_ws);
     const int nzero = static_cast<int>(gemm_zero_bytes(a.M, a.H) / 4);
     const unsigned M = static_cast<unsigned>(a.M);
+    // launched as the previous kernel's programmatic dependent (it waits before it reads)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(M, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = pdl_attr();
+    cfg.numAttrs = 1;
+    cudaError_t e;
     switch ((H / 8 + 255) / 256) {  // 16-byte vectors a thread per half
-    case 1: di::k_draft_norm_reg<1><<<M, 256, 0, stream>>>(ve, vh, we, wh, xn, H, a.eps, zero, nzero); break;
-    case 2: di::k_draft_norm_reg<2><<<M, 256, 0, stream>>>(ve, vh, we, wh, xn, H, a.eps, zero, nzero); break;
-    case 3: di::k_draft_norm_reg<3><<<M, 256, 0, stream>>>(ve, vh, we, wh, xn, H, a.eps, zero, nzero); break;
-    case 4: di::k_draft_norm_reg<4><<<M, 256, 0, stream>>>(ve, vh, we, wh, xn, H, a.eps, zero, nzero); break;
+    case 1: e = cudaLaunchKernelEx(&cfg, di::k_draft_norm_reg<1>, ve, vh, we, wh, xn, H, a.eps, zero, nzero); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, di::k_draft_norm_reg<2>, ve, vh, we, wh, xn, H, a.eps, zero, nzero); break;
+    case 3: e = cudaLaunchKernelEx(&cfg, di::k_draft_norm_reg<3>, ve, vh, we, wh, xn, H, a.eps, zero, nzero); break;
+    case 4: e = cudaLaunchKernelEx(&cfg, di::k_draft_norm_reg<4>, ve, vh, we, wh, xn, H, a.eps, zero, nzero); break;
     default:
-        di::k_draft_norm<<<2 * M, 256, 0, stream>>>(ve, vh, we, wh, xn, H, a.eps, zero, nzero);
+        cfg.gridDim = dim3(2 * M, 1, 1);
+        e = cudaLaunchKernelEx(&cfg, di::k_draft_norm, ve, vh, we, wh, xn, H, a.eps, zero, nzero);
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launches(1);
     return run_gemm_bf16_nt(a.W, xn, a.y, a.H, a.M, 2 * a.H, gemm_ws, true, stream);
