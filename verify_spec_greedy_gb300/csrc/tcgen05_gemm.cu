@@ -549,7 +549,8 @@ constexpr int kPlanSMs = 152;
 // Tile widths and K splits.  Up to 256 tokens, one token tile (the narrowest width that
 // holds them): the weight, the bulk of the bytes, is streamed once.  Beyond, the width of
 // 128, 192 or 256 whose tiles fill the SMs in the fewest waves of the least work (waves x
-// width).  Then K is split so that the grid fills one wave, keeping >= 8 K-blocks a split.
+// width).  Then K is split so that the grid fills one wave (of one CTA an SM, or two for
+// tiles up to 64 tokens wide), keeping at least 8 (or 4) K-blocks a split.
 static GemmPlan plan_gemm(int64_t H, int64_t Mt, int64_t K) {
     GemmPlan g;
     g.o_tiles = static_cast<int>((H + tg::BM - 1) / tg::BM);
@@ -569,8 +570,12 @@ static GemmPlan plan_gemm(int64_t H, int64_t Mt, int64_t K) {
     }
     g.t_tiles = static_cast<int>((Mt + g.BN - 1) / g.BN);
     const int tiles = g.o_tiles * g.t_tiles;
-    int splits = tiles >= kPlanSMs ? 1 : kPlanSMs / tiles;
-    splits = std::max(1, std::min(splits, g.kb_total / 8));
+    // token tiles up to 64 wide run two CTAs an SM (rings of 4 to 6 stages), so the weight
+    // stream spreads over twice the CTAs, with splits of at least 4 K-blocks
+    const int slots = g.BN <= 64 ? 2 * kPlanSMs : kPlanSMs;
+    const int minkb = g.BN <= 64 ? 4 : 8;
+    int splits = tiles >= slots ? 1 : slots / tiles;
+    splits = std::max(1, std::min(splits, g.kb_total / minkb));
     g.kb_per_split = (g.kb_total + splits - 1) / splits;
     g.splits = (g.kb_total + g.kb_per_split - 1) / g.kb_per_split;
     return g;
@@ -629,9 +634,9 @@ cudaError_t run_gemm_bf16_nt(const void *A, const void *B, void *Y, int64_t H, i
     p.pdl = pdl ? 1 : 0;
     cudaError_t e;
     switch (g.BN) {
-    case 16: e = launch_gemm<16, 10>(ma, mb, p, g, pdl, stream); break;
-    case 32: e = launch_gemm<32, 10>(ma, mb, p, g, pdl, stream); break;
-    case 64: e = launch_gemm<64, 8>(ma, mb, p, g, pdl, stream); break;
+    case 16: e = launch_gemm<16, 6>(ma, mb, p, g, pdl, stream); break;  // two CTAs an SM
+    case 32: e = launch_gemm<32, 5>(ma, mb, p, g, pdl, stream); break;
+    case 64: e = launch_gemm<64, 4>(ma, mb, p, g, pdl, stream); break;
     case 128: e = launch_gemm<128, 6>(ma, mb, p, g, pdl, stream); break;
     case 192: e = launch_gemm<192, 5>(ma, mb, p, g, pdl, stream); break;
     default: e = launch_gemm<256, 4>(ma, mb, p, g, pdl, stream); break;
