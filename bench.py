@@ -37,7 +37,8 @@ DEFAULT_WORKLOAD = "serve_b256_d3_v152k"
 L2_BYTES = 129 * 1024 * 1024
 PROFILE_FILE = os.path.join(ROOT, "profiles", "verify_sample_serve_b256_d3_v152k.md")
 KERNEL_SOURCES = ["verify_spec_greedy_gb300/csrc/verify_sample.cu",
-                  "verify_spec_greedy_gb300/csrc/common.cuh"]
+                  "verify_spec_greedy_gb300/csrc/common.cuh",
+                  "verify_spec_greedy_gb300/csrc/philox.cuh"]
 
 
 def parse_args():
