@@ -372,6 +372,23 @@ int mtp_state_fixup(const int32_t *num_accepted, int32_t D, const int32_t *kv_le
 /* A static, human-readable name for an mtpspec_status value. */
 const char *mtpspec_status_string(int code);
 
+/* mtpspec_selftest_wait_timeout — a diagnostic of the kernels' bounded waits (every wait on
+ * a copy, a barrier or another CTA gives up after a fixed number of polls and ORs
+ * MTPSPEC_STATUS_TIMEOUT into the status word, so that a call that cannot finish returns
+ * and leaves the context usable).  It launches one CTA that runs the wait of one kernel
+ * family on a barrier or counter that nothing completes, with `limit` polls instead of the
+ * kernels' own limit:
+ *   which 0  the cluster verifier's two mbarrier wait forms (local, and acquire at cluster
+ *            scope);
+ *   which 1  the chunked verifier's counter poll in global memory (which also raises its
+ *            abort flag);
+ *   which 2  the tcgen05 GEMM's stage wait.
+ * Each wait must give up; then MTPSPEC_STATUS_TIMEOUT is OR-ed into *status (device memory,
+ * int32 [1], not cleared by the call).  1 <= limit <= 2^20.  The pages have no counterpart;
+ * this entry point exists so that the timeout path can be tested without a fault.
+ * Returns MTPSPEC_OK, MTPSPEC_ERR_ARG or MTPSPEC_ERR_CUDA. */
+int mtpspec_selftest_wait_timeout(int which, uint32_t limit, int32_t *status, void *stream);
+
 /* Diagnostics (no counterpart in the pages): the number of kernel launches this library
  * has enqueued, on any stream and device, since it was loaded.  Thread-safe. */
 uint64_t mtpspec_launch_count(void);

@@ -38,7 +38,8 @@ def test_header_declares_the_boundary():
         "mtp_state_snapshot", "mtp_state_fixup", "mtp_draft_steps",
         "mtp_draft_steps_workspace_bytes",
         "spec_verify_greedy", "spec_verify_sample", "spec_verify_workspace_bytes",
-        "spec_verify_sample_static", "mtpspec_status_string", "mtpspec_launch_count"])
+        "spec_verify_sample_static", "mtpspec_status_string", "mtpspec_launch_count",
+        "mtpspec_selftest_wait_timeout"])
 
 
 def test_every_declared_symbol_is_exported(so):
@@ -183,3 +184,14 @@ def test_draft_steps_host_checks(so):
 
 def test_launch_count_starts_at_zero_on_the_host(so):
     assert lib.mtpspec_launch_count() >= 0
+
+
+def test_wait_selftest_host_checks(so):
+    f = so.mtpspec_selftest_wait_timeout
+    st = C.c_void_p(256)
+    assert f(3, 100, st, None) == -1        # which
+    assert f(-1, 100, st, None) == -1
+    assert f(0, 0, st, None) == -1          # limit
+    assert f(0, (1 << 20) + 1, st, None) == -1
+    assert f(0, 100, None, None) == -1      # status
+    assert f(0, 100, C.c_void_p(258), None) == -1  # misaligned

@@ -60,6 +60,7 @@ def load():
         "mtp_draft_steps_workspace_bytes": ([i64, i64, i64], sz),
         "mtpspec_status_string": ([C.c_int], C.c_char_p),
         "mtpspec_launch_count": ([], C.c_uint64),
+        "mtpspec_selftest_wait_timeout": ([C.c_int, C.c_uint32, C.c_void_p, C.c_void_p], C.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name, None)
@@ -153,6 +154,13 @@ def _call(name, *args):
 
 
 # ---------------------------------------------------------------- entry points
+
+def mtpspec_selftest_wait_timeout(which: int, limit: int, status, stream=None):
+    """Run one kernel family's bounded wait on a barrier that nothing completes (see
+    include/libmtpspec.h); MTPSPEC_STATUS_TIMEOUT is OR-ed into `status` when it gives up."""
+    _call("mtpspec_selftest_wait_timeout", int(which), int(limit),
+          _arg(status, "status", _I32, 1), _stream(stream))
+
 
 def mtp_draft_input_workspace_bytes(M: int, H: int) -> int:
     return int(load().mtp_draft_input_workspace_bytes(int(M), int(H)))

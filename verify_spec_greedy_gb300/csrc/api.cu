@@ -62,6 +62,20 @@ std::atomic<unsigned long long> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n)); }
 }  // namespace mtpspec
 
+MTPSPEC_API int mtpspec_selftest_wait_timeout(int which, uint32_t limit, int32_t *status,
+                                              void *stream) {
+    if (which < 0 || which > 2) return MTPSPEC_ERR_ARG;
+    if (limit < 1 || limit > (1u << 20)) return MTPSPEC_ERR_ARG;
+    if (!status || !aligned(status, 4)) return MTPSPEC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = prepare_device(s);
+    if (rc != MTPSPEC_OK) return rc;
+    cudaError_t e = which == 0 ? mtpspec::run_wait_selftest_clusters(limit, status, s)
+                    : which == 1 ? mtpspec::run_wait_selftest_chunks(limit, status, s)
+                                 : mtpspec::run_wait_selftest_gemm(limit, status, s);
+    return launched(e);
+}
+
 MTPSPEC_API uint64_t mtpspec_launch_count(void) {
     return static_cast<uint64_t>(mtpspec::g_launches.load());
 }

@@ -102,6 +102,13 @@ size_t verify_chunks_workspace_bytes(int64_t B, int32_t D, int64_t V);
 bool verify_chunks_fits(int64_t V, size_t elem_bytes);
 cudaError_t run_verify_chunks(const VerifySampleArgs &a, cudaStream_t stream);
 
+// Diagnostics of the bounded waits (one CTA each): the cluster verifier's two wait forms,
+// the chunked verifier's counter poll and the GEMM's stage wait, each on a barrier or counter
+// that nothing completes, with `limit` polls.
+cudaError_t run_wait_selftest_clusters(uint32_t limit, int32_t *status, cudaStream_t stream);
+cudaError_t run_wait_selftest_chunks(uint32_t limit, int32_t *status, cudaStream_t stream);
+cudaError_t run_wait_selftest_gemm(uint32_t limit, int32_t *status, cudaStream_t stream);
+
 // The fixed-scratch variant: per-unit records in the library's static device array
 // (a.workspace is ignored).  Units B * (D + 1) must not exceed kStaticVerifyUnits.
 constexpr int64_t kStaticVerifyUnits = 65536;

@@ -35,7 +35,7 @@ constexpr int BM = 128;          // output features per tile (MMA M)
 constexpr int BK = 64;           // K per stage: one 128-byte swizzle row of bf16
 constexpr int UK = 16;           // K per tcgen05.mma of kind::f16
 constexpr int NTHREADS = 192;    // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
-constexpr uint32_t WAIT_LIMIT = 1u << 25;
+constexpr uint32_t WAIT_LIMIT = 1u << 18;  // polls: ~3.8 us each when unsuccessful, ~1 s in all
 constexpr int A_BYTES = BM * BK * 2;
 
 struct Params {
@@ -62,9 +62,9 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait; false if the phase never completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t it = 0; it < WAIT_LIMIT; ++it)
+// Bounded wait; false if the phase never completed within `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit = WAIT_LIMIT) {
+    for (uint32_t it = 0; it < limit; ++it)
         if (mbar_test(bar, parity)) return true;
     return false;
 }
@@ -503,7 +503,26 @@ __global__ void k_split_reduce(const float *__restrict__ part, uint16_t *__restr
         make_uint2(o[0] | (static_cast<uint32_t>(o[1]) << 16), o[2] | (static_cast<uint32_t>(o[3]) << 16));
 }
 
+// Diagnostic of the bounded wait: a barrier of two arrivals gets one, so the wait must give
+// up after `limit` polls; then MTPSPEC_STATUS_TIMEOUT is OR-ed into the status word, as the
+// kernels do.
+__global__ void k_wait_selftest(uint32_t limit, int32_t *status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 2);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&bar)) : "memory");
+    if (!mbar_wait(&bar, 0, limit)) atomicOr(status, MTPSPEC_STATUS_TIMEOUT);
+}
+
 }  // namespace tg
+
+cudaError_t run_wait_selftest_gemm(uint32_t limit, int32_t *status, cudaStream_t stream) {
+    tg::k_wait_selftest<<<1, 32, 0, stream>>>(limit, status);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
 
 // ---------------------------------------------------------------- host side
 

@@ -254,9 +254,9 @@ __device__ __forceinline__ ChunkStat ldcg(const ChunkStat *p) {
 
 // Thread 0 waits until *p >= target.  False (after raising the abort flag and the timeout
 // status) if the wait gave up, or if the call was aborted elsewhere.
-__device__ bool wait_geq(uint32_t *p, uint32_t target, const Params &P) {
+__device__ bool wait_geq(uint32_t *p, uint32_t target, const Params &P, uint32_t limit = POLL_LIMIT) {
     // spin first: a poll is an L2 round trip already, and a sleeping warp can wake up late
-    for (uint32_t it = 0; it < POLL_LIMIT; ++it) {
+    for (uint32_t it = 0; it < limit; ++it) {
         if (ld_acq(p) >= target) return true;
         if ((it & 255u) == 255u) {
             if (ld_acq(P.hdr + 1) != 0u) return false;
@@ -266,6 +266,23 @@ __device__ bool wait_geq(uint32_t *p, uint32_t target, const Params &P) {
     atomicExch(P.hdr + 1, 1u);
     if (P.status) atomicOr(P.status, MTPSPEC_STATUS_TIMEOUT);
     return false;
+}
+
+// Diagnostic of the bounded wait: a counter that nothing raises (zeroed here, with the abort
+// flag) must make wait_geq give up after `limit` polls, raise the abort flag and OR
+// MTPSPEC_STATUS_TIMEOUT into the status word, as the kernel does.
+__device__ uint32_t g_wait_selftest[4];
+__global__ void k_wait_selftest(uint32_t limit, int32_t *status) {
+    if (threadIdx.x != 0) return;
+    g_wait_selftest[0] = 0u;  // the counter
+    g_wait_selftest[1] = 0u;  // hdr[1]: the abort flag
+    __threadfence();
+    Params P = {};
+    P.hdr = g_wait_selftest;
+    P.status = status;
+    const bool ok = wait_geq(&g_wait_selftest[0], 1u, P, limit);
+    // a wait that did not give up, or gave up without the abort flag, leaves no timeout bit
+    if (ok || ld_acq(&g_wait_selftest[1]) != 1u) atomicAnd(status, ~MTPSPEC_STATUS_TIMEOUT);
 }
 
 __device__ __forceinline__ void mbar_init1(unsigned long long *bar) {
@@ -1986,6 +2003,13 @@ extern "C" __attribute__((visibility("default"))) int mtpspec_vc_trace(void *dst
     return cudaMemcpyFromSymbol(dst, vc::g_trace, n) == cudaSuccess ? 0 : -1;
 }
 #endif
+
+cudaError_t run_wait_selftest_chunks(uint32_t limit, int32_t *status, cudaStream_t stream) {
+    vc::k_wait_selftest<<<1, 32, 0, stream>>>(limit, status);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
 
 cudaError_t run_verify_chunks(const VerifySampleArgs &a, cudaStream_t stream) {
     return a.dtype == MTPSPEC_F32 ? launch_chunks<float>(a, stream) : launch_chunks<uint16_t>(a, stream);

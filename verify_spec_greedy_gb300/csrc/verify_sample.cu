@@ -92,7 +92,10 @@ constexpr int CAPT = RSN;        // candidate slots per row in a cluster (CAPT /
                                  // as many as the histograms they share storage with
 constexpr int NCH = 4;           // bulk-copy chunks per row
 constexpr int WVEC_SHARED = 6400;  // draw: vector weights kept in the shared state's storage
-constexpr uint32_t WAIT_LIMIT = 1u << 22;
+// polls of a bounded wait: an unsuccessful mbarrier poll suspends the thread for about
+// 3.8 us (measured), so a wait gives up after about a second, far beyond any wait of a
+// working call (microseconds, a peer's phase at most)
+constexpr uint32_t WAIT_LIMIT = 1u << 18;
 constexpr float FX = 2147483648.0f;  // 2^31: fixed-point scale of weights (weights <= 1)
 
 // exchange barriers
@@ -313,16 +316,18 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long *bar, uint32_t 
         : "memory");
     return ok != 0;
 }
-// Wait for the phase of the given parity; false after WAIT_LIMIT polls.
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, uint32_t parity) {
-    for (uint32_t it = 0; it < WAIT_LIMIT; ++it)
+// Wait for the phase of the given parity; false after `limit` polls.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, uint32_t parity,
+                                                  uint32_t limit = WAIT_LIMIT) {
+    for (uint32_t it = 0; it < limit; ++it)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
 // The same with acquire semantics at cluster scope: the peers' writes released by their
 // arrivals are visible after it returns true.
-__device__ __forceinline__ bool xbar_wait_bounded(unsigned long long *bar, uint32_t parity) {
-    for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
+__device__ __forceinline__ bool xbar_wait_bounded(unsigned long long *bar, uint32_t parity,
+                                                  uint32_t limit = WAIT_LIMIT) {
+    for (uint32_t it = 0; it < limit; ++it) {
         uint32_t ok;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
@@ -1797,6 +1802,20 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     if (tid == 0 && (sh.flags & 3) && P.status) atomicOr(P.status, MTPSPEC_STATUS_TIMEOUT);
 }
 
+// Diagnostic of the bounded waits: an mbarrier of two arrivals gets one, so its phase never
+// completes; both of the kernel's wait forms must give up after `limit` polls, and then
+// MTPSPEC_STATUS_TIMEOUT is OR-ed into the status word, as the kernel does.
+__global__ void k_wait_selftest(uint32_t limit, int32_t *status) {
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 2);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_arrive(&bar);
+    const bool a = mbar_wait_bounded(&bar, 0, limit);
+    const bool x = xbar_wait_bounded(&bar, 0, limit);
+    if (!a && !x) atomicOr(status, MTPSPEC_STATUS_TIMEOUT);
+}
+
 // One thread per row: the first rejected position decides what the row emits.
 __global__ void k_verify_finalize(const UnitResult *__restrict__ res, const int32_t *__restrict__ d,
                                   int64_t B, int32_t D, int32_t *__restrict__ out,
@@ -2035,6 +2054,13 @@ static cudaError_t run_verify_sample_impl(const VerifySampleArgs &a, bool row_fl
         static_cast<const vs::UnitResult *>(a.workspace), a.draft_ids, a.B, a.D, a.out_tokens,
         a.num_accepted, a.p_target, a.p_draft);
     e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
+cudaError_t run_wait_selftest_clusters(uint32_t limit, int32_t *status, cudaStream_t stream) {
+    vs::k_wait_selftest<<<1, 32, 0, stream>>>(limit, status);
+    const cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
