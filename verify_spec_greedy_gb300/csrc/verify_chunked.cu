@@ -7,9 +7,11 @@
 //
 // A unit is one (row b, position j): the target row T[b, j] and, for j < D, the draft row
 // Q[b, j].  Each unit is cut into NC chunks of CH vocabulary ids; a work item is one chunk.
-// A persistent grid of CTAs (several per SM) claims items in order from a global counter;
-// a CTA holds one item at a time, so a unit's chunks are always held by running CTAs and
-// the waits below always end (the earliest unfinished unit can always progress).
+// A persistent grid of CTAs (several per SM, as many as are resident) claims items in
+// order from a global counter; a CTA holds one item at a time, so a unit's chunks are held
+// by running CTAs and the waits below end as long as the GPU runs at least as many of them
+// as a unit has chunks (the earliest unfinished unit can always progress); otherwise the
+// waits give up and the call reports MTPSPEC_STATUS_TIMEOUT.
 //
 // One item:
 //   stage    bulk asynchronous copies bring the chunk's target and draft logits into shared
@@ -194,26 +196,6 @@ struct Misc {
 constexpr int CCAP = 384;               // a chunk's candidates, staged in shared memory
 constexpr int SCR_BYTES = NBL * 8 + NT * 4 + CCAP * 8;   // histogram, thread maxima, candidates
 static_assert(NCMAX * NW * 16 <= ROW_BYTES, "the resolver's per-range draw sums fit a staging buffer");
-
-// ---------------------------------------------------------------- phase timestamps
-// Built with -DMTPSPEC_VC_TRACE, thread 0 of each CTA records the global timer at the end of
-// each phase of the first 65536 items (mtpspec_vc_trace copies them out); otherwise nothing.
-#ifdef MTPSPEC_VC_TRACE
-constexpr int TRACE_ITEMS = 65536, TRACE_PH = 12;
-__device__ unsigned long long g_trace[TRACE_ITEMS][TRACE_PH];
-#define VC_STAMP(item, k)                                                                \
-    do {                                                                                 \
-        if (threadIdx.x == 0 && (item) < static_cast<uint32_t>(TRACE_ITEMS)) {           \
-            unsigned long long t_;                                                       \
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                       \
-            g_trace[(item)][(k)] = t_;                                                   \
-        }                                                                                \
-    } while (0)
-#else
-#define VC_STAMP(item, k) \
-    do {                  \
-    } while (0)
-#endif
 
 // ---------------------------------------------------------------- small device helpers
 
@@ -1303,7 +1285,6 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_chunks(const Params P) {
         __syncthreads();
         const uint32_t item = ms.item;
         if (item == 0xFFFFFFFFu || static_cast<int64_t>(item) >= P.items) break;
-        VC_STAMP(item, 0);
 
         // ---- the unit
         const int64_t u = static_cast<int64_t>(item) / P.NC;
@@ -1356,7 +1337,6 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_chunks(const Params P) {
             parity[r] ^= 1u;
         }
         if (!ok && tid == 0 && P.status) atomicOr(P.status, MTPSPEC_STATUS_TIMEOUT);
-        VC_STAMP(item, 1);
         __syncthreads();
         const int nvec[2] = {(padE[0] * ES + n * ES + 15) / 16, (padE[1] * ES + n * ES + 15) / 16};
 
@@ -1470,7 +1450,6 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_chunks(const Params P) {
 
         // ---- W1
         __syncthreads();
-        VC_STAMP(item, 2);
         if (tid == 0 && alive) {
             __threadfence();
             atom_add_ar(&Z->c1, 1u);
@@ -1479,12 +1458,10 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_chunks(const Params P) {
         __syncthreads();
         alive = !ms.leave;
         if (!alive) continue;
-        VC_STAMP(item, 3);
 
         // ---- plan A (warp r plans row r)
         if (warp < nrows) plan_a(P, N, warp, ms.xref[warp], c2, kk, pp, ms.plan[warp]);
         __syncthreads();
-        VC_STAMP(item, 8);
         bool fallback = false;
         for (int r = 0; r < nrows; ++r) fallback |= ms.plan[r].fallback != 0;
         // the unit may have to draw unless an earlier position of its row is known rejected
@@ -1595,7 +1572,6 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_chunks(const Params P) {
                 __syncthreads();
             }
             // ---- W1b
-            VC_STAMP(item, 4);
             if (tid == 0) {
                 __threadfence();
                 atom_add_ar(&Z->c1b, 1u);
@@ -1603,10 +1579,8 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_chunks(const Params P) {
             }
             __syncthreads();
             if (ms.leave) continue;
-            VC_STAMP(item, 5);
             // ---- plan B (the whole CTA)
             plan_b_block(Z, nrows, kk, pp, P.V, ms);
-            VC_STAMP(item, 7);
             for (int r = 0; r < nrows; ++r) fallback |= ms.plan[r].fallback != 0;
         }
 
@@ -1740,7 +1714,6 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_chunks(const Params P) {
 
         // ---- W2: every chunk arrives; the last one resolves the unit
         __syncthreads();
-        VC_STAMP(item, 6);
         if (tid == 0) {
             __threadfence();
             const uint32_t old = atom_add_ar(&Z->c2, 1u);
@@ -1873,7 +1846,6 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_chunks(const Params P) {
 
         // ---- done with the unit: the last chunk releases the slot
         __syncthreads();
-        VC_STAMP(item, 9);
         if (tid == 0) {
             __threadfence();
             const uint32_t old = atom_add_ar(&Z->done, 1u);
@@ -1996,13 +1968,6 @@ static cudaError_t launch_chunks(const VerifySampleArgs &a, cudaStream_t stream)
     count_launches(1);
     return launch_verify_finalize(P.rec, a, stream);
 }
-
-#ifdef MTPSPEC_VC_TRACE
-extern "C" __attribute__((visibility("default"))) int mtpspec_vc_trace(void *dst, size_t bytes) {
-    const size_t n = sizeof(vc::g_trace) < bytes ? sizeof(vc::g_trace) : bytes;
-    return cudaMemcpyFromSymbol(dst, vc::g_trace, n) == cudaSuccess ? 0 : -1;
-}
-#endif
 
 cudaError_t run_wait_selftest_chunks(uint32_t limit, int32_t *status, cudaStream_t stream) {
     vc::k_wait_selftest<<<1, 32, 0, stream>>>(limit, status);
