@@ -121,6 +121,11 @@ struct UnitParams {
     float tau, pp;
     int32_t kk, d;
 };
+// The parameters of a unit beside its index (which gives b and j); sent as one 16-byte store.
+struct __align__(16) NextParams {
+    float tau, pp;
+    int32_t kk, d;
+};
 
 struct __align__(16) Shared {
     unsigned long long dbar[2][NCH];   // [row][chunk] bulk-copy barriers
@@ -182,16 +187,18 @@ struct __align__(16) Shared {
     float tzb[2];     // m * c2 * R: the bin coordinate tz = -z * R = x * (-c2 * R) + tzb
     uint32_t uwd[2];  // the unit's two Philox words (accept test, draw)
     float nmc[2];     // -m * c2: z = x * c2 + nmc
-    int32_t deg[2];   // a row of all -inf: a point mass on id 0
-    int32_t mode[2];  // 0 no filter, 1 candidates, 2 exact bisection
-    int32_t b1[2], b2[2], nbu[2];
+    int8_t deg[2];    // a row of all -inf: a point mass on id 0
+    int8_t mode[2];   // 0 no filter, 1 candidates, 2 exact bisection
+    int16_t b1[2], b2[2], nbu[2];  // bins (at most NB)
     unsigned long long tgt[2];
     int32_t flags;    // bit 0: a bulk copy timed out; bit 1: an exchange timed out
     float fpick[2];
-    // the unit after the next one (-1: none) and its parameters, found by one warp while
-    // the current unit works
-    int32_t su;
-    UnitParams sp;
+    // E1, by unit parity: the cluster's unit after the next one (-1: none) and its
+    // parameters, chosen by CTA 0 two units ahead (skipping the bonus units of rows it sees
+    // rejected) and sent with its E1 message, so that every CTA takes the same sequence; in
+    // CTA 0 the slot of the other parity holds the unit after that, chosen during this E1
+    int32_t e1su[2];
+    NextParams e1sp[2];
 };
 
 __device__ __forceinline__ float ex2(float z) {
@@ -538,23 +545,27 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         q.d = q.j < D ? P.d[q.b * D + q.j] : -1;
         return q;
     };
-    // one whole warp: the first sampled unit after unit `from` in this cluster's sequence,
-    // with its parameters, into sh.su / sh.sp.  Each lane loads a candidate's parameters, so
-    // 32 candidates cost one round of loads.
-    auto find_next = [&](int from) {
+    // one whole warp (of CTA 0): the first unit after unit `from` in this cluster's sequence
+    // that is sampled and not the bonus unit (j = D, read only when every draft of the row
+    // is accepted) of a row already seen rejected (a flag not yet set only costs that unit's
+    // work), with its parameters, into slot `slot` of e1su / e1sp.  Each lane loads a
+    // candidate's parameters, so 32 candidates cost one round of loads.
+    auto find_next = [&](int from, int slot) {
         int found = -1;
         for (int base = from + G; from >= 0 && base < U && found < 0; base += 32 * G) {
             const int cand = base + lane * G;
             UnitParams q = {0, 0, 0.0f, 1.0f, 0, -1};
             if (cand < U) q = load_params(cand);
-            const unsigned msk = __ballot_sync(0xFFFFFFFFu, cand < U && q.tau > 0.0f && q.pp > 0.0f);
+            const bool dead = P.dead && q.j == D &&
+                              *reinterpret_cast<volatile const uint32_t *>(P.dead + q.b) < static_cast<uint32_t>(D);
+            const unsigned msk = __ballot_sync(0xFFFFFFFFu, cand < U && q.tau > 0.0f && q.pp > 0.0f && !dead);
             if (msk) {
                 const int l = __ffs(msk) - 1;
                 found = __shfl_sync(0xFFFFFFFFu, cand, l);
-                if (lane == l) sh.sp = q;
+                if (lane == l) sh.e1sp[slot] = NextParams{q.tau, q.pp, q.kk, q.d};
             }
         }
-        if (lane == 0) sh.su = found;
+        if (lane == 0) sh.e1su[slot] = found;
     };
     auto row_ptr = [&](int b, int j, int r) -> const T * {
         return r == 0 ? static_cast<const T *>(P.T) + (static_cast<int64_t>(b) * (D + 1) + j) * V + lo
@@ -621,6 +632,15 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         issue(cnx.b, cnx.j, false);
         un = next_unit(u);
         if (un >= 0) nxt = load_params(un);
+    }
+    // CTA 0 holds the cluster's third unit for its first E1 message
+    if (rank == 0 && tid == 0) {
+        const int u2 = un >= 0 ? next_unit(un) : -1;
+        sh.e1su[0] = u2;
+        if (u2 >= 0) {
+            const UnitParams q = load_params(u2);
+            sh.e1sp[0] = NextParams{q.tau, q.pp, q.kk, q.d};
+        }
     }
     bool started = false;
 
@@ -729,6 +749,12 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             if (lane != static_cast<int>(rank))
                 st_peer_u32(peer_addr(smem_addr(&sh.e1k[ep][rank]), lane), sh.e1k[ep][rank]);
             if (d_here) st_peer_v2(peer_addr(smem_addr(&sh.e1d[ep]), lane), make_float2(sh.xd[0], sh.xd[1]));
+            if (rank == 0 && lane != 0) {  // the unit after the next one, and its parameters
+                const NextParams q = sh.e1sp[ep];
+                st_peer_u32(peer_addr(smem_addr(&sh.e1su[ep]), lane), static_cast<uint32_t>(sh.e1su[ep]));
+                st_peer_v4(peer_addr(smem_addr(&sh.e1sp[ep]), lane),
+                           make_float4(q.tau, q.pp, __int_as_float(q.kk), __int_as_float(q.d)));
+            }
             xarrive(&sh.xbar[XB_E1 + ep], lane);
         }
         if (warp == NW - 1) {  // work whose latency the wait hides
@@ -739,7 +765,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 sh.uwd[0] = c4[0];
                 sh.uwd[1] = c4[1];
             }
-            find_next(un);
+            if (rank == 0) find_next(sh.e1su[ep], ep ^ 1);  // sent with the next E1
         }
         xwait(XB_E1 + ep);
 
@@ -1791,8 +1817,12 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         if (draw && un >= 0) issue(nxt.b, nxt.j, true);
         u = un;
         cnx = nxt;
-        un = sh.su;  // written during this unit, before E1; rewritten only after the next set-up
-        nxt = sh.sp;
+        un = sh.e1su[ep];  // CTA 0's choice, sent with this unit's E1 (rewritten two E1s later)
+        if (un >= 0) {
+            const NextParams q = sh.e1sp[ep];
+            const int nb = unit_row(un);
+            nxt = UnitParams{nb, pmajor ? un / Bi : un - nb * (D + 1), q.tau, q.pp, q.kk, q.d};
+        }
     }
     if (!started) cluster_wait_acquire();  // a cluster with no unit still completes its start
     // no CTA leaves while a peer may still write into its shared memory or arrive on its
