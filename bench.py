@@ -331,8 +331,10 @@ def run_gpu(args, rank, world, dist):
         if timed:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
+        # as a decode loop calls it: the tokens and accepted counts, no per-position
+        # probabilities (so positions behind a row's first rejection need not be read)
         lib.spec_verify_sample(s["T"], s["Q"], s["d"], tau, top_k, top_p, x["seed"], out, na,
-                               pt, pd, ws_v, status)
+                               None, None, ws_v, status)
         if timed:
             b.record(stream)
             ev_v.append((a, b))
@@ -366,6 +368,18 @@ def run_gpu(args, rank, world, dist):
     verify_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_v)
     rows_per_step = B * (D + 1)
     value = whole_job_value(rows_per_step, args.steps, world, ms_max)
+    # the same call with p_target and p_draft requested: every draft position is computed
+    pev = []
+    for i in range(max(3, min(args.steps, 20))):
+        s_ = sets[i % copies]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        lib.spec_verify_sample(s_["T"], s_["Q"], s_["d"], tau, top_k, top_p, x["seed"], out, na,
+                               pt, pd, ws_v, status)
+        b.record(stream)
+        pev.append((a, b))
+    torch.cuda.synchronize()
+    verify_p_ms = statistics.median(a.elapsed_time(b) for a, b in pev[2:])
 
     # end to end through the C ABI with host buffers: pinned inputs copied in, results out
     host_in = {k: torch.from_numpy(np.ascontiguousarray(
@@ -374,8 +388,6 @@ def run_gpu(args, rank, world, dist):
                          W=di["W"]).items()}
     host_out = dict(out=torch.empty((B, D + 1), dtype=torch.int32).pin_memory(),
                     na=torch.empty(B, dtype=torch.int32).pin_memory(),
-                    pt=torch.empty((B, D), dtype=torch.float32).pin_memory(),
-                    pd=torch.empty((B, D), dtype=torch.float32).pin_memory(),
                     y=torch.empty((M, H), dtype=torch.bfloat16).pin_memory())
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
@@ -401,8 +413,6 @@ def run_gpu(args, rank, world, dist):
         ev_free[i % 2].record(stream)
         host_out["out"].copy_(out, non_blocking=True)
         host_out["na"].copy_(na, non_blocking=True)
-        host_out["pt"].copy_(pt, non_blocking=True)
-        host_out["pd"].copy_(pd, non_blocking=True)
         host_out["y"].copy_(y, non_blocking=True)
 
     for i in range(2):
@@ -425,12 +435,19 @@ def run_gpu(args, rank, world, dist):
     vb = verify_bytes(x)
     achieved = vb / (verify_ms / 1e3) / 1e9
     traffic = profiled_traffic(args.workload)
+    # achieved counts every unit's logits (the call's algorithmic bytes); the call skips the
+    # positions behind a row's first rejection once it knows of it, so the DRAM bytes it
+    # reads (traffic, from the committed ncu summary) are fewer: their rate is given beside
     roofline = {"bound": "hbm", "kernel": "spec_verify_sample: k_verify_rr + k_argmax_verify_rows + k_verify_finalize",
                 "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "frac_vs_nominal_8tbs": round(achieved / 8000.0, 4),
                 "algorithmic_bytes_per_launch": vb,
-                "launch_ms": round(verify_ms, 5), "traffic": traffic}
+                "launch_ms": round(verify_ms, 5), "traffic": traffic,
+                "traffic_frac": (round(traffic / (verify_ms / 1e3) / 1e9 / peak, 4)
+                                 if traffic else None),
+                "with_probabilities": {"launch_ms": round(verify_p_ms, 5),
+                                       "frac": round(vb / (verify_p_ms / 1e3) / 1e9 / peak, 4)}}
 
     res = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": max(3, args.warmup),
@@ -440,7 +457,8 @@ def run_gpu(args, rank, world, dist):
            "config": {"workload": w.name, "B": B, "D": D, "V": V, "H": H, "draft_tokens": M,
                       "greedy_rows": ng, "top_k": int(w.top_k), "top_p": float(w.top_p),
                       "logits": x["dtype"], "step": "mtp_draft_input + mtp_greedy_draft + "
-                      "spec_verify_sample", "parallelism": f"replicas x{world}",
+                      "spec_verify_sample", "verify_outputs": "out_tokens, num_accepted",
+                      "parallelism": f"replicas x{world}",
                       "l2": ("inputs larger than L2" if copies == 1 else
                              f"{copies} rotating input copies, {copies * step_bytes / 1e6:.0f} MB")},
            "clocks": clk,
@@ -549,6 +567,13 @@ def measure_per_config(dev, cached=None, graph_calls=20, reps=15):
         entry["verify_us"] = round(vms * 1e3, 2)
         entry["verify_rows_per_s"] = round(B * (D + 1) / (vms / 1e3), 1)
         entry["verify_roofline"] = roof(vbytes, vms)
+        if w.mode != "greedy":
+            # with p_target and p_draft requested: every draft position is computed
+            ptp = torch.empty((B, D), device=dev)
+            pdp = torch.empty((B, D), device=dev)
+            pms = timed_call(lambda: lib.spec_verify_sample(T, Q, d, tau, top_k, top_p, x["seed"],
+                                                            out, na, ptp, pdp, ws))
+            entry["verify_with_probabilities_us"] = round(pms * 1e3, 2)
         if vbytes < L2_BYTES:
             # back-to-back calls as a decode loop issues them: a CUDA graph of calls, each on
             # its own copy of the logits

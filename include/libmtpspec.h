@@ -264,7 +264,9 @@ int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draf
  *   top_p          float [B] or NULL   >= 1 => off; must be > 0
  *   seed           Philox key
  *   out_tokens, num_accepted   as in spec_verify_greedy
- *   p_target, p_draft  float [B, D] or NULL   p_j(d_j) and q_j(d_j) for every j < D
+ *   p_target, p_draft  float [B, D] or NULL   p_j(d_j) and q_j(d_j) for every j < D; when
+ *                  both are NULL the call may skip the positions behind each row's first
+ *                  rejection (no output depends on them), which makes it faster
  *   workspace      >= spec_verify_workspace_bytes(B, D, V) bytes, 256-byte aligned;
  *                  no initial contents are needed
  *   status         int32 [1] or NULL

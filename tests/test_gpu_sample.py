@@ -307,3 +307,41 @@ def test_long_drafts(V, D, dtype):
     assert o["num_accepted"].max() >= min(D, 9)
     assert g["status"] == o["status"] == 0
     compare(g, o, x, label=f"V={V} D={D} {dtype}")
+
+
+@pytest.mark.parametrize("one_hot", [False, True])
+def test_outputs_without_probabilities_equal_those_with(one_hot):
+    # without p_target and p_draft only the positions up to each row's first rejection are
+    # read, so a unit behind a rejection the cluster already knows of is skipped; the
+    # tokens and accepted counts must be the same, bit for bit, as when every position's
+    # probabilities are requested (units position-major at this batch size)
+    w = WORKLOADS["serve_b256_d3_v152k"].scaled(B=96, seed=61, philox_seed=67)
+    x = make_verify_inputs(w)
+    if one_hot:
+        x = _greedy_half(x, np.random.default_rng(61))
+    B, D = x["d"].shape
+    T, Q = _dev(x["T"]), (None if one_hot else _dev(x["Q"]))
+    args = (T, Q, _dev(x["d"]), _dev(x["tau"]), None, _dev(x["top_p"]), x["seed"])
+    ws = torch.empty(lib.spec_verify_workspace_bytes(B, D, T.shape[-1]), dtype=torch.uint8,
+                     device=DEV)
+
+    def run(with_p):
+        out = torch.full((B, D + 1), -9, dtype=torch.int32, device=DEV)
+        na = torch.full((B,), -9, dtype=torch.int32, device=DEV)
+        pt = torch.full((B, D), -1.0, device=DEV) if with_p else None
+        pd = torch.full((B, D), -1.0, device=DEV) if with_p else None
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        lib.spec_verify_sample(*args, out, na, pt, pd, ws, st)
+        torch.cuda.synchronize()
+        return out.cpu().numpy(), na.cpu().numpy(), pt, pd, int(st.item())
+
+    o1, n1, pt, pd, s1 = run(True)
+    for _ in range(2):
+        o0, n0, _, _, s0 = run(False)
+        np.testing.assert_array_equal(o0, o1)
+        np.testing.assert_array_equal(n0, n1)
+        assert s0 == s1 == 0
+    g = dict(out=o1, num_accepted=n1, p_target=pt.cpu().numpy(), p_draft=pd.cpu().numpy(), status=s1)
+    rows = list(range(0, B, 3))
+    compare(g, oracle_verify(x, rows=rows, one_hot=one_hot), x, rows=rows,
+            label=f"with probabilities, one_hot={one_hot}", one_hot=one_hot)

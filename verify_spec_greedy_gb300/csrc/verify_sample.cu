@@ -478,6 +478,9 @@ struct Params {
     // unit behind a rejected position of its row skips its draw, which no output reads
     uint32_t *dead;
     int32_t pmajor;  // units position-major (u = j B + b) rather than row-major (u = b (D+1) + j)
+    // p_target or p_draft requested: every draft position's probabilities are an output;
+    // otherwise only the positions up to a row's first rejection are read
+    int32_t need_p;
 };
 
 __device__ __forceinline__ bool row_sampled(const Params &P, int64_t b) {
@@ -546,18 +549,19 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         return q;
     };
     // one whole warp (of CTA 0): the first unit after unit `from` in this cluster's sequence
-    // that is sampled and not the bonus unit (j = D, read only when every draft of the row
-    // is accepted) of a row already seen rejected (a flag not yet set only costs that unit's
-    // work), with its parameters, into slot `slot` of e1su / e1sp.  Each lane loads a
-    // candidate's parameters, so 32 candidates cost one round of loads.
+    // that is sampled and has an output to give: not behind a position of its row already
+    // seen rejected, when that position's outputs are not read (the bonus unit, j = D, or
+    // any position when p_target and p_draft are not requested; a flag not yet set only
+    // costs that unit's work), with its parameters, into slot `slot` of e1su / e1sp.  Each
+    // lane loads a candidate's parameters, so 32 candidates cost one round of loads.
     auto find_next = [&](int from, int slot) {
         int found = -1;
         for (int base = from + G; from >= 0 && base < U && found < 0; base += 32 * G) {
             const int cand = base + lane * G;
             UnitParams q = {0, 0, 0.0f, 1.0f, 0, -1};
             if (cand < U) q = load_params(cand);
-            const bool dead = P.dead && q.j == D &&
-                              *reinterpret_cast<volatile const uint32_t *>(P.dead + q.b) < static_cast<uint32_t>(D);
+            const bool dead = P.dead && (q.j == D || !P.need_p) &&
+                              *reinterpret_cast<volatile const uint32_t *>(P.dead + q.b) < static_cast<uint32_t>(q.j);
             const unsigned msk = __ballot_sync(0xFFFFFFFFu, cand < U && q.tau > 0.0f && q.pp > 0.0f && !dead);
             if (msk) {
                 const int l = __ffs(msk) - 1;
@@ -808,13 +812,15 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         }
         __syncthreads();
 
-        // A row's bonus unit is read only when every draft of the row is accepted.  When the
-        // cluster's agreed view of the row (exchanged at E1) already holds a rejection, the
-        // unit's filters are not computed, and its draw is skipped below.
+        // A row's bonus unit is read only when every draft of the row is accepted, and (when
+        // p_target and p_draft are not requested) a draft position only up to the row's first
+        // rejection.  When the cluster's agreed view of the row (exchanged at E1) already holds
+        // a rejection before such a unit, its filters are not computed, and its draw is
+        // skipped below; its record is never read.
         uint32_t dk1 = 0xFFFFFFFFu;
         for (uint32_t c = 0; c < C; ++c) dk1 = min(dk1, sh.e1k[ep][c]);
-        const bool dead_bonus = j == D && dk1 < static_cast<uint32_t>(D);
-        if (filt && !dead_bonus) {
+        const bool dead_unit = (j == D || !P.need_p) && dk1 < static_cast<uint32_t>(j);
+        if (filt && !dead_unit) {
             // ---- pass 2: histogram of the elements in the bins that can hold the boundary.
             // Top-k counts them; top-p adds each element's weight scaled by its bin's octave,
             // round(w * 2^(16 + o)): an exponent add, then rounding by the sum with 2^23.  Bin
@@ -2024,10 +2030,13 @@ static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     int64_t G = resident_clusters<T>(C, smem);
     if (G > units) G = units;
     p.G = static_cast<int32_t>(G);
-    // position-major order and draw skipping pay once each cluster runs many units, or
-    // with a one-hot draft, whose units are short beside their draws (with two staged rows
-    // and a few rounds of units they cost a few per cent: measured on 32 and 128 units)
-    p.pmajor = (!p.Q || units >= 8 * G) ? 1 : 0;
+    // Position-major order lets a cluster skip the units behind a rejection it knows of.  It
+    // pays once each cluster runs many units; with a one-hot draft, whose units are short
+    // beside their draws; and with more than one round of units and two drafts or more a
+    // row (the later positions and the bonus units fall in the later rounds: 32 units of
+    // three drafts, 74.8 -> 64.6 us).  With one draft a row and a few rounds it costs a few
+    // per cent (128 units: 93.2 -> 94.8 us).
+    p.pmajor = (!p.Q || units >= 8 * G || (units > G && p.D >= 2)) ? 1 : 0;
     if (const char *o = getenv("MTPSPEC_VERIFY_ORDER"))  // "row" or "position" forces the order
         p.pmajor = o[0] == 'p' ? 1 : (o[0] == 'r' ? 0 : p.pmajor);
     if (!p.pmajor) {
@@ -2071,6 +2080,7 @@ static cudaError_t run_verify_sample_impl(const VerifySampleArgs &a, bool row_fl
     p.res = static_cast<vs::UnitResult *>(a.workspace);
     p.status = a.status;
     p.pmajor = 0;
+    p.need_p = (a.p_target || a.p_draft) ? 1 : 0;
     p.dead = row_flags ? reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(a.workspace) +
                                                       verify_records_bytes(a.B, a.D))
                        : nullptr;  // reset (and used) by the launch when the order is position-major
