@@ -141,6 +141,25 @@ def test_large_k_and_flat_rows_use_exact_search():
     compare(gpu_verify(x2), oracle_verify(x2), x2, label="flat bf16")
 
 
+@pytest.mark.parametrize("C", [2, 6, 16])
+def test_top_k_bound_edge_cases(C, monkeypatch):
+    # top-k rows with a small k gather every element at or above a lower bound on the k-th
+    # largest logit: k on both sides of the largest k that takes the bound, the top logits
+    # packed into the first CTA's slice (the bound then admits too many candidates, and the
+    # exact search takes over), and logits on a coarse grid (many ties at the bound)
+    monkeypatch.setenv("MTPSPEC_VERIFY_CLUSTER", str(C))
+    w = Workload(name="kb", B=8, D=2, V=30011, H=8, tau=0.8, top_k=50, top_p=0.95, t_std=3.0,
+                 q_noise=1.0, seed=30 + C, philox_seed=30 + C)
+    x = make_verify_inputs(w)
+    x["top_k"] = np.array([1, 2, 7, 64, 127, 128, 129, 50], np.int32)
+    x["top_p"][5] = 1.0
+    x["T"][1, :, :500] += 12.0
+    x["Q"][1, :, :500] += 12.0
+    x["T"][2] = np.round(x["T"][2] * 2.0) / 2.0
+    x["Q"][2] = np.round(x["Q"][2] * 2.0) / 2.0
+    compare(gpu_verify(x), oracle_verify(x), x, label=f"top-k bound C={C}")
+
+
 def test_negative_infinity_and_degenerate_rows():
     w = Workload(name="ninf", B=12, D=2, V=5000, H=8, tau=1.0, top_k=30, top_p=0.9, seed=7,
                  philox_seed=7)

@@ -110,6 +110,9 @@ constexpr int NXB = 9;
 using UnitResult = VerifyUnitRecord;
 
 constexpr int NSMALL = NT / 2;   // candidates per row ranked by counting (both rows at once)
+// Top-k rows with k <= KFAST skip the histogram: every element at or above a lower bound on
+// the k-th largest logit, found in pass 1, is a candidate.
+constexpr int KFAST = 128;
 constexpr int PW = 8;            // plan: warps per row
 constexpr int PL = PW * 32;      // plan: lanes per row
 constexpr int BPL = NB / PL;     // plan: bins per lane
@@ -198,8 +201,12 @@ struct __align__(16) Shared {
     // rejected) and sent with its E1 message, so that every CTA takes the same sequence; in
     // CTA 0 the slot of the other parity holds the unit after that, chosen during this E1
     int32_t e1su[2];
+    // top-k rows with a small k: per row, the cluster's lower bound on the k-th largest logit
+    float kbd[2];
     NextParams e1sp[2];
 };
+// The state above fills the padding before e1sp: the staged slices keep their room.
+static_assert(sizeof(Shared) == 28544, "the slices' shared-memory budget assumes this size");
 
 __device__ __forceinline__ float ex2(float z) {
     float r;
@@ -402,17 +409,21 @@ __device__ __forceinline__ void for_row(const T *s, int nv, F &&f) {
     }
 }
 
-// Maximum of a 16-byte vector of logits.
-template <typename T>
-__device__ __forceinline__ float vec_max(const uint4 &raw) {
-    constexpr int EPV = elems_per_16B<T>::value;
-    float x[EPV];
-    unpack(raw, x);
-#pragma unroll
-    for (int w = 1; w < EPV; w <<= 1)
-#pragma unroll
-        for (int e = 0; e + w < EPV; e += 2 * w) x[e] = fmaxf(x[e], x[e + w]);
-    return x[0];
+// Maximum of a 16-byte vector of logits (bf16 pairs compared packed, exactly: a bf16
+// maximum widens to the fp32 maximum of the widened values).
+template <typename T> __device__ __forceinline__ float vec_max(const uint4 &raw);
+template <> __device__ __forceinline__ float vec_max<float>(const uint4 &raw) {
+    return fmaxf(fmaxf(__uint_as_float(raw.x), __uint_as_float(raw.y)),
+                 fmaxf(__uint_as_float(raw.z), __uint_as_float(raw.w)));
+}
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+template <> __device__ __forceinline__ float vec_max<uint16_t>(const uint4 &raw) {
+    const uint32_t m = bf16x2_max(bf16x2_max(raw.x, raw.y), bf16x2_max(raw.z, raw.w));
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
 }
 // Sum of 2^(x * c2 + nm) over a 16-byte vector of logits.
 template <typename T>
@@ -458,6 +469,9 @@ __device__ __forceinline__ void bin_bounds(unsigned long long qs, int b, unsigne
     err = (mid >> 18) + 2ull + (sft >= 1 ? static_cast<unsigned long long>(cnt) << (sft - 1)
                                          : static_cast<unsigned long long>(cnt));
 }
+
+// Top-k rows with k <= KFAST: the rank each CTA's bound is taken at (see pass 1).
+__device__ __forceinline__ int kfast_nth(int k, int C) { return C > 1 ? (k + C - 2) / (C - 1) : k; }
 
 struct Params {
     const void *T;
@@ -626,6 +640,65 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         }
     };
 
+    // one whole warp: the bin of h (256 bins, scanned from the top) where the count of
+    // values, starting from `above`, reaches nth; out[0] = the bin, out[1] = the count in the
+    // bins above it
+    auto pick_bin = [&](const uint32_t *h, uint32_t above, uint32_t nth, uint32_t *out) {
+        const int top = 255 - 8 * lane;
+        uint32_t s = 0;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) s += h[top - t];
+        uint32_t incl = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, above + incl >= nth);
+        const int hl = hit ? __ffs(hit) - 1 : 31;
+        if (lane == hl) {
+            uint32_t acc = above + incl - s;
+            int bin = top - 7;
+            for (int t = 0; t < 8; ++t) {
+                const uint32_t c = h[top - t];
+                if (acc + c >= nth) {
+                    bin = top - t;
+                    break;
+                }
+                acc += c;
+            }
+            out[0] = static_cast<uint32_t>(bin);
+            out[1] = acc;
+        }
+    };
+    // The nth largest of the threads' values t0 (row 0) and t1 (row 1), rounded down to the
+    // lowest value of its 16-bit key prefix: two rounds of a 256-bin radix selection over
+    // the order keys, in the zeroed histogram storage (row r: the first round's bins at
+    // r * RSN, the second's at r * RSN + 256, the picks at r * RSN + 512).  nth <= NT, so
+    // a bin always holds it; a bound within the bin of -inf is -inf.
+    auto kth_bound = [&](float t0, float t1, int nth, int rows, float &o0, float &o1) {
+        uint32_t *hs = &sh.a.h.hloc[0][0];
+        const uint32_t key[2] = {order_key(t0), order_key(t1)};
+        for (int r = 0; r < rows; ++r) atomicAdd(&hs[r * RSN + (key[r] >> 24)], 1u);
+        __syncthreads();
+        if (warp < rows) pick_bin(hs + warp * RSN, 0u, static_cast<uint32_t>(nth), hs + warp * RSN + 512);
+        __syncthreads();
+        for (int r = 0; r < rows; ++r)
+            if ((key[r] >> 24) == hs[r * RSN + 512]) atomicAdd(&hs[r * RSN + 256 + ((key[r] >> 16) & 255u)], 1u);
+        __syncthreads();
+        if (warp < rows)
+            pick_bin(hs + warp * RSN + 256, hs[warp * RSN + 513], static_cast<uint32_t>(nth), hs + warp * RSN + 514);
+        __syncthreads();
+        float o[2] = {-INFINITY, -INFINITY};
+        for (int r = 0; r < rows; ++r) {
+            const uint32_t edge = (hs[r * RSN + 512] << 24) | (hs[r * RSN + 514] << 16);
+            o[r] = edge > order_key(-INFINITY) ? key_to_float(edge) : -INFINITY;
+        }
+        o0 = o[0];
+        o1 = o[1];
+    };
+    static_assert(RSN >= 516 && KFAST <= NT, "the selection's bins and picks fit a histogram row");
+
     int u = -1;
     if (g < U) u = row_sampled(P, unit_row(g)) ? g : next_unit(g);
     UnitParams cnx = {0, 0, 1.0f, 1.0f, 0, -1};  // this unit's parameters
@@ -658,6 +731,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         const int nrows = j < D && !one_hot ? 2 : 1;
         const bool k_on = kk >= 1 && kk < V;
         const bool p_on = pp < 1.0f;
+        const bool kfast = k_on && kk <= KFAST;
         const float c2 = __fdiv_rn(1.44269504088896340736f, tau);
         const bool dvalid = d >= 0 && d < V;
         const bool d_here = dvalid && d >= lo && d < lo + n;
@@ -711,6 +785,14 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 sh.xd[0] = widen(sdat(0)[d - lo]);
                 sh.xd[1] = widen(sdat(1)[d - lo]);
             }
+            // top-k with a small k: the kth-largest of the threads' maxima, rounded down to its
+            // 16-bit key prefix, has at least kth elements of this slice at or above it (kth =
+            // ceil(k / (C - 1))); the kq-th largest of these bounds over the C CTAs (kq =
+            // ceil(k / kth) <= C) then has at least k elements of the row at or above it, so it
+            // lies at or below the row's k-th largest logit, and a CTA with a short slice does
+            // not weaken it
+            float bd0 = -INFINITY, bd1 = -INFINITY;
+            if (kfast) kth_bound(mx0, mx1, kfast_nth(kk, static_cast<int>(C)), nrows, bd0, bd1);
             mx0 = warp_max(mx0);
             mx1 = warp_max(mx1);
             if (lane == 0) {
@@ -721,24 +803,31 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             // every warp reduces the warps' maxima the same way
             cm0 = warp_max(lane < NW ? sh.w.p1.rf[0][lane] : -INFINITY);
             cm1 = warp_max(lane < NW ? sh.w.p1.rf[1][lane] : -INFINITY);
-            // z = x * c2 + nm, nm = -cm * c2 (0 for a slice of -inf alone, whose sum is 0)
-            const float nm0 = cm0 > -INFINITY ? -cm0 * c2 : 0.0f;
-            const float nm1 = cm1 > -INFINITY ? -cm1 * c2 : 0.0f;
-            float a0 = 0.0f, a1 = 0.0f;
+            if (kfast) {
+                // the top-k set is renormalised on its own: no row sum is needed, and the E1
+                // message carries the bounds in its place
+                cs0 = bd0;
+                cs1 = bd1;
+            } else {
+                // z = x * c2 + nm, nm = -cm * c2 (0 for a slice of -inf alone, whose sum is 0)
+                const float nm0 = cm0 > -INFINITY ? -cm0 * c2 : 0.0f;
+                const float nm1 = cm1 > -INFINITY ? -cm1 * c2 : 0.0f;
+                float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll 2
-            for (int v = tid; v < nvr; v += NT) {
-                a0 += vec_sum_ex2<T>(sv0[v], c2, nm0);
-                if (nrows > 1) a1 += vec_sum_ex2<T>(sv1[v], c2, nm1);
+                for (int v = tid; v < nvr; v += NT) {
+                    a0 += vec_sum_ex2<T>(sv0[v], c2, nm0);
+                    if (nrows > 1) a1 += vec_sum_ex2<T>(sv1[v], c2, nm1);
+                }
+                a0 = warp_sum_f32(a0);
+                a1 = warp_sum_f32(a1);
+                if (lane == 0) {
+                    sh.w.p1.rs[0][warp] = a0;
+                    sh.w.p1.rs[1][warp] = a1;
+                }
+                __syncthreads();
+                cs0 = warp_sum_f32(lane < NW ? sh.w.p1.rs[0][lane] : 0.0f);
+                cs1 = warp_sum_f32(lane < NW ? sh.w.p1.rs[1][lane] : 0.0f);
             }
-            a0 = warp_sum_f32(a0);
-            a1 = warp_sum_f32(a1);
-            if (lane == 0) {
-                sh.w.p1.rs[0][warp] = a0;
-                sh.w.p1.rs[1][warp] = a1;
-            }
-            __syncthreads();
-            cs0 = warp_sum_f32(lane < NW ? sh.w.p1.rs[0][lane] : 0.0f);
-            cs1 = warp_sum_f32(lane < NW ? sh.w.p1.rs[1][lane] : 0.0f);
         }
         if (!started) {
             cluster_wait_acquire();  // every CTA of the cluster has initialised its barriers
@@ -776,17 +865,34 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         // ---- row statistics (every CTA, identical): warp 0 merges the CTAs' partials
         if (warp == 0) {
             const int r = lane >> 4, c = lane & 15;
+            const bool in = r < nrows && c < static_cast<int>(C);
             float tm = -INFINITY, ts = 0.0f;
-            if (r < nrows && c < static_cast<int>(C)) {
+            if (in) {
                 const float4 e = sh.e1[ep][c];
                 tm = r == 0 ? e.x : e.z;
                 ts = r == 0 ? e.y : e.w;
             }
+            if (kfast) {
+                // the maximum, and the kq-th largest of the CTAs' bounds: kq CTAs hold at
+                // least kth elements each at or above it, kq * kth >= k
+                const int kth = kfast_nth(kk, static_cast<int>(C));
+                const int kq = (kk + kth - 1) / kth;
+                int rk = 0;
+                for (int q = 0; q < static_cast<int>(C); ++q) {
+                    const float y = __shfl_sync(0xFFFFFFFFu, ts, (lane & 16) | q);
+                    if (y > ts || (y == ts && q < c)) ++rk;
+                }
+                const unsigned hm = __ballot_sync(0xFFFFFFFFu, in && rk == kq - 1) & (r ? 0xFFFF0000u : 0x0000FFFFu);
+                ts = __shfl_sync(0xFFFFFFFFu, ts, hm ? __ffs(hm) - 1 : lane);
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {
-                const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
-                const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
-                ms_merge(tm, ts, m2, s2, c2);
+                for (int o = 8; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, o));
+            } else {
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) {
+                    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
+                    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, ts, o);
+                    ms_merge(tm, ts, m2, s2, c2);
+                }
             }
             if (c == 0 && r < nrows) {
                 sh.m[r] = tm;
@@ -795,8 +901,10 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 sh.deg[r] = !(tm > -INFINITY);
                 sh.mode[r] = 0;
                 sh.theta[r] = -INFINITY;
-                sh.Z[r] = ts;
-                sh.tgt[r] = fx_target(pp, ts);  // the fixed-point top-p target of the plan
+                sh.Z[r] = kfast ? 1.0f : ts;
+                // the fixed-point top-p target of the plan
+                sh.tgt[r] = kfast ? 0ull : fx_target(pp, ts);
+                sh.kbd[r] = kfast ? ts : -INFINITY;
                 // the bins that can hold a top-p boundary: a kept token weighs at least
                 // (1 - p) Z / V, since the tokens below that level weigh less than (1 - p) Z
                 // together
@@ -821,261 +929,271 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         for (uint32_t c = 0; c < C; ++c) dk1 = min(dk1, sh.e1k[ep][c]);
         const bool dead_unit = (j == D || !P.need_p) && dk1 < static_cast<uint32_t>(j);
         if (filt && !dead_unit) {
-            // ---- pass 2: histogram of the elements in the bins that can hold the boundary.
-            // Top-k counts them; top-p adds each element's weight scaled by its bin's octave,
-            // round(w * 2^(16 + o)): an exponent add, then rounding by the sum with 2^23.  Bin
-            // and weight leave fp32 without conversion instructions.  One shared atomic per
-            // element: its cost grows with the lanes it serves, which the bins' range keeps
-            // few.
-            constexpr float MAG = 8388608.0f;  // 2^23
-            const float tza = -c2 * static_cast<float>(R);
-            if (nrows > 1 && !sh.deg[0] && !sh.deg[1] && !k_on) {
-                // both rows in one sweep: twice the independent work per iteration
-                const float nmA = sh.nmc[0], tzbA = sh.tzb[0], fnbA = static_cast<float>(sh.nbu[0]);
-                const float nmB = sh.nmc[1], tzbB = sh.tzb[1], fnbB = static_cast<float>(sh.nbu[1]);
-                uint32_t *hA = sh.a.h.hloc[0];
-                uint32_t *hB = sh.a.h.hloc[1];
-                auto bin_w = [&](float x, float nm, float tzb, float fnb, uint32_t *hh) {
-                    const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
-                    const float tb = __fadd_rz(tz, MAG);
-                    const int bn = __float_as_int(tb) - 0x4B000000;
-                    const float ws = __uint_as_float(__float_as_uint(ex2(fmaf(x, c2, nm))) +
-                                                     (static_cast<uint32_t>((bn >> 5) + 16) << 23));
-                    const uint32_t q = __float_as_uint(ws + MAG) - 0x4B000000u;
-                    if (tz < fnb) atomicAdd(&hh[bn], q);
-                };
+            if (!kfast) {
+                // ---- pass 2: histogram of the elements in the bins that can hold the boundary.
+                // Top-k counts them; top-p adds each element's weight scaled by its bin's octave,
+                // round(w * 2^(16 + o)): an exponent add, then rounding by the sum with 2^23.  Bin
+                // and weight leave fp32 without conversion instructions.  One shared atomic per
+                // element: its cost grows with the lanes it serves, which the bins' range keeps
+                // few.
+                constexpr float MAG = 8388608.0f;  // 2^23
+                const float tza = -c2 * static_cast<float>(R);
+                if (nrows > 1 && !sh.deg[0] && !sh.deg[1] && !k_on) {
+                    // both rows in one sweep: twice the independent work per iteration
+                    const float nmA = sh.nmc[0], tzbA = sh.tzb[0], fnbA = static_cast<float>(sh.nbu[0]);
+                    const float nmB = sh.nmc[1], tzbB = sh.tzb[1], fnbB = static_cast<float>(sh.nbu[1]);
+                    uint32_t *hA = sh.a.h.hloc[0];
+                    uint32_t *hB = sh.a.h.hloc[1];
+                    auto bin_w = [&](float x, float nm, float tzb, float fnb, uint32_t *hh) {
+                        const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
+                        const float tb = __fadd_rz(tz, MAG);
+                        const int bn = __float_as_int(tb) - 0x4B000000;
+                        const float ws = __uint_as_float(__float_as_uint(ex2(fmaf(x, c2, nm))) +
+                                                         (static_cast<uint32_t>((bn >> 5) + 16) << 23));
+                        const uint32_t q = __float_as_uint(ws + MAG) - 0x4B000000u;
+                        if (tz < fnb) atomicAdd(&hh[bn], q);
+                    };
 #pragma unroll 2
-                for (int v = tid; v < nvr; v += NT) {
-                    float xa[EPV], xb[EPV];
-                    unpack(sv0[v], xa);
-                    unpack(sv1[v], xb);
+                    for (int v = tid; v < nvr; v += NT) {
+                        float xa[EPV], xb[EPV];
+                        unpack(sv0[v], xa);
+                        unpack(sv1[v], xb);
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        bin_w(xa[e], nmA, tzbA, fnbA, hA);
-                        bin_w(xb[e], nmB, tzbB, fnbB, hB);
+                        for (int e = 0; e < EPV; ++e) {
+                            bin_w(xa[e], nmA, tzbA, fnbA, hA);
+                            bin_w(xb[e], nmB, tzbB, fnbB, hB);
+                        }
                     }
+                } else {
+#pragma unroll 1
+                    for (int r = 0; r < nrows; ++r) {
+                        if (sh.deg[r]) continue;
+                        const float nm = sh.nmc[r], tzb = sh.tzb[r];
+                        const float fnb = static_cast<float>(sh.nbu[r]);
+                        uint32_t *hh = sh.a.h.hloc[r];
+                        if (k_on) {
+                            for_row(sdat(r), nvr, [&](float x, int) {
+                                const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
+                                const float tb = __fadd_rz(tz, MAG);  // 2^23 + trunc(tz) below 2^23
+                                if (tz < fnb) atomicAdd(&hh[__float_as_int(tb) - 0x4B000000], 1u);
+                            });
+                        } else {
+                            for_row(sdat(r), nvr, [&](float x, int) {
+                                // -z * R >= 0 (clamped: rounding can make it a hair negative at the
+                                // maximum); bins at its integer part
+                                const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
+                                const float tb = __fadd_rz(tz, MAG);
+                                const int bn = __float_as_int(tb) - 0x4B000000;
+                                const float ws = __uint_as_float(__float_as_uint(ex2(fmaf(x, c2, nm))) +
+                                                                 (static_cast<uint32_t>((bn >> 5) + 16) << 23));
+                                const uint32_t q = __float_as_uint(ws + MAG) - 0x4B000000u;
+                                if (tz < fnb) atomicAdd(&hh[bn], q);
+                            });
+                        }
+                    }
+                }
+                __syncthreads();
+                // ---- E2a: reduce-scatter in groups of four bins, each CTA's bins to their owner
+                const int nb0 = sh.nbu[0], nb1 = nrows > 1 ? sh.nbu[1] : 0;
+                const int rs0 = (((nb0 + C - 1) / C) + 3) & ~3, rs1 = (((nb1 + C - 1) / C) + 3) & ~3;
+                const int g0 = static_cast<int>(C) * (rs0 >> 2), g1 = static_cast<int>(C) * (rs1 >> 2);
+                for (int idx = tid; idx < g0 + g1; idx += NT) {
+                    const int r = idx < g0 ? 0 : 1;
+                    const int q4 = r == 0 ? idx : idx - g0;  // group of 4 bins, in bin order
+                    const int rsz = r == 0 ? rs0 : rs1;
+                    const int owner = (q4 * 4) / rsz, kq = q4 * 4 - owner * rsz;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(&sh.a.h.hloc[r][q4 * 4]);
+                    st_peer_u32x4(peer_addr(smem_addr(&sh.a.h.rsin[r][static_cast<int>(rank) * rsz + kq]), owner), v);
+                }
+                __syncthreads();
+                if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_RS], tid);
+                xwait(XB_RS);
+                // ---- E2b: sum the owned bins (in 64 bits: a bin of the whole row can exceed 32)
+                // and broadcast them, two bins per store
+                for (int idx = tid; idx < ((rs0 + rs1) >> 1); idx += NT) {
+                    const int r = idx < (rs0 >> 1) ? 0 : 1;
+                    const int kq = (r == 0 ? idx : idx - (rs0 >> 1)) * 2;
+                    const int rsz = r == 0 ? rs0 : rs1;
+                    unsigned long long c0 = 0, c1 = 0;
+                    for (uint32_t c = 0; c < C; ++c) {
+                        const uint2 v = *reinterpret_cast<const uint2 *>(&sh.a.h.rsin[r][c * rsz + kq]);
+                        c0 += v.x;
+                        c1 += v.y;
+                    }
+                    // bin b goes to [b % BPL][b / BPL] (bins past NB lie past every used range)
+                    const int b0 = static_cast<int>(rank) * rsz + kq;
+                    const uint32_t a0 = smem_addr(&sh.b.hist[r][(b0 % BPL) * PL + b0 / BPL]);
+                    const uint32_t a1 = smem_addr(&sh.b.hist[r][((b0 + 1) % BPL) * PL + (b0 + 1) / BPL]);
+                    for (uint32_t c = 0; c < C; ++c) {
+                        if (b0 < NB) st_peer_u64(peer_addr(a0, c), c0);
+                        if (b0 + 1 < NB) st_peer_u64(peer_addr(a1, c), c1);
+                    }
+                }
+                __syncthreads();
+                if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_AG], tid);
+                xwait(XB_AG);
+
+                // ---- plan per row: the bin range that holds the boundary, or the exact search.
+                // The PW warps of group r take row r, BPL bins a lane (the gathered histogram is
+                // stored transposed, bin b at [b % BPL][b / BPL], so that these loads are free of
+                // bank conflicts); scans of the per-bin counts (top-k) or weights and their
+                // margins (top-p) over the group's lanes find the crossing bins and the exact
+                // weight of the bins before them.  The other warps go on to the barrier.
+                {
+                    const int r = warp / PW, j = tid - r * PL, hw = warp - r * PW;
+                    if (r < nrows && !sh.deg[r]) {
+                        const int nbu = sh.nbu[r];
+                        const unsigned long long tgt = k_on ? 0ull : sh.tgt[r];
+                        const unsigned long long *hr = sh.b.hist[r];
+                        // weight, margin and element-count bound of bin bn (0 past the used bins)
+                        auto bounds = [&](int bn, unsigned long long &bm, unsigned long long &be, uint32_t &bc) {
+                            bm = be = 0;
+                            bc = 0;
+                            if (bn < nbu) {
+                                const unsigned long long qs = hr[(bn % BPL) * PL + bn / BPL];
+                                if (k_on) bc = static_cast<uint32_t>(qs);
+                                else bin_bounds(qs, bn, bm, be, bc);
+                            }
+                        };
+                        unsigned long long m_s = 0, e_s = 0;
+                        uint32_t cn_s = 0;
+#pragma unroll
+                        for (int t = 0; t < BPL; ++t) {
+                            unsigned long long bm, be;
+                            uint32_t bc;
+                            bounds(BPL * j + t, bm, be, bc);
+                            m_s += bm;
+                            e_s += be;
+                            cn_s += bc;
+                        }
+                        unsigned long long m_i = m_s, e_i = e_s;
+                        uint32_t cn_i = cn_s;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const unsigned long long a1 = __shfl_up_sync(0xFFFFFFFFu, m_i, o);
+                            const unsigned long long a2 = __shfl_up_sync(0xFFFFFFFFu, e_i, o);
+                            const uint32_t a3 = __shfl_up_sync(0xFFFFFFFFu, cn_i, o);
+                            if (lane >= o) {
+                                m_i += a1;
+                                e_i += a2;
+                                cn_i += a3;
+                            }
+                        }
+                        if (lane == 31) {
+                            sh.w.pl.lo[warp] = m_i;
+                            sh.w.pl.hi[warp] = e_i;
+                            sh.w.pl.cn[warp] = cn_i;
+                        }
+                        if (j == 0) {
+                            sh.pb1[r] = nbu;
+                            sh.pb2[r] = nbu;
+                            sh.pcc1[r] = 0;
+                            sh.pcc2[r] = 0;
+                            sh.pma[r] = 0;
+                        }
+                        group_barrier<PL>(r);
+                        // the group's earlier warps, and the row's total count
+                        uint32_t cn_tot = 0;
+#pragma unroll
+                        for (int q = 0; q < PW; ++q) {
+                            const int wi = r * PW + q;
+                            if (q < hw) {
+                                m_i += sh.w.pl.lo[wi];
+                                e_i += sh.w.pl.hi[wi];
+                                cn_i += sh.w.pl.cn[wi];
+                            }
+                            cn_tot += sh.w.pl.cn[wi];
+                        }
+                        if (k_on) {
+                            // the bin holding the k-th largest value; every bin up to it is gathered
+                            const uint32_t need = static_cast<uint32_t>(kk);
+                            if (cn_i - cn_s < need && cn_i >= need) {
+                                uint32_t acc = cn_i - cn_s;
+                                for (int t = 0; t < BPL; ++t) {
+                                    unsigned long long bm, be;
+                                    uint32_t bc;
+                                    bounds(BPL * j + t, bm, be, bc);
+                                    acc += bc;
+                                    if (acc >= need) {
+                                        sh.pb2[r] = BPL * j + t;
+                                        sh.pcc2[r] = acc;
+                                        break;
+                                    }
+                                }
+                            }
+                        } else {
+                            // b1: the first bin whose upper cumulative bound reaches the target
+                            // (every earlier bin is kept whole); b2: the first whose lower bound
+                            // reaches it (every later bin is dropped)
+                            if (m_i + e_i - (m_s + e_s) < tgt && m_i + e_i >= tgt) {
+                                unsigned long long am = m_i - m_s, ae = e_i - e_s;
+                                uint32_t cb = cn_i - cn_s;
+                                for (int t = 0; t < BPL; ++t) {
+                                    unsigned long long bm, be;
+                                    uint32_t bc;
+                                    bounds(BPL * j + t, bm, be, bc);
+                                    if (am + bm + ae + be >= tgt) {
+                                        sh.pb1[r] = BPL * j + t;
+                                        sh.pcc1[r] = cb;
+                                        sh.pma[r] = am;
+                                        break;
+                                    }
+                                    am += bm;
+                                    ae += be;
+                                    cb += bc;
+                                }
+                            }
+                            const unsigned long long lo_i = m_i > e_i ? m_i - e_i : 0ull;
+                            const unsigned long long lo_x = (m_i - m_s) > (e_i - e_s) ? (m_i - m_s) - (e_i - e_s) : 0ull;
+                            if (lo_x < tgt && lo_i >= tgt) {
+                                unsigned long long am = m_i - m_s, ae = e_i - e_s;
+                                uint32_t cb = cn_i - cn_s;
+                                for (int t = 0; t < BPL; ++t) {
+                                    unsigned long long bm, be;
+                                    uint32_t bc;
+                                    bounds(BPL * j + t, bm, be, bc);
+                                    am += bm;
+                                    ae += be;
+                                    cb += bc;
+                                    if (am > ae && am - ae >= tgt) {
+                                        sh.pb2[r] = BPL * j + t;
+                                        sh.pcc2[r] = cb;
+                                        break;
+                                    }
+                                }
+                            }
+                        }
+                        group_barrier<PL>(r);
+                        if (j == 0) {
+                            int32_t b1 = 0, b2 = sh.pb2[r];
+                            uint32_t ncand;
+                            bool slow;
+                            if (k_on) {
+                                ncand = sh.pcc2[r];
+                                slow = b2 >= nbu;
+                                sh.pma[r] = 0;
+                            } else {
+                                b1 = sh.pb1[r];
+                                slow = b1 >= nbu;
+                                const uint32_t c2b = b2 >= nbu ? cn_tot : sh.pcc2[r];
+                                if (b2 >= nbu) b2 = nbu - 1;
+                                ncand = c2b - sh.pcc1[r];
+                            }
+                            if (ncand > static_cast<uint32_t>(NT) || ncand == 0) slow = true;
+                            sh.mode[r] = slow ? 2 : 1;
+                            sh.b1[r] = b1;
+                            sh.b2[r] = b2;
+                            sh.lcnt[r] = 0;
+                        }
+                    }
+                    __syncthreads();
                 }
             } else {
-#pragma unroll 1
-                for (int r = 0; r < nrows; ++r) {
-                    if (sh.deg[r]) continue;
-                    const float nm = sh.nmc[r], tzb = sh.tzb[r];
-                    const float fnb = static_cast<float>(sh.nbu[r]);
-                    uint32_t *hh = sh.a.h.hloc[r];
-                    if (k_on) {
-                        for_row(sdat(r), nvr, [&](float x, int) {
-                            const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
-                            const float tb = __fadd_rz(tz, MAG);  // 2^23 + trunc(tz) below 2^23
-                            if (tz < fnb) atomicAdd(&hh[__float_as_int(tb) - 0x4B000000], 1u);
-                        });
-                    } else {
-                        for_row(sdat(r), nvr, [&](float x, int) {
-                            // -z * R >= 0 (clamped: rounding can make it a hair negative at the
-                            // maximum); bins at its integer part
-                            const float tz = fmaxf(fmaf(x, tza, tzb), 0.0f);
-                            const float tb = __fadd_rz(tz, MAG);
-                            const int bn = __float_as_int(tb) - 0x4B000000;
-                            const float ws = __uint_as_float(__float_as_uint(ex2(fmaf(x, c2, nm))) +
-                                                             (static_cast<uint32_t>((bn >> 5) + 16) << 23));
-                            const uint32_t q = __float_as_uint(ws + MAG) - 0x4B000000u;
-                            if (tz < fnb) atomicAdd(&hh[bn], q);
-                        });
-                    }
-                }
-            }
-            __syncthreads();
-            // ---- E2a: reduce-scatter in groups of four bins, each CTA's bins to their owner
-            const int nb0 = sh.nbu[0], nb1 = nrows > 1 ? sh.nbu[1] : 0;
-            const int rs0 = (((nb0 + C - 1) / C) + 3) & ~3, rs1 = (((nb1 + C - 1) / C) + 3) & ~3;
-            const int g0 = static_cast<int>(C) * (rs0 >> 2), g1 = static_cast<int>(C) * (rs1 >> 2);
-            for (int idx = tid; idx < g0 + g1; idx += NT) {
-                const int r = idx < g0 ? 0 : 1;
-                const int q4 = r == 0 ? idx : idx - g0;  // group of 4 bins, in bin order
-                const int rsz = r == 0 ? rs0 : rs1;
-                const int owner = (q4 * 4) / rsz, kq = q4 * 4 - owner * rsz;
-                const uint4 v = *reinterpret_cast<const uint4 *>(&sh.a.h.hloc[r][q4 * 4]);
-                st_peer_u32x4(peer_addr(smem_addr(&sh.a.h.rsin[r][static_cast<int>(rank) * rsz + kq]), owner), v);
-            }
-            __syncthreads();
-            if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_RS], tid);
-            xwait(XB_RS);
-            // ---- E2b: sum the owned bins (in 64 bits: a bin of the whole row can exceed 32)
-            // and broadcast them, two bins per store
-            for (int idx = tid; idx < ((rs0 + rs1) >> 1); idx += NT) {
-                const int r = idx < (rs0 >> 1) ? 0 : 1;
-                const int kq = (r == 0 ? idx : idx - (rs0 >> 1)) * 2;
-                const int rsz = r == 0 ? rs0 : rs1;
-                unsigned long long c0 = 0, c1 = 0;
-                for (uint32_t c = 0; c < C; ++c) {
-                    const uint2 v = *reinterpret_cast<const uint2 *>(&sh.a.h.rsin[r][c * rsz + kq]);
-                    c0 += v.x;
-                    c1 += v.y;
-                }
-                // bin b goes to [b % BPL][b / BPL] (bins past NB lie past every used range)
-                const int b0 = static_cast<int>(rank) * rsz + kq;
-                const uint32_t a0 = smem_addr(&sh.b.hist[r][(b0 % BPL) * PL + b0 / BPL]);
-                const uint32_t a1 = smem_addr(&sh.b.hist[r][((b0 + 1) % BPL) * PL + (b0 + 1) / BPL]);
-                for (uint32_t c = 0; c < C; ++c) {
-                    if (b0 < NB) st_peer_u64(peer_addr(a0, c), c0);
-                    if (b0 + 1 < NB) st_peer_u64(peer_addr(a1, c), c1);
-                }
-            }
-            __syncthreads();
-            if (tid < static_cast<int>(C)) xarrive(&sh.xbar[XB_AG], tid);
-            xwait(XB_AG);
-
-            // ---- plan per row: the bin range that holds the boundary, or the exact search.
-            // The PW warps of group r take row r, BPL bins a lane (the gathered histogram is
-            // stored transposed, bin b at [b % BPL][b / BPL], so that these loads are free of
-            // bank conflicts); scans of the per-bin counts (top-k) or weights and their
-            // margins (top-p) over the group's lanes find the crossing bins and the exact
-            // weight of the bins before them.  The other warps go on to the barrier.
-            {
-                const int r = warp / PW, j = tid - r * PL, hw = warp - r * PW;
-                if (r < nrows && !sh.deg[r]) {
-                    const int nbu = sh.nbu[r];
-                    const unsigned long long tgt = k_on ? 0ull : sh.tgt[r];
-                    const unsigned long long *hr = sh.b.hist[r];
-                    // weight, margin and element-count bound of bin bn (0 past the used bins)
-                    auto bounds = [&](int bn, unsigned long long &bm, unsigned long long &be, uint32_t &bc) {
-                        bm = be = 0;
-                        bc = 0;
-                        if (bn < nbu) {
-                            const unsigned long long qs = hr[(bn % BPL) * PL + bn / BPL];
-                            if (k_on) bc = static_cast<uint32_t>(qs);
-                            else bin_bounds(qs, bn, bm, be, bc);
-                        }
-                    };
-                    unsigned long long m_s = 0, e_s = 0;
-                    uint32_t cn_s = 0;
-#pragma unroll
-                    for (int t = 0; t < BPL; ++t) {
-                        unsigned long long bm, be;
-                        uint32_t bc;
-                        bounds(BPL * j + t, bm, be, bc);
-                        m_s += bm;
-                        e_s += be;
-                        cn_s += bc;
-                    }
-                    unsigned long long m_i = m_s, e_i = e_s;
-                    uint32_t cn_i = cn_s;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const unsigned long long a1 = __shfl_up_sync(0xFFFFFFFFu, m_i, o);
-                        const unsigned long long a2 = __shfl_up_sync(0xFFFFFFFFu, e_i, o);
-                        const uint32_t a3 = __shfl_up_sync(0xFFFFFFFFu, cn_i, o);
-                        if (lane >= o) {
-                            m_i += a1;
-                            e_i += a2;
-                            cn_i += a3;
-                        }
-                    }
-                    if (lane == 31) {
-                        sh.w.pl.lo[warp] = m_i;
-                        sh.w.pl.hi[warp] = e_i;
-                        sh.w.pl.cn[warp] = cn_i;
-                    }
-                    if (j == 0) {
-                        sh.pb1[r] = nbu;
-                        sh.pb2[r] = nbu;
-                        sh.pcc1[r] = 0;
-                        sh.pcc2[r] = 0;
-                        sh.pma[r] = 0;
-                    }
-                    group_barrier<PL>(r);
-                    // the group's earlier warps, and the row's total count
-                    uint32_t cn_tot = 0;
-#pragma unroll
-                    for (int q = 0; q < PW; ++q) {
-                        const int wi = r * PW + q;
-                        if (q < hw) {
-                            m_i += sh.w.pl.lo[wi];
-                            e_i += sh.w.pl.hi[wi];
-                            cn_i += sh.w.pl.cn[wi];
-                        }
-                        cn_tot += sh.w.pl.cn[wi];
-                    }
-                    if (k_on) {
-                        // the bin holding the k-th largest value; every bin up to it is gathered
-                        const uint32_t need = static_cast<uint32_t>(kk);
-                        if (cn_i - cn_s < need && cn_i >= need) {
-                            uint32_t acc = cn_i - cn_s;
-                            for (int t = 0; t < BPL; ++t) {
-                                unsigned long long bm, be;
-                                uint32_t bc;
-                                bounds(BPL * j + t, bm, be, bc);
-                                acc += bc;
-                                if (acc >= need) {
-                                    sh.pb2[r] = BPL * j + t;
-                                    sh.pcc2[r] = acc;
-                                    break;
-                                }
-                            }
-                        }
-                    } else {
-                        // b1: the first bin whose upper cumulative bound reaches the target
-                        // (every earlier bin is kept whole); b2: the first whose lower bound
-                        // reaches it (every later bin is dropped)
-                        if (m_i + e_i - (m_s + e_s) < tgt && m_i + e_i >= tgt) {
-                            unsigned long long am = m_i - m_s, ae = e_i - e_s;
-                            uint32_t cb = cn_i - cn_s;
-                            for (int t = 0; t < BPL; ++t) {
-                                unsigned long long bm, be;
-                                uint32_t bc;
-                                bounds(BPL * j + t, bm, be, bc);
-                                if (am + bm + ae + be >= tgt) {
-                                    sh.pb1[r] = BPL * j + t;
-                                    sh.pcc1[r] = cb;
-                                    sh.pma[r] = am;
-                                    break;
-                                }
-                                am += bm;
-                                ae += be;
-                                cb += bc;
-                            }
-                        }
-                        const unsigned long long lo_i = m_i > e_i ? m_i - e_i : 0ull;
-                        const unsigned long long lo_x = (m_i - m_s) > (e_i - e_s) ? (m_i - m_s) - (e_i - e_s) : 0ull;
-                        if (lo_x < tgt && lo_i >= tgt) {
-                            unsigned long long am = m_i - m_s, ae = e_i - e_s;
-                            uint32_t cb = cn_i - cn_s;
-                            for (int t = 0; t < BPL; ++t) {
-                                unsigned long long bm, be;
-                                uint32_t bc;
-                                bounds(BPL * j + t, bm, be, bc);
-                                am += bm;
-                                ae += be;
-                                cb += bc;
-                                if (am > ae && am - ae >= tgt) {
-                                    sh.pb2[r] = BPL * j + t;
-                                    sh.pcc2[r] = cb;
-                                    break;
-                                }
-                            }
-                        }
-                    }
-                    group_barrier<PL>(r);
-                    if (j == 0) {
-                        int32_t b1 = 0, b2 = sh.pb2[r];
-                        uint32_t ncand;
-                        bool slow;
-                        if (k_on) {
-                            ncand = sh.pcc2[r];
-                            slow = b2 >= nbu;
-                            sh.pma[r] = 0;
-                        } else {
-                            b1 = sh.pb1[r];
-                            slow = b1 >= nbu;
-                            const uint32_t c2b = b2 >= nbu ? cn_tot : sh.pcc2[r];
-                            if (b2 >= nbu) b2 = nbu - 1;
-                            ncand = c2b - sh.pcc1[r];
-                        }
-                        if (ncand > static_cast<uint32_t>(NT) || ncand == 0) slow = true;
-                        sh.mode[r] = slow ? 2 : 1;
-                        sh.b1[r] = b1;
-                        sh.b2[r] = b2;
-                        sh.lcnt[r] = 0;
-                    }
+                // every element at or above the row's bound is a candidate, and none lies
+                // above the candidates
+                if (tid < nrows) {
+                    sh.mode[tid] = sh.deg[tid] ? 0 : 1;
+                    sh.pma[tid] = 0;
                 }
                 __syncthreads();
             }
@@ -1084,18 +1202,27 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             const bool any_fast = sh.mode[0] == 1 || (nrows > 1 && sh.mode[1] == 1);
             if (any_fast) {
                 // the candidates of row r: elements of bins [b1, b2] (bin bn = trunc(tz):
-                // bn >= b1 iff tz >= b1, bn <= b2 iff tz < b2 + 1); a vector that holds
+                // bn >= b1 iff tz >= b1, bn <= b2 iff tz < b2 + 1), or, for a top-k row with a
+                // small k, every element at or above the row's bound; a vector that holds
                 // candidates claims their slots at once (the order of the slots does not
                 // matter: every later step depends on values)
                 const float tza = -c2 * static_cast<float>(R);
-                auto gather_vec = [&](int r, int v, const float (&x)[EPV], float tzb, float fb1,
-                                      float fb2) {
+                auto in_bins = [&](const float (&x)[EPV], float tzb, float fb1, float fb2) -> uint32_t {
                     uint32_t msk = 0;
 #pragma unroll
                     for (int e = 0; e < EPV; ++e) {
                         const float tz = fmaxf(fmaf(x[e], tza, tzb), 0.0f);
                         msk |= (tz >= fb1 && tz < fb2) ? (1u << e) : 0u;
                     }
+                    return msk;
+                };
+                auto at_least = [&](const float (&x)[EPV], float bnd) -> uint32_t {
+                    uint32_t msk = 0;
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) msk |= x[e] >= bnd ? (1u << e) : 0u;
+                    return msk;
+                };
+                auto put = [&](int r, int v, const float (&x)[EPV], uint32_t msk) {
                     if (msk) {
                         unsigned long long *cr = &sh.a.cand[r][static_cast<int>(rank) * capc];
                         uint32_t slot = atomicAdd(&sh.lcnt[r], static_cast<uint32_t>(__popc(msk)));
@@ -1110,28 +1237,50 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 };
                 if (nrows > 1 && sh.mode[0] == 1 && sh.mode[1] == 1) {
                     // both rows in one sweep
-                    const float tzbA = sh.tzb[0], f1A = static_cast<float>(sh.b1[0]), f2A = static_cast<float>(sh.b2[0] + 1);
-                    const float tzbB = sh.tzb[1], f1B = static_cast<float>(sh.b1[1]), f2B = static_cast<float>(sh.b2[1] + 1);
+                    if (kfast) {
+                        const float bA = sh.kbd[0], bB = sh.kbd[1];
 #pragma unroll 2
-                    for (int v = tid; v < nvr; v += NT) {
-                        float xa[EPV], xb[EPV];
-                        unpack(sv0[v], xa);
-                        unpack(sv1[v], xb);
-                        gather_vec(0, v, xa, tzbA, f1A, f2A);
-                        gather_vec(1, v, xb, tzbB, f1B, f2B);
+                        for (int v = tid; v < nvr; v += NT) {
+                            float xa[EPV], xb[EPV];
+                            unpack(sv0[v], xa);
+                            unpack(sv1[v], xb);
+                            put(0, v, xa, at_least(xa, bA));
+                            put(1, v, xb, at_least(xb, bB));
+                        }
+                    } else {
+                        const float tzbA = sh.tzb[0], f1A = static_cast<float>(sh.b1[0]), f2A = static_cast<float>(sh.b2[0] + 1);
+                        const float tzbB = sh.tzb[1], f1B = static_cast<float>(sh.b1[1]), f2B = static_cast<float>(sh.b2[1] + 1);
+#pragma unroll 2
+                        for (int v = tid; v < nvr; v += NT) {
+                            float xa[EPV], xb[EPV];
+                            unpack(sv0[v], xa);
+                            unpack(sv1[v], xb);
+                            put(0, v, xa, in_bins(xa, tzbA, f1A, f2A));
+                            put(1, v, xb, in_bins(xb, tzbB, f1B, f2B));
+                        }
                     }
                 } else {
 #pragma unroll 1
                     for (int r = 0; r < nrows; ++r) {
                         if (sh.mode[r] != 1) continue;
-                        const float tzb = sh.tzb[r];
-                        const float fb1 = static_cast<float>(sh.b1[r]), fb2 = static_cast<float>(sh.b2[r] + 1);
                         const uint4 *vp = reinterpret_cast<const uint4 *>(sdat(r));
+                        if (kfast) {
+                            const float bnd = sh.kbd[r];
 #pragma unroll 2
-                        for (int v = tid; v < nvr; v += NT) {
-                            float x[EPV];
-                            unpack(vp[v], x);
-                            gather_vec(r, v, x, tzb, fb1, fb2);
+                            for (int v = tid; v < nvr; v += NT) {
+                                float x[EPV];
+                                unpack(vp[v], x);
+                                put(r, v, x, at_least(x, bnd));
+                            }
+                        } else {
+                            const float tzb = sh.tzb[r];
+                            const float fb1 = static_cast<float>(sh.b1[r]), fb2 = static_cast<float>(sh.b2[r] + 1);
+#pragma unroll 2
+                            for (int v = tid; v < nvr; v += NT) {
+                                float x[EPV];
+                                unpack(vp[v], x);
+                                put(r, v, x, in_bins(x, tzb, fb1, fb2));
+                            }
                         }
                     }
                 }
@@ -1650,12 +1799,10 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             const uint4 *sv0 = reinterpret_cast<const uint4 *>(sdat(0));
             const uint4 *sv1 = reinterpret_cast<const uint4 *>(sdat(1));
             auto vec_weight = [&](int v) -> uint32_t {
+                const uint4 rx = sv0[v];
+                if (!(vec_max<T>(rx) >= th0)) return 0u;  // no target logit of the vector is kept
                 float x[EPV], y[EPV];
-                unpack(sv0[v], x);
-                float xm = x[0];
-#pragma unroll
-                for (int e = 1; e < EPV; ++e) xm = fmaxf(xm, x[e]);
-                if (!(xm >= th0)) return 0u;  // no target logit of the vector is kept
+                unpack(rx, x);
                 unpack(sv1[v], y);
                 uint32_t s = 0;
 #pragma unroll
