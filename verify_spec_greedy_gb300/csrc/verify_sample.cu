@@ -35,6 +35,10 @@
 //   E2       reduce-scatter of the histograms to owner CTAs, then all-gather of the sums
 //   plan     the bins that may hold the boundary: by exact counts (top-k) or by rigorous
 //            bounds on the cumulative weight (top-p)
+//            A top-k row with k <= KFAST skips its sums, pass 2, E2 and the plan: pass 1
+//            also finds a lower bound on each CTA's k-th largest logit (a radix selection
+//            over the threads' maxima), E1 carries the bounds, and the gather takes every
+//            element at or above the cluster's bound.
 //   gather   elements of those bins go to every CTA (E3); the candidates, compacted with
 //            their exact weights, are ranked by counting (or sorted, when there are many)
 //            for the exact thresholds.  If the boundary lies outside the binned range or too
