@@ -509,7 +509,10 @@ __device__ __forceinline__ bool row_sampled(const Params &P, int64_t b) {
 
 // ---------------------------------------------------------------- the persistent kernel
 
-template <typename T>
+// KT: the call passes per-row top-k values.  Without them no row has a top-k filter, and
+// the top-k paths (counting histograms, the bound of small k, the draw from candidates)
+// compile out of the instance that runs.
+template <typename T, bool KT>
 __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Shared &sh = *reinterpret_cast<Shared *>(smem_raw);
@@ -733,7 +736,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         const float tau = cur.tau, pp = cur.pp;
         const int32_t kk = cur.kk, d = cur.d;
         const int nrows = j < D && !one_hot ? 2 : 1;
-        const bool k_on = kk >= 1 && kk < V;
+        const bool k_on = KT && kk >= 1 && kk < V;
         const bool p_on = pp < 1.0f;
         const bool kfast = k_on && kk <= KFAST;
         const float c2 = __fdiv_rn(1.44269504088896340736f, tau);
@@ -1774,7 +1777,12 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         for (uint32_t c = 0; c < C; ++c) dkmin = min(dkmin, sh.e1k[ep][c]);
         // the slice buffer is free unless a draw reads it: bring in the next unit now
         const bool draw = ((j == D) || !accept) && !(dkmin < static_cast<uint32_t>(j));
-        if (!draw && un >= 0) issue(nxt.b, nxt.j, true);
+        // A top-k row resolved from its candidates holds every kept element among them, in
+        // every CTA (and so does the draft row when its residual needs q): such a draw reads
+        // no slice
+        const bool qpoint = one_hot || deg1;  // the draft is a point mass (q = 0 elsewhere)
+        const bool local = kfast && sh.mode[0] == 1 && (j == D || qpoint || sh.mode[1] == 1);
+        if ((!draw || local) && un >= 0) issue(nxt.b, nxt.j, true);
 
         // ---- draw (a rejected draft's residual, or the bonus).  Weights in fixed point,
         // summed as integers: the cumulative sums at every level (lane, warp, CTA, cluster)
@@ -1784,11 +1792,95 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         UnitResult *res = P.res + (static_cast<int64_t>(b) * (D + 1) + j);
         if (draw && deg0) {
             if (rank == 0 && tid == 0) res->token = 0;
+        } else if (draw && local) {
+            if (rank == 0) {
+                // CTA 0 alone, from the gathered candidates: the kept target elements (value
+                // >= theta0) in id order, the draft logit of each where the draft keeps that
+                // id (else q = 0), then the weights the sweep below would form, summed in id
+                // order as integers, so the token is the one the sweep would draw
+                unsigned long long *kl = sh.b.s.skey;      // kept, as found: id << 32 | x bits
+                unsigned long long *sl = &sh.a.cand[0][0];  // kept, in id order
+                float *qx = sh.b.s.sval;                    // draft logit at sl[k], or -inf
+                const int nslot = static_cast<int>(C) * capc;
+                if (tid == 0) sh.lcnt[0] = 0;
+                __syncthreads();
+                for (int t = tid; t < nslot; t += NT) {
+                    const int c = t / capc, i = t - c * capc;
+                    if (i < static_cast<int>(min(sh.ccnt[c][0], static_cast<uint32_t>(capc)))) {
+                        const unsigned long long cv = sh.a.cand[0][t];
+                        const uint32_t xb = static_cast<uint32_t>(cv >> 32);
+                        if (__uint_as_float(xb) >= th0)
+                            kl[atomicAdd(&sh.lcnt[0], 1u)] = (static_cast<unsigned long long>(static_cast<uint32_t>(cv)) << 32) | xb;
+                    }
+                }
+                __syncthreads();
+                const int nk = static_cast<int>(sh.lcnt[0]);
+                for (int k = tid; k < nk; k += NT) {  // rank by id (ids are distinct)
+                    const unsigned long long me = kl[k];
+                    int rk = 0;
+                    for (int q = 0; q < nk; ++q) rk += (kl[q] >> 32) < (me >> 32) ? 1 : 0;
+                    sl[rk] = me;
+                    qx[rk] = -INFINITY;
+                }
+                __syncthreads();
+                if (j < D && !qpoint) {
+                    for (int t = tid; t < nslot; t += NT) {
+                        const int c = t / capc, i = t - c * capc;
+                        if (i < static_cast<int>(min(sh.ccnt[c][1], static_cast<uint32_t>(capc)))) {
+                            const unsigned long long cv = sh.a.cand[1][t];
+                            const float xq = __uint_as_float(static_cast<uint32_t>(cv >> 32));
+                            const uint32_t id = static_cast<uint32_t>(cv);
+                            if (xq >= th1) {
+                                int l0 = 0, l1 = nk;  // the first kept id >= id
+                                while (l0 < l1) {
+                                    const int m = (l0 + l1) >> 1;
+                                    if (static_cast<uint32_t>(sl[m] >> 32) < id) l0 = m + 1;
+                                    else l1 = m;
+                                }
+                                if (l0 < nk && static_cast<uint32_t>(sl[l0] >> 32) == id) qx[l0] = xq;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+                const int pmid = one_hot ? d : 0;  // the point draft's id
+                int wmode = (j == D) ? 1 : 0;      // 0: max(0, p - q), 1: p
+                // (a kept set always carries weight; should rounding leave none, the lowest
+                // kept id stands; the crossing element's id overwrites it below)
+                if (tid == 0) res->token = nk > 0 ? static_cast<int>(sl[0] >> 32) : 0;
+#pragma unroll 1
+                for (int attempt = 0; attempt < 2; ++attempt) {
+                    unsigned long long w = 0;
+                    int myid = 0;
+                    if (tid < nk) {
+                        const unsigned long long e = sl[tid];
+                        myid = static_cast<int>(e >> 32);
+                        float pw = ex2(fmaf(__uint_as_float(static_cast<uint32_t>(e)), c2, nm0)) * iz0;
+                        if (wmode == 0) {
+                            if (qpoint) {
+                                if (myid == pmid) pw = 0.0f;
+                            } else if (qx[tid] > -INFINITY) {
+                                pw = fmaxf(pw - ex2(fmaf(qx[tid], c2, nm1)) * iz1, 0.0f);
+                            }
+                        }
+                        w = fix31(pw);
+                    }
+                    const unsigned long long before = block_excl_scan_u64(w, sh.w.so.scan);
+                    const unsigned long long Rt = block_sum_u64(w, sh.w.so.ru[0]);
+                    if (Rt > 0 || wmode == 1) {
+                        // the smallest id whose cumulative weight exceeds u_smp * R (see below)
+                        const unsigned long long tt =
+                            (static_cast<unsigned long long>(2u * (uw1 >> 9) + 1u) * Rt) >> 24;
+                        if (w > 0 && before <= tt && before + w > tt) res->token = myid;
+                        break;
+                    }
+                    wmode = 1;  // the residual is identically zero: draw from p instead
+                }
+            }
         } else if (draw) {
             int wmode = (j == D) ? 1 : 0;  // 0: max(0, p - q), 1: p
             // a point-mass draft (a one-hot draft on d, or a degenerate draft row on id 0):
             // q = 0 elsewhere, and at its id the residual is p - 1 <= 0
-            const bool qpoint = one_hot || deg1;
             const float thq = qpoint ? INFINITY : th1;
             const int pm = one_hot ? d : 0;  // the point's id
             const bool pm_here = qpoint && pm >= lo && pm < lo + n;
@@ -1971,7 +2063,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             if (P.status && j < D && !dvalid) atomicOr(P.status, MTPSPEC_STATUS_BAD_DRAFT_ID);
         }
         __syncthreads();  // every thread is done with this unit's shared state
-        if (draw && un >= 0) issue(nxt.b, nxt.j, true);
+        if (draw && !local && un >= 0) issue(nxt.b, nxt.j, true);
         u = un;
         cnx = nxt;
         un = sh.e1su[ep];  // CTA 0's choice, sent with this unit's E1 (rewritten two E1s later)
@@ -2111,7 +2203,7 @@ static int resident_clusters(int C, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, vs::k_verify_rr<T>, &cfg) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveClusters(&n, vs::k_verify_rr<T, true>, &cfg) != cudaSuccess || n < 1)
         n = 1;
     const int i = used < NC ? used++ : NC - 1;
     dev_of[i] = dev;
@@ -2158,19 +2250,25 @@ static VerifyGeometry verify_geometry(int64_t V, int64_t units, int rows) {
     return gm;
 }
 
+// The kernel may take the largest shared memory and clusters up to MAXC (the occupancy
+// queries of the geometry need both, on the instance with the top-k paths).
+template <typename T, bool KT>
+static cudaError_t prepare_verify_rr() {
+    static AttrCache a_smem, a_carve, a_cluster;
+    cudaError_t e = ensure_attr(vs::k_verify_rr<T, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kSmemLimit), a_smem);
+    if (e != cudaSuccess) return e;
+    e = ensure_attr(vs::k_verify_rr<T, KT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                    static_cast<int>(cudaSharedmemCarveoutMaxShared), a_carve);
+    if (e != cudaSuccess) return e;
+    return ensure_attr(vs::k_verify_rr<T, KT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1, a_cluster);
+}
+
 template <typename T>
 static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     const int64_t units = p.B * (p.D + 1);
-    // the kernel may take the largest shared memory and clusters up to MAXC (the occupancy
-    // queries of the geometry need both)
-    static AttrCache a_smem, a_carve, a_cluster;
-    cudaError_t e = ensure_attr(vs::k_verify_rr<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kSmemLimit), a_smem);
-    if (e != cudaSuccess) return e;
-    e = ensure_attr(vs::k_verify_rr<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                    static_cast<int>(cudaSharedmemCarveoutMaxShared), a_carve);
-    if (e != cudaSuccess) return e;
-    e = ensure_attr(vs::k_verify_rr<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1, a_cluster);
+    cudaError_t e = prepare_verify_rr<T, true>();
+    if (e == cudaSuccess && !p.topk) e = prepare_verify_rr<T, false>();
     if (e != cudaSuccess) return e;
     const int rows = p.Q ? 2 : 1;
     const VerifyGeometry gm = verify_geometry<T>(p.V, units, rows);
@@ -2208,7 +2306,8 @@ static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, vs::k_verify_rr<T>, p);
+    e = p.topk ? cudaLaunchKernelEx(&cfg, vs::k_verify_rr<T, true>, p)
+               : cudaLaunchKernelEx(&cfg, vs::k_verify_rr<T, false>, p);
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
