@@ -328,14 +328,28 @@ def test_long_drafts(V, D, dtype):
     compare(g, o, x, label=f"V={V} D={D} {dtype}")
 
 
-@pytest.mark.parametrize("one_hot", [False, True])
-def test_outputs_without_probabilities_equal_those_with(one_hot):
+WITHOUT_P = {
+    # the serving mix (its sampled rows are top-p only)
+    "serve": lambda: WORKLOADS["serve_b256_d3_v152k"].scaled(B=96, seed=61, philox_seed=67),
+    # bf16 top-p rows, four drafts
+    "topp_bf16": lambda: Workload(name="tpb", B=64, D=4, V=65537, H=8, dtype="bf16",
+                                  tau_range=(0.5, 1.5), top_p=0.95, t_std=3.0,
+                                  q_noise_range=(0.2, 1.5), seed=71, philox_seed=73),
+    # drafts close to their targets: most drafts accepted
+    "topp_close": lambda: Workload(name="tpc", B=128, D=3, V=30011, H=8, tau_range=(0.6, 1.2),
+                                   top_p=0.8, t_std=3.0, q_noise=0.1, seed=81, philox_seed=83),
+}
+
+
+@pytest.mark.parametrize("case,one_hot", [("serve", False), ("serve", True),
+                                          ("topp_bf16", False), ("topp_close", False)])
+def test_outputs_without_probabilities_equal_those_with(case, one_hot):
     # without p_target and p_draft only the positions up to each row's first rejection are
-    # read, so a unit behind a rejection the cluster already knows of is skipped; the
-    # tokens and accepted counts must be the same, bit for bit, as when every position's
-    # probabilities are requested (units position-major at this batch size)
-    w = WORKLOADS["serve_b256_d3_v152k"].scaled(B=96, seed=61, philox_seed=67)
-    x = make_verify_inputs(w)
+    # read, so a unit behind a rejection the cluster already knows of is skipped, and a
+    # draft whose acceptance is certain before the thresholds skips them; the tokens and
+    # accepted counts must be the same, bit for bit, as when every position's
+    # probabilities are requested (units position-major at these batch sizes)
+    x = make_verify_inputs(WITHOUT_P[case]())
     if one_hot:
         x = _greedy_half(x, np.random.default_rng(61))
     B, D = x["d"].shape
@@ -363,4 +377,4 @@ def test_outputs_without_probabilities_equal_those_with(one_hot):
     g = dict(out=o1, num_accepted=n1, p_target=pt.cpu().numpy(), p_draft=pd.cpu().numpy(), status=s1)
     rows = list(range(0, B, 3))
     compare(g, oracle_verify(x, rows=rows, one_hot=one_hot), x, rows=rows,
-            label=f"with probabilities, one_hot={one_hot}", one_hot=one_hot)
+            label=f"{case} with probabilities, one_hot={one_hot}", one_hot=one_hot)

@@ -207,6 +207,7 @@ struct __align__(16) Shared {
     int32_t e1su[2];
     // top-k rows with a small k: per row, the cluster's lower bound on the k-th largest logit
     float kbd[2];
+    int32_t early;    // the unit's draft is certainly accepted before its thresholds (see below)
     NextParams e1sp[2];
 };
 // The state above fills the padding before e1sp: the staged slices keep their room.
@@ -935,6 +936,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         uint32_t dk1 = 0xFFFFFFFFu;
         for (uint32_t c = 0; c < C; ++c) dk1 = min(dk1, sh.e1k[ep][c]);
         const bool dead_unit = (j == D || !P.need_p) && dk1 < static_cast<uint32_t>(j);
+        bool early = false;  // the draft's acceptance is already certain (see below)
         if (filt && !dead_unit) {
             if (!kfast) {
                 // ---- pass 2: histogram of the elements in the bins that can hold the boundary.
@@ -1205,519 +1207,577 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 __syncthreads();
             }
 
-            // ---- gather the boundary candidates into every CTA (E3)
-            const bool any_fast = sh.mode[0] == 1 || (nrows > 1 && sh.mode[1] == 1);
-            if (any_fast) {
-                // the candidates of row r: elements of bins [b1, b2] (bin bn = trunc(tz):
-                // bn >= b1 iff tz >= b1, bn <= b2 iff tz < b2 + 1), or, for a top-k row with a
-                // small k, every element at or above the row's bound; a vector that holds
-                // candidates claims their slots at once (the order of the slots does not
-                // matter: every later step depends on values)
-                const float tza = -c2 * static_cast<float>(R);
-                auto in_bins = [&](const float (&x)[EPV], float tzb, float fb1, float fb2) -> uint32_t {
-                    uint32_t msk = 0;
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        const float tz = fmaxf(fmaf(x[e], tza, tzb), 0.0f);
-                        msk |= (tz >= fb1 && tz < fb2) ? (1u << e) : 0u;
+            // ---- A decode loop reads a draft position's record only for its accept flag when
+            // the draft is accepted.  After the plan every CTA holds rigorous bounds on each
+            // row's kept mass: at least the top-p target (the kept groups reach it) and less
+            // than the target plus the boundary bins' weight (the last kept group lies among
+            // them), with a relative slack for the sums' rounding.  When the draft token's bin
+            // lies before the boundary bins (kept for sure), and U_acc lies below the ratio's
+            // lower bound (or the draft surely drops the token: q(d) = 0), the acceptance is
+            // certain: the gather and the thresholds are skipped, and the staged rows are
+            // released at once.  Every CTA decides from the same exchanged values.
+            if (!P.need_p && j < D && dvalid && !k_on && p_on) {
+                if (tid == 0) {
+                    const float tza = -c2 * static_cast<float>(R);
+                    const float2 xdv = sh.e1d[ep];
+                    auto tz_of = [&](float x, int r) { return fmaxf(fmaf(x, tza, sh.tzb[r]), 0.0f); };
+                    // the row's kept mass, as the thresholds would give it, lies in [lo, hi]
+                    auto zb = [&](int r, float &lo, float &hi) {
+                        const unsigned long long t = sh.tgt[r];
+                        unsigned long long extra = 0;
+                        const int nbu = sh.nbu[r];
+                        for (int bn = sh.b1[r]; bn <= sh.b2[r] && bn < nbu; ++bn) {
+                            unsigned long long mid, err;
+                            uint32_t cnt;
+                            bin_bounds(sh.b.hist[r][(bn % BPL) * PL + bn / BPL], bn, mid, err, cnt);
+                            extra += mid + err + cnt;
+                        }
+                        lo = fx_to_float(t) * (1.0f - 1e-4f);
+                        hi = fx_to_float(t + extra) * (1.0f + 1e-4f);
+                    };
+                    const float u = word_uniform(sh.uwd[0]);
+                    bool ok = !sh.deg[0] && sh.mode[0] == 1 && tz_of(xdv.x, 0) < static_cast<float>(sh.b1[0]);
+                    if (ok) {
+                        float z0lo, z0hi;
+                        zb(0, z0lo, z0hi);
+                        if (one_hot) {
+                            ok = u <= ex2(fmaf(xdv.x, c2, sh.nmc[0])) / z0hi * (1.0f - 1e-4f);
+                        } else if (sh.deg[1] || sh.mode[1] != 1) {
+                            ok = false;
+                        } else {
+                            const float tq = tz_of(xdv.y, 1);
+                            if (tq >= static_cast<float>(sh.b2[1] + 1)) {
+                                ok = true;  // q(d) = 0
+                            } else if (tq < static_cast<float>(sh.b1[1])) {
+                                float z1lo, z1hi;
+                                zb(1, z1lo, z1hi);
+                                const float r0 = ex2(__fmul_rn((xdv.x - sh.m[0]) - (xdv.y - sh.m[1]), c2));
+                                ok = u <= r0 * (z1lo / z0hi) * (1.0f - 1e-4f);
+                            } else {
+                                ok = false;
+                            }
+                        }
                     }
-                    return msk;
-                };
-                auto at_least = [&](const float (&x)[EPV], float bnd) -> uint32_t {
-                    uint32_t msk = 0;
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) msk |= x[e] >= bnd ? (1u << e) : 0u;
-                    return msk;
-                };
-                auto put = [&](int r, int v, const float (&x)[EPV], uint32_t msk) {
-                    if (msk) {
-                        unsigned long long *cr = &sh.a.cand[r][static_cast<int>(rank) * capc];
-                        uint32_t slot = atomicAdd(&sh.lcnt[r], static_cast<uint32_t>(__popc(msk)));
+                    sh.early = ok ? 1 : 0;
+                }
+                __syncthreads();
+                early = sh.early != 0;
+            }
+            if (!early) {
+                // ---- gather the boundary candidates into every CTA (E3)
+                const bool any_fast = sh.mode[0] == 1 || (nrows > 1 && sh.mode[1] == 1);
+                if (any_fast) {
+                    // the candidates of row r: elements of bins [b1, b2] (bin bn = trunc(tz):
+                    // bn >= b1 iff tz >= b1, bn <= b2 iff tz < b2 + 1), or, for a top-k row with a
+                    // small k, every element at or above the row's bound; a vector that holds
+                    // candidates claims their slots at once (the order of the slots does not
+                    // matter: every later step depends on values)
+                    const float tza = -c2 * static_cast<float>(R);
+                    auto in_bins = [&](const float (&x)[EPV], float tzb, float fb1, float fb2) -> uint32_t {
+                        uint32_t msk = 0;
 #pragma unroll
                         for (int e = 0; e < EPV; ++e) {
-                            if (((msk >> e) & 1u) && slot < static_cast<uint32_t>(capc))
-                                cr[slot] = (static_cast<unsigned long long>(__float_as_uint(x[e])) << 32) |
-                                           static_cast<uint32_t>(lo + v * EPV + e);
-                            slot += (msk >> e) & 1u;
+                            const float tz = fmaxf(fmaf(x[e], tza, tzb), 0.0f);
+                            msk |= (tz >= fb1 && tz < fb2) ? (1u << e) : 0u;
                         }
-                    }
-                };
-                if (nrows > 1 && sh.mode[0] == 1 && sh.mode[1] == 1) {
-                    // both rows in one sweep
-                    if (kfast) {
-                        const float bA = sh.kbd[0], bB = sh.kbd[1];
+                        return msk;
+                    };
+                    auto at_least = [&](const float (&x)[EPV], float bnd) -> uint32_t {
+                        uint32_t msk = 0;
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) msk |= x[e] >= bnd ? (1u << e) : 0u;
+                        return msk;
+                    };
+                    auto put = [&](int r, int v, const float (&x)[EPV], uint32_t msk) {
+                        if (msk) {
+                            unsigned long long *cr = &sh.a.cand[r][static_cast<int>(rank) * capc];
+                            uint32_t slot = atomicAdd(&sh.lcnt[r], static_cast<uint32_t>(__popc(msk)));
+#pragma unroll
+                            for (int e = 0; e < EPV; ++e) {
+                                if (((msk >> e) & 1u) && slot < static_cast<uint32_t>(capc))
+                                    cr[slot] = (static_cast<unsigned long long>(__float_as_uint(x[e])) << 32) |
+                                               static_cast<uint32_t>(lo + v * EPV + e);
+                                slot += (msk >> e) & 1u;
+                            }
+                        }
+                    };
+                    if (nrows > 1 && sh.mode[0] == 1 && sh.mode[1] == 1) {
+                        // both rows in one sweep
+                        if (kfast) {
+                            const float bA = sh.kbd[0], bB = sh.kbd[1];
 #pragma unroll 2
-                        for (int v = tid; v < nvr; v += NT) {
-                            float xa[EPV], xb[EPV];
-                            unpack(sv0[v], xa);
-                            unpack(sv1[v], xb);
-                            put(0, v, xa, at_least(xa, bA));
-                            put(1, v, xb, at_least(xb, bB));
+                            for (int v = tid; v < nvr; v += NT) {
+                                float xa[EPV], xb[EPV];
+                                unpack(sv0[v], xa);
+                                unpack(sv1[v], xb);
+                                put(0, v, xa, at_least(xa, bA));
+                                put(1, v, xb, at_least(xb, bB));
+                            }
+                        } else {
+                            const float tzbA = sh.tzb[0], f1A = static_cast<float>(sh.b1[0]), f2A = static_cast<float>(sh.b2[0] + 1);
+                            const float tzbB = sh.tzb[1], f1B = static_cast<float>(sh.b1[1]), f2B = static_cast<float>(sh.b2[1] + 1);
+#pragma unroll 2
+                            for (int v = tid; v < nvr; v += NT) {
+                                float xa[EPV], xb[EPV];
+                                unpack(sv0[v], xa);
+                                unpack(sv1[v], xb);
+                                put(0, v, xa, in_bins(xa, tzbA, f1A, f2A));
+                                put(1, v, xb, in_bins(xb, tzbB, f1B, f2B));
+                            }
                         }
                     } else {
-                        const float tzbA = sh.tzb[0], f1A = static_cast<float>(sh.b1[0]), f2A = static_cast<float>(sh.b2[0] + 1);
-                        const float tzbB = sh.tzb[1], f1B = static_cast<float>(sh.b1[1]), f2B = static_cast<float>(sh.b2[1] + 1);
+#pragma unroll 1
+                        for (int r = 0; r < nrows; ++r) {
+                            if (sh.mode[r] != 1) continue;
+                            const uint4 *vp = reinterpret_cast<const uint4 *>(sdat(r));
+                            if (kfast) {
+                                const float bnd = sh.kbd[r];
 #pragma unroll 2
-                        for (int v = tid; v < nvr; v += NT) {
-                            float xa[EPV], xb[EPV];
-                            unpack(sv0[v], xa);
-                            unpack(sv1[v], xb);
-                            put(0, v, xa, in_bins(xa, tzbA, f1A, f2A));
-                            put(1, v, xb, in_bins(xb, tzbB, f1B, f2B));
+                                for (int v = tid; v < nvr; v += NT) {
+                                    float x[EPV];
+                                    unpack(vp[v], x);
+                                    put(r, v, x, at_least(x, bnd));
+                                }
+                            } else {
+                                const float tzb = sh.tzb[r];
+                                const float fb1 = static_cast<float>(sh.b1[r]), fb2 = static_cast<float>(sh.b2[r] + 1);
+#pragma unroll 2
+                                for (int v = tid; v < nvr; v += NT) {
+                                    float x[EPV];
+                                    unpack(vp[v], x);
+                                    put(r, v, x, in_bins(x, tzb, fb1, fb2));
+                                }
+                            }
                         }
                     }
-                } else {
+                    __syncthreads();
+                    // ---- push this CTA's candidates into the other CTAs' copies of its slots
 #pragma unroll 1
                     for (int r = 0; r < nrows; ++r) {
                         if (sh.mode[r] != 1) continue;
-                        const uint4 *vp = reinterpret_cast<const uint4 *>(sdat(r));
-                        if (kfast) {
-                            const float bnd = sh.kbd[r];
-#pragma unroll 2
-                            for (int v = tid; v < nvr; v += NT) {
-                                float x[EPV];
-                                unpack(vp[v], x);
-                                put(r, v, x, at_least(x, bnd));
-                            }
-                        } else {
-                            const float tzb = sh.tzb[r];
-                            const float fb1 = static_cast<float>(sh.b1[r]), fb2 = static_cast<float>(sh.b2[r] + 1);
-#pragma unroll 2
-                            for (int v = tid; v < nvr; v += NT) {
-                                float x[EPV];
-                                unpack(vp[v], x);
-                                put(r, v, x, in_bins(x, tzb, fb1, fb2));
-                            }
+                        const int nl = min(static_cast<int>(sh.lcnt[r]), capc);
+                        const int np = static_cast<int>(C) - 1;
+                        for (int q = tid; q < nl * np; q += NT) {
+                            const int i = q / np, c0 = q - i * np;
+                            const uint32_t c = c0 >= static_cast<int>(rank) ? static_cast<uint32_t>(c0 + 1)
+                                                                             : static_cast<uint32_t>(c0);
+                            unsigned long long *slot = &sh.a.cand[r][static_cast<int>(rank) * capc + i];
+                            st_peer_u64(peer_addr(smem_addr(slot), c), *slot);
                         }
                     }
-                }
-                __syncthreads();
-                // ---- push this CTA's candidates into the other CTAs' copies of its slots
-#pragma unroll 1
-                for (int r = 0; r < nrows; ++r) {
-                    if (sh.mode[r] != 1) continue;
-                    const int nl = min(static_cast<int>(sh.lcnt[r]), capc);
-                    const int np = static_cast<int>(C) - 1;
-                    for (int q = tid; q < nl * np; q += NT) {
-                        const int i = q / np, c0 = q - i * np;
-                        const uint32_t c = c0 >= static_cast<int>(rank) ? static_cast<uint32_t>(c0 + 1)
-                                                                         : static_cast<uint32_t>(c0);
-                        unsigned long long *slot = &sh.a.cand[r][static_cast<int>(rank) * capc + i];
-                        st_peer_u64(peer_addr(smem_addr(slot), c), *slot);
+                    __syncthreads();
+                    if (tid < static_cast<int>(C)) {
+                        for (int r = 0; r < 2; ++r)
+                            st_peer_u32(peer_addr(smem_addr(&sh.ccnt[rank][r]), tid), sh.lcnt[r]);
+                        xarrive(&sh.xbar[XB_E3], tid);
                     }
-                }
-                __syncthreads();
-                if (tid < static_cast<int>(C)) {
-                    for (int r = 0; r < 2; ++r)
-                        st_peer_u32(peer_addr(smem_addr(&sh.ccnt[rank][r]), tid), sh.lcnt[r]);
-                    xarrive(&sh.xbar[XB_E3], tid);
-                }
-                xwait(XB_E3);
+                    xwait(XB_E3);
 
-                // ---- exact thresholds.  Every warp, per row (lane c holding CTA c's count):
-                // the candidates' number, the CTAs' offsets in the row's list, and whether
-                // the row can be ranked by its plan group (1 to PL candidates, no CTA over its
-                // slots)
-                uint32_t ccl[2], cpl[2];
-                int ncnt[2];
-                bool grp = true;
+                    // ---- exact thresholds.  Every warp, per row (lane c holding CTA c's count):
+                    // the candidates' number, the CTAs' offsets in the row's list, and whether
+                    // the row can be ranked by its plan group (1 to PL candidates, no CTA over its
+                    // slots)
+                    uint32_t ccl[2], cpl[2];
+                    int ncnt[2];
+                    bool grp = true;
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const bool on = r < nrows && sh.mode[r] == 1;
-                    const uint32_t cc = on && lane < static_cast<int>(C) ? sh.ccnt[lane][r] : 0u;
-                    const bool over = __any_sync(0xFFFFFFFFu, cc > static_cast<uint32_t>(capc));
-                    uint32_t incl = cc;
+                    for (int r = 0; r < 2; ++r) {
+                        const bool on = r < nrows && sh.mode[r] == 1;
+                        const uint32_t cc = on && lane < static_cast<int>(C) ? sh.ccnt[lane][r] : 0u;
+                        const bool over = __any_sync(0xFFFFFFFFu, cc > static_cast<uint32_t>(capc));
+                        uint32_t incl = cc;
 #pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                        if (lane >= o) incl += y;
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                            if (lane >= o) incl += y;
+                        }
+                        ccl[r] = cc;
+                        cpl[r] = incl - cc;
+                        ncnt[r] = static_cast<int>(__shfl_sync(0xFFFFFFFFu, incl, 31));
+                        if (on && (over || ncnt[r] == 0 || ncnt[r] > PL)) grp = false;
                     }
-                    ccl[r] = cc;
-                    cpl[r] = incl - cc;
-                    ncnt[r] = static_cast<int>(__shfl_sync(0xFFFFFFFFu, incl, 31));
-                    if (on && (over || ncnt[r] == 0 || ncnt[r] > PL)) grp = false;
-                }
-                if (grp) {
-                    // ---- rank by counting in the plan's groups (PW warps a row): lane jj
-                    // fetches candidate jj and its fixed-point weight; then S lanes a
-                    // candidate sum the weight and number of the candidates strictly above
-                    // it; the row's reductions go through its group barrier
-                    const int r = warp / PW, jj = tid - r * PL;
-                    if (warp < 2 * PW && r < nrows && sh.mode[r] == 1) {
-                        const int nr = ncnt[r];
-                        const uint32_t cpr = r == 0 ? cpl[0] : cpl[1], ccr = r == 0 ? ccl[0] : ccl[1];
-                        // candidate jj's CTA: the last with candidates whose offset is <= jj
-                        int c = 0;
-                        for (int k = 1; k < static_cast<int>(C); ++k) {
-                            const uint32_t pk = __shfl_sync(0xFFFFFFFFu, cpr, k);
-                            const uint32_t ck = __shfl_sync(0xFFFFFFFFu, ccr, k);
-                            if (static_cast<uint32_t>(jj) >= pk && ck > 0u) c = k;
-                        }
-                        const uint32_t pre_c = __shfl_sync(0xFFFFFFFFu, cpr, c);
-                        float *cv = sh.b.s.sval + r * PL;
-                        uint32_t *cw = reinterpret_cast<uint32_t *>(sh.b.s.skey) + r * PL;
-                        if (jj < nr) {
-                            const float vj = __uint_as_float(static_cast<uint32_t>(
-                                sh.a.cand[r][c * capc + jj - static_cast<int>(pre_c)] >> 32));
-                            cv[jj] = vj;
-                            cw[jj] = fix31(ex2(fmaf(vj, c2, sh.nmc[r])));
-                        }
-                        group_barrier<PL>(r);
-                        int p2 = 1;
-                        while (p2 < nr) p2 <<= 1;
-                        const int S = min(32, PL / p2);
-                        const int i = jj / S, sub = jj - i * S;
-                        const bool real = i < nr;
-                        const float v = real ? cv[i] : -INFINITY;
-                        const uint32_t w = real ? cw[i] : 0u;
-                        unsigned long long sgt = 0;
-                        int cgt = 0;
-                        if (real) {
+                    if (grp) {
+                        // ---- rank by counting in the plan's groups (PW warps a row): lane jj
+                        // fetches candidate jj and its fixed-point weight; then S lanes a
+                        // candidate sum the weight and number of the candidates strictly above
+                        // it; the row's reductions go through its group barrier
+                        const int r = warp / PW, jj = tid - r * PL;
+                        if (warp < 2 * PW && r < nrows && sh.mode[r] == 1) {
+                            const int nr = ncnt[r];
+                            const uint32_t cpr = r == 0 ? cpl[0] : cpl[1], ccr = r == 0 ? ccl[0] : ccl[1];
+                            // candidate jj's CTA: the last with candidates whose offset is <= jj
+                            int c = 0;
+                            for (int k = 1; k < static_cast<int>(C); ++k) {
+                                const uint32_t pk = __shfl_sync(0xFFFFFFFFu, cpr, k);
+                                const uint32_t ck = __shfl_sync(0xFFFFFFFFu, ccr, k);
+                                if (static_cast<uint32_t>(jj) >= pk && ck > 0u) c = k;
+                            }
+                            const uint32_t pre_c = __shfl_sync(0xFFFFFFFFu, cpr, c);
+                            float *cv = sh.b.s.sval + r * PL;
+                            uint32_t *cw = reinterpret_cast<uint32_t *>(sh.b.s.skey) + r * PL;
+                            if (jj < nr) {
+                                const float vj = __uint_as_float(static_cast<uint32_t>(
+                                    sh.a.cand[r][c * capc + jj - static_cast<int>(pre_c)] >> 32));
+                                cv[jj] = vj;
+                                cw[jj] = fix31(ex2(fmaf(vj, c2, sh.nmc[r])));
+                            }
+                            group_barrier<PL>(r);
+                            int p2 = 1;
+                            while (p2 < nr) p2 <<= 1;
+                            const int S = min(32, PL / p2);
+                            const int i = jj / S, sub = jj - i * S;
+                            const bool real = i < nr;
+                            const float v = real ? cv[i] : -INFINITY;
+                            const uint32_t w = real ? cw[i] : 0u;
+                            unsigned long long sgt = 0;
+                            int cgt = 0;
+                            if (real) {
 #pragma unroll 4
-                            for (int q = sub; q < nr; q += S) {
-                                if (cv[q] > v) {
-                                    sgt += cw[q];
-                                    ++cgt;
-                                }
-                            }
-                        }
-                        for (int o = S >> 1; o > 0; o >>= 1) {
-                            sgt += __shfl_xor_sync(0xFFFFFFFFu, sgt, o);
-                            cgt += __shfl_xor_sync(0xFFFFFFFFu, cgt, o);
-                        }
-                        const bool lead = real && sub == 0;  // one lane per candidate contributes
-                        const bool kept_k = lead && (!k_on || cgt < kk);
-                        const unsigned long long MA = sh.pma[r];
-                        unsigned long long tgt = 0;
-                        if (k_on && p_on) {
-                            // the top-p target within the top-k set
-                            const unsigned long long ws = warp_sum_u64(kept_k ? static_cast<unsigned long long>(w) : 0ull);
-                            if (lane == 0) sh.w.ct.w[warp] = ws;
-                            group_barrier<PL>(r);
-                            unsigned long long zk = MA;
-                            for (int q = 0; q < PW; ++q) zk += sh.w.ct.w[r * PW + q];
-                            tgt = fx_target_fx(pp, zk);
-                            group_barrier<PL>(r);
-                        } else if (p_on) {
-                            tgt = sh.tgt[r];
-                        }
-                        const bool kept = kept_k && (!p_on || MA + sgt < tgt);
-                        // the smallest kept value and the kept weight
-                        float vmin = kept ? v : INFINITY;
-                        unsigned long long wk = kept ? static_cast<unsigned long long>(w) : 0ull;
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) {
-                            vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
-                            wk += __shfl_xor_sync(0xFFFFFFFFu, wk, o);
-                        }
-                        if (lane == 0) {
-                            sh.w.ct.v[warp] = vmin;
-                            sh.w.ct.w[warp] = wk;
-                        }
-                        group_barrier<PL>(r);
-                        if (jj == 0) {
-                            float th = INFINITY;
-                            unsigned long long zf = MA;
-                            for (int q = 0; q < PW; ++q) {
-                                th = fminf(th, sh.w.ct.v[r * PW + q]);
-                                zf += sh.w.ct.w[r * PW + q];
-                            }
-                            sh.theta[r] = th;
-                            sh.Z[r] = fx_to_float(zf);
-                        }
-                    }
-                    __syncthreads();
-                } else {
-                    // ---- exact thresholds.  Warp 0, per row: the candidates' count (-1 when some
-                    // CTA overflowed its slots, or with too many or none: then the exact search)
-                    // and each CTA's offset in the row's list in CTA order
-                    if (warp == 0) {
-    #pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            const bool on = r < nrows && sh.mode[r] == 1;
-                            const uint32_t cc = on && lane < static_cast<int>(C) ? sh.ccnt[lane][r] : 0u;
-                            const bool over = __any_sync(0xFFFFFFFFu, cc > static_cast<uint32_t>(capc));
-                            uint32_t incl = cc;
-    #pragma unroll
-                            for (int o = 1; o < 32; o <<= 1) {
-                                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                                if (lane >= o) incl += y;
-                            }
-                            if (lane < static_cast<int>(C)) sh.cpre[r][lane] = incl - cc;
-                            if (lane == 31)
-                                sh.ncr[r] = !on ? 0 : (over || incl > static_cast<uint32_t>(NT) || incl == 0) ? -1
-                                                                                                        : static_cast<int>(incl);
-                        }
-                    }
-                    __syncthreads();
-                    const int ncr[2] = {sh.ncr[0], sh.ncr[1]};
-                    const unsigned long long MAr[2] = {sh.mode[0] == 1 ? sh.pma[0] : 0ull,
-                                                       nrows > 1 && sh.mode[1] == 1 ? sh.pma[1] : 0ull};
-                    // candidate i of row r, counted over the CTAs' slots in CTA order
-                    auto cand_at = [&](int r, int i) -> float {
-                        int c = 0;
-                        while (c + 1 < static_cast<int>(C) && i >= static_cast<int>(sh.cpre[r][c + 1])) ++c;
-                        return __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][c * capc + i - static_cast<int>(sh.cpre[r][c])] >> 32));
-                    };
-                    const bool small = ncr[0] <= NSMALL && (nrows < 2 || ncr[1] <= NSMALL);
-                    if (small) {
-                        // both rows' candidates into contiguous lists, with their fixed-point weights
-                        for (int t = tid; t < 2 * CAPT; t += NT) {
-                            const int r = t >= CAPT ? 1 : 0, slot = t - r * CAPT;
-                            const int c = slot / capc, i = slot - c * capc;
-                            if (ncr[r] > 0 && c < static_cast<int>(C) && i < static_cast<int>(sh.ccnt[c][r])) {
-                                const int pos = r * NSMALL + static_cast<int>(sh.cpre[r][c]) + i;
-                                const float v = __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][slot] >> 32));
-                                sh.b.s.sval[pos] = v;
-                                reinterpret_cast<uint32_t *>(sh.b.s.skey)[pos] = fix31(ex2(fmaf(v, c2, sh.nmc[r])));
-                            }
-                        }
-                        __syncthreads();
-                        // ---- rank by counting, both rows at once (threads [0, NSMALL) take row
-                        // 0, the rest row 1): for each candidate, the weight and number of the
-                        // candidates strictly above it, each counted by S consecutive lanes over
-                        // every S-th candidate; then block reductions
-                        const int r = tid / NSMALL, tt = tid - r * NSMALL;
-                        const int nr = r < nrows ? ncr[r] : -1;
-                        int p2 = 1;
-                        while (p2 < nr) p2 <<= 1;
-                        const int S = min(32, NSMALL / p2);
-                        const int i = tt / S, sub = tt - i * S;
-                        const bool real = nr > 0 && i < nr;
-                        const float *cv = sh.b.s.sval + r * NSMALL;
-                        const uint32_t *cw = reinterpret_cast<const uint32_t *>(sh.b.s.skey) + r * NSMALL;
-                        const float v = real ? cv[i] : -INFINITY;
-                        const uint32_t w = real ? cw[i] : 0u;
-                        unsigned long long sgt = 0;
-                        int cgt = 0;
-                        if (real) {
-    #pragma unroll 4
-                            for (int q = sub; q < nr; q += S) {
-                                const float vq = cv[q];
-                                if (vq > v) {
-                                    sgt += cw[q];
-                                    ++cgt;
-                                }
-                            }
-                        }
-                        for (int o = S >> 1; o > 0; o >>= 1) {
-                            sgt += __shfl_xor_sync(0xFFFFFFFFu, sgt, o);
-                            cgt += __shfl_xor_sync(0xFFFFFFFFu, cgt, o);
-                        }
-                        const bool lead = real && sub == 0;  // one lane per candidate contributes
-                        const bool kept_k = lead && (!k_on || cgt < kk);
-                        const unsigned long long MA = MAr[r < 2 ? r : 0];
-                        // reduction 1 (top-k with top-p): the weight of the top-k set
-                        unsigned long long tgt = 0;
-                        if (k_on && p_on) {
-                            const unsigned long long ws = warp_sum_u64(kept_k ? static_cast<unsigned long long>(w) : 0ull);
-                            if (lane == 0) sh.w.ct.w[warp] = ws;
-                            __syncthreads();
-                            unsigned long long zk = MA;
-                            for (int wq = 0; wq < NW / 2; ++wq) zk += sh.w.ct.w[r * (NW / 2) + wq];
-                            tgt = fx_target_fx(pp, zk);
-                            __syncthreads();
-                        } else if (p_on) {
-                            tgt = fx_target(pp, sh.Z[r < nrows ? r : 0]);
-                        }
-                        const bool kept = kept_k && (!p_on || MA + sgt < tgt);
-                        // reduction 2: the smallest kept value and the kept weight
-                        float vmin = kept ? v : INFINITY;
-                        unsigned long long wk = kept ? static_cast<unsigned long long>(w) : 0ull;
-    #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) {
-                            vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
-                            wk += __shfl_xor_sync(0xFFFFFFFFu, wk, o);
-                        }
-                        if (lane == 0) {
-                            sh.w.ct.v[warp] = vmin;
-                            sh.w.ct.w[warp] = wk;
-                        }
-                        __syncthreads();
-                        if (tt == 0 && nr > 0) {
-                            float th = INFINITY;
-                            unsigned long long zf = MA;
-                            for (int wq = 0; wq < NW / 2; ++wq) {
-                                th = fminf(th, sh.w.ct.v[r * (NW / 2) + wq]);
-                                zf += sh.w.ct.w[r * (NW / 2) + wq];
-                            }
-                            sh.theta[r] = th;
-                            sh.Z[r] = fx_to_float(zf);
-                        }
-    #pragma unroll
-                        for (int rr = 0; rr < 2; ++rr)
-                            if (rr < nrows && sh.mode[rr] == 1 && ncr[rr] < 0 && tid == 0) sh.mode[rr] = 2;
-                        __syncthreads();
-                    } else {
-                        // ---- sort the candidates by value (descending) and scan, one row at a time
-    #pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            if (r >= nrows || sh.mode[r] != 1) continue;
-                            const int nc = ncr[r];
-                            if (nc < 0) {
-                                __syncthreads();
-                                if (tid == 0) sh.mode[r] = 2;
-                                __syncthreads();
-                                continue;
-                            }
-                            const unsigned long long MA = MAr[r];
-                            int P2 = 1;
-                            while (P2 < nc) P2 <<= 1;
-                            // bitonic sort of (value key, position), one key per thread; strides
-                            // below 32 exchange through shuffles, wider ones through shared memory
-                            unsigned long long key = 0ull;
-                            if (tid < nc)
-                                key = (static_cast<unsigned long long>(order_key(cand_at(r, tid))) << 32) |
-                                      static_cast<uint32_t>(tid);
-                            for (int kb = 2; kb <= P2; kb <<= 1) {
-                                for (int jb = kb >> 1; jb > 0; jb >>= 1) {
-                                    unsigned long long other;
-                                    if (jb >= 32) {
-                                        __syncthreads();
-                                        sh.b.s.skey[tid] = key;
-                                        __syncthreads();
-                                        other = sh.b.s.skey[tid ^ jb];
-                                    } else {
-                                        other = __shfl_xor_sync(0xFFFFFFFFu, key, jb);
+                                for (int q = sub; q < nr; q += S) {
+                                    if (cv[q] > v) {
+                                        sgt += cw[q];
+                                        ++cgt;
                                     }
-                                    const bool lower = (tid & jb) == 0;
-                                    const bool desc = (tid & kb) == 0;
-                                    key = (lower == desc) ? max(key, other) : min(key, other);
                                 }
                             }
-                            const bool real = tid < nc;
-                            const float v = real ? key_to_float(static_cast<uint32_t>(key >> 32)) : -INFINITY;
-                            const unsigned long long w =
-                                real ? static_cast<unsigned long long>(fix31(ex2(fmaf(v, c2, sh.nmc[r])))) : 0ull;
-                            __syncthreads();
-                            sh.b.s.sval[tid] = v;
-                            // top-k: the k-th largest value (no element lies above the candidates)
-                            if (k_on && tid == kk - 1) sh.fpick[r] = v;
-                            __syncthreads();
-                            const float thk = k_on ? sh.fpick[r] : -INFINITY;
-                            const unsigned long long wk = (real && v >= thk) ? w : 0ull;
-                            // weight strictly above each value: the exclusive prefix of the weights
-                            // at the first position of its tie group (sorted descending)
-                            const unsigned long long excl = block_excl_scan_u64(wk, sh.w.so.scan);
-                            const int32_t headpos = (tid == 0 || sh.b.s.sval[tid - 1] != v) ? tid : -1;
-                            const int32_t first = block_incl_max_i32(headpos, sh.w.so.scani);
-                            sh.b.s.skey[tid] = excl;
-                            const unsigned long long zk = MA + block_sum_u64(wk, sh.w.so.ru[r]);
-                            if (tid == 0) {
-                                sh.tgt[r] = k_on ? fx_target_fx(pp, zk) : fx_target(pp, sh.Z[r]);
+                            for (int o = S >> 1; o > 0; o >>= 1) {
+                                sgt += __shfl_xor_sync(0xFFFFFFFFu, sgt, o);
+                                cgt += __shfl_xor_sync(0xFFFFFFFFu, cgt, o);
                             }
-                            __syncthreads();
-                            const unsigned long long above = MA + sh.b.s.skey[first];
-                            const bool kept = real && v >= thk && (!p_on || above < sh.tgt[r]);
-                            int32_t lastk = kept ? tid : -1;
-    #pragma unroll
-                            for (int o = 16; o > 0; o >>= 1)
-                                lastk = max(lastk, __shfl_xor_sync(0xFFFFFFFFu, lastk, o));
-                            __syncthreads();
-                            if (lane == 0) sh.w.so.scani[warp] = lastk;
-                            __syncthreads();
-                            int32_t lk = -1;
-                            for (int wq = 0; wq < NW; ++wq) lk = max(lk, sh.w.so.scani[wq]);
-                            const float th = sh.b.s.sval[lk < 0 ? 0 : lk];  // the smallest kept value
-                            const unsigned long long zf =
-                                MA + block_sum_u64((real && v >= th) ? wk : 0ull, sh.w.so.ru[r]);
-                            if (tid == 0) {
+                            const bool lead = real && sub == 0;  // one lane per candidate contributes
+                            const bool kept_k = lead && (!k_on || cgt < kk);
+                            const unsigned long long MA = sh.pma[r];
+                            unsigned long long tgt = 0;
+                            if (k_on && p_on) {
+                                // the top-p target within the top-k set
+                                const unsigned long long ws = warp_sum_u64(kept_k ? static_cast<unsigned long long>(w) : 0ull);
+                                if (lane == 0) sh.w.ct.w[warp] = ws;
+                                group_barrier<PL>(r);
+                                unsigned long long zk = MA;
+                                for (int q = 0; q < PW; ++q) zk += sh.w.ct.w[r * PW + q];
+                                tgt = fx_target_fx(pp, zk);
+                                group_barrier<PL>(r);
+                            } else if (p_on) {
+                                tgt = sh.tgt[r];
+                            }
+                            const bool kept = kept_k && (!p_on || MA + sgt < tgt);
+                            // the smallest kept value and the kept weight
+                            float vmin = kept ? v : INFINITY;
+                            unsigned long long wk = kept ? static_cast<unsigned long long>(w) : 0ull;
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) {
+                                vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
+                                wk += __shfl_xor_sync(0xFFFFFFFFu, wk, o);
+                            }
+                            if (lane == 0) {
+                                sh.w.ct.v[warp] = vmin;
+                                sh.w.ct.w[warp] = wk;
+                            }
+                            group_barrier<PL>(r);
+                            if (jj == 0) {
+                                float th = INFINITY;
+                                unsigned long long zf = MA;
+                                for (int q = 0; q < PW; ++q) {
+                                    th = fminf(th, sh.w.ct.v[r * PW + q]);
+                                    zf += sh.w.ct.w[r * PW + q];
+                                }
                                 sh.theta[r] = th;
                                 sh.Z[r] = fx_to_float(zf);
                             }
-                            __syncthreads();
                         }
-                    }
-                }
-            }
-            // ---- exact bisection over value keys (boundary outside the binned range, or
-            // too many elements in its bins); both rows advance in lockstep
-            const bool any_slow = sh.mode[0] == 2 || (nrows > 1 && sh.mode[1] == 2);
-            if (any_slow) {
-                const int lim_n = n;
-                // F(t) per row: count (wt = 0) or fixed-point weight (wt = 1) of the elements
-                // with key >= max(t, floor); returns the cluster-wide sums
-                auto eval = [&](const uint32_t t[2], const uint32_t fl[2], int wt,
-                                unsigned long long out[2]) {
-                    unsigned long long acc0 = 0, acc1 = 0;
-#pragma unroll 1
-                    for (int r = 0; r < nrows; ++r) {
-                        if (sh.mode[r] != 2) continue;
-                        const float nmc = sh.nmc[r];
-                        const uint32_t lim = max(t[r], fl[r]);
-                        float a = 0.0f;
-                        uint32_t cnum = 0;
-                        for_row(sdat(r), nvr, [&](float x, int li) {
-                            if (li < lim_n && order_key(x) >= lim) {
-                                if (wt) a += ex2(fmaf(x, c2, nmc));
-                                else ++cnum;
+                        __syncthreads();
+                    } else {
+                        // ---- exact thresholds.  Warp 0, per row: the candidates' count (-1 when some
+                        // CTA overflowed its slots, or with too many or none: then the exact search)
+                        // and each CTA's offset in the row's list in CTA order
+                        if (warp == 0) {
+        #pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const bool on = r < nrows && sh.mode[r] == 1;
+                                const uint32_t cc = on && lane < static_cast<int>(C) ? sh.ccnt[lane][r] : 0u;
+                                const bool over = __any_sync(0xFFFFFFFFu, cc > static_cast<uint32_t>(capc));
+                                uint32_t incl = cc;
+        #pragma unroll
+                                for (int o = 1; o < 32; o <<= 1) {
+                                    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                                    if (lane >= o) incl += y;
+                                }
+                                if (lane < static_cast<int>(C)) sh.cpre[r][lane] = incl - cc;
+                                if (lane == 31)
+                                    sh.ncr[r] = !on ? 0 : (over || incl > static_cast<uint32_t>(NT) || incl == 0) ? -1
+                                                                                                            : static_cast<int>(incl);
                             }
-                        });
-                        const unsigned long long ac = wt ? fix_sum(a) : static_cast<unsigned long long>(cnum);
-                        if (r == 0) acc0 = ac;
-                        else acc1 = ac;
-                    }
-                    const unsigned long long s0 = block_sum_u64(acc0, sh.w.so.ru[0]);
-                    const unsigned long long s1 = block_sum_u64(acc1, sh.w.so.ru[1]);
-                    const int sp = static_cast<int>(sstep & 1u);
-                    if (tid < static_cast<int>(C)) {
-                        st_peer_u64(peer_addr(smem_addr(&sh.sx[sp][rank][0]), tid), s0);
-                        st_peer_u64(peer_addr(smem_addr(&sh.sx[sp][rank][1]), tid), s1);
-                        xarrive(&sh.xbar[XB_S + sp], tid);
-                    }
-                    xwait(XB_S + sp);
-                    for (int r = 0; r < 2; ++r) {
-                        unsigned long long sum = 0;
-                        for (uint32_t c = 0; c < C; ++c) sum += sh.sx[sp][c][r];
-                        out[r] = sum;
-                    }
-                    ++sstep;
-                    __syncthreads();  // every thread has read this step's sums
-                };
-                // largest key t with F(t) >= need, by bisection over the 32-bit key space
-                auto search = [&](const uint32_t fl[2], int wt, const unsigned long long need[2],
-                                  uint32_t res_t[2]) {
-                    uint32_t lo[2] = {0u, 0u}, hi[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};
-                    for (int it = 0; it < 32; ++it) {
-                        uint32_t mid[2];
-                        for (int r = 0; r < 2; ++r)
-                            mid[r] = lo[r] + static_cast<uint32_t>((static_cast<uint64_t>(hi[r]) - lo[r] + 1) / 2);
-                        unsigned long long f[2];
-                        eval(mid, fl, wt, f);
-                        for (int r = 0; r < 2; ++r) {
-                            if (lo[r] >= hi[r]) continue;
-                            if (f[r] >= need[r]) lo[r] = mid[r];
-                            else hi[r] = mid[r] - 1;
+                        }
+                        __syncthreads();
+                        const int ncr[2] = {sh.ncr[0], sh.ncr[1]};
+                        const unsigned long long MAr[2] = {sh.mode[0] == 1 ? sh.pma[0] : 0ull,
+                                                           nrows > 1 && sh.mode[1] == 1 ? sh.pma[1] : 0ull};
+                        // candidate i of row r, counted over the CTAs' slots in CTA order
+                        auto cand_at = [&](int r, int i) -> float {
+                            int c = 0;
+                            while (c + 1 < static_cast<int>(C) && i >= static_cast<int>(sh.cpre[r][c + 1])) ++c;
+                            return __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][c * capc + i - static_cast<int>(sh.cpre[r][c])] >> 32));
+                        };
+                        const bool small = ncr[0] <= NSMALL && (nrows < 2 || ncr[1] <= NSMALL);
+                        if (small) {
+                            // both rows' candidates into contiguous lists, with their fixed-point weights
+                            for (int t = tid; t < 2 * CAPT; t += NT) {
+                                const int r = t >= CAPT ? 1 : 0, slot = t - r * CAPT;
+                                const int c = slot / capc, i = slot - c * capc;
+                                if (ncr[r] > 0 && c < static_cast<int>(C) && i < static_cast<int>(sh.ccnt[c][r])) {
+                                    const int pos = r * NSMALL + static_cast<int>(sh.cpre[r][c]) + i;
+                                    const float v = __uint_as_float(static_cast<uint32_t>(sh.a.cand[r][slot] >> 32));
+                                    sh.b.s.sval[pos] = v;
+                                    reinterpret_cast<uint32_t *>(sh.b.s.skey)[pos] = fix31(ex2(fmaf(v, c2, sh.nmc[r])));
+                                }
+                            }
+                            __syncthreads();
+                            // ---- rank by counting, both rows at once (threads [0, NSMALL) take row
+                            // 0, the rest row 1): for each candidate, the weight and number of the
+                            // candidates strictly above it, each counted by S consecutive lanes over
+                            // every S-th candidate; then block reductions
+                            const int r = tid / NSMALL, tt = tid - r * NSMALL;
+                            const int nr = r < nrows ? ncr[r] : -1;
+                            int p2 = 1;
+                            while (p2 < nr) p2 <<= 1;
+                            const int S = min(32, NSMALL / p2);
+                            const int i = tt / S, sub = tt - i * S;
+                            const bool real = nr > 0 && i < nr;
+                            const float *cv = sh.b.s.sval + r * NSMALL;
+                            const uint32_t *cw = reinterpret_cast<const uint32_t *>(sh.b.s.skey) + r * NSMALL;
+                            const float v = real ? cv[i] : -INFINITY;
+                            const uint32_t w = real ? cw[i] : 0u;
+                            unsigned long long sgt = 0;
+                            int cgt = 0;
+                            if (real) {
+        #pragma unroll 4
+                                for (int q = sub; q < nr; q += S) {
+                                    const float vq = cv[q];
+                                    if (vq > v) {
+                                        sgt += cw[q];
+                                        ++cgt;
+                                    }
+                                }
+                            }
+                            for (int o = S >> 1; o > 0; o >>= 1) {
+                                sgt += __shfl_xor_sync(0xFFFFFFFFu, sgt, o);
+                                cgt += __shfl_xor_sync(0xFFFFFFFFu, cgt, o);
+                            }
+                            const bool lead = real && sub == 0;  // one lane per candidate contributes
+                            const bool kept_k = lead && (!k_on || cgt < kk);
+                            const unsigned long long MA = MAr[r < 2 ? r : 0];
+                            // reduction 1 (top-k with top-p): the weight of the top-k set
+                            unsigned long long tgt = 0;
+                            if (k_on && p_on) {
+                                const unsigned long long ws = warp_sum_u64(kept_k ? static_cast<unsigned long long>(w) : 0ull);
+                                if (lane == 0) sh.w.ct.w[warp] = ws;
+                                __syncthreads();
+                                unsigned long long zk = MA;
+                                for (int wq = 0; wq < NW / 2; ++wq) zk += sh.w.ct.w[r * (NW / 2) + wq];
+                                tgt = fx_target_fx(pp, zk);
+                                __syncthreads();
+                            } else if (p_on) {
+                                tgt = fx_target(pp, sh.Z[r < nrows ? r : 0]);
+                            }
+                            const bool kept = kept_k && (!p_on || MA + sgt < tgt);
+                            // reduction 2: the smallest kept value and the kept weight
+                            float vmin = kept ? v : INFINITY;
+                            unsigned long long wk = kept ? static_cast<unsigned long long>(w) : 0ull;
+        #pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) {
+                                vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
+                                wk += __shfl_xor_sync(0xFFFFFFFFu, wk, o);
+                            }
+                            if (lane == 0) {
+                                sh.w.ct.v[warp] = vmin;
+                                sh.w.ct.w[warp] = wk;
+                            }
+                            __syncthreads();
+                            if (tt == 0 && nr > 0) {
+                                float th = INFINITY;
+                                unsigned long long zf = MA;
+                                for (int wq = 0; wq < NW / 2; ++wq) {
+                                    th = fminf(th, sh.w.ct.v[r * (NW / 2) + wq]);
+                                    zf += sh.w.ct.w[r * (NW / 2) + wq];
+                                }
+                                sh.theta[r] = th;
+                                sh.Z[r] = fx_to_float(zf);
+                            }
+        #pragma unroll
+                            for (int rr = 0; rr < 2; ++rr)
+                                if (rr < nrows && sh.mode[rr] == 1 && ncr[rr] < 0 && tid == 0) sh.mode[rr] = 2;
+                            __syncthreads();
+                        } else {
+                            // ---- sort the candidates by value (descending) and scan, one row at a time
+        #pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                if (r >= nrows || sh.mode[r] != 1) continue;
+                                const int nc = ncr[r];
+                                if (nc < 0) {
+                                    __syncthreads();
+                                    if (tid == 0) sh.mode[r] = 2;
+                                    __syncthreads();
+                                    continue;
+                                }
+                                const unsigned long long MA = MAr[r];
+                                int P2 = 1;
+                                while (P2 < nc) P2 <<= 1;
+                                // bitonic sort of (value key, position), one key per thread; strides
+                                // below 32 exchange through shuffles, wider ones through shared memory
+                                unsigned long long key = 0ull;
+                                if (tid < nc)
+                                    key = (static_cast<unsigned long long>(order_key(cand_at(r, tid))) << 32) |
+                                          static_cast<uint32_t>(tid);
+                                for (int kb = 2; kb <= P2; kb <<= 1) {
+                                    for (int jb = kb >> 1; jb > 0; jb >>= 1) {
+                                        unsigned long long other;
+                                        if (jb >= 32) {
+                                            __syncthreads();
+                                            sh.b.s.skey[tid] = key;
+                                            __syncthreads();
+                                            other = sh.b.s.skey[tid ^ jb];
+                                        } else {
+                                            other = __shfl_xor_sync(0xFFFFFFFFu, key, jb);
+                                        }
+                                        const bool lower = (tid & jb) == 0;
+                                        const bool desc = (tid & kb) == 0;
+                                        key = (lower == desc) ? max(key, other) : min(key, other);
+                                    }
+                                }
+                                const bool real = tid < nc;
+                                const float v = real ? key_to_float(static_cast<uint32_t>(key >> 32)) : -INFINITY;
+                                const unsigned long long w =
+                                    real ? static_cast<unsigned long long>(fix31(ex2(fmaf(v, c2, sh.nmc[r])))) : 0ull;
+                                __syncthreads();
+                                sh.b.s.sval[tid] = v;
+                                // top-k: the k-th largest value (no element lies above the candidates)
+                                if (k_on && tid == kk - 1) sh.fpick[r] = v;
+                                __syncthreads();
+                                const float thk = k_on ? sh.fpick[r] : -INFINITY;
+                                const unsigned long long wk = (real && v >= thk) ? w : 0ull;
+                                // weight strictly above each value: the exclusive prefix of the weights
+                                // at the first position of its tie group (sorted descending)
+                                const unsigned long long excl = block_excl_scan_u64(wk, sh.w.so.scan);
+                                const int32_t headpos = (tid == 0 || sh.b.s.sval[tid - 1] != v) ? tid : -1;
+                                const int32_t first = block_incl_max_i32(headpos, sh.w.so.scani);
+                                sh.b.s.skey[tid] = excl;
+                                const unsigned long long zk = MA + block_sum_u64(wk, sh.w.so.ru[r]);
+                                if (tid == 0) {
+                                    sh.tgt[r] = k_on ? fx_target_fx(pp, zk) : fx_target(pp, sh.Z[r]);
+                                }
+                                __syncthreads();
+                                const unsigned long long above = MA + sh.b.s.skey[first];
+                                const bool kept = real && v >= thk && (!p_on || above < sh.tgt[r]);
+                                int32_t lastk = kept ? tid : -1;
+        #pragma unroll
+                                for (int o = 16; o > 0; o >>= 1)
+                                    lastk = max(lastk, __shfl_xor_sync(0xFFFFFFFFu, lastk, o));
+                                __syncthreads();
+                                if (lane == 0) sh.w.so.scani[warp] = lastk;
+                                __syncthreads();
+                                int32_t lk = -1;
+                                for (int wq = 0; wq < NW; ++wq) lk = max(lk, sh.w.so.scani[wq]);
+                                const float th = sh.b.s.sval[lk < 0 ? 0 : lk];  // the smallest kept value
+                                const unsigned long long zf =
+                                    MA + block_sum_u64((real && v >= th) ? wk : 0ull, sh.w.so.ru[r]);
+                                if (tid == 0) {
+                                    sh.theta[r] = th;
+                                    sh.Z[r] = fx_to_float(zf);
+                                }
+                                __syncthreads();
+                            }
                         }
                     }
-                    res_t[0] = lo[0];
-                    res_t[1] = lo[1];
-                };
-                uint32_t zero[2] = {0u, 0u}, thk[2] = {0u, 0u}, th[2] = {0u, 0u};
-                if (k_on) {
-                    const unsigned long long need[2] = {static_cast<unsigned long long>(kk),
-                                                        static_cast<unsigned long long>(kk)};
-                    search(zero, 0, need, thk);
                 }
-                th[0] = thk[0];
-                th[1] = thk[1];
-                if (p_on) {
-                    unsigned long long zk[2] = {0, 0};
-                    if (k_on) eval(thk, zero, 1, zk);
-                    unsigned long long need[2];
-                    for (int r = 0; r < 2; ++r) {
-                        need[r] = k_on ? fx_target_fx(pp, zk[r]) : fx_target(pp, sh.Z[r < nrows ? r : 0]);
-                        if (need[r] == 0) need[r] = 1;
+                // ---- exact bisection over value keys (boundary outside the binned range, or
+                // too many elements in its bins); both rows advance in lockstep
+                const bool any_slow = sh.mode[0] == 2 || (nrows > 1 && sh.mode[1] == 2);
+                if (any_slow) {
+                    const int lim_n = n;
+                    // F(t) per row: count (wt = 0) or fixed-point weight (wt = 1) of the elements
+                    // with key >= max(t, floor); returns the cluster-wide sums
+                    auto eval = [&](const uint32_t t[2], const uint32_t fl[2], int wt,
+                                    unsigned long long out[2]) {
+                        unsigned long long acc0 = 0, acc1 = 0;
+#pragma unroll 1
+                        for (int r = 0; r < nrows; ++r) {
+                            if (sh.mode[r] != 2) continue;
+                            const float nmc = sh.nmc[r];
+                            const uint32_t lim = max(t[r], fl[r]);
+                            float a = 0.0f;
+                            uint32_t cnum = 0;
+                            for_row(sdat(r), nvr, [&](float x, int li) {
+                                if (li < lim_n && order_key(x) >= lim) {
+                                    if (wt) a += ex2(fmaf(x, c2, nmc));
+                                    else ++cnum;
+                                }
+                            });
+                            const unsigned long long ac = wt ? fix_sum(a) : static_cast<unsigned long long>(cnum);
+                            if (r == 0) acc0 = ac;
+                            else acc1 = ac;
+                        }
+                        const unsigned long long s0 = block_sum_u64(acc0, sh.w.so.ru[0]);
+                        const unsigned long long s1 = block_sum_u64(acc1, sh.w.so.ru[1]);
+                        const int sp = static_cast<int>(sstep & 1u);
+                        if (tid < static_cast<int>(C)) {
+                            st_peer_u64(peer_addr(smem_addr(&sh.sx[sp][rank][0]), tid), s0);
+                            st_peer_u64(peer_addr(smem_addr(&sh.sx[sp][rank][1]), tid), s1);
+                            xarrive(&sh.xbar[XB_S + sp], tid);
+                        }
+                        xwait(XB_S + sp);
+                        for (int r = 0; r < 2; ++r) {
+                            unsigned long long sum = 0;
+                            for (uint32_t c = 0; c < C; ++c) sum += sh.sx[sp][c][r];
+                            out[r] = sum;
+                        }
+                        ++sstep;
+                        __syncthreads();  // every thread has read this step's sums
+                    };
+                    // largest key t with F(t) >= need, by bisection over the 32-bit key space
+                    auto search = [&](const uint32_t fl[2], int wt, const unsigned long long need[2],
+                                      uint32_t res_t[2]) {
+                        uint32_t lo[2] = {0u, 0u}, hi[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};
+                        for (int it = 0; it < 32; ++it) {
+                            uint32_t mid[2];
+                            for (int r = 0; r < 2; ++r)
+                                mid[r] = lo[r] + static_cast<uint32_t>((static_cast<uint64_t>(hi[r]) - lo[r] + 1) / 2);
+                            unsigned long long f[2];
+                            eval(mid, fl, wt, f);
+                            for (int r = 0; r < 2; ++r) {
+                                if (lo[r] >= hi[r]) continue;
+                                if (f[r] >= need[r]) lo[r] = mid[r];
+                                else hi[r] = mid[r] - 1;
+                            }
+                        }
+                        res_t[0] = lo[0];
+                        res_t[1] = lo[1];
+                    };
+                    uint32_t zero[2] = {0u, 0u}, thk[2] = {0u, 0u}, th[2] = {0u, 0u};
+                    if (k_on) {
+                        const unsigned long long need[2] = {static_cast<unsigned long long>(kk),
+                                                            static_cast<unsigned long long>(kk)};
+                        search(zero, 0, need, thk);
                     }
-                    search(thk, 1, need, th);
+                    th[0] = thk[0];
+                    th[1] = thk[1];
+                    if (p_on) {
+                        unsigned long long zk[2] = {0, 0};
+                        if (k_on) eval(thk, zero, 1, zk);
+                        unsigned long long need[2];
+                        for (int r = 0; r < 2; ++r) {
+                            need[r] = k_on ? fx_target_fx(pp, zk[r]) : fx_target(pp, sh.Z[r < nrows ? r : 0]);
+                            if (need[r] == 0) need[r] = 1;
+                        }
+                        search(thk, 1, need, th);
+                    }
+                    unsigned long long zf[2];
+                    eval(th, zero, 1, zf);
+                    if (tid < nrows && sh.mode[tid] == 2) {
+                        sh.theta[tid] = key_to_float(th[tid]);
+                        sh.Z[tid] = fx_to_float(zf[tid]);
+                    }
+                    __syncthreads();
                 }
-                unsigned long long zf[2];
-                eval(th, zero, 1, zf);
-                if (tid < nrows && sh.mode[tid] == 2) {
-                    sh.theta[tid] = key_to_float(th[tid]);
-                    sh.Z[tid] = fx_to_float(zf[tid]);
-                }
-                __syncthreads();
             }
         }
         if (tid < nrows) sh.invZ[tid] = 1.0f / sh.Z[tid];
@@ -1742,7 +1802,9 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
 
         bool accept = false;
         float pt = 0.0f, pd = 0.0f;
-        if (j < D && dvalid && one_hot) {
+        if (early) {
+            accept = true;  // (no output reads its probabilities)
+        } else if (j < D && dvalid && one_hot) {
             // the draft is the point mass on d: q(d) = 1, held iff U_acc <= p(d)
             const float xt = sh.e1d[ep].x;
             const bool in_p = deg0 ? d == 0 : xt >= th0;
