@@ -266,7 +266,9 @@ int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draf
  *   out_tokens, num_accepted   as in spec_verify_greedy
  *   p_target, p_draft  float [B, D] or NULL   p_j(d_j) and q_j(d_j) for every j < D; when
  *                  both are NULL the call may skip the positions behind each row's first
- *                  rejection (no output depends on them), which makes it faster
+ *                  rejection, and the top-p thresholds of a draft whose acceptance is
+ *                  already certain (no output depends on them), which makes it faster; the
+ *                  tokens and accepted counts are the same either way
  *   workspace      >= spec_verify_workspace_bytes(B, D, V) bytes, 256-byte aligned;
  *                  no initial contents are needed
  *   status         int32 [1] or NULL
