@@ -146,10 +146,13 @@ k_argmax_groups(const T *__restrict__ logits, int64_t V, int P, int mode,
     cluster_sync();
 }
 
-// Cluster size: enough CTAs per row to keep the slices near 2-4K elements, at most 8.
-static int argmax_cluster_size(int64_t V) {
+// Cluster size: enough CTAs per row to keep the slices near 2-4K elements, at most 8; at
+// most 4 when there are many rows, which fill the GPU with fewer, longer slices (192 rows of
+// 151,936 fp32: 29.4 -> 27.3 us; 1024 rows: 121.5 -> 108.8 us).
+static int argmax_cluster_size(int64_t V, int64_t groups) {
+    const int cmax = groups >= 64 ? 4 : 8;
     int C = 1;
-    while (C < 8 && V / (2 * C) >= 2048) C *= 2;
+    while (C < cmax && V / (2 * C) >= 2048) C *= 2;
     return C;
 }
 
@@ -157,7 +160,7 @@ template <typename T>
 static cudaError_t launch_argmax(const void *logits, int64_t groups, int P, int64_t V, int mode,
                                  const int32_t *d, int32_t *out_a, int32_t *out_b,
                                  int32_t *status, cudaStream_t stream) {
-    const int C = argmax_cluster_size(V);
+    const int C = argmax_cluster_size(V, groups);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(groups * C), 1, 1);
     cfg.blockDim = dim3(kArgmaxThreads, 1, 1);
@@ -278,7 +281,9 @@ k_argmax_verify_rows(const T *__restrict__ logits, int64_t V, int D,
 
 template <typename T>
 static cudaError_t launch_verify_greedy_rows(const VerifySampleArgs &a, cudaStream_t stream) {
-    const int C = argmax_cluster_size(a.V);
+    // (beside the sampling verifier's persistent grid, on the SMs it leaves: slices of the
+    // original width)
+    const int C = argmax_cluster_size(a.V, 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.B * C), 1, 1);
     cfg.blockDim = dim3(kArgmaxThreads, 1, 1);
