@@ -216,6 +216,12 @@ def profiled_traffic(workload):
 
 # ---------------------------------------------------------------- CPU oracle baseline
 
+def optional_top_p(x, to_dev):
+    """The workload's per-row top-p on the device, or None when no row filters (every p is
+    1): the call then runs without top-p values, as it does without top-k values."""
+    return None if (x["top_p"] >= 1.0).all() else to_dev(x["top_p"])
+
+
 def sample_rows(x, rows):
     """`rows` rows of the verify with the workload's mix of greedy rows (temperature 0,
     the first ones of the batch) and sampled rows."""
@@ -309,7 +315,7 @@ def run_gpu(args, rank, world, dist):
             T=T0 if c == 0 else T0.clone(), Q=Q0 if c == 0 else Q0.clone(),
             d=to_dev(x["d"]), e=to_dev(di["e"][0]), h=to_dev(di["h"][0]),
             W=to_dev(di["W"]) if c == 0 else sets[0]["W"].clone()))
-    tau, top_p = to_dev(x["tau"]), to_dev(x["top_p"])
+    tau, top_p = to_dev(x["tau"]), optional_top_p(x, to_dev)
     top_k = to_dev(x["top_k"]) if (x["top_k"] > 0).any() else None
     we, wh = to_dev(di["we"]), to_dev(di["wh"])
     M, H = w.tokens, w.H
@@ -553,7 +559,7 @@ def measure_per_config(dev, cached=None, graph_calls=20, reps=15):
             vbytes = B * (D + 1) * V * es
             entry["verify_call"] = "spec_verify_greedy"
         else:
-            tau, top_p = to_dev(x["tau"]), to_dev(x["top_p"])
+            tau, top_p = to_dev(x["tau"]), optional_top_p(x, to_dev)
             top_k = to_dev(x["top_k"]) if (x["top_k"] > 0).any() else None
             ws = torch.empty(lib.spec_verify_workspace_bytes(B, D, V), dtype=torch.uint8,
                              device=dev)
@@ -701,7 +707,7 @@ def run_sweep(args):
             vbytes = B * (D + 1) * V * (4 if x["dtype"] == "f32" else 2)
             vcall = "spec_verify_greedy"
         else:
-            tau, top_p = to_dev(x["tau"]), to_dev(x["top_p"])
+            tau, top_p = to_dev(x["tau"]), optional_top_p(x, to_dev)
             top_k = to_dev(x["top_k"]) if (x["top_k"] > 0).any() else None
             ws = torch.empty(lib.spec_verify_workspace_bytes(B, D, V), dtype=torch.uint8, device=dev)
             vfn = lambda: lib.spec_verify_sample(T, Q, d, tau, top_k, top_p, x["seed"], out, na,
@@ -911,7 +917,7 @@ def run_graph_batch(args):
                      for i in range(NB)]
             vbytes = B * (D + 1) * V * (4 if x["dtype"] == "f32" else 2)
         else:
-            tau, top_p = to_dev(x["tau"]), to_dev(x["top_p"])
+            tau, top_p = to_dev(x["tau"]), optional_top_p(x, to_dev)
             top_k = to_dev(x["top_k"]) if (x["top_k"] > 0).any() else None
             ws = torch.empty(lib.spec_verify_workspace_bytes(B, D, V), dtype=torch.uint8,
                              device=dev)

@@ -275,7 +275,7 @@ int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draf
  *   B >= 0, 1 <= D <= 64, 1 <= V <= 2,097,152 (fp32) or 4,194,304 (bf16); a larger V
  *   returns MTPSPEC_ERR_SHAPE.
  *   Two verifiers compute these results.  Up to V = 407,552 (fp32) or 815,104 (bf16) with
- *   draft logits, 652,288 or 1,304,576 with a one-hot draft, a cluster of at most 16 CTAs
+ *   draft logits, 651,776 or 1,303,552 with a one-hot draft, a cluster of at most 16 CTAs
  *   stages a unit's rows in shared memory and verifies the unit alone.  Past those limits
  *   (or with the environment variable MTPSPEC_VERIFY_IMPL=chunks) the chunked verifier
  *   cuts each unit's rows into up to 256 chunks of 32 KB of logits, spread over the CTAs

@@ -68,8 +68,8 @@ def test_host_side_validation(so):
 
 
 def test_sampling_vocabulary_limit(so):
-    # a cluster stages V up to 407,552 (fp32) or 815,104 (bf16) with draft logits, 652,288
-    # or 1,304,576 one-hot; beyond that the chunked verifier takes V up to 256 chunks of
+    # a cluster stages V up to 407,552 (fp32) or 815,104 (bf16) with draft logits, 651,776
+    # or 1,303,552 one-hot; beyond that the chunked verifier takes V up to 256 chunks of
     # 32 KB of logits (2,097,152 fp32, 4,194,304 bf16) in either mode.  An empty batch
     # (B = 0) passes every check that does not touch device memory
     nul, draft = None, C.c_void_p(256)

@@ -301,8 +301,8 @@ def test_one_hot_draft_serving_mix():
 @pytest.mark.parametrize("dtype,one_hot,V,k", [
     ("f32", False, 407552, 0),      # the largest vocabularies a cluster stages
     ("bf16", False, 815104, 50),
-    ("f32", True, 652288, 50),
-    ("bf16", True, 1304576, 0),
+    ("f32", True, 651776, 50),
+    ("bf16", True, 1303552, 0),
 ])
 def test_maximum_vocabulary(dtype, one_hot, V, k):
     w = Workload(name="vmax", B=2, D=2, V=V, H=8, dtype=dtype, tau=1.0, top_k=k, top_p=0.9,

@@ -168,6 +168,7 @@ struct __align__(16) Shared {
     union {
         struct {
             float rf[2][NW], rs[2][NW];    // pass 1: maxima and sums
+            float ra[NW];                  // pass 1: the target mass above the draft token
         } p1;
         struct {
             unsigned long long lo[NW], hi[NW];  // plan: totals of the bound scans
@@ -205,13 +206,22 @@ struct __align__(16) Shared {
     // rejected) and sent with its E1 message, so that every CTA takes the same sequence; in
     // CTA 0 the slot of the other parity holds the unit after that, chosen during this E1
     int32_t e1su[2];
-    // top-k rows with a small k: per row, the cluster's lower bound on the k-th largest logit
-    float kbd[2];
+    union {
+        // top-k rows with a small k: per row, the cluster's lower bound on the k-th largest logit
+        float kbd[2];
+        // top-p rows of a decode loop: the target's mass strictly above the draft token's
+        // logit, relative to the row maximum like Z
+        float above;
+    };
     int32_t early;    // the unit's draft is certainly accepted before its thresholds (see below)
     NextParams e1sp[2];
+    // E1, by unit parity: each CTA's target mass above the draft token (last, so that the
+    // fields above keep their places)
+    float e1ab[2][MAXC];
 };
-// The state above fills the padding before e1sp: the staged slices keep their room.
-static_assert(sizeof(Shared) == 28544, "the slices' shared-memory budget assumes this size");
+// The slices' shared-memory budget (the vocabulary limits stated with the entry points)
+// assumes this size.
+static_assert(sizeof(Shared) == 28672, "the slices' shared-memory budget assumes this size");
 
 __device__ __forceinline__ float ex2(float z) {
     float r;
@@ -444,6 +454,26 @@ __device__ __forceinline__ float vec_sum_ex2(const uint4 &raw, float c2, float n
         for (int e = 0; e + w < EPV; e += 2 * w) x[e] += x[e + w];
     return x[0];
 }
+// The same sum, and into `above` the sum over the elements above xd: the same weights,
+// and the same order for the sum itself, so that it is bit for bit vec_sum_ex2's.
+template <typename T>
+__device__ __forceinline__ float vec_sum_ex2_above(const uint4 &raw, float c2, float nm, float xd,
+                                                   float &above) {
+    constexpr int EPV = elems_per_16B<T>::value;
+    float x[EPV];
+    unpack(raw, x);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+        const float w = ex2(fmaf(x[e], c2, nm));
+        above += x[e] > xd ? w : 0.0f;
+        x[e] = w;
+    }
+#pragma unroll
+    for (int w = 1; w < EPV; w <<= 1)
+#pragma unroll
+        for (int e = 0; e + w < EPV; e += 2 * w) x[e] += x[e + w];
+    return x[0];
+}
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -512,8 +542,10 @@ __device__ __forceinline__ bool row_sampled(const Params &P, int64_t b) {
 
 // KT: the call passes per-row top-k values.  Without them no row has a top-k filter, and
 // the top-k paths (counting histograms, the bound of small k, the draw from candidates)
-// compile out of the instance that runs.
-template <typename T, bool KT>
+// compile out of the instance that runs.  EA: a decode loop's call without top-k values
+// (no p_target, p_draft), whose top-p drafts may be seen accepted at E1; the other
+// instances compile that path out.
+template <typename T, bool KT, bool EA>
 __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Shared &sh = *reinterpret_cast<Shared *>(smem_raw);
@@ -743,6 +775,11 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         const float c2 = __fdiv_rn(1.44269504088896340736f, tau);
         const bool dvalid = d >= 0 && d < V;
         const bool d_here = dvalid && d >= lo && d < lo + n;
+        // a decode loop's top-p draft may be seen accepted at E1 (see the decision after the
+        // row statistics): pass 1 then also sums the target mass above the draft token's logit
+        const bool e1try = EA && !P.need_p && j < D && dvalid && !k_on && p_on;
+        const float xdt =
+            e1try ? widen(static_cast<const T *>(P.T)[(static_cast<int64_t>(b) * (D + 1) + j) * V + d]) : 0.0f;
 
         // the parts the bulk copies do not cover: a ragged tail, or a misaligned row
         for (int r = 0; r < nrows; ++r) {
@@ -770,7 +807,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         const bool filt = k_on || p_on;
         const uint4 *sv0 = reinterpret_cast<const uint4 *>(sdat(0));
         const uint4 *sv1 = reinterpret_cast<const uint4 *>(sdat(1));
-        float cm0, cm1, cs0, cs1;
+        float cm0, cm1, cs0, cs1, cab = 0.0f;
         {
             float mx0 = -INFINITY, mx1 = -INFINITY;
             bool timed_out = false;
@@ -820,21 +857,32 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 // z = x * c2 + nm, nm = -cm * c2 (0 for a slice of -inf alone, whose sum is 0)
                 const float nm0 = cm0 > -INFINITY ? -cm0 * c2 : 0.0f;
                 const float nm1 = cm1 > -INFINITY ? -cm1 * c2 : 0.0f;
-                float a0 = 0.0f, a1 = 0.0f;
+                float a0 = 0.0f, a1 = 0.0f, ab = 0.0f;
+                if (e1try) {
 #pragma unroll 2
-                for (int v = tid; v < nvr; v += NT) {
-                    a0 += vec_sum_ex2<T>(sv0[v], c2, nm0);
-                    if (nrows > 1) a1 += vec_sum_ex2<T>(sv1[v], c2, nm1);
+                    for (int v = tid; v < nvr; v += NT) {
+                        a0 += vec_sum_ex2_above<T>(sv0[v], c2, nm0, xdt, ab);
+                        if (nrows > 1) a1 += vec_sum_ex2<T>(sv1[v], c2, nm1);
+                    }
+                } else {
+#pragma unroll 2
+                    for (int v = tid; v < nvr; v += NT) {
+                        a0 += vec_sum_ex2<T>(sv0[v], c2, nm0);
+                        if (nrows > 1) a1 += vec_sum_ex2<T>(sv1[v], c2, nm1);
+                    }
                 }
                 a0 = warp_sum_f32(a0);
                 a1 = warp_sum_f32(a1);
+                if (e1try) ab = warp_sum_f32(ab);
                 if (lane == 0) {
                     sh.w.p1.rs[0][warp] = a0;
                     sh.w.p1.rs[1][warp] = a1;
+                    if (e1try) sh.w.p1.ra[warp] = ab;
                 }
                 __syncthreads();
                 cs0 = warp_sum_f32(lane < NW ? sh.w.p1.rs[0][lane] : 0.0f);
                 cs1 = warp_sum_f32(lane < NW ? sh.w.p1.rs[1][lane] : 0.0f);
+                if (e1try) cab = warp_sum_f32(lane < NW ? sh.w.p1.ra[lane] : 0.0f);
             }
         }
         if (!started) {
@@ -849,6 +897,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
             st_peer_v4(peer_addr(smem_addr(&sh.e1[ep][rank]), lane), part);
             if (lane != static_cast<int>(rank))
                 st_peer_u32(peer_addr(smem_addr(&sh.e1k[ep][rank]), lane), sh.e1k[ep][rank]);
+            if (e1try) st_peer_u32(peer_addr(smem_addr(&sh.e1ab[ep][rank]), lane), __float_as_uint(cab));
             if (d_here) st_peer_v2(peer_addr(smem_addr(&sh.e1d[ep]), lane), make_float2(sh.xd[0], sh.xd[1]));
             if (rank == 0 && lane != 0) {  // the unit after the next one, and its parameters
                 const NextParams q = sh.e1sp[ep];
@@ -895,6 +944,21 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
 #pragma unroll
                 for (int o = 8; o > 0; o >>= 1) tm = fmaxf(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, o));
             } else {
+                if (e1try) {
+                    // the target's mass above the draft token, rescaled like the sums
+                    float ta = (in && r == 0) ? sh.e1ab[ep][c] : 0.0f;
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) {
+                        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
+                        const float a2 = __shfl_xor_sync(0xFFFFFFFFu, ta, o);
+                        const float M = fmaxf(tm, m2);
+                        ta = (ta > 0.0f ? ta * ex2(__fmul_rn(tm - M, c2)) : 0.0f) +
+                             (a2 > 0.0f ? a2 * ex2(__fmul_rn(m2 - M, c2)) : 0.0f);
+                        tm = M;
+                    }
+                    if (lane == 0) sh.above = ta;
+                    tm = (r < nrows && c < static_cast<int>(C)) ? (r == 0 ? sh.e1[ep][c].x : sh.e1[ep][c].z) : -INFINITY;
+                }
 #pragma unroll
                 for (int o = 8; o > 0; o >>= 1) {
                     const float m2 = __shfl_xor_sync(0xFFFFFFFFu, tm, o);
@@ -912,7 +976,7 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
                 sh.Z[r] = kfast ? 1.0f : ts;
                 // the fixed-point top-p target of the plan
                 sh.tgt[r] = kfast ? 0ull : fx_target(pp, ts);
-                sh.kbd[r] = kfast ? ts : -INFINITY;
+                if (kfast) sh.kbd[r] = ts;
                 // the bins that can hold a top-p boundary: a kept token weighs at least
                 // (1 - p) Z / V, since the tokens below that level weigh less than (1 - p) Z
                 // together
@@ -936,8 +1000,37 @@ __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
         uint32_t dk1 = 0xFFFFFFFFu;
         for (uint32_t c = 0; c < C; ++c) dk1 = min(dk1, sh.e1k[ep][c]);
         const bool dead_unit = (j == D || !P.need_p) && dk1 < static_cast<uint32_t>(j);
-        bool early = false;  // the draft's acceptance is already certain (see below)
-        if (filt && !dead_unit) {
+        // ---- A decode loop reads a draft position's record only for its accept flag when
+        // the draft is accepted.  At E1 every CTA knows each row's sum Z and the target mass
+        // strictly above the draft token's logit.  The token's group is then surely kept if
+        // that mass lies below the top-p target.  A kept mass lies between its target
+        // (p Z) and Z, so p/q is at least (w_t / w_q) p Z_q / Z_t, and a draft the draft row
+        // drops (q = 0) is accepted anyway.  When U_acc lies below that bound (with a
+        // relative slack for the sums' rounding), the acceptance is certain: the filters
+        // are skipped and the staged rows released at once.  Every CTA decides from the
+        // same exchanged values.
+        bool early = false;  // the draft's acceptance is already certain
+        if (e1try && !dead_unit) {
+            if (tid == 0) {
+                const float2 xdv = sh.e1d[ep];
+                const float u = word_uniform(sh.uwd[0]);
+                bool ok = !sh.deg[0] && sh.above < pp * sh.Z[0] * (1.0f - 1e-4f);
+                if (ok) {
+                    if (one_hot) {
+                        ok = u <= ex2(fmaf(xdv.x, c2, sh.nmc[0])) / sh.Z[0] * (1.0f - 1e-4f);
+                    } else if (sh.deg[1]) {
+                        ok = false;
+                    } else {
+                        const float r0 = ex2(__fmul_rn((xdv.x - sh.m[0]) - (xdv.y - sh.m[1]), c2));
+                        ok = u <= r0 * (pp * sh.Z[1] / sh.Z[0]) * (1.0f - 1e-4f);
+                    }
+                }
+                sh.early = ok ? 1 : 0;
+            }
+            __syncthreads();
+            early = sh.early != 0;
+        }
+        if (filt && !dead_unit && !early) {
             if (!kfast) {
                 // ---- pass 2: histogram of the elements in the bins that can hold the boundary.
                 // Top-k counts them; top-p adds each element's weight scaled by its bin's octave,
@@ -2265,7 +2358,7 @@ static int resident_clusters(int C, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, vs::k_verify_rr<T, true>, &cfg) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveClusters(&n, vs::k_verify_rr<T, true, false>, &cfg) != cudaSuccess || n < 1)
         n = 1;
     const int i = used < NC ? used++ : NC - 1;
     dev_of[i] = dev;
@@ -2314,23 +2407,27 @@ static VerifyGeometry verify_geometry(int64_t V, int64_t units, int rows) {
 
 // The kernel may take the largest shared memory and clusters up to MAXC (the occupancy
 // queries of the geometry need both, on the instance with the top-k paths).
-template <typename T, bool KT>
+template <typename T, bool KT, bool EA>
 static cudaError_t prepare_verify_rr() {
     static AttrCache a_smem, a_carve, a_cluster;
-    cudaError_t e = ensure_attr(vs::k_verify_rr<T, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = ensure_attr(vs::k_verify_rr<T, KT, EA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(kSmemLimit), a_smem);
     if (e != cudaSuccess) return e;
-    e = ensure_attr(vs::k_verify_rr<T, KT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = ensure_attr(vs::k_verify_rr<T, KT, EA>, cudaFuncAttributePreferredSharedMemoryCarveout,
                     static_cast<int>(cudaSharedmemCarveoutMaxShared), a_carve);
     if (e != cudaSuccess) return e;
-    return ensure_attr(vs::k_verify_rr<T, KT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1, a_cluster);
+    return ensure_attr(vs::k_verify_rr<T, KT, EA>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1, a_cluster);
 }
 
 template <typename T>
 static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     const int64_t units = p.B * (p.D + 1);
-    cudaError_t e = prepare_verify_rr<T, true>();
-    if (e == cudaSuccess && !p.topk) e = prepare_verify_rr<T, false>();
+    // the instance: with the top-k paths when the call passes top-k values; else with the
+    // E1 acceptance path for a decode loop's call (top-p values, no probabilities), else
+    // without either
+    const bool ea = !p.topk && p.topp && !p.need_p;
+    cudaError_t e = prepare_verify_rr<T, true, false>();
+    if (e == cudaSuccess && !p.topk) e = ea ? prepare_verify_rr<T, false, true>() : prepare_verify_rr<T, false, false>();
     if (e != cudaSuccess) return e;
     const int rows = p.Q ? 2 : 1;
     const VerifyGeometry gm = verify_geometry<T>(p.V, units, rows);
@@ -2368,8 +2465,9 @@ static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = p.topk ? cudaLaunchKernelEx(&cfg, vs::k_verify_rr<T, true>, p)
-               : cudaLaunchKernelEx(&cfg, vs::k_verify_rr<T, false>, p);
+    e = p.topk ? cudaLaunchKernelEx(&cfg, vs::k_verify_rr<T, true, false>, p)
+        : ea   ? cudaLaunchKernelEx(&cfg, vs::k_verify_rr<T, false, true>, p)
+               : cudaLaunchKernelEx(&cfg, vs::k_verify_rr<T, false, false>, p);
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
