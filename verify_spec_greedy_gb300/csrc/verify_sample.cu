@@ -542,9 +542,9 @@ __device__ __forceinline__ bool row_sampled(const Params &P, int64_t b) {
 
 // KT: the call passes per-row top-k values.  Without them no row has a top-k filter, and
 // the top-k paths (counting histograms, the bound of small k, the draw from candidates)
-// compile out of the instance that runs.  EA: a decode loop's call without top-k values
-// (no p_target, p_draft), whose top-p drafts may be seen accepted at E1; the other
-// instances compile that path out.
+// compile out of the instance that runs.  EA: a decode loop's call with draft logits and
+// without top-k values (no p_target, p_draft), whose top-p drafts may be seen accepted at
+// E1; the other instances compile that path out.
 template <typename T, bool KT, bool EA>
 __global__ void __launch_bounds__(NT, CPS) k_verify_rr(const Params P) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -2423,9 +2423,10 @@ template <typename T>
 static cudaError_t launch_verify_rr(vs::Params p, cudaStream_t stream) {
     const int64_t units = p.B * (p.D + 1);
     // the instance: with the top-k paths when the call passes top-k values; else with the
-    // E1 acceptance path for a decode loop's call (top-p values, no probabilities), else
-    // without either
-    const bool ea = !p.topk && p.topp && !p.need_p;
+    // E1 acceptance path for a decode loop's call with draft logits (top-p values, no
+    // probabilities; a one-hot draft's units are short enough that the path costs more
+    // than it saves: 267 -> 283 us on the serving workload), else without either
+    const bool ea = !p.topk && p.topp && !p.need_p && p.Q;
     cudaError_t e = prepare_verify_rr<T, true, false>();
     if (e == cudaSuccess && !p.topk) e = ea ? prepare_verify_rr<T, false, true>() : prepare_verify_rr<T, false, false>();
     if (e != cudaSuccess) return e;
