@@ -47,7 +47,16 @@
 //   accept   p(d), q(d) and U_acc <= p/q (ratio formed with both maxima factored out)
 //   draw     only for a rejected draft or the bonus position: draw weights in fixed point
 //            (2^31 per unit of probability), per-warp sums in id order, CTA sums exchanged
-//            (E4), and the warp holding the target walks its run to the token.
+//            (E4), and the warp holding the target walks its run to the token.  A top-k
+//            row resolved from its candidates draws in CTA 0 from them alone, with the
+//            same weights in id order (no slice is read).
+//
+// Work that no output reads is skipped when the call requests no probabilities: a draft
+// whose acceptance is already certain needs nothing but its flag.  It is seen at E1
+// (in the instance built for such calls: the target mass above the draft token, summed
+// in pass 1, settles that the token is kept, and U_acc lies below a lower bound of p/q),
+// or after the plan (the kept masses then lie within rigorous bounds).  Such a unit skips
+// the rest of its filters and releases its staged rows at once.
 //
 // Exchanges are point to point: a CTA writes its part into every peer's shared memory and
 // then arrives (release, cluster scope) on that peer's mbarrier for the exchange; a CTA
@@ -57,8 +66,8 @@
 // unit k + 1, i.e. after it finished unit k.  All waits are bounded and raise
 // MTPSPEC_STATUS_TIMEOUT when they give up.
 //
-// The kernel is bound by instruction issue rather than by memory: each phase is written
-// for few instructions per element (no per-element branch, bins and weights leave fp32
+// The kernel is bound by the residency of its staged rows and by instruction issue, not by
+// memory bandwidth: each phase is written for few instructions per element (no per-element branch, bins and weights leave fp32
 // through exponent arithmetic, not conversions), and the latency-bound bookkeeping
 // (scheduling the next unit, its L2 prefetch, the Philox words) runs in one warp while the
 // others wait for E1.
